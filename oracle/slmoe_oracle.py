@@ -1,0 +1,273 @@
+"""Oracle for the Stable LatentMoE forward path and its Quantile Balancing engine.
+
+TEST INFRASTRUCTURE ONLY.  This module is a plain, slow, obviously correct fp64 CPU
+statement of what the layer computes.  Only the tests, the smoke check of
+``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` may import it; the product
+library never does, and it shares no code with the CUDA path.
+
+Sources (page title, then section):
+  [K3-news]  "苏神复盘 Kimi K3：896 个专家背后，藏着哪些关键技术取舍？", §01 LatentMoE 如何重新分配
+             专家预算 and §02 Stable LatentMoE 如何处理数值与负载风险.
+  [K3-arch]  the K3 architecture write-up (tahou.com), sections 混合专家, SiTU激活优化,
+             归一化策略调整, 负载均衡优化.
+  [SLMoE]    "Stable Latent MoE" concept note, sections TL;DR, 路由机制, Quantile Balancing,
+             Latent-Space MoE, SiTU 激活.
+
+Readings where the pages are silent (all listed again in the design notes):
+  * router score = sigmoid(x . W_r^T + mu_e); the selection uses score + b_e; the gate
+    weights renormalise the raw scores of the chosen experts to sum 1 (the bias steers
+    selection only, [K3-news] §02; no extra scale factor, [K3-arch] 归一化策略调整).
+  * top-k ties go to the lower expert index; slot order is biased score descending.
+  * an expert is gate/up -> SiTU-GLU -> expert down (I -> d_latent); the "four chained
+    matmuls" of [K3-arch] 归一化策略调整 are down, expert up, expert down, up.
+  * QB histograms bin the raw scores; the quantile is read by linear interpolation inside
+    the bin that holds fractional rank r = (1 - k/E) * N; the update b_e <- mean(q) - q_e
+    overwrites the bias.
+
+Parity pins live in ``tests/test_oracle_pins.py``.  Two quantities stay "parity unpinned"
+by the pages: the exact bias-update formula (the pages defer it to a technical report)
+and the balance that QB reaches on a given input.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+# [K3-arch] SiTU激活优化: beta_1 = 4 on the gate branch, beta_2 = 25 on the linear branch.
+BETA1 = 4.0
+BETA2 = 25.0
+# [K3-arch] 负载均衡优化: 1000 bins over [0, 1] were as good as 10000.
+NBINS = 1000
+EPS = 1e-6
+
+
+def f64(a):
+    """Widen an array-like (numpy array or torch tensor, any float type) to float64 numpy."""
+    if hasattr(a, "detach"):
+        return a.detach().cpu().double().numpy()
+    return np.asarray(a, dtype=np.float64)
+
+
+# ----------------------------------------------------------------------------------------
+# Activations  ([K3-arch] SiTU激活优化; [SLMoE] SiTU 激活)
+# ----------------------------------------------------------------------------------------
+
+def sigmoid(v):
+    v = np.asarray(v, dtype=np.float64)
+    out = np.empty_like(v)
+    pos = v >= 0
+    out[pos] = 1.0 / (1.0 + np.exp(-v[pos]))
+    ev = np.exp(v[~pos])
+    out[~pos] = ev / (1.0 + ev)
+    return out
+
+
+def situ(g, beta=BETA1):
+    """Sigmoid Tanh Unit: beta * tanh(g / beta) * sigmoid(g); bounded in (-beta, beta)."""
+    g = np.asarray(g, dtype=np.float64)
+    return beta * np.tanh(g / beta) * sigmoid(g)
+
+
+def softcap(u, beta=BETA2):
+    """Soft cap of the linear (up) branch: beta * tanh(u / beta)."""
+    u = np.asarray(u, dtype=np.float64)
+    return beta * np.tanh(u / beta)
+
+
+def situ_glu(gu, beta1=BETA1, beta2=BETA2):
+    """SiTU-GLU on the last axis: the first half is the gate branch, the second the up branch."""
+    half = gu.shape[-1] // 2
+    return situ(gu[..., :half], beta1) * softcap(gu[..., half:], beta2)
+
+
+# ----------------------------------------------------------------------------------------
+# Router and biased top-k  ([K3-news] §01-§02; [SLMoE] 路由机制)
+# ----------------------------------------------------------------------------------------
+
+def router_scores(x, W_r, logit_offset=None):
+    """s[t, e] = sigmoid(x_t . W_r[e] + mu_e) in fp64."""
+    logits = f64(x) @ f64(W_r).T
+    if logit_offset is not None:
+        logits = logits + f64(logit_offset)[None, :]
+    return sigmoid(logits)
+
+
+def select_topk(scores, bias, k):
+    """Top-k experts per token by biased score s + b.
+
+    Returns (topk_idx [T,k] int32 in slot order, gates [T,k] fp64, gap [T] fp64) where the
+    slot order is biased score descending with ties to the lower expert index, the gates
+    are the chosen raw scores renormalised to sum 1, and gap is the distance between the
+    k-th and (k+1)-th biased scores (inf when k == E).
+    """
+    s = f64(scores)
+    T, E = s.shape
+    biased = s + f64(bias)[None, :]
+    idx = np.broadcast_to(np.arange(E), (T, E))
+    order = np.lexsort((idx, -biased), axis=-1)          # primary -biased, then index
+    sel = order[:, :k].astype(np.int32)
+    rows = np.arange(T)[:, None]
+    chosen = s[rows, sel]
+    gates = chosen / chosen.sum(axis=1, keepdims=True)
+    if k < E:
+        gap = biased[rows[:, 0], order[:, k - 1]] - biased[rows[:, 0], order[:, k]]
+    else:
+        gap = np.full(T, np.inf)
+    return sel, gates, gap
+
+
+def permutation(topk_idx, E):
+    """Expert-sorted token index: (counts[E], offsets[E+1], perm[T*k], slot_pos[T,k]).
+
+    perm lists token ids grouped by expert (ascending) and, inside an expert, by token id
+    (ascending); slot_pos[t, j] is the position in perm of the pair (t, topk_idx[t, j]).
+    """
+    ti = np.asarray(topk_idx, dtype=np.int64)
+    T, k = ti.shape
+    e_of = ti.reshape(-1)
+    t_of = np.repeat(np.arange(T), k)
+    j_of = np.tile(np.arange(k), T)
+    order = np.lexsort((t_of, e_of))                      # expert ascending, then token
+    perm = t_of[order]
+    slot_pos = np.zeros((T, k), dtype=np.int64)
+    slot_pos[t_of[order], j_of[order]] = np.arange(T * k)
+    counts = np.bincount(e_of, minlength=E).astype(np.int64)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    return counts, offsets, perm, slot_pos
+
+
+def expert_loads(topk_idx, E):
+    return np.bincount(np.asarray(topk_idx).reshape(-1), minlength=E)
+
+
+# ----------------------------------------------------------------------------------------
+# The layer  ([K3-news] §01-§02; [K3-arch] 归一化策略调整; [SLMoE] Latent-Space MoE)
+# ----------------------------------------------------------------------------------------
+
+def rmsnorm(c, gamma, eps=EPS):
+    c = f64(c)
+    return f64(gamma)[None, :] * c / np.sqrt(np.mean(c * c, axis=1, keepdims=True) + eps)
+
+
+def forward(inp, k, beta1=BETA1, beta2=BETA2, eps=EPS, forced_topk_idx=None, tokens=None):
+    """One Stable LatentMoE layer (the FFN branch, no residual add) in fp64.
+
+    inp: dict of the layer inputs (see ``synthetic.layer_inputs``).  ``tokens`` restricts
+    the computation to a subset of token rows (every step is per token);
+    ``forced_topk_idx`` [T_all, k] replaces the oracle's own selection (the gates are
+    still the oracle's renormalised fp64 scores of the forced experts).
+
+    Returns a dict with scores, topk_idx, gates, gap, x_lat, c (the gate-weighted combine),
+    z (after RMSNorm), y_routed (z projected up), y_shared and y.
+    """
+    x_all = inp["x"]
+    T_all = x_all.shape[0]
+    tok = np.arange(T_all) if tokens is None else np.asarray(tokens)
+    x = f64(x_all[tok] if tokens is not None else x_all)
+    T = x.shape[0]
+
+    # router: sigmoid scores, selection by biased score, renormalised raw-score gates
+    s = router_scores(x, inp["W_r"], inp.get("logit_offset"))
+    if forced_topk_idx is None:
+        sel, gates, gap = select_topk(s, inp["bias"], k)
+    else:
+        sel = np.asarray(forced_topk_idx)[tok].astype(np.int32)
+        chosen = s[np.arange(T)[:, None], sel]
+        gates = chosen / chosen.sum(axis=1, keepdims=True)
+        _, _, gap = select_topk(s, inp["bias"], k)
+
+    # latent down-projection d -> d_latent
+    x_lat = x @ f64(inp["W_in"]).T
+
+    # routed experts in latent space, gate-weighted sum over the k chosen experts
+    W13, W2 = inp["W13"], inp["W2"]
+    d_lat = x_lat.shape[1]
+    c = np.zeros((T, d_lat))
+    for e in np.unique(sel):
+        tt, jj = np.nonzero(sel == e)
+        gu = x_lat[tt] @ f64(W13[int(e)]).T               # [n, 2I]: gate rows first
+        h = situ_glu(gu, beta1, beta2)
+        y_e = h @ f64(W2[int(e)]).T                        # [n, d_latent]
+        np.add.at(c, tt, gates[tt, jj][:, None] * y_e)
+
+    # RMSNorm after the combine, before the up-projection only
+    z = rmsnorm(c, inp["gamma"], eps)
+    y_routed = z @ f64(inp["W_out"]).T
+
+    # two always-on shared experts on the full hidden width
+    y_shared = np.zeros_like(y_routed)
+    W13_s, W2_s = inp["W13_s"], inp["W2_s"]
+    for si in range(W13_s.shape[0]):
+        gu = x @ f64(W13_s[si]).T
+        y_shared += situ_glu(gu, beta1, beta2) @ f64(W2_s[si]).T
+
+    return dict(scores=s, topk_idx=sel, gates=gates, gap=gap, x_lat=x_lat, c=c, z=z,
+                y_routed=y_routed, y_shared=y_shared, y=y_routed + y_shared, tokens=tok)
+
+
+def expert_hidden(inp, e, rows_lat, beta1=BETA1, beta2=BETA2):
+    """h = SiTU-GLU(W13[e] . x_lat) for given latent rows (used to check one stage)."""
+    return situ_glu(f64(rows_lat) @ f64(inp["W13"][int(e)]).T, beta1, beta2)
+
+
+# ----------------------------------------------------------------------------------------
+# Quantile Balancing  ([K3-arch] 负载均衡优化; [K3-news] §02; [SLMoE] Quantile Balancing)
+# ----------------------------------------------------------------------------------------
+
+def qb_bins(scores_f32, nbins=NBINS):
+    """Bin index of each fp32 score: floor(fl32(s * nbins)) clamped to [0, nbins-1].
+
+    The product is one IEEE fp32 round-to-nearest multiply, exactly as the GPU does it.
+    Returns (bins int64, valid mask); NaN scores are invalid and left out of the counts.
+    """
+    s = np.asarray(scores_f32, dtype=np.float32)
+    valid = ~np.isnan(s)
+    scaled = np.where(valid, s, np.float32(0)) * np.float32(nbins)   # fp32 * fp32 -> fp32
+    b = np.floor(scaled.astype(np.float64)).astype(np.int64)
+    return np.clip(b, 0, nbins - 1), valid
+
+
+def qb_histogram(scores_f32, nbins=NBINS, hist=None):
+    """Add the per-expert bin counts of a [T, E] fp32 score block into hist [E, nbins].
+
+    Histograms of micro-batches add ([K3-arch] 负载均衡优化: the distribution is additive
+    across machines and gradient-accumulation steps).
+    """
+    s = np.asarray(scores_f32, dtype=np.float32)
+    T, E = s.shape
+    b, valid = qb_bins(s, nbins)
+    flat = (np.arange(E)[None, :] * nbins + b)[valid]
+    add = np.bincount(flat, minlength=E * nbins).reshape(E, nbins).astype(np.uint64)
+    if hist is None:
+        return add
+    return np.asarray(hist, dtype=np.uint64) + add
+
+
+def qb_quantile(hist, k):
+    """q_e: the (1 - k/E) quantile of expert e's scores, read from its histogram.
+
+    With N_e counts and fractional rank r = (1 - k/E) * N_e, j is the first bin whose
+    cumulative count C_j reaches r, and q_e = (j + (r - C_{j-1}) / hist[j]) / nbins
+    (linear inside bin j).  An empty histogram (r = 0) gives q_e = 0.
+    """
+    h = np.asarray(hist, dtype=np.int64)
+    E, nb = h.shape
+    p = 1.0 - float(k) / float(E)
+    q = np.zeros(E)
+    for e in range(E):
+        N = int(h[e].sum())
+        r = p * float(N)
+        if r == 0.0:
+            q[e] = 0.0
+            continue
+        C = np.cumsum(h[e])
+        j = int(np.searchsorted(C, r, side="left"))
+        prev = float(C[j - 1]) if j > 0 else 0.0
+        q[e] = (j + (r - prev) / float(h[e, j])) / nb
+    return q
+
+
+def qb_update(hist, k):
+    """Bias update b_e <- mean_e(q) - q_e from the histograms (overwrites the bias)."""
+    q = qb_quantile(hist, k)
+    cbar = q.mean()
+    return q, cbar - q
