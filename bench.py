@@ -1,0 +1,393 @@
+"""Benchmark of the Stable LatentMoE forward hot path on GB300.
+
+One step = one slmoe_forward over one batch of the workload (router scores, biased top-k,
+permutation, QB histogram of the step's scores, latent down-projection, both routed-expert
+GEMMs with the fused SiTU-GLU, combine + RMSNorm, shared experts, up-projection) followed by
+the QB bias update (slmoe_qb_update).  Inputs and weights are resident in HBM when timing
+starts; weights (10.2 GB at the K3 shape) exceed the 126 MB L2, so no flush is needed.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload k3_prefill|k3_decode|mid]
+                  [--impl ours|reference]
+
+Prints one JSON line (rank 0).  N > 1 runs one independent replica per GPU (weak scaling):
+the layer has no data-path exchange on one node in this design.  --impl reference times the
+fp64 oracle on the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "LatentMoE fwd tokens/s at K3 shape (1xGB300)"
+UNIT = "tokens/s"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+STAGES = ["start", "router", "topk+permute+hist", "down", "expert gate|up", "expert down",
+          "combine+rmsnorm", "shared gate|up", "up+shared down"]
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+def work_model(shp, counts=None):
+    """Algorithmic FLOPs and bytes per stage for one step (weights touched + kernel I/O)."""
+    T, d, dl, E, k, I, ns, Is = shp.T, shp.d, shp.d_latent, shp.E, shp.k, shp.I, shp.n_shared, shp.I_shared
+    touched = E if counts is None else int((counts > 0).sum())
+    st = {
+        "router": dict(flops=2 * T * d * E, bytes=T * d * 2 + E * d * 4 + T * E * 4, bound="tensor"),
+        "topk+permute+hist": dict(flops=0, bytes=2 * T * E * 4 + T * k * 16, bound="hbm"),
+        "down": dict(flops=2 * T * d * dl, bytes=T * d * 2 + dl * d * 2 + T * dl * 2, bound="tensor"),
+        "expert gate|up": dict(flops=2 * T * k * dl * 2 * I,
+                               bytes=touched * 2 * I * dl * 2 + T * dl * 2 + T * k * I * 2, bound="hbm"),
+        "expert down": dict(flops=2 * T * k * I * dl,
+                            bytes=touched * dl * I * 2 + T * k * I * 2 + T * k * dl * 2, bound="hbm"),
+        "combine+rmsnorm": dict(flops=0, bytes=T * k * dl * 2 + T * dl * 2, bound="hbm"),
+        "shared gate|up": dict(flops=2 * T * d * 2 * Is * ns, bytes=T * d * 2 + ns * 2 * Is * d * 2 + T * ns * Is * 2,
+                               bound="tensor"),
+        "up+shared down": dict(flops=2 * T * (dl + ns * Is) * d,
+                               bytes=T * dl * 2 + T * ns * Is * 2 + d * (dl + ns * Is) * 2 + T * d * 2,
+                               bound="tensor"),
+    }
+    layer_flops = sum(v["flops"] for v in st.values())
+    layer_bytes = (E * d * 4 + dl * d * 2 + touched * 3 * I * dl * 2 + d * dl * 2 + ns * 3 * Is * d * 2
+                   + T * d * 2 * 2)
+    return st, layer_flops, layer_bytes
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during a region."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait()
+        self.f.seek(0)
+        rows = [r.split(", ") for r in self.f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        samples = []
+        for r in rows:
+            try:
+                ts = time.mktime(time.strptime(r[0].split(".")[0], "%Y/%m/%d %H:%M:%S")) + float("0." + r[0].split(".")[1])
+                samples.append((ts, float(r[2]), float(r[3]), r[5:]))
+            except (ValueError, IndexError):
+                continue
+        inside = [s for s in samples if t0 - 0.2 <= s[0] <= t1 + 0.2] or samples
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in inside for i, v in enumerate(s[3][1:5]) if v.strip() == "Active"})
+        return {"sm_mhz": statistics.median(s[1] for s in inside) if inside else None,
+                "sm_max_mhz": max(s[2] for s in inside) if inside else None,
+                "reasons": reasons, "samples": len(inside)}
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def oracle_sample(shp, inp_cpu, n_tok):
+    """Time the fp64 oracle on n_tok tokens of the workload (routing included)."""
+    import numpy as np
+    import oracle
+    tok = np.arange(n_tok)
+    t0 = time.perf_counter()
+    oracle.forward(inp_cpu, shp.k, tokens=tok)
+    dt = time.perf_counter() - t0
+    return n_tok / dt, dt
+
+
+def cpu_cores():
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        n = max((i.get("num_threads", 1) for i in info), default=1)
+        return int(n)
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    """The oracle as the reference arm: fp64 CPU forward on a bounded token sample per step."""
+    import torch
+    import synthetic
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    shp = synthetic.LAYERS[args.workload]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = synthetic.layer_inputs(shp, seed=0, device=dev)
+    inp_cpu = {k: (v.cpu() if v is not None else None) for k, v in inp.items()}
+    del inp
+    n_tok = args.ref_tokens
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        oracle_sample(shp, inp_cpu, 1)
+    t = []
+    for _ in range(args.steps):
+        _, dt = oracle_sample(shp, inp_cpu, n_tok)
+        t.append(dt)
+    total = sum(t)
+    value = n_tok * args.steps / total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "T": shp.T, "d": shp.d, "d_latent": shp.d_latent,
+                       "E": shp.E, "k": shp.k, "I": shp.I, "n_shared": shp.n_shared,
+                       "I_shared": shp.I_shared, "sample_tokens_per_step": n_tok},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                             "sample": f"{n_tok} tokens of the {args.workload} batch per step (routing, "
+                                       f"experts, norm, shared experts; per-token cost is constant)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="k3_prefill", choices=["k3_prefill", "k3_decode", "mid"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-tokens", type=int, default=4)
+    ap.add_argument("--cpu-baseline-tokens", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--skew", action="store_true", help="heavy skew (10%% hot experts)")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import numpy as np
+    import torch
+    import latent_space_experts_gb300 as lse
+    import synthetic
+
+    world, rank, local = dist_setup(args)
+    lse.build()
+    lse.load()
+    shp = synthetic.LAYERS[args.workload]
+    cfg = lse.config(shp)
+    inp = synthetic.layer_inputs(shp, seed=rank, device="cuda", heavy_skew=args.skew)
+    act = torch.bfloat16 if shp.dtype == "bf16" else torch.float32
+    ws = torch.zeros(lse.slmoe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    y = torch.empty(shp.T, shp.d, dtype=act, device="cuda")
+    hist = torch.zeros(shp.E, shp.nbins, dtype=torch.int32, device="cuda")
+    bias = inp["bias"].clone()
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    W = lse.weights(inp)
+    stream = torch.cuda.current_stream()
+
+    def step(x):
+        lse.slmoe_forward(cfg, x, W, bias, inp["logit_offset"], y, None, hist, status, ws)
+        lse.slmoe_qb_update(hist, shp.E, shp.nbins, shp.k, None, bias)
+
+    for _ in range(max(3, args.warmup)):
+        step(inp["x"])
+    torch.cuda.synchronize()
+    assert status.cpu().tolist()[1:3] == [0, 0], f"device status {status.cpu().tolist()}"
+
+    # ---------------- device-resident timing
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    l0 = lse.slmoe_launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0 = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(inp["x"])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    barrier(world)
+    launches = lse.slmoe_launch_count() - l0
+    ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
+    clocks = sampler.stop(w0, w1) if sampler else None
+
+    # ---------------- per-stage timing (events recorded by the library on this stream)
+    nst = len(STAGES)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)] for _ in range(min(args.steps, 50))]
+    for row in ev:
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+    stage_ms = [0.0] * nst
+    for row in ev:
+        lse.slmoe_set_stage_events(row)
+        step(inp["x"])
+    lse.slmoe_set_stage_events(None)
+    torch.cuda.synchronize()
+    for row in ev:
+        for i in range(1, nst):
+            stage_ms[i] += row[i - 1].elapsed_time(row[i]) / len(ev)
+    counts = lse.workspace_views(cfg, ws)["counts"].cpu().numpy()
+    st_model, layer_flops, layer_bytes = work_model(shp, counts)
+    pk, pk_kind = peaks()
+    hbm = pk["hbm_gbs"]
+    tc = pk["bf16_tflops_sustained"]
+    stages = {}
+    for i in range(1, nst):
+        m = st_model[STAGES[i]]
+        t = stage_ms[i] * 1e-3
+        stages[STAGES[i]] = {"ms": round(stage_ms[i], 4),
+                             "GB/s": round(m["bytes"] / t / 1e9, 1) if t > 0 else None,
+                             "TFLOP/s": round(m["flops"] / t / 1e12, 1) if t > 0 else None,
+                             "bound": m["bound"]}
+    dom = max(range(1, nst), key=lambda i: stage_ms[i])
+    dm = st_model[STAGES[dom]]
+    t_dom = stage_ms[dom] * 1e-3
+    if dm["bound"] == "hbm":
+        roof = {"bound": "hbm", "achieved": round(dm["bytes"] / t_dom / 1e9, 1), "peak": hbm, "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": round(dm["flops"] / t_dom / 1e12, 1), "peak": tc,
+                "unit": "TFLOP/s"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["traffic"] = None
+    roof["kernel"] = STAGES[dom]
+    roof["peak_source"] = f"{pk_kind} ({'sustained bf16' if roof['bound'] == 'tensor' else 'hbm copy'})"
+    t_layer = max(layer_flops / (tc * 1e12), layer_bytes / (hbm * 1e9))
+
+    # ---------------- end to end through the public API, host buffers
+    x_host = inp["x"].cpu().pin_memory()
+    y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    x_dev = torch.empty_like(inp["x"])
+    for _ in range(3):
+        x_dev.copy_(x_host, non_blocking=True)
+        step(x_dev)
+        y_host.copy_(y, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    n_e2e = max(3, min(args.steps, 100))
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(n_e2e):
+        x_dev.copy_(x_host, non_blocking=True)
+        step(x_dev)
+        y_host.copy_(y, non_blocking=True)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = max_over_ranks(f0.elapsed_time(f1), world) / n_e2e
+
+    # ---------------- QB engine histogram bandwidth (65536 x 896 fp32 per micro-batch)
+    qb = None
+    if rank == 0:
+        q = synthetic.QB
+        sc = synthetic.qb_scores(0, q, device="cuda")
+        qh = torch.zeros(q.E, q.nbins, dtype=torch.int32, device="cuda")
+        for _ in range(3):
+            lse.slmoe_qb_histogram(sc, q.T, q.E, q.nbins, qh)
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 50
+        g0.record(stream)
+        for _ in range(reps):
+            lse.slmoe_qb_histogram(sc, q.T, q.E, q.nbins, qh)
+        g1.record(stream)
+        torch.cuda.synchronize()
+        tq = g0.elapsed_time(g1) / reps * 1e-3
+        qbytes = q.T * q.E * 4 + 2 * q.E * q.nbins * 4
+        qb = {"GB/s": round(qbytes / tq / 1e9, 1), "frac_of_hbm": round(qbytes / tq / 1e9 / hbm, 4),
+              "us_per_micro_batch": round(tq * 1e6, 2), "bytes": qbytes, "note": "scores > L2 per call (235 MB)"}
+        del sc, qh
+
+    # ---------------- oracle on the host cores (bounded sample)
+    cpu_base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        inp_cpu = {k: (v.cpu() if v is not None else None) for k, v in inp.items()}
+        n_tok = args.cpu_baseline_tokens
+        v, dt = oracle_sample(shp, inp_cpu, n_tok)
+        cpu_base = {"value": round(v, 3), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                    "sample": f"{n_tok} tokens of the {args.workload} batch, fp64 numpy ({dt:.1f} s)"}
+
+    if rank == 0:
+        tokens = shp.T * world
+        line = {
+            "metric": METRIC, "value": round(tokens / (ms * 1e-3), 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": shp.dtype,
+            "data": "synthetic",
+            "config": {"workload": args.workload, "T": shp.T, "d": shp.d, "d_latent": shp.d_latent,
+                       "E": shp.E, "k": shp.k, "I": shp.I, "n_shared": shp.n_shared, "I_shared": shp.I_shared,
+                       "router": "fp32 logits (3-piece bf16 split)", "skew": bool(args.skew),
+                       "parallelism": f"replicas x{world}",
+                       "l2": "no flush: weights (10.2 GB at K3) exceed L2 every step"},
+            "roofline": roof,
+            "layer_roofline": {"ms": round(t_layer * 1e3, 4), "frac": round(t_layer * 1e3 / ms, 4),
+                               "flops": layer_flops, "bytes": layer_bytes,
+                               "peaks": f"{pk_kind}: {tc} TFLOP/s sustained bf16, {hbm} GB/s"},
+            "stages": stages,
+            "qb_histogram": qb,
+            "cpu_baseline": cpu_base,
+            "e2e": {"value": round(tokens / (ms_e2e * 1e-3), 1), "unit": UNIT,
+                    "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
+                    "d2h_bytes_per_step": y_host.numel() * y_host.element_size()},
+            "gpu_launches": launches,
+            "clocks": clocks,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,205 @@
+/*
+ * slmoe.h - C ABI of the Stable LatentMoE forward path and its Quantile Balancing engine
+ * on one NVIDIA GB300 (sm_103a).
+ *
+ * Sources, cited by page title and section:
+ *   [K3-news] "苏神复盘 Kimi K3：896 个专家背后，藏着哪些关键技术取舍？"
+ *             §01 LatentMoE 如何重新分配专家预算, §02 Stable LatentMoE 如何处理数值与负载风险
+ *   [K3-arch] K3 architecture write-up (tahou.com): SiTU激活优化, 归一化策略调整, 负载均衡优化
+ *   [SLMoE]   "Stable Latent MoE" concept note: 路由机制, Quantile Balancing,
+ *             Latent-Space MoE, SiTU 激活, 训练基础设施 (static shapes, no host sync)
+ *
+ * Conventions shared by every call
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller.  Matrices are dense,
+ *     row-major, with the nn.Linear convention W[out, in].
+ *   - "stream" is a cudaStream_t passed as void* (NULL = the legacy default stream).  All
+ *     work is enqueued on it; no call synchronises the host or copies device->host, so a
+ *     call returns before its kernels finish ([SLMoE] 训练基础设施: no host sync on the
+ *     critical path).  Calls that share output buffers must be ordered on one stream.
+ *   - The library allocates nothing.  Scratch lives in a caller-provided workspace of at
+ *     least slmoe_workspace_size() bytes, 256-byte aligned.
+ *   - Return value: SLMOE_OK (0) or a negative code.  Arguments are validated on the host
+ *     before any launch; on error nothing is launched and slmoe_last_error() gives a
+ *     thread-local message.  No C++ exception crosses the ABI.
+ *   - Optional device status words (int32_t status[4], may be NULL) report anomalies
+ *     without trapping: status[0] += number of NaN router scores met (a NaN score is never
+ *     selected and is left out of histograms); status[1] is set to 1 when a histogram bin
+ *     would pass 2^32-1; status[2] is set to 1 when a bounded device-side wait gave up (the
+ *     outputs of that call are then invalid); status[3] is reserved.  The caller zeroes
+ *     the words; calls only add or set.
+ *   - Contraction work is the dense and grouped GEMMs on tcgen05 tensor cores (bf16 in,
+ *     fp32 accumulate).  The fp32 layer type runs every step in fp32 on CUDA cores.
+ */
+#ifndef SLMOE_H
+#define SLMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SLMOE_API __attribute__((visibility("default")))
+#else
+#define SLMOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SLMOE_OK            0
+#define SLMOE_EINVAL       (-1)  /* null pointer, misalignment, bad shape or k > E       */
+#define SLMOE_EUNSUPPORTED (-2)  /* shape or type outside what the kernels are built for */
+#define SLMOE_ECUDA        (-3)  /* a CUDA runtime or launch error                       */
+#define SLMOE_ENOSPACE     (-4)  /* the workspace is smaller than slmoe_workspace_size() */
+
+#define SLMOE_F32  0             /* x, projection weights, y and intermediates in fp32  */
+#define SLMOE_BF16 1             /* the same in bf16 (fp32 accumulation, fp32 router)   */
+
+/* Shape and constants of one layer.  beta1 / beta2 are the SiTU and soft-cap constants
+ * ([K3-arch] SiTU激活优化: 4 and 25), eps the RMSNorm epsilon, nbins the QB histogram
+ * width ([K3-arch] 负载均衡优化: 1000).
+ * Limits: 1 <= k <= E <= 4096, k <= 32; d, d_latent, I, I_shared multiples of 8 (of 64 for
+ * the bf16 type); n_shared <= 3; T >= 0 (T = 0 is a no-op). */
+typedef struct slmoe_config {
+    int32_t T;           /* tokens in the call                                   */
+    int32_t d;           /* hidden width                                         */
+    int32_t d_latent;    /* latent width of the routed experts                   */
+    int32_t E;           /* routed experts                                       */
+    int32_t k;           /* experts selected per token                           */
+    int32_t I;           /* routed-expert intermediate width                     */
+    int32_t n_shared;    /* always-on shared experts                             */
+    int32_t I_shared;    /* shared-expert intermediate width                     */
+    int32_t nbins;       /* QB histogram bins over [0, 1]                        */
+    float   beta1;       /* SiTU gate bound                                      */
+    float   beta2;       /* soft cap of the up branch                            */
+    float   eps;         /* RMSNorm epsilon                                      */
+    int32_t dtype;       /* SLMOE_F32 or SLMOE_BF16                              */
+} slmoe_config;
+
+/* Layer weights.  "act" = the layer type (fp32 for SLMOE_F32, bf16 for SLMOE_BF16).
+ * Expert gate/up matrices hold the gate rows first ([SLMoE] SiTU 激活: the first half of
+ * the last axis is the gate). */
+typedef struct slmoe_weights {
+    const float *W_r;    /* [E, d]                    fp32 router               */
+    const void  *W_in;   /* [d_latent, d]             act  latent down-proj     */
+    const void  *W13;    /* [E, 2I, d_latent]         act  expert gate|up       */
+    const void  *W2;     /* [E, d_latent, I]          act  expert down          */
+    const float *gamma;  /* [d_latent]                fp32 RMSNorm weight       */
+    const void  *W_out;  /* [d, d_latent]             act  latent up-proj       */
+    const void  *W13_s;  /* [n_shared, 2I_shared, d]  act  shared gate|up       */
+    const void  *W2_s;   /* [n_shared, d, I_shared]   act  shared down          */
+} slmoe_weights;
+
+/* Byte offsets of the intermediates inside the workspace, so that a caller can read a
+ * stage's result after slmoe_forward (or slmoe_route) without a second code path.
+ * Types: scores fp32 [T,E]; topk_idx int32 [T,k]; topk_w fp32 [T,k]; counts int32 [E];
+ * offsets int32 [E+1]; perm int32 [T*k]; slot_pos int32 [T*k]; x_lat act [T,d_latent];
+ * h act [T*k, I] (rows in perm order); y_e act [T*k, d_latent] (rows in perm order);
+ * z act [T,d_latent]; h_s act [T, n_shared*I_shared]; status int32 [4]. */
+typedef struct slmoe_workspace_layout {
+    size_t scores, topk_idx, topk_w, counts, offsets, perm, slot_pos;
+    size_t x_lat, h, y_e, z, h_s, status;
+    size_t total;
+} slmoe_workspace_layout;
+
+/* Bytes of workspace a slmoe_route or slmoe_forward call with this config needs
+ * (0 on an invalid config; see slmoe_last_error). */
+SLMOE_API size_t slmoe_workspace_size(const slmoe_config *cfg);
+
+/* Fill *out with the workspace layout for cfg.  Returns SLMOE_OK or SLMOE_EINVAL. */
+SLMOE_API int slmoe_workspace_layout_get(const slmoe_config *cfg, slmoe_workspace_layout *out);
+
+/* Thread-local message of the last failed call on this thread ("" if none). */
+SLMOE_API const char *slmoe_last_error(void);
+
+/* Number of streaming multiprocessors of the current device (for sizing tests). */
+SLMOE_API int slmoe_device_sm_count(void);
+
+/* Stage profiling hook (thread-local).  When events is not NULL, slmoe_forward records
+ * events[i] (a cudaEvent_t created by the caller, passed as void*) on its stream right after
+ * stage i, for i < n:  0 start, 1 router scores, 2 top-k + permutation (+ histogram),
+ * 3 latent down-projection, 4 expert gate|up + SiTU-GLU, 5 expert down, 6 combine + RMSNorm,
+ * 7 shared gate|up + SiTU-GLU, 8 up-projection + shared down.  NULL turns it off. */
+SLMOE_API int slmoe_set_stage_events(void **events, int n);
+
+/* Number of kernels this library has launched in this process (all threads). */
+SLMOE_API long long slmoe_launch_count(void);
+
+/*
+ * slmoe_route - router scores, biased top-k and the expert-sorted permutation.
+ *   [K3-news] §01-§02, [K3-arch] 负载均衡优化, [SLMoE] 路由机制.
+ *   s[t,e]  = sigmoid(x_t . W_r[e] + logit_offset[e])      (fp32 logits)
+ *   choose the k experts with the largest s[t,e] + bias[e]; ties go to the lower index;
+ *   slots are ordered by biased score descending;
+ *   topk_w[t,j] = s[t, topk_idx[t,j]] / sum_j s[t, topk_idx[t,j]]   (raw scores)
+ *   counts[e] = tokens that chose e; offsets = exclusive scan of counts (offsets[E] = T*k);
+ *   perm lists token ids by expert ascending, then token ascending;
+ *   slot_pos[t*k+j] = position of (t, topk_idx[t,j]) in perm.
+ * Arguments: x [T,d] act; W_r [E,d] fp32; bias [E] fp32; logit_offset [E] fp32 or NULL;
+ *   outputs topk_idx [T,k] int32, topk_w [T,k] fp32, counts [E], offsets [E+1], perm [T*k],
+ *   slot_pos [T*k] (all int32, all required); scores [T,E] fp32 or NULL (when NULL the
+ *   scores stay in the workspace); hist [E,nbins] uint32 or NULL: when given, the scores'
+ *   QB histogram is added into it (as slmoe_qb_histogram); status as above.
+ * Errors: SLMOE_EINVAL on a null required pointer or a bad config, SLMOE_ENOSPACE on a
+ *   short workspace, SLMOE_ECUDA on a launch failure.
+ */
+SLMOE_API int slmoe_route(const slmoe_config *cfg, const void *x, const float *W_r, const float *bias,
+                const float *logit_offset, int32_t *topk_idx, float *topk_w, float *scores,
+                int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *slot_pos,
+                uint32_t *hist, int32_t *status, void *workspace, size_t workspace_bytes,
+                void *stream);
+
+/*
+ * slmoe_qb_histogram - add per-expert score histograms of one micro-batch.
+ *   [K3-arch] 负载均衡优化: scores in [0,1] are binned, 1000 bins; histograms of
+ *   micro-batches and machines add.
+ *   For every t < T, e < E with scores[t*E+e] not NaN:
+ *     bin = min(nbins-1, max(0, floor(fl32(scores[t*E+e] * nbins))))  (one fp32 multiply)
+ *     hist[e*nbins + bin] += 1
+ *   scores [T,E] fp32, row-major; hist [E,nbins] uint32, accumulated in place (the caller
+ *   zeroes it before the first micro-batch).  T may be 0.  No workspace.
+ * Errors: SLMOE_EINVAL on null pointers, E < 1, nbins < 1 or nbins > 4096.
+ */
+SLMOE_API int slmoe_qb_histogram(const float *scores, int64_t T, int32_t E, int32_t nbins,
+                       uint32_t *hist, int32_t *status, void *stream);
+
+/*
+ * slmoe_qb_update - read each expert's (1 - k/E) quantile from its histogram and re-centre
+ * the biases.  [K3-arch] 负载均衡优化 (quantile read from the binned distribution);
+ * [K3-news] §02 (thresholds placed so that each expert gets its share).  The pages do not
+ * print the update; this library fixes it as:
+ *   N_e = sum_b hist[e,b];  r = (1 - k/E) * N_e;  j = first bin with C_j >= r
+ *   q_e = (j + (r - C_{j-1}) / hist[e,j]) / nbins      (q_e = 0 when r = 0)
+ *   bias[e] = mean_e(q) - q_e                           (overwrites bias)
+ *   computed in fp64 and stored in fp32.  hist [E,nbins] uint32; q_out [E] fp32 or NULL;
+ *   bias [E] fp32.  E <= 8192.  One block; no workspace.
+ */
+SLMOE_API int slmoe_qb_update(const uint32_t *hist, int32_t E, int32_t nbins, int32_t k,
+                    float *q_out, float *bias, void *stream);
+
+/*
+ * slmoe_forward - one Stable LatentMoE layer (the FFN branch; the residual add is left to
+ * the caller).  [K3-news] §01-§02, [K3-arch] SiTU激活优化 / 归一化策略调整,
+ * [SLMoE] Latent-Space MoE.
+ *   route as slmoe_route;  x_lat = x . W_in^T;
+ *   for each chosen (t, e):  [g | u] = x_lat_t . W13[e]^T,
+ *       h = beta1 tanh(g/beta1) sigmoid(g) * beta2 tanh(u/beta2),   y_e = h . W2[e]^T;
+ *   c_t = sum_j topk_w[t,j] y_e(t,j)  (fp32, slot order);
+ *   z_t = gamma * c_t / sqrt(mean(c_t^2) + eps);
+ *   y_t = z_t . W_out^T + sum_s W2_s[s] . SiTU-GLU(W13_s[s] . x_t)
+ * Arguments: x [T,d] act; w as slmoe_weights; bias [E] fp32; logit_offset [E] or NULL;
+ *   y [T,d] act (written, not accumulated); topk_idx_out [T,k] int32 or NULL: when given,
+ *   the routing is exported there; hist [E,nbins] or NULL: QB histogram of the scores is
+ *   added; status as above; workspace as slmoe_workspace_size().  The intermediates stay
+ *   readable in the workspace (slmoe_workspace_layout_get).
+ * Errors: as slmoe_route.
+ */
+SLMOE_API int slmoe_forward(const slmoe_config *cfg, const void *x, const slmoe_weights *w,
+                  const float *bias, const float *logit_offset, void *y,
+                  int32_t *topk_idx_out, uint32_t *hist, int32_t *status,
+                  void *workspace, size_t workspace_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SLMOE_H */

@@ -1,0 +1,209 @@
+"""Python binding of the slmoe C ABI (``include/slmoe.h``): argument marshalling only.
+
+Every step of the layer runs in the CUDA kernels of ``libslmoe.so``; this module turns
+torch tensors into device pointers and ctypes structs, calls the C entry points with the
+same names, and raises ``SlmoeError`` on a non-zero return code.  There is no fallback:
+if the library is missing the import of an entry point fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+__all__ = ["SlmoeError", "Config", "Weights", "WorkspaceLayout", "load", "build", "config",
+           "weights", "slmoe_workspace_size", "slmoe_workspace_layout_get", "slmoe_route",
+           "slmoe_qb_histogram", "slmoe_qb_update", "slmoe_forward", "slmoe_device_sm_count",
+           "workspace_views", "slmoe_last_error", "slmoe_set_stage_events", "slmoe_launch_count", "F32", "BF16", "LIB_PATH"]
+
+F32, BF16 = 0, 1
+LIB_PATH = _build.LIB
+
+
+class SlmoeError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"slmoe error {code}: {msg}")
+        self.code = code
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("d_latent", ctypes.c_int32),
+                ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("I", ctypes.c_int32),
+                ("n_shared", ctypes.c_int32), ("I_shared", ctypes.c_int32), ("nbins", ctypes.c_int32),
+                ("beta1", ctypes.c_float), ("beta2", ctypes.c_float), ("eps", ctypes.c_float),
+                ("dtype", ctypes.c_int32)]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("W_r", "W_in", "W13", "W2", "gamma", "W_out", "W13_s", "W2_s")]
+
+
+class WorkspaceLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in
+                ("scores", "topk_idx", "topk_w", "counts", "offsets", "perm", "slot_pos", "x_lat",
+                 "h", "y_e", "z", "h_s", "status", "total")]
+
+
+_lib = None
+
+
+def build(force=False):
+    return _build.build(force=force)
+
+
+def load():
+    """The loaded ``libslmoe.so`` (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with latent_space_experts_gb300.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    CP, WP = ctypes.POINTER(Config), ctypes.POINTER(Weights)
+    sig = {
+        "slmoe_workspace_size": (SZ, [CP]),
+        "slmoe_workspace_layout_get": (ctypes.c_int, [CP, ctypes.POINTER(WorkspaceLayout)]),
+        "slmoe_last_error": (ctypes.c_char_p, []),
+        "slmoe_device_sm_count": (ctypes.c_int, []),
+        "slmoe_route": (ctypes.c_int, [CP, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
+        "slmoe_qb_histogram": (ctypes.c_int, [P, I64, I32, I32, P, P, P]),
+        "slmoe_qb_update": (ctypes.c_int, [P, I32, I32, I32, P, P, P]),
+        "slmoe_forward": (ctypes.c_int, [CP, P, WP, P, P, P, P, P, P, P, SZ, P]),
+        "slmoe_set_stage_events": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]),
+        "slmoe_launch_count": (ctypes.c_longlong, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype, f.argtypes = res, args
+    _lib = lib
+    return lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("slmoe entry points take CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("slmoe entry points take contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(rc):
+    if rc != 0:
+        raise SlmoeError(rc, load().slmoe_last_error().decode())
+
+
+def config(shape, T=None) -> Config:
+    """A Config from a ``synthetic.LayerShape``-like object (T overridable)."""
+    return Config(T=shape.T if T is None else T, d=shape.d, d_latent=shape.d_latent, E=shape.E,
+                  k=shape.k, I=shape.I, n_shared=shape.n_shared, I_shared=shape.I_shared,
+                  nbins=shape.nbins, beta1=shape.beta1, beta2=shape.beta2, eps=shape.eps,
+                  dtype=BF16 if shape.dtype == "bf16" else F32)
+
+
+def weights(inp: dict) -> Weights:
+    return Weights(*[_ptr(inp[n]) for n in ("W_r", "W_in", "W13", "W2", "gamma", "W_out",
+                                             "W13_s", "W2_s")])
+
+
+def slmoe_last_error() -> str:
+    return load().slmoe_last_error().decode()
+
+
+_event_array = None
+
+
+def slmoe_set_stage_events(events):
+    """Hand the library torch.cuda.Event objects (recorded once, so that they exist) to be
+    recorded after each stage of slmoe_forward on this thread; None turns it off."""
+    global _event_array
+    if not events:
+        _event_array = None
+        return load().slmoe_set_stage_events(None, 0)
+    _event_array = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    return load().slmoe_set_stage_events(_event_array, len(events))
+
+
+def slmoe_launch_count() -> int:
+    return load().slmoe_launch_count()
+
+
+def slmoe_device_sm_count() -> int:
+    return load().slmoe_device_sm_count()
+
+
+def slmoe_workspace_size(cfg: Config) -> int:
+    n = load().slmoe_workspace_size(ctypes.byref(cfg))
+    if n == 0:
+        raise SlmoeError(-1, load().slmoe_last_error().decode())
+    return n
+
+
+def slmoe_workspace_layout_get(cfg: Config) -> dict:
+    out = WorkspaceLayout()
+    _check(load().slmoe_workspace_layout_get(ctypes.byref(cfg), ctypes.byref(out)))
+    return {n: getattr(out, n) for n, _ in WorkspaceLayout._fields_}
+
+
+def workspace_views(cfg: Config, ws):
+    """torch views of the intermediates inside a workspace tensor (uint8, on the device)."""
+    import torch
+    L = slmoe_workspace_layout_get(cfg)
+    act = torch.bfloat16 if cfg.dtype == BF16 else torch.float32
+    T, k, E = cfg.T, cfg.k, cfg.E
+
+    def view(name, dtype, shape):
+        n = 1
+        for s in shape:
+            n *= s
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        return ws[L[name]:L[name] + nbytes].view(dtype).view(*shape)
+
+    return dict(scores=view("scores", torch.float32, (T, E)),
+                topk_idx=view("topk_idx", torch.int32, (T, k)),
+                topk_w=view("topk_w", torch.float32, (T, k)),
+                counts=view("counts", torch.int32, (E,)),
+                offsets=view("offsets", torch.int32, (E + 1,)),
+                perm=view("perm", torch.int32, (T * k,)),
+                slot_pos=view("slot_pos", torch.int32, (T, k)),
+                x_lat=view("x_lat", act, (T, cfg.d_latent)),
+                h=view("h", act, (T * k, cfg.I)),
+                y_e=view("y_e", act, (T * k, cfg.d_latent)),
+                z=view("z", act, (T, cfg.d_latent)),
+                h_s=view("h_s", act, (T, cfg.n_shared * cfg.I_shared)),
+                status=view("status", torch.int32, (4,)))
+
+
+def slmoe_route(cfg, x, W_r, bias, logit_offset, topk_idx, topk_w, scores, counts, offsets, perm,
+                slot_pos, hist, status, workspace, stream=None):
+    _check(load().slmoe_route(ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(bias), _ptr(logit_offset),
+                              _ptr(topk_idx), _ptr(topk_w), _ptr(scores), _ptr(counts), _ptr(offsets),
+                              _ptr(perm), _ptr(slot_pos), _ptr(hist), _ptr(status), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def slmoe_qb_histogram(scores, T, E, nbins, hist, status=None, stream=None):
+    _check(load().slmoe_qb_histogram(_ptr(scores), T, E, nbins, _ptr(hist), _ptr(status),
+                                     _stream(stream)))
+
+
+def slmoe_qb_update(hist, E, nbins, k, q_out, bias, stream=None):
+    _check(load().slmoe_qb_update(_ptr(hist), E, nbins, k, _ptr(q_out), _ptr(bias), _stream(stream)))
+
+
+def slmoe_forward(cfg, x, w: Weights, bias, logit_offset, y, topk_idx_out, hist, status, workspace,
+                  stream=None):
+    _check(load().slmoe_forward(ctypes.byref(cfg), _ptr(x), ctypes.byref(w), _ptr(bias),
+                                _ptr(logit_offset), _ptr(y), _ptr(topk_idx_out), _ptr(hist),
+                                _ptr(status), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _stream(stream)))

@@ -1,0 +1,375 @@
+// The C ABI of slmoe.h: argument validation, the workspace layout, and the sequencing of
+// the kernels of one call on the caller's stream.  Nothing here synchronises the host.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "internal.h"
+#include "tc_gemm.h"
+
+namespace slmoe {
+
+static thread_local char g_err[512];
+static thread_local void **g_events = nullptr;
+static thread_local int g_nevents = 0;
+static std::atomic<long long> g_launches{0};
+
+void stage_event(int i, cudaStream_t st) {
+    if (g_events && i < g_nevents && g_events[i])
+        cudaEventRecord(static_cast<cudaEvent_t>(g_events[i]), st);
+}
+
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int check_launch(const char *what) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(SLMOE_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+    return SLMOE_OK;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int validate_config(const slmoe_config *c) {
+    if (!c) return fail(SLMOE_EINVAL, "config is NULL");
+    if (c->dtype != SLMOE_F32 && c->dtype != SLMOE_BF16)
+        return fail(SLMOE_EINVAL, "dtype %d is neither SLMOE_F32 nor SLMOE_BF16", c->dtype);
+    if (c->T < 0) return fail(SLMOE_EINVAL, "T = %d < 0", c->T);
+    if (c->E < 1 || c->E > 4096) return fail(SLMOE_EINVAL, "E = %d outside [1, 4096]", c->E);
+    if (c->k < 1 || c->k > c->E || c->k > 32)
+        return fail(SLMOE_EINVAL, "k = %d outside [1, min(E, 32)]", c->k);
+    if (c->nbins < 1 || c->nbins > 2048) return fail(SLMOE_EINVAL, "nbins = %d outside [1, 2048]", c->nbins);
+    if (c->n_shared < 0 || c->n_shared > 3) return fail(SLMOE_EINVAL, "n_shared = %d outside [0, 3]", c->n_shared);
+    const int m = c->dtype == SLMOE_BF16 ? 64 : 8;
+    if (c->d < m || c->d % m) return fail(SLMOE_EINVAL, "d = %d is not a positive multiple of %d", c->d, m);
+    if (c->d_latent < m || c->d_latent % m)
+        return fail(SLMOE_EINVAL, "d_latent = %d is not a positive multiple of %d", c->d_latent, m);
+    if (c->I < m || c->I % m) return fail(SLMOE_EINVAL, "I = %d is not a positive multiple of %d", c->I, m);
+    if (c->n_shared > 0 && (c->I_shared < m || c->I_shared % m))
+        return fail(SLMOE_EINVAL, "I_shared = %d is not a positive multiple of %d", c->I_shared, m);
+    if (!(c->beta1 > 0.f) || !(c->beta2 > 0.f) || !(c->eps >= 0.f))
+        return fail(SLMOE_EINVAL, "beta1, beta2 must be > 0 and eps >= 0");
+    if ((int64_t)c->T * c->k > (int64_t)INT32_MAX / 2)
+        return fail(SLMOE_EUNSUPPORTED, "T * k = %lld too large", (long long)c->T * c->k);
+    return SLMOE_OK;
+}
+
+int make_layout(const slmoe_config *c, Layout *L) {
+    int rc = validate_config(c);
+    if (rc) return rc;
+    const size_t T = c->T, E = c->E, k = c->k, es = c->dtype == SLMOE_BF16 ? 2 : 4;
+    const size_t nchunks = (T + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = off;
+        off = align_up(off + (bytes ? bytes : 1), 256);
+        return at;
+    };
+    memset(L, 0, sizeof(*L));
+    L->nchunks = nchunks;
+    L->pub.scores = take(T * E * 4);
+    L->pub.topk_idx = take(T * k * 4);
+    L->pub.topk_w = take(T * k * 4);
+    L->pub.counts = take(E * 4);
+    L->pub.offsets = take((E + 1) * 4);
+    L->pub.perm = take(T * k * 4);
+    L->pub.slot_pos = take(T * k * 4);
+    L->chunk_counts = take(nchunks * E * 4);
+    L->pub.x_lat = take(T * c->d_latent * es);
+    L->pub.h = take(T * k * c->I * es);
+    L->pub.y_e = take(T * k * c->d_latent * es);
+    L->pub.z = take(T * c->d_latent * es);
+    L->pub.h_s = take(T * (size_t)c->n_shared * c->I_shared * es);
+    L->pub.status = take(16);
+    L->wr_split = c->dtype == SLMOE_BF16 ? take(3 * E * c->d * 2) : 0;
+    L->pub.total = off;
+    return SLMOE_OK;
+}
+
+static bool misaligned(const void *p) { return ((uintptr_t)p & 15u) != 0; }
+
+#define REQ(p, name)                                                                    \
+    do {                                                                                \
+        if (!(p)) return fail(SLMOE_EINVAL, "%s is NULL", name);                        \
+        if (misaligned(p)) return fail(SLMOE_EINVAL, "%s is not 16-byte aligned", name); \
+    } while (0)
+#define OPT(p, name)                                                                    \
+    do {                                                                                \
+        if ((p) && misaligned(p)) return fail(SLMOE_EINVAL, "%s is not 16-byte aligned", name); \
+    } while (0)
+
+struct Routing {
+    float *scores;
+    int32_t *topk_idx;
+    float *topk_w;
+    int32_t *counts, *offsets, *perm, *slot_pos, *chunk_counts;
+};
+
+// Router scores, top-k and permutation.  (苏神复盘 Kimi K3 §01-§02.)
+static int route_impl(const slmoe_config *c, const Layout &L, char *ws, const void *x,
+                      const float *W_r, const float *bias, const float *mu, const Routing &R,
+                      uint32_t *hist, int32_t *status, cudaStream_t st) {
+    int rc;
+    stage_event(0, st);
+    if (c->dtype == SLMOE_BF16) {
+        rc = tc_router_scores(c, x, W_r, mu, reinterpret_cast<__nv_bfloat16 *>(ws + L.wr_split),
+                              R.scores, status, st);
+    } else {
+        SimtGemm g = {};
+        g.seg[0] = {x, W_r, c->d, c->d, c->d, 0};
+        g.nseg = 1;
+        g.groups = 1;
+        g.M = c->T;
+        g.N = c->E;
+        g.C = R.scores;
+        g.ldc = c->E;
+        g.mu = mu;
+        g.epi = SIMT_SIGMOID;
+        g.a_type = DT_F32;
+        g.b_type = DT_F32;
+        g.c_type = DT_F32;
+        rc = launch_simt_gemm(g, st);
+    }
+    if (rc) return rc;
+    stage_event(1, st);
+    if ((rc = launch_topk(R.scores, bias, c->T, c->E, c->k, R.topk_idx, R.topk_w, R.chunk_counts,
+                          status, st)))
+        return rc;
+    if ((rc = launch_scan(R.chunk_counts, (int)L.nchunks, c->E, R.counts, R.offsets, st))) return rc;
+    if ((rc = launch_scatter(R.topk_idx, R.chunk_counts, R.offsets, c->T, c->E, c->k, R.perm,
+                             R.slot_pos, st)))
+        return rc;
+    if (hist) {
+        if ((rc = launch_qb_histogram(R.scores, c->T, c->E, c->nbins, hist, status, st))) return rc;
+    }
+    stage_event(2, st);
+    return SLMOE_OK;
+}
+
+// The fp32 layer type: every contraction on CUDA cores in fp32.
+static int forward_f32(const slmoe_config *c, const Layout &L, char *ws, const void *x,
+                       const slmoe_weights *w, const Routing &R, void *y, cudaStream_t st) {
+    const int T = c->T, d = c->d, dl = c->d_latent, E = c->E, k = c->k, I = c->I;
+    const int ns = c->n_shared, Is = c->I_shared;
+    float *x_lat = reinterpret_cast<float *>(ws + L.pub.x_lat);
+    float *h = reinterpret_cast<float *>(ws + L.pub.h);
+    float *y_e = reinterpret_cast<float *>(ws + L.pub.y_e);
+    float *z = reinterpret_cast<float *>(ws + L.pub.z);
+    float *h_s = reinterpret_cast<float *>(ws + L.pub.h_s);
+    int rc;
+    auto base = [&]() {
+        SimtGemm g = {};
+        g.nseg = 1;
+        g.groups = 1;
+        g.beta1 = c->beta1;
+        g.beta2 = c->beta2;
+        g.a_type = g.b_type = g.c_type = DT_F32;
+        return g;
+    };
+    {   // latent down-projection
+        SimtGemm g = base();
+        g.seg[0] = {x, w->W_in, d, d, d, 0};
+        g.M = T; g.N = dl; g.C = x_lat; g.ldc = dl; g.epi = SIMT_STORE;
+        if ((rc = launch_simt_gemm(g, st))) return rc;
+    }
+    stage_event(3, st);
+    {   // expert gate|up with SiTU-GLU, rows gathered by perm, grouped by expert
+        SimtGemm g = base();
+        g.seg[0] = {x_lat, w->W13, dl, dl, dl, (int64_t)2 * I * dl};
+        g.a_index = R.perm; g.group_offsets = R.offsets; g.groups = E;
+        g.M = T; g.N = I; g.glu_up_row = I; g.C = h; g.ldc = I; g.epi = SIMT_GLU;
+        if ((rc = launch_simt_gemm(g, st))) return rc;
+    }
+    stage_event(4, st);
+    {   // expert down-projection
+        SimtGemm g = base();
+        g.seg[0] = {h, w->W2, I, I, I, (int64_t)dl * I};
+        g.group_offsets = R.offsets; g.groups = E;
+        g.M = T; g.N = dl; g.C = y_e; g.ldc = dl; g.epi = SIMT_STORE;
+        if ((rc = launch_simt_gemm(g, st))) return rc;
+    }
+    stage_event(5, st);
+    if ((rc = launch_combine_rmsnorm(DT_F32, y_e, R.topk_w, R.slot_pos, w->gamma, T, dl, k, c->eps,
+                                     z, st)))
+        return rc;
+    stage_event(6, st);
+    for (int s = 0; s < ns; ++s) {   // shared experts: gate|up with SiTU-GLU
+        SimtGemm g = base();
+        g.seg[0] = {x, static_cast<const float *>(w->W13_s) + (size_t)s * 2 * Is * d, d, d, d, 0};
+        g.M = T; g.N = Is; g.glu_up_row = Is; g.C = h_s + (size_t)s * Is; g.ldc = (int64_t)ns * Is;
+        g.epi = SIMT_GLU;
+        if ((rc = launch_simt_gemm(g, st))) return rc;
+    }
+    stage_event(7, st);
+    {   // y = z W_out^T + sum_s h_s W2_s^T in one K-segmented product
+        SimtGemm g = base();
+        g.seg[0] = {z, w->W_out, dl, dl, dl, 0};
+        for (int s = 0; s < ns; ++s)
+            g.seg[1 + s] = {h_s + (size_t)s * Is, static_cast<const float *>(w->W2_s) + (size_t)s * d * Is,
+                            (int64_t)ns * Is, Is, Is, 0};
+        g.nseg = 1 + ns;
+        g.M = T; g.N = d; g.C = y; g.ldc = d; g.epi = SIMT_STORE;
+        if ((rc = launch_simt_gemm(g, st))) return rc;
+    }
+    stage_event(8, st);
+    (void)E;
+    return SLMOE_OK;
+}
+
+}  // namespace slmoe
+
+using namespace slmoe;
+
+extern "C" {
+
+const char *slmoe_last_error(void) { return g_err; }
+
+int slmoe_set_stage_events(void **events, int n) {
+    g_events = n > 0 ? events : nullptr;
+    g_nevents = n > 0 ? n : 0;
+    return SLMOE_OK;
+}
+
+long long slmoe_launch_count(void) { return g_launches.load(); }
+
+int slmoe_device_sm_count(void) { return sm_count(); }
+
+size_t slmoe_workspace_size(const slmoe_config *cfg) {
+    Layout L;
+    if (make_layout(cfg, &L)) return 0;
+    return L.pub.total;
+}
+
+int slmoe_workspace_layout_get(const slmoe_config *cfg, slmoe_workspace_layout *out) {
+    if (!out) return fail(SLMOE_EINVAL, "out is NULL");
+    Layout L;
+    int rc = make_layout(cfg, &L);
+    if (rc) return rc;
+    *out = L.pub;
+    return SLMOE_OK;
+}
+
+int slmoe_route(const slmoe_config *cfg, const void *x, const float *W_r, const float *bias,
+                const float *logit_offset, int32_t *topk_idx, float *topk_w, float *scores,
+                int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *slot_pos,
+                uint32_t *hist, int32_t *status, void *workspace, size_t workspace_bytes,
+                void *stream) {
+    g_err[0] = 0;
+    Layout L;
+    int rc = make_layout(cfg, &L);
+    if (rc) return rc;
+    REQ(workspace, "workspace");
+    if (workspace_bytes < L.pub.total)
+        return fail(SLMOE_ENOSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, L.pub.total);
+    REQ(counts, "counts");
+    REQ(offsets, "offsets");
+    if (cfg->T > 0) {
+        REQ(x, "x"); REQ(W_r, "W_r"); REQ(bias, "bias"); OPT(logit_offset, "logit_offset");
+        REQ(topk_idx, "topk_idx"); REQ(topk_w, "topk_w"); REQ(perm, "perm"); REQ(slot_pos, "slot_pos");
+        OPT(scores, "scores"); OPT(hist, "hist");
+    }
+    OPT(status, "status");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    if (cfg->T == 0) {
+        if (cudaMemsetAsync(counts, 0, cfg->E * 4, st) != cudaSuccess ||
+            cudaMemsetAsync(offsets, 0, (cfg->E + 1) * 4, st) != cudaSuccess)
+            return check_launch("memset");
+        return SLMOE_OK;
+    }
+    Routing R = {scores ? scores : reinterpret_cast<float *>(ws + L.pub.scores), topk_idx, topk_w,
+                 counts, offsets, perm, slot_pos, reinterpret_cast<int32_t *>(ws + L.chunk_counts)};
+    return route_impl(cfg, L, ws, x, W_r, bias, logit_offset, R, hist, status, st);
+}
+
+int slmoe_qb_histogram(const float *scores, int64_t T, int32_t E, int32_t nbins, uint32_t *hist,
+                       int32_t *status, void *stream) {
+    g_err[0] = 0;
+    if (T < 0) return fail(SLMOE_EINVAL, "T < 0");
+    if (E < 1) return fail(SLMOE_EINVAL, "E < 1");
+    if (nbins < 1 || nbins > 2048) return fail(SLMOE_EINVAL, "nbins outside [1, 2048]");
+    if (!hist) return fail(SLMOE_EINVAL, "hist is NULL");
+    if (T > 0 && !scores) return fail(SLMOE_EINVAL, "scores is NULL");
+    if (((uintptr_t)scores & 3u) || ((uintptr_t)hist & 3u) || ((uintptr_t)status & 3u))
+        return fail(SLMOE_EINVAL, "scores, hist and status must be 4-byte aligned");
+    return launch_qb_histogram(scores, T, E, nbins, hist, status, static_cast<cudaStream_t>(stream));
+}
+
+int slmoe_qb_update(const uint32_t *hist, int32_t E, int32_t nbins, int32_t k, float *q_out,
+                    float *bias, void *stream) {
+    g_err[0] = 0;
+    if (E < 1 || E > 8192) return fail(SLMOE_EINVAL, "E outside [1, 8192]");
+    if (k < 1 || k > E) return fail(SLMOE_EINVAL, "k outside [1, E]");
+    if (nbins < 1 || nbins > 2048) return fail(SLMOE_EINVAL, "nbins outside [1, 2048]");
+    if (!hist || !bias) return fail(SLMOE_EINVAL, "hist and bias are required");
+    if (((uintptr_t)hist & 3u) || ((uintptr_t)bias & 3u) || ((uintptr_t)q_out & 3u))
+        return fail(SLMOE_EINVAL, "hist, bias and q_out must be 4-byte aligned");
+    return launch_qb_update(hist, E, nbins, k, q_out, bias, static_cast<cudaStream_t>(stream));
+}
+
+int slmoe_forward(const slmoe_config *cfg, const void *x, const slmoe_weights *w,
+                  const float *bias, const float *logit_offset, void *y, int32_t *topk_idx_out,
+                  uint32_t *hist, int32_t *status, void *workspace, size_t workspace_bytes,
+                  void *stream) {
+    g_err[0] = 0;
+    Layout L;
+    int rc = make_layout(cfg, &L);
+    if (rc) return rc;
+    if (cfg->T == 0) return SLMOE_OK;
+    REQ(workspace, "workspace");
+    if (workspace_bytes < L.pub.total)
+        return fail(SLMOE_ENOSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, L.pub.total);
+    if (!w) return fail(SLMOE_EINVAL, "weights is NULL");
+    REQ(x, "x"); REQ(y, "y"); REQ(bias, "bias"); OPT(logit_offset, "logit_offset");
+    REQ(w->W_r, "W_r"); REQ(w->W_in, "W_in"); REQ(w->W13, "W13"); REQ(w->W2, "W2");
+    REQ(w->gamma, "gamma"); REQ(w->W_out, "W_out");
+    if (cfg->n_shared > 0) { REQ(w->W13_s, "W13_s"); REQ(w->W2_s, "W2_s"); }
+    OPT(topk_idx_out, "topk_idx_out"); OPT(hist, "hist"); OPT(status, "status");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    int32_t *stat = status ? status : reinterpret_cast<int32_t *>(ws + L.pub.status);
+    if (!status && cudaMemsetAsync(stat, 0, 16, st) != cudaSuccess) return check_launch("memset");
+    Routing R = {reinterpret_cast<float *>(ws + L.pub.scores),
+                 reinterpret_cast<int32_t *>(ws + L.pub.topk_idx),
+                 reinterpret_cast<float *>(ws + L.pub.topk_w),
+                 reinterpret_cast<int32_t *>(ws + L.pub.counts),
+                 reinterpret_cast<int32_t *>(ws + L.pub.offsets),
+                 reinterpret_cast<int32_t *>(ws + L.pub.perm),
+                 reinterpret_cast<int32_t *>(ws + L.pub.slot_pos),
+                 reinterpret_cast<int32_t *>(ws + L.chunk_counts)};
+    if ((rc = route_impl(cfg, L, ws, x, w->W_r, bias, logit_offset, R, hist, stat, st))) return rc;
+    if (topk_idx_out &&
+        cudaMemcpyAsync(topk_idx_out, R.topk_idx, (size_t)cfg->T * cfg->k * 4, cudaMemcpyDeviceToDevice,
+                        st) != cudaSuccess)
+        return check_launch("copy topk_idx");
+    if (cfg->dtype == SLMOE_F32) return forward_f32(cfg, L, ws, x, w, R, y, st);
+    TcForward tf = {};
+    tf.x_lat = ws + L.pub.x_lat;
+    tf.h = ws + L.pub.h;
+    tf.y_e = ws + L.pub.y_e;
+    tf.z = ws + L.pub.z;
+    tf.h_s = ws + L.pub.h_s;
+    tf.topk_w = R.topk_w;
+    tf.counts = R.counts;
+    tf.offsets = R.offsets;
+    tf.perm = R.perm;
+    tf.slot_pos = R.slot_pos;
+    tf.status = stat;
+    return tc_forward_bf16(cfg, x, w, tf, y, st);
+}
+
+}  // extern "C"

@@ -1,0 +1,82 @@
+// Internal launcher interface shared by the library's translation units (host side).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "slmoe.h"
+
+namespace slmoe {
+
+// Sets the thread-local error message and returns code.
+int fail(int code, const char *fmt, ...);
+// Maps a pending CUDA error (cudaGetLastError) to SLMOE_ECUDA with a message.
+int check_launch(const char *what);
+
+int sm_count();
+// Records the caller's stage event i on st when stage events are set (profiling hook).
+void stage_event(int i, cudaStream_t st);
+
+// ---------------------------------------------------------------- full workspace layout
+struct Layout {
+    slmoe_workspace_layout pub;
+    size_t chunk_counts;   // int32 [nchunks, E]: per-chunk expert counts, then bases
+    size_t wr_split;       // bf16 [3, E, d]: router weight split hi / mid / lo
+    size_t nchunks;
+};
+int make_layout(const slmoe_config *cfg, Layout *L);
+int validate_config(const slmoe_config *cfg);
+
+// ---------------------------------------------------------------- SIMT GEMM (CUDA cores)
+// C[r, n] = epilogue( sum_s sum_k A_s[arow(r), k] * B_s[brow(n), k] ),  fp32 accumulate.
+enum SimtEpi { SIMT_STORE = 0, SIMT_GLU = 1, SIMT_SIGMOID = 2 };
+enum DType { DT_F32 = 0, DT_BF16 = 1 };
+
+struct SimtSeg {
+    const void *A;           // [rows, lda]
+    const void *B;           // [N (or 2N for GLU), ldb] per group
+    int64_t lda, ldb;
+    int K;
+    int64_t b_group_stride;  // elements between groups' B matrices
+};
+
+struct SimtGemm {
+    SimtSeg seg[4];
+    int nseg;
+    const int32_t *a_index;        // nullable: A row of output row r is a_index[r]
+    const int32_t *group_offsets;  // nullable: rows of group g are [off[g], off[g+1])
+    int groups;                    // grid z (1 when not grouped)
+    int M;                         // rows when not grouped; max rows per group when grouped
+    int N;                         // output columns
+    int glu_up_row;                // GLU: B row of the up half of column n is n + glu_up_row
+    void *C;
+    int64_t ldc;
+    const float *mu;               // SIGMOID: logit offset per column (nullable)
+    float beta1, beta2;
+    int epi;
+    int a_type, b_type, c_type;    // DType
+};
+int launch_simt_gemm(const SimtGemm &g, cudaStream_t st);
+
+// ---------------------------------------------------------------- routing
+int launch_topk(const float *scores, const float *bias, int T, int E, int k, int32_t *topk_idx,
+                float *topk_w, int32_t *chunk_counts, int32_t *status, cudaStream_t st);
+int launch_scan(int32_t *chunk_counts, int nchunks, int E, int32_t *counts, int32_t *offsets,
+                cudaStream_t st);
+int launch_scatter(const int32_t *topk_idx, const int32_t *chunk_base, const int32_t *offsets,
+                   int T, int E, int k, int32_t *perm, int32_t *slot_pos, cudaStream_t st);
+constexpr int ROUTE_CHUNK = 64;  // tokens per top-k block / permutation chunk
+
+// ---------------------------------------------------------------- QB
+int launch_qb_histogram(const float *scores, int64_t T, int E, int nbins, uint32_t *hist,
+                        int32_t *status, cudaStream_t st);
+int launch_qb_update(const uint32_t *hist, int E, int nbins, int k, float *q_out, float *bias,
+                     cudaStream_t st);
+
+// ---------------------------------------------------------------- combine + RMSNorm
+int launch_combine_rmsnorm(int dtype, const void *y_e, const float *topk_w,
+                           const int32_t *slot_pos, const float *gamma, int T, int d_latent,
+                           int k, float eps, void *z, cudaStream_t st);
+
+}  // namespace slmoe

@@ -1,0 +1,227 @@
+// Quantile Balancing: per-expert score histograms and the bias update.
+//
+// K3 architecture write-up, 负载均衡优化: scores in [0, 1] are binned (1000 bins suffice), the
+// target quantile is read from the binned distribution, and histograms add across
+// micro-batches and machines.  The bias update (b_e <- mean(q) - q_e) is this library's
+// fixed reading; the pages defer the exact rule to a technical report.
+//
+// Histogram design.  scores [T, E] fp32 is streamed once from HBM.  The experts are cut
+// into slabs of 32 (one 128-byte line per row: lane = expert), and each slab is counted by
+// one thread-block cluster of QB_CLUSTER CTAs that split the tokens.  Counters are 16-bit
+// halves of 32-bit shared-memory words (a CTA counts at most 65535 tokens per window, so a
+// half never carries into its neighbour).  At the end of a window the cluster adds its
+// CTAs' counters through distributed shared memory and each bin of global memory is
+// read-modified-written by exactly one thread: no global atomics and no partial
+// histograms in HBM.
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace slmoe {
+namespace {
+
+constexpr int QB_SLAB = 32;
+constexpr int QB_THREADS = 512;
+constexpr int QB_CLUSTER = 8;
+constexpr int64_t QB_WINDOW = 65535;     // tokens per CTA per window (16-bit counters)
+constexpr int QB_UNROLL = 8;
+
+__device__ __forceinline__ int qb_bin(float s, float nb, int nbins) {
+    // one IEEE fp32 round-to-nearest multiply, then floor, clamped to [0, nbins-1]
+    float p = __fmul_rn(s, nb);
+    int b = (int)floorf(p);
+    b = b < 0 ? 0 : b;
+    return b > nbins - 1 ? nbins - 1 : b;
+}
+
+__global__ void __launch_bounds__(QB_THREADS)
+qb_hist_kernel(const float *__restrict__ scores, int64_t T, int E, int nbins, int wstride,
+               uint32_t *__restrict__ hist, int32_t *status) {
+    extern __shared__ uint32_t hs[];                 // [QB_SLAB][wstride] packed 16-bit
+    cg::cluster_group cluster = cg::this_cluster();
+    const int P = (int)cluster.num_blocks();
+    const int rank = (int)cluster.block_rank();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nwarps = QB_THREADS / 32;
+    const int e0 = blockIdx.x * QB_SLAB;
+    const int ne = min(QB_SLAB, E - e0);
+    const float nb = (float)nbins;
+    const int nwords_e = (nbins + 1) >> 1;
+    int nan_count = 0;
+    bool overflow = false;
+
+    for (int64_t w0 = 0; w0 < T; w0 += QB_WINDOW * P) {
+        for (int i = tid; i < QB_SLAB * wstride; i += QB_THREADS) hs[i] = 0u;
+        __syncthreads();
+        const int64_t wt1 = min(T, w0 + QB_WINDOW * P);
+        const int64_t per = (wt1 - w0 + P - 1) / P;
+        const int64_t t0 = w0 + rank * per;
+        const int64_t t1 = min(wt1, t0 + per);
+        if (lane < ne) {
+            const float *col = scores + e0 + lane;
+            uint32_t *h = hs + lane * wstride;
+            int64_t t = t0 + warp;
+            for (; t + (QB_UNROLL - 1) * nwarps < t1; t += QB_UNROLL * nwarps) {
+                float v[QB_UNROLL];
+#pragma unroll
+                for (int u = 0; u < QB_UNROLL; ++u) v[u] = __ldcs(col + (t + u * nwarps) * (int64_t)E);
+#pragma unroll
+                for (int u = 0; u < QB_UNROLL; ++u) {
+                    if (isnan(v[u])) { ++nan_count; continue; }
+                    const int b = qb_bin(v[u], nb, nbins);
+                    atomicAdd(&h[b >> 1], 1u << ((b & 1) << 4));
+                }
+            }
+            for (; t < t1; t += nwarps) {
+                const float v = __ldcs(col + t * (int64_t)E);
+                if (isnan(v)) { ++nan_count; continue; }
+                const int b = qb_bin(v, nb, nbins);
+                atomicAdd(&h[b >> 1], 1u << ((b & 1) << 4));
+            }
+        }
+        cluster.sync();
+        // each CTA of the cluster adds a share of the slab's words across all CTAs
+        const int total = ne * nwords_e;
+        const int share = (total + P - 1) / P;
+        const int f0 = rank * share, f1 = min(total, f0 + share);
+        for (int f = f0 + tid; f < f1; f += QB_THREADS) {
+            const int e = f / nwords_e, wd = f - e * nwords_e;
+            uint32_t lo = 0, hi = 0;
+            for (int r = 0; r < P; ++r) {
+                const uint32_t *rh = cluster.map_shared_rank(hs, r);
+                const uint32_t v = rh[e * wstride + wd];
+                lo += v & 0xffffu;
+                hi += v >> 16;
+            }
+            uint32_t *g = hist + (int64_t)(e0 + e) * nbins + 2 * wd;
+            if (lo) {
+                uint64_t nv = (uint64_t)g[0] + lo;
+                if (nv > 0xffffffffull) { overflow = true; nv = 0xffffffffull; }
+                g[0] = (uint32_t)nv;
+            }
+            if (hi && 2 * wd + 1 < nbins) {
+                uint64_t nv = (uint64_t)g[1] + hi;
+                if (nv > 0xffffffffull) { overflow = true; nv = 0xffffffffull; }
+                g[1] = (uint32_t)nv;
+            }
+        }
+        cluster.sync();
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) nan_count += __shfl_xor_sync(0xffffffffu, nan_count, o);
+    if (status) {
+        if (lane == 0 && nan_count) atomicAdd(&status[ST_NAN], nan_count);
+        if (overflow) atomicExch(&status[ST_OVERFLOW], 1);
+    }
+}
+
+// One block.  Warp w reads expert e's histogram, finds the first bin whose cumulative count
+// reaches r = (1 - k/E) N_e (a ballot over an inclusive warp scan) and interpolates inside
+// it, in fp64.  The mean over experts is a fixed-order reduction.
+__global__ void __launch_bounds__(1024)
+qb_update_kernel(const uint32_t *__restrict__ hist, int E, int nbins, int k,
+                 float *__restrict__ q_out, float *__restrict__ bias) {
+    extern __shared__ double q_s[];
+    __shared__ double red[32];
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const double p = 1.0 - (double)k / (double)E;
+    for (int e = w; e < E; e += 32) {
+        const uint32_t *h = hist + (int64_t)e * nbins;
+        unsigned long long N = 0;
+        for (int b = lane; b < nbins; b += 32) N += h[b];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) N += __shfl_xor_sync(0xffffffffu, N, o);
+        const double r = p * (double)N;
+        double q = 0.0;
+        if (r > 0.0) {
+            unsigned long long carry = 0;
+            for (int b0 = 0; b0 < nbins; b0 += 32) {
+                const bool in = b0 + lane < nbins;
+                const unsigned long long c = in ? h[b0 + lane] : 0ull;
+                unsigned long long inc = c;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    unsigned long long n = __shfl_up_sync(0xffffffffu, inc, o);
+                    if (lane >= o) inc += n;
+                }
+                const unsigned long long C = carry + inc;
+                const unsigned m = __ballot_sync(0xffffffffu, in && (double)C >= r);
+                if (m) {
+                    const int l = __ffs(m) - 1;
+                    double qq = 0.0;
+                    if (lane == l)
+                        qq = ((double)(b0 + l) + (r - (double)(C - c)) / (double)c) / (double)nbins;
+                    q = __shfl_sync(0xffffffffu, qq, l);
+                    break;
+                }
+                carry += __shfl_sync(0xffffffffu, inc, 31);
+            }
+        }
+        if (lane == 0) q_s[e] = q;
+    }
+    __syncthreads();
+    double s = 0.0;
+    for (int e = tid; e < E; e += blockDim.x) s += q_s[e];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) red[w] = s;
+    __syncthreads();
+    if (w == 0) {
+        double v = red[lane];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) red[0] = v;
+    }
+    __syncthreads();
+    const double cbar = red[0] / (double)E;
+    for (int e = tid; e < E; e += blockDim.x) {
+        bias[e] = (float)(cbar - q_s[e]);
+        if (q_out) q_out[e] = (float)q_s[e];
+    }
+}
+
+}  // namespace
+
+int launch_qb_histogram(const float *scores, int64_t T, int E, int nbins, uint32_t *hist,
+                        int32_t *status, cudaStream_t st) {
+    if (T <= 0) return SLMOE_OK;
+    const int nwords_e = (nbins + 1) >> 1;
+    const int wstride = nwords_e | 1;                 // odd stride spreads lanes over banks
+    const size_t smem = (size_t)QB_SLAB * wstride * sizeof(uint32_t);
+    cudaError_t e = cudaFuncSetAttribute(qb_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return fail(SLMOE_ECUDA, "qb smem attribute: %s", cudaGetErrorString(e));
+    const int nslabs = (E + QB_SLAB - 1) / QB_SLAB;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(nslabs, QB_CLUSTER, 1);
+    cfg.blockDim = dim3(QB_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = QB_CLUSTER;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, qb_hist_kernel, scores, T, E, nbins, wstride, hist, status);
+    if (e != cudaSuccess) return fail(SLMOE_ECUDA, "qb histogram launch: %s", cudaGetErrorString(e));
+    return check_launch("qb_histogram");
+}
+
+int launch_qb_update(const uint32_t *hist, int E, int nbins, int k, float *q_out, float *bias,
+                     cudaStream_t st) {
+    const size_t smem = (size_t)E * sizeof(double);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(qb_update_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return fail(SLMOE_ECUDA, "qb update smem: %s", cudaGetErrorString(e));
+    }
+    qb_update_kernel<<<1, 1024, smem, st>>>(hist, E, nbins, k, q_out, bias);
+    return check_launch("qb_update");
+}
+
+}  // namespace slmoe

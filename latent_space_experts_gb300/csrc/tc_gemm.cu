@@ -1,0 +1,817 @@
+// tcgen05 / TMEM / TMA kernels of the bf16 layer type (sm_103a).
+//
+// Two persistent, warp-specialised GEMM kernels carry every contraction of the layer:
+//
+//  * dense_kernel  C[T, N] = epi(A[T, K] B[N, K]^T) with A = activations, B = weights, both
+//    loaded by TMA into 128-byte-swizzled shared memory; one thread issues
+//    tcgen05.mma (M = 128, N = BN, K = 16) into a double-buffered TMEM accumulator, four
+//    epilogue warps read it back with tcgen05.ld.  K may be cut into up to four segments,
+//    each with its own pair of tensor maps; the segments add into one accumulator
+//    (used for y = z W_out^T + sum_s h_s W2_s^T and for the three router weight pieces).
+//    Epilogues: bf16 store, SiTU-GLU (gate tile rows 0..127, up rows 128..255 of B) and
+//    the router's sigmoid(logit + mu) in fp32 from PACC partial accumulators.
+//
+//  * grouped_kernel  the routed experts, with the weights as the MMA's M operand
+//    ("swap AB"): for expert e and a block of 256 output features it computes
+//    D[feature, token] = W_e[feature, :] . X[token, :] for all tokens routed to e (up to 256
+//    per pass, N rounded to 16).  The tokens' rows are gathered by index with cp.async into
+//    the same swizzled layout a TMA load would produce, so the weights - the bytes that
+//    bound this step - stream from HBM once per expert while the few tokens of each expert
+//    cost a 16-wide MMA column granule instead of a 128-row tile.
+//    Epilogues: SiTU-GLU -> h (expert gate/up), bf16 store -> y_e (expert down).
+//
+// Every wait on an mbarrier is bounded (%globaltimer); on expiry the kernel sets a shared
+// abort flag, every role leaves its loop, status[2] is set and TMEM is freed.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+
+#include "common.cuh"
+#include "tc_gemm.h"
+
+namespace slmoe {
+namespace {
+
+constexpr uint64_t WAIT_LIMIT_NS = 4000000000ull;
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t su32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t gtimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t n) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(n) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t addr, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for the phase of the given parity.  False = gave up (abort flag set).
+__device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, volatile int *abort_flag) {
+    const uint32_t a = su32(b);
+    if (mbar_try(a, parity)) return true;
+    const uint64_t t0 = gtimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try(a, parity)) return true;
+        if ((it & 255u) == 0) {
+            if (*abort_flag) return false;
+            if (gtimer() - t0 > WAIT_LIMIT_NS) {
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint64_t *bar,
+                                            int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(map), "r"(su32(bar)), "r"(c0), "r"(c1)
+        : "memory");
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                     uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     su32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+#define TMEM_LD16(taddr, r)                                                                        \
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 "                                         \
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"                \
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),       \
+                   "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),     \
+                   "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])                           \
+                 : "r"(taddr))
+
+// K-major operand tile of rows x 64 bf16 (128 bytes per row) with the 128-byte swizzle:
+// 8-row groups 1024 bytes apart.  The start address advances 32 bytes per K = 16 step.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Instruction descriptor, kind::f16: bf16 A and B (K-major), fp32 D, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// ---------------------------------------------------------------- dense kernel
+constexpr int EPI_BF16 = 0, EPI_GLU = 1, EPI_ROUTER = 2;
+
+struct TmaPack {
+    CUtensorMap a[4];
+    CUtensorMap b[4];
+};
+
+struct DenseArgs {
+    int M, N;              // output rows and columns (GLU: h columns)
+    int nseg;
+    int kblocks[4];        // 64-wide K blocks per segment
+    int glu_up_row;        // GLU: B-map row of the up half of h column n is n + glu_up_row
+    int tiles_n, tiles;
+    void *C;
+    long long ldc;
+    const float *mu;       // ROUTER: logit offset per column (nullable)
+    float beta1, beta2;
+    int32_t *status;
+};
+
+template <int BN, int EPI, int PACC>
+struct DenseCfg {
+    static constexpr int BM = 128, BK = 64;
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE = A_BYTES + B_BYTES;
+    static constexpr int STAGES = (196 * 1024) / STAGE;
+    static constexpr int BN_OUT = EPI == EPI_GLU ? BN / 2 : BN;
+    static constexpr int ACC = BN * PACC;                 // columns of one accumulator set
+    static constexpr int NBUF = 2 * ACC <= 512 ? 2 : 1;
+    static constexpr int TMEM_COLS = NBUF * ACC;          // a power of two here
+    static constexpr int SMEM = STAGES * STAGE + 1024 + 256;
+    static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM columns");
+};
+
+template <int BN, int EPI, int PACC>
+__global__ void __launch_bounds__(192, 1) dense_kernel(const __grid_constant__ TmaPack maps,
+                                                       const DenseArgs a) {
+    using Cfg = DenseCfg<BN, EPI, PACC>;
+    constexpr int STAGES = Cfg::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * Cfg::STAGE);
+    uint64_t *empty = full + STAGES;
+    uint64_t *tfull = empty + STAGES;
+    uint64_t *tempty = tfull + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 4);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    tc_before();
+    __syncthreads();
+    tc_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int tile = blockIdx.x; tile < a.tiles; tile += gridDim.x) {
+            const int m0 = (tile / a.tiles_n) * Cfg::BM;
+            const int n0 = (tile % a.tiles_n) * Cfg::BN_OUT;
+            for (int s = 0; s < a.nseg; ++s) {
+                for (int kb = 0; kb < a.kblocks[s]; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) goto done;
+                    mbar_expect_tx(&full[stage], Cfg::STAGE);
+                    const uint32_t sa = su32(smem + stage * Cfg::STAGE);
+                    const uint32_t sb = sa + Cfg::A_BYTES;
+                    tma_load_2d(sa, &maps.a[s], &full[stage], kb * Cfg::BK, m0);
+                    if (EPI == EPI_GLU) {
+                        tma_load_2d(sb, &maps.b[s], &full[stage], kb * Cfg::BK, n0);
+                        tma_load_2d(sb + (BN / 2) * 128, &maps.b[s], &full[stage], kb * Cfg::BK,
+                                    n0 + a.glu_up_row);
+                    } else {
+                        tma_load_2d(sb, &maps.b[s], &full[stage], kb * Cfg::BK, n0);
+                    }
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------ MMA issuer
+        constexpr uint32_t IDESC = idesc_bf16(128, BN);
+        int stage = 0;
+        uint32_t phase = 0;
+        int buf = 0;
+        uint32_t bphase = 0;
+        for (int tile = blockIdx.x; tile < a.tiles; tile += gridDim.x) {
+            if (!mbar_wait(&tempty[buf], bphase ^ 1, abort_flag)) goto done;
+            tc_after();
+            const uint32_t dbase = tmem_base + buf * Cfg::ACC;
+            int kg = 0;
+            for (int s = 0; s < a.nseg; ++s) {
+                for (int kb = 0; kb < a.kblocks[s]; ++kb, ++kg) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag)) goto done;
+                    tc_after();
+                    const uint32_t d = dbase + (kg % PACC) * BN;
+                    const uint32_t sa = su32(smem + stage * Cfg::STAGE);
+                    const uint32_t sb = sa + Cfg::A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma(d, sdesc(sa + kk * 32), sdesc(sb + kk * 32), IDESC,
+                             (kg >= PACC || kk > 0) ? 1u : 0u);
+                    umma_commit(&empty[stage]);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+            umma_commit(&tfull[buf]);
+            if (++buf == 2) { buf = 0; bphase ^= 1; }
+        }
+    } else if (warp >= 2) {
+        // ------------------------------------------------ epilogue warps
+        const int q = warp & 3;                       // TMEM lane quarter of this warp
+        const int row_in_tile = q * 32 + lane;
+        int ktot = 0;
+        for (int s = 0; s < a.nseg; ++s) ktot += a.kblocks[s];
+        const int nparts = ktot < PACC ? ktot : PACC;
+        int buf = 0;
+        uint32_t bphase = 0;
+        for (int tile = blockIdx.x; tile < a.tiles; tile += gridDim.x) {
+            if (!mbar_wait(&tfull[buf], bphase, abort_flag)) goto done;
+            tc_after();
+            const int row = (tile / a.tiles_n) * Cfg::BM + row_in_tile;
+            const int n0 = (tile % a.tiles_n) * Cfg::BN_OUT;
+            const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + buf * Cfg::ACC;
+            const bool row_ok = row < a.M;
+            if (EPI == EPI_BF16) {
+                __nv_bfloat16 *C = static_cast<__nv_bfloat16 *>(a.C) + (long long)row * a.ldc;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 16) {
+                    uint32_t r[16];
+                    TMEM_LD16(tb + c, r);
+                    tmem_wait_ld();
+                    const int n = n0 + c;
+                    if (row_ok) {
+                        if (n + 16 <= a.N) {
+                            uint4 v0 = make_uint4(pack_bf16(__uint_as_float(r[0]), __uint_as_float(r[1])),
+                                                  pack_bf16(__uint_as_float(r[2]), __uint_as_float(r[3])),
+                                                  pack_bf16(__uint_as_float(r[4]), __uint_as_float(r[5])),
+                                                  pack_bf16(__uint_as_float(r[6]), __uint_as_float(r[7])));
+                            uint4 v1 = make_uint4(pack_bf16(__uint_as_float(r[8]), __uint_as_float(r[9])),
+                                                  pack_bf16(__uint_as_float(r[10]), __uint_as_float(r[11])),
+                                                  pack_bf16(__uint_as_float(r[12]), __uint_as_float(r[13])),
+                                                  pack_bf16(__uint_as_float(r[14]), __uint_as_float(r[15])));
+                            *reinterpret_cast<uint4 *>(C + n) = v0;
+                            *reinterpret_cast<uint4 *>(C + n + 8) = v1;
+                        } else {
+                            for (int i = 0; i < 16 && n + i < a.N; ++i)
+                                C[n + i] = __float2bfloat16_rn(__uint_as_float(r[i]));
+                        }
+                    }
+                }
+            } else if (EPI == EPI_GLU) {
+                __nv_bfloat16 *C = static_cast<__nv_bfloat16 *>(a.C) + (long long)row * a.ldc;
+                const float ib1 = 1.0f / a.beta1, ib2 = 1.0f / a.beta2;
+#pragma unroll 1
+                for (int c = 0; c < BN / 2; c += 16) {
+                    uint32_t g[16], u[16];
+                    TMEM_LD16(tb + c, g);
+                    TMEM_LD16(tb + BN / 2 + c, u);
+                    tmem_wait_ld();
+                    const int n = n0 + c;
+                    if (row_ok) {
+                        float h[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            h[i] = situ_glu_fast(__uint_as_float(g[i]), __uint_as_float(u[i]), ib1, a.beta1,
+                                                 ib2, a.beta2);
+                        if (n + 16 <= a.N) {
+                            uint4 v0 = make_uint4(pack_bf16(h[0], h[1]), pack_bf16(h[2], h[3]),
+                                                  pack_bf16(h[4], h[5]), pack_bf16(h[6], h[7]));
+                            uint4 v1 = make_uint4(pack_bf16(h[8], h[9]), pack_bf16(h[10], h[11]),
+                                                  pack_bf16(h[12], h[13]), pack_bf16(h[14], h[15]));
+                            *reinterpret_cast<uint4 *>(C + n) = v0;
+                            *reinterpret_cast<uint4 *>(C + n + 8) = v1;
+                        } else {
+                            for (int i = 0; i < 16 && n + i < a.N; ++i) C[n + i] = __float2bfloat16_rn(h[i]);
+                        }
+                    }
+                }
+            } else {   // EPI_ROUTER
+                float *C = static_cast<float *>(a.C) + (long long)row * a.ldc;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 16) {
+                    float acc[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+                    for (int p = 0; p < nparts; ++p) {
+                        uint32_t r[16];
+                        TMEM_LD16(tb + p * BN + c, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) acc[i] += __uint_as_float(r[i]);
+                    }
+                    const int n = n0 + c;
+                    if (row_ok) {
+                        for (int i = 0; i < 16 && n + i < a.N; ++i) {
+                            float v = acc[i] + (a.mu ? a.mu[n + i] : 0.f);
+                            C[n + i] = 1.0f / (1.0f + expf(-v));
+                        }
+                    }
+                }
+            }
+            tc_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[buf]);
+            if (++buf == 2) { buf = 0; bphase ^= 1; }
+        }
+    }
+done:
+    __syncthreads();
+    if (warp == 1) {
+        tc_after();
+        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+    if (threadIdx.x == 0 && *abort_flag && a.status) atomicExch(&a.status[ST_TIMEOUT], 1);
+}
+
+// ---------------------------------------------------------------- grouped (routed experts)
+constexpr int G_NMAX = 256;           // tokens per pass (MMA N, rounded up to 16)
+constexpr int G_STAGES = 3;
+constexpr int G_A_BYTES = 2 * 128 * 128;          // two 128-row weight sub-tiles
+constexpr int G_B_BYTES = G_NMAX * 128;           // up to 256 token rows
+constexpr int G_STAGE = G_A_BYTES + G_B_BYTES;
+constexpr int G_SMEM = G_STAGES * G_STAGE + 1024 + 256;
+constexpr int G_THREADS = 320;                    // TMA, MMA, 4 epilogue, 4 gather warps
+constexpr int G_GATHER_THREADS = 128;
+
+struct GroupedArgs {
+    int E, kblocks, nfb;
+    int a_rows_pe;        // rows of the weight view per expert
+    int a_sub1;           // row offset of sub-tile 1 inside a feature block
+    int a_fb_stride;      // rows between feature blocks
+    const int32_t *counts, *offsets;
+    const int32_t *b_index;               // nullable: token row = b_index[off + r]
+    const __nv_bfloat16 *b_src;
+    long long b_ld;
+    int b_K;
+    __nv_bfloat16 *out;
+    long long out_ld;
+    int out_cols;
+    float beta1, beta2;
+    int32_t *status;
+};
+
+template <int EPI>
+__global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                               const GroupedArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + G_STAGES * G_STAGE);
+    uint64_t *empty = full + G_STAGES;
+    uint64_t *tfull = empty + G_STAGES;
+    uint64_t *tempty = tfull + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < G_STAGES; ++s) {
+            mbar_init(&full[s], 1 + G_GATHER_THREADS);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(tfull, 1);
+        mbar_init(tempty, 4);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, 512);
+    tc_before();
+    __syncthreads();
+    tc_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int units = a.E * a.nfb;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ weights by TMA
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int u = blockIdx.x; u < units; u += gridDim.x) {
+            const int e = u / a.nfb, fb = u - e * a.nfb;
+            const int n_e = a.counts[e];
+            const int row0 = e * a.a_rows_pe + fb * a.a_fb_stride;
+            for (int c0 = 0; c0 < n_e; c0 += G_NMAX) {
+                for (int kb = 0; kb < a.kblocks; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) goto done;
+                    mbar_expect_tx(&full[stage], G_A_BYTES);
+                    const uint32_t sa = su32(smem + stage * G_STAGE);
+                    tma_load_2d(sa, &wmap, &full[stage], kb * 64, row0);
+                    tma_load_2d(sa + 128 * 128, &wmap, &full[stage], kb * 64, row0 + a.a_sub1);
+                    if (++stage == G_STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------ MMA issuer
+        int stage = 0;
+        uint32_t phase = 0, tphase = 0;
+        for (int u = blockIdx.x; u < units; u += gridDim.x) {
+            const int e = u / a.nfb;
+            const int n_e = a.counts[e];
+            for (int c0 = 0; c0 < n_e; c0 += G_NMAX) {
+                const int N = min(G_NMAX, n_e - c0);
+                const int Np = (N + 15) & ~15;
+                const uint32_t idesc = idesc_bf16(128, Np);
+                if (!mbar_wait(tempty, tphase ^ 1, abort_flag)) goto done;
+                tc_after();
+                for (int kb = 0; kb < a.kblocks; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag)) goto done;
+                    tc_after();
+                    const uint32_t sa = su32(smem + stage * G_STAGE);
+                    const uint32_t sb = sa + G_A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+                        const uint64_t bd = sdesc(sb + kk * 32);
+                        umma(tmem_base, sdesc(sa + kk * 32), bd, idesc, acc);
+                        umma(tmem_base + 256, sdesc(sa + 128 * 128 + kk * 32), bd, idesc, acc);
+                    }
+                    umma_commit(&empty[stage]);
+                    if (++stage == G_STAGES) { stage = 0; phase ^= 1; }
+                }
+                umma_commit(tfull);
+                tphase ^= 1;
+            }
+        }
+    } else if (warp >= 2 && warp < 6) {
+        // ------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const int lf = q * 32 + lane;                 // feature inside a 128-row sub-tile
+        const float ib1 = 1.0f / a.beta1, ib2 = 1.0f / a.beta2;
+        uint32_t tphase = 0;
+        for (int u = blockIdx.x; u < units; u += gridDim.x) {
+            const int e = u / a.nfb, fb = u - e * a.nfb;
+            const int n_e = a.counts[e];
+            const int off = a.offsets[e];
+            for (int c0 = 0; c0 < n_e; c0 += G_NMAX) {
+                const int N = min(G_NMAX, n_e - c0);
+                const int Np = (N + 15) & ~15;
+                if (!mbar_wait(tfull, tphase, abort_flag)) goto done;
+                tc_after();
+                const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16);
+                if (EPI == EPI_GLU) {
+                    const int f = fb * 128 + lf;
+                    const bool ok = f < a.out_cols;
+                    __nv_bfloat16 *o = a.out + (long long)(off + c0) * a.out_ld + f;
+                    for (int c = 0; c < Np; c += 16) {
+                        uint32_t g[16], v[16];
+                        TMEM_LD16(tb + c, g);
+                        TMEM_LD16(tb + 256 + c, v);
+                        tmem_wait_ld();
+                        if (ok) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                if (c + i < N)
+                                    o[(long long)(c + i) * a.out_ld] = __float2bfloat16_rn(situ_glu_fast(
+                                        __uint_as_float(g[i]), __uint_as_float(v[i]), ib1, a.beta1, ib2, a.beta2));
+                            }
+                        }
+                    }
+                } else {
+                    const int f0 = fb * 256 + lf, f1 = f0 + 128;
+                    const bool ok0 = f0 < a.out_cols, ok1 = f1 < a.out_cols;
+                    __nv_bfloat16 *o = a.out + (long long)(off + c0) * a.out_ld;
+                    for (int c = 0; c < Np; c += 16) {
+                        uint32_t r0[16], r1[16];
+                        TMEM_LD16(tb + c, r0);
+                        TMEM_LD16(tb + 256 + c, r1);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            if (c + i < N) {
+                                __nv_bfloat16 *orow = o + (long long)(c + i) * a.out_ld;
+                                if (ok0) orow[f0] = __float2bfloat16_rn(__uint_as_float(r0[i]));
+                                if (ok1) orow[f1] = __float2bfloat16_rn(__uint_as_float(r1[i]));
+                            }
+                        }
+                    }
+                }
+                tc_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty);
+                tphase ^= 1;
+            }
+        }
+    } else if (warp >= 6) {
+        // ------------------------------------------------ token-row gather (cp.async)
+        const int gt = threadIdx.x - 6 * 32;          // 0..127
+        const int ch = gt & 7;                         // 16-byte chunk of the 128-byte row
+        const int rsub = gt >> 3;                      // rows rsub, rsub + 16, ...
+        int stage = 0;
+        uint32_t phase = 0;
+        int pending = -1;
+        for (int u = blockIdx.x; u < units; u += gridDim.x) {
+            const int e = u / a.nfb;
+            const int n_e = a.counts[e];
+            const int off = a.offsets[e];
+            for (int c0 = 0; c0 < n_e; c0 += G_NMAX) {
+                const int N = min(G_NMAX, n_e - c0);
+                const int Np = (N + 15) & ~15;
+                const __nv_bfloat16 *src[G_NMAX / 16];
+#pragma unroll
+                for (int j = 0; j < G_NMAX / 16; ++j) {
+                    const int r = rsub + 16 * j;
+                    long long row = 0;
+                    if (r < N) row = a.b_index ? a.b_index[off + c0 + r] : (long long)(off + c0 + r);
+                    src[j] = a.b_src + row * a.b_ld + ch * 8;
+                }
+                for (int kb = 0; kb < a.kblocks; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
+                        cp_async_wait<0>();
+                        goto done;
+                    }
+                    const uint32_t sb = su32(smem + stage * G_STAGE + G_A_BYTES);
+                    const bool kok = kb * 64 + ch * 8 < a.b_K;
+#pragma unroll
+                    for (int j = 0; j < G_NMAX / 16; ++j) {
+                        const int r = rsub + 16 * j;
+                        if (r < Np) {
+                            const uint32_t dst = sb + r * 128 + ((ch ^ (r & 7)) << 4);
+                            cp_async16(dst, src[j] + kb * 64, (r < N && kok) ? 16u : 0u);
+                        }
+                    }
+                    cp_async_commit();
+                    if (pending >= 0) {
+                        cp_async_wait<1>();
+                        fence_proxy_async();
+                        mbar_arrive(&full[pending]);
+                    }
+                    pending = stage;
+                    if (++stage == G_STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+        }
+        cp_async_wait<0>();
+        fence_proxy_async();
+        if (pending >= 0) mbar_arrive(&full[pending]);
+    }
+done:
+    __syncthreads();
+    if (warp == 1) {
+        tc_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+    if (threadIdx.x == 0 && *abort_flag && a.status) atomicExch(&a.status[ST_TIMEOUT], 1);
+}
+
+// ---------------------------------------------------------------- router weight split
+// hi = bf16(w), mid = bf16(w - hi), lo = bf16(w - hi - mid): each difference is exact in
+// fp32 and the last one has at most 8 significant bits, so hi + mid + lo == w.
+__global__ void split_router_kernel(const float *__restrict__ w, __nv_bfloat16 *__restrict__ out,
+                                    long long n) {
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x) {
+        const float v = w[i];
+        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+        const float r1 = v - __bfloat162float(hi);
+        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+        const float r2 = r1 - __bfloat162float(mid);
+        out[i] = hi;
+        out[n + i] = mid;
+        out[2 * n + i] = __float2bfloat16_rn(r2);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int get_encode() {
+    if (g_encode) return SLMOE_OK;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return fail(SLMOE_ECUDA, "cuTensorMapEncodeTiled not available");
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return SLMOE_OK;
+}
+
+// 2-D bf16 tensor map: rows x cols (cols innermost), row pitch in elements, box 64 x box_rows,
+// 128-byte swizzle, out-of-range elements read as zero.
+int make_map(CUtensorMap *m, const void *base, long long rows, long long cols, long long pitch,
+             int box_rows) {
+    int rc = get_encode();
+    if (rc) return rc;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)pitch * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(SLMOE_ECUDA, "cuTensorMapEncodeTiled failed (%d): rows %lld cols %lld pitch %lld box %d",
+                    (int)r, rows, cols, pitch, box_rows);
+    return SLMOE_OK;
+}
+
+template <typename K>
+int set_smem(K kern, int bytes) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return fail(SLMOE_ECUDA, "smem attribute: %s", cudaGetErrorString(e));
+    return SLMOE_OK;
+}
+
+template <int BN, int EPI, int PACC>
+int launch_dense(const TmaPack &maps, DenseArgs a, cudaStream_t st) {
+    using Cfg = DenseCfg<BN, EPI, PACC>;
+    a.tiles_n = (a.N + Cfg::BN_OUT - 1) / Cfg::BN_OUT;
+    a.tiles = ((a.M + Cfg::BM - 1) / Cfg::BM) * a.tiles_n;
+    if (a.tiles == 0) return SLMOE_OK;
+    auto kern = dense_kernel<BN, EPI, PACC>;
+    int rc = set_smem(kern, Cfg::SMEM);
+    if (rc) return rc;
+    const int sms = sm_count();
+    const int grid = a.tiles < sms ? a.tiles : sms;
+    kern<<<grid, 192, Cfg::SMEM, st>>>(maps, a);
+    return check_launch("dense_kernel");
+}
+
+template <int EPI>
+int launch_grouped(const CUtensorMap &wmap, const GroupedArgs &a, cudaStream_t st) {
+    auto kern = grouped_kernel<EPI>;
+    int rc = set_smem(kern, G_SMEM);
+    if (rc) return rc;
+    const int units = a.E * a.nfb;
+    const int sms = sm_count();
+    const int grid = units < sms ? units : sms;
+    if (grid == 0) return SLMOE_OK;
+    kern<<<grid, G_THREADS, G_SMEM, st>>>(wmap, a);
+    return check_launch("grouped_kernel");
+}
+
+}  // namespace
+
+int tc_router_scores(const slmoe_config *c, const void *x, const float *W_r, const float *mu,
+                     __nv_bfloat16 *wsplit, float *scores, int32_t *status, cudaStream_t st) {
+    const long long n = (long long)c->E * c->d;
+    split_router_kernel<<<(int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096), 256, 0, st>>>(W_r, wsplit, n);
+    int rc = check_launch("split_router");
+    if (rc) return rc;
+    TmaPack maps;
+    memset(&maps, 0, sizeof(maps));
+    DenseArgs a = {};
+    a.M = c->T;
+    a.N = c->E;
+    a.nseg = 3;
+    for (int s = 0; s < 3; ++s) {
+        if ((rc = make_map(&maps.a[s], x, c->T, c->d, c->d, 128))) return rc;
+        if ((rc = make_map(&maps.b[s], wsplit + (size_t)s * n, c->E, c->d, c->d, 128))) return rc;
+        a.kblocks[s] = (c->d + 63) / 64;
+    }
+    a.C = scores;
+    a.ldc = c->E;
+    a.mu = mu;
+    a.status = status;
+    return launch_dense<128, EPI_ROUTER, 2>(maps, a, st);
+}
+
+int tc_forward_bf16(const slmoe_config *c, const void *x, const slmoe_weights *w, const TcForward &f,
+                    void *y, cudaStream_t st) {
+    const int T = c->T, d = c->d, dl = c->d_latent, E = c->E, k = c->k, I = c->I;
+    const int ns = c->n_shared, Is = c->I_shared;
+    const long long Tk = (long long)T * k;
+    int rc;
+    using bf = __nv_bfloat16;
+
+    {   // latent down-projection: x_lat = x W_in^T
+        TmaPack maps;
+        memset(&maps, 0, sizeof(maps));
+        if ((rc = make_map(&maps.a[0], x, T, d, d, 128))) return rc;
+        if ((rc = make_map(&maps.b[0], w->W_in, dl, d, d, 256))) return rc;
+        DenseArgs a = {};
+        a.M = T; a.N = dl; a.nseg = 1; a.kblocks[0] = (d + 63) / 64;
+        a.C = f.x_lat; a.ldc = dl; a.status = f.status;
+        if ((rc = launch_dense<256, EPI_BF16, 1>(maps, a, st))) return rc;
+    }
+    stage_event(3, st);
+    {   // routed experts, gate|up + SiTU-GLU: h[perm row] = GLU(W13[e] x_lat[token])
+        CUtensorMap wm;
+        if ((rc = make_map(&wm, w->W13, (long long)E * 2 * I, dl, dl, 128))) return rc;
+        GroupedArgs a = {};
+        a.E = E; a.kblocks = (dl + 63) / 64; a.nfb = (I + 127) / 128;
+        a.a_rows_pe = 2 * I; a.a_sub1 = I; a.a_fb_stride = 128;
+        a.counts = f.counts; a.offsets = f.offsets; a.b_index = f.perm;
+        a.b_src = static_cast<const bf *>(f.x_lat); a.b_ld = dl; a.b_K = dl;
+        a.out = static_cast<bf *>(f.h); a.out_ld = I; a.out_cols = I;
+        a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
+        if ((rc = launch_grouped<EPI_GLU>(wm, a, st))) return rc;
+    }
+    stage_event(4, st);
+    {   // routed experts, down: y_e[row] = W2[e] h[row]
+        CUtensorMap wm;
+        if ((rc = make_map(&wm, w->W2, (long long)E * dl, I, I, 128))) return rc;
+        GroupedArgs a = {};
+        a.E = E; a.kblocks = (I + 63) / 64; a.nfb = (dl + 255) / 256;
+        a.a_rows_pe = dl; a.a_sub1 = 128; a.a_fb_stride = 256;
+        a.counts = f.counts; a.offsets = f.offsets; a.b_index = nullptr;
+        a.b_src = static_cast<const bf *>(f.h); a.b_ld = I; a.b_K = I;
+        a.out = static_cast<bf *>(f.y_e); a.out_ld = dl; a.out_cols = dl;
+        a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
+        if ((rc = launch_grouped<EPI_BF16>(wm, a, st))) return rc;
+    }
+    stage_event(5, st);
+    (void)Tk;
+    if ((rc = launch_combine_rmsnorm(DT_BF16, f.y_e, f.topk_w, f.slot_pos, w->gamma, T, dl, k, c->eps, f.z, st)))
+        return rc;
+    stage_event(6, st);
+    for (int s = 0; s < ns; ++s) {   // shared experts, gate|up + SiTU-GLU on full d
+        TmaPack maps;
+        memset(&maps, 0, sizeof(maps));
+        if ((rc = make_map(&maps.a[0], x, T, d, d, 128))) return rc;
+        if ((rc = make_map(&maps.b[0], static_cast<const bf *>(w->W13_s) + (size_t)s * 2 * Is * d, 2 * Is, d, d,
+                           128)))
+            return rc;
+        DenseArgs a = {};
+        a.M = T; a.N = Is; a.nseg = 1; a.kblocks[0] = (d + 63) / 64; a.glu_up_row = Is;
+        a.C = static_cast<bf *>(f.h_s) + (size_t)s * Is; a.ldc = (long long)ns * Is;
+        a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
+        if ((rc = launch_dense<256, EPI_GLU, 1>(maps, a, st))) return rc;
+    }
+    stage_event(7, st);
+    {   // y = z W_out^T + sum_s h_s W2_s^T, K cut into 1 + n_shared segments
+        TmaPack maps;
+        memset(&maps, 0, sizeof(maps));
+        DenseArgs a = {};
+        a.M = T; a.N = d; a.nseg = 1 + ns;
+        if ((rc = make_map(&maps.a[0], f.z, T, dl, dl, 128))) return rc;
+        if ((rc = make_map(&maps.b[0], w->W_out, d, dl, dl, 256))) return rc;
+        a.kblocks[0] = (dl + 63) / 64;
+        for (int s = 0; s < ns; ++s) {
+            if ((rc = make_map(&maps.a[1 + s], static_cast<const bf *>(f.h_s) + (size_t)s * Is, T, Is,
+                               (long long)ns * Is, 128)))
+                return rc;
+            if ((rc = make_map(&maps.b[1 + s], static_cast<const bf *>(w->W2_s) + (size_t)s * d * Is, d, Is, Is,
+                               256)))
+                return rc;
+            a.kblocks[1 + s] = (Is + 63) / 64;
+        }
+        a.C = y; a.ldc = d; a.status = f.status;
+        if ((rc = launch_dense<256, EPI_BF16, 1>(maps, a, st))) return rc;
+    }
+    stage_event(8, st);
+    return SLMOE_OK;
+}
+
+}  // namespace slmoe

@@ -271,3 +271,8 @@ def qb_update(hist, k):
     q = qb_quantile(hist, k)
     cbar = q.mean()
     return q, cbar - q
+
+
+def expert_output(inp, e, h):
+    """y_e = W2[e] . h for given hidden rows (used to check one stage)."""
+    return f64(h) @ f64(inp["W2"][int(e)]).T

@@ -1,0 +1,117 @@
+"""GPU parity of the Quantile Balancing engine: histogram counts bit-exact against the oracle
+on the same fp32 scores, quantiles and biases within 1e-6 (both in fp64 from identical counts)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+import latent_space_experts_gb300 as lse
+from gpu_util import need_gpu, run_route, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_hist(scores, nbins=1000, hist=None, status=None):
+    T, E = scores.shape
+    if hist is None:
+        hist = torch.zeros(E, nbins, dtype=torch.int32, device="cuda")
+    lse.slmoe_qb_histogram(scores, T, E, nbins, hist, status)
+    return hist
+
+
+def test_qb_engine_full_size_eight_micro_batches():
+    """65536 tokens x 896 experts per micro-batch, 8 micro-batches added in place, then the
+    (1 - 16/896) quantile and the bias update."""
+    need_gpu()
+    q = synthetic.QB
+    hist = torch.zeros(q.E, q.nbins, dtype=torch.int32, device="cuda")
+    ref = np.zeros((q.E, q.nbins), dtype=np.uint64)
+    for m in range(q.micro_batches):
+        s = synthetic.qb_scores(m, q, device="cuda")
+        gpu_hist(s, q.nbins, hist)
+        ref = oracle.qb_histogram(s.cpu().numpy(), q.nbins, ref)
+    torch.cuda.synchronize()
+    h = hist.cpu().numpy().view(np.uint32).astype(np.uint64)
+    assert np.array_equal(h, ref)
+    assert np.all(h.sum(axis=1) == q.T * q.micro_batches)
+    q_out = torch.empty(q.E, device="cuda")
+    bias = torch.empty(q.E, device="cuda")
+    lse.slmoe_qb_update(hist, q.E, q.nbins, q.k, q_out, bias)
+    q_ref, b_ref = oracle.qb_update(ref, q.k)
+    assert np.max(np.abs(q_out.cpu().numpy() - q_ref)) <= 1e-6
+    assert np.max(np.abs(bias.cpu().numpy() - b_ref)) <= 1e-6
+
+
+@pytest.mark.parametrize("T,E,nbins", [(1, 1, 1000), (1000, 33, 1000), (5000, 64, 999), (777, 100, 10),
+                                       (200000, 40, 1000), (3, 2048, 1000)])
+def test_histogram_shapes(T, E, nbins):
+    need_gpu()
+    g = torch.Generator(device="cpu").manual_seed(T + E)
+    s = torch.rand(T, E, generator=g, dtype=torch.float32)
+    s[0, 0] = 0.0
+    s[-1, -1] = 1.0
+    hist = gpu_hist(s.cuda(), nbins)
+    torch.cuda.synchronize()
+    assert np.array_equal(hist.cpu().numpy().view(np.uint32), oracle.qb_histogram(s.numpy(), nbins))
+
+
+def test_histogram_edges_and_nan():
+    need_gpu()
+    edges = (np.arange(0, 1001) / 1000.0).astype(np.float32)
+    vals = np.concatenate([edges, np.nextafter(edges, np.float32(0)), np.nextafter(edges, np.float32(2)),
+                           [np.nan, np.nan]]).astype(np.float32)
+    vals = np.clip(np.nan_to_num(vals, nan=-1.0), 0, 1).astype(np.float32)
+    vals[-2:] = np.nan
+    s = np.stack([vals, vals[::-1]], axis=1).copy()
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    hist = gpu_hist(torch.from_numpy(s).cuda(), 1000, status=status)
+    torch.cuda.synchronize()
+    assert np.array_equal(hist.cpu().numpy().view(np.uint32), oracle.qb_histogram(s, 1000))
+    assert int(status[0]) == 4
+
+
+def test_update_closed_forms_on_gpu():
+    need_gpu()
+    E, k = 8, 2
+    uni = torch.ones(E, 1000, dtype=torch.int32, device="cuda")
+    q_out = torch.empty(E, device="cuda")
+    bias = torch.empty(E, device="cuda")
+    lse.slmoe_qb_update(uni, E, 1000, k, q_out, bias)
+    assert np.allclose(q_out.cpu().numpy(), 1 - k / E, atol=1e-7)
+    assert np.allclose(bias.cpu().numpy(), 0.0, atol=1e-7)
+    empty = torch.zeros(E, 1000, dtype=torch.int32, device="cuda")
+    lse.slmoe_qb_update(empty, E, 1000, k, q_out, bias)
+    assert np.all(q_out.cpu().numpy() == 0.0)
+
+
+def test_fused_route_histogram_matches_standalone():
+    """slmoe_route(hist=...) bins the GPU's own fp32 scores: identical to binning them on the host."""
+    need_gpu()
+    shp = synthetic.LAYERS["mid"]
+    inp = to_dev(synthetic.layer_inputs(shp, seed=0))
+    hist = torch.zeros(shp.E, shp.nbins, dtype=torch.int32, device="cuda")
+    out = run_route(lse.config(shp), inp, hist=hist)
+    ref = oracle.qb_histogram(out["scores"].numpy(), shp.nbins)
+    assert np.array_equal(hist.cpu().numpy().view(np.uint32), ref)
+
+
+def test_qb_rebalances_k3_routing():
+    """Route 8 micro-batches of K3-shaped scores, update the bias by QB, route a held-out
+    micro-batch: report max/mean load before and after (the pages fix no target value)."""
+    need_gpu()
+    q = synthetic.QB
+    T = 8192
+    hist = torch.zeros(q.E, q.nbins, dtype=torch.int32, device="cuda")
+    for m in range(q.micro_batches):
+        gpu_hist(synthetic.qb_scores(m, q, device="cuda", T=T), q.nbins, hist)
+    bias = torch.empty(q.E, device="cuda")
+    lse.slmoe_qb_update(hist, q.E, q.nbins, q.k, None, bias)
+    held = synthetic.qb_scores(q.micro_batches, q, device="cuda", T=T).cpu().numpy()
+    sel0, _, _ = oracle.select_topk(held, np.zeros(q.E), q.k)
+    sel1, _, _ = oracle.select_topk(held, bias.cpu().numpy(), q.k)
+    L0, L1 = oracle.expert_loads(sel0, q.E), oracle.expert_loads(sel1, q.E)
+    assert L0.sum() == L1.sum() == T * q.k
+    r0, r1 = L0.max() / L0.mean(), L1.max() / L1.mean()
+    print(f"max/mean load before QB {r0:.2f}, after {r1:.2f}")
+    assert r1 < r0

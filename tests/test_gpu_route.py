@@ -1,0 +1,139 @@
+"""GPU parity of slmoe_route against the oracle: router scores, biased top-k selection
+(bit-exact outside near ties), gate weights, and the expert-sorted permutation (bit-exact)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+import latent_space_experts_gb300 as lse
+from gpu_util import NEAR_TIE, need_gpu, run_route, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def check_route(shape, inp_cpu, score_tol):
+    cfg = lse.config(shape)
+    inp = to_dev(inp_cpu)
+    out = run_route(cfg, inp)
+    T, E, k = shape.T, shape.E, shape.k
+    s_ref = oracle.router_scores(inp_cpu["x"], inp_cpu["W_r"], inp_cpu.get("logit_offset"))
+    s_gpu = out["scores"].double().numpy()
+    serr = np.max(np.abs(s_gpu - s_ref)) if T else 0.0
+    assert serr <= score_tol, f"score error {serr:.2e}"
+
+    sel_ref, gates_ref, gap = oracle.select_topk(s_ref, inp_cpu["bias"], k)
+    sel = out["topk_idx"].numpy()
+    w = out["topk_w"].double().numpy()
+    keep = gap >= NEAR_TIE
+    for t in np.nonzero(keep)[0]:
+        assert set(sel[t].tolist()) == set(sel_ref[t].tolist()), f"token {t}"
+        ref_w = dict(zip(sel_ref[t].tolist(), gates_ref[t].tolist()))
+        for j in range(k):
+            assert abs(w[t, j] - ref_w[int(sel[t, j])]) <= 1e-5
+    # every token (excluded ones too): k distinct experts, slot order valid under the GPU's
+    # own fp32 biased scores, weights sum to 1
+    b = inp_cpu["bias"].numpy()
+    for t in range(T):
+        assert len(set(sel[t].tolist())) == k and sel[t].min() >= 0 and sel[t].max() < E
+        v = (out["scores"][t].numpy() + b)[sel[t]]
+        for j in range(k - 1):
+            assert v[j] > v[j + 1] or (v[j] == v[j + 1] and sel[t, j] < sel[t, j + 1])
+        rest = np.setdiff1d(np.arange(E), sel[t])
+        if rest.size:
+            vb = out["scores"][t].numpy() + b
+            worst = v.min()
+            assert np.all((vb[rest] < worst) | ((vb[rest] == worst) & (rest > sel[t][v == worst].max())))
+        assert abs(w[t].sum() - 1.0) < 1e-5
+
+    counts, offsets, perm, slot_pos = oracle.permutation(sel, E)
+    assert np.array_equal(out["counts"].numpy(), counts)
+    assert np.array_equal(out["offsets"].numpy(), offsets)
+    assert np.array_equal(out["perm"].numpy()[:T * k], perm)
+    assert np.array_equal(out["slot_pos"].numpy()[:T * k].reshape(T, k), slot_pos)
+    return int((~keep).sum()), serr
+
+
+@pytest.mark.parametrize("name", ["tiny", "mid"])
+def test_route_configs(name):
+    need_gpu()
+    shp = synthetic.LAYERS[name]
+    inp = synthetic.layer_inputs(shp, seed=0)
+    excluded, serr = check_route(shp, inp, score_tol=2e-6)
+    print(f"{name}: near-tie tokens excluded {excluded}/{shp.T}, max score err {serr:.2e}")
+
+
+@pytest.mark.parametrize("over", [dict(T=1), dict(T=65, E=33, k=5), dict(T=130, E=4, k=4),
+                                  dict(T=200, E=96, k=8), dict(T=3, E=1, k=1)])
+def test_route_edge_shapes_f32(over):
+    need_gpu()
+    shp = synthetic.shape_with("tiny", **over)
+    inp = synthetic.layer_inputs(shp, seed=1)
+    check_route(shp, inp, score_tol=2e-6)
+
+
+@pytest.mark.parametrize("over", [dict(T=1), dict(T=77, E=40, k=3), dict(T=300, E=256, k=16, d=512)])
+def test_route_edge_shapes_bf16(over):
+    need_gpu()
+    shp = synthetic.shape_with("mid", **over)
+    inp = synthetic.layer_inputs(shp, seed=2)
+    check_route(shp, inp, score_tol=2e-6)
+
+
+def test_route_exact_ties_and_saturated_scores():
+    """All-equal scores pick the lowest indices; s = 1.0 exactly (saturated sigmoid) ties too."""
+    need_gpu()
+    shp = synthetic.shape_with("tiny", T=64, E=16, k=4)
+    inp = synthetic.layer_inputs(shp, seed=3)
+    inp["W_r"].zero_()
+    out = run_route(lse.config(shp), to_dev(inp))
+    assert np.all(out["scores"].numpy() == 0.5)
+    assert np.array_equal(out["topk_idx"].numpy(), np.tile(np.arange(4), (64, 1)))
+    assert np.allclose(out["topk_w"].numpy(), 0.25)
+    mu = torch.zeros(16)
+    mu[[3, 9, 12]] = 100.0                       # sigmoid saturates to exactly 1.0 in fp32
+    inp["logit_offset"] = mu
+    out = run_route(lse.config(shp), to_dev(inp))
+    assert np.all(out["scores"].numpy()[:, [3, 9, 12]] == 1.0)
+    assert np.array_equal(out["topk_idx"].numpy()[:, :3], np.tile([3, 9, 12], (64, 1)))
+    assert np.all(out["topk_idx"].numpy()[:, 3] == 0)
+
+
+def test_route_zero_token_experts_and_bias():
+    """A large negative bias empties experts; counts are 0 and offsets stay monotone."""
+    need_gpu()
+    shp = synthetic.shape_with("tiny", T=64, E=16, k=2)
+    inp = synthetic.layer_inputs(shp, seed=4)
+    inp["bias"] = torch.zeros(16)
+    inp["bias"][8:] = -10.0
+    out = run_route(lse.config(shp), to_dev(inp))
+    assert np.all(out["counts"].numpy()[8:] == 0)
+    assert np.all(out["topk_idx"].numpy() < 8)
+    check_route(shp, inp, score_tol=2e-6)
+
+
+def test_route_nan_scores_are_counted():
+    need_gpu()
+    shp = synthetic.shape_with("tiny", T=8, E=16, k=2)
+    inp = synthetic.layer_inputs(shp, seed=5)
+    inp["x"][5, 0] = float("nan")
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    out = run_route(lse.config(shp), to_dev(inp), status=status)
+    assert int(status[0]) == 16
+    assert np.array_equal(out["topk_idx"].numpy()[5], [0, 1])   # nothing but NaN: lowest index
+    ref = oracle.router_scores(inp["x"][[0, 1, 2]], inp["W_r"])
+    sel_ref, _, _ = oracle.select_topk(ref, inp["bias"][:], 2)
+    assert np.array_equal(np.sort(out["topk_idx"].numpy()[[0, 1, 2]], 1), np.sort(sel_ref, 1))
+
+
+def test_route_empty_batch():
+    need_gpu()
+    shp = synthetic.shape_with("tiny", T=0)
+    cfg = lse.config(shp)
+    counts = torch.full((16,), 7, dtype=torch.int32, device="cuda")
+    offsets = torch.full((17,), 7, dtype=torch.int32, device="cuda")
+    ws = torch.empty(lse.slmoe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    lse.slmoe_route(cfg, None, None, None, None, None, None, None, counts, offsets, None, None, None,
+                    None, ws)
+    torch.cuda.synchronize()
+    assert counts.sum().item() == 0 and offsets.sum().item() == 0

@@ -1,0 +1,93 @@
+"""The C ABI library builds, loads without a GPU, exports every symbol the header declares,
+and rejects bad arguments on the host before any launch.  CPU only."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import synthetic
+import latent_space_experts_gb300 as lse
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "slmoe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    lse.build()
+    return lse.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(slmoe_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_four_calls():
+    syms = declared_symbols()
+    for s in ("slmoe_route", "slmoe_qb_histogram", "slmoe_qb_update", "slmoe_forward",
+              "slmoe_workspace_size", "slmoe_last_error"):
+        assert s in syms
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for s in declared_symbols():
+        assert hasattr(lib, s), s
+        assert s in lse.__all__, f"binding does not expose {s}"
+
+
+def test_workspace_size_and_layout(lib):
+    for name, shp in synthetic.LAYERS.items():
+        cfg = lse.config(shp)
+        n = lse.slmoe_workspace_size(cfg)
+        L = lse.slmoe_workspace_layout_get(cfg)
+        assert L["total"] == n > 0
+        offs = [L[k] for k in ("scores", "topk_idx", "topk_w", "counts", "offsets", "perm",
+                               "slot_pos", "x_lat", "h", "y_e", "z", "h_s", "status")]
+        assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+        es = 2 if shp.dtype == "bf16" else 4
+        assert L["h"] - L["x_lat"] >= shp.T * shp.d_latent * es
+        assert L["z"] - L["y_e"] >= shp.T * shp.k * shp.d_latent * es
+
+
+@pytest.mark.parametrize("field,value", [("k", 0), ("k", 33), ("E", 0), ("E", 5000), ("d", 100),
+                                         ("dtype", 7), ("nbins", 0), ("n_shared", 4), ("T", -1)])
+def test_bad_configs_are_rejected(lib, field, value):
+    cfg = lse.config(synthetic.LAYERS["mid"])
+    setattr(cfg, field, value)
+    assert lib.slmoe_workspace_size(ctypes.byref(cfg)) == 0
+    assert lib.slmoe_last_error().decode() != ""
+    with pytest.raises(lse.SlmoeError):
+        lse.slmoe_workspace_size(cfg)
+
+
+def test_k_above_E_is_rejected(lib):
+    cfg = lse.config(synthetic.LAYERS["tiny"])
+    cfg.k = cfg.E + 1
+    assert lib.slmoe_workspace_size(ctypes.byref(cfg)) == 0
+    assert "k" in lib.slmoe_last_error().decode()
+
+
+def test_null_and_misaligned_arguments_fail_before_launch(lib):
+    cfg = lse.config(synthetic.LAYERS["tiny"])
+    n = lse.slmoe_workspace_size(cfg)
+    fake = ctypes.c_void_p(1 << 20)                 # never dereferenced: validation fails first
+    args = [ctypes.byref(cfg)] + [None] * 13 + [fake, n, None]
+    rc = lib.slmoe_route(*args)
+    assert rc == -1 and "NULL" in lib.slmoe_last_error().decode()
+    mis = ctypes.c_void_p((1 << 20) + 4)
+    rc = lib.slmoe_route(ctypes.byref(cfg), *([fake] * 11), None, None, mis, n, None)
+    assert rc == -1 and "aligned" in lib.slmoe_last_error().decode()
+    rc = lib.slmoe_route(ctypes.byref(cfg), *([fake] * 11), None, None, fake, n - 256, None)
+    assert rc == -4
+    rc = lib.slmoe_qb_histogram(None, 10, 4, 1000, fake, None, None)
+    assert rc == -1
+    rc = lib.slmoe_qb_histogram(fake, 10, 4, 5000, fake, None, None)
+    assert rc == -1
+    rc = lib.slmoe_qb_update(fake, 4, 1000, 5, None, fake, None)
+    assert rc == -1
+    w = lse.Weights()
+    rc = lib.slmoe_forward(ctypes.byref(cfg), fake, ctypes.byref(w), fake, None, fake, None, None,
+                           None, fake, n, None)
+    assert rc == -1 and "W_r" in lib.slmoe_last_error().decode()
