@@ -225,9 +225,8 @@ def main():
     shp = synthetic.LAYERS[args.workload]
     cfg = lse.config(shp)
     inp = synthetic.layer_inputs(shp, seed=rank, device="cuda", heavy_skew=args.skew)
-    act = torch.bfloat16 if shp.dtype == "bf16" else torch.float32
     ws = torch.zeros(lse.slmoe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
-    y = torch.empty(shp.T, shp.d, dtype=act, device="cuda")
+    y = torch.empty(shp.T, shp.d, dtype=torch.float32, device="cuda")
     hist = torch.zeros(shp.E, shp.nbins, dtype=torch.int32, device="cuda")
     bias = inp["bias"].clone()
     status = torch.zeros(4, dtype=torch.int32, device="cuda")

@@ -52,8 +52,8 @@ extern "C" {
 #define SLMOE_ECUDA        (-3)  /* a CUDA runtime or launch error                       */
 #define SLMOE_ENOSPACE     (-4)  /* the workspace is smaller than slmoe_workspace_size() */
 
-#define SLMOE_F32  0             /* x, projection weights, y and intermediates in fp32  */
-#define SLMOE_BF16 1             /* the same in bf16 (fp32 accumulation, fp32 router)   */
+#define SLMOE_F32  0             /* x, projection weights and intermediates in fp32      */
+#define SLMOE_BF16 1             /* the same in bf16 (fp32 accumulation, fp32 router)    */
 
 /* Shape and constants of one layer.  beta1 / beta2 are the SiTU and soft-cap constants
  * ([K3-arch] SiTU激活优化: 4 and 25), eps the RMSNorm epsilon, nbins the QB histogram
@@ -188,7 +188,8 @@ SLMOE_API int slmoe_qb_update(const uint32_t *hist, int32_t E, int32_t nbins, in
  *   z_t = gamma * c_t / sqrt(mean(c_t^2) + eps);
  *   y_t = z_t . W_out^T + sum_s W2_s[s] . SiTU-GLU(W13_s[s] . x_t)
  * Arguments: x [T,d] act; w as slmoe_weights; bias [E] fp32; logit_offset [E] or NULL;
- *   y [T,d] act (written, not accumulated); topk_idx_out [T,k] int32 or NULL: when given,
+ *   y [T,d] fp32 for both layer types (written, not accumulated; the branch output is kept
+ *   in fp32 because bf16 storage of a heavy-tailed output alone costs up to ~2% of its RMS); topk_idx_out [T,k] int32 or NULL: when given,
  *   the routing is exported there; hist [E,nbins] or NULL: QB histogram of the scores is
  *   added; status as above; workspace as slmoe_workspace_size().  The intermediates stay
  *   readable in the workspace (slmoe_workspace_layout_get).

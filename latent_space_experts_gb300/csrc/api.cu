@@ -149,8 +149,8 @@ static int route_impl(const slmoe_config *c, const Layout &L, char *ws, const vo
     if ((rc = launch_topk(R.scores, bias, c->T, c->E, c->k, R.topk_idx, R.topk_w, R.chunk_counts,
                           status, st)))
         return rc;
-    if ((rc = launch_scan(R.chunk_counts, (int)L.nchunks, c->E, R.counts, R.offsets, st))) return rc;
-    if ((rc = launch_scatter(R.topk_idx, R.chunk_counts, R.offsets, c->T, c->E, c->k, R.perm,
+    if ((rc = launch_scan(R.chunk_counts, (int)L.nchunks, c->E, R.counts, st))) return rc;
+    if ((rc = launch_scatter(R.topk_idx, R.chunk_counts, R.counts, c->T, c->E, c->k, R.offsets, R.perm,
                              R.slot_pos, st)))
         return rc;
     if (hist) {

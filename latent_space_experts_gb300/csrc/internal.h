@@ -62,11 +62,10 @@ int launch_simt_gemm(const SimtGemm &g, cudaStream_t st);
 // ---------------------------------------------------------------- routing
 int launch_topk(const float *scores, const float *bias, int T, int E, int k, int32_t *topk_idx,
                 float *topk_w, int32_t *chunk_counts, int32_t *status, cudaStream_t st);
-int launch_scan(int32_t *chunk_counts, int nchunks, int E, int32_t *counts, int32_t *offsets,
-                cudaStream_t st);
-int launch_scatter(const int32_t *topk_idx, const int32_t *chunk_base, const int32_t *offsets,
-                   int T, int E, int k, int32_t *perm, int32_t *slot_pos, cudaStream_t st);
-constexpr int ROUTE_CHUNK = 64;  // tokens per top-k block / permutation chunk
+int launch_scan(int32_t *chunk_counts, int nchunks, int E, int32_t *counts, cudaStream_t st);
+int launch_scatter(const int32_t *topk_idx, const int32_t *chunk_base, const int32_t *counts, int T,
+                   int E, int k, int32_t *offsets, int32_t *perm, int32_t *slot_pos, cudaStream_t st);
+constexpr int ROUTE_CHUNK = 32;  // tokens per top-k block / permutation chunk
 
 // ---------------------------------------------------------------- QB
 int launch_qb_histogram(const float *scores, int64_t T, int E, int nbins, uint32_t *hist,

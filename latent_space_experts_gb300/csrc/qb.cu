@@ -24,10 +24,10 @@ namespace slmoe {
 namespace {
 
 constexpr int QB_SLAB = 32;
-constexpr int QB_THREADS = 512;
+constexpr int QB_THREADS = 1024;
 constexpr int QB_CLUSTER = 8;
 constexpr int64_t QB_WINDOW = 65535;     // tokens per CTA per window (16-bit counters)
-constexpr int QB_UNROLL = 8;
+constexpr int QB_UNROLL = 16;
 
 __device__ __forceinline__ int qb_bin(float s, float nb, int nbins) {
     // one IEEE fp32 round-to-nearest multiply, then floor, clamped to [0, nbins-1]
@@ -118,69 +118,95 @@ qb_hist_kernel(const float *__restrict__ scores, int64_t T, int E, int nbins, in
     }
 }
 
-// One block.  Warp w reads expert e's histogram, finds the first bin whose cumulative count
-// reaches r = (1 - k/E) N_e (a ballot over an inclusive warp scan) and interpolates inside
-// it, in fp64.  The mean over experts is a fixed-order reduction.
-__global__ void __launch_bounds__(1024)
+// One cluster of QBU_CTAS CTAs; CTA r owns a contiguous range of experts.  A warp loads an
+// expert's whole histogram into registers up front (lane l holds bins l, l + 32, ...), then
+// walks the 32-bin chunks with an inclusive warp scan until the cumulative count reaches
+// r = (1 - k/E) N_e, and interpolates inside that bin, in fp64.  The mean over experts is a
+// fixed-order sum: per CTA in shared memory, then across the cluster's CTAs in rank order
+// through distributed shared memory.  No global scratch.
+constexpr int QBU_CTAS = 8;
+constexpr int QBU_MAXC = 2048 / 32;          // 32-bin chunks per expert (nbins <= 2048)
+
+constexpr int QBU_THREADS = 512;
+
+__global__ void __launch_bounds__(QBU_THREADS, 1)
 qb_update_kernel(const uint32_t *__restrict__ hist, int E, int nbins, int k,
                  float *__restrict__ q_out, float *__restrict__ bias) {
     extern __shared__ double q_s[];
-    __shared__ double red[32];
+    __shared__ double red[QBU_THREADS / 32];
+    __shared__ double part;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int P = (int)cluster.num_blocks();
+    const int rank = (int)cluster.block_rank();
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int per = (E + P - 1) / P;
+    const int e0 = rank * per, e1 = min(E, e0 + per);
     const double p = 1.0 - (double)k / (double)E;
-    for (int e = w; e < E; e += 32) {
+    const int nch = (nbins + 31) / 32;
+    for (int e = e0 + w; e < e1; e += QBU_THREADS / 32) {
         const uint32_t *h = hist + (int64_t)e * nbins;
+        uint32_t v[QBU_MAXC];
         unsigned long long N = 0;
-        for (int b = lane; b < nbins; b += 32) N += h[b];
+#pragma unroll
+        for (int i = 0; i < QBU_MAXC; ++i) {
+            const int b = i * 32 + lane;
+            v[i] = (i < nch && b < nbins) ? h[b] : 0u;
+            N += v[i];
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) N += __shfl_xor_sync(0xffffffffu, N, o);
         const double r = p * (double)N;
         double q = 0.0;
         if (r > 0.0) {
             unsigned long long carry = 0;
-            for (int b0 = 0; b0 < nbins; b0 += 32) {
-                const bool in = b0 + lane < nbins;
-                const unsigned long long c = in ? h[b0 + lane] : 0ull;
-                unsigned long long inc = c;
+            bool found = false;
 #pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    unsigned long long n = __shfl_up_sync(0xffffffffu, inc, o);
-                    if (lane >= o) inc += n;
+            for (int i = 0; i < QBU_MAXC; ++i) {
+                if (!found && i < nch) {
+                    const unsigned long long c = v[i];
+                    unsigned long long inc = c;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const unsigned long long n = __shfl_up_sync(0xffffffffu, inc, o);
+                        if (lane >= o) inc += n;
+                    }
+                    const unsigned long long C = carry + inc;
+                    const unsigned m = __ballot_sync(0xffffffffu, (i * 32 + lane < nbins) && (double)C >= r);
+                    if (m) {
+                        const int l = __ffs(m) - 1;
+                        double qq = 0.0;
+                        if (lane == l)
+                            qq = ((double)(i * 32 + l) + (r - (double)(C - c)) / (double)c) / (double)nbins;
+                        q = __shfl_sync(0xffffffffu, qq, l);
+                        found = true;
+                    }
+                    carry += __shfl_sync(0xffffffffu, inc, 31);
                 }
-                const unsigned long long C = carry + inc;
-                const unsigned m = __ballot_sync(0xffffffffu, in && (double)C >= r);
-                if (m) {
-                    const int l = __ffs(m) - 1;
-                    double qq = 0.0;
-                    if (lane == l)
-                        qq = ((double)(b0 + l) + (r - (double)(C - c)) / (double)c) / (double)nbins;
-                    q = __shfl_sync(0xffffffffu, qq, l);
-                    break;
-                }
-                carry += __shfl_sync(0xffffffffu, inc, 31);
             }
         }
-        if (lane == 0) q_s[e] = q;
+        if (lane == 0) q_s[e - e0] = q;
     }
     __syncthreads();
     double s = 0.0;
-    for (int e = tid; e < E; e += blockDim.x) s += q_s[e];
+    for (int i = tid; i < e1 - e0; i += blockDim.x) s += q_s[i];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     if (lane == 0) red[w] = s;
     __syncthreads();
-    if (w == 0) {
-        double v = red[lane];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) red[0] = v;
+    if (tid == 0) {
+        double t = 0.0;
+        for (int i = 0; i < QBU_THREADS / 32; ++i) t += red[i];
+        part = t;
     }
-    __syncthreads();
-    const double cbar = red[0] / (double)E;
-    for (int e = tid; e < E; e += blockDim.x) {
-        bias[e] = (float)(cbar - q_s[e]);
-        if (q_out) q_out[e] = (float)q_s[e];
+    cluster.sync();
+    double total = 0.0;
+    for (int r = 0; r < P; ++r) total += *cluster.map_shared_rank(&part, r);
+    const double cbar = total / (double)E;
+    for (int e = e0 + tid; e < e1; e += blockDim.x) {
+        bias[e] = (float)(cbar - q_s[e - e0]);
+        if (q_out) q_out[e] = (float)q_s[e - e0];
     }
+    cluster.sync();
 }
 
 }  // namespace
@@ -214,13 +240,24 @@ int launch_qb_histogram(const float *scores, int64_t T, int E, int nbins, uint32
 
 int launch_qb_update(const uint32_t *hist, int E, int nbins, int k, float *q_out, float *bias,
                      cudaStream_t st) {
-    const size_t smem = (size_t)E * sizeof(double);
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(qb_update_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return fail(SLMOE_ECUDA, "qb update smem: %s", cudaGetErrorString(e));
-    }
-    qb_update_kernel<<<1, 1024, smem, st>>>(hist, E, nbins, k, q_out, bias);
+    const size_t smem = (size_t)((E + QBU_CTAS - 1) / QBU_CTAS) * sizeof(double);
+    cudaError_t e = cudaFuncSetAttribute(qb_update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(smem < 48 * 1024 ? 48 * 1024 : smem));
+    if (e != cudaSuccess) return fail(SLMOE_ECUDA, "qb update smem: %s", cudaGetErrorString(e));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(QBU_CTAS, 1, 1);
+    cfg.blockDim = dim3(QBU_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = QBU_CTAS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, qb_update_kernel, hist, E, nbins, k, q_out, bias);
+    if (e != cudaSuccess) return fail(SLMOE_ECUDA, "qb update launch: %s", cudaGetErrorString(e));
     return check_launch("qb_update");
 }
 

@@ -16,13 +16,32 @@ namespace slmoe {
 namespace {
 
 constexpr int TOPK_WARPS = 8;
-constexpr int MAX_E = 4096;          // E per lane <= 128 -> 4 words of "taken" bits
+constexpr int MAX_E = 4096;
+constexpr int LIST = 4;              // candidates each lane keeps in registers
 
 __device__ __forceinline__ bool beats(float v, int i, float w, int j) {
     return v > w || (v == w && i < j);
 }
 
-// One block per chunk of ROUTE_CHUNK tokens, one warp per token at a time.
+// Insert (v, i) into a lane's descending candidate list of LIST entries.
+__device__ __forceinline__ void list_insert(float (&lv)[LIST], int (&li)[LIST], float v, int i) {
+    if (!beats(v, i, lv[LIST - 1], li[LIST - 1])) return;
+    lv[LIST - 1] = v;
+    li[LIST - 1] = i;
+#pragma unroll
+    for (int p = LIST - 1; p > 0; --p) {
+        if (beats(lv[p], li[p], lv[p - 1], li[p - 1])) {
+            float tv = lv[p]; lv[p] = lv[p - 1]; lv[p - 1] = tv;
+            int ti = li[p]; li[p] = li[p - 1]; li[p - 1] = ti;
+        }
+    }
+}
+
+// One block per chunk of ROUTE_CHUNK tokens, one warp per token at a time.  Lane l owns the
+// experts e = l, l + 32, ...; it keeps its best LIST (biased score, index) pairs in
+// registers.  Each of the k rounds takes the warp-wide best head (ties to the lower index)
+// and the owning lane pops it; a lane whose list runs dry rescans its experts for the best
+// ones that its last popped pair beats (everything above that was taken already).
 __global__ void __launch_bounds__(TOPK_WARPS * 32)
 topk_kernel(const float *__restrict__ scores, const float *__restrict__ bias, int T, int E,
             int k, int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
@@ -41,49 +60,50 @@ topk_kernel(const float *__restrict__ scores, const float *__restrict__ bias, in
 
     float *row = rows + (size_t)warp * E;
     const int t_begin = blockIdx.x * ROUTE_CHUNK;
+    const int n_local = lane < E ? (E - lane + 31) / 32 : 0;
     int nan_count = 0;
     for (int tt = warp; tt < ROUTE_CHUNK; tt += TOPK_WARPS) {
         const int t = t_begin + tt;
         if (t >= T) break;
         const float *srow = scores + (int64_t)t * E;
-        float best_v = -INFINITY;
-        int best_i = INT_MAX;
+        float lv[LIST];
+        int li[LIST];
+#pragma unroll
+        for (int p = 0; p < LIST; ++p) { lv[p] = -INFINITY; li[p] = INT_MAX; }
         for (int e = lane; e < E; e += 32) {
-            float s = srow[e];
+            const float s = srow[e];
             row[e] = s;
             float v;
-            if (isnan(s)) {
-                ++nan_count;
-                v = -INFINITY;
-            } else {
-                v = s + bias_s[e];
-            }
-            if (beats(v, e, best_v, best_i)) { best_v = v; best_i = e; }
+            if (isnan(s)) { ++nan_count; v = -INFINITY; } else { v = s + bias_s[e]; }
+            list_insert(lv, li, v, e);
         }
         __syncwarp();
-        uint32_t taken[MAX_E / 32 / 32] = {0, 0, 0, 0};
+        int popped = 0;
         int my_e = 0;
         for (int j = 0; j < k; ++j) {
-            float v = best_v;
-            int i = best_i;
+            float v = lv[0];
+            int i = li[0];
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
-                float ov = __shfl_xor_sync(0xffffffffu, v, o);
-                int oi = __shfl_xor_sync(0xffffffffu, i, o);
+                const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, i, o);
                 if (beats(ov, oi, v, i)) { v = ov; i = oi; }
             }
             if (lane == j) my_e = i;
-            if ((i & 31) == lane) {          // the owner drops the winner and rescans
-                const int q = i >> 5;
-                taken[q >> 5] |= 1u << (q & 31);
-                best_v = -INFINITY;
-                best_i = INT_MAX;
-                int qq = 0;
-                for (int e = lane; e < E; e += 32, ++qq) {
-                    if (taken[qq >> 5] & (1u << (qq & 31))) continue;
-                    float s = row[e];
-                    float bv = isnan(s) ? -INFINITY : s + bias_s[e];
-                    if (beats(bv, e, best_v, best_i)) { best_v = bv; best_i = e; }
+            if (li[0] == i) {                    // this lane owned the winner: pop it
+                const float last_v = lv[0];
+                const int last_i = li[0];
+#pragma unroll
+                for (int p = 0; p < LIST - 1; ++p) { lv[p] = lv[p + 1]; li[p] = li[p + 1]; }
+                lv[LIST - 1] = -INFINITY;
+                li[LIST - 1] = INT_MAX;
+                ++popped;
+                if (li[0] == INT_MAX && popped < n_local) {
+                    for (int e = lane; e < E; e += 32) {
+                        const float s = row[e];
+                        const float bv = isnan(s) ? -INFINITY : s + bias_s[e];
+                        if (beats(last_v, last_i, bv, e)) list_insert(lv, li, bv, e);
+                    }
                 }
             }
         }
@@ -108,82 +128,85 @@ topk_kernel(const float *__restrict__ scores, const float *__restrict__ bias, in
     for (int i = tid; i < E; i += blockDim.x) cc[i] = cnt[i];
 }
 
-// One block: per expert, turn chunk counts into exclusive chunk bases; then the exclusive
-// scan of the expert totals.
-__global__ void __launch_bounds__(1024)
-scan_kernel(int32_t *__restrict__ cc, int nchunks, int E, int32_t *__restrict__ counts,
-            int32_t *__restrict__ offsets) {
-    __shared__ int32_t tot[MAX_E];
-    __shared__ int32_t warp_tot[32];
-    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    for (int e = tid; e < E; e += blockDim.x) {
-        int run = 0;
-        int c = 0;
-        for (; c + 8 <= nchunks; c += 8) {
-            int v[8];
+// Per-expert exclusive scan of the chunk counts (chunk_counts becomes the chunk bases) and
+// the expert totals.  One block per 32 experts (lane = expert); warp w covers a contiguous
+// range of chunks; the warps' partial sums are scanned in shared memory.
+constexpr int SCAN_WARPS = 32;
+constexpr int SCAN_UNROLL = 8;
+__global__ void __launch_bounds__(SCAN_WARPS * 32)
+scan_kernel(int32_t *__restrict__ cc, int nchunks, int E, int32_t *__restrict__ counts) {
+    __shared__ int32_t part[SCAN_WARPS][33];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int e = blockIdx.x * 32 + lane;
+    const bool ok = e < E;
+    const int per = (nchunks + SCAN_WARPS - 1) / SCAN_WARPS;
+    const int c0 = w * per, c1 = min(nchunks, c0 + per);
+    int sum = 0;
+    for (int c = c0; c < c1; c += SCAN_UNROLL) {
+        int v[SCAN_UNROLL];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = cc[(int64_t)(c + u) * E + e];
+        for (int u = 0; u < SCAN_UNROLL; ++u) v[u] = (ok && c + u < c1) ? cc[(int64_t)(c + u) * E + e] : 0;
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                cc[(int64_t)(c + u) * E + e] = run;
-                run += v[u];
-            }
-        }
-        for (; c < nchunks; ++c) {
-            int v = cc[(int64_t)c * E + e];
-            cc[(int64_t)c * E + e] = run;
-            run += v;
-        }
-        counts[e] = run;
-        tot[e] = run;
+        for (int u = 0; u < SCAN_UNROLL; ++u) sum += v[u];
     }
+    part[w][lane] = sum;
     __syncthreads();
-    const int base = tid * 4;
-    int loc[4], s = 0;
+    int base = 0;
+    for (int ww = 0; ww < w; ++ww) base += part[ww][lane];
+    if (w == SCAN_WARPS - 1 && ok) counts[e] = base + sum;
+    int run = base;
+    for (int c = c0; c < c1; c += SCAN_UNROLL) {
+        int v[SCAN_UNROLL];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        loc[i] = (base + i < E) ? tot[base + i] : 0;
-        s += loc[i];
-    }
-    int incl = s;
+        for (int u = 0; u < SCAN_UNROLL; ++u) v[u] = (ok && c + u < c1) ? cc[(int64_t)(c + u) * E + e] : 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        int n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += n;
-    }
-    if (lane == 31) warp_tot[w] = incl;
-    __syncthreads();
-    if (w == 0) {
-        int v = warp_tot[lane], inc = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            int n = __shfl_up_sync(0xffffffffu, inc, o);
-            if (lane >= o) inc += n;
+        for (int u = 0; u < SCAN_UNROLL; ++u) {
+            if (ok && c + u < c1) cc[(int64_t)(c + u) * E + e] = run;
+            run += v[u];
         }
-        warp_tot[lane] = inc - v;
     }
-    __syncthreads();
-    int run = warp_tot[w] + incl - s;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        if (base + i < E) offsets[base + i] = run;
-        run += loc[i];
-    }
-    if (tid == blockDim.x - 1) offsets[E] = run;
 }
 
-// One block per chunk: walk the chunk's tokens in order; lane j places slot j.  The k
-// experts of one token are distinct, so the lanes of one step never share a counter.
-__global__ void __launch_bounds__(128)
+// One block per chunk.  The block first scans the expert totals into offsets (block 0 also
+// writes them out), then one warp walks the chunk's tokens in order; lane j places slot j.
+// The k experts of one token are distinct, so the lanes of one step never share a counter.
+__global__ void __launch_bounds__(256)
 scatter_kernel(const int32_t *__restrict__ topk_idx, const int32_t *__restrict__ chunk_base,
-               const int32_t *__restrict__ offsets, int T, int E, int k,
-               int32_t *__restrict__ perm, int32_t *__restrict__ slot_pos) {
-    extern __shared__ int32_t next[];
-    const int32_t *cb = chunk_base + (int64_t)blockIdx.x * E;
-    for (int i = threadIdx.x; i < E; i += blockDim.x) next[i] = offsets[i] + cb[i];
+               const int32_t *__restrict__ counts, int T, int E, int k,
+               int32_t *__restrict__ offsets, int32_t *__restrict__ perm,
+               int32_t *__restrict__ slot_pos) {
+    extern __shared__ int32_t next[];              // [E]
+    __shared__ int32_t wsum[8];
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    // exclusive scan of counts[0..E): thread-contiguous runs, then a warp/block scan
+    const int per = (E + 255) / 256;
+    const int b0 = tid * per;
+    int loc = 0;
+    for (int i = 0; i < per; ++i)
+        if (b0 + i < E) loc += counts[b0 + i];
+    int incl = loc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) wsum[w] = incl;
     __syncthreads();
-    if (threadIdx.x >= 32) return;
-    const int lane = threadIdx.x;
+    int wbase = 0;
+    for (int i = 0; i < w; ++i) wbase += wsum[i];
+    int run = wbase + incl - loc;
+    const int32_t *cb = chunk_base + (int64_t)blockIdx.x * E;
+    for (int i = 0; i < per; ++i) {
+        const int e = b0 + i;
+        if (e < E) {
+            if (blockIdx.x == 0) offsets[e] = run;
+            next[e] = run + cb[e];
+            run += counts[e];
+        }
+    }
+    if (blockIdx.x == 0 && tid == 255) offsets[E] = run;
+    __syncthreads();
+    if (tid >= 32) return;
     const int t0 = blockIdx.x * ROUTE_CHUNK;
     const int t1 = min(T, t0 + ROUTE_CHUNK);
     for (int t = t0; t < t1; ++t) {
@@ -215,18 +238,17 @@ int launch_topk(const float *scores, const float *bias, int T, int E, int k, int
     return check_launch("topk");
 }
 
-int launch_scan(int32_t *chunk_counts, int nchunks, int E, int32_t *counts, int32_t *offsets,
-                cudaStream_t st) {
-    scan_kernel<<<1, 1024, 0, st>>>(chunk_counts, nchunks, E, counts, offsets);
+int launch_scan(int32_t *chunk_counts, int nchunks, int E, int32_t *counts, cudaStream_t st) {
+    scan_kernel<<<(E + 31) / 32, SCAN_WARPS * 32, 0, st>>>(chunk_counts, nchunks, E, counts);
     return check_launch("scan");
 }
 
-int launch_scatter(const int32_t *topk_idx, const int32_t *chunk_base, const int32_t *offsets,
-                   int T, int E, int k, int32_t *perm, int32_t *slot_pos, cudaStream_t st) {
+int launch_scatter(const int32_t *topk_idx, const int32_t *chunk_base, const int32_t *counts, int T,
+                   int E, int k, int32_t *offsets, int32_t *perm, int32_t *slot_pos, cudaStream_t st) {
     const int nchunks = (T + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
     if (nchunks == 0) return SLMOE_OK;
-    scatter_kernel<<<nchunks, 128, E * sizeof(int32_t), st>>>(topk_idx, chunk_base, offsets, T, E,
-                                                              k, perm, slot_pos);
+    scatter_kernel<<<nchunks, 256, E * sizeof(int32_t), st>>>(topk_idx, chunk_base, counts, T, E, k,
+                                                              offsets, perm, slot_pos);
     return check_launch("scatter");
 }
 

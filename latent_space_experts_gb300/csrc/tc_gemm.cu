@@ -8,8 +8,11 @@
 //    epilogue warps read it back with tcgen05.ld.  K may be cut into up to four segments,
 //    each with its own pair of tensor maps; the segments add into one accumulator
 //    (used for y = z W_out^T + sum_s h_s W2_s^T and for the three router weight pieces).
-//    Epilogues: bf16 store, SiTU-GLU (gate tile rows 0..127, up rows 128..255 of B) and
-//    the router's sigmoid(logit + mu) in fp32 from PACC partial accumulators.
+//    Epilogues: bf16 store, fp32 store and SiTU-GLU (gate tile rows 0..127, up rows
+//    128..255 of B).
+//
+//  * router_kernel  the router logits over three bf16 pieces of W_r with the TMEM
+//    accumulator drained into fp32 registers every few K blocks, then sigmoid(logit + mu).
 //
 //  * grouped_kernel  the routed experts, with the weights as the MMA's M operand
 //    ("swap AB"): for expert e and a block of 256 output features it computes
@@ -155,7 +158,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 }
 
 // ---------------------------------------------------------------- dense kernel
-constexpr int EPI_BF16 = 0, EPI_GLU = 1, EPI_ROUTER = 2;
+constexpr int EPI_BF16 = 0, EPI_GLU = 1, EPI_F32 = 3;
 
 struct TmaPack {
     CUtensorMap a[4];
@@ -282,10 +285,7 @@ __global__ void __launch_bounds__(192, 1) dense_kernel(const __grid_constant__ T
         // ------------------------------------------------ epilogue warps
         const int q = warp & 3;                       // TMEM lane quarter of this warp
         const int row_in_tile = q * 32 + lane;
-        int ktot = 0;
-        for (int s = 0; s < a.nseg; ++s) ktot += a.kblocks[s];
-        const int nparts = ktot < PACC ? ktot : PACC;
-        int buf = 0;
+            int buf = 0;
         uint32_t bphase = 0;
         for (int tile = blockIdx.x; tile < a.tiles; tile += gridDim.x) {
             if (!mbar_wait(&tfull[buf], bphase, abort_flag)) goto done;
@@ -320,6 +320,26 @@ __global__ void __launch_bounds__(192, 1) dense_kernel(const __grid_constant__ T
                         }
                     }
                 }
+            } else if (EPI == EPI_F32) {
+                float *C = static_cast<float *>(a.C) + (long long)row * a.ldc;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 16) {
+                    uint32_t r[16];
+                    TMEM_LD16(tb + c, r);
+                    tmem_wait_ld();
+                    const int n = n0 + c;
+                    if (row_ok) {
+                        if (n + 16 <= a.N) {
+#pragma unroll
+                            for (int i = 0; i < 16; i += 4)
+                                *reinterpret_cast<float4 *>(C + n + i) =
+                                    make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
+                                                __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+                        } else {
+                            for (int i = 0; i < 16 && n + i < a.N; ++i) C[n + i] = __uint_as_float(r[i]);
+                        }
+                    }
+                }
             } else if (EPI == EPI_GLU) {
                 __nv_bfloat16 *C = static_cast<__nv_bfloat16 *>(a.C) + (long long)row * a.ldc;
                 const float ib1 = 1.0f / a.beta1, ib2 = 1.0f / a.beta2;
@@ -348,28 +368,6 @@ __global__ void __launch_bounds__(192, 1) dense_kernel(const __grid_constant__ T
                         }
                     }
                 }
-            } else {   // EPI_ROUTER
-                float *C = static_cast<float *>(a.C) + (long long)row * a.ldc;
-#pragma unroll 1
-                for (int c = 0; c < BN; c += 16) {
-                    float acc[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-                    for (int p = 0; p < nparts; ++p) {
-                        uint32_t r[16];
-                        TMEM_LD16(tb + p * BN + c, r);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) acc[i] += __uint_as_float(r[i]);
-                    }
-                    const int n = n0 + c;
-                    if (row_ok) {
-                        for (int i = 0; i < 16 && n + i < a.N; ++i) {
-                            float v = acc[i] + (a.mu ? a.mu[n + i] : 0.f);
-                            C[n + i] = 1.0f / (1.0f + expf(-v));
-                        }
-                    }
-                }
             }
             tc_before();
             __syncwarp();
@@ -382,6 +380,150 @@ done:
     if (warp == 1) {
         tc_after();
         tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+    if (threadIdx.x == 0 && *abort_flag && a.status) atomicExch(&a.status[ST_TIMEOUT], 1);
+}
+
+// ---------------------------------------------------------------- router logits
+// C[T, E] = sigmoid(x . (W_hi + W_mid + W_lo)^T + mu) in fp32.  The three bf16 weight pieces
+// are three K segments added into one accumulator.  To keep the logits fp32-faithful, the
+// MMA accumulates only RT_DRAIN K blocks into a fresh TMEM buffer; the epilogue warps drain
+// each such partial sum into fp32 registers (round-to-nearest adds) while the next chunk
+// fills the other buffer, so no tensor-core accumulation chain is longer than
+// 4 * RT_DRAIN MMA steps.
+constexpr int RT_BN = 128, RT_DRAIN = 4;
+constexpr int RT_STAGE = 128 * 128 + RT_BN * 128;
+constexpr int RT_STAGES = (196 * 1024) / RT_STAGE;
+constexpr int RT_SMEM = RT_STAGES * RT_STAGE + 1024 + 256;
+
+__global__ void __launch_bounds__(192, 1) router_kernel(const __grid_constant__ TmaPack maps,
+                                                        const DenseArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + RT_STAGES * RT_STAGE);
+    uint64_t *empty = full + RT_STAGES;
+    uint64_t *tfull = empty + RT_STAGES;
+    uint64_t *tempty = tfull + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < RT_STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 4);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, 2 * RT_BN);
+    tc_before();
+    __syncthreads();
+    tc_after();
+    const uint32_t tmem_base = *tmem_slot;
+    int ktot = 0;
+    for (int s = 0; s < a.nseg; ++s) ktot += a.kblocks[s];
+
+    if (warp == 0 && lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int tile = blockIdx.x; tile < a.tiles; tile += gridDim.x) {
+            const int m0 = (tile / a.tiles_n) * 128;
+            const int n0 = (tile % a.tiles_n) * RT_BN;
+            for (int s = 0; s < a.nseg; ++s) {
+                for (int kb = 0; kb < a.kblocks[s]; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) goto done;
+                    mbar_expect_tx(&full[stage], RT_STAGE);
+                    const uint32_t sa = su32(smem + stage * RT_STAGE);
+                    tma_load_2d(sa, &maps.a[s], &full[stage], kb * 64, m0);
+                    tma_load_2d(sa + 128 * 128, &maps.b[s], &full[stage], kb * 64, n0);
+                    if (++stage == RT_STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        constexpr uint32_t IDESC = idesc_bf16(128, RT_BN);
+        int stage = 0;
+        uint32_t phase = 0;
+        int buf = 0;
+        uint32_t bphase = 0;
+        for (int tile = blockIdx.x; tile < a.tiles; tile += gridDim.x) {
+            int kg = 0;
+            for (int s = 0; s < a.nseg; ++s) {
+                for (int kb = 0; kb < a.kblocks[s]; ++kb, ++kg) {
+                    const bool first = (kg % RT_DRAIN) == 0;
+                    if (first) {
+                        if (!mbar_wait(&tempty[buf], bphase ^ 1, abort_flag)) goto done;
+                        tc_after();
+                    }
+                    if (!mbar_wait(&full[stage], phase, abort_flag)) goto done;
+                    tc_after();
+                    const uint32_t d = tmem_base + buf * RT_BN;
+                    const uint32_t sa = su32(smem + stage * RT_STAGE);
+                    const uint32_t sb = sa + 128 * 128;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma(d, sdesc(sa + kk * 32), sdesc(sb + kk * 32), IDESC, (!first || kk > 0) ? 1u : 0u);
+                    umma_commit(&empty[stage]);
+                    if (++stage == RT_STAGES) { stage = 0; phase ^= 1; }
+                    if ((kg % RT_DRAIN) == RT_DRAIN - 1 || kg == ktot - 1) {
+                        umma_commit(&tfull[buf]);
+                        if (++buf == 2) { buf = 0; bphase ^= 1; }
+                    }
+                }
+            }
+        }
+    } else if (warp >= 2) {
+        const int q = warp & 3;
+        const int row_in_tile = q * 32 + lane;
+        const int nchunks = (ktot + RT_DRAIN - 1) / RT_DRAIN;
+        int buf = 0;
+        uint32_t bphase = 0;
+        for (int tile = blockIdx.x; tile < a.tiles; tile += gridDim.x) {
+            float acc[RT_BN];
+#pragma unroll
+            for (int i = 0; i < RT_BN; ++i) acc[i] = 0.f;
+            for (int ch = 0; ch < nchunks; ++ch) {
+                if (!mbar_wait(&tfull[buf], bphase, abort_flag)) goto done;
+                tc_after();
+                const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + buf * RT_BN;
+#pragma unroll
+                for (int c = 0; c < RT_BN; c += 16) {
+                    uint32_t r[16];
+                    TMEM_LD16(tb + c, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[c + i] += __uint_as_float(r[i]);
+                }
+                tc_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[buf]);
+                if (++buf == 2) { buf = 0; bphase ^= 1; }
+            }
+            const int row = (tile / a.tiles_n) * 128 + row_in_tile;
+            const int n0 = (tile % a.tiles_n) * RT_BN;
+            if (row < a.M) {
+                float *C = static_cast<float *>(a.C) + (long long)row * a.ldc;
+#pragma unroll
+                for (int i = 0; i < RT_BN; ++i) {
+                    const int n = n0 + i;
+                    if (n < a.N) {
+                        const float v = acc[i] + (a.mu ? a.mu[n] : 0.f);
+                        C[n] = 1.0f / (1.0f + expf(-v));
+                    }
+                }
+            }
+        }
+    }
+done:
+    __syncthreads();
+    if (warp == 1) {
+        tc_after();
+        tmem_dealloc(tmem_base, 2 * RT_BN);
     }
     if (threadIdx.x == 0 && *abort_flag && a.status) atomicExch(&a.status[ST_TIMEOUT], 1);
 }
@@ -717,14 +859,20 @@ int tc_router_scores(const slmoe_config *c, const void *x, const float *W_r, con
     a.nseg = 3;
     for (int s = 0; s < 3; ++s) {
         if ((rc = make_map(&maps.a[s], x, c->T, c->d, c->d, 128))) return rc;
-        if ((rc = make_map(&maps.b[s], wsplit + (size_t)s * n, c->E, c->d, c->d, 128))) return rc;
+        if ((rc = make_map(&maps.b[s], wsplit + (size_t)s * n, c->E, c->d, c->d, RT_BN))) return rc;
         a.kblocks[s] = (c->d + 63) / 64;
     }
     a.C = scores;
     a.ldc = c->E;
     a.mu = mu;
     a.status = status;
-    return launch_dense<128, EPI_ROUTER, 2>(maps, a, st);
+    a.tiles_n = (a.N + RT_BN - 1) / RT_BN;
+    a.tiles = ((a.M + 127) / 128) * a.tiles_n;
+    if (a.tiles == 0) return SLMOE_OK;
+    if ((rc = set_smem(router_kernel, RT_SMEM))) return rc;
+    const int sms = sm_count();
+    router_kernel<<<a.tiles < sms ? a.tiles : sms, 192, RT_SMEM, st>>>(maps, a);
+    return check_launch("router_kernel");
 }
 
 int tc_forward_bf16(const slmoe_config *c, const void *x, const slmoe_weights *w, const TcForward &f,
@@ -808,7 +956,7 @@ int tc_forward_bf16(const slmoe_config *c, const void *x, const slmoe_weights *w
             a.kblocks[1 + s] = (Is + 63) / 64;
         }
         a.C = y; a.ldc = d; a.status = f.status;
-        if ((rc = launch_dense<256, EPI_BF16, 1>(maps, a, st))) return rc;
+        if ((rc = launch_dense<256, EPI_F32, 1>(maps, a, st))) return rc;
     }
     stage_event(8, st);
     return SLMOE_OK;

@@ -103,6 +103,8 @@ def _normal(shape, std, seed, tid, device, chunk_rows=None):
     """N(0, std^2) fp32, drawn in row chunks so that large tensors never need two fp32 copies."""
     g = _gen(seed, tid, device)
     out = torch.empty(shape, dtype=torch.float32, device=device)
+    if out.numel() == 0:
+        return out
     flat = out.view(shape[0], -1)
     step = chunk_rows or flat.shape[0]
     for r0 in range(0, flat.shape[0], step):

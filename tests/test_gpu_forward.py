@@ -12,7 +12,7 @@ import torch
 import oracle
 import synthetic
 import latent_space_experts_gb300 as lse
-from gpu_util import BF16_TOL, F32_TOL, assert_close_rms, need_gpu, to_dev
+from gpu_util import BF16_STORE, BF16_TOL, F32_TOL, assert_close_rms, need_gpu, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -20,8 +20,7 @@ pytestmark = pytest.mark.gpu
 def run_forward(shape, inp, hist=None):
     cfg = lse.config(shape)
     ws = torch.zeros(lse.slmoe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
-    act = torch.bfloat16 if shape.dtype == "bf16" else torch.float32
-    y = torch.empty(shape.T, shape.d, dtype=act, device="cuda")
+    y = torch.empty(shape.T, shape.d, dtype=torch.float32, device="cuda")
     topk = torch.empty(shape.T, shape.k, dtype=torch.int32, device="cuda")
     status = torch.zeros(4, dtype=torch.int32, device="cuda")
     lse.slmoe_forward(cfg, inp["x"], lse.weights(inp), inp["bias"], inp.get("logit_offset"), y, topk,
@@ -32,23 +31,32 @@ def run_forward(shape, inp, hist=None):
 
 
 def check_stages(shape, inp, topk, views, ref, tol, rows=None):
-    """x_lat, h, y_e, z against the oracle (rows: perm positions to check; all if None)."""
+    """x_lat, h, y_e, z against the oracle, each stage judged on its own arithmetic.
+
+    x_lat comes from the exact inputs; h is the oracle's SiTU-GLU expert hidden of the GPU's
+    x_lat rows; y_e is W2[e] applied to the GPU's h rows; z is the oracle's RMSNorm of the
+    oracle-gated combine of the GPU's y_e rows.  rows: perm positions to check (all if None).
+    Intermediates that the bf16 layer stores in bf16 get the storage allowance."""
     T, k = shape.T, shape.k
-    assert_close_rms(views["x_lat"], ref["x_lat"], tol, "x_lat")
+    rel = BF16_STORE if shape.dtype == "bf16" else 0.0
+    assert_close_rms(views["x_lat"], ref["x_lat"], tol, "x_lat", rel)
     perm = views["perm"].cpu().numpy()
     offsets = views["offsets"].cpu().numpy()
+    xl_gpu = views["x_lat"].float().cpu().double().numpy()
     h_gpu = views["h"].float().cpu().numpy()
-    ye_gpu = views["y_e"].float().cpu().numpy()
-    E = shape.E
+    ye_gpu = views["y_e"].float().cpu().double().numpy()
     pos = np.arange(T * k) if rows is None else rows
     expert_of = np.searchsorted(offsets, pos, side="right") - 1
     for e in np.unique(expert_of):
         p = pos[expert_of == e]
-        h_ref = oracle.expert_hidden(inp, e, ref["x_lat"][perm[p]])
-        assert_close_rms(h_gpu[p], h_ref, tol, f"h expert {e}")
+        h_ref = oracle.expert_hidden(inp, e, xl_gpu[perm[p]])
+        assert_close_rms(h_gpu[p], h_ref, tol, f"h expert {e}", rel)
         ye_ref = oracle.expert_output(inp, e, h_gpu[p])
-        assert_close_rms(ye_gpu[p], ye_ref, tol, f"y_e expert {e}")
-    assert_close_rms(views["z"], ref["z"], tol, "z")
+        assert_close_rms(ye_gpu[p], ye_ref, tol, f"y_e expert {e}", rel)
+    slot_pos = views["slot_pos"].cpu().numpy().reshape(T, k)
+    c = np.einsum("tj,tjd->td", ref["gates"], ye_gpu[slot_pos])
+    z_ref = oracle.rmsnorm(c, inp["gamma"], shape.eps)
+    assert_close_rms(views["z"], z_ref, tol, "z", rel)
 
 
 def test_forward_tiny_fp32():
@@ -78,7 +86,7 @@ def test_forward_mid_bf16(seed, gamma_ones):
 
 
 @pytest.mark.parametrize("over", [dict(T=1), dict(T=100, E=8, k=8), dict(T=129, E=40, k=3, I=128),
-                                  dict(T=300, E=4, k=2, I=384, d_latent=320),
+                                  dict(T=600, E=2, k=1, I=384, d_latent=320),
                                   dict(T=64, n_shared=0), dict(T=70, n_shared=3, I_shared=192)])
 def test_forward_bf16_edge_shapes(over):
     """Ragged expert segments (> 256 tokens on one expert, 1 token, none), k = E, widths that
@@ -140,7 +148,7 @@ def test_forward_k3_prefill_sampled_tokens():
     need_gpu()
     shp, inp, y, topk, views, tok, ref = _k3_sampled("k3_prefill", False, 30)
     # the routed branch alone, and z, on the sampled tokens
-    assert_close_rms(views["z"][torch.as_tensor(tok, device="cuda")], ref["z"], BF16_TOL, "z")
+    assert_close_rms(views["z"][torch.as_tensor(tok, device="cuda")], ref["z"], BF16_TOL, "z", BF16_STORE)
     sel_ref, _, gap = oracle.select_topk(ref["scores"], inp["bias"], shp.k)
     keep = gap >= 1e-5
     assert all(set(topk[t].tolist()) == set(sel_ref[i].tolist())

@@ -9,6 +9,10 @@ import synthetic
 import latent_space_experts_gb300 as lse
 from gpu_util import NEAR_TIE, need_gpu, run_route, to_dev
 
+# Router scores must stay within half the near-tie gap of the oracle: then every token whose
+# k-th/(k+1)-th biased gap is >= 1e-5 is decided the same way on both sides.
+SCORE_TOL = NEAR_TIE / 2
+
 pytestmark = pytest.mark.gpu
 
 
@@ -59,7 +63,7 @@ def test_route_configs(name):
     need_gpu()
     shp = synthetic.LAYERS[name]
     inp = synthetic.layer_inputs(shp, seed=0)
-    excluded, serr = check_route(shp, inp, score_tol=2e-6)
+    excluded, serr = check_route(shp, inp, score_tol=SCORE_TOL)
     print(f"{name}: near-tie tokens excluded {excluded}/{shp.T}, max score err {serr:.2e}")
 
 
@@ -69,7 +73,7 @@ def test_route_edge_shapes_f32(over):
     need_gpu()
     shp = synthetic.shape_with("tiny", **over)
     inp = synthetic.layer_inputs(shp, seed=1)
-    check_route(shp, inp, score_tol=2e-6)
+    check_route(shp, inp, score_tol=SCORE_TOL)
 
 
 @pytest.mark.parametrize("over", [dict(T=1), dict(T=77, E=40, k=3), dict(T=300, E=256, k=16, d=512)])
@@ -77,7 +81,7 @@ def test_route_edge_shapes_bf16(over):
     need_gpu()
     shp = synthetic.shape_with("mid", **over)
     inp = synthetic.layer_inputs(shp, seed=2)
-    check_route(shp, inp, score_tol=2e-6)
+    check_route(shp, inp, score_tol=SCORE_TOL)
 
 
 def test_route_exact_ties_and_saturated_scores():
@@ -109,7 +113,7 @@ def test_route_zero_token_experts_and_bias():
     out = run_route(lse.config(shp), to_dev(inp))
     assert np.all(out["counts"].numpy()[8:] == 0)
     assert np.all(out["topk_idx"].numpy() < 8)
-    check_route(shp, inp, score_tol=2e-6)
+    check_route(shp, inp, score_tol=SCORE_TOL)
 
 
 def test_route_nan_scores_are_counted():
