@@ -9,7 +9,8 @@
 // into slabs of 32 (one 128-byte line per row: lane = expert), and each slab is counted by
 // one thread-block cluster of QB_CLUSTER CTAs that split the tokens.  Counters are 16-bit
 // halves of 32-bit shared-memory words (a CTA counts at most 65535 tokens per window, so a
-// half never carries into its neighbour).  At the end of a window the cluster adds its
+// half never carries into its neighbour), stored word-major with the 32 experts of the slab
+// interleaved ([word][lane]), so the 32 lanes of an atomic always hit 32 distinct banks.  At the end of a window the cluster adds its
 // CTAs' counters through distributed shared memory and each bin of global memory is
 // read-modified-written by exactly one thread: no global atomics and no partial
 // histograms in HBM.
@@ -38,9 +39,9 @@ __device__ __forceinline__ int qb_bin(float s, float nb, int nbins) {
 }
 
 __global__ void __launch_bounds__(QB_THREADS)
-qb_hist_kernel(const float *__restrict__ scores, int64_t T, int E, int nbins, int wstride,
+qb_hist_kernel(const float *__restrict__ scores, int64_t T, int E, int nbins,
                uint32_t *__restrict__ hist, int32_t *status) {
-    extern __shared__ uint32_t hs[];                 // [QB_SLAB][wstride] packed 16-bit
+    extern __shared__ uint32_t hs[];                 // [nwords][QB_SLAB] packed 16-bit
     cg::cluster_group cluster = cg::this_cluster();
     const int P = (int)cluster.num_blocks();
     const int rank = (int)cluster.block_rank();
@@ -54,7 +55,7 @@ qb_hist_kernel(const float *__restrict__ scores, int64_t T, int E, int nbins, in
     bool overflow = false;
 
     for (int64_t w0 = 0; w0 < T; w0 += QB_WINDOW * P) {
-        for (int i = tid; i < QB_SLAB * wstride; i += QB_THREADS) hs[i] = 0u;
+        for (int i = tid; i < QB_SLAB * nwords_e; i += QB_THREADS) hs[i] = 0u;
         __syncthreads();
         const int64_t wt1 = min(T, w0 + QB_WINDOW * P);
         const int64_t per = (wt1 - w0 + P - 1) / P;
@@ -62,7 +63,7 @@ qb_hist_kernel(const float *__restrict__ scores, int64_t T, int E, int nbins, in
         const int64_t t1 = min(wt1, t0 + per);
         if (lane < ne) {
             const float *col = scores + e0 + lane;
-            uint32_t *h = hs + lane * wstride;
+            uint32_t *h = hs + lane;
             int64_t t = t0 + warp;
             for (; t + (QB_UNROLL - 1) * nwarps < t1; t += QB_UNROLL * nwarps) {
                 float v[QB_UNROLL];
@@ -72,14 +73,14 @@ qb_hist_kernel(const float *__restrict__ scores, int64_t T, int E, int nbins, in
                 for (int u = 0; u < QB_UNROLL; ++u) {
                     if (isnan(v[u])) { ++nan_count; continue; }
                     const int b = qb_bin(v[u], nb, nbins);
-                    atomicAdd(&h[b >> 1], 1u << ((b & 1) << 4));
+                    atomicAdd(&h[(b >> 1) * QB_SLAB], 1u << ((b & 1) << 4));
                 }
             }
             for (; t < t1; t += nwarps) {
                 const float v = __ldcs(col + t * (int64_t)E);
                 if (isnan(v)) { ++nan_count; continue; }
                 const int b = qb_bin(v, nb, nbins);
-                atomicAdd(&h[b >> 1], 1u << ((b & 1) << 4));
+                atomicAdd(&h[(b >> 1) * QB_SLAB], 1u << ((b & 1) << 4));
             }
         }
         cluster.sync();
@@ -88,11 +89,11 @@ qb_hist_kernel(const float *__restrict__ scores, int64_t T, int E, int nbins, in
         const int share = (total + P - 1) / P;
         const int f0 = rank * share, f1 = min(total, f0 + share);
         for (int f = f0 + tid; f < f1; f += QB_THREADS) {
-            const int e = f / nwords_e, wd = f - e * nwords_e;
+            const int wd = f / ne, e = f - wd * ne;
             uint32_t lo = 0, hi = 0;
             for (int r = 0; r < P; ++r) {
                 const uint32_t *rh = cluster.map_shared_rank(hs, r);
-                const uint32_t v = rh[e * wstride + wd];
+                const uint32_t v = rh[wd * QB_SLAB + e];
                 lo += v & 0xffffu;
                 hi += v >> 16;
             }
@@ -125,8 +126,7 @@ qb_hist_kernel(const float *__restrict__ scores, int64_t T, int E, int nbins, in
 // fixed-order sum: per CTA in shared memory, then across the cluster's CTAs in rank order
 // through distributed shared memory.  No global scratch.
 constexpr int QBU_CTAS = 8;
-constexpr int QBU_MAXC = 2048 / 32;          // 32-bin chunks per expert (nbins <= 2048)
-
+constexpr int QBU_MAXB = 2048 / 32;          // bins per lane (nbins <= 2048)
 constexpr int QBU_THREADS = 512;
 
 __global__ void __launch_bounds__(QBU_THREADS, 1)
@@ -142,47 +142,46 @@ qb_update_kernel(const uint32_t *__restrict__ hist, int E, int nbins, int k,
     const int per = (E + P - 1) / P;
     const int e0 = rank * per, e1 = min(E, e0 + per);
     const double p = 1.0 - (double)k / (double)E;
-    const int nch = (nbins + 31) / 32;
+    const int B = (nbins + 31) / 32;             // bins owned by each lane, contiguous
+    const int b0 = lane * B;
     for (int e = e0 + w; e < e1; e += QBU_THREADS / 32) {
         const uint32_t *h = hist + (int64_t)e * nbins;
-        uint32_t v[QBU_MAXC];
-        unsigned long long N = 0;
+        uint32_t v[QBU_MAXB];
+        unsigned long long S = 0;
 #pragma unroll
-        for (int i = 0; i < QBU_MAXC; ++i) {
-            const int b = i * 32 + lane;
-            v[i] = (i < nch && b < nbins) ? h[b] : 0u;
-            N += v[i];
+        for (int i = 0; i < QBU_MAXB; ++i) {
+            v[i] = (i < B && b0 + i < nbins) ? h[b0 + i] : 0u;
+            S += v[i];
         }
+        unsigned long long inc = S;              // inclusive scan of the lanes' sums
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) N += __shfl_xor_sync(0xffffffffu, N, o);
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long n = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += n;
+        }
+        const unsigned long long N = __shfl_sync(0xffffffffu, inc, 31);
         const double r = p * (double)N;
         double q = 0.0;
         if (r > 0.0) {
-            unsigned long long carry = 0;
-            bool found = false;
+            const unsigned m = __ballot_sync(0xffffffffu, (double)inc >= r);
+            const int l = __ffs(m) - 1;          // the lane whose bins hold rank r
+            double qq = 0.0;
+            if (lane == l) {
+                unsigned long long C = inc - S;  // cumulative count before this lane's bins
+                bool done = false;
 #pragma unroll
-            for (int i = 0; i < QBU_MAXC; ++i) {
-                if (!found && i < nch) {
-                    const unsigned long long c = v[i];
-                    unsigned long long inc = c;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const unsigned long long n = __shfl_up_sync(0xffffffffu, inc, o);
-                        if (lane >= o) inc += n;
+                for (int i = 0; i < QBU_MAXB; ++i) {
+                    if (!done && i < B) {
+                        const unsigned long long prev = C;
+                        C += v[i];
+                        if ((double)C >= r) {
+                            qq = ((double)(b0 + i) + (r - (double)prev) / (double)v[i]) / (double)nbins;
+                            done = true;
+                        }
                     }
-                    const unsigned long long C = carry + inc;
-                    const unsigned m = __ballot_sync(0xffffffffu, (i * 32 + lane < nbins) && (double)C >= r);
-                    if (m) {
-                        const int l = __ffs(m) - 1;
-                        double qq = 0.0;
-                        if (lane == l)
-                            qq = ((double)(i * 32 + l) + (r - (double)(C - c)) / (double)c) / (double)nbins;
-                        q = __shfl_sync(0xffffffffu, qq, l);
-                        found = true;
-                    }
-                    carry += __shfl_sync(0xffffffffu, inc, 31);
                 }
             }
+            q = __shfl_sync(0xffffffffu, qq, l);
         }
         if (lane == 0) q_s[e - e0] = q;
     }
@@ -215,8 +214,7 @@ int launch_qb_histogram(const float *scores, int64_t T, int E, int nbins, uint32
                         int32_t *status, cudaStream_t st) {
     if (T <= 0) return SLMOE_OK;
     const int nwords_e = (nbins + 1) >> 1;
-    const int wstride = nwords_e | 1;                 // odd stride spreads lanes over banks
-    const size_t smem = (size_t)QB_SLAB * wstride * sizeof(uint32_t);
+    const size_t smem = (size_t)QB_SLAB * nwords_e * sizeof(uint32_t);
     cudaError_t e = cudaFuncSetAttribute(qb_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return fail(SLMOE_ECUDA, "qb smem attribute: %s", cudaGetErrorString(e));
@@ -233,7 +231,7 @@ int launch_qb_histogram(const float *scores, int64_t T, int E, int nbins, uint32
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, qb_hist_kernel, scores, T, E, nbins, wstride, hist, status);
+    e = cudaLaunchKernelEx(&cfg, qb_hist_kernel, scores, T, E, nbins, hist, status);
     if (e != cudaSuccess) return fail(SLMOE_ECUDA, "qb histogram launch: %s", cudaGetErrorString(e));
     return check_launch("qb_histogram");
 }

@@ -70,9 +70,18 @@ topk_kernel(const float *__restrict__ scores, const float *__restrict__ bias, in
         int li[LIST];
 #pragma unroll
         for (int p = 0; p < LIST; ++p) { lv[p] = -INFINITY; li[p] = INT_MAX; }
+        // stage the row in shared memory with independent loads first (latency once per
+        // batch, not once per element), then build the candidate lists from it
+        for (int e0 = lane; e0 < E; e0 += 32 * 16) {
+            float v[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) v[u] = (e0 + 32 * u < E) ? __ldcs(srow + e0 + 32 * u) : 0.f;
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+                if (e0 + 32 * u < E) row[e0 + 32 * u] = v[u];
+        }
         for (int e = lane; e < E; e += 32) {
-            const float s = srow[e];
-            row[e] = s;
+            const float s = row[e];
             float v;
             if (isnan(s)) { ++nan_count; v = -INFINITY; } else { v = s + bias_s[e]; }
             list_insert(lv, li, v, e);

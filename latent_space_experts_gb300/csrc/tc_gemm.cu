@@ -387,17 +387,31 @@ done:
 // ---------------------------------------------------------------- router logits
 // C[T, E] = sigmoid(x . (W_hi + W_mid + W_lo)^T + mu) in fp32.  The three bf16 weight pieces
 // are three K segments added into one accumulator.  To keep the logits fp32-faithful, the
-// MMA accumulates only RT_DRAIN K blocks into a fresh TMEM buffer; the epilogue warps drain
-// each such partial sum into fp32 registers (round-to-nearest adds) while the next chunk
-// fills the other buffer, so no tensor-core accumulation chain is longer than
-// 4 * RT_DRAIN MMA steps.
-constexpr int RT_BN = 128, RT_DRAIN = 4;
+// MMA accumulates only RT_DRAIN K blocks into a fresh TMEM buffer; two epilogue
+// warpgroups (columns 0..111 and 112..223) drain each such partial sum into fp32 registers
+// (round-to-nearest adds) while the next chunk fills the other buffer, so no tensor-core
+// accumulation chain is longer than 4 * RT_DRAIN MMA steps.  BN = 224 tiles E = 896 exactly.
+constexpr int RT_BN = 224, RT_HALF = RT_BN / 2, RT_DRAIN = 4;
 constexpr int RT_STAGE = 128 * 128 + RT_BN * 128;
 constexpr int RT_STAGES = (196 * 1024) / RT_STAGE;
 constexpr int RT_SMEM = RT_STAGES * RT_STAGE + 1024 + 256;
+constexpr int RT_THREADS = 320;               // TMA, MMA, 8 epilogue warps
 
-__global__ void __launch_bounds__(192, 1) router_kernel(const __grid_constant__ TmaPack maps,
-                                                        const DenseArgs a) {
+template <int N>
+__device__ __forceinline__ void drain_add(uint32_t taddr, float *acc) {
+    // N x 16 columns: issue all loads, one wait, then add
+    uint32_t r[N][16];
+#pragma unroll
+    for (int b = 0; b < N; ++b) TMEM_LD16(taddr + 16 * b, r[b]);
+    tmem_wait_ld();
+#pragma unroll
+    for (int b = 0; b < N; ++b)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[16 * b + i] += __uint_as_float(r[b][i]);
+}
+
+__global__ void __launch_bounds__(RT_THREADS, 1) router_kernel(const __grid_constant__ TmaPack maps,
+                                                               const DenseArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + RT_STAGES * RT_STAGE);
@@ -415,12 +429,12 @@ __global__ void __launch_bounds__(192, 1) router_kernel(const __grid_constant__ 
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], 4);
+            mbar_init(&tempty[b], 8);
         }
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == 1) tmem_alloc(tmem_slot, 2 * RT_BN);
+    if (warp == 1) tmem_alloc(tmem_slot, 512);
     tc_before();
     __syncthreads();
     tc_after();
@@ -462,7 +476,7 @@ __global__ void __launch_bounds__(192, 1) router_kernel(const __grid_constant__ 
                     }
                     if (!mbar_wait(&full[stage], phase, abort_flag)) goto done;
                     tc_after();
-                    const uint32_t d = tmem_base + buf * RT_BN;
+                    const uint32_t d = tmem_base + buf * 256;
                     const uint32_t sa = su32(smem + stage * RT_STAGE);
                     const uint32_t sb = sa + 128 * 128;
 #pragma unroll
@@ -479,37 +493,32 @@ __global__ void __launch_bounds__(192, 1) router_kernel(const __grid_constant__ 
         }
     } else if (warp >= 2) {
         const int q = warp & 3;
+        const int half = (warp - 2) >> 2;             // column half drained by this warp
         const int row_in_tile = q * 32 + lane;
         const int nchunks = (ktot + RT_DRAIN - 1) / RT_DRAIN;
         int buf = 0;
         uint32_t bphase = 0;
         for (int tile = blockIdx.x; tile < a.tiles; tile += gridDim.x) {
-            float acc[RT_BN];
+            float acc[RT_HALF];
 #pragma unroll
-            for (int i = 0; i < RT_BN; ++i) acc[i] = 0.f;
+            for (int i = 0; i < RT_HALF; ++i) acc[i] = 0.f;
             for (int ch = 0; ch < nchunks; ++ch) {
                 if (!mbar_wait(&tfull[buf], bphase, abort_flag)) goto done;
                 tc_after();
-                const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + buf * RT_BN;
-#pragma unroll
-                for (int c = 0; c < RT_BN; c += 16) {
-                    uint32_t r[16];
-                    TMEM_LD16(tb + c, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) acc[c + i] += __uint_as_float(r[i]);
-                }
+                const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + buf * 256 + half * RT_HALF;
+                drain_add<4>(tb, acc);
+                drain_add<3>(tb + 64, acc + 64);
                 tc_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty[buf]);
                 if (++buf == 2) { buf = 0; bphase ^= 1; }
             }
             const int row = (tile / a.tiles_n) * 128 + row_in_tile;
-            const int n0 = (tile % a.tiles_n) * RT_BN;
+            const int n0 = (tile % a.tiles_n) * RT_BN + half * RT_HALF;
             if (row < a.M) {
                 float *C = static_cast<float *>(a.C) + (long long)row * a.ldc;
 #pragma unroll
-                for (int i = 0; i < RT_BN; ++i) {
+                for (int i = 0; i < RT_HALF; ++i) {
                     const int n = n0 + i;
                     if (n < a.N) {
                         const float v = acc[i] + (a.mu ? a.mu[n] : 0.f);
@@ -523,7 +532,7 @@ done:
     __syncthreads();
     if (warp == 1) {
         tc_after();
-        tmem_dealloc(tmem_base, 2 * RT_BN);
+        tmem_dealloc(tmem_base, 512);
     }
     if (threadIdx.x == 0 && *abort_flag && a.status) atomicExch(&a.status[ST_TIMEOUT], 1);
 }
@@ -871,7 +880,7 @@ int tc_router_scores(const slmoe_config *c, const void *x, const float *W_r, con
     if (a.tiles == 0) return SLMOE_OK;
     if ((rc = set_smem(router_kernel, RT_SMEM))) return rc;
     const int sms = sm_count();
-    router_kernel<<<a.tiles < sms ? a.tiles : sms, 192, RT_SMEM, st>>>(maps, a);
+    router_kernel<<<a.tiles < sms ? a.tiles : sms, RT_THREADS, RT_SMEM, st>>>(maps, a);
     return check_launch("router_kernel");
 }
 

@@ -63,6 +63,10 @@ LAYERS = {
                              n_shared=2, I_shared=2048, dtype="bf16", mu_std=0.5),
     "k3_decode": LayerShape("k3_decode", T=128, d=7168, d_latent=3584, E=896, k=16, I=512,
                             n_shared=2, I_shared=2048, dtype="bf16", mu_std=0.5),
+    # a 1/7 slice of the K3 prefill layer for profiler captures: the same per-expert shapes
+    # and about the same tokens per expert (1170 * 16 / 128 = 146), 1.5 GB on the device
+    "k3_slice": LayerShape("k3_slice", T=1170, d=7168, d_latent=3584, E=128, k=16, I=512,
+                           n_shared=2, I_shared=2048, dtype="bf16", mu_std=0.5),
 }
 
 
