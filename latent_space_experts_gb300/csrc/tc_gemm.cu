@@ -538,19 +538,31 @@ done:
 }
 
 // ---------------------------------------------------------------- grouped (routed experts)
-constexpr int G_NMAX = 256;           // tokens per pass (MMA N, rounded up to 16)
-constexpr int G_STAGES = 3;
-constexpr int G_A_BYTES = 2 * 128 * 128;          // two 128-row weight sub-tiles
-constexpr int G_B_BYTES = G_NMAX * 128;           // up to 256 token rows
-constexpr int G_STAGE = G_A_BYTES + G_B_BYTES;
-constexpr int G_SMEM = G_STAGES * G_STAGE + 1024 + 256;
+// Work unit = (expert e, feature block fb).  NSUB weight sub-tiles of 128 rows (the MMA's M)
+// stream from HBM through an A ring of 128 KB; the expert's token rows (N <= 256 per pass,
+// rounded to 16) are gathered by cp.async from L2 into a 2-deep B ring.  NSUB = 2 pairs the
+// gate rows fb*128.. with the up rows I + fb*128.. for the fused SiTU-GLU; NSUB = 1 (expert
+// down) keeps two TMEM accumulators so a unit's epilogue overlaps the next unit's loads.
+// Each CTA stages its (count, offset) pairs in shared memory at start.
+constexpr int G_NMAX = 256;
 constexpr int G_THREADS = 320;                    // TMA, MMA, 4 epilogue, 4 gather warps
 constexpr int G_GATHER_THREADS = 128;
+constexpr int G_LIST = 1024;                      // units listed in shared memory per CTA
+
+template <int NSUB>
+struct GCfg {
+    static constexpr int A_BYTES = NSUB * 128 * 128;
+    static constexpr int A_STAGES = (128 * 1024) / A_BYTES;
+    static constexpr int B_BYTES = G_NMAX * 128;
+    static constexpr int B_STAGES = 2;
+    static constexpr int NBUF = NSUB == 2 ? 1 : 2;
+    static constexpr int SMEM = A_STAGES * A_BYTES + B_STAGES * B_BYTES + G_LIST * 8 + 1024 + 512;
+};
 
 struct GroupedArgs {
     int E, kblocks, nfb;
     int a_rows_pe;        // rows of the weight view per expert
-    int a_sub1;           // row offset of sub-tile 1 inside a feature block
+    int a_sub1;           // row offset of sub-tile 1 inside a feature block (NSUB = 2)
     int a_fb_stride;      // rows between feature blocks
     const int32_t *counts, *offsets;
     const int32_t *b_index;               // nullable: token row = b_index[off + r]
@@ -564,85 +576,138 @@ struct GroupedArgs {
     int32_t *status;
 };
 
-template <int EPI>
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *map, uint64_t *bar,
+                                                 int c0, int c1, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(map), "r"(su32(bar)), "r"(c0), "r"(c1), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ void cp_async16_hint(uint32_t dst, const void *src, uint32_t src_bytes,
+                                                uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes), "l"(policy)
+                 : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+template <int EPI, int NSUB>
 __global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_constant__ CUtensorMap wmap,
                                                                const GroupedArgs a) {
+    using Cfg = GCfg<NSUB>;
+    constexpr int AST = Cfg::A_STAGES, BST = Cfg::B_STAGES, NBUF = Cfg::NBUF;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + G_STAGES * G_STAGE);
-    uint64_t *empty = full + G_STAGES;
-    uint64_t *tfull = empty + G_STAGES;
-    uint64_t *tempty = tfull + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 1);
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + AST * Cfg::A_BYTES;
+    int2 *list = reinterpret_cast<int2 *>(sB + BST * Cfg::B_BYTES);
+    uint64_t *a_full = reinterpret_cast<uint64_t *>(list + G_LIST);
+    uint64_t *a_empty = a_full + AST;
+    uint64_t *b_full = a_empty + AST;
+    uint64_t *b_empty = b_full + BST;
+    uint64_t *tfull = b_empty + BST;
+    uint64_t *tempty = tfull + NBUF;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + NBUF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int units = a.E * a.nfb;
+    const int my_n = blockIdx.x < units ? (units - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < G_STAGES; ++s) {
-            mbar_init(&full[s], 1 + G_GATHER_THREADS);
-            mbar_init(&empty[s], 1);
+        for (int s = 0; s < AST; ++s) {
+            mbar_init(&a_full[s], 1);
+            mbar_init(&a_empty[s], 1);
         }
-        mbar_init(tfull, 1);
-        mbar_init(tempty, 4);
+        for (int s = 0; s < BST; ++s) {
+            mbar_init(&b_full[s], G_GATHER_THREADS);
+            mbar_init(&b_empty[s], 1);
+        }
+        for (int b = 0; b < NBUF; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 4);
+        }
         *abort_flag = 0;
         fence_barrier_init();
+    }
+    for (int i = threadIdx.x; i < my_n && i < G_LIST; i += blockDim.x) {
+        const int e = (blockIdx.x + i * gridDim.x) / a.nfb;
+        list[i] = make_int2(a.counts[e], a.offsets[e]);
     }
     if (warp == 1) tmem_alloc(tmem_slot, 512);
     tc_before();
     __syncthreads();
     tc_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int units = a.E * a.nfb;
+    auto entry = [&](int i) -> int2 {
+        if (i < G_LIST) return list[i];
+        const int e = (blockIdx.x + i * gridDim.x) / a.nfb;
+        return make_int2(a.counts[e], a.offsets[e]);
+    };
 
     if (warp == 0 && lane == 0) {
-        // ------------------------------------------------ weights by TMA
+        // ------------------------------------------------ weights by TMA (streamed once)
+        const uint64_t pol = policy_evict_first();
         int stage = 0;
         uint32_t phase = 0;
-        for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        for (int i = 0; i < my_n; ++i) {
+            const int u = blockIdx.x + i * gridDim.x;
             const int e = u / a.nfb, fb = u - e * a.nfb;
-            const int n_e = a.counts[e];
+            const int n_e = entry(i).x;
             const int row0 = e * a.a_rows_pe + fb * a.a_fb_stride;
             for (int c0 = 0; c0 < n_e; c0 += G_NMAX) {
                 for (int kb = 0; kb < a.kblocks; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) goto done;
-                    mbar_expect_tx(&full[stage], G_A_BYTES);
-                    const uint32_t sa = su32(smem + stage * G_STAGE);
-                    tma_load_2d(sa, &wmap, &full[stage], kb * 64, row0);
-                    tma_load_2d(sa + 128 * 128, &wmap, &full[stage], kb * 64, row0 + a.a_sub1);
-                    if (++stage == G_STAGES) { stage = 0; phase ^= 1; }
+                    if (!mbar_wait(&a_empty[stage], phase ^ 1, abort_flag)) goto done;
+                    mbar_expect_tx(&a_full[stage], Cfg::A_BYTES);
+                    const uint32_t sa = su32(sA + stage * Cfg::A_BYTES);
+                    tma_load_2d_hint(sa, &wmap, &a_full[stage], kb * 64, row0, pol);
+                    if (NSUB == 2)
+                        tma_load_2d_hint(sa + 128 * 128, &wmap, &a_full[stage], kb * 64, row0 + a.a_sub1, pol);
+                    if (++stage == AST) { stage = 0; phase ^= 1; }
                 }
             }
         }
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------ MMA issuer
-        int stage = 0;
-        uint32_t phase = 0, tphase = 0;
-        for (int u = blockIdx.x; u < units; u += gridDim.x) {
-            const int e = u / a.nfb;
-            const int n_e = a.counts[e];
+        int as = 0, bs = 0, buf = 0;
+        uint32_t aph = 0, bph = 0, tph = 0;
+        for (int i = 0; i < my_n; ++i) {
+            const int n_e = entry(i).x;
             for (int c0 = 0; c0 < n_e; c0 += G_NMAX) {
                 const int N = min(G_NMAX, n_e - c0);
-                const int Np = (N + 15) & ~15;
-                const uint32_t idesc = idesc_bf16(128, Np);
-                if (!mbar_wait(tempty, tphase ^ 1, abort_flag)) goto done;
+                const uint32_t idesc = idesc_bf16(128, (N + 15) & ~15);
+                if (!mbar_wait(&tempty[buf], tph ^ 1, abort_flag)) goto done;
                 tc_after();
+                const uint32_t d = tmem_base + (NSUB == 2 ? 0 : buf * 256);
                 for (int kb = 0; kb < a.kblocks; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, abort_flag)) goto done;
+                    if (!mbar_wait(&a_full[as], aph, abort_flag)) goto done;
+                    if (!mbar_wait(&b_full[bs], bph, abort_flag)) goto done;
                     tc_after();
-                    const uint32_t sa = su32(smem + stage * G_STAGE);
-                    const uint32_t sb = sa + G_A_BYTES;
+                    const uint32_t sa = su32(sA + as * Cfg::A_BYTES);
+                    const uint32_t sb = su32(sB + bs * Cfg::B_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
                         const uint64_t bd = sdesc(sb + kk * 32);
-                        umma(tmem_base, sdesc(sa + kk * 32), bd, idesc, acc);
-                        umma(tmem_base + 256, sdesc(sa + 128 * 128 + kk * 32), bd, idesc, acc);
+                        umma(d, sdesc(sa + kk * 32), bd, idesc, acc);
+                        if (NSUB == 2) umma(d + 256, sdesc(sa + 128 * 128 + kk * 32), bd, idesc, acc);
                     }
-                    umma_commit(&empty[stage]);
-                    if (++stage == G_STAGES) { stage = 0; phase ^= 1; }
+                    umma_commit(&a_empty[as]);
+                    umma_commit(&b_empty[bs]);
+                    if (++as == AST) { as = 0; aph ^= 1; }
+                    if (++bs == BST) { bs = 0; bph ^= 1; }
                 }
-                umma_commit(tfull);
-                tphase ^= 1;
+                umma_commit(&tfull[buf]);
+                if (++buf == NBUF) { buf = 0; tph ^= 1; }
             }
         }
     } else if (warp >= 2 && warp < 6) {
@@ -650,72 +715,64 @@ __global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_cons
         const int q = warp & 3;
         const int lf = q * 32 + lane;                 // feature inside a 128-row sub-tile
         const float ib1 = 1.0f / a.beta1, ib2 = 1.0f / a.beta2;
-        uint32_t tphase = 0;
-        for (int u = blockIdx.x; u < units; u += gridDim.x) {
-            const int e = u / a.nfb, fb = u - e * a.nfb;
-            const int n_e = a.counts[e];
-            const int off = a.offsets[e];
+        int buf = 0;
+        uint32_t tph = 0;
+        for (int i = 0; i < my_n; ++i) {
+            const int u = blockIdx.x + i * gridDim.x;
+            const int fb = u % a.nfb;
+            const int2 ent = entry(i);
+            const int n_e = ent.x, off = ent.y;
             for (int c0 = 0; c0 < n_e; c0 += G_NMAX) {
                 const int N = min(G_NMAX, n_e - c0);
                 const int Np = (N + 15) & ~15;
-                if (!mbar_wait(tfull, tphase, abort_flag)) goto done;
+                if (!mbar_wait(&tfull[buf], tph, abort_flag)) goto done;
                 tc_after();
-                const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16);
-                if (EPI == EPI_GLU) {
-                    const int f = fb * 128 + lf;
-                    const bool ok = f < a.out_cols;
-                    __nv_bfloat16 *o = a.out + (long long)(off + c0) * a.out_ld + f;
-                    for (int c = 0; c < Np; c += 16) {
+                const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (NSUB == 2 ? 0 : buf * 256);
+                const int f = fb * 128 + lf;
+                const bool ok = f < a.out_cols;
+                __nv_bfloat16 *o = a.out + (long long)(off + c0) * a.out_ld + f;
+                for (int c = 0; c < Np; c += 16) {
+                    if (EPI == EPI_GLU) {
                         uint32_t g[16], v[16];
                         TMEM_LD16(tb + c, g);
                         TMEM_LD16(tb + 256 + c, v);
                         tmem_wait_ld();
                         if (ok) {
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                if (c + i < N)
-                                    o[(long long)(c + i) * a.out_ld] = __float2bfloat16_rn(situ_glu_fast(
-                                        __uint_as_float(g[i]), __uint_as_float(v[i]), ib1, a.beta1, ib2, a.beta2));
-                            }
+                            for (int j = 0; j < 16; ++j)
+                                if (c + j < N)
+                                    o[(long long)(c + j) * a.out_ld] = __float2bfloat16_rn(situ_glu_fast(
+                                        __uint_as_float(g[j]), __uint_as_float(v[j]), ib1, a.beta1, ib2, a.beta2));
                         }
-                    }
-                } else {
-                    const int f0 = fb * 256 + lf, f1 = f0 + 128;
-                    const bool ok0 = f0 < a.out_cols, ok1 = f1 < a.out_cols;
-                    __nv_bfloat16 *o = a.out + (long long)(off + c0) * a.out_ld;
-                    for (int c = 0; c < Np; c += 16) {
-                        uint32_t r0[16], r1[16];
+                    } else {
+                        uint32_t r0[16];
                         TMEM_LD16(tb + c, r0);
-                        TMEM_LD16(tb + 256 + c, r1);
                         tmem_wait_ld();
+                        if (ok) {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            if (c + i < N) {
-                                __nv_bfloat16 *orow = o + (long long)(c + i) * a.out_ld;
-                                if (ok0) orow[f0] = __float2bfloat16_rn(__uint_as_float(r0[i]));
-                                if (ok1) orow[f1] = __float2bfloat16_rn(__uint_as_float(r1[i]));
-                            }
+                            for (int j = 0; j < 16; ++j)
+                                if (c + j < N) o[(long long)(c + j) * a.out_ld] = __float2bfloat16_rn(__uint_as_float(r0[j]));
                         }
                     }
                 }
                 tc_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(tempty);
-                tphase ^= 1;
+                if (lane == 0) mbar_arrive(&tempty[buf]);
+                if (++buf == NBUF) { buf = 0; tph ^= 1; }
             }
         }
     } else if (warp >= 6) {
-        // ------------------------------------------------ token-row gather (cp.async)
+        // ------------------------------------------------ token-row gather (cp.async, kept in L2)
+        const uint64_t pol = policy_evict_last();
         const int gt = threadIdx.x - 6 * 32;          // 0..127
         const int ch = gt & 7;                         // 16-byte chunk of the 128-byte row
         const int rsub = gt >> 3;                      // rows rsub, rsub + 16, ...
         int stage = 0;
         uint32_t phase = 0;
         int pending = -1;
-        for (int u = blockIdx.x; u < units; u += gridDim.x) {
-            const int e = u / a.nfb;
-            const int n_e = a.counts[e];
-            const int off = a.offsets[e];
+        for (int i = 0; i < my_n; ++i) {
+            const int2 ent = entry(i);
+            const int n_e = ent.x, off = ent.y;
             for (int c0 = 0; c0 < n_e; c0 += G_NMAX) {
                 const int N = min(G_NMAX, n_e - c0);
                 const int Np = (N + 15) & ~15;
@@ -728,34 +785,34 @@ __global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_cons
                     src[j] = a.b_src + row * a.b_ld + ch * 8;
                 }
                 for (int kb = 0; kb < a.kblocks; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
+                    if (!mbar_wait(&b_empty[stage], phase ^ 1, abort_flag)) {
                         cp_async_wait<0>();
                         goto done;
                     }
-                    const uint32_t sb = su32(smem + stage * G_STAGE + G_A_BYTES);
+                    const uint32_t sb = su32(sB + stage * Cfg::B_BYTES);
                     const bool kok = kb * 64 + ch * 8 < a.b_K;
 #pragma unroll
                     for (int j = 0; j < G_NMAX / 16; ++j) {
                         const int r = rsub + 16 * j;
                         if (r < Np) {
                             const uint32_t dst = sb + r * 128 + ((ch ^ (r & 7)) << 4);
-                            cp_async16(dst, src[j] + kb * 64, (r < N && kok) ? 16u : 0u);
+                            cp_async16_hint(dst, src[j] + kb * 64, (r < N && kok) ? 16u : 0u, pol);
                         }
                     }
                     cp_async_commit();
                     if (pending >= 0) {
                         cp_async_wait<1>();
                         fence_proxy_async();
-                        mbar_arrive(&full[pending]);
+                        mbar_arrive(&b_full[pending]);
                     }
                     pending = stage;
-                    if (++stage == G_STAGES) { stage = 0; phase ^= 1; }
+                    if (++stage == BST) { stage = 0; phase ^= 1; }
                 }
             }
         }
         cp_async_wait<0>();
         fence_proxy_async();
-        if (pending >= 0) mbar_arrive(&full[pending]);
+        if (pending >= 0) mbar_arrive(&b_full[pending]);
     }
 done:
     __syncthreads();
@@ -839,16 +896,16 @@ int launch_dense(const TmaPack &maps, DenseArgs a, cudaStream_t st) {
     return check_launch("dense_kernel");
 }
 
-template <int EPI>
+template <int EPI, int NSUB>
 int launch_grouped(const CUtensorMap &wmap, const GroupedArgs &a, cudaStream_t st) {
-    auto kern = grouped_kernel<EPI>;
-    int rc = set_smem(kern, G_SMEM);
+    auto kern = grouped_kernel<EPI, NSUB>;
+    int rc = set_smem(kern, GCfg<NSUB>::SMEM);
     if (rc) return rc;
     const int units = a.E * a.nfb;
     const int sms = sm_count();
     const int grid = units < sms ? units : sms;
     if (grid == 0) return SLMOE_OK;
-    kern<<<grid, G_THREADS, G_SMEM, st>>>(wmap, a);
+    kern<<<grid, G_THREADS, GCfg<NSUB>::SMEM, st>>>(wmap, a);
     return check_launch("grouped_kernel");
 }
 
@@ -913,20 +970,20 @@ int tc_forward_bf16(const slmoe_config *c, const void *x, const slmoe_weights *w
         a.b_src = static_cast<const bf *>(f.x_lat); a.b_ld = dl; a.b_K = dl;
         a.out = static_cast<bf *>(f.h); a.out_ld = I; a.out_cols = I;
         a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
-        if ((rc = launch_grouped<EPI_GLU>(wm, a, st))) return rc;
+        if ((rc = launch_grouped<EPI_GLU, 2>(wm, a, st))) return rc;
     }
     stage_event(4, st);
     {   // routed experts, down: y_e[row] = W2[e] h[row]
         CUtensorMap wm;
         if ((rc = make_map(&wm, w->W2, (long long)E * dl, I, I, 128))) return rc;
         GroupedArgs a = {};
-        a.E = E; a.kblocks = (I + 63) / 64; a.nfb = (dl + 255) / 256;
-        a.a_rows_pe = dl; a.a_sub1 = 128; a.a_fb_stride = 256;
+        a.E = E; a.kblocks = (I + 63) / 64; a.nfb = (dl + 127) / 128;
+        a.a_rows_pe = dl; a.a_sub1 = 0; a.a_fb_stride = 128;
         a.counts = f.counts; a.offsets = f.offsets; a.b_index = nullptr;
         a.b_src = static_cast<const bf *>(f.h); a.b_ld = I; a.b_K = I;
         a.out = static_cast<bf *>(f.y_e); a.out_ld = dl; a.out_cols = dl;
         a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
-        if ((rc = launch_grouped<EPI_BF16>(wm, a, st))) return rc;
+        if ((rc = launch_grouped<EPI_BF16, 1>(wm, a, st))) return rc;
     }
     stage_event(5, st);
     (void)Tk;
