@@ -97,6 +97,11 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32
                  : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Arrive on the mbarrier once all of this thread's earlier cp.async copies have landed;
+// the barrier's expected count includes this arrival (noinc).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(su32(bar)) : "memory");
+}
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 __device__ __forceinline__ void fence_proxy_async() {
@@ -391,9 +396,9 @@ done:
 // warpgroups (columns 0..111 and 112..223) drain each such partial sum into fp32 registers
 // (round-to-nearest adds) while the next chunk fills the other buffer, so no tensor-core
 // accumulation chain is longer than 4 * RT_DRAIN MMA steps.  BN = 224 tiles E = 896 exactly.
-constexpr int RT_BN = 224, RT_HALF = RT_BN / 2, RT_DRAIN = 4;
+constexpr int RT_BN = 224, RT_HALF = RT_BN / 2, RT_DRAIN = 8;
 constexpr int RT_STAGE = 128 * 128 + RT_BN * 128;
-constexpr int RT_STAGES = (196 * 1024) / RT_STAGE;
+constexpr int RT_STAGES = 5;
 constexpr int RT_SMEM = RT_STAGES * RT_STAGE + 1024 + 256;
 constexpr int RT_THREADS = 320;               // TMA, MMA, 8 epilogue warps
 
@@ -540,23 +545,26 @@ done:
 // ---------------------------------------------------------------- grouped (routed experts)
 // Work unit = (expert e, feature block fb).  NSUB weight sub-tiles of 128 rows (the MMA's M)
 // stream from HBM through an A ring of 128 KB; the expert's token rows (N <= 256 per pass,
-// rounded to 16) are gathered by cp.async from L2 into a 2-deep B ring.  NSUB = 2 pairs the
+// rounded to 16) are gathered by cp.async from L2 into a 3-deep B ring; each gather thread
+// signals a stage with cp.async.mbarrier.arrive.noinc (fires when its copies land) and never
+// waits on its own copies, and the MMA thread fences the generic-proxy writes to the async
+// proxy after its wait, before tcgen05.mma reads them.  NSUB = 2 pairs the
 // gate rows fb*128.. with the up rows I + fb*128.. for the fused SiTU-GLU; NSUB = 1 (expert
 // down) keeps two TMEM accumulators so a unit's epilogue overlaps the next unit's loads.
 // Each CTA stages its (count, offset) pairs in shared memory at start.
 constexpr int G_NMAX = 256;
 constexpr int G_THREADS = 320;                    // TMA, MMA, 4 epilogue, 4 gather warps
 constexpr int G_GATHER_THREADS = 128;
-constexpr int G_LIST = 1024;                      // units listed in shared memory per CTA
+constexpr int G_LIST = 192;                       // units listed in shared memory per CTA
 
 template <int NSUB>
 struct GCfg {
     static constexpr int A_BYTES = NSUB * 128 * 128;
     static constexpr int A_STAGES = (128 * 1024) / A_BYTES;
     static constexpr int B_BYTES = G_NMAX * 128;
-    static constexpr int B_STAGES = 2;
+    static constexpr int B_STAGES = 3;
     static constexpr int NBUF = NSUB == 2 ? 1 : 2;
-    static constexpr int SMEM = A_STAGES * A_BYTES + B_STAGES * B_BYTES + G_LIST * 8 + 1024 + 512;
+    static constexpr int SMEM = A_STAGES * A_BYTES + B_STAGES * B_BYTES + G_LIST * 8 + 1024 + 256;
 };
 
 struct GroupedArgs {
@@ -691,6 +699,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_cons
                 for (int kb = 0; kb < a.kblocks; ++kb) {
                     if (!mbar_wait(&a_full[as], aph, abort_flag)) goto done;
                     if (!mbar_wait(&b_full[bs], bph, abort_flag)) goto done;
+                    fence_proxy_async();
                     tc_after();
                     const uint32_t sa = su32(sA + as * Cfg::A_BYTES);
                     const uint32_t sb = su32(sB + bs * Cfg::B_BYTES);
@@ -769,7 +778,6 @@ __global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_cons
         const int rsub = gt >> 3;                      // rows rsub, rsub + 16, ...
         int stage = 0;
         uint32_t phase = 0;
-        int pending = -1;
         for (int i = 0; i < my_n; ++i) {
             const int2 ent = entry(i);
             const int n_e = ent.x, off = ent.y;
@@ -799,20 +807,12 @@ __global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_cons
                             cp_async16_hint(dst, src[j] + kb * 64, (r < N && kok) ? 16u : 0u, pol);
                         }
                     }
-                    cp_async_commit();
-                    if (pending >= 0) {
-                        cp_async_wait<1>();
-                        fence_proxy_async();
-                        mbar_arrive(&b_full[pending]);
-                    }
-                    pending = stage;
+                    cp_async_arrive_noinc(&b_full[stage]);
                     if (++stage == BST) { stage = 0; phase ^= 1; }
                 }
             }
         }
         cp_async_wait<0>();
-        fence_proxy_async();
-        if (pending >= 0) mbar_arrive(&b_full[pending]);
     }
 done:
     __syncthreads();
