@@ -57,7 +57,7 @@ extern "C" {
 
 /* Shape and constants of one layer.  beta1 / beta2 are the SiTU and soft-cap constants
  * ([K3-arch] SiTU激活优化: 4 and 25), eps the RMSNorm epsilon, nbins the QB histogram
- * width ([K3-arch] 负载均衡优化: 1000).
+ * width ([K3-arch] 负载均衡优化: 1000; at most 1024 here).
  * Limits: 1 <= k <= E <= 4096, k <= 32; d, d_latent, I, I_shared multiples of 8 (of 64 for
  * the bf16 type); n_shared <= 3; T >= 0 (T = 0 is a no-op). */
 typedef struct slmoe_config {
@@ -158,7 +158,7 @@ SLMOE_API int slmoe_route(const slmoe_config *cfg, const void *x, const float *W
  *     hist[e*nbins + bin] += 1
  *   scores [T,E] fp32, row-major; hist [E,nbins] uint32, accumulated in place (the caller
  *   zeroes it before the first micro-batch).  T may be 0.  No workspace.
- * Errors: SLMOE_EINVAL on null pointers, E < 1, nbins < 1 or nbins > 4096.
+ * Errors: SLMOE_EINVAL on null pointers, E < 1, nbins < 1 or nbins > 1024.
  */
 SLMOE_API int slmoe_qb_histogram(const float *scores, int64_t T, int32_t E, int32_t nbins,
                        uint32_t *hist, int32_t *status, void *stream);
@@ -172,7 +172,7 @@ SLMOE_API int slmoe_qb_histogram(const float *scores, int64_t T, int32_t E, int3
  *   q_e = (j + (r - C_{j-1}) / hist[e,j]) / nbins      (q_e = 0 when r = 0)
  *   bias[e] = mean_e(q) - q_e                           (overwrites bias)
  *   computed in fp64 and stored in fp32.  hist [E,nbins] uint32; q_out [E] fp32 or NULL;
- *   bias [E] fp32.  E <= 8192.  One block; no workspace.
+ *   bias [E] fp32.  E <= 8192, nbins <= 1024.  One thread-block cluster; no workspace.
  */
 SLMOE_API int slmoe_qb_update(const uint32_t *hist, int32_t E, int32_t nbins, int32_t k,
                     float *q_out, float *bias, void *stream);

@@ -52,7 +52,7 @@ int validate_config(const slmoe_config *c) {
     if (c->E < 1 || c->E > 4096) return fail(SLMOE_EINVAL, "E = %d outside [1, 4096]", c->E);
     if (c->k < 1 || c->k > c->E || c->k > 32)
         return fail(SLMOE_EINVAL, "k = %d outside [1, min(E, 32)]", c->k);
-    if (c->nbins < 1 || c->nbins > 2048) return fail(SLMOE_EINVAL, "nbins = %d outside [1, 2048]", c->nbins);
+    if (c->nbins < 1 || c->nbins > 1024) return fail(SLMOE_EINVAL, "nbins = %d outside [1, 1024]", c->nbins);
     if (c->n_shared < 0 || c->n_shared > 3) return fail(SLMOE_EINVAL, "n_shared = %d outside [0, 3]", c->n_shared);
     const int m = c->dtype == SLMOE_BF16 ? 64 : 8;
     if (c->d < m || c->d % m) return fail(SLMOE_EINVAL, "d = %d is not a positive multiple of %d", c->d, m);
@@ -301,7 +301,7 @@ int slmoe_qb_histogram(const float *scores, int64_t T, int32_t E, int32_t nbins,
     g_err[0] = 0;
     if (T < 0) return fail(SLMOE_EINVAL, "T < 0");
     if (E < 1) return fail(SLMOE_EINVAL, "E < 1");
-    if (nbins < 1 || nbins > 2048) return fail(SLMOE_EINVAL, "nbins outside [1, 2048]");
+    if (nbins < 1 || nbins > 1024) return fail(SLMOE_EINVAL, "nbins outside [1, 1024]");
     if (!hist) return fail(SLMOE_EINVAL, "hist is NULL");
     if (T > 0 && !scores) return fail(SLMOE_EINVAL, "scores is NULL");
     if (((uintptr_t)scores & 3u) || ((uintptr_t)hist & 3u) || ((uintptr_t)status & 3u))
@@ -314,7 +314,7 @@ int slmoe_qb_update(const uint32_t *hist, int32_t E, int32_t nbins, int32_t k, f
     g_err[0] = 0;
     if (E < 1 || E > 8192) return fail(SLMOE_EINVAL, "E outside [1, 8192]");
     if (k < 1 || k > E) return fail(SLMOE_EINVAL, "k outside [1, E]");
-    if (nbins < 1 || nbins > 2048) return fail(SLMOE_EINVAL, "nbins outside [1, 2048]");
+    if (nbins < 1 || nbins > 1024) return fail(SLMOE_EINVAL, "nbins outside [1, 1024]");
     if (!hist || !bias) return fail(SLMOE_EINVAL, "hist and bias are required");
     if (((uintptr_t)hist & 3u) || ((uintptr_t)bias & 3u) || ((uintptr_t)q_out & 3u))
         return fail(SLMOE_EINVAL, "hist, bias and q_out must be 4-byte aligned");

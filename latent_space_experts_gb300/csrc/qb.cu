@@ -7,13 +7,12 @@
 //
 // Histogram design.  scores [T, E] fp32 is streamed once from HBM.  The experts are cut
 // into slabs of 32 (one 128-byte line per row: lane = expert), and each slab is counted by
-// one thread-block cluster of QB_CLUSTER CTAs that split the tokens.  Counters are 16-bit
-// halves of 32-bit shared-memory words (a CTA counts at most 65535 tokens per window, so a
-// half never carries into its neighbour), stored word-major with the 32 experts of the slab
-// interleaved ([word][lane]), so the 32 lanes of an atomic always hit 32 distinct banks.  At the end of a window the cluster adds its
-// CTAs' counters through distributed shared memory and each bin of global memory is
-// read-modified-written by exactly one thread: no global atomics and no partial
-// histograms in HBM.
+// one thread-block cluster of P CTAs that split the tokens (P is chosen so that the
+// clusters fill the SMs).  Each CTA keeps 32-bit counters [bin][32 experts] in shared
+// memory, so the 32 lanes of an atomic always hit 32 distinct banks, and keeps 32 row
+// loads in flight per lane.  At the end the cluster adds its CTAs' counters through
+// distributed shared memory and each bin of global memory is read-modified-written by
+// exactly one thread: no global atomics and no partial histograms in HBM.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -26,91 +25,70 @@ namespace {
 
 constexpr int QB_SLAB = 32;
 constexpr int QB_THREADS = 1024;
-constexpr int QB_CLUSTER = 8;
-constexpr int64_t QB_WINDOW = 65535;     // tokens per CTA per window (16-bit counters)
-constexpr int QB_UNROLL = 16;
+constexpr int QB_MAX_CLUSTER = 8;
+constexpr int QB_UNROLL = 32;
 
-__device__ __forceinline__ int qb_bin(float s, float nb, int nbins) {
-    // one IEEE fp32 round-to-nearest multiply, then floor, clamped to [0, nbins-1]
-    float p = __fmul_rn(s, nb);
-    int b = (int)floorf(p);
-    b = b < 0 ? 0 : b;
-    return b > nbins - 1 ? nbins - 1 : b;
-}
-
-__global__ void __launch_bounds__(QB_THREADS)
+__global__ void __launch_bounds__(QB_THREADS, 1)
 qb_hist_kernel(const float *__restrict__ scores, int64_t T, int E, int nbins,
                uint32_t *__restrict__ hist, int32_t *status) {
-    extern __shared__ uint32_t hs[];                 // [nwords][QB_SLAB] packed 16-bit
+    extern __shared__ uint32_t hs[];                 // [nbins][QB_SLAB]
     cg::cluster_group cluster = cg::this_cluster();
     const int P = (int)cluster.num_blocks();
     const int rank = (int)cluster.block_rank();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nwarps = QB_THREADS / 32;
+    constexpr int nwarps = QB_THREADS / 32;
     const int e0 = blockIdx.x * QB_SLAB;
     const int ne = min(QB_SLAB, E - e0);
     const float nb = (float)nbins;
-    const int nwords_e = (nbins + 1) >> 1;
+    const int top = nbins - 1;
     int nan_count = 0;
     bool overflow = false;
 
-    for (int64_t w0 = 0; w0 < T; w0 += QB_WINDOW * P) {
-        for (int i = tid; i < QB_SLAB * nwords_e; i += QB_THREADS) hs[i] = 0u;
-        __syncthreads();
-        const int64_t wt1 = min(T, w0 + QB_WINDOW * P);
-        const int64_t per = (wt1 - w0 + P - 1) / P;
-        const int64_t t0 = w0 + rank * per;
-        const int64_t t1 = min(wt1, t0 + per);
-        if (lane < ne) {
-            const float *col = scores + e0 + lane;
-            uint32_t *h = hs + lane;
-            int64_t t = t0 + warp;
-            for (; t + (QB_UNROLL - 1) * nwarps < t1; t += QB_UNROLL * nwarps) {
-                float v[QB_UNROLL];
+    for (int i = tid; i < QB_SLAB * nbins; i += QB_THREADS) hs[i] = 0u;
+    __syncthreads();
+    const int64_t per = (T + P - 1) / P;
+    const int64_t t0 = rank * per;
+    const int64_t t1 = min(T, t0 + per);
+    if (lane < ne) {
+        const float *col = scores + e0 + lane;
+        uint32_t *h = hs + lane;
+        int64_t t = t0 + warp;
+        for (; t + (QB_UNROLL - 1) * nwarps < t1; t += QB_UNROLL * nwarps) {
+            float v[QB_UNROLL];
 #pragma unroll
-                for (int u = 0; u < QB_UNROLL; ++u) v[u] = __ldcs(col + (t + u * nwarps) * (int64_t)E);
+            for (int u = 0; u < QB_UNROLL; ++u) v[u] = __ldcs(col + (t + u * nwarps) * (int64_t)E);
 #pragma unroll
-                for (int u = 0; u < QB_UNROLL; ++u) {
-                    if (isnan(v[u])) { ++nan_count; continue; }
-                    const int b = qb_bin(v[u], nb, nbins);
-                    atomicAdd(&h[(b >> 1) * QB_SLAB], 1u << ((b & 1) << 4));
-                }
-            }
-            for (; t < t1; t += nwarps) {
-                const float v = __ldcs(col + t * (int64_t)E);
-                if (isnan(v)) { ++nan_count; continue; }
-                const int b = qb_bin(v, nb, nbins);
-                atomicAdd(&h[(b >> 1) * QB_SLAB], 1u << ((b & 1) << 4));
+            for (int u = 0; u < QB_UNROLL; ++u) {
+                // one IEEE fp32 round-to-nearest multiply, floor, clamp to [0, nbins-1]
+                const int b = min(max(__float2int_rd(__fmul_rn(v[u], nb)), 0), top);
+                if (isnan(v[u])) ++nan_count;
+                else atomicAdd(&h[b * QB_SLAB], 1u);
             }
         }
-        cluster.sync();
-        // each CTA of the cluster adds a share of the slab's words across all CTAs
-        const int total = ne * nwords_e;
-        const int share = (total + P - 1) / P;
-        const int f0 = rank * share, f1 = min(total, f0 + share);
-        for (int f = f0 + tid; f < f1; f += QB_THREADS) {
-            const int wd = f / ne, e = f - wd * ne;
-            uint32_t lo = 0, hi = 0;
-            for (int r = 0; r < P; ++r) {
-                const uint32_t *rh = cluster.map_shared_rank(hs, r);
-                const uint32_t v = rh[wd * QB_SLAB + e];
-                lo += v & 0xffffu;
-                hi += v >> 16;
-            }
-            uint32_t *g = hist + (int64_t)(e0 + e) * nbins + 2 * wd;
-            if (lo) {
-                uint64_t nv = (uint64_t)g[0] + lo;
-                if (nv > 0xffffffffull) { overflow = true; nv = 0xffffffffull; }
-                g[0] = (uint32_t)nv;
-            }
-            if (hi && 2 * wd + 1 < nbins) {
-                uint64_t nv = (uint64_t)g[1] + hi;
-                if (nv > 0xffffffffull) { overflow = true; nv = 0xffffffffull; }
-                g[1] = (uint32_t)nv;
-            }
+        for (; t < t1; t += nwarps) {
+            const float v = __ldcs(col + t * (int64_t)E);
+            const int b = min(max(__float2int_rd(__fmul_rn(v, nb)), 0), top);
+            if (isnan(v)) ++nan_count;
+            else atomicAdd(&h[b * QB_SLAB], 1u);
         }
-        cluster.sync();
     }
+    cluster.sync();
+    // each CTA of the cluster adds a share of the slab's bins across all CTAs
+    const int total = ne * nbins;
+    const int share = (total + P - 1) / P;
+    const int f0 = rank * share, f1 = min(total, f0 + share);
+    for (int f = f0 + tid; f < f1; f += QB_THREADS) {
+        const int b = f / ne, e = f - b * ne;
+        uint64_t sum = 0;
+        for (int r = 0; r < P; ++r) sum += cluster.map_shared_rank(hs, r)[b * QB_SLAB + e];
+        if (sum) {
+            uint32_t *g = hist + (int64_t)(e0 + e) * nbins + b;
+            uint64_t nv = (uint64_t)*g + sum;
+            if (nv > 0xffffffffull) { overflow = true; nv = 0xffffffffull; }
+            *g = (uint32_t)nv;
+        }
+    }
+    cluster.sync();
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) nan_count += __shfl_xor_sync(0xffffffffu, nan_count, o);
     if (status) {
@@ -126,7 +104,7 @@ qb_hist_kernel(const float *__restrict__ scores, int64_t T, int E, int nbins,
 // fixed-order sum: per CTA in shared memory, then across the cluster's CTAs in rank order
 // through distributed shared memory.  No global scratch.
 constexpr int QBU_CTAS = 8;
-constexpr int QBU_MAXB = 2048 / 32;          // bins per lane (nbins <= 2048)
+constexpr int QBU_MAXB = 1024 / 32;          // bins per lane (nbins <= 1024)
 constexpr int QBU_THREADS = 512;
 
 __global__ void __launch_bounds__(QBU_THREADS, 1)
@@ -213,21 +191,22 @@ qb_update_kernel(const uint32_t *__restrict__ hist, int E, int nbins, int k,
 int launch_qb_histogram(const float *scores, int64_t T, int E, int nbins, uint32_t *hist,
                         int32_t *status, cudaStream_t st) {
     if (T <= 0) return SLMOE_OK;
-    const int nwords_e = (nbins + 1) >> 1;
-    const size_t smem = (size_t)QB_SLAB * nwords_e * sizeof(uint32_t);
+    const size_t smem = (size_t)QB_SLAB * nbins * sizeof(uint32_t);
     cudaError_t e = cudaFuncSetAttribute(qb_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return fail(SLMOE_ECUDA, "qb smem attribute: %s", cudaGetErrorString(e));
     const int nslabs = (E + QB_SLAB - 1) / QB_SLAB;
+    int P = sm_count() / nslabs;
+    P = P < 1 ? 1 : (P > QB_MAX_CLUSTER ? QB_MAX_CLUSTER : P);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(nslabs, QB_CLUSTER, 1);
+    cfg.gridDim = dim3(nslabs, P, 1);
     cfg.blockDim = dim3(QB_THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = QB_CLUSTER;
+    attr[0].val.clusterDim.y = P;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;

@@ -549,8 +549,9 @@ done:
 // signals a stage with cp.async.mbarrier.arrive.noinc (fires when its copies land) and never
 // waits on its own copies, and the MMA thread fences the generic-proxy writes to the async
 // proxy after its wait, before tcgen05.mma reads them.  NSUB = 2 pairs the
-// gate rows fb*128.. with the up rows I + fb*128.. for the fused SiTU-GLU; NSUB = 1 (expert
-// down) keeps two TMEM accumulators so a unit's epilogue overlaps the next unit's loads.
+// gate rows fb*128.. with the up rows I + fb*128.. for the fused SiTU-GLU, or two blocks of
+// 128 output features (expert down).  While a unit's epilogue drains TMEM, the weight ring
+// keeps streaming the next unit.  (NSUB = 1 would keep two TMEM accumulators instead.)
 // Each CTA stages its (count, offset) pairs in shared memory at start.
 constexpr int G_NMAX = 256;
 constexpr int G_THREADS = 320;                    // TMA, MMA, 4 epilogue, 4 gather warps
@@ -737,8 +738,11 @@ __global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_cons
                 if (!mbar_wait(&tfull[buf], tph, abort_flag)) goto done;
                 tc_after();
                 const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (NSUB == 2 ? 0 : buf * 256);
-                const int f = fb * 128 + lf;
+                // GLU: sub-tiles are the gate and up rows of h column fb*128 + lf.  Plain: the
+                // NSUB sub-tiles are output features fb*128*NSUB + lf + 128*sub.
+                const int f = (EPI == EPI_GLU ? fb * 128 : fb * 128 * NSUB) + lf;
                 const bool ok = f < a.out_cols;
+                const bool ok1 = NSUB == 2 && f + 128 < a.out_cols;
                 __nv_bfloat16 *o = a.out + (long long)(off + c0) * a.out_ld + f;
                 for (int c = 0; c < Np; c += 16) {
                     if (EPI == EPI_GLU) {
@@ -754,13 +758,17 @@ __global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_cons
                                         __uint_as_float(g[j]), __uint_as_float(v[j]), ib1, a.beta1, ib2, a.beta2));
                         }
                     } else {
-                        uint32_t r0[16];
+                        uint32_t r0[16], r1[16];
                         TMEM_LD16(tb + c, r0);
+                        if (NSUB == 2) TMEM_LD16(tb + 256 + c, r1);
                         tmem_wait_ld();
-                        if (ok) {
 #pragma unroll
-                            for (int j = 0; j < 16; ++j)
-                                if (c + j < N) o[(long long)(c + j) * a.out_ld] = __float2bfloat16_rn(__uint_as_float(r0[j]));
+                        for (int j = 0; j < 16; ++j) {
+                            if (c + j < N) {
+                                __nv_bfloat16 *orow = o + (long long)(c + j) * a.out_ld;
+                                if (ok) orow[0] = __float2bfloat16_rn(__uint_as_float(r0[j]));
+                                if (ok1) orow[128] = __float2bfloat16_rn(__uint_as_float(r1[j]));
+                            }
                         }
                     }
                 }
@@ -977,13 +985,13 @@ int tc_forward_bf16(const slmoe_config *c, const void *x, const slmoe_weights *w
         CUtensorMap wm;
         if ((rc = make_map(&wm, w->W2, (long long)E * dl, I, I, 128))) return rc;
         GroupedArgs a = {};
-        a.E = E; a.kblocks = (I + 63) / 64; a.nfb = (dl + 127) / 128;
-        a.a_rows_pe = dl; a.a_sub1 = 0; a.a_fb_stride = 128;
+        a.E = E; a.kblocks = (I + 63) / 64; a.nfb = (dl + 255) / 256;
+        a.a_rows_pe = dl; a.a_sub1 = 128; a.a_fb_stride = 256;
         a.counts = f.counts; a.offsets = f.offsets; a.b_index = nullptr;
         a.b_src = static_cast<const bf *>(f.h); a.b_ld = I; a.b_K = I;
         a.out = static_cast<bf *>(f.y_e); a.out_ld = dl; a.out_cols = dl;
         a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
-        if ((rc = launch_grouped<EPI_BF16, 1>(wm, a, st))) return rc;
+        if ((rc = launch_grouped<EPI_BF16, 2>(wm, a, st))) return rc;
     }
     stage_event(5, st);
     (void)Tk;

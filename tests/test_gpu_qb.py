@@ -44,7 +44,7 @@ def test_qb_engine_full_size_eight_micro_batches():
 
 
 @pytest.mark.parametrize("T,E,nbins", [(1, 1, 1000), (1000, 33, 1000), (5000, 64, 999), (777, 100, 10),
-                                       (200000, 40, 1000), (3, 2048, 1000)])
+                                       (200000, 40, 1000), (3, 2048, 1000), (2000, 70, 1024)])
 def test_histogram_shapes(T, E, nbins):
     need_gpu()
     g = torch.Generator(device="cpu").manual_seed(T + E)

@@ -83,7 +83,7 @@ def test_null_and_misaligned_arguments_fail_before_launch(lib):
     assert rc == -4
     rc = lib.slmoe_qb_histogram(None, 10, 4, 1000, fake, None, None)
     assert rc == -1
-    rc = lib.slmoe_qb_histogram(fake, 10, 4, 5000, fake, None, None)
+    rc = lib.slmoe_qb_histogram(fake, 10, 4, 1025, fake, None, None)
     assert rc == -1
     rc = lib.slmoe_qb_update(fake, 4, 1000, 5, None, fake, None)
     assert rc == -1
