@@ -275,14 +275,9 @@ def main():
         step(inp["x"])
     lse.slmoe_set_stage_events(None)
     torch.cuda.synchronize()
-    # stage i ends at event i; stage 7 (shared gate|up) runs on the library's auxiliary
-    # stream from the end of stage 3, concurrently with stages 4-6; stage 8 starts when both
-    # stage 6 and stage 7 are done
     for row in ev:
-        t = [row[0].elapsed_time(e) for e in row]
-        start = {7: t[3], 8: max(t[6], t[7])}
         for i in range(1, nst):
-            stage_ms[i] += (t[i] - start.get(i, t[i - 1])) / len(ev)
+            stage_ms[i] += row[i - 1].elapsed_time(row[i]) / len(ev)
     counts = lse.workspace_views(cfg, ws)["counts"].cpu().numpy()
     st_model, layer_flops, layer_bytes = work_model(shp, counts)
     pk, pk_kind = peaks()
@@ -296,7 +291,7 @@ def main():
                              "GB/s": round(m["bytes"] / t / 1e9, 1) if t > 0 else None,
                              "TFLOP/s": round(m["flops"] / t / 1e12, 1) if t > 0 else None,
                              "bound": m["bound"]}
-    dom = max(range(1, nst), key=lambda i: stage_ms[i] if i != 7 else 0.0)
+    dom = max(range(1, nst), key=lambda i: stage_ms[i])
     dm = st_model[STAGES[dom]]
     t_dom = stage_ms[dom] * 1e-3
     if dm["bound"] == "hbm":

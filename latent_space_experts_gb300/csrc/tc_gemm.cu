@@ -29,7 +29,6 @@
 #include <cudaTypedefs.h>
 
 #include <cstring>
-#include <mutex>
 
 #include "common.cuh"
 #include "tc_gemm.h"
@@ -891,7 +890,7 @@ int set_smem(K kern, int bytes) {
 }
 
 template <int BN, int EPI, int PACC>
-int launch_dense(const TmaPack &maps, DenseArgs a, cudaStream_t st, int max_ctas = 0) {
+int launch_dense(const TmaPack &maps, DenseArgs a, cudaStream_t st) {
     using Cfg = DenseCfg<BN, EPI, PACC>;
     a.tiles_n = (a.N + Cfg::BN_OUT - 1) / Cfg::BN_OUT;
     a.tiles = ((a.M + Cfg::BM - 1) / Cfg::BM) * a.tiles_n;
@@ -899,64 +898,23 @@ int launch_dense(const TmaPack &maps, DenseArgs a, cudaStream_t st, int max_ctas
     auto kern = dense_kernel<BN, EPI, PACC>;
     int rc = set_smem(kern, Cfg::SMEM);
     if (rc) return rc;
-    const int cap = max_ctas > 0 ? max_ctas : sm_count();
-    const int grid = a.tiles < cap ? a.tiles : cap;
+    const int sms = sm_count();
+    const int grid = a.tiles < sms ? a.tiles : sms;
     kern<<<grid, 192, Cfg::SMEM, st>>>(maps, a);
     return check_launch("dense_kernel");
 }
 
 template <int EPI, int NSUB>
-int launch_grouped(const CUtensorMap &wmap, const GroupedArgs &a, cudaStream_t st, int max_ctas = 0) {
+int launch_grouped(const CUtensorMap &wmap, const GroupedArgs &a, cudaStream_t st) {
     auto kern = grouped_kernel<EPI, NSUB>;
     int rc = set_smem(kern, GCfg<NSUB>::SMEM);
     if (rc) return rc;
     const int units = a.E * a.nfb;
-    const int cap = max_ctas > 0 ? max_ctas : sm_count();
-    const int grid = units < cap ? units : cap;
+    const int sms = sm_count();
+    const int grid = units < sms ? units : sms;
     if (grid == 0) return SLMOE_OK;
     kern<<<grid, G_THREADS, GCfg<NSUB>::SMEM, st>>>(wmap, a);
     return check_launch("grouped_kernel");
-}
-
-// One auxiliary stream and a fork/join event pair per device, created on first use and
-// kept for the life of the process.  The shared-expert gate/up GEMM runs there,
-// concurrently with the routed-expert GEMMs on the caller's stream.
-struct AuxStreams {
-    cudaStream_t aux = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
-};
-constexpr int MAX_DEVICES = 64;
-AuxStreams g_aux[MAX_DEVICES];
-std::mutex g_aux_mu;
-
-int aux_streams(AuxStreams **out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES)
-        return fail(SLMOE_ECUDA, "no current device");
-    std::lock_guard<std::mutex> lock(g_aux_mu);
-    AuxStreams &a = g_aux[dev];
-    if (!a.aux) {
-        if (cudaStreamCreateWithFlags(&a.aux, cudaStreamNonBlocking) != cudaSuccess ||
-            cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming) != cudaSuccess)
-            return check_launch("aux stream");
-    }
-    *out = &a;
-    return SLMOE_OK;
-}
-
-// SMs given to the shared-expert GEMM while the routed experts stream their weights: the
-// share that makes its compute time (at the tensor-core rate) match the routed experts'
-// weight-streaming time (at the HBM rate), using planning figures of 1.7 PFLOP/s and 6.7 TB/s.
-int shared_sm_share(const slmoe_config *c, int sms) {
-    const double flops = 2.0 * c->T * c->d * 2.0 * c->I_shared * c->n_shared;
-    const double touched = c->E < (double)c->T * c->k ? c->E : (double)c->T * c->k;
-    const double bytes = touched * 3.0 * c->I * c->d_latent * 2.0 + 2.0 * c->T * c->k * (double)c->d_latent * 2.0;
-    const double t_c = flops / 1.7e15, t_m = bytes / 6.7e12;
-    int S = (int)(sms * t_c / (t_m > 0 ? t_m : 1e-9) + 0.5);
-    if (S < 8) S = 8;
-    if (S > sms / 3) S = sms / 3;
-    return S;
 }
 
 }  // namespace
@@ -1010,35 +968,6 @@ int tc_forward_bf16(const slmoe_config *c, const void *x, const slmoe_weights *w
         if ((rc = launch_dense<256, EPI_BF16, 1>(maps, a, st))) return rc;
     }
     stage_event(3, st);
-    // shared experts, gate|up + SiTU-GLU on full d: on the auxiliary stream, on a share of
-    // the SMs, concurrently with the routed experts below
-    const int sms = sm_count();
-    int S = 0;
-    AuxStreams *aux = nullptr;
-    if (ns > 0) {
-        if ((rc = aux_streams(&aux))) return rc;
-        S = shared_sm_share(c, sms);
-        if (cudaEventRecord(aux->fork, st) != cudaSuccess || cudaStreamWaitEvent(aux->aux, aux->fork, 0) != cudaSuccess)
-            return check_launch("fork");
-    }
-    for (int s = 0; s < ns; ++s) {
-        TmaPack maps;
-        memset(&maps, 0, sizeof(maps));
-        if ((rc = make_map(&maps.a[0], x, T, d, d, 128))) return rc;
-        if ((rc = make_map(&maps.b[0], static_cast<const bf *>(w->W13_s) + (size_t)s * 2 * Is * d, 2 * Is, d, d,
-                           128)))
-            return rc;
-        DenseArgs a = {};
-        a.M = T; a.N = Is; a.nseg = 1; a.kblocks[0] = (d + 63) / 64; a.glu_up_row = Is;
-        a.C = static_cast<bf *>(f.h_s) + (size_t)s * Is; a.ldc = (long long)ns * Is;
-        a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
-        if ((rc = launch_dense<256, EPI_GLU, 1>(maps, a, aux->aux, S))) return rc;
-    }
-    if (ns > 0) {
-        stage_event(7, aux->aux);
-        if (cudaEventRecord(aux->join, aux->aux) != cudaSuccess) return check_launch("join");
-    }
-    const int routed_ctas = sms - S;
     {   // routed experts, gate|up + SiTU-GLU: h[perm row] = GLU(W13[e] x_lat[token])
         CUtensorMap wm;
         if ((rc = make_map(&wm, w->W13, (long long)E * 2 * I, dl, dl, 128))) return rc;
@@ -1049,7 +978,7 @@ int tc_forward_bf16(const slmoe_config *c, const void *x, const slmoe_weights *w
         a.b_src = static_cast<const bf *>(f.x_lat); a.b_ld = dl; a.b_K = dl;
         a.out = static_cast<bf *>(f.h); a.out_ld = I; a.out_cols = I;
         a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
-        if ((rc = launch_grouped<EPI_GLU, 2>(wm, a, st, routed_ctas))) return rc;
+        if ((rc = launch_grouped<EPI_GLU, 2>(wm, a, st))) return rc;
     }
     stage_event(4, st);
     {   // routed experts, down: y_e[row] = W2[e] h[row]
@@ -1062,14 +991,27 @@ int tc_forward_bf16(const slmoe_config *c, const void *x, const slmoe_weights *w
         a.b_src = static_cast<const bf *>(f.h); a.b_ld = I; a.b_K = I;
         a.out = static_cast<bf *>(f.y_e); a.out_ld = dl; a.out_cols = dl;
         a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
-        if ((rc = launch_grouped<EPI_BF16, 2>(wm, a, st, routed_ctas))) return rc;
+        if ((rc = launch_grouped<EPI_BF16, 2>(wm, a, st))) return rc;
     }
     stage_event(5, st);
     (void)Tk;
     if ((rc = launch_combine_rmsnorm(DT_BF16, f.y_e, f.topk_w, f.slot_pos, w->gamma, T, dl, k, c->eps, f.z, st)))
         return rc;
     stage_event(6, st);
-    if (ns > 0 && cudaStreamWaitEvent(st, aux->join, 0) != cudaSuccess) return check_launch("join wait");
+    for (int s = 0; s < ns; ++s) {   // shared experts, gate|up + SiTU-GLU on full d
+        TmaPack maps;
+        memset(&maps, 0, sizeof(maps));
+        if ((rc = make_map(&maps.a[0], x, T, d, d, 128))) return rc;
+        if ((rc = make_map(&maps.b[0], static_cast<const bf *>(w->W13_s) + (size_t)s * 2 * Is * d, 2 * Is, d, d,
+                           128)))
+            return rc;
+        DenseArgs a = {};
+        a.M = T; a.N = Is; a.nseg = 1; a.kblocks[0] = (d + 63) / 64; a.glu_up_row = Is;
+        a.C = static_cast<bf *>(f.h_s) + (size_t)s * Is; a.ldc = (long long)ns * Is;
+        a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
+        if ((rc = launch_dense<256, EPI_GLU, 1>(maps, a, st))) return rc;
+    }
+    stage_event(7, st);
     {   // y = z W_out^T + sum_s h_s W2_s^T, K cut into 1 + n_shared segments
         TmaPack maps;
         memset(&maps, 0, sizeof(maps));
