@@ -65,7 +65,7 @@ int launch_topk(const float *scores, const float *bias, int T, int E, int k, int
 int launch_scan(int32_t *chunk_counts, int nchunks, int E, int32_t *counts, cudaStream_t st);
 int launch_scatter(const int32_t *topk_idx, const int32_t *chunk_base, const int32_t *counts, int T,
                    int E, int k, int32_t *offsets, int32_t *perm, int32_t *slot_pos, cudaStream_t st);
-constexpr int ROUTE_CHUNK = 32;  // tokens per top-k block / permutation chunk
+constexpr int ROUTE_CHUNK = 16;  // tokens per top-k block / permutation chunk
 
 // ---------------------------------------------------------------- QB
 int launch_qb_histogram(const float *scores, int64_t T, int E, int nbins, uint32_t *hist,

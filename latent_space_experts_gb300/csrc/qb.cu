@@ -106,13 +106,17 @@ qb_hist_kernel(const float *__restrict__ scores, int64_t T, int E, int nbins,
 constexpr int QBU_CTAS = 8;
 constexpr int QBU_MAXB = 1024 / 32;          // bins per lane (nbins <= 1024)
 constexpr int QBU_THREADS = 512;
+constexpr int QBU_STAGE_WORDS = (QBU_THREADS / 32) * QBU_MAXB * 33;
 
 __global__ void __launch_bounds__(QBU_THREADS, 1)
 qb_update_kernel(const uint32_t *__restrict__ hist, int E, int nbins, int k,
                  float *__restrict__ q_out, float *__restrict__ bias) {
-    extern __shared__ double q_s[];
+    // dynamic shared memory: per-warp staging tiles, then q of this CTA's experts
+    extern __shared__ uint32_t dyn[];
     __shared__ double red[QBU_THREADS / 32];
     __shared__ double part;
+    uint32_t *stage = dyn;
+    double *q_s = reinterpret_cast<double *>(dyn + QBU_STAGE_WORDS);
     cg::cluster_group cluster = cg::this_cluster();
     const int P = (int)cluster.num_blocks();
     const int rank = (int)cluster.block_rank();
@@ -122,15 +126,26 @@ qb_update_kernel(const uint32_t *__restrict__ hist, int E, int nbins, int k,
     const double p = 1.0 - (double)k / (double)E;
     const int B = (nbins + 31) / 32;             // bins owned by each lane, contiguous
     const int b0 = lane * B;
+    // per-warp staging tile: bin b at word b + b / 32 (one pad word per 32 bins) so that the
+    // coalesced stores and the lane-contiguous reads are both free of bank conflicts
+    uint32_t *tile = stage + w * (QBU_MAXB * 33);
     for (int e = e0 + w; e < e1; e += QBU_THREADS / 32) {
         const uint32_t *h = hist + (int64_t)e * nbins;
+#pragma unroll
+        for (int i = 0; i < QBU_MAXB; ++i) {
+            const int b = i * 32 + lane;
+            if (i < B) tile[b + i] = b < nbins ? h[b] : 0u;
+        }
+        __syncwarp();
         uint32_t v[QBU_MAXB];
         unsigned long long S = 0;
 #pragma unroll
         for (int i = 0; i < QBU_MAXB; ++i) {
-            v[i] = (i < B && b0 + i < nbins) ? h[b0 + i] : 0u;
+            const int b = b0 + i;
+            v[i] = (i < B) ? tile[b + (b >> 5)] : 0u;
             S += v[i];
         }
+        __syncwarp();
         unsigned long long inc = S;              // inclusive scan of the lanes' sums
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -217,9 +232,10 @@ int launch_qb_histogram(const float *scores, int64_t T, int E, int nbins, uint32
 
 int launch_qb_update(const uint32_t *hist, int E, int nbins, int k, float *q_out, float *bias,
                      cudaStream_t st) {
-    const size_t smem = (size_t)((E + QBU_CTAS - 1) / QBU_CTAS) * sizeof(double);
+    const size_t smem = QBU_STAGE_WORDS * sizeof(uint32_t) +
+                        (size_t)((E + QBU_CTAS - 1) / QBU_CTAS) * sizeof(double);
     cudaError_t e = cudaFuncSetAttribute(qb_update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(smem < 48 * 1024 ? 48 * 1024 : smem));
+                                         (int)smem);
     if (e != cudaSuccess) return fail(SLMOE_ECUDA, "qb update smem: %s", cudaGetErrorString(e));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(QBU_CTAS, 1, 1);

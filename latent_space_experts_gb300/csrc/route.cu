@@ -15,7 +15,7 @@
 namespace slmoe {
 namespace {
 
-constexpr int TOPK_WARPS = 8;
+constexpr int TOPK_MAX_WARPS = 16;    // one token per warp when shared memory allows
 constexpr int MAX_E = 4096;
 constexpr int LIST = 4;              // candidates each lane keeps in registers
 
@@ -37,12 +37,13 @@ __device__ __forceinline__ void list_insert(float (&lv)[LIST], int (&li)[LIST], 
     }
 }
 
-// One block per chunk of ROUTE_CHUNK tokens, one warp per token at a time.  Lane l owns the
+// One block per chunk of ROUTE_CHUNK tokens, one warp per token (fewer warps, looping, when
+// E is too large for a staging row per warp).  Lane l owns the
 // experts e = l, l + 32, ...; it keeps its best LIST (biased score, index) pairs in
 // registers.  Each of the k rounds takes the warp-wide best head (ties to the lower index)
 // and the owning lane pops it; a lane whose list runs dry rescans its experts for the best
 // ones that its last popped pair beats (everything above that was taken already).
-__global__ void __launch_bounds__(TOPK_WARPS * 32)
+__global__ void __launch_bounds__(TOPK_MAX_WARPS * 32)
 topk_kernel(const float *__restrict__ scores, const float *__restrict__ bias, int T, int E,
             int k, int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
             int32_t *__restrict__ chunk_counts, int32_t *status) {
@@ -62,7 +63,8 @@ topk_kernel(const float *__restrict__ scores, const float *__restrict__ bias, in
     const int t_begin = blockIdx.x * ROUTE_CHUNK;
     const int n_local = lane < E ? (E - lane + 31) / 32 : 0;
     int nan_count = 0;
-    for (int tt = warp; tt < ROUTE_CHUNK; tt += TOPK_WARPS) {
+    const int nwarps = blockDim.x >> 5;
+    for (int tt = warp; tt < ROUTE_CHUNK; tt += nwarps) {
         const int t = t_begin + tt;
         if (t >= T) break;
         const float *srow = scores + (int64_t)t * E;
@@ -236,14 +238,13 @@ int launch_topk(const float *scores, const float *bias, int T, int E, int k, int
                 float *topk_w, int32_t *chunk_counts, int32_t *status, cudaStream_t st) {
     const int nchunks = (T + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
     if (nchunks == 0) return SLMOE_OK;
-    const size_t smem = (size_t)(2 + TOPK_WARPS) * E * sizeof(float);
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess) return fail(SLMOE_ECUDA, "topk smem attribute: %s", cudaGetErrorString(e));
-    }
-    topk_kernel<<<nchunks, TOPK_WARPS * 32, smem, st>>>(scores, bias, T, E, k, topk_idx, topk_w,
-                                                        chunk_counts, status);
+    // bias + counters + one staging row per warp must fit in 227 KB of shared memory
+    int warps = (int)(232448 / ((size_t)4 * E)) - 2;
+    warps = warps > TOPK_MAX_WARPS ? TOPK_MAX_WARPS : (warps < 1 ? 1 : warps);
+    const size_t smem = (size_t)(2 + warps) * E * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return fail(SLMOE_ECUDA, "topk smem attribute: %s", cudaGetErrorString(e));
+    topk_kernel<<<nchunks, warps * 32, smem, st>>>(scores, bias, T, E, k, topk_idx, topk_w, chunk_counts, status);
     return check_launch("topk");
 }
 
