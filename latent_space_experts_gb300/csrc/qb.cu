@@ -131,11 +131,15 @@ qb_update_kernel(const uint32_t *__restrict__ hist, int E, int nbins, int k,
     uint32_t *tile = stage + w * (QBU_MAXB * 33);
     for (int e = e0 + w; e < e1; e += QBU_THREADS / 32) {
         const uint32_t *h = hist + (int64_t)e * nbins;
+        uint32_t ld[QBU_MAXB];                   // all loads first: one memory latency
 #pragma unroll
         for (int i = 0; i < QBU_MAXB; ++i) {
             const int b = i * 32 + lane;
-            if (i < B) tile[b + i] = b < nbins ? h[b] : 0u;
+            ld[i] = (i < B && b < nbins) ? __ldg(h + b) : 0u;
         }
+#pragma unroll
+        for (int i = 0; i < QBU_MAXB; ++i)
+            if (i < B) tile[i * 32 + lane + i] = ld[i];
         __syncwarp();
         uint32_t v[QBU_MAXB];
         unsigned long long S = 0;

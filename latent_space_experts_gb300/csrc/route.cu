@@ -139,103 +139,6 @@ topk_kernel(const float *__restrict__ scores, const float *__restrict__ bias, in
     for (int i = tid; i < E; i += blockDim.x) cc[i] = cnt[i];
 }
 
-// Register variant for E <= 32 * TOPK_MAXQ: lane l keeps the scores of experts l, l + 32, ...
-// in registers (loaded in one batch), so a block needs shared memory only for the bias and
-// the chunk counters and every block of the grid is resident at once.  The raw score of each
-// winner is broadcast from its owner lane.
-constexpr int TOPK_MAXQ = 32;
-__global__ void __launch_bounds__(TOPK_MAX_WARPS * 32, 2)
-topk_reg_kernel(const float *__restrict__ scores, const float *__restrict__ bias, int T, int E,
-                int k, int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
-                int32_t *__restrict__ chunk_counts, int32_t *status) {
-    extern __shared__ float sm[];
-    float *bias_s = sm;
-    int *cnt = reinterpret_cast<int *>(sm + E);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int i = tid; i < E; i += blockDim.x) {
-        bias_s[i] = bias[i];
-        cnt[i] = 0;
-    }
-    __syncthreads();
-    const int nwarps = blockDim.x >> 5;
-    const int t_begin = blockIdx.x * ROUTE_CHUNK;
-    const int n_local = lane < E ? (E - lane + 31) / 32 : 0;
-    int nan_count = 0;
-    for (int tt = warp; tt < ROUTE_CHUNK; tt += nwarps) {
-        const int t = t_begin + tt;
-        if (t >= T) break;
-        const float *srow = scores + (int64_t)t * E;
-        float raw[TOPK_MAXQ];
-#pragma unroll
-        for (int q = 0; q < TOPK_MAXQ; ++q) raw[q] = (lane + 32 * q < E) ? __ldcs(srow + lane + 32 * q) : 0.f;
-        float lv[LIST];
-        int li[LIST];
-#pragma unroll
-        for (int p = 0; p < LIST; ++p) { lv[p] = -INFINITY; li[p] = INT_MAX; }
-#pragma unroll
-        for (int q = 0; q < TOPK_MAXQ; ++q) {
-            const int e = lane + 32 * q;
-            if (e < E) {
-                float b;
-                if (isnan(raw[q])) { ++nan_count; raw[q] = NAN; b = -INFINITY; }
-                else b = raw[q] + bias_s[e];
-                list_insert(lv, li, b, e);
-            }
-        }
-        int popped = 0;
-        int my_e = 0;
-        float my_s = 0.f;
-        for (int j = 0; j < k; ++j) {
-            float v = lv[0];
-            int i = li[0];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-                const int oi = __shfl_xor_sync(0xffffffffu, i, o);
-                if (beats(ov, oi, v, i)) { v = ov; i = oi; }
-            }
-            const bool owner = li[0] == i;
-            float s_own = 0.f;
-            if (owner) {                          // pop the winner; refill from registers if dry
-                const float last_v = lv[0];
-                const int last_i = li[0];
-#pragma unroll
-                for (int q = 0; q < TOPK_MAXQ; ++q)
-                    if (lane + 32 * q == last_i) s_own = isnan(raw[q]) ? 0.f : raw[q];
-#pragma unroll
-                for (int p = 0; p < LIST - 1; ++p) { lv[p] = lv[p + 1]; li[p] = li[p + 1]; }
-                lv[LIST - 1] = -INFINITY;
-                li[LIST - 1] = INT_MAX;
-                ++popped;
-                if (li[0] == INT_MAX && popped < n_local) {
-#pragma unroll
-                    for (int q = 0; q < TOPK_MAXQ; ++q) {
-                        const int e = lane + 32 * q;
-                        if (e < E) {
-                            const float b = isnan(raw[q]) ? -INFINITY : raw[q] + bias_s[e];
-                            if (beats(last_v, last_i, b, e)) list_insert(lv, li, b, e);
-                        }
-                    }
-                }
-            }
-            const float s_win = __shfl_sync(0xffffffffu, s_own, i & 31);
-            if (lane == j) { my_e = i; my_s = s_win; }
-        }
-        const float sum = warp_sum(lane < k ? my_s : 0.f);
-        if (lane < k) {
-            topk_idx[(int64_t)t * k + lane] = my_e;
-            topk_w[(int64_t)t * k + lane] = sum > 0.f ? my_s / sum : 1.0f / (float)k;
-            atomicAdd(&cnt[my_e], 1);
-        }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) nan_count += __shfl_xor_sync(0xffffffffu, nan_count, o);
-    if (lane == 0 && nan_count && status) atomicAdd(&status[ST_NAN], nan_count);
-    __syncthreads();
-    int32_t *cc = chunk_counts + (int64_t)blockIdx.x * E;
-    for (int i = tid; i < E; i += blockDim.x) cc[i] = cnt[i];
-}
-
 // Per-expert exclusive scan of the chunk counts (chunk_counts becomes the chunk bases) and
 // the expert totals.  One block per 32 experts (lane = expert); warp w covers a contiguous
 // range of chunks; the warps' partial sums are scanned in shared memory.
@@ -335,11 +238,6 @@ int launch_topk(const float *scores, const float *bias, int T, int E, int k, int
                 float *topk_w, int32_t *chunk_counts, int32_t *status, cudaStream_t st) {
     const int nchunks = (T + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
     if (nchunks == 0) return SLMOE_OK;
-    if (E <= 32 * TOPK_MAXQ) {
-        topk_reg_kernel<<<nchunks, TOPK_MAX_WARPS * 32, (size_t)2 * E * sizeof(float), st>>>(
-            scores, bias, T, E, k, topk_idx, topk_w, chunk_counts, status);
-        return check_launch("topk");
-    }
     // bias + counters + one staging row per warp must fit in 227 KB of shared memory
     int warps = (int)(232448 / ((size_t)4 * E)) - 2;
     warps = warps > TOPK_MAX_WARPS ? TOPK_MAX_WARPS : (warps < 1 ? 1 : warps);

@@ -522,12 +522,23 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_kernel(const __grid_cons
             const int n0 = (tile % a.tiles_n) * RT_BN + half * RT_HALF;
             if (row < a.M) {
                 float *C = static_cast<float *>(a.C) + (long long)row * a.ldc;
+                const bool vec = (a.ldc & 3) == 0;       // rows 16-byte aligned: float4 stores
 #pragma unroll
-                for (int i = 0; i < RT_HALF; ++i) {
+                for (int i = 0; i < RT_HALF; i += 4) {
+                    float o[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int n = n0 + i + j;
+                        const float v = acc[i + j] + ((a.mu && n < a.N) ? a.mu[n] : 0.f);
+                        o[j] = 1.0f / (1.0f + expf(-v));
+                    }
                     const int n = n0 + i;
-                    if (n < a.N) {
-                        const float v = acc[i] + (a.mu ? a.mu[n] : 0.f);
-                        C[n] = 1.0f / (1.0f + expf(-v));
+                    if (vec && n + 4 <= a.N) {
+                        *reinterpret_cast<float4 *>(C + n) = make_float4(o[0], o[1], o[2], o[3]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (n + j < a.N) C[n + j] = o[j];
                     }
                 }
             }
