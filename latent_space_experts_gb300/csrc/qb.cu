@@ -160,23 +160,26 @@ qb_update_kernel(const uint32_t *__restrict__ hist, int E, int nbins, int k,
         const double r = p * (double)N;
         double q = 0.0;
         if (r > 0.0) {
-            const unsigned m = __ballot_sync(0xffffffffu, (double)inc >= r);
+            // C_j >= r  <=>  C_j >= ceil(r) for integer counts: the search is integer-only
+            // (fp64 is slow on this part) and decides exactly as the fp64 comparison would
+            const unsigned long long rc = (unsigned long long)ceil(r);
+            const unsigned m = __ballot_sync(0xffffffffu, inc >= rc);
             const int l = __ffs(m) - 1;          // the lane whose bins hold rank r
             double qq = 0.0;
             if (lane == l) {
                 unsigned long long C = inc - S;  // cumulative count before this lane's bins
+                int j = 0;
+                unsigned long long prev = C, hj = 1;
                 bool done = false;
 #pragma unroll
                 for (int i = 0; i < QBU_MAXB; ++i) {
                     if (!done && i < B) {
-                        const unsigned long long prev = C;
+                        const unsigned long long before = C;
                         C += v[i];
-                        if ((double)C >= r) {
-                            qq = ((double)(b0 + i) + (r - (double)prev) / (double)v[i]) / (double)nbins;
-                            done = true;
-                        }
+                        if (C >= rc) { j = b0 + i; prev = before; hj = v[i]; done = true; }
                     }
                 }
+                qq = ((double)j + (r - (double)prev) / (double)hj) / (double)nbins;
             }
             q = __shfl_sync(0xffffffffu, qq, l);
         }
