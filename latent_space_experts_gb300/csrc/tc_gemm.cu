@@ -569,15 +569,28 @@ constexpr int G_THREADS = 320;                    // TMA, MMA, 4 epilogue, 4 gat
 constexpr int G_GATHER_THREADS = 128;
 constexpr int G_LIST = 192;                       // units listed in shared memory per CTA
 
-template <int NSUB>
+template <bool DBUF>
 struct GCfg {
+    static constexpr int NSUB = 2;
     static constexpr int A_BYTES = NSUB * 128 * 128;
     static constexpr int A_STAGES = (128 * 1024) / A_BYTES;
     static constexpr int B_BYTES = G_NMAX * 128;
     static constexpr int B_STAGES = 3;
-    static constexpr int NBUF = NSUB == 2 ? 1 : 2;
+    // DBUF: an expert's tokens go in balanced passes of <= 128, alternating between two TMEM
+    // accumulator sets (sub-tile 1 at column +128), so a pass's epilogue overlaps the next
+    // pass's MMAs.  Otherwise passes of <= 256 tokens share one set (sub-tile 1 at +256).
+    static constexpr int NBUF = DBUF ? 2 : 1;
+    static constexpr int PASS = DBUF ? 128 : G_NMAX;
+    static constexpr int SUB1_COL = DBUF ? 128 : 256;
     static constexpr int SMEM = A_STAGES * A_BYTES + B_STAGES * B_BYTES + G_LIST * 8 + 1024 + 256;
 };
+
+// Token passes of an expert with n tokens: npass passes of `chunk` tokens (the last shorter).
+template <int PASS>
+__device__ __forceinline__ int pass_chunk(int n) {
+    const int npass = (n + PASS - 1) / PASS;
+    return npass > 0 ? (n + npass - 1) / npass : 0;
+}
 
 struct GroupedArgs {
     int E, kblocks, nfb;
@@ -621,10 +634,11 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
     return p;
 }
 
-template <int EPI, int NSUB>
+template <int EPI, bool DBUF>
 __global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_constant__ CUtensorMap wmap,
                                                                const GroupedArgs a) {
-    using Cfg = GCfg<NSUB>;
+    using Cfg = GCfg<DBUF>;
+    constexpr int NSUB = Cfg::NSUB, PASS = Cfg::PASS, SUB1 = Cfg::SUB1_COL;
     constexpr int AST = Cfg::A_STAGES, BST = Cfg::B_STAGES, NBUF = Cfg::NBUF;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -676,7 +690,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_cons
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ weights by TMA (streamed once)
-        const uint64_t pol = policy_evict_first();
+        const uint64_t pol_first = policy_evict_first(), pol_last = policy_evict_last();
         int stage = 0;
         uint32_t phase = 0;
         for (int i = 0; i < my_n; ++i) {
@@ -684,14 +698,16 @@ __global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_cons
             const int e = u / a.nfb, fb = u - e * a.nfb;
             const int n_e = entry(i).x;
             const int row0 = e * a.a_rows_pe + fb * a.a_fb_stride;
-            for (int c0 = 0; c0 < n_e; c0 += G_NMAX) {
+            const int chunk = pass_chunk<PASS>(n_e);
+            for (int c0 = 0; c0 < n_e; c0 += chunk) {
+                // the weight tile is streamed once: keep it in L2 only for a following pass
+                const uint64_t pol = c0 + chunk < n_e ? pol_last : pol_first;
                 for (int kb = 0; kb < a.kblocks; ++kb) {
                     if (!mbar_wait(&a_empty[stage], phase ^ 1, abort_flag)) goto done;
                     mbar_expect_tx(&a_full[stage], Cfg::A_BYTES);
                     const uint32_t sa = su32(sA + stage * Cfg::A_BYTES);
                     tma_load_2d_hint(sa, &wmap, &a_full[stage], kb * 64, row0, pol);
-                    if (NSUB == 2)
-                        tma_load_2d_hint(sa + 128 * 128, &wmap, &a_full[stage], kb * 64, row0 + a.a_sub1, pol);
+                    tma_load_2d_hint(sa + 128 * 128, &wmap, &a_full[stage], kb * 64, row0 + a.a_sub1, pol);
                     if (++stage == AST) { stage = 0; phase ^= 1; }
                 }
             }
@@ -702,12 +718,13 @@ __global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_cons
         uint32_t aph = 0, bph = 0, tph = 0;
         for (int i = 0; i < my_n; ++i) {
             const int n_e = entry(i).x;
-            for (int c0 = 0; c0 < n_e; c0 += G_NMAX) {
-                const int N = min(G_NMAX, n_e - c0);
+            const int chunk = pass_chunk<PASS>(n_e);
+            for (int c0 = 0; c0 < n_e; c0 += chunk) {
+                const int N = min(chunk, n_e - c0);
                 const uint32_t idesc = idesc_bf16(128, (N + 15) & ~15);
                 if (!mbar_wait(&tempty[buf], tph ^ 1, abort_flag)) goto done;
                 tc_after();
-                const uint32_t d = tmem_base + (NSUB == 2 ? 0 : buf * 256);
+                const uint32_t d = tmem_base + buf * 256;
                 for (int kb = 0; kb < a.kblocks; ++kb) {
                     if (!mbar_wait(&a_full[as], aph, abort_flag)) goto done;
                     if (!mbar_wait(&b_full[bs], bph, abort_flag)) goto done;
@@ -720,7 +737,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_cons
                         const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
                         const uint64_t bd = sdesc(sb + kk * 32);
                         umma(d, sdesc(sa + kk * 32), bd, idesc, acc);
-                        if (NSUB == 2) umma(d + 256, sdesc(sa + 128 * 128 + kk * 32), bd, idesc, acc);
+                        umma(d + SUB1, sdesc(sa + 128 * 128 + kk * 32), bd, idesc, acc);
                     }
                     umma_commit(&a_empty[as]);
                     umma_commit(&b_empty[bs]);
@@ -743,23 +760,24 @@ __global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_cons
             const int fb = u % a.nfb;
             const int2 ent = entry(i);
             const int n_e = ent.x, off = ent.y;
-            for (int c0 = 0; c0 < n_e; c0 += G_NMAX) {
-                const int N = min(G_NMAX, n_e - c0);
+            const int chunk = pass_chunk<PASS>(n_e);
+            for (int c0 = 0; c0 < n_e; c0 += chunk) {
+                const int N = min(chunk, n_e - c0);
                 const int Np = (N + 15) & ~15;
                 if (!mbar_wait(&tfull[buf], tph, abort_flag)) goto done;
                 tc_after();
-                const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (NSUB == 2 ? 0 : buf * 256);
+                const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + buf * 256;
                 // GLU: sub-tiles are the gate and up rows of h column fb*128 + lf.  Plain: the
                 // NSUB sub-tiles are output features fb*128*NSUB + lf + 128*sub.
                 const int f = (EPI == EPI_GLU ? fb * 128 : fb * 128 * NSUB) + lf;
                 const bool ok = f < a.out_cols;
-                const bool ok1 = NSUB == 2 && f + 128 < a.out_cols;
+                const bool ok1 = f + 128 < a.out_cols;
                 __nv_bfloat16 *o = a.out + (long long)(off + c0) * a.out_ld + f;
                 for (int c = 0; c < Np; c += 16) {
                     if (EPI == EPI_GLU) {
                         uint32_t g[16], v[16];
                         TMEM_LD16(tb + c, g);
-                        TMEM_LD16(tb + 256 + c, v);
+                        TMEM_LD16(tb + SUB1 + c, v);
                         tmem_wait_ld();
                         if (ok) {
 #pragma unroll
@@ -771,7 +789,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_cons
                     } else {
                         uint32_t r0[16], r1[16];
                         TMEM_LD16(tb + c, r0);
-                        if (NSUB == 2) TMEM_LD16(tb + 256 + c, r1);
+                        TMEM_LD16(tb + SUB1 + c, r1);
                         tmem_wait_ld();
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
@@ -800,8 +818,9 @@ __global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_cons
         for (int i = 0; i < my_n; ++i) {
             const int2 ent = entry(i);
             const int n_e = ent.x, off = ent.y;
-            for (int c0 = 0; c0 < n_e; c0 += G_NMAX) {
-                const int N = min(G_NMAX, n_e - c0);
+            const int chunk = pass_chunk<PASS>(n_e);
+            for (int c0 = 0; c0 < n_e; c0 += chunk) {
+                const int N = min(chunk, n_e - c0);
                 const int Np = (N + 15) & ~15;
                 const __nv_bfloat16 *src[G_NMAX / 16];
 #pragma unroll
@@ -915,16 +934,16 @@ int launch_dense(const TmaPack &maps, DenseArgs a, cudaStream_t st) {
     return check_launch("dense_kernel");
 }
 
-template <int EPI, int NSUB>
+template <int EPI, bool DBUF>
 int launch_grouped(const CUtensorMap &wmap, const GroupedArgs &a, cudaStream_t st) {
-    auto kern = grouped_kernel<EPI, NSUB>;
-    int rc = set_smem(kern, GCfg<NSUB>::SMEM);
+    auto kern = grouped_kernel<EPI, DBUF>;
+    int rc = set_smem(kern, GCfg<DBUF>::SMEM);
     if (rc) return rc;
     const int units = a.E * a.nfb;
     const int sms = sm_count();
     const int grid = units < sms ? units : sms;
     if (grid == 0) return SLMOE_OK;
-    kern<<<grid, G_THREADS, GCfg<NSUB>::SMEM, st>>>(wmap, a);
+    kern<<<grid, G_THREADS, GCfg<DBUF>::SMEM, st>>>(wmap, a);
     return check_launch("grouped_kernel");
 }
 
@@ -989,7 +1008,7 @@ int tc_forward_bf16(const slmoe_config *c, const void *x, const slmoe_weights *w
         a.b_src = static_cast<const bf *>(f.x_lat); a.b_ld = dl; a.b_K = dl;
         a.out = static_cast<bf *>(f.h); a.out_ld = I; a.out_cols = I;
         a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
-        if ((rc = launch_grouped<EPI_GLU, 2>(wm, a, st))) return rc;
+        if ((rc = launch_grouped<EPI_GLU, false>(wm, a, st))) return rc;
     }
     stage_event(4, st);
     {   // routed experts, down: y_e[row] = W2[e] h[row]
@@ -1002,7 +1021,7 @@ int tc_forward_bf16(const slmoe_config *c, const void *x, const slmoe_weights *w
         a.b_src = static_cast<const bf *>(f.h); a.b_ld = I; a.b_K = I;
         a.out = static_cast<bf *>(f.y_e); a.out_ld = dl; a.out_cols = dl;
         a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
-        if ((rc = launch_grouped<EPI_BF16, 2>(wm, a, st))) return rc;
+        if ((rc = launch_grouped<EPI_BF16, true>(wm, a, st))) return rc;
     }
     stage_event(5, st);
     (void)Tk;
