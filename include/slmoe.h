@@ -16,8 +16,14 @@
  *     work is enqueued on it; no call synchronises the host or copies device->host, so a
  *     call returns before its kernels finish ([SLMoE] 训练基础设施: no host sync on the
  *     critical path).  Calls that share output buffers must be ordered on one stream.
- *   - The library allocates nothing.  Scratch lives in a caller-provided workspace of at
- *     least slmoe_workspace_size() bytes, 256-byte aligned.
+ *   - The library allocates no memory.  Scratch lives in a caller-provided workspace of at
+ *     least slmoe_workspace_size() bytes, 256-byte aligned.  On the bf16 type,
+ *     slmoe_forward creates, on its first call on a device, one auxiliary CUDA stream (lowest
+ *     priority) and two events, kept until the process exits: it forks the down-projection
+ *     and the shared experts' gate|up onto that stream, routes on the caller's stream
+ *     meanwhile, and joins back through an event before the routed experts.  Consecutive
+ *     calls on one device therefore share that stream; calls from several host threads on
+ *     one device must be serialised by the caller.
  *   - Return value: SLMOE_OK (0) or a negative code.  Arguments are validated on the host
  *     before any launch; on error nothing is launched and slmoe_last_error() gives a
  *     thread-local message.  No C++ exception crosses the ABI.
@@ -116,10 +122,12 @@ SLMOE_API const char *slmoe_last_error(void);
 SLMOE_API int slmoe_device_sm_count(void);
 
 /* Stage profiling hook (thread-local).  When events is not NULL, slmoe_forward records
- * events[i] (a cudaEvent_t created by the caller, passed as void*) on its stream right after
- * stage i, for i < n:  0 start, 1 router scores, 2 top-k + permutation (+ histogram),
- * 3 latent down-projection, 4 expert gate|up + SiTU-GLU, 5 expert down, 6 combine + RMSNorm,
- * 7 shared gate|up + SiTU-GLU, 8 up-projection + shared down.  NULL turns it off. */
+ * events[i] (a cudaEvent_t created by the caller, passed as void*) right after stage i, for
+ * i < n:  0 start, 1 router scores, 2 top-k + permutation (+ histogram), 3 latent
+ * down-projection, 4 expert gate|up + SiTU-GLU, 5 expert down, 6 combine + RMSNorm, 7 shared
+ * gate|up + SiTU-GLU, 8 up-projection + shared down.  On the bf16 type, stages 3 and 7 run
+ * on the library's auxiliary stream (recorded there), started at stage 0 and concurrent
+ * with stages 1-2; stage 4 starts when 2 and 7 are both done.  NULL turns it off. */
 SLMOE_API int slmoe_set_stage_events(void **events, int n);
 
 /* Number of kernels this library has launched in this process (all threads). */

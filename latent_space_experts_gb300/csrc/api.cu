@@ -1,6 +1,7 @@
 // The C ABI of slmoe.h: argument validation, the workspace layout, and the sequencing of
 // the kernels of one call on the caller's stream.  Nothing here synchronises the host.
 #include <atomic>
+#include <mutex>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -96,6 +97,7 @@ int make_layout(const slmoe_config *c, Layout *L) {
     L->pub.h_s = take(T * (size_t)c->n_shared * c->I_shared * es);
     L->pub.status = take(16);
     L->wr_split = c->dtype == SLMOE_BF16 ? take(3 * E * c->d * 2) : 0;
+    L->counters = take(16 * 4);
     L->pub.total = off;
     return SLMOE_OK;
 }
@@ -117,17 +119,46 @@ struct Routing {
     int32_t *topk_idx;
     float *topk_w;
     int32_t *counts, *offsets, *perm, *slot_pos, *chunk_counts;
+    int *counters;          // zeroed tile counters; [0] is the router's
 };
+
+// One auxiliary stream (lowest priority) and a fork/join event pair per device, created on
+// first use and kept until the process exits.  The bf16 forward runs the parts of the layer
+// that need only x there, concurrently with routing on the caller's stream.
+struct AuxStreams {
+    cudaStream_t aux = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+constexpr int MAX_DEVICES = 64;
+static AuxStreams g_aux[MAX_DEVICES];
+static std::mutex g_aux_mu;
+
+static int aux_streams(AuxStreams **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES)
+        return fail(SLMOE_ECUDA, "no current device");
+    std::lock_guard<std::mutex> lock(g_aux_mu);
+    AuxStreams &a = g_aux[dev];
+    if (!a.aux) {
+        int least = 0, greatest = 0;
+        if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
+            cudaStreamCreateWithPriority(&a.aux, cudaStreamNonBlocking, least) != cudaSuccess ||
+            cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming) != cudaSuccess)
+            return check_launch("auxiliary stream");
+    }
+    *out = &a;
+    return SLMOE_OK;
+}
 
 // Router scores, top-k and permutation.  (苏神复盘 Kimi K3 §01-§02.)
 static int route_impl(const slmoe_config *c, const Layout &L, char *ws, const void *x,
                       const float *W_r, const float *bias, const float *mu, const Routing &R,
                       uint32_t *hist, int32_t *status, cudaStream_t st) {
     int rc;
-    stage_event(0, st);
     if (c->dtype == SLMOE_BF16) {
         rc = tc_router_scores(c, x, W_r, mu, reinterpret_cast<__nv_bfloat16 *>(ws + L.wr_split),
-                              R.scores, status, st);
+                              R.scores, status, R.counters, st);
     } else {
         SimtGemm g = {};
         g.seg[0] = {x, W_r, c->d, c->d, c->d, 0};
@@ -292,7 +323,10 @@ int slmoe_route(const slmoe_config *cfg, const void *x, const float *W_r, const 
         return SLMOE_OK;
     }
     Routing R = {scores ? scores : reinterpret_cast<float *>(ws + L.pub.scores), topk_idx, topk_w,
-                 counts, offsets, perm, slot_pos, reinterpret_cast<int32_t *>(ws + L.chunk_counts)};
+                 counts, offsets, perm, slot_pos, reinterpret_cast<int32_t *>(ws + L.chunk_counts),
+                 reinterpret_cast<int *>(ws + L.counters)};
+    if (cudaMemsetAsync(R.counters, 0, 16 * sizeof(int), st) != cudaSuccess) return check_launch("memset");
+    stage_event(0, st);
     return route_impl(cfg, L, ws, x, W_r, bias, logit_offset, R, hist, status, st);
 }
 
@@ -350,13 +384,18 @@ int slmoe_forward(const slmoe_config *cfg, const void *x, const slmoe_weights *w
                  reinterpret_cast<int32_t *>(ws + L.pub.offsets),
                  reinterpret_cast<int32_t *>(ws + L.pub.perm),
                  reinterpret_cast<int32_t *>(ws + L.pub.slot_pos),
-                 reinterpret_cast<int32_t *>(ws + L.chunk_counts)};
-    if ((rc = route_impl(cfg, L, ws, x, w->W_r, bias, logit_offset, R, hist, stat, st))) return rc;
-    if (topk_idx_out &&
-        cudaMemcpyAsync(topk_idx_out, R.topk_idx, (size_t)cfg->T * cfg->k * 4, cudaMemcpyDeviceToDevice,
-                        st) != cudaSuccess)
-        return check_launch("copy topk_idx");
-    if (cfg->dtype == SLMOE_F32) return forward_f32(cfg, L, ws, x, w, R, y, st);
+                 reinterpret_cast<int32_t *>(ws + L.chunk_counts),
+                 reinterpret_cast<int *>(ws + L.counters)};
+    if (cudaMemsetAsync(R.counters, 0, 16 * sizeof(int), st) != cudaSuccess) return check_launch("memset");
+    stage_event(0, st);
+    if (cfg->dtype == SLMOE_F32) {
+        if ((rc = route_impl(cfg, L, ws, x, w->W_r, bias, logit_offset, R, hist, stat, st))) return rc;
+        if (topk_idx_out &&
+            cudaMemcpyAsync(topk_idx_out, R.topk_idx, (size_t)cfg->T * cfg->k * 4, cudaMemcpyDeviceToDevice,
+                            st) != cudaSuccess)
+            return check_launch("copy topk_idx");
+        return forward_f32(cfg, L, ws, x, w, R, y, st);
+    }
     TcForward tf = {};
     tf.x_lat = ws + L.pub.x_lat;
     tf.h = ws + L.pub.h;
@@ -369,7 +408,22 @@ int slmoe_forward(const slmoe_config *cfg, const void *x, const slmoe_weights *w
     tf.perm = R.perm;
     tf.slot_pos = R.slot_pos;
     tf.status = stat;
-    return tc_forward_bf16(cfg, x, w, tf, y, st);
+    tf.counters = R.counters;
+    // the down-projection and the shared experts' gate|up need only x: fork them onto the
+    // auxiliary stream, route on the caller's stream meanwhile, join before the routed experts
+    AuxStreams *aux = nullptr;
+    if ((rc = aux_streams(&aux))) return rc;
+    if (cudaEventRecord(aux->fork, st) != cudaSuccess || cudaStreamWaitEvent(aux->aux, aux->fork, 0) != cudaSuccess)
+        return check_launch("fork");
+    if ((rc = tc_forward_front(cfg, x, w, tf, aux->aux))) return rc;
+    if (cudaEventRecord(aux->join, aux->aux) != cudaSuccess) return check_launch("join");
+    if ((rc = route_impl(cfg, L, ws, x, w->W_r, bias, logit_offset, R, hist, stat, st))) return rc;
+    if (topk_idx_out &&
+        cudaMemcpyAsync(topk_idx_out, R.topk_idx, (size_t)cfg->T * cfg->k * 4, cudaMemcpyDeviceToDevice,
+                        st) != cudaSuccess)
+        return check_launch("copy topk_idx");
+    if (cudaStreamWaitEvent(st, aux->join, 0) != cudaSuccess) return check_launch("join wait");
+    return tc_forward_back(cfg, w, tf, y, st);
 }
 
 }  // extern "C"

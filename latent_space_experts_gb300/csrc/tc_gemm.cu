@@ -146,6 +146,35 @@ __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.
                    "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])                           \
                  : "r"(taddr))
 
+// Tile ids flow from the producer thread to the MMA thread and the epilogue warps through a
+// TQ-slot shared-memory queue guarded by mbarriers.  The producer draws ids from a global
+// counter when one is given (dynamic scheduling: a CTA that starts late, while another
+// kernel still holds its SM, simply takes fewer tiles), else walks the static sequence
+// blockIdx.x, blockIdx.x + gridDim.x, ...; an id >= tiles ends every role's loop.
+constexpr int TQ = 2;
+__device__ __forceinline__ bool tq_push(int *ids, uint64_t *full, uint64_t *empty, int &slot, uint32_t &ph,
+                                        int tile, volatile int *abort_flag) {
+    if (!mbar_wait(&empty[slot], ph ^ 1, abort_flag)) return false;
+    ids[slot] = tile;
+    mbar_arrive(&full[slot]);
+    if (++slot == TQ) { slot = 0; ph ^= 1; }
+    return true;
+}
+// pop for a single consumer thread (arrives itself) or a warp (lane 0 arrives after the warp read)
+__device__ __forceinline__ bool tq_pop(int *ids, uint64_t *full, uint64_t *empty, int &slot, uint32_t &ph,
+                                       int &tile, volatile int *abort_flag, bool warp_wide) {
+    if (!mbar_wait(&full[slot], ph, abort_flag)) return false;
+    tile = ids[slot];
+    if (warp_wide) {
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(&empty[slot]);
+    } else {
+        mbar_arrive(&empty[slot]);
+    }
+    if (++slot == TQ) { slot = 0; ph ^= 1; }
+    return true;
+}
+
 // K-major operand tile of rows x 64 bf16 (128 bytes per row) with the 128-byte swizzle:
 // 8-row groups 1024 bytes apart.  The start address advances 32 bytes per K = 16 step.
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
@@ -178,9 +207,10 @@ struct DenseArgs {
     int tiles_n, tiles;
     void *C;
     long long ldc;
-    const float *mu;       // ROUTER: logit offset per column (nullable)
+    const float *mu;       // router: logit offset per column (nullable)
     float beta1, beta2;
     int32_t *status;
+    int *counter;          // nullable: global tile counter (zeroed) for dynamic scheduling
 };
 
 template <int BN, int EPI, int PACC>
@@ -209,7 +239,10 @@ __global__ void __launch_bounds__(192, 1) dense_kernel(const __grid_constant__ T
     uint64_t *empty = full + STAGES;
     uint64_t *tfull = empty + STAGES;
     uint64_t *tempty = tfull + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+    uint64_t *tq_full = tempty + 2;
+    uint64_t *tq_empty = tq_full + TQ;
+    int *tq_ids = reinterpret_cast<int *>(tq_empty + TQ);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tq_ids + TQ);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -221,6 +254,10 @@ __global__ void __launch_bounds__(192, 1) dense_kernel(const __grid_constant__ T
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
             mbar_init(&tempty[b], 4);
+        }
+        for (int q = 0; q < TQ; ++q) {
+            mbar_init(&tq_full[q], 1);
+            mbar_init(&tq_empty[q], 5);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -235,7 +272,12 @@ __global__ void __launch_bounds__(192, 1) dense_kernel(const __grid_constant__ T
         // ------------------------------------------------ TMA producer
         int stage = 0;
         uint32_t phase = 0;
-        for (int tile = blockIdx.x; tile < a.tiles; tile += gridDim.x) {
+        int qs = 0, it = 0;
+        uint32_t qp = 0;
+        for (;;) {
+            const int tile = a.counter ? atomicAdd(a.counter, 1) : (int)blockIdx.x + (it++) * (int)gridDim.x;
+            if (!tq_push(tq_ids, tq_full, tq_empty, qs, qp, tile, abort_flag)) goto done;
+            if (tile >= a.tiles) break;
             const int m0 = (tile / a.tiles_n) * Cfg::BM;
             const int n0 = (tile % a.tiles_n) * Cfg::BN_OUT;
             for (int s = 0; s < a.nseg; ++s) {
@@ -263,7 +305,12 @@ __global__ void __launch_bounds__(192, 1) dense_kernel(const __grid_constant__ T
         uint32_t phase = 0;
         int buf = 0;
         uint32_t bphase = 0;
-        for (int tile = blockIdx.x; tile < a.tiles; tile += gridDim.x) {
+        int qs = 0;
+        uint32_t qp = 0;
+        for (;;) {
+            int tile;
+            if (!tq_pop(tq_ids, tq_full, tq_empty, qs, qp, tile, abort_flag, false)) goto done;
+            if (tile >= a.tiles) break;
             if (!mbar_wait(&tempty[buf], bphase ^ 1, abort_flag)) goto done;
             tc_after();
             const uint32_t dbase = tmem_base + buf * Cfg::ACC;
@@ -292,7 +339,12 @@ __global__ void __launch_bounds__(192, 1) dense_kernel(const __grid_constant__ T
         const int row_in_tile = q * 32 + lane;
             int buf = 0;
         uint32_t bphase = 0;
-        for (int tile = blockIdx.x; tile < a.tiles; tile += gridDim.x) {
+        int qs = 0;
+        uint32_t qp = 0;
+        for (;;) {
+            int tile;
+            if (!tq_pop(tq_ids, tq_full, tq_empty, qs, qp, tile, abort_flag, true)) goto done;
+            if (tile >= a.tiles) break;
             if (!mbar_wait(&tfull[buf], bphase, abort_flag)) goto done;
             tc_after();
             const int row = (tile / a.tiles_n) * Cfg::BM + row_in_tile;
@@ -423,7 +475,10 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_kernel(const __grid_cons
     uint64_t *empty = full + RT_STAGES;
     uint64_t *tfull = empty + RT_STAGES;
     uint64_t *tempty = tfull + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+    uint64_t *tq_full = tempty + 2;
+    uint64_t *tq_empty = tq_full + TQ;
+    int *tq_ids = reinterpret_cast<int *>(tq_empty + TQ);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tq_ids + TQ);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -435,6 +490,10 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_kernel(const __grid_cons
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
             mbar_init(&tempty[b], 8);
+        }
+        for (int q = 0; q < TQ; ++q) {
+            mbar_init(&tq_full[q], 1);
+            mbar_init(&tq_empty[q], 9);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -450,7 +509,12 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_kernel(const __grid_cons
     if (warp == 0 && lane == 0) {
         int stage = 0;
         uint32_t phase = 0;
-        for (int tile = blockIdx.x; tile < a.tiles; tile += gridDim.x) {
+        int qs = 0, it = 0;
+        uint32_t qp = 0;
+        for (;;) {
+            const int tile = a.counter ? atomicAdd(a.counter, 1) : (int)blockIdx.x + (it++) * (int)gridDim.x;
+            if (!tq_push(tq_ids, tq_full, tq_empty, qs, qp, tile, abort_flag)) goto done;
+            if (tile >= a.tiles) break;
             const int m0 = (tile / a.tiles_n) * 128;
             const int n0 = (tile % a.tiles_n) * RT_BN;
             for (int s = 0; s < a.nseg; ++s) {
@@ -470,7 +534,12 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_kernel(const __grid_cons
         uint32_t phase = 0;
         int buf = 0;
         uint32_t bphase = 0;
-        for (int tile = blockIdx.x; tile < a.tiles; tile += gridDim.x) {
+        int qs = 0;
+        uint32_t qp = 0;
+        for (;;) {
+            int tile;
+            if (!tq_pop(tq_ids, tq_full, tq_empty, qs, qp, tile, abort_flag, false)) goto done;
+            if (tile >= a.tiles) break;
             int kg = 0;
             for (int s = 0; s < a.nseg; ++s) {
                 for (int kb = 0; kb < a.kblocks[s]; ++kb, ++kg) {
@@ -503,7 +572,12 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_kernel(const __grid_cons
         const int nchunks = (ktot + RT_DRAIN - 1) / RT_DRAIN;
         int buf = 0;
         uint32_t bphase = 0;
-        for (int tile = blockIdx.x; tile < a.tiles; tile += gridDim.x) {
+        int qs = 0;
+        uint32_t qp = 0;
+        for (;;) {
+            int tile;
+            if (!tq_pop(tq_ids, tq_full, tq_empty, qs, qp, tile, abort_flag, true)) goto done;
+            if (tile >= a.tiles) break;
             float acc[RT_HALF];
 #pragma unroll
             for (int i = 0; i < RT_HALF; ++i) acc[i] = 0.f;
@@ -950,7 +1024,8 @@ int launch_grouped(const CUtensorMap &wmap, const GroupedArgs &a, cudaStream_t s
 }  // namespace
 
 int tc_router_scores(const slmoe_config *c, const void *x, const float *W_r, const float *mu,
-                     __nv_bfloat16 *wsplit, float *scores, int32_t *status, cudaStream_t st) {
+                     __nv_bfloat16 *wsplit, float *scores, int32_t *status, int *counter,
+                     cudaStream_t st) {
     const long long n = (long long)c->E * c->d;
     split_router_kernel<<<(int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096), 256, 0, st>>>(W_r, wsplit, n);
     int rc = check_launch("split_router");
@@ -970,6 +1045,7 @@ int tc_router_scores(const slmoe_config *c, const void *x, const float *W_r, con
     a.ldc = c->E;
     a.mu = mu;
     a.status = status;
+    a.counter = counter;
     a.tiles_n = (a.N + RT_BN - 1) / RT_BN;
     a.tiles = ((a.M + 127) / 128) * a.tiles_n;
     if (a.tiles == 0) return SLMOE_OK;
@@ -979,14 +1055,12 @@ int tc_router_scores(const slmoe_config *c, const void *x, const float *W_r, con
     return check_launch("router_kernel");
 }
 
-int tc_forward_bf16(const slmoe_config *c, const void *x, const slmoe_weights *w, const TcForward &f,
-                    void *y, cudaStream_t st) {
-    const int T = c->T, d = c->d, dl = c->d_latent, E = c->E, k = c->k, I = c->I;
+int tc_forward_front(const slmoe_config *c, const void *x, const slmoe_weights *w, const TcForward &f,
+                     cudaStream_t st) {
+    const int T = c->T, d = c->d, dl = c->d_latent;
     const int ns = c->n_shared, Is = c->I_shared;
-    const long long Tk = (long long)T * k;
     int rc;
     using bf = __nv_bfloat16;
-
     {   // latent down-projection: x_lat = x W_in^T
         TmaPack maps;
         memset(&maps, 0, sizeof(maps));
@@ -994,10 +1068,35 @@ int tc_forward_bf16(const slmoe_config *c, const void *x, const slmoe_weights *w
         if ((rc = make_map(&maps.b[0], w->W_in, dl, d, d, 256))) return rc;
         DenseArgs a = {};
         a.M = T; a.N = dl; a.nseg = 1; a.kblocks[0] = (d + 63) / 64;
-        a.C = f.x_lat; a.ldc = dl; a.status = f.status;
+        a.C = f.x_lat; a.ldc = dl; a.status = f.status; a.counter = f.counters + 1;
         if ((rc = launch_dense<256, EPI_BF16, 1>(maps, a, st))) return rc;
     }
     stage_event(3, st);
+    for (int s = 0; s < ns; ++s) {   // shared experts, gate|up + SiTU-GLU on full d
+        TmaPack maps;
+        memset(&maps, 0, sizeof(maps));
+        if ((rc = make_map(&maps.a[0], x, T, d, d, 128))) return rc;
+        if ((rc = make_map(&maps.b[0], static_cast<const bf *>(w->W13_s) + (size_t)s * 2 * Is * d, 2 * Is, d, d,
+                           128)))
+            return rc;
+        DenseArgs a = {};
+        a.M = T; a.N = Is; a.nseg = 1; a.kblocks[0] = (d + 63) / 64; a.glu_up_row = Is;
+        a.C = static_cast<bf *>(f.h_s) + (size_t)s * Is; a.ldc = (long long)ns * Is;
+        a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status; a.counter = f.counters + 2 + s;
+        if ((rc = launch_dense<256, EPI_GLU, 1>(maps, a, st))) return rc;
+    }
+    stage_event(7, st);
+    return SLMOE_OK;
+}
+
+int tc_forward_back(const slmoe_config *c, const slmoe_weights *w, const TcForward &f, void *y,
+                    cudaStream_t st) {
+    const int T = c->T, d = c->d, dl = c->d_latent, E = c->E, k = c->k, I = c->I;
+    const int ns = c->n_shared, Is = c->I_shared;
+    const long long Tk = (long long)T * k;
+    int rc;
+    using bf = __nv_bfloat16;
+
     {   // routed experts, gate|up + SiTU-GLU: h[perm row] = GLU(W13[e] x_lat[token])
         CUtensorMap wm;
         if ((rc = make_map(&wm, w->W13, (long long)E * 2 * I, dl, dl, 128))) return rc;
@@ -1028,20 +1127,6 @@ int tc_forward_bf16(const slmoe_config *c, const void *x, const slmoe_weights *w
     if ((rc = launch_combine_rmsnorm(DT_BF16, f.y_e, f.topk_w, f.slot_pos, w->gamma, T, dl, k, c->eps, f.z, st)))
         return rc;
     stage_event(6, st);
-    for (int s = 0; s < ns; ++s) {   // shared experts, gate|up + SiTU-GLU on full d
-        TmaPack maps;
-        memset(&maps, 0, sizeof(maps));
-        if ((rc = make_map(&maps.a[0], x, T, d, d, 128))) return rc;
-        if ((rc = make_map(&maps.b[0], static_cast<const bf *>(w->W13_s) + (size_t)s * 2 * Is * d, 2 * Is, d, d,
-                           128)))
-            return rc;
-        DenseArgs a = {};
-        a.M = T; a.N = Is; a.nseg = 1; a.kblocks[0] = (d + 63) / 64; a.glu_up_row = Is;
-        a.C = static_cast<bf *>(f.h_s) + (size_t)s * Is; a.ldc = (long long)ns * Is;
-        a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
-        if ((rc = launch_dense<256, EPI_GLU, 1>(maps, a, st))) return rc;
-    }
-    stage_event(7, st);
     {   // y = z W_out^T + sum_s h_s W2_s^T, K cut into 1 + n_shared segments
         TmaPack maps;
         memset(&maps, 0, sizeof(maps));
@@ -1059,7 +1144,7 @@ int tc_forward_bf16(const slmoe_config *c, const void *x, const slmoe_weights *w
                 return rc;
             a.kblocks[1 + s] = (Is + 63) / 64;
         }
-        a.C = y; a.ldc = d; a.status = f.status;
+        a.C = y; a.ldc = d; a.status = f.status; a.counter = f.counters + 5;
         if ((rc = launch_dense<256, EPI_F32, 1>(maps, a, st))) return rc;
     }
     stage_event(8, st);

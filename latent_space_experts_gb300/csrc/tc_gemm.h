@@ -12,17 +12,25 @@ struct TcForward {
     const float *topk_w;
     const int32_t *counts, *offsets, *perm, *slot_pos;
     int32_t *status;
+    int *counters;                      // zeroed tile counters: [1] down, [2..4] shared, [5] up
 };
 
 // Router scores s = sigmoid(x W_r^T + mu) with fp32-faithful logits: W_r is split into three
 // bf16 pieces (hi + mid + lo == W_r exactly) whose products with the bf16 x are exact in
 // fp32, accumulated on the tensor cores.  wsplit: workspace [3, E, d] bf16.
+// counter: nullable zeroed tile counter for dynamic scheduling.
 int tc_router_scores(const slmoe_config *c, const void *x, const float *W_r, const float *mu,
-                     __nv_bfloat16 *wsplit, float *scores, int32_t *status, cudaStream_t st);
+                     __nv_bfloat16 *wsplit, float *scores, int32_t *status, int *counter,
+                     cudaStream_t st);
 
-// Everything after routing: down-projection, the two grouped expert GEMMs, combine +
-// RMSNorm, shared experts and the up-projection.
-int tc_forward_bf16(const slmoe_config *c, const void *x, const slmoe_weights *w,
-                    const TcForward &f, void *y, cudaStream_t st);
+// The parts of the layer that need only x: latent down-projection and the shared experts'
+// gate|up + SiTU-GLU (run concurrently with routing).
+int tc_forward_front(const slmoe_config *c, const void *x, const slmoe_weights *w,
+                     const TcForward &f, cudaStream_t st);
+
+// Everything after routing and the front part: the two grouped expert GEMMs, combine +
+// RMSNorm, and the up-projection with the shared experts' down-projection.
+int tc_forward_back(const slmoe_config *c, const slmoe_weights *w, const TcForward &f, void *y,
+                    cudaStream_t st);
 
 }  // namespace slmoe
