@@ -411,13 +411,15 @@ int slmoe_forward(const slmoe_config *cfg, const void *x, const slmoe_weights *w
     tf.counters = R.counters;
     // the down-projection and the shared experts' gate|up need only x: fork them onto the
     // auxiliary stream, route on the caller's stream meanwhile, join before the routed experts
+    // (the routing kernels are launched first so that they take the SMs first; the
+    // persistent front kernels fill SMs as the router's tail wave frees them)
     AuxStreams *aux = nullptr;
     if ((rc = aux_streams(&aux))) return rc;
-    if (cudaEventRecord(aux->fork, st) != cudaSuccess || cudaStreamWaitEvent(aux->aux, aux->fork, 0) != cudaSuccess)
-        return check_launch("fork");
+    if (cudaEventRecord(aux->fork, st) != cudaSuccess) return check_launch("fork");
+    if ((rc = route_impl(cfg, L, ws, x, w->W_r, bias, logit_offset, R, hist, stat, st))) return rc;
+    if (cudaStreamWaitEvent(aux->aux, aux->fork, 0) != cudaSuccess) return check_launch("fork wait");
     if ((rc = tc_forward_front(cfg, x, w, tf, aux->aux))) return rc;
     if (cudaEventRecord(aux->join, aux->aux) != cudaSuccess) return check_launch("join");
-    if ((rc = route_impl(cfg, L, ws, x, w->W_r, bias, logit_offset, R, hist, stat, st))) return rc;
     if (topk_idx_out &&
         cudaMemcpyAsync(topk_idx_out, R.topk_idx, (size_t)cfg->T * cfg->k * 4, cudaMemcpyDeviceToDevice,
                         st) != cudaSuccess)
