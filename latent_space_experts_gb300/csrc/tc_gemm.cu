@@ -642,7 +642,6 @@ constexpr int G_NMAX = 256;
 constexpr int G_THREADS = 320;                    // TMA, MMA, 4 epilogue, 4 gather warps
 constexpr int G_GATHER_THREADS = 128;
 constexpr int G_LIST = 192;                       // units listed in shared memory per CTA
-constexpr int G_PF = 8;                           // weight K blocks prefetched into L2 ahead
 
 template <bool DBUF>
 struct GCfg {
@@ -691,12 +690,6 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
         " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
         "l"(map), "r"(su32(bar)), "r"(c0), "r"(c1), "l"(policy)
         : "memory");
-}
-// Prefetch a tile into L2 (no shared memory, no completion): keeps HBM busy further ahead than
-// the shared-memory ring alone can.
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int c0, int c1) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(c0), "r"(c1)
-                 : "memory");
 }
 __device__ __forceinline__ void cp_async16_hint(uint32_t dst, const void *src, uint32_t src_bytes,
                                                 uint64_t policy) {
@@ -774,19 +767,6 @@ __global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_cons
         const uint64_t pol_first = policy_evict_first(), pol_last = policy_evict_last();
         int stage = 0;
         uint32_t phase = 0;
-        // L2 prefetch cursor over the first pass of each unit, G_PF K blocks ahead of the loads
-        int pi = 0, pkb = 0;
-        auto prefetch_next = [&]() {
-            while (pi < my_n && entry(pi).x == 0) ++pi;
-            if (pi >= my_n) return;
-            const int pu = blockIdx.x + pi * gridDim.x;
-            const int pe = pu / a.nfb, pfb = pu - pe * a.nfb;
-            const int prow = pe * a.a_rows_pe + pfb * a.a_fb_stride;
-            tma_prefetch_2d(&wmap, pkb * 64, prow);
-            tma_prefetch_2d(&wmap, pkb * 64, prow + a.a_sub1);
-            if (++pkb == a.kblocks) { pkb = 0; ++pi; }
-        };
-        for (int q = 0; q < G_PF; ++q) prefetch_next();
         for (int i = 0; i < my_n; ++i) {
             const int u = blockIdx.x + i * gridDim.x;
             const int e = u / a.nfb, fb = u - e * a.nfb;
@@ -797,7 +777,6 @@ __global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_cons
                 // the weight tile is streamed once: keep it in L2 only for a following pass
                 const uint64_t pol = c0 + chunk < n_e ? pol_last : pol_first;
                 for (int kb = 0; kb < a.kblocks; ++kb) {
-                    if (c0 == 0) prefetch_next();
                     if (!mbar_wait(&a_empty[stage], phase ^ 1, abort_flag)) goto done;
                     mbar_expect_tx(&a_full[stage], Cfg::A_BYTES);
                     const uint32_t sa = su32(sA + stage * Cfg::A_BYTES);
