@@ -98,6 +98,13 @@ int make_layout(const slmoe_config *c, Layout *L) {
     L->pub.status = take(16);
     L->wr_split = c->dtype == SLMOE_BF16 ? take(3 * E * c->d * 2) : 0;
     L->counters = take(16 * 4);
+    if (c->dtype == SLMOE_BF16) {
+        // work items: nfb feature blocks x (one pass per expert + one per full pass of tokens)
+        const size_t Tk = T * k;
+        const size_t nfb1 = (c->I + 127) / 128, nfb2 = (c->d_latent + 255) / 256;
+        L->items1 = take(nfb1 * (E + (Tk + 255) / 256) * 16);
+        L->items2 = take(nfb2 * (E + (Tk + 127) / 128) * 16);
+    }
     L->pub.total = off;
     return SLMOE_OK;
 }
@@ -409,6 +416,8 @@ int slmoe_forward(const slmoe_config *cfg, const void *x, const slmoe_weights *w
     tf.slot_pos = R.slot_pos;
     tf.status = stat;
     tf.counters = R.counters;
+    tf.items1 = reinterpret_cast<int4 *>(ws + L.items1);
+    tf.items2 = reinterpret_cast<int4 *>(ws + L.items2);
     // the down-projection and the shared experts' gate|up need only x: fork them onto the
     // auxiliary stream, route on the caller's stream meanwhile, join before the routed experts
     // (the routing kernels are launched first so that they take the SMs first; the

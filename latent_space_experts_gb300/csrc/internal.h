@@ -24,6 +24,7 @@ struct Layout {
     size_t chunk_counts;   // int32 [nchunks, E]: per-chunk expert counts, then bases
     size_t wr_split;       // bf16 [3, E, d]: router weight split hi / mid / lo
     size_t counters;       // int32 [16]: tile counters of the dynamically scheduled kernels
+    size_t items1, items2; // int4 work lists of the routed-expert GEMMs (bf16 type)
     size_t nchunks;
 };
 int make_layout(const slmoe_config *cfg, Layout *L);

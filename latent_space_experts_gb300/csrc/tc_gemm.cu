@@ -628,20 +628,22 @@ done:
 }
 
 // ---------------------------------------------------------------- grouped (routed experts)
-// Work unit = (expert e, feature block fb).  NSUB weight sub-tiles of 128 rows (the MMA's M)
-// stream from HBM through an A ring of 128 KB; the expert's token rows (N <= 256 per pass,
-// rounded to 16) are gathered by cp.async from L2 into a 3-deep B ring; each gather thread
-// signals a stage with cp.async.mbarrier.arrive.noinc (fires when its copies land) and never
-// waits on its own copies, and the MMA thread fences the generic-proxy writes to the async
-// proxy after its wait, before tcgen05.mma reads them.  NSUB = 2 pairs the
-// gate rows fb*128.. with the up rows I + fb*128.. for the fused SiTU-GLU, or two blocks of
-// 128 output features (expert down).  While a unit's epilogue drains TMEM, the weight ring
-// keeps streaming the next unit.  (NSUB = 1 would keep two TMEM accumulators instead.)
-// Each CTA stages its (count, offset) pairs in shared memory at start.
+// A work item is (expert e, feature block fb, token pass): two weight sub-tiles of 128 rows
+// (the MMA's M) times the pass's tokens (N <= PASS, rounded to 16).  NSUB = 2 pairs the gate
+// rows fb*128.. with the up rows I + fb*128.. for the fused SiTU-GLU, or two blocks of 128
+// output features (expert down).  The weights stream from HBM through a 128 KB ring of TMA
+// loads; the pass's token rows are gathered from L2 by cp.async into a 3-deep ring, each
+// gather thread signalling a stage with cp.async.mbarrier.arrive.noinc (the MMA thread fences
+// the generic-proxy writes to the async proxy after its wait).  Items come from a list built
+// on the device (expert-major, then feature block, then pass, so the passes of one weight tile
+// are adjacent and the CTAs that take them together share it through L2) and are handed out
+// dynamically through a global counter, so the heavy skew of expert loads cannot leave one
+// CTA with all the hot experts.  With DBUF, passes hold <= 128 tokens and alternate between
+// two TMEM accumulator sets so that an item's epilogue overlaps the next item's MMAs.
 constexpr int G_NMAX = 256;
 constexpr int G_THREADS = 320;                    // TMA, MMA, 4 epilogue, 4 gather warps
 constexpr int G_GATHER_THREADS = 128;
-constexpr int G_LIST = 192;                       // units listed in shared memory per CTA
+constexpr int G_TQ = 4;                           // item queue slots
 
 template <bool DBUF>
 struct GCfg {
@@ -650,29 +652,21 @@ struct GCfg {
     static constexpr int A_STAGES = (128 * 1024) / A_BYTES;
     static constexpr int B_BYTES = G_NMAX * 128;
     static constexpr int B_STAGES = 3;
-    // DBUF: an expert's tokens go in balanced passes of <= 128, alternating between two TMEM
-    // accumulator sets (sub-tile 1 at column +128), so a pass's epilogue overlaps the next
-    // pass's MMAs.  Otherwise passes of <= 256 tokens share one set (sub-tile 1 at +256).
     static constexpr int NBUF = DBUF ? 2 : 1;
     static constexpr int PASS = DBUF ? 128 : G_NMAX;
     static constexpr int SUB1_COL = DBUF ? 128 : 256;
-    static constexpr int SMEM = A_STAGES * A_BYTES + B_STAGES * B_BYTES + G_LIST * 8 + 1024 + 256;
+    static constexpr int SMEM = A_STAGES * A_BYTES + B_STAGES * B_BYTES + 1024 + 512;
 };
 
-// Token passes of an expert with n tokens: npass passes of `chunk` tokens (the last shorter).
-template <int PASS>
-__device__ __forceinline__ int pass_chunk(int n) {
-    const int npass = (n + PASS - 1) / PASS;
-    return npass > 0 ? (n + npass - 1) / npass : 0;
-}
-
 struct GroupedArgs {
-    int E, kblocks, nfb;
+    int kblocks;
     int a_rows_pe;        // rows of the weight view per expert
-    int a_sub1;           // row offset of sub-tile 1 inside a feature block (NSUB = 2)
+    int a_sub1;           // row offset of sub-tile 1 inside a feature block
     int a_fb_stride;      // rows between feature blocks
-    const int32_t *counts, *offsets;
-    const int32_t *b_index;               // nullable: token row = b_index[off + r]
+    const int4 *items;    // {e, fb | multi_pass << 16, first row in perm order, tokens}
+    const int *n_items;
+    int *counter;         // zeroed item counter
+    const int32_t *b_index;               // nullable: token row = b_index[row]
     const __nv_bfloat16 *b_src;
     long long b_ld;
     int b_K;
@@ -708,18 +702,70 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
     return p;
 }
 
+// Work lists of both routed-expert GEMMs in one block: per expert ceil(n_e / cap) passes of
+// balanced size (0 when n_e = 0) times nfb feature blocks, exclusive-scanned into bases.
+__global__ void __launch_bounds__(1024)
+worklist_kernel(const int32_t *__restrict__ counts, const int32_t *__restrict__ offsets, int E,
+                int nfb1, int cap1, int4 *__restrict__ items1, int nfb2, int cap2,
+                int4 *__restrict__ items2, int *__restrict__ n_items) {
+    __shared__ int wsum[2][32];
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int per = (E + blockDim.x - 1) / blockDim.x;
+    const int e0 = tid * per;
+    int loc[2] = {0, 0};
+    for (int e = e0; e < e0 + per && e < E; ++e) {
+        const int n = counts[e];
+        loc[0] += nfb1 * ((n + cap1 - 1) / cap1);
+        loc[1] += nfb2 * ((n + cap2 - 1) / cap2);
+    }
+    int incl[2] = {loc[0], loc[1]};
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+        for (int l = 0; l < 2; ++l) {
+            const int v = __shfl_up_sync(0xffffffffu, incl[l], o);
+            if (lane >= o) incl[l] += v;
+        }
+    }
+    if (lane == 31) { wsum[0][w] = incl[0]; wsum[1][w] = incl[1]; }
+    __syncthreads();
+    int base[2] = {0, 0};
+    for (int i = 0; i < w; ++i) { base[0] += wsum[0][i]; base[1] += wsum[1][i]; }
+    base[0] += incl[0] - loc[0];
+    base[1] += incl[1] - loc[1];
+    if (tid == blockDim.x - 1) { n_items[0] = base[0] + loc[0]; n_items[1] = base[1] + loc[1]; }
+    for (int e = e0; e < e0 + per && e < E; ++e) {
+        const int n = counts[e], off = offsets[e];
+        const int caps[2] = {cap1, cap2}, nfbs[2] = {nfb1, nfb2};
+        int4 *lists[2] = {items1, items2};
+#pragma unroll
+        for (int l = 0; l < 2; ++l) {
+            const int np = (n + caps[l] - 1) / caps[l];
+            if (np == 0) continue;
+            const int chunk = (n + np - 1) / np;
+            const int multi = np > 1 ? 1 : 0;
+            for (int fb = 0; fb < nfbs[l]; ++fb)
+                for (int p = 0; p < np; ++p) {
+                    const int c0 = p * chunk;
+                    lists[l][base[l]++] = make_int4(e, fb | (multi << 16), off + c0, min(chunk, n - c0));
+                }
+        }
+    }
+}
+
 template <int EPI, bool DBUF>
 __global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_constant__ CUtensorMap wmap,
                                                                const GroupedArgs a) {
     using Cfg = GCfg<DBUF>;
-    constexpr int NSUB = Cfg::NSUB, PASS = Cfg::PASS, SUB1 = Cfg::SUB1_COL;
-    constexpr int AST = Cfg::A_STAGES, BST = Cfg::B_STAGES, NBUF = Cfg::NBUF;
+    constexpr int AST = Cfg::A_STAGES, BST = Cfg::B_STAGES, NBUF = Cfg::NBUF, SUB1 = Cfg::SUB1_COL;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;
     uint8_t *sB = smem + AST * Cfg::A_BYTES;
-    int2 *list = reinterpret_cast<int2 *>(sB + BST * Cfg::B_BYTES);
-    uint64_t *a_full = reinterpret_cast<uint64_t *>(list + G_LIST);
+    int4 *q_items = reinterpret_cast<int4 *>(sB + BST * Cfg::B_BYTES);
+    uint64_t *q_full = reinterpret_cast<uint64_t *>(q_items + G_TQ);
+    uint64_t *q_empty = q_full + G_TQ;
+    uint64_t *a_full = q_empty + G_TQ;
     uint64_t *a_empty = a_full + AST;
     uint64_t *b_full = a_empty + AST;
     uint64_t *b_empty = b_full + BST;
@@ -729,9 +775,11 @@ __global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_cons
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int units = a.E * a.nfb;
-    const int my_n = blockIdx.x < units ? (units - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     if (threadIdx.x == 0) {
+        for (int s = 0; s < G_TQ; ++s) {
+            mbar_init(&q_full[s], 1);
+            mbar_init(&q_empty[s], 1 + 4 + 4);     // MMA thread, 4 epilogue warps, 4 gather warps
+        }
         for (int s = 0; s < AST; ++s) {
             mbar_init(&a_full[s], 1);
             mbar_init(&a_empty[s], 1);
@@ -747,139 +795,144 @@ __global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_cons
         *abort_flag = 0;
         fence_barrier_init();
     }
-    for (int i = threadIdx.x; i < my_n && i < G_LIST; i += blockDim.x) {
-        const int e = (blockIdx.x + i * gridDim.x) / a.nfb;
-        list[i] = make_int2(a.counts[e], a.offsets[e]);
-    }
     if (warp == 1) tmem_alloc(tmem_slot, 512);
     tc_before();
     __syncthreads();
     tc_after();
     const uint32_t tmem_base = *tmem_slot;
-    auto entry = [&](int i) -> int2 {
-        if (i < G_LIST) return list[i];
-        const int e = (blockIdx.x + i * gridDim.x) / a.nfb;
-        return make_int2(a.counts[e], a.offsets[e]);
+
+    // consumers take the next item from the queue; a negative token count ends the loop
+    auto pop = [&](int &qs, uint32_t &qp, int4 &it, bool warp_wide) -> bool {
+        if (!mbar_wait(&q_full[qs], qp, abort_flag)) return false;
+        it = q_items[qs];
+        if (warp_wide) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&q_empty[qs]);
+        } else {
+            mbar_arrive(&q_empty[qs]);
+        }
+        if (++qs == G_TQ) { qs = 0; qp ^= 1; }
+        return true;
     };
 
     if (warp == 0 && lane == 0) {
-        // ------------------------------------------------ weights by TMA (streamed once)
-        const uint64_t pol_first = policy_evict_first(), pol_last = policy_evict_last();
-        int stage = 0;
-        uint32_t phase = 0;
-        for (int i = 0; i < my_n; ++i) {
-            const int u = blockIdx.x + i * gridDim.x;
-            const int e = u / a.nfb, fb = u - e * a.nfb;
-            const int n_e = entry(i).x;
-            const int row0 = e * a.a_rows_pe + fb * a.a_fb_stride;
-            const int chunk = pass_chunk<PASS>(n_e);
-            for (int c0 = 0; c0 < n_e; c0 += chunk) {
-                // the weight tile is streamed once: keep it in L2 only for a following pass
-                const uint64_t pol = c0 + chunk < n_e ? pol_last : pol_first;
-                for (int kb = 0; kb < a.kblocks; ++kb) {
-                    if (!mbar_wait(&a_empty[stage], phase ^ 1, abort_flag)) goto done;
-                    mbar_expect_tx(&a_full[stage], Cfg::A_BYTES);
-                    const uint32_t sa = su32(sA + stage * Cfg::A_BYTES);
-                    tma_load_2d_hint(sa, &wmap, &a_full[stage], kb * 64, row0, pol);
-                    tma_load_2d_hint(sa + 128 * 128, &wmap, &a_full[stage], kb * 64, row0 + a.a_sub1, pol);
-                    if (++stage == AST) { stage = 0; phase ^= 1; }
+        // ------------------------------------------------ item fetch + weights by TMA
+        const uint64_t pol_first = policy_evict_first();
+        const int n_items = *a.n_items;
+        int stage = 0, qs = 0;
+        uint32_t phase = 0, qp = 0;
+        for (;;) {
+            const int idx = atomicAdd(a.counter, 1);
+            const int4 it = idx < n_items ? a.items[idx] : make_int4(0, 0, 0, -1);
+            if (!mbar_wait(&q_empty[qs], qp ^ 1, abort_flag)) goto done;
+            q_items[qs] = it;
+            mbar_arrive(&q_full[qs]);
+            if (++qs == G_TQ) { qs = 0; qp ^= 1; }
+            if (it.w < 0) break;
+            const int fb = it.y & 0xffff;
+            const bool multi = (it.y >> 16) != 0;
+            const int row0 = it.x * a.a_rows_pe + fb * a.a_fb_stride;
+            for (int kb = 0; kb < a.kblocks; ++kb) {
+                if (!mbar_wait(&a_empty[stage], phase ^ 1, abort_flag)) goto done;
+                mbar_expect_tx(&a_full[stage], Cfg::A_BYTES);
+                const uint32_t sa = su32(sA + stage * Cfg::A_BYTES);
+                if (multi) {       // other passes of this tile run alongside: normal L2 policy
+                    tma_load_2d(sa, &wmap, &a_full[stage], kb * 64, row0);
+                    tma_load_2d(sa + 128 * 128, &wmap, &a_full[stage], kb * 64, row0 + a.a_sub1);
+                } else {           // streamed once
+                    tma_load_2d_hint(sa, &wmap, &a_full[stage], kb * 64, row0, pol_first);
+                    tma_load_2d_hint(sa + 128 * 128, &wmap, &a_full[stage], kb * 64, row0 + a.a_sub1, pol_first);
                 }
+                if (++stage == AST) { stage = 0; phase ^= 1; }
             }
         }
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------ MMA issuer
-        int as = 0, bs = 0, buf = 0;
-        uint32_t aph = 0, bph = 0, tph = 0;
-        for (int i = 0; i < my_n; ++i) {
-            const int n_e = entry(i).x;
-            const int chunk = pass_chunk<PASS>(n_e);
-            for (int c0 = 0; c0 < n_e; c0 += chunk) {
-                const int N = min(chunk, n_e - c0);
-                const uint32_t idesc = idesc_bf16(128, (N + 15) & ~15);
-                if (!mbar_wait(&tempty[buf], tph ^ 1, abort_flag)) goto done;
+        int as = 0, bs = 0, buf = 0, qs = 0;
+        uint32_t aph = 0, bph = 0, tph = 0, qp = 0;
+        for (;;) {
+            int4 it;
+            if (!pop(qs, qp, it, false)) goto done;
+            if (it.w < 0) break;
+            const uint32_t idesc = idesc_bf16(128, (it.w + 15) & ~15);
+            if (!mbar_wait(&tempty[buf], tph ^ 1, abort_flag)) goto done;
+            tc_after();
+            const uint32_t d = tmem_base + buf * 256;
+            for (int kb = 0; kb < a.kblocks; ++kb) {
+                if (!mbar_wait(&a_full[as], aph, abort_flag)) goto done;
+                if (!mbar_wait(&b_full[bs], bph, abort_flag)) goto done;
+                fence_proxy_async();
                 tc_after();
-                const uint32_t d = tmem_base + buf * 256;
-                for (int kb = 0; kb < a.kblocks; ++kb) {
-                    if (!mbar_wait(&a_full[as], aph, abort_flag)) goto done;
-                    if (!mbar_wait(&b_full[bs], bph, abort_flag)) goto done;
-                    fence_proxy_async();
-                    tc_after();
-                    const uint32_t sa = su32(sA + as * Cfg::A_BYTES);
-                    const uint32_t sb = su32(sB + bs * Cfg::B_BYTES);
+                const uint32_t sa = su32(sA + as * Cfg::A_BYTES);
+                const uint32_t sb = su32(sB + bs * Cfg::B_BYTES);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-                        const uint64_t bd = sdesc(sb + kk * 32);
-                        umma(d, sdesc(sa + kk * 32), bd, idesc, acc);
-                        umma(d + SUB1, sdesc(sa + 128 * 128 + kk * 32), bd, idesc, acc);
-                    }
-                    umma_commit(&a_empty[as]);
-                    umma_commit(&b_empty[bs]);
-                    if (++as == AST) { as = 0; aph ^= 1; }
-                    if (++bs == BST) { bs = 0; bph ^= 1; }
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+                    const uint64_t bd = sdesc(sb + kk * 32);
+                    umma(d, sdesc(sa + kk * 32), bd, idesc, acc);
+                    umma(d + SUB1, sdesc(sa + 128 * 128 + kk * 32), bd, idesc, acc);
                 }
-                umma_commit(&tfull[buf]);
-                if (++buf == NBUF) { buf = 0; tph ^= 1; }
+                umma_commit(&a_empty[as]);
+                umma_commit(&b_empty[bs]);
+                if (++as == AST) { as = 0; aph ^= 1; }
+                if (++bs == BST) { bs = 0; bph ^= 1; }
             }
+            umma_commit(&tfull[buf]);
+            if (++buf == NBUF) { buf = 0; tph ^= 1; }
         }
     } else if (warp >= 2 && warp < 6) {
         // ------------------------------------------------ epilogue
         const int q = warp & 3;
         const int lf = q * 32 + lane;                 // feature inside a 128-row sub-tile
         const float ib1 = 1.0f / a.beta1, ib2 = 1.0f / a.beta2;
-        int buf = 0;
-        uint32_t tph = 0;
-        for (int i = 0; i < my_n; ++i) {
-            const int u = blockIdx.x + i * gridDim.x;
-            const int fb = u % a.nfb;
-            const int2 ent = entry(i);
-            const int n_e = ent.x, off = ent.y;
-            const int chunk = pass_chunk<PASS>(n_e);
-            for (int c0 = 0; c0 < n_e; c0 += chunk) {
-                const int N = min(chunk, n_e - c0);
-                const int Np = (N + 15) & ~15;
-                if (!mbar_wait(&tfull[buf], tph, abort_flag)) goto done;
-                tc_after();
-                const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + buf * 256;
-                // GLU: sub-tiles are the gate and up rows of h column fb*128 + lf.  Plain: the
-                // NSUB sub-tiles are output features fb*128*NSUB + lf + 128*sub.
-                const int f = (EPI == EPI_GLU ? fb * 128 : fb * 128 * NSUB) + lf;
-                const bool ok = f < a.out_cols;
-                const bool ok1 = f + 128 < a.out_cols;
-                __nv_bfloat16 *o = a.out + (long long)(off + c0) * a.out_ld + f;
-                for (int c = 0; c < Np; c += 16) {
-                    if (EPI == EPI_GLU) {
-                        uint32_t g[16], v[16];
-                        TMEM_LD16(tb + c, g);
-                        TMEM_LD16(tb + SUB1 + c, v);
-                        tmem_wait_ld();
-                        if (ok) {
+        int buf = 0, qs = 0;
+        uint32_t tph = 0, qp = 0;
+        for (;;) {
+            int4 it;
+            if (!pop(qs, qp, it, true)) goto done;
+            if (it.w < 0) break;
+            const int fb = it.y & 0xffff, N = it.w, Np = (N + 15) & ~15;
+            if (!mbar_wait(&tfull[buf], tph, abort_flag)) goto done;
+            tc_after();
+            const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + buf * 256;
+            // GLU: the sub-tiles are the gate and up rows of h column fb*128 + lf.  Plain: they
+            // are output features fb*256 + lf and fb*256 + 128 + lf.
+            const int f = (EPI == EPI_GLU ? fb * 128 : fb * 256) + lf;
+            const bool ok = f < a.out_cols;
+            const bool ok1 = f + 128 < a.out_cols;
+            __nv_bfloat16 *o = a.out + (long long)it.z * a.out_ld + f;
+            for (int c = 0; c < Np; c += 16) {
+                if (EPI == EPI_GLU) {
+                    uint32_t g[16], v[16];
+                    TMEM_LD16(tb + c, g);
+                    TMEM_LD16(tb + SUB1 + c, v);
+                    tmem_wait_ld();
+                    if (ok) {
 #pragma unroll
-                            for (int j = 0; j < 16; ++j)
-                                if (c + j < N)
-                                    o[(long long)(c + j) * a.out_ld] = __float2bfloat16_rn(situ_glu_fast(
-                                        __uint_as_float(g[j]), __uint_as_float(v[j]), ib1, a.beta1, ib2, a.beta2));
-                        }
-                    } else {
-                        uint32_t r0[16], r1[16];
-                        TMEM_LD16(tb + c, r0);
-                        TMEM_LD16(tb + SUB1 + c, r1);
-                        tmem_wait_ld();
+                        for (int j = 0; j < 16; ++j)
+                            if (c + j < N)
+                                o[(long long)(c + j) * a.out_ld] = __float2bfloat16_rn(situ_glu_fast(
+                                    __uint_as_float(g[j]), __uint_as_float(v[j]), ib1, a.beta1, ib2, a.beta2));
+                    }
+                } else {
+                    uint32_t r0[16], r1[16];
+                    TMEM_LD16(tb + c, r0);
+                    TMEM_LD16(tb + SUB1 + c, r1);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            if (c + j < N) {
-                                __nv_bfloat16 *orow = o + (long long)(c + j) * a.out_ld;
-                                if (ok) orow[0] = __float2bfloat16_rn(__uint_as_float(r0[j]));
-                                if (ok1) orow[128] = __float2bfloat16_rn(__uint_as_float(r1[j]));
-                            }
+                    for (int j = 0; j < 16; ++j) {
+                        if (c + j < N) {
+                            __nv_bfloat16 *orow = o + (long long)(c + j) * a.out_ld;
+                            if (ok) orow[0] = __float2bfloat16_rn(__uint_as_float(r0[j]));
+                            if (ok1) orow[128] = __float2bfloat16_rn(__uint_as_float(r1[j]));
                         }
                     }
                 }
-                tc_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[buf]);
-                if (++buf == NBUF) { buf = 0; tph ^= 1; }
             }
+            tc_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[buf]);
+            if (++buf == NBUF) { buf = 0; tph ^= 1; }
         }
     } else if (warp >= 6) {
         // ------------------------------------------------ token-row gather (cp.async, kept in L2)
@@ -887,41 +940,41 @@ __global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_cons
         const int gt = threadIdx.x - 6 * 32;          // 0..127
         const int ch = gt & 7;                         // 16-byte chunk of the 128-byte row
         const int rsub = gt >> 3;                      // rows rsub, rsub + 16, ...
-        int stage = 0;
-        uint32_t phase = 0;
-        for (int i = 0; i < my_n; ++i) {
-            const int2 ent = entry(i);
-            const int n_e = ent.x, off = ent.y;
-            const int chunk = pass_chunk<PASS>(n_e);
-            for (int c0 = 0; c0 < n_e; c0 += chunk) {
-                const int N = min(chunk, n_e - c0);
-                const int Np = (N + 15) & ~15;
-                const __nv_bfloat16 *src[G_NMAX / 16];
+        int stage = 0, qs = 0;
+        uint32_t phase = 0, qp = 0;
+        for (;;) {
+            int4 it;
+            if (!pop(qs, qp, it, true)) {
+                cp_async_wait<0>();
+                goto done;
+            }
+            if (it.w < 0) break;
+            const int N = it.w, Np = (N + 15) & ~15;
+            const __nv_bfloat16 *src[G_NMAX / 16];
+#pragma unroll
+            for (int j = 0; j < G_NMAX / 16; ++j) {
+                const int r = rsub + 16 * j;
+                long long row = 0;
+                if (r < N) row = a.b_index ? a.b_index[it.z + r] : (long long)(it.z + r);
+                src[j] = a.b_src + row * a.b_ld + ch * 8;
+            }
+            for (int kb = 0; kb < a.kblocks; ++kb) {
+                if (!mbar_wait(&b_empty[stage], phase ^ 1, abort_flag)) {
+                    cp_async_wait<0>();
+                    goto done;
+                }
+                const uint32_t sb = su32(sB + stage * Cfg::B_BYTES);
+                const bool kok = kb * 64 + ch * 8 < a.b_K;
 #pragma unroll
                 for (int j = 0; j < G_NMAX / 16; ++j) {
                     const int r = rsub + 16 * j;
-                    long long row = 0;
-                    if (r < N) row = a.b_index ? a.b_index[off + c0 + r] : (long long)(off + c0 + r);
-                    src[j] = a.b_src + row * a.b_ld + ch * 8;
-                }
-                for (int kb = 0; kb < a.kblocks; ++kb) {
-                    if (!mbar_wait(&b_empty[stage], phase ^ 1, abort_flag)) {
-                        cp_async_wait<0>();
-                        goto done;
+                    if (r < Np) {
+                        const uint32_t dst = sb + r * 128 + ((ch ^ (r & 7)) << 4);
+                        cp_async16_hint(dst, src[j] + kb * 64, (r < N && kok) ? 16u : 0u, pol);
                     }
-                    const uint32_t sb = su32(sB + stage * Cfg::B_BYTES);
-                    const bool kok = kb * 64 + ch * 8 < a.b_K;
-#pragma unroll
-                    for (int j = 0; j < G_NMAX / 16; ++j) {
-                        const int r = rsub + 16 * j;
-                        if (r < Np) {
-                            const uint32_t dst = sb + r * 128 + ((ch ^ (r & 7)) << 4);
-                            cp_async16_hint(dst, src[j] + kb * 64, (r < N && kok) ? 16u : 0u, pol);
-                        }
-                    }
-                    cp_async_arrive_noinc(&b_full[stage]);
-                    if (++stage == BST) { stage = 0; phase ^= 1; }
                 }
+                cp_async_arrive_noinc(&b_full[stage]);
+                if (++stage == BST) { stage = 0; phase ^= 1; }
             }
         }
         cp_async_wait<0>();
@@ -1013,11 +1066,7 @@ int launch_grouped(const CUtensorMap &wmap, const GroupedArgs &a, cudaStream_t s
     auto kern = grouped_kernel<EPI, DBUF>;
     int rc = set_smem(kern, GCfg<DBUF>::SMEM);
     if (rc) return rc;
-    const int units = a.E * a.nfb;
-    const int sms = sm_count();
-    const int grid = units < sms ? units : sms;
-    if (grid == 0) return SLMOE_OK;
-    kern<<<grid, G_THREADS, GCfg<DBUF>::SMEM, st>>>(wmap, a);
+    kern<<<sm_count(), G_THREADS, GCfg<DBUF>::SMEM, st>>>(wmap, a);
     return check_launch("grouped_kernel");
 }
 
@@ -1097,13 +1146,19 @@ int tc_forward_back(const slmoe_config *c, const slmoe_weights *w, const TcForwa
     int rc;
     using bf = __nv_bfloat16;
 
+    // work lists of both routed-expert GEMMs (device-built from the expert counts)
+    const int nfb1 = (I + 127) / 128, nfb2 = (dl + 255) / 256;
+    worklist_kernel<<<1, 1024, 0, st>>>(f.counts, f.offsets, E, nfb1, G_NMAX, f.items1, nfb2,
+                                        GCfg<true>::PASS, f.items2, f.counters + 8);
+    if ((rc = check_launch("worklist"))) return rc;
     {   // routed experts, gate|up + SiTU-GLU: h[perm row] = GLU(W13[e] x_lat[token])
         CUtensorMap wm;
         if ((rc = make_map(&wm, w->W13, (long long)E * 2 * I, dl, dl, 128))) return rc;
         GroupedArgs a = {};
-        a.E = E; a.kblocks = (dl + 63) / 64; a.nfb = (I + 127) / 128;
+        a.kblocks = (dl + 63) / 64;
         a.a_rows_pe = 2 * I; a.a_sub1 = I; a.a_fb_stride = 128;
-        a.counts = f.counts; a.offsets = f.offsets; a.b_index = f.perm;
+        a.items = f.items1; a.n_items = f.counters + 8; a.counter = f.counters + 6;
+        a.b_index = f.perm;
         a.b_src = static_cast<const bf *>(f.x_lat); a.b_ld = dl; a.b_K = dl;
         a.out = static_cast<bf *>(f.h); a.out_ld = I; a.out_cols = I;
         a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
@@ -1114,9 +1169,10 @@ int tc_forward_back(const slmoe_config *c, const slmoe_weights *w, const TcForwa
         CUtensorMap wm;
         if ((rc = make_map(&wm, w->W2, (long long)E * dl, I, I, 128))) return rc;
         GroupedArgs a = {};
-        a.E = E; a.kblocks = (I + 63) / 64; a.nfb = (dl + 255) / 256;
+        a.kblocks = (I + 63) / 64;
         a.a_rows_pe = dl; a.a_sub1 = 128; a.a_fb_stride = 256;
-        a.counts = f.counts; a.offsets = f.offsets; a.b_index = nullptr;
+        a.items = f.items2; a.n_items = f.counters + 9; a.counter = f.counters + 7;
+        a.b_index = nullptr;
         a.b_src = static_cast<const bf *>(f.h); a.b_ld = I; a.b_K = I;
         a.out = static_cast<bf *>(f.y_e); a.out_ld = dl; a.out_cols = dl;
         a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;

@@ -12,7 +12,9 @@ struct TcForward {
     const float *topk_w;
     const int32_t *counts, *offsets, *perm, *slot_pos;
     int32_t *status;
-    int *counters;                      // zeroed tile counters: [1] down, [2..4] shared, [5] up
+    int *counters;    // zeroed: tile counters [1] down, [2..4] shared, [5] up; item counters
+                      // [6] expert gate|up, [7] expert down; item counts [8], [9]
+    int4 *items1, *items2;              // work lists of the two routed-expert GEMMs
 };
 
 // Router scores s = sigmoid(x W_r^T + mu) with fp32-faithful logits: W_r is split into three
