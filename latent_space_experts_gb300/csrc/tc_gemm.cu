@@ -648,14 +648,15 @@ constexpr int G_TQ = 4;                           // item queue slots
 template <bool DBUF>
 struct GCfg {
     static constexpr int NSUB = 2;
+    static constexpr int PASS = DBUF ? 128 : G_NMAX;     // tokens per pass
     static constexpr int A_BYTES = NSUB * 128 * 128;
-    static constexpr int A_STAGES = (128 * 1024) / A_BYTES;
-    static constexpr int B_BYTES = G_NMAX * 128;
-    static constexpr int B_STAGES = 3;
+    static constexpr int A_STAGES = DBUF ? 5 : 4;         // 160 KB / 128 KB of weights in flight
+    static constexpr int B_BYTES = PASS * 128;
+    static constexpr int B_STAGES = DBUF ? 4 : 3;
     static constexpr int NBUF = DBUF ? 2 : 1;
-    static constexpr int PASS = DBUF ? 128 : G_NMAX;
     static constexpr int SUB1_COL = DBUF ? 128 : 256;
     static constexpr int SMEM = A_STAGES * A_BYTES + B_STAGES * B_BYTES + 1024 + 512;
+    static_assert(SMEM <= 232448, "shared memory");
 };
 
 struct GroupedArgs {
@@ -950,9 +951,10 @@ __global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_cons
             }
             if (it.w < 0) break;
             const int N = it.w, Np = (N + 15) & ~15;
-            const __nv_bfloat16 *src[G_NMAX / 16];
+            constexpr int RJ = Cfg::PASS / 16;
+            const __nv_bfloat16 *src[RJ];
 #pragma unroll
-            for (int j = 0; j < G_NMAX / 16; ++j) {
+            for (int j = 0; j < RJ; ++j) {
                 const int r = rsub + 16 * j;
                 long long row = 0;
                 if (r < N) row = a.b_index ? a.b_index[it.z + r] : (long long)(it.z + r);
@@ -966,7 +968,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_cons
                 const uint32_t sb = su32(sB + stage * Cfg::B_BYTES);
                 const bool kok = kb * 64 + ch * 8 < a.b_K;
 #pragma unroll
-                for (int j = 0; j < G_NMAX / 16; ++j) {
+                for (int j = 0; j < RJ; ++j) {
                     const int r = rsub + 16 * j;
                     if (r < Np) {
                         const uint32_t dst = sb + r * 128 + ((ch ^ (r & 7)) << 4);
@@ -1148,7 +1150,7 @@ int tc_forward_back(const slmoe_config *c, const slmoe_weights *w, const TcForwa
 
     // work lists of both routed-expert GEMMs (device-built from the expert counts)
     const int nfb1 = (I + 127) / 128, nfb2 = (dl + 255) / 256;
-    worklist_kernel<<<1, 1024, 0, st>>>(f.counts, f.offsets, E, nfb1, G_NMAX, f.items1, nfb2,
+    worklist_kernel<<<1, 1024, 0, st>>>(f.counts, f.offsets, E, nfb1, GCfg<true>::PASS, f.items1, nfb2,
                                         GCfg<true>::PASS, f.items2, f.counters + 8);
     if ((rc = check_launch("worklist"))) return rc;
     {   // routed experts, gate|up + SiTU-GLU: h[perm row] = GLU(W13[e] x_lat[token])
@@ -1162,7 +1164,7 @@ int tc_forward_back(const slmoe_config *c, const slmoe_weights *w, const TcForwa
         a.b_src = static_cast<const bf *>(f.x_lat); a.b_ld = dl; a.b_K = dl;
         a.out = static_cast<bf *>(f.h); a.out_ld = I; a.out_cols = I;
         a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
-        if ((rc = launch_grouped<EPI_GLU, false>(wm, a, st))) return rc;
+        if ((rc = launch_grouped<EPI_GLU, true>(wm, a, st))) return rc;
     }
     stage_event(4, st);
     {   // routed experts, down: y_e[row] = W2[e] h[row]
