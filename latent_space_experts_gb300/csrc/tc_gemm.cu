@@ -1150,7 +1150,7 @@ int tc_forward_back(const slmoe_config *c, const slmoe_weights *w, const TcForwa
 
     // work lists of both routed-expert GEMMs (device-built from the expert counts)
     const int nfb1 = (I + 127) / 128, nfb2 = (dl + 255) / 256;
-    worklist_kernel<<<1, 1024, 0, st>>>(f.counts, f.offsets, E, nfb1, GCfg<true>::PASS, f.items1, nfb2,
+    worklist_kernel<<<1, 1024, 0, st>>>(f.counts, f.offsets, E, nfb1, GCfg<false>::PASS, f.items1, nfb2,
                                         GCfg<true>::PASS, f.items2, f.counters + 8);
     if ((rc = check_launch("worklist"))) return rc;
     {   // routed experts, gate|up + SiTU-GLU: h[perm row] = GLU(W13[e] x_lat[token])
@@ -1164,7 +1164,7 @@ int tc_forward_back(const slmoe_config *c, const slmoe_weights *w, const TcForwa
         a.b_src = static_cast<const bf *>(f.x_lat); a.b_ld = dl; a.b_K = dl;
         a.out = static_cast<bf *>(f.h); a.out_ld = I; a.out_cols = I;
         a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
-        if ((rc = launch_grouped<EPI_GLU, true>(wm, a, st))) return rc;
+        if ((rc = launch_grouped<EPI_GLU, false>(wm, a, st))) return rc;
     }
     stage_event(4, st);
     {   // routed experts, down: y_e[row] = W2[e] h[row]
