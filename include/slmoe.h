@@ -17,7 +17,8 @@
  *     call returns before its kernels finish ([SLMoE] 训练基础设施: no host sync on the
  *     critical path).  Calls that share output buffers must be ordered on one stream.
  *   - The library allocates no memory.  Scratch lives in a caller-provided workspace of at
- *     least slmoe_workspace_size() bytes, 256-byte aligned.  On the bf16 type,
+ *     least slmoe_workspace_size() bytes, 256-byte aligned (slmoe_route_noalloc instead
+ *     uses a fixed device array inside the library).  On the bf16 type,
  *     slmoe_forward creates, on its first call on a device, one auxiliary CUDA stream (lowest
  *     priority) and two events, kept until the process exits: it forks the down-projection
  *     and the shared experts' gate|up onto that stream, routes on the caller's stream
@@ -156,6 +157,51 @@ SLMOE_API int slmoe_route(const slmoe_config *cfg, const void *x, const float *W
                 int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *slot_pos,
                 uint32_t *hist, int32_t *status, void *workspace, size_t workspace_bytes,
                 void *stream);
+
+/*
+ * slmoe_route_noalloc - slmoe_route without a workspace argument: the same kernels, the same
+ * arithmetic and the same outputs, with the call's scratch taken from a fixed device array
+ * inside this library instead of from the caller.  The pages describe no such call: it is
+ * a convenience of this library for callers that cannot hand out device memory per call,
+ * for instance a serving loop whose allocator has already given all of the device's memory
+ * to weights and caches, or a latency-critical loop that must not call cudaMalloc or
+ * cudaFree (cudaFree waits for the whole device).  The call makes no allocation call of any
+ * kind (no cudaMalloc, cudaMallocAsync, cudaFree, nor a library routine that allocates); the
+ * array itself is device memory that the CUDA runtime reserves together with this library's
+ * device code on each device where that code is loaded.
+ *
+ * Scratch limit: SLMOE_ROUTE_NOALLOC_SCRATCH_BYTES (48 MiB) per device.  A call needs
+ *   16 * 4 bytes of tile counters + ceil(T/16) * E * 4 bytes of per-chunk expert counts
+ *   + 3 * E * d * 2 bytes of split router weights (bf16 type only)
+ *   + T * E * 4 bytes of scores when scores is NULL,
+ * each piece rounded up to 256 bytes.  With E = 896 and d = 7168 (bf16) that is 36.8 MiB
+ * plus about 0.2 KiB per token with a caller scores buffer, 3.7 KiB per token without one.
+ * A call that needs more returns SLMOE_ENOSPACE before anything is launched, and
+ * slmoe_last_error() gives the bytes it needed.
+ *
+ * Zeroing: nothing in the scratch has to be zeroed by the caller.  The tile counters, the
+ * only part that must start at zero, are cleared by each call on its own stream before its
+ * first kernel; everything else in the scratch is written before it is read.  hist (when
+ * given) accumulates as in slmoe_route, so the caller zeroes it.
+ *
+ * Set-up: the first call on each device looks up the scratch's device address with that
+ * device current (cudaGetSymbolAddress) and keeps it; make that first call before any
+ * stream capture.  Later calls on the device reuse the address.
+ *
+ * Overlap: there is one scratch per device, shared by every call on that device.  Two calls
+ * that can run at the same time on one device (different streams not ordered by events, or
+ * different host threads) race on it and give wrong results; order them on one stream or
+ * with events.  When scores is NULL the scores are kept only in the scratch, and the next
+ * call on the device overwrites them.
+ *
+ * Arguments and errors: as slmoe_route, without workspace and workspace_bytes; plus
+ *   SLMOE_ENOSPACE when the call needs more scratch than the limit above.
+ */
+#define SLMOE_ROUTE_NOALLOC_SCRATCH_BYTES (48u * 1024u * 1024u)
+SLMOE_API int slmoe_route_noalloc(const slmoe_config *cfg, const void *x, const float *W_r,
+                const float *bias, const float *logit_offset, int32_t *topk_idx, float *topk_w,
+                float *scores, int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *slot_pos,
+                uint32_t *hist, int32_t *status, void *stream);
 
 /*
  * slmoe_qb_histogram - add per-expert score histograms of one micro-batch.

@@ -14,6 +14,7 @@ from . import _build
 
 __all__ = ["SlmoeError", "Config", "Weights", "WorkspaceLayout", "load", "build", "config",
            "weights", "slmoe_workspace_size", "slmoe_workspace_layout_get", "slmoe_route",
+           "slmoe_route_noalloc",
            "slmoe_qb_histogram", "slmoe_qb_update", "slmoe_forward", "slmoe_device_sm_count",
            "workspace_views", "slmoe_last_error", "slmoe_set_stage_events", "slmoe_launch_count", "F32", "BF16", "LIB_PATH"]
 
@@ -69,6 +70,7 @@ def load():
         "slmoe_last_error": (ctypes.c_char_p, []),
         "slmoe_device_sm_count": (ctypes.c_int, []),
         "slmoe_route": (ctypes.c_int, [CP, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
+        "slmoe_route_noalloc": (ctypes.c_int, [CP, P, P, P, P, P, P, P, P, P, P, P, P, P, P]),
         "slmoe_qb_histogram": (ctypes.c_int, [P, I64, I32, I32, P, P, P]),
         "slmoe_qb_update": (ctypes.c_int, [P, I32, I32, I32, P, P, P]),
         "slmoe_forward": (ctypes.c_int, [CP, P, WP, P, P, P, P, P, P, P, SZ, P]),
@@ -190,6 +192,17 @@ def slmoe_route(cfg, x, W_r, bias, logit_offset, topk_idx, topk_w, scores, count
                               _ptr(topk_idx), _ptr(topk_w), _ptr(scores), _ptr(counts), _ptr(offsets),
                               _ptr(perm), _ptr(slot_pos), _ptr(hist), _ptr(status), _ptr(workspace),
                               workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def slmoe_route_noalloc(cfg, x, W_r, bias, logit_offset, topk_idx, topk_w, scores, counts, offsets,
+                        perm, slot_pos, hist, status, stream=None):
+    """slmoe_route with the library's fixed per-device scratch instead of a workspace: for
+    callers that cannot hand out device memory per call.  Calls that may overlap on one
+    device race on that scratch; the first call on a device sets it up."""
+    _check(load().slmoe_route_noalloc(ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(bias),
+                                      _ptr(logit_offset), _ptr(topk_idx), _ptr(topk_w), _ptr(scores),
+                                      _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(slot_pos),
+                                      _ptr(hist), _ptr(status), _stream(stream)))
 
 
 def slmoe_qb_histogram(scores, T, E, nbins, hist, status=None, stream=None):

@@ -438,3 +438,99 @@ int slmoe_forward(const slmoe_config *cfg, const void *x, const slmoe_weights *w
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------
+// Routing with the library's own fixed scratch instead of a caller-supplied workspace.
+// The scratch is one file-scope device array; its device address is looked up once per
+// device (with that device current) and cached.  Same kernels and arithmetic as slmoe_route.
+
+namespace slmoe {
+
+static __device__ __align__(256) unsigned char g_route_scratch[SLMOE_ROUTE_NOALLOC_SCRATCH_BYTES];
+static char *g_route_scratch_ptr[MAX_DEVICES];
+static std::mutex g_route_scratch_mu;
+
+static int route_scratch(char **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES)
+        return fail(SLMOE_ECUDA, "no current device");
+    std::lock_guard<std::mutex> lock(g_route_scratch_mu);
+    if (!g_route_scratch_ptr[dev]) {
+        char *ptr = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress((void **)&ptr, g_route_scratch);
+        if (e != cudaSuccess || !ptr) {
+            cudaGetLastError();
+            return fail(SLMOE_ECUDA, "device address of the routing scratch: %s", cudaGetErrorString(e));
+        }
+        g_route_scratch_ptr[dev] = ptr;
+    }
+    *out = g_route_scratch_ptr[dev];
+    return SLMOE_OK;
+}
+
+// Offsets of what a routing call keeps in the scratch: the zeroed tile counters, the
+// per-chunk expert counts, the split router weights (bf16 type) and, when the caller passes
+// no scores buffer, the scores.  Returns the bytes needed.
+struct RouteScratch {
+    size_t counters, chunk_counts, wr_split, scores, total;
+};
+
+static RouteScratch route_scratch_layout(const slmoe_config *c, size_t nchunks, bool own_scores) {
+    RouteScratch s = {};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align_up(off + (bytes ? bytes : 1), 256);
+        return o;
+    };
+    s.counters = take(16 * sizeof(int));
+    s.chunk_counts = take(nchunks * (size_t)c->E * 4);
+    s.wr_split = c->dtype == SLMOE_BF16 ? take((size_t)3 * c->E * c->d * 2) : 0;
+    s.scores = own_scores ? take((size_t)c->T * c->E * 4) : 0;
+    s.total = off;
+    return s;
+}
+
+}  // namespace slmoe
+
+extern "C" int slmoe_route_noalloc(const slmoe_config *cfg, const void *x, const float *W_r,
+                                   const float *bias, const float *logit_offset, int32_t *topk_idx,
+                                   float *topk_w, float *scores, int32_t *counts, int32_t *offsets,
+                                   int32_t *perm, int32_t *slot_pos, uint32_t *hist, int32_t *status,
+                                   void *stream) {
+    g_err[0] = 0;
+    Layout L;
+    int rc = make_layout(cfg, &L);
+    if (rc) return rc;
+    REQ(counts, "counts");
+    REQ(offsets, "offsets");
+    if (cfg->T > 0) {
+        REQ(x, "x"); REQ(W_r, "W_r"); REQ(bias, "bias"); OPT(logit_offset, "logit_offset");
+        REQ(topk_idx, "topk_idx"); REQ(topk_w, "topk_w"); REQ(perm, "perm"); REQ(slot_pos, "slot_pos");
+        OPT(scores, "scores"); OPT(hist, "hist");
+    }
+    OPT(status, "status");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cfg->T == 0) {
+        if (cudaMemsetAsync(counts, 0, cfg->E * 4, st) != cudaSuccess ||
+            cudaMemsetAsync(offsets, 0, (cfg->E + 1) * 4, st) != cudaSuccess)
+            return check_launch("memset");
+        return SLMOE_OK;
+    }
+    const RouteScratch S = route_scratch_layout(cfg, L.nchunks, scores == nullptr);
+    if (S.total > (size_t)SLMOE_ROUTE_NOALLOC_SCRATCH_BYTES)
+        return fail(SLMOE_ENOSPACE,
+                    "this routing call needs %zu bytes of scratch, more than the fixed %zu bytes "
+                    "(pass a scores buffer, route fewer tokens per call, or use slmoe_route)",
+                    S.total, (size_t)SLMOE_ROUTE_NOALLOC_SCRATCH_BYTES);
+    char *scr = nullptr;
+    if ((rc = route_scratch(&scr))) return rc;
+    // route_impl reads the split router weights at ws + L.wr_split
+    L.wr_split = S.wr_split;
+    Routing R = {scores ? scores : reinterpret_cast<float *>(scr + S.scores), topk_idx, topk_w,
+                 counts, offsets, perm, slot_pos, reinterpret_cast<int32_t *>(scr + S.chunk_counts),
+                 reinterpret_cast<int *>(scr + S.counters)};
+    if (cudaMemsetAsync(R.counters, 0, 16 * sizeof(int), st) != cudaSuccess) return check_launch("memset");
+    stage_event(0, st);
+    return route_impl(cfg, L, scr, x, W_r, bias, logit_offset, R, hist, status, st);
+}
