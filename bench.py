@@ -4,21 +4,26 @@ One step = one slmoe_forward over one batch of the workload (router scores, bias
 permutation, QB histogram of the step's scores, latent down-projection, both routed-expert
 GEMMs with the fused SiTU-GLU, combine + RMSNorm, shared experts, up-projection) followed by
 the QB bias update (slmoe_qb_update).  Inputs and weights are resident in HBM when timing
-starts; weights (10.2 GB at the K3 shape) exceed the 126 MB L2, so no flush is needed.
+starts; weights (10.2 GB at the K3 shape) exceed the L2 (about 129 MB), so no flush is
+needed.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload k3_prefill|k3_decode|mid]
-                  [--impl ours|reference]
+                  [--impl ours|reference] [--skew] [--qb-only]
 
 Prints one JSON line (rank 0).  N > 1 runs one independent replica per GPU (weak scaling):
 the layer has no data-path exchange on one node in this design.  --impl reference times the
-fp64 oracle on the host cores on a bounded sample of the same workload.
+fp64 oracle on the host cores on a bounded sample of the same workload.  --qb-only runs just
+the QB engine measurement (histogram of 65536 x 896 scores + bias update), a small process
+for profiling that kernel.
 """
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -153,6 +158,43 @@ def oracle_sample(shp, inp_cpu, n_tok):
     return n_tok / dt, dt
 
 
+def oracle_tokens(shp, inp_cpu, target_s):
+    """Tokens per oracle sample so that one sample takes at most about target_s seconds.
+    Trials double the token count until one takes a quarter of the target; the count is then
+    scaled by target / trial time.  A sample's cost grows more slowly than its token count
+    (the dense weights are widened once per sample, and tokens share experts), so the
+    scaled sample does not overshoot."""
+    n = min(4, shp.T)
+    while True:
+        _, dt = oracle_sample(shp, inp_cpu, n)
+        if dt >= target_s / 4 or n >= min(shp.T, 1024):
+            break
+        n = min(2 * n, shp.T, 1024)
+    return max(1, min(shp.T, 1024, int(n * target_s / max(dt, 1e-6))))
+
+
+def profiled_traffic(stage):
+    """DRAM bytes per launch of a stage's kernel at the bench workload, as recorded in the
+    committed ncu summaries under profiles/ ("bench-traffic:" lines), used only while the
+    kernel's source file still has the SHA-256 recorded with the capture; else None."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    pat = re.compile(r"bench-traffic: (.+?) = (\d+) bytes per launch; source (\S+) sha256 ([0-9a-f]{64})")
+    for name in sorted(os.listdir(pdir)):
+        with open(os.path.join(pdir, name), errors="replace") as f:
+            for line in f:
+                m = pat.search(line)
+                if not m or m.group(1) != stage:
+                    continue
+                src = os.path.join(ROOT, m.group(3))
+                if not os.path.exists(src):
+                    continue
+                if hashlib.sha256(open(src, "rb").read()).hexdigest() == m.group(4):
+                    return int(m.group(2))
+    return None
+
+
 def cpu_cores():
     try:
         import threadpoolctl
@@ -176,9 +218,10 @@ def run_reference(args):
     inp = synthetic.layer_inputs(shp, seed=0, device=dev)
     inp_cpu = {k: (v.cpu() if v is not None else None) for k, v in inp.items()}
     del inp
-    n_tok = args.ref_tokens
-    for _ in range(args.warmup if args.warmup < 1 else 1):
-        oracle_sample(shp, inp_cpu, 1)
+    # each step is a bounded sample: the whole run (warm-up + timed) takes about ref_seconds
+    n_tok = args.ref_tokens or oracle_tokens(shp, inp_cpu, args.ref_seconds / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample(shp, inp_cpu, n_tok)
     t = []
     for _ in range(args.steps):
         _, dt = oracle_sample(shp, inp_cpu, n_tok)
@@ -194,9 +237,48 @@ def run_reference(args):
                        "I_shared": shp.I_shared, "sample_tokens_per_step": n_tok},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                              "sample": f"{n_tok} tokens of the {args.workload} batch per step (routing, "
-                                       f"experts, norm, shared experts; per-token cost is constant)"},
+                                       f"experts, norm, shared experts), fp64 numpy"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
+
+
+def qb_engine(hbm):
+    """QB engine on one GPU: histogram bandwidth over one 65536 x 896 fp32 micro-batch of
+    scores (235 MB, larger than L2) and the time of one bias update, CUDA events on the
+    launching stream after warm-up."""
+    import torch
+    import latent_space_experts_gb300 as lse
+    import synthetic
+    stream = torch.cuda.current_stream()
+    q = synthetic.QB
+    sc = synthetic.qb_scores(0, q, device="cuda")
+    qh = torch.zeros(q.E, q.nbins, dtype=torch.int32, device="cuda")
+    for _ in range(3):
+        lse.slmoe_qb_histogram(sc, q.T, q.E, q.nbins, qh)
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 50
+    g0.record(stream)
+    for _ in range(reps):
+        lse.slmoe_qb_histogram(sc, q.T, q.E, q.nbins, qh)
+    g1.record(stream)
+    torch.cuda.synchronize()
+    tq = g0.elapsed_time(g1) / reps * 1e-3
+    qbias = torch.empty(q.E, device="cuda")
+    for _ in range(3):
+        lse.slmoe_qb_update(qh, q.E, q.nbins, q.k, None, qbias)
+    g0.record(stream)
+    for _ in range(reps):
+        lse.slmoe_qb_update(qh, q.E, q.nbins, q.k, None, qbias)
+    g1.record(stream)
+    torch.cuda.synchronize()
+    tu = g0.elapsed_time(g1) / reps * 1e-3
+    qbytes = q.T * q.E * 4 + 2 * q.E * q.nbins * 4
+    return {"GB/s": round(qbytes / tq / 1e9, 1), "frac_of_hbm": round(qbytes / tq / 1e9 / hbm, 4),
+            "us_per_micro_batch": round(tq * 1e6, 2), "bytes": qbytes,
+            "update_us": round(tu * 1e6, 2),
+            "engine_ms": round((q.micro_batches * tq + tu) * 1e3, 4),
+            "note": "65536 x 896 fp32 scores per micro-batch (235 MB > L2); engine = 8 histograms + 1 update"}
 
 
 def main():
@@ -206,9 +288,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="k3_prefill", choices=["k3_prefill", "k3_decode", "mid", "k3_slice"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--ref-tokens", type=int, default=4)
-    ap.add_argument("--cpu-baseline-tokens", type=int, default=4)
+    ap.add_argument("--ref-tokens", type=int, default=None,
+                    help="oracle tokens per reference step (default: sized from --ref-seconds)")
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="about how long the whole reference run (warm-up + timed steps) takes")
+    ap.add_argument("--cpu-baseline-tokens", type=int, default=None,
+                    help="oracle tokens of the cpu_baseline sample (default: sized from --cpu-seconds)")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--qb-only", action="store_true", help="only the QB engine measurement")
     ap.add_argument("--skew", action="store_true", help="heavy skew (10%% hot experts)")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -222,6 +310,11 @@ def main():
     world, rank, local = dist_setup(args)
     lse.build()
     lse.load()
+    if args.qb_only:
+        if rank == 0:
+            pk, pk_kind = peaks()
+            print(json.dumps({"qb_histogram": qb_engine(pk["hbm_gbs"]), "peak_source": pk_kind}))
+        return
     shp = synthetic.LAYERS[args.workload]
     cfg = lse.config(shp)
     inp = synthetic.layer_inputs(shp, seed=rank, device="cuda", heavy_skew=args.skew)
@@ -312,7 +405,7 @@ def main():
         roof = {"bound": "tensor", "achieved": round(dm["flops"] / t_dom / 1e12, 1), "peak": tc,
                 "unit": "TFLOP/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    roof["traffic"] = None
+    roof["traffic"] = profiled_traffic(STAGES[dom]) if args.workload == "k3_prefill" else None
     roof["kernel"] = STAGES[dom]
     roof["peak_source"] = f"{pk_kind} ({'sustained bf16' if roof['bound'] == 'tensor' else 'hbm copy'})"
     t_layer = max(layer_flops / (tc * 1e12), layer_bytes / (hbm * 1e9))
@@ -339,44 +432,13 @@ def main():
     ms_e2e = max_over_ranks(f0.elapsed_time(f1), world) / n_e2e
 
     # ---------------- QB engine histogram bandwidth (65536 x 896 fp32 per micro-batch)
-    qb = None
-    if rank == 0:
-        q = synthetic.QB
-        sc = synthetic.qb_scores(0, q, device="cuda")
-        qh = torch.zeros(q.E, q.nbins, dtype=torch.int32, device="cuda")
-        for _ in range(3):
-            lse.slmoe_qb_histogram(sc, q.T, q.E, q.nbins, qh)
-        torch.cuda.synchronize()
-        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        reps = 50
-        g0.record(stream)
-        for _ in range(reps):
-            lse.slmoe_qb_histogram(sc, q.T, q.E, q.nbins, qh)
-        g1.record(stream)
-        torch.cuda.synchronize()
-        tq = g0.elapsed_time(g1) / reps * 1e-3
-        qbias = torch.empty(q.E, device="cuda")
-        for _ in range(3):
-            lse.slmoe_qb_update(qh, q.E, q.nbins, q.k, None, qbias)
-        g0.record(stream)
-        for _ in range(reps):
-            lse.slmoe_qb_update(qh, q.E, q.nbins, q.k, None, qbias)
-        g1.record(stream)
-        torch.cuda.synchronize()
-        tu = g0.elapsed_time(g1) / reps * 1e-3
-        qbytes = q.T * q.E * 4 + 2 * q.E * q.nbins * 4
-        qb = {"GB/s": round(qbytes / tq / 1e9, 1), "frac_of_hbm": round(qbytes / tq / 1e9 / hbm, 4),
-              "us_per_micro_batch": round(tq * 1e6, 2), "bytes": qbytes,
-              "update_us": round(tu * 1e6, 2),
-              "engine_ms": round((q.micro_batches * tq + tu) * 1e3, 4),
-              "note": "65536 x 896 fp32 scores per micro-batch (235 MB > L2); engine = 8 histograms + 1 update"}
-        del sc, qh
+    qb = qb_engine(hbm) if rank == 0 else None
 
     # ---------------- oracle on the host cores (bounded sample)
     cpu_base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         inp_cpu = {k: (v.cpu() if v is not None else None) for k, v in inp.items()}
-        n_tok = args.cpu_baseline_tokens
+        n_tok = args.cpu_baseline_tokens or oracle_tokens(shp, inp_cpu, args.cpu_seconds)
         v, dt = oracle_sample(shp, inp_cpu, n_tok)
         cpu_base = {"value": round(v, 3), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                     "sample": f"{n_tok} tokens of the {args.workload} batch, fp64 numpy ({dt:.1f} s)"}
