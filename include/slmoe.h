@@ -211,7 +211,8 @@ SLMOE_API int slmoe_route_noalloc(const slmoe_config *cfg, const void *x, const 
  *     bin = min(nbins-1, max(0, floor(fl32(scores[t*E+e] * nbins))))  (one fp32 multiply)
  *     hist[e*nbins + bin] += 1
  *   scores [T,E] fp32, row-major; hist [E,nbins] uint32, accumulated in place (the caller
- *   zeroes it before the first micro-batch).  T may be 0.  No workspace.
+ *   zeroes it before the first micro-batch).  0 <= T < 2^31 (so that no count of one call
+ *   can wrap); the running totals are checked against 2^32 - 1.  No workspace.
  * Errors: SLMOE_EINVAL on null pointers, E < 1, nbins < 1 or nbins > 1024.
  */
 SLMOE_API int slmoe_qb_histogram(const float *scores, int64_t T, int32_t E, int32_t nbins,

@@ -340,7 +340,7 @@ int slmoe_route(const slmoe_config *cfg, const void *x, const float *W_r, const 
 int slmoe_qb_histogram(const float *scores, int64_t T, int32_t E, int32_t nbins, uint32_t *hist,
                        int32_t *status, void *stream) {
     g_err[0] = 0;
-    if (T < 0) return fail(SLMOE_EINVAL, "T < 0");
+    if (T < 0 || T > INT32_MAX) return fail(SLMOE_EINVAL, "T outside [0, 2^31 - 1]");
     if (E < 1) return fail(SLMOE_EINVAL, "E < 1");
     if (nbins < 1 || nbins > 1024) return fail(SLMOE_EINVAL, "nbins outside [1, 1024]");
     if (!hist) return fail(SLMOE_EINVAL, "hist is NULL");

@@ -1,0 +1,87 @@
+// Inline-PTX wrappers shared by the library's TMA / mbarrier kernels (sm_103a): shared-memory
+// addresses, mbarrier set-up, arrivals and bounded waits, 2-D tensor loads and proxy fences.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+namespace slmoe {
+
+// Every mbarrier wait gives up after this long (%globaltimer, ns): the kernel then sets its
+// abort flag, every role leaves its loop and the launch reports status[2].
+constexpr uint64_t WAIT_LIMIT_NS = 4000000000ull;
+
+__device__ __forceinline__ uint32_t su32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t gtimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t n) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(n) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t addr, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for the phase of the given parity.  False = gave up (abort flag set, or set
+// by another role meanwhile).
+__device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, volatile int *abort_flag) {
+    const uint32_t a = su32(b);
+    if (mbar_try(a, parity)) return true;
+    const uint64_t t0 = gtimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try(a, parity)) return true;
+        if ((it & 255u) == 0) {
+            if (*abort_flag) return false;
+            if (gtimer() - t0 > WAIT_LIMIT_NS) {
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+// The same wait with its own time limit and no abort flag: used to drain copies still in
+// flight after an abort, so that nothing lands in shared memory after the block exits.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t *b, uint32_t parity) {
+    const uint32_t a = su32(b);
+    const uint64_t t0 = gtimer();
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try(a, parity)) return true;
+        if ((it & 255u) == 0 && gtimer() - t0 > WAIT_LIMIT_NS) return false;
+    }
+}
+// 2-D tiled TMA load of one box at (c0 = innermost, c1) into shared memory; completion is
+// counted in bytes on the mbarrier.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint64_t *bar,
+                                            int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(map), "r"(su32(bar)), "r"(c0), "r"(c1)
+        : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+}  // namespace slmoe

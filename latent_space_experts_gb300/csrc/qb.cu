@@ -7,13 +7,18 @@
 //
 // Histogram design.  scores [T, E] fp32 is streamed once from HBM.  The experts are cut
 // into slabs of 32 (one 128-byte line per row: lane = expert), and each slab is counted by
-// one thread-block cluster of P CTAs that split the tokens (P is chosen so that the
-// clusters fill the SMs).  Each CTA keeps 32-bit counters [bin][32 experts] in shared
-// memory, so the 32 lanes of an atomic always hit 32 distinct banks, and keeps 32 row
-// loads in flight per lane.  At the end the cluster adds its CTAs' counters through
-// distributed shared memory and each bin of global memory is read-modified-written by
-// exactly one thread: no global atomics and no partial histograms in HBM.
+// one thread-block cluster of P CTAs that split the tokens (P from the SMs' cluster
+// occupancy).  Each CTA keeps 32-bit counters [bin][32 experts] in shared memory, so the 32
+// lanes of an atomic always hit 32 distinct banks, plus one extra row that counts NaN
+// scores; every lane keeps 32 row loads in flight, and a score's counter row takes a few
+// full-rate FP32 / integer instructions (qb_bin).  At the end the cluster adds its CTAs'
+// counters through distributed shared memory and each bin of global memory is read and
+// written exactly once, coalesced: no global atomics and no partial histograms in HBM.
 #include <cooperative_groups.h>
+
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "common.cuh"
 #include "internal.h"
@@ -24,75 +29,165 @@ namespace slmoe {
 namespace {
 
 constexpr int QB_SLAB = 32;
-constexpr int QB_THREADS = 1024;
 constexpr int QB_MAX_CLUSTER = 8;
+
+// Counter row of a score: min(nbins - 1, max(0, floor(fl32(s * nbins)))), and the extra row
+// nbins for NaN.  The floor is taken exactly on the FP32 pipe: the product is clamped to
+// [0, nbins - 1] with NaN kept, and adding 2^23 rounded toward minus infinity leaves floor(q)
+// in the low mantissa bits (exact for q < 2^23).  Any NaN bit pattern lies above every bin
+// and is capped at nbins.
+__device__ __forceinline__ uint32_t qb_bin(float v, float nb, float top_f, uint32_t nbins) {
+    const float p = __fmul_rn(v, nb);
+    float q;
+    asm("max.NaN.f32 %0, %1, 0f00000000;" : "=f"(q) : "f"(p));
+    asm("min.NaN.f32 %0, %0, %1;" : "+f"(q) : "f"(top_f));
+    const uint32_t bits = __float_as_uint(__fadd_rd(q, 8388608.0f));
+    return min(bits - 0x4B000000u, nbins);
+}
+
+
+// Staging tile of the flush: [32 experts][QB_SB + 1] u32 (odd pitch: conflict-free both ways).
+constexpr int QB_SB = 224;
+constexpr size_t QB_STAGE_BYTES = (size_t)QB_SLAB * (QB_SB + 1) * 4;
+constexpr int QB_THREADS = 1024;
 constexpr int QB_UNROLL = 32;
 
+__device__ __forceinline__ void cp_async4(uint32_t *dst, const uint32_t *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+
+// Load hist rows [cb, cb + nbc) of the slab's experts into the staging tile (consecutive
+// threads on consecutive bins of one expert: coalesced), asynchronously; the NaN row's slot
+// starts at 0.
+__device__ __forceinline__ void qb_stage_load(uint32_t *stage, const uint32_t *hist, int e0, int ne, int nbins,
+                                              int cb, int nbc) {
+    for (int i = threadIdx.x; i < ne * nbc; i += blockDim.x) {
+        const int e = i / nbc, bl = i - e * nbc, b = cb + bl;
+        uint32_t *dst = stage + e * (QB_SB + 1) + bl;
+        if (b < nbins) cp_async4(dst, hist + (int64_t)(e0 + e) * nbins + b);
+        else *dst = 0u;
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Histogram of one slab of 32 experts over this CTA's share of the tokens (see the file
+// comment), then the cluster's reduction into hist.  CTA `rank` of the cluster owns counter
+// rows [b_lo, b_hi) of the slab (the NaN row nbins included) and settles them in chunks of
+// QB_SB rows: (0) the chunk's hist values are loaded into the staging tile, coalesced (for
+// the first chunk this is issued before the counting and lands meanwhile); (1) threads with
+// lane = expert add the P CTAs' counters of those rows (local and distributed shared memory,
+// all ranks' loads in flight at once) into the tile; (2) the tile is stored back into hist,
+// coalesced, and the NaN row goes to status[0].  A closing cluster.sync() keeps every CTA's
+// counters alive until the whole cluster has read them.
 __global__ void __launch_bounds__(QB_THREADS, 1)
 qb_hist_kernel(const float *__restrict__ scores, int64_t T, int E, int nbins,
                uint32_t *__restrict__ hist, int32_t *status) {
-    extern __shared__ uint32_t hs[];                 // [nbins][QB_SLAB]
+    extern __shared__ uint32_t hs[];                 // [nbins + 1][QB_SLAB], then the staging tile
+    uint32_t *stage = hs + (nbins + 1) * QB_SLAB;
     cg::cluster_group cluster = cg::this_cluster();
     const int P = (int)cluster.num_blocks();
     const int rank = (int)cluster.block_rank();
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     constexpr int nwarps = QB_THREADS / 32;
     const int e0 = blockIdx.x * QB_SLAB;
     const int ne = min(QB_SLAB, E - e0);
-    const float nb = (float)nbins;
-    const int top = nbins - 1;
-    int nan_count = 0;
-    bool overflow = false;
+    const float nb = (float)nbins, top_f = (float)(nbins - 1);
+    const int64_t per_t = (T + P - 1) / P;
+    const int64_t t0 = min(T, rank * per_t);
+    const int64_t t1 = min(T, t0 + per_t);
+    const int nrows = nbins + 1;
+    const int per_b = (nrows + P - 1) / P;
+    const int b_lo = min(nrows, rank * per_b), b_hi = min(nrows, b_lo + per_b);
 
-    for (int i = tid; i < QB_SLAB * nbins; i += QB_THREADS) hs[i] = 0u;
+    qb_stage_load(stage, hist, e0, ne, nbins, b_lo, min(QB_SB, b_hi - b_lo));
+
+    // counting: lane = expert; each lane keeps QB_UNROLL row loads in flight.  The first batch
+    // is issued before the counters are cleared.
+    const bool active = lane < ne;
+    const float *col = scores + e0 + (active ? lane : 0);
+    uint32_t *h = hs + lane;
+    int64_t t = t0 + warp;
+    const bool full_batch = active && t + (QB_UNROLL - 1) * nwarps < t1;
+    float v[QB_UNROLL];
+    if (full_batch) {
+#pragma unroll
+        for (int u = 0; u < QB_UNROLL; ++u) v[u] = __ldcs(col + (t + u * nwarps) * (int64_t)E);
+    }
+    {
+        uint4 *h4 = reinterpret_cast<uint4 *>(hs);
+        for (int i = threadIdx.x; i < nrows * QB_SLAB / 4; i += QB_THREADS) h4[i] = make_uint4(0, 0, 0, 0);
+    }
     __syncthreads();
-    const int64_t per = (T + P - 1) / P;
-    const int64_t t0 = rank * per;
-    const int64_t t1 = min(T, t0 + per);
-    if (lane < ne) {
-        const float *col = scores + e0 + lane;
-        uint32_t *h = hs + lane;
-        int64_t t = t0 + warp;
-        for (; t + (QB_UNROLL - 1) * nwarps < t1; t += QB_UNROLL * nwarps) {
-            float v[QB_UNROLL];
+    if (full_batch) {
+        for (;;) {
+#pragma unroll
+            for (int u = 0; u < QB_UNROLL; ++u) atomicAdd(h + qb_bin(v[u], nb, top_f, nbins) * QB_SLAB, 1u);
+            t += QB_UNROLL * nwarps;
+            if (t + (QB_UNROLL - 1) * nwarps >= t1) break;
 #pragma unroll
             for (int u = 0; u < QB_UNROLL; ++u) v[u] = __ldcs(col + (t + u * nwarps) * (int64_t)E);
+        }
+    }
+    if (active)
+        for (; t < t1; t += nwarps) atomicAdd(h + qb_bin(__ldcs(col + t * (int64_t)E), nb, top_f, nbins) * QB_SLAB, 1u);
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    cluster.sync();
+
+    // the cluster's reduction of the owned rows
+    const uint32_t *src[QB_MAX_CLUSTER];
 #pragma unroll
-            for (int u = 0; u < QB_UNROLL; ++u) {
-                // one IEEE fp32 round-to-nearest multiply, floor, clamp to [0, nbins-1]
-                const int b = min(max(__float2int_rd(__fmul_rn(v[u], nb)), 0), top);
-                if (isnan(v[u])) ++nan_count;
-                else atomicAdd(&h[b * QB_SLAB], 1u);
+    for (int r = 0; r < QB_MAX_CLUSTER; ++r) src[r] = r < P ? cluster.map_shared_rank(hs, r) : hs;
+    bool overflow = false;
+    uint32_t nan_count = 0;
+    for (int cb = b_lo; cb < b_hi; cb += QB_SB) {
+        const int nbc = min(QB_SB, b_hi - cb);
+        if (cb != b_lo) {
+            qb_stage_load(stage, hist, e0, ne, nbins, cb, nbc);
+            asm volatile("cp.async.wait_all;" ::: "memory");
+            __syncthreads();
+        }
+        constexpr int CH = 2;
+        for (int i0 = threadIdx.x; i0 < nbc * QB_SLAB; i0 += CH * QB_THREADS) {
+            uint32_t c[CH][QB_MAX_CLUSTER];
+#pragma unroll
+            for (int k = 0; k < CH; ++k) {
+                const int i = i0 + k * QB_THREADS;
+#pragma unroll
+                for (int r = 0; r < QB_MAX_CLUSTER; ++r)
+                    c[k][r] = (i < nbc * QB_SLAB && r < P) ? src[r][cb * QB_SLAB + i] : 0u;
+            }
+#pragma unroll
+            for (int k = 0; k < CH; ++k) {
+                const int i = i0 + k * QB_THREADS;
+                if (i < nbc * QB_SLAB && (i & 31) < ne) {
+                    uint32_t *slot = stage + (i & 31) * (QB_SB + 1) + (i >> 5);
+                    uint64_t sum = *slot;
+#pragma unroll
+                    for (int r = 0; r < QB_MAX_CLUSTER; ++r) sum += c[k][r];
+                    if (sum > 0xffffffffull) {
+                        if (cb + (i >> 5) < nbins) overflow = true;
+                        sum = 0xffffffffull;
+                    }
+                    *slot = (uint32_t)sum;
+                }
             }
         }
-        for (; t < t1; t += nwarps) {
-            const float v = __ldcs(col + t * (int64_t)E);
-            const int b = min(max(__float2int_rd(__fmul_rn(v, nb)), 0), top);
-            if (isnan(v)) ++nan_count;
-            else atomicAdd(&h[b * QB_SLAB], 1u);
+        __syncthreads();
+        for (int i = threadIdx.x; i < ne * nbc; i += QB_THREADS) {
+            const int e = i / nbc, bl = i - e * nbc, b = cb + bl;
+            const uint32_t val = stage[e * (QB_SB + 1) + bl];
+            if (b < nbins) hist[(int64_t)(e0 + e) * nbins + b] = val;
+            else nan_count += val;
         }
+        __syncthreads();
     }
+    // other CTAs of the cluster may still be reading this CTA's counters (a CTA that owns no
+    // rows gets here at once): no CTA leaves before all of them are done
     cluster.sync();
-    // each CTA of the cluster adds a share of the slab's bins across all CTAs
-    const int total = ne * nbins;
-    const int share = (total + P - 1) / P;
-    const int f0 = rank * share, f1 = min(total, f0 + share);
-    for (int f = f0 + tid; f < f1; f += QB_THREADS) {
-        const int b = f / ne, e = f - b * ne;
-        uint64_t sum = 0;
-        for (int r = 0; r < P; ++r) sum += cluster.map_shared_rank(hs, r)[b * QB_SLAB + e];
-        if (sum) {
-            uint32_t *g = hist + (int64_t)(e0 + e) * nbins + b;
-            uint64_t nv = (uint64_t)*g + sum;
-            if (nv > 0xffffffffull) { overflow = true; nv = 0xffffffffull; }
-            *g = (uint32_t)nv;
-        }
-    }
-    cluster.sync();
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) nan_count += __shfl_xor_sync(0xffffffffu, nan_count, o);
     if (status) {
-        if (lane == 0 && nan_count) atomicAdd(&status[ST_NAN], nan_count);
+        if (nan_count) atomicAdd(&status[ST_NAN], (int)nan_count);
         if (overflow) atomicExch(&status[ST_OVERFLOW], 1);
     }
 }
@@ -210,16 +305,62 @@ qb_update_kernel(const uint32_t *__restrict__ hist, int E, int nbins, int k,
 
 }  // namespace
 
+// Cluster size P (CTAs per 32-expert slab) of a histogram launch.  Every CTA needs a whole SM
+// and a cluster's CTAs must share one GPC, so how many clusters of a given size fit at once
+// depends on how the SMs are grouped (cudaOccupancyMaxActiveClusters): 28 clusters of 5 may
+// need two waves where 28 clusters of 4 fit in one.  P minimises waves / P (the per-CTA work
+// falls as 1 / P), fewer waves breaking ties.  Cached per device, kernel and shape.
+template <typename K>
+static int qb_cluster_size(K kern, int nslabs, int threads, size_t smem) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, const void *, int, size_t>, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_tuple(dev, reinterpret_cast<const void *>(kern), nslabs, smem);
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    int best = 1;
+    double best_cost = 1e30;
+    int best_waves = 1 << 30;
+    for (int P = 1; P <= QB_MAX_CLUSTER; ++P) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(nslabs, P, 1);
+        cfg.blockDim = dim3(threads, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = P;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
+            cudaGetLastError();
+            continue;
+        }
+        const int waves = (nslabs + n - 1) / n;
+        const double cost = (double)waves / P;
+        if (cost < best_cost - 1e-12 || (cost < best_cost + 1e-12 && waves < best_waves)) {
+            best = P;
+            best_cost = cost;
+            best_waves = waves;
+        }
+    }
+    cache[key] = best;
+    return best;
+}
+
 int launch_qb_histogram(const float *scores, int64_t T, int E, int nbins, uint32_t *hist,
                         int32_t *status, cudaStream_t st) {
     if (T <= 0) return SLMOE_OK;
-    const size_t smem = (size_t)QB_SLAB * nbins * sizeof(uint32_t);
+    const size_t smem = (size_t)QB_SLAB * (nbins + 1) * sizeof(uint32_t) + QB_STAGE_BYTES;
     cudaError_t e = cudaFuncSetAttribute(qb_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return fail(SLMOE_ECUDA, "qb smem attribute: %s", cudaGetErrorString(e));
     const int nslabs = (E + QB_SLAB - 1) / QB_SLAB;
-    int P = sm_count() / nslabs;
-    P = P < 1 ? 1 : (P > QB_MAX_CLUSTER ? QB_MAX_CLUSTER : P);
+    const int P = qb_cluster_size(qb_hist_kernel, nslabs, QB_THREADS, smem);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(nslabs, P, 1);
     cfg.blockDim = dim3(QB_THREADS, 1, 1);

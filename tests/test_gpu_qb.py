@@ -71,6 +71,36 @@ def test_histogram_edges_and_nan():
     assert int(status[0]) == 4
 
 
+@pytest.mark.parametrize("T,E", [(4099, 96), (1000, 896)])
+def test_histogram_edges_nan_and_alignment_match_the_oracle(T, E):
+    """Bin edges, out-of-range values and NaN spread over rows and experts, at a shape whose
+    rows do not divide evenly among a cluster's CTAs, from a 16-byte aligned matrix and from
+    the same values one float further on (4-byte aligned)."""
+    need_gpu()
+    g = torch.Generator(device="cpu").manual_seed(T * 7 + E)
+    s = torch.rand(T, E, generator=g, dtype=torch.float32)
+    edges = torch.arange(0, 1001, dtype=torch.float32) / 1000
+    s.view(-1)[:edges.numel()] = edges
+    s.view(-1)[edges.numel():2 * edges.numel()] = torch.nextafter(edges, torch.zeros(()))
+    s[5, :] = float("nan")
+    s[T - 1, 3] = float("nan")
+    s[:, 7] = 1.0
+    s[9, 3], s[10, 4] = -0.5, 2.0
+    ref = oracle.qb_histogram(s.numpy(), 1000)
+    n_nan = int(torch.isnan(s).sum())
+    aligned = s.cuda()
+    buf = torch.empty(T * E + 1, dtype=torch.float32, device="cuda")
+    buf[1:] = aligned.view(-1)
+    shifted = buf[1:].view(T, E)
+    assert aligned.data_ptr() % 16 == 0 and shifted.data_ptr() % 16 == 4
+    for x in (aligned, shifted):
+        status = torch.zeros(4, dtype=torch.int32, device="cuda")
+        hist = gpu_hist(x, 1000, status=status)
+        torch.cuda.synchronize()
+        assert np.array_equal(hist.cpu().numpy().view(np.uint32), ref)
+        assert int(status[0]) == n_nan and int(status[1]) == 0
+
+
 def test_update_closed_forms_on_gpu():
     need_gpu()
     E, k = 8, 2
