@@ -200,7 +200,7 @@ qb_hist_kernel(const float *__restrict__ scores, int64_t T, int E, int nbins,
 // through distributed shared memory.  No global scratch.
 constexpr int QBU_CTAS = 8;
 constexpr int QBU_MAXB = 1024 / 32;          // bins per lane (nbins <= 1024)
-constexpr int QBU_THREADS = 512;
+constexpr int QBU_THREADS = 1024;
 constexpr int QBU_STAGE_WORDS = (QBU_THREADS / 32) * QBU_MAXB * 33;
 
 __global__ void __launch_bounds__(QBU_THREADS, 1)
@@ -226,25 +226,25 @@ qb_update_kernel(const uint32_t *__restrict__ hist, int E, int nbins, int k,
     uint32_t *tile = stage + w * (QBU_MAXB * 33);
     for (int e = e0 + w; e < e1; e += QBU_THREADS / 32) {
         const uint32_t *h = hist + (int64_t)e * nbins;
-        uint32_t ld[QBU_MAXB];                   // all loads first: one memory latency
+        // the expert's bins go straight to the staging tile (coalesced, all in flight at once)
 #pragma unroll
         for (int i = 0; i < QBU_MAXB; ++i) {
             const int b = i * 32 + lane;
-            ld[i] = (i < B && b < nbins) ? __ldg(h + b) : 0u;
+            if (i < B) {
+                if (b < nbins) cp_async4(tile + i * 32 + lane + i, h + b);
+                else tile[i * 32 + lane + i] = 0u;
+            }
         }
-#pragma unroll
-        for (int i = 0; i < QBU_MAXB; ++i)
-            if (i < B) tile[i * 32 + lane + i] = ld[i];
+        asm volatile("cp.async.wait_all;" ::: "memory");
         __syncwarp();
-        uint32_t v[QBU_MAXB];
+        // lane-contiguous bins are read from the tile twice (for the lane sum, and by the one
+        // lane that finds the rank) instead of being held in registers
         unsigned long long S = 0;
 #pragma unroll
         for (int i = 0; i < QBU_MAXB; ++i) {
             const int b = b0 + i;
-            v[i] = (i < B) ? tile[b + (b >> 5)] : 0u;
-            S += v[i];
+            if (i < B) S += tile[b + (b >> 5)];
         }
-        __syncwarp();
         unsigned long long inc = S;              // inclusive scan of the lanes' sums
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -266,19 +266,19 @@ qb_update_kernel(const uint32_t *__restrict__ hist, int E, int nbins, int k,
                 int j = 0;
                 unsigned long long prev = C, hj = 1;
                 bool done = false;
-#pragma unroll
-                for (int i = 0; i < QBU_MAXB; ++i) {
-                    if (!done && i < B) {
-                        const unsigned long long before = C;
-                        C += v[i];
-                        if (C >= rc) { j = b0 + i; prev = before; hj = v[i]; done = true; }
-                    }
+                for (int i = 0; i < B && !done; ++i) {
+                    const int b = b0 + i;
+                    const uint32_t vi = tile[b + (b >> 5)];
+                    const unsigned long long before = C;
+                    C += vi;
+                    if (C >= rc) { j = b; prev = before; hj = vi; done = true; }
                 }
                 qq = ((double)j + (r - (double)prev) / (double)hj) / (double)nbins;
             }
             q = __shfl_sync(0xffffffffu, qq, l);
         }
         if (lane == 0) q_s[e - e0] = q;
+        __syncwarp();                            // the tile is refilled for the warp's next expert
     }
     __syncthreads();
     double s = 0.0;

@@ -153,6 +153,22 @@ struct DenseArgs {
     int *counter;          // nullable: global tile counter (zeroed) for dynamic scheduling
 };
 
+// Tile order of the dense kernel: bands of DENSE_BAND row tiles, rows fastest inside a band,
+// so that the tiles in flight at once (about one per SM) share a few activation strips and a
+// few weight strips that stay in L2, and each weight strip is read from HBM once per band
+// instead of once per row tile.
+constexpr int DENSE_BAND = 16;
+__device__ __forceinline__ void dense_tile_mn(int tile, int tiles, int tiles_n, int &tm, int &tn) {
+    const int tiles_m = tiles / tiles_n;
+    const int per_band = DENSE_BAND * tiles_n;
+    const int band = tile / per_band;
+    const int m_first = band * DENSE_BAND;
+    const int bm = min(DENSE_BAND, tiles_m - m_first);    // the last band may be short
+    const int r = tile - band * per_band;
+    tm = m_first + r % bm;
+    tn = r / bm;
+}
+
 template <int BN, int EPI, int PACC>
 struct DenseCfg {
     static constexpr int BM = 128, BK = 64;
@@ -218,8 +234,10 @@ __global__ void __launch_bounds__(192, 1) dense_kernel(const __grid_constant__ T
             const int tile = a.counter ? atomicAdd(a.counter, 1) : (int)blockIdx.x + (it++) * (int)gridDim.x;
             if (!tq_push(tq_ids, tq_full, tq_empty, qs, qp, tile, abort_flag)) goto done;
             if (tile >= a.tiles) break;
-            const int m0 = (tile / a.tiles_n) * Cfg::BM;
-            const int n0 = (tile % a.tiles_n) * Cfg::BN_OUT;
+            int tm, tn;
+            dense_tile_mn(tile, a.tiles, a.tiles_n, tm, tn);
+            const int m0 = tm * Cfg::BM;
+            const int n0 = tn * Cfg::BN_OUT;
             for (int s = 0; s < a.nseg; ++s) {
                 for (int kb = 0; kb < a.kblocks[s]; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) goto done;
@@ -287,8 +305,10 @@ __global__ void __launch_bounds__(192, 1) dense_kernel(const __grid_constant__ T
             if (tile >= a.tiles) break;
             if (!mbar_wait(&tfull[buf], bphase, abort_flag)) goto done;
             tc_after();
-            const int row = (tile / a.tiles_n) * Cfg::BM + row_in_tile;
-            const int n0 = (tile % a.tiles_n) * Cfg::BN_OUT;
+            int tm, tn;
+            dense_tile_mn(tile, a.tiles, a.tiles_n, tm, tn);
+            const int row = tm * Cfg::BM + row_in_tile;
+            const int n0 = tn * Cfg::BN_OUT;
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + buf * Cfg::ACC;
             const bool row_ok = row < a.M;
             if (EPI == EPI_BF16) {
@@ -644,15 +664,21 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
 }
 
 // Work lists of both routed-expert GEMMs in one block: per expert ceil(n_e / cap) passes of
-// balanced size (0 when n_e = 0) times nfb feature blocks, exclusive-scanned into bases.
+// balanced size (0 when n_e = 0) times nfb feature blocks.  The threads scan the experts'
+// item counts into per-expert bases (kept in shared memory), then each warp writes one
+// expert's items at a time with its lanes in parallel, so a hot expert's items do not fall
+// to a single thread.
+constexpr int WL_MAX_E = 4096;
 __global__ void __launch_bounds__(1024)
 worklist_kernel(const int32_t *__restrict__ counts, const int32_t *__restrict__ offsets, int E,
                 int nfb1, int cap1, int4 *__restrict__ items1, int nfb2, int cap2,
                 int4 *__restrict__ items2, int *__restrict__ n_items) {
     __shared__ int wsum[2][32];
+    __shared__ int ebase[2][WL_MAX_E];
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int per = (E + blockDim.x - 1) / blockDim.x;
     const int e0 = tid * per;
+    const int caps[2] = {cap1, cap2}, nfbs[2] = {nfb1, nfb2};
     int loc[2] = {0, 0};
     for (int e = e0; e < e0 + per && e < E; ++e) {
         const int n = counts[e];
@@ -676,20 +702,28 @@ worklist_kernel(const int32_t *__restrict__ counts, const int32_t *__restrict__ 
     base[1] += incl[1] - loc[1];
     if (tid == blockDim.x - 1) { n_items[0] = base[0] + loc[0]; n_items[1] = base[1] + loc[1]; }
     for (int e = e0; e < e0 + per && e < E; ++e) {
+        const int n = counts[e];
+#pragma unroll
+        for (int l = 0; l < 2; ++l) {
+            ebase[l][e] = base[l];
+            base[l] += nfbs[l] * ((n + caps[l] - 1) / caps[l]);
+        }
+    }
+    __syncthreads();
+    int4 *lists[2] = {items1, items2};
+    for (int e = w; e < E; e += blockDim.x >> 5) {
         const int n = counts[e], off = offsets[e];
-        const int caps[2] = {cap1, cap2}, nfbs[2] = {nfb1, nfb2};
-        int4 *lists[2] = {items1, items2};
 #pragma unroll
         for (int l = 0; l < 2; ++l) {
             const int np = (n + caps[l] - 1) / caps[l];
             if (np == 0) continue;
             const int chunk = (n + np - 1) / np;
             const int multi = np > 1 ? 1 : 0;
-            for (int fb = 0; fb < nfbs[l]; ++fb)
-                for (int p = 0; p < np; ++p) {
-                    const int c0 = p * chunk;
-                    lists[l][base[l]++] = make_int4(e, fb | (multi << 16), off + c0, min(chunk, n - c0));
-                }
+            for (int j = lane; j < nfbs[l] * np; j += 32) {
+                const int fb = j / np, pass = j - fb * np;
+                const int c0 = pass * chunk;
+                lists[l][ebase[l][e] + j] = make_int4(e, fb | (multi << 16), off + c0, min(chunk, n - c0));
+            }
         }
     }
 }
