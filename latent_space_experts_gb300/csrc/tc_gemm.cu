@@ -601,7 +601,6 @@ done:
 // CTA with all the hot experts.  With DBUF, passes hold <= 128 tokens and alternate between
 // two TMEM accumulator sets so that an item's epilogue overlaps the next item's MMAs.
 constexpr int G_NMAX = 256;
-constexpr int G_THREADS = 320;                    // TMA, MMA, 4 epilogue, 4 gather warps
 constexpr int G_GATHER_THREADS = 128;
 constexpr int G_TQ = 4;                           // item queue slots
 
@@ -615,6 +614,11 @@ struct GCfg {
     static constexpr int B_STAGES = DBUF ? 4 : 3;
     static constexpr int NBUF = DBUF ? 2 : 1;
     static constexpr int SUB1_COL = DBUF ? 128 : 256;
+    // epilogue warps: the single-buffered accumulator (long passes) stalls the MMAs while it
+    // drains, so it gets two warps per TMEM lane quadrant; the double-buffered one overlaps
+    static constexpr int EPI_WARPS = DBUF ? 4 : 8;
+    static constexpr int GATHER_WARP0 = 2 + EPI_WARPS;
+    static constexpr int THREADS = (2 + EPI_WARPS + 4) * 32;   // TMA, MMA, epilogue, 4 gather warps
     static constexpr int SMEM = A_STAGES * A_BYTES + B_STAGES * B_BYTES + 1024 + 512;
     static_assert(SMEM <= 232448, "shared memory");
 };
@@ -729,7 +733,7 @@ worklist_kernel(const int32_t *__restrict__ counts, const int32_t *__restrict__ 
 }
 
 template <int EPI, bool DBUF>
-__global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_constant__ CUtensorMap wmap,
+__global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const __grid_constant__ CUtensorMap wmap,
                                                                const GroupedArgs a) {
     using Cfg = GCfg<DBUF>;
     constexpr int AST = Cfg::A_STAGES, BST = Cfg::B_STAGES, NBUF = Cfg::NBUF, SUB1 = Cfg::SUB1_COL;
@@ -753,7 +757,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_cons
     if (threadIdx.x == 0) {
         for (int s = 0; s < G_TQ; ++s) {
             mbar_init(&q_full[s], 1);
-            mbar_init(&q_empty[s], 1 + 4 + 4);     // MMA thread, 4 epilogue warps, 4 gather warps
+            mbar_init(&q_empty[s], 1 + Cfg::EPI_WARPS + 4);  // MMA thread, epilogue and gather warps
         }
         for (int s = 0; s < AST; ++s) {
             mbar_init(&a_full[s], 1);
@@ -765,7 +769,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_cons
         }
         for (int b = 0; b < NBUF; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], 4);
+            mbar_init(&tempty[b], Cfg::EPI_WARPS);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -855,9 +859,12 @@ __global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_cons
             umma_commit(&tfull[buf]);
             if (++buf == NBUF) { buf = 0; tph ^= 1; }
         }
-    } else if (warp >= 2 && warp < 6) {
-        // ------------------------------------------------ epilogue
+    } else if (warp >= 2 && warp < Cfg::GATHER_WARP0) {
+        // ------------------------------------------------ epilogue: warp w reads TMEM lane
+        // quadrant w % 4; the EPI_WARPS / 4 warps of a quadrant take alternate 16-column chunks
+        constexpr int WPQ = Cfg::EPI_WARPS / 4;
         const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
         const int lf = q * 32 + lane;                 // feature inside a 128-row sub-tile
         const float ib1 = 1.0f / a.beta1, ib2 = 1.0f / a.beta2;
         int buf = 0, qs = 0;
@@ -876,7 +883,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_cons
             const bool ok = f < a.out_cols;
             const bool ok1 = f + 128 < a.out_cols;
             __nv_bfloat16 *o = a.out + (long long)it.z * a.out_ld + f;
-            for (int c = 0; c < Np; c += 16) {
+            for (int c = half * 16; c < Np; c += 16 * WPQ) {
                 if (EPI == EPI_GLU) {
                     uint32_t g[16], v[16];
                     TMEM_LD16(tb + c, g);
@@ -909,10 +916,10 @@ __global__ void __launch_bounds__(G_THREADS, 1) grouped_kernel(const __grid_cons
             if (lane == 0) mbar_arrive(&tempty[buf]);
             if (++buf == NBUF) { buf = 0; tph ^= 1; }
         }
-    } else if (warp >= 6) {
+    } else if (warp >= Cfg::GATHER_WARP0) {
         // ------------------------------------------------ token-row gather (cp.async, kept in L2)
         const uint64_t pol = policy_evict_last();
-        const int gt = threadIdx.x - 6 * 32;          // 0..127
+        const int gt = threadIdx.x - Cfg::GATHER_WARP0 * 32;   // 0..127
         const int ch = gt & 7;                         // 16-byte chunk of the 128-byte row
         const int rsub = gt >> 3;                      // rows rsub, rsub + 16, ...
         int stage = 0, qs = 0;
@@ -1018,7 +1025,7 @@ int launch_grouped(const CUtensorMap &wmap, const GroupedArgs &a, cudaStream_t s
     auto kern = grouped_kernel<EPI, DBUF>;
     int rc = set_smem(kern, GCfg<DBUF>::SMEM);
     if (rc) return rc;
-    kern<<<sm_count(), G_THREADS, GCfg<DBUF>::SMEM, st>>>(wmap, a);
+    kern<<<sm_count(), GCfg<DBUF>::THREADS, GCfg<DBUF>::SMEM, st>>>(wmap, a);
     return check_launch("grouped_kernel");
 }
 
