@@ -226,7 +226,10 @@ SLMOE_API int slmoe_qb_histogram(const float *scores, int64_t T, int32_t E, int3
  *   N_e = sum_b hist[e,b];  r = (1 - k/E) * N_e;  j = first bin with C_j >= r
  *   q_e = (j + (r - C_{j-1}) / hist[e,j]) / nbins      (q_e = 0 when r = 0)
  *   bias[e] = mean_e(q) - q_e                           (overwrites bias)
- *   computed in fp64 and stored in fp32.  hist [E,nbins] uint32; q_out [E] fp32 or NULL;
+ *   The rank search is exact integer arithmetic (ceil(r) = N_e - floor(N_e k / E)); q_e is
+ *   interpolated in fp32 (absolute error below 3e-7) and the mean is an exact fixed-point sum
+ *   (q_e * 2^31 rounded, added in int64), so the result does not depend on summation order;
+ *   stored in fp32.  hist [E,nbins] uint32; q_out [E] fp32 or NULL;
  *   bias [E] fp32.  E <= 8192, nbins <= 1024.  One thread-block cluster; no workspace.
  */
 SLMOE_API int slmoe_qb_update(const uint32_t *hist, int32_t E, int32_t nbins, int32_t k,

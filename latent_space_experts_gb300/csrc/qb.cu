@@ -192,59 +192,59 @@ qb_hist_kernel(const float *__restrict__ scores, int64_t T, int E, int nbins,
     }
 }
 
-// One cluster of QBU_CTAS CTAs; CTA r owns a contiguous range of experts.  A warp loads an
-// expert's whole histogram into registers up front (lane l holds bins l, l + 32, ...), then
-// walks the 32-bin chunks with an inclusive warp scan until the cumulative count reaches
-// r = (1 - k/E) N_e, and interpolates inside that bin, in fp64.  The mean over experts is a
-// fixed-order sum: per CTA in shared memory, then across the cluster's CTAs in rank order
-// through distributed shared memory.  No global scratch.
-constexpr int QBU_CTAS = 8;
+// One cluster of P CTAs (16 where the device can place such a cluster, else 8); CTA r owns a
+// contiguous range of experts and each warp takes
+// one expert at a time.  Lane l holds the expert's bins l*B .. l*B + B - 1 in registers
+// (16-byte loads when the rows allow); an inclusive warp scan of the lanes' sums gives the
+// cumulative counts.  The arithmetic avoids fp64 (a small fraction of the fp32 rate on this
+// part) without giving up exactness where it matters:
+//   r = (1 - k/E) N = N - N k / E;  with N k = E qd + rm (integer division),
+//   ceil(r) = N - qd exactly, so "first bin with C_j >= r" is an integer search, and
+//   r - C_{j-1} = (N - qd - C_{j-1}) - rm / E is an integer minus a fraction in [0, 1),
+//   so q = (j + (r - C_{j-1}) / h_j) / nbins is formed in fp32 with an error below 3e-7.
+// The mean over experts is an exact fixed-point sum (q * 2^31 rounded to an integer, added in
+// int64 in any order, so the result does not depend on the order), shared across the
+// cluster through distributed shared memory.  No global scratch.
+constexpr int QBU_CTAS = 16;                 // largest cluster tried
+constexpr int QBU_MIN_CTAS = 8;
 constexpr int QBU_MAXB = 1024 / 32;          // bins per lane (nbins <= 1024)
-constexpr int QBU_THREADS = 1024;
-constexpr int QBU_STAGE_WORDS = (QBU_THREADS / 32) * QBU_MAXB * 33;
+constexpr int QBU_THREADS = 512;
+constexpr int QBU_MAX_PER_CTA = 8192 / QBU_MIN_CTAS;
+constexpr float QBU_FIX = 2147483648.0f;     // 2^31
 
 __global__ void __launch_bounds__(QBU_THREADS, 1)
 qb_update_kernel(const uint32_t *__restrict__ hist, int E, int nbins, int k,
                  float *__restrict__ q_out, float *__restrict__ bias) {
-    // dynamic shared memory: per-warp staging tiles, then q of this CTA's experts
-    extern __shared__ uint32_t dyn[];
-    __shared__ double red[QBU_THREADS / 32];
-    __shared__ double part;
-    uint32_t *stage = dyn;
-    double *q_s = reinterpret_cast<double *>(dyn + QBU_STAGE_WORDS);
+    __shared__ float q_s[QBU_MAX_PER_CTA];
+    __shared__ long long red[QBU_THREADS / 32];
+    __shared__ long long part;
     cg::cluster_group cluster = cg::this_cluster();
     const int P = (int)cluster.num_blocks();
     const int rank = (int)cluster.block_rank();
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int per = (E + P - 1) / P;
-    const int e0 = rank * per, e1 = min(E, e0 + per);
-    const double p = 1.0 - (double)k / (double)E;
+    const int e0 = min(E, rank * per), e1 = min(E, e0 + per);
     const int B = (nbins + 31) / 32;             // bins owned by each lane, contiguous
     const int b0 = lane * B;
-    // per-warp staging tile: bin b at word b + b / 32 (one pad word per 32 bins) so that the
-    // coalesced stores and the lane-contiguous reads are both free of bank conflicts
-    uint32_t *tile = stage + w * (QBU_MAXB * 33);
+    // 16-byte loads: each lane's first bin and each expert's row start on a 16-byte boundary
+    const bool vec = (B % 4) == 0 && (nbins % 4) == 0 && ((uintptr_t)hist & 15u) == 0;
     for (int e = e0 + w; e < e1; e += QBU_THREADS / 32) {
-        const uint32_t *h = hist + (int64_t)e * nbins;
-        // the expert's bins go straight to the staging tile (coalesced, all in flight at once)
+        const uint32_t *h = hist + (int64_t)e * nbins + b0;
+        uint32_t v[QBU_MAXB];
+        if (vec) {
 #pragma unroll
-        for (int i = 0; i < QBU_MAXB; ++i) {
-            const int b = i * 32 + lane;
-            if (i < B) {
-                if (b < nbins) cp_async4(tile + i * 32 + lane + i, h + b);
-                else tile[i * 32 + lane + i] = 0u;
+            for (int i = 0; i < QBU_MAXB; i += 4) {
+                uint4 t = make_uint4(0, 0, 0, 0);
+                if (i < B && b0 + i < nbins) t = __ldg(reinterpret_cast<const uint4 *>(h + i));
+                v[i] = t.x; v[i + 1] = t.y; v[i + 2] = t.z; v[i + 3] = t.w;
             }
+        } else {
+#pragma unroll
+            for (int i = 0; i < QBU_MAXB; ++i) v[i] = (i < B && b0 + i < nbins) ? __ldg(h + i) : 0u;
         }
-        asm volatile("cp.async.wait_all;" ::: "memory");
-        __syncwarp();
-        // lane-contiguous bins are read from the tile twice (for the lane sum, and by the one
-        // lane that finds the rank) instead of being held in registers
         unsigned long long S = 0;
 #pragma unroll
-        for (int i = 0; i < QBU_MAXB; ++i) {
-            const int b = b0 + i;
-            if (i < B) S += tile[b + (b >> 5)];
-        }
+        for (int i = 0; i < QBU_MAXB; ++i) S += v[i];
         unsigned long long inc = S;              // inclusive scan of the lanes' sums
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -252,53 +252,59 @@ qb_update_kernel(const uint32_t *__restrict__ hist, int E, int nbins, int k,
             if (lane >= o) inc += n;
         }
         const unsigned long long N = __shfl_sync(0xffffffffu, inc, 31);
-        const double r = p * (double)N;
-        double q = 0.0;
-        if (r > 0.0) {
-            // C_j >= r  <=>  C_j >= ceil(r) for integer counts: the search is integer-only
-            // (fp64 is slow on this part) and decides exactly as the fp64 comparison would
-            const unsigned long long rc = (unsigned long long)ceil(r);
+        const unsigned long long nk = N * (unsigned long long)k;
+        const unsigned long long qd = nk / (unsigned long long)E;
+        const unsigned long long rm = nk - qd * (unsigned long long)E;
+        const unsigned long long rc = N - qd;    // ceil(r); r > 0 exactly when rc >= 1
+        float q = 0.0f;
+        if (rc >= 1) {
             const unsigned m = __ballot_sync(0xffffffffu, inc >= rc);
             const int l = __ffs(m) - 1;          // the lane whose bins hold rank r
-            double qq = 0.0;
+            float qq = 0.0f;
             if (lane == l) {
                 unsigned long long C = inc - S;  // cumulative count before this lane's bins
-                int j = 0;
+                int j = b0;
                 unsigned long long prev = C, hj = 1;
-                bool done = false;
-                for (int i = 0; i < B && !done; ++i) {
-                    const int b = b0 + i;
-                    const uint32_t vi = tile[b + (b >> 5)];
+                bool found = false;
+#pragma unroll
+                for (int i = 0; i < QBU_MAXB; ++i) {
                     const unsigned long long before = C;
-                    C += vi;
-                    if (C >= rc) { j = b; prev = before; hj = vi; done = true; }
+                    C += v[i];
+                    const bool hit = !found && i < B && C >= rc;
+                    if (hit) { j = b0 + i; prev = before; hj = v[i]; }
+                    found = found || hit;
                 }
-                qq = ((double)j + (r - (double)prev) / (double)hj) / (double)nbins;
+                const float frac = (float)(rc - prev) - (float)rm / (float)E;
+                qq = ((float)j + frac / (float)hj) / (float)nbins;
             }
             q = __shfl_sync(0xffffffffu, qq, l);
         }
         if (lane == 0) q_s[e - e0] = q;
-        __syncwarp();                            // the tile is refilled for the warp's next expert
     }
     __syncthreads();
-    double s = 0.0;
-    for (int i = tid; i < e1 - e0; i += blockDim.x) s += q_s[i];
+    long long fx = 0;
+    for (int i = tid; i < e1 - e0; i += blockDim.x) fx += __float2ll_rn(q_s[i] * QBU_FIX);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) red[w] = s;
+    for (int o = 16; o > 0; o >>= 1) fx += __shfl_xor_sync(0xffffffffu, fx, o);
+    if (lane == 0) red[w] = fx;
     __syncthreads();
     if (tid == 0) {
-        double t = 0.0;
+        long long t = 0;
         for (int i = 0; i < QBU_THREADS / 32; ++i) t += red[i];
         part = t;
     }
     cluster.sync();
-    double total = 0.0;
-    for (int r = 0; r < P; ++r) total += *cluster.map_shared_rank(&part, r);
-    const double cbar = total / (double)E;
+    long long pv[QBU_CTAS];
+#pragma unroll
+    for (int r = 0; r < QBU_CTAS; ++r) pv[r] = r < P ? *cluster.map_shared_rank(&part, r) : 0;
+    long long total = 0;
+#pragma unroll
+    for (int r = 0; r < QBU_CTAS; ++r) total += pv[r];
+    const float cbar = (float)(total / E) * (1.0f / QBU_FIX);
     for (int e = e0 + tid; e < e1; e += blockDim.x) {
-        bias[e] = (float)(cbar - q_s[e - e0]);
-        if (q_out) q_out[e] = (float)q_s[e - e0];
+        const float qe = q_s[e - e0];
+        bias[e] = cbar - qe;
+        if (q_out) q_out[e] = qe;
     }
     cluster.sync();
 }
@@ -378,26 +384,52 @@ int launch_qb_histogram(const float *scores, int64_t T, int E, int nbins, uint32
     return check_launch("qb_histogram");
 }
 
+// Cluster size of the bias update: 16 CTAs when the device can place a cluster of 16 such
+// CTAs (a non-portable size), else 8.  Looked up once per device.
+static int qb_update_cluster_size() {
+    static std::mutex mu;
+    static std::map<int, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(dev);
+    if (it != cache.end()) return it->second;
+    int P = QBU_MIN_CTAS;
+    if (cudaFuncSetAttribute(qb_update_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(QBU_CTAS, 1, 1);
+        cfg.blockDim = dim3(QBU_THREADS, 1, 1);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = QBU_CTAS;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, qb_update_kernel, &cfg) == cudaSuccess && n >= 1) P = QBU_CTAS;
+    }
+    cudaGetLastError();
+    cache[dev] = P;
+    return P;
+}
+
 int launch_qb_update(const uint32_t *hist, int E, int nbins, int k, float *q_out, float *bias,
                      cudaStream_t st) {
-    const size_t smem = QBU_STAGE_WORDS * sizeof(uint32_t) +
-                        (size_t)((E + QBU_CTAS - 1) / QBU_CTAS) * sizeof(double);
-    cudaError_t e = cudaFuncSetAttribute(qb_update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return fail(SLMOE_ECUDA, "qb update smem: %s", cudaGetErrorString(e));
+    const int P = qb_update_cluster_size();
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(QBU_CTAS, 1, 1);
+    cfg.gridDim = dim3(P, 1, 1);
     cfg.blockDim = dim3(QBU_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = QBU_CTAS;
+    attr[0].val.clusterDim.x = P;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, qb_update_kernel, hist, E, nbins, k, q_out, bias);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, qb_update_kernel, hist, E, nbins, k, q_out, bias);
     if (e != cudaSuccess) return fail(SLMOE_ECUDA, "qb update launch: %s", cudaGetErrorString(e));
     return check_launch("qb_update");
 }
