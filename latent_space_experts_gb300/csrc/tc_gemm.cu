@@ -157,7 +157,7 @@ struct DenseArgs {
 // so that the tiles in flight at once (about one per SM) share a few activation strips and a
 // few weight strips that stay in L2, and each weight strip is read from HBM once per band
 // instead of once per row tile.
-constexpr int DENSE_BAND = 16;
+constexpr int DENSE_BAND = 8;
 __device__ __forceinline__ void dense_tile_mn(int tile, int tiles, int tiles_n, int &tm, int &tn) {
     const int tiles_m = tiles / tiles_n;
     const int per_band = DENSE_BAND * tiles_n;
@@ -169,24 +169,33 @@ __device__ __forceinline__ void dense_tile_mn(int tile, int tiles, int tiles_n, 
     tn = r / bm;
 }
 
+// A tile is MSUB row sub-tiles of 128 (the MMA's M) sharing one weight tile of BN rows, so a
+// 64-wide K block is MSUB * 16 KB of activations + BN * 128 bytes of weights feeding MSUB * 4
+// MMAs: with MSUB = 2 a stage (64 KB) covers 1024 MMA cycles and three stages cover the
+// ~3000-cycle latency of a loaded L2, where single-row-tile stages (48 KB, 512 cycles) left
+// the tensor pipe waiting a third of the time.  The sub-tiles' accumulators fill the 512 TMEM
+// columns, so the accumulator is single-buffered; each sub-tile has its own 4 epilogue
+// warps to drain it quickly.
 template <int BN, int EPI, int PACC>
 struct DenseCfg {
-    static constexpr int BM = 128, BK = 64;
-    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int BM = 128, BK = 64, MSUB = 2, BM_TILE = BM * MSUB;
+    static constexpr int A_BYTES = BM * BK * 2;           // one row sub-tile
     static constexpr int B_BYTES = BN * BK * 2;
-    static constexpr int STAGE = A_BYTES + B_BYTES;
+    static constexpr int STAGE = MSUB * A_BYTES + B_BYTES;
     static constexpr int STAGES = (196 * 1024) / STAGE;
     static constexpr int BN_OUT = EPI == EPI_GLU ? BN / 2 : BN;
-    static constexpr int ACC = BN * PACC;                 // columns of one accumulator set
-    static constexpr int NBUF = 2 * ACC <= 512 ? 2 : 1;
-    static constexpr int TMEM_COLS = NBUF * ACC;          // a power of two here
+    static constexpr int ACC = BN * PACC;                 // columns of one sub-tile's accumulator
+    static constexpr int NBUF = 1;
+    static constexpr int TMEM_COLS = MSUB * ACC;
+    static constexpr int EPI_WARPS = 4 * MSUB;
+    static constexpr int THREADS = (2 + EPI_WARPS) * 32;  // TMA, MMA, epilogue
     static constexpr int SMEM = STAGES * STAGE + 1024 + 256;
-    static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM columns");
+    static_assert(TMEM_COLS == 512 && STAGES >= 3, "dense tile shape");
 };
 
 template <int BN, int EPI, int PACC>
-__global__ void __launch_bounds__(192, 1) dense_kernel(const __grid_constant__ TmaPack maps,
-                                                       const DenseArgs a) {
+__global__ void __launch_bounds__(DenseCfg<BN, EPI, PACC>::THREADS, 1) dense_kernel(const __grid_constant__ TmaPack maps,
+                                                                                  const DenseArgs a) {
     using Cfg = DenseCfg<BN, EPI, PACC>;
     constexpr int STAGES = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -209,11 +218,11 @@ __global__ void __launch_bounds__(192, 1) dense_kernel(const __grid_constant__ T
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], 4);
+            mbar_init(&tempty[b], Cfg::EPI_WARPS);
         }
         for (int q = 0; q < TQ; ++q) {
             mbar_init(&tq_full[q], 1);
-            mbar_init(&tq_empty[q], 5);
+            mbar_init(&tq_empty[q], 1 + Cfg::EPI_WARPS);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -236,15 +245,17 @@ __global__ void __launch_bounds__(192, 1) dense_kernel(const __grid_constant__ T
             if (tile >= a.tiles) break;
             int tm, tn;
             dense_tile_mn(tile, a.tiles, a.tiles_n, tm, tn);
-            const int m0 = tm * Cfg::BM;
+            const int m0 = tm * Cfg::BM_TILE;
             const int n0 = tn * Cfg::BN_OUT;
             for (int s = 0; s < a.nseg; ++s) {
                 for (int kb = 0; kb < a.kblocks[s]; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) goto done;
                     mbar_expect_tx(&full[stage], Cfg::STAGE);
                     const uint32_t sa = su32(smem + stage * Cfg::STAGE);
-                    const uint32_t sb = sa + Cfg::A_BYTES;
-                    tma_load_2d(sa, &maps.a[s], &full[stage], kb * Cfg::BK, m0);
+                    const uint32_t sb = sa + Cfg::MSUB * Cfg::A_BYTES;
+#pragma unroll
+                    for (int j = 0; j < Cfg::MSUB; ++j)
+                        tma_load_2d(sa + j * Cfg::A_BYTES, &maps.a[s], &full[stage], kb * Cfg::BK, m0 + j * Cfg::BM);
                     if (EPI == EPI_GLU) {
                         tma_load_2d(sb, &maps.b[s], &full[stage], kb * Cfg::BK, n0);
                         tma_load_2d(sb + (BN / 2) * 128, &maps.b[s], &full[stage], kb * Cfg::BK,
@@ -271,30 +282,34 @@ __global__ void __launch_bounds__(192, 1) dense_kernel(const __grid_constant__ T
             if (tile >= a.tiles) break;
             if (!mbar_wait(&tempty[buf], bphase ^ 1, abort_flag)) goto done;
             tc_after();
-            const uint32_t dbase = tmem_base + buf * Cfg::ACC;
             int kg = 0;
             for (int s = 0; s < a.nseg; ++s) {
                 for (int kb = 0; kb < a.kblocks[s]; ++kb, ++kg) {
                     if (!mbar_wait(&full[stage], phase, abort_flag)) goto done;
                     tc_after();
-                    const uint32_t d = dbase + (kg % PACC) * BN;
                     const uint32_t sa = su32(smem + stage * Cfg::STAGE);
-                    const uint32_t sb = sa + Cfg::A_BYTES;
+                    const uint32_t sb = sa + Cfg::MSUB * Cfg::A_BYTES;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        umma(d, sdesc(sa + kk * 32), sdesc(sb + kk * 32), IDESC,
-                             (kg >= PACC || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t bd = sdesc(sb + kk * 32);
+#pragma unroll
+                        for (int j = 0; j < Cfg::MSUB; ++j)
+                            umma(tmem_base + j * Cfg::ACC + (kg % PACC) * BN, sdesc(sa + j * Cfg::A_BYTES + kk * 32), bd,
+                                 IDESC, (kg >= PACC || kk > 0) ? 1u : 0u);
+                    }
                     umma_commit(&empty[stage]);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
             }
             umma_commit(&tfull[buf]);
-            if (++buf == 2) { buf = 0; bphase ^= 1; }
+            if (++buf == Cfg::NBUF) { buf = 0; bphase ^= 1; }
         }
     } else if (warp >= 2) {
-        // ------------------------------------------------ epilogue warps
+        // ------------------------------------------------ epilogue warps: warp w drains TMEM
+        // lane quarter w % 4 of row sub-tile (w - 2) / 4
         const int q = warp & 3;                       // TMEM lane quarter of this warp
-        const int row_in_tile = q * 32 + lane;
+        const int sub = (warp - 2) >> 2;
+        const int row_in_tile = sub * Cfg::BM + q * 32 + lane;
             int buf = 0;
         uint32_t bphase = 0;
         int qs = 0;
@@ -307,9 +322,9 @@ __global__ void __launch_bounds__(192, 1) dense_kernel(const __grid_constant__ T
             tc_after();
             int tm, tn;
             dense_tile_mn(tile, a.tiles, a.tiles_n, tm, tn);
-            const int row = tm * Cfg::BM + row_in_tile;
+            const int row = tm * Cfg::BM_TILE + row_in_tile;
             const int n0 = tn * Cfg::BN_OUT;
-            const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + buf * Cfg::ACC;
+            const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + sub * Cfg::ACC;
             const bool row_ok = row < a.M;
             if (EPI == EPI_BF16) {
                 __nv_bfloat16 *C = static_cast<__nv_bfloat16 *>(a.C) + (long long)row * a.ldc;
@@ -389,7 +404,7 @@ __global__ void __launch_bounds__(192, 1) dense_kernel(const __grid_constant__ T
             tc_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[buf]);
-            if (++buf == 2) { buf = 0; bphase ^= 1; }
+            if (++buf == Cfg::NBUF) { buf = 0; bphase ^= 1; }
         }
     }
 done:
@@ -1009,14 +1024,14 @@ template <int BN, int EPI, int PACC>
 int launch_dense(const TmaPack &maps, DenseArgs a, cudaStream_t st) {
     using Cfg = DenseCfg<BN, EPI, PACC>;
     a.tiles_n = (a.N + Cfg::BN_OUT - 1) / Cfg::BN_OUT;
-    a.tiles = ((a.M + Cfg::BM - 1) / Cfg::BM) * a.tiles_n;
+    a.tiles = ((a.M + Cfg::BM_TILE - 1) / Cfg::BM_TILE) * a.tiles_n;
     if (a.tiles == 0) return SLMOE_OK;
     auto kern = dense_kernel<BN, EPI, PACC>;
     int rc = set_smem(kern, Cfg::SMEM);
     if (rc) return rc;
     const int sms = sm_count();
     const int grid = a.tiles < sms ? a.tiles : sms;
-    kern<<<grid, 192, Cfg::SMEM, st>>>(maps, a);
+    kern<<<grid, Cfg::THREADS, Cfg::SMEM, st>>>(maps, a);
     return check_launch("dense_kernel");
 }
 
