@@ -613,8 +613,11 @@ done:
 // on the device (expert-major, then feature block, then pass, so the passes of one weight tile
 // are adjacent and the CTAs that take them together share it through L2) and are handed out
 // dynamically through a global counter, so the heavy skew of expert loads cannot leave one
-// CTA with all the hot experts.  With DBUF, passes hold <= 128 tokens and alternate between
-// two TMEM accumulator sets so that an item's epilogue overlaps the next item's MMAs.
+// CTA with all the hot experts.  Both routed-expert GEMMs use 256-token passes with one TMEM
+// accumulator set drained by 8 epilogue warps while the weight ring keeps streaming.  (With
+// DBUF, passes hold <= 128 tokens and alternate between two accumulator sets so that an
+// item's epilogue overlaps the next item's MMAs; measured slower, because tcgen05.ld traffic
+// beside running MMAs slows them by up to 2x at these widths.)
 constexpr int G_NMAX = 256;
 constexpr int G_GATHER_THREADS = 128;
 constexpr int G_TQ = 4;                           // item queue slots
@@ -1123,7 +1126,7 @@ int tc_forward_back(const slmoe_config *c, const slmoe_weights *w, const TcForwa
     // work lists of both routed-expert GEMMs (device-built from the expert counts)
     const int nfb1 = (I + 127) / 128, nfb2 = (dl + 255) / 256;
     worklist_kernel<<<1, 1024, 0, st>>>(f.counts, f.offsets, E, nfb1, GCfg<false>::PASS, f.items1, nfb2,
-                                        GCfg<true>::PASS, f.items2, f.counters + 8);
+                                        GCfg<false>::PASS, f.items2, f.counters + 8);
     if ((rc = check_launch("worklist"))) return rc;
     {   // routed experts, gate|up + SiTU-GLU: h[perm row] = GLU(W13[e] x_lat[token])
         CUtensorMap wm;
@@ -1150,7 +1153,7 @@ int tc_forward_back(const slmoe_config *c, const slmoe_weights *w, const TcForwa
         a.b_src = static_cast<const bf *>(f.h); a.b_ld = I; a.b_K = I;
         a.out = static_cast<bf *>(f.y_e); a.out_ld = dl; a.out_cols = dl;
         a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
-        if ((rc = launch_grouped<EPI_BF16, true>(wm, a, st))) return rc;
+        if ((rc = launch_grouped<EPI_BF16, false>(wm, a, st))) return rc;
     }
     stage_event(5, st);
     (void)Tk;
