@@ -618,18 +618,17 @@ done:
 // DBUF, passes hold <= 128 tokens and alternate between two accumulator sets so that an
 // item's epilogue overlaps the next item's MMAs; measured slower, because tcgen05.ld traffic
 // beside running MMAs slows them by up to 2x at these widths.)
-constexpr int G_NMAX = 256;
 constexpr int G_GATHER_THREADS = 128;
 constexpr int G_TQ = 4;                           // item queue slots
 
 template <bool DBUF>
 struct GCfg {
     static constexpr int NSUB = 2;
-    static constexpr int PASS = DBUF ? 128 : G_NMAX;     // tokens per pass
+    static constexpr int PASS = DBUF ? 128 : 192;        // tokens per pass
     static constexpr int A_BYTES = NSUB * 128 * 128;
     static constexpr int A_STAGES = DBUF ? 5 : 4;         // 160 KB / 128 KB of weights in flight
     static constexpr int B_BYTES = PASS * 128;
-    static constexpr int B_STAGES = DBUF ? 4 : 3;
+    static constexpr int B_STAGES = 4;
     static constexpr int NBUF = DBUF ? 2 : 1;
     static constexpr int SUB1_COL = DBUF ? 128 : 256;
     // epilogue warps: the single-buffered accumulator (long passes) stalls the MMAs while it
