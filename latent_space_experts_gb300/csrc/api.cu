@@ -102,8 +102,9 @@ int make_layout(const slmoe_config *c, Layout *L) {
         // work items: nfb feature blocks x (one pass per expert + one per full pass of tokens)
         const size_t Tk = T * k;
         const size_t nfb1 = (c->I + 127) / 128, nfb2 = (c->d_latent + 255) / 256;
-        L->items1 = take(nfb1 * (E + (Tk + 255) / 256) * 16);
-        L->items2 = take(nfb2 * (E + (Tk + 127) / 128) * 16);
+        // per feature block at most E + ceil(T k / pass) passes (sum of ceil(n_e / pass))
+        L->items1 = take(nfb1 * (E + (Tk + GROUPED_PASS - 1) / GROUPED_PASS) * 16);
+        L->items2 = take(nfb2 * (E + (Tk + GROUPED_PASS - 1) / GROUPED_PASS) * 16);
     }
     L->pub.total = off;
     return SLMOE_OK;

@@ -68,6 +68,9 @@ int launch_scan(int32_t *chunk_counts, int nchunks, int E, int32_t *counts, cuda
 int launch_scatter(const int32_t *topk_idx, const int32_t *chunk_base, const int32_t *counts, int T,
                    int E, int k, int32_t *offsets, int32_t *perm, int32_t *slot_pos, cudaStream_t st);
 constexpr int ROUTE_CHUNK = 16;  // tokens per top-k block / permutation chunk
+// Tokens per pass of the routed-expert GEMMs: an expert with n tokens makes ceil(n / pass)
+// work items per feature block, which also sizes the work lists in the workspace.
+constexpr int GROUPED_PASS = 192;
 
 // ---------------------------------------------------------------- QB
 int launch_qb_histogram(const float *scores, int64_t T, int E, int nbins, uint32_t *hist,

@@ -624,7 +624,7 @@ constexpr int G_TQ = 4;                           // item queue slots
 template <bool DBUF>
 struct GCfg {
     static constexpr int NSUB = 2;
-    static constexpr int PASS = DBUF ? 128 : 192;        // tokens per pass
+    static constexpr int PASS = DBUF ? 128 : GROUPED_PASS;   // tokens per pass
     static constexpr int A_BYTES = NSUB * 128 * 128;
     static constexpr int A_STAGES = DBUF ? 5 : 4;         // 160 KB / 128 KB of weights in flight
     static constexpr int B_BYTES = PASS * 128;
@@ -693,7 +693,7 @@ constexpr int WL_MAX_E = 4096;
 __global__ void __launch_bounds__(1024)
 worklist_kernel(const int32_t *__restrict__ counts, const int32_t *__restrict__ offsets, int E,
                 int nfb1, int cap1, int4 *__restrict__ items1, int nfb2, int cap2,
-                int4 *__restrict__ items2, int *__restrict__ n_items) {
+                int4 *__restrict__ items2, int *__restrict__ n_items, int max1, int max2) {
     __shared__ int wsum[2][32];
     __shared__ int ebase[2][WL_MAX_E];
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -721,7 +721,10 @@ worklist_kernel(const int32_t *__restrict__ counts, const int32_t *__restrict__ 
     for (int i = 0; i < w; ++i) { base[0] += wsum[0][i]; base[1] += wsum[1][i]; }
     base[0] += incl[0] - loc[0];
     base[1] += incl[1] - loc[1];
-    if (tid == blockDim.x - 1) { n_items[0] = base[0] + loc[0]; n_items[1] = base[1] + loc[1]; }
+    if (tid == blockDim.x - 1) {
+        n_items[0] = min(base[0] + loc[0], max1);
+        n_items[1] = min(base[1] + loc[1], max2);
+    }
     for (int e = e0; e < e0 + per && e < E; ++e) {
         const int n = counts[e];
 #pragma unroll
@@ -740,10 +743,13 @@ worklist_kernel(const int32_t *__restrict__ counts, const int32_t *__restrict__ 
             if (np == 0) continue;
             const int chunk = (n + np - 1) / np;
             const int multi = np > 1 ? 1 : 0;
+            const int maxl = l == 0 ? max1 : max2;
             for (int j = lane; j < nfbs[l] * np; j += 32) {
                 const int fb = j / np, pass = j - fb * np;
                 const int c0 = pass * chunk;
-                lists[l][ebase[l][e] + j] = make_int4(e, fb | (multi << 16), off + c0, min(chunk, n - c0));
+                // the workspace holds the largest possible list; never write past it
+                if (ebase[l][e] + j < maxl)
+                    lists[l][ebase[l][e] + j] = make_int4(e, fb | (multi << 16), off + c0, min(chunk, n - c0));
             }
         }
     }
@@ -1124,8 +1130,10 @@ int tc_forward_back(const slmoe_config *c, const slmoe_weights *w, const TcForwa
 
     // work lists of both routed-expert GEMMs (device-built from the expert counts)
     const int nfb1 = (I + 127) / 128, nfb2 = (dl + 255) / 256;
+    const long long Tk_items = (Tk + GROUPED_PASS - 1) / GROUPED_PASS;
     worklist_kernel<<<1, 1024, 0, st>>>(f.counts, f.offsets, E, nfb1, GCfg<false>::PASS, f.items1, nfb2,
-                                        GCfg<false>::PASS, f.items2, f.counters + 8);
+                                        GCfg<false>::PASS, f.items2, f.counters + 8,
+                                        (int)(nfb1 * (E + Tk_items)), (int)(nfb2 * (E + Tk_items)));
     if ((rc = check_launch("worklist"))) return rc;
     {   // routed experts, gate|up + SiTU-GLU: h[perm row] = GLU(W13[e] x_lat[token])
         CUtensorMap wm;
