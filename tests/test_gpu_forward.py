@@ -111,6 +111,34 @@ def test_forward_fp32_edge_shapes(over):
     assert_close_rms(y, ref["y"], F32_TOL, "y")
 
 
+def test_forward_expert_loads_just_over_a_pass():
+    """Every expert gets 196 tokens, a few more than the routed GEMMs' 192-token pass, so each
+    (expert, feature block) splits into two passes and the work lists come within one item per
+    feature block of the capacity the workspace reserves for them.  The routing is set by the
+    router weights: W_r is the identity on the first 16 input dimensions and token t has +4 on
+    dimensions t..t+3 (mod 16) and -4 on the other twelve."""
+    need_gpu()
+    E, k = 16, 4
+    shp = synthetic.shape_with("mid", d=512, T=784, E=E, k=k, I=256)
+    inp = synthetic.layer_inputs(shp, seed=7)
+    T, d = shp.T, shp.d
+    W_r = torch.zeros(E, d)
+    W_r[torch.arange(E), torch.arange(E)] = 1.0
+    x = inp["x"].float()
+    x[:, :E] = -4.0
+    x[torch.arange(T)[:, None], (torch.arange(T)[:, None] + torch.arange(k)[None, :]) % E] = 4.0
+    inp["x"] = x.to(inp["x"].dtype)
+    inp["W_r"] = W_r
+    inp["bias"] = torch.zeros(E)
+    inp["logit_offset"] = None
+    y, topk, views = run_forward(shp, to_dev(inp))
+    counts = views["counts"].cpu().numpy()
+    assert counts.min() == counts.max() == T * k // E
+    ref = oracle.forward(inp, shp.k, forced_topk_idx=topk)
+    check_stages(shp, inp, topk, views, ref, BF16_TOL)
+    assert_close_rms(y, ref["y"], BF16_TOL, "y")
+
+
 def test_identical_experts_reduce_to_dense_on_gpu():
     """If every routed expert is the same, routing cannot matter: compare with the oracle's
     own routing (no forcing)."""
