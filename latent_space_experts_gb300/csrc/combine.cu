@@ -4,8 +4,9 @@
 // Stable LatentMoE block sits after the combine and before the up-projection.
 //   c_t = sum_j topk_w[t,j] * y_e[slot_pos[t,j]]       (fp32, slots in order j = 0..k-1)
 //   z_t = gamma * c_t / sqrt(mean(c_t^2) + eps)
-// One CTA per token; 16-byte vector loads of the k expert rows; c_t is staged in shared
-// memory between the two passes.  HBM-bound: it reads k rows of d_latent per token.
+// One CTA per token; 16-byte vector loads of the k expert rows, eight rows in flight per
+// thread; c_t is staged in shared memory between the two passes.  HBM-bound: it reads k rows
+// of d_latent per token.
 #include "common.cuh"
 #include "internal.h"
 
@@ -13,6 +14,7 @@ namespace slmoe {
 namespace {
 
 constexpr int CB_THREADS = 256;
+constexpr int CB_GROUP = 8;        // expert rows loaded before they are added
 
 template <typename T> struct Vec;
 template <> struct Vec<float> { static constexpr int N = 4; using U = float4; };
@@ -71,13 +73,23 @@ combine_rmsnorm_kernel(const T *__restrict__ y_e, const float *__restrict__ topk
         float acc[V];
 #pragma unroll
         for (int i = 0; i < V; ++i) acc[i] = 0.f;
-        for (int j = 0; j < k; ++j) {
-            const U u = *reinterpret_cast<const U *>(y_e + rows[j] + (int64_t)q * V);
-            float f[V];
-            unpack<T>(u, f);
-            const float wj = wts[j];
+        // the slots' rows are loaded CB_GROUP at a time before any is added, so that a thread
+        // keeps that many loads in flight; the adds stay in slot order j = 0..k-1
+        for (int j0 = 0; j0 < k; j0 += CB_GROUP) {
+            U u[CB_GROUP];
 #pragma unroll
-            for (int i = 0; i < V; ++i) acc[i] = fmaf(wj, f[i], acc[i]);
+            for (int g = 0; g < CB_GROUP; ++g)
+                if (j0 + g < k) u[g] = *reinterpret_cast<const U *>(y_e + rows[j0 + g] + (int64_t)q * V);
+#pragma unroll
+            for (int g = 0; g < CB_GROUP; ++g) {
+                if (j0 + g < k) {
+                    float f[V];
+                    unpack<T>(u[g], f);
+                    const float wj = wts[j0 + g];
+#pragma unroll
+                    for (int i = 0; i < V; ++i) acc[i] = fmaf(wj, f[i], acc[i]);
+                }
+            }
         }
 #pragma unroll
         for (int i = 0; i < V; ++i) {
