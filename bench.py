@@ -297,6 +297,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--qb-only", action="store_true", help="only the QB engine measurement")
+    ap.add_argument("--no-graph", action="store_true", help="time the step without a CUDA graph")
     ap.add_argument("--skew", action="store_true", help="heavy skew (10%% hot experts)")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -335,6 +336,22 @@ def main():
     torch.cuda.synchronize()
     assert status.cpu().tolist()[1:3] == [0, 0], f"device status {status.cpu().tolist()}"
 
+    # the timed step is replayed from a CUDA graph of the same calls (the library's launches are
+    # stream-ordered, its auxiliary stream joins the capture through the fork/join events);
+    # the graph only removes host launch gaps between the step's ~15 kernels
+    graph = None
+    launches_per_step = None
+    if not args.no_graph:
+        l_cap = lse.slmoe_launch_count()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step(inp["x"])
+        launches_per_step = lse.slmoe_launch_count() - l_cap
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        assert status.cpu().tolist()[1:3] == [0, 0], f"device status {status.cpu().tolist()}"
+
     # ---------------- device-resident timing
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if sampler:
@@ -346,12 +363,16 @@ def main():
     w0 = time.time()
     e0.record(stream)
     for _ in range(args.steps):
-        step(inp["x"])
+        if graph is not None:
+            graph.replay()
+        else:
+            step(inp["x"])
     e1.record(stream)
     torch.cuda.synchronize()
     w1 = time.time()
     barrier(world)
-    launches = lse.slmoe_launch_count() - l0
+    launches = (launches_per_step * args.steps if graph is not None
+                else lse.slmoe_launch_count() - l0)
     ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
     clocks = sampler.stop(w0, w1) if sampler else None
 
@@ -454,7 +475,8 @@ def main():
                        "E": shp.E, "k": shp.k, "I": shp.I, "n_shared": shp.n_shared, "I_shared": shp.I_shared,
                        "router": "fp32 logits (3-piece bf16 split)", "skew": bool(args.skew),
                        "parallelism": f"replicas x{world}",
-                       "l2": "no flush: weights (10.2 GB at K3) exceed L2 every step"},
+                       "l2": "no flush: weights (10.2 GB at K3) exceed L2 every step",
+                       "cuda_graph": graph is not None},
             "roofline": roof,
             "layer_roofline": {"ms": round(t_layer * 1e3, 4), "frac": round(t_layer * 1e3 / ms, 4),
                                "flops": layer_flops, "bytes": layer_bytes,

@@ -434,6 +434,7 @@ int slmoe_forward(const slmoe_config *cfg, const void *x, const slmoe_weights *w
         cudaMemcpyAsync(topk_idx_out, R.topk_idx, (size_t)cfg->T * cfg->k * 4, cudaMemcpyDeviceToDevice,
                         st) != cudaSuccess)
         return check_launch("copy topk_idx");
+    if ((rc = tc_worklists(cfg, tf, st))) return rc;
     if (cudaStreamWaitEvent(st, aux->join, 0) != cudaSuccess) return check_launch("join wait");
     return tc_forward_back(cfg, w, tf, y, st);
 }

@@ -1120,6 +1120,17 @@ int tc_forward_front(const slmoe_config *c, const void *x, const slmoe_weights *
     return SLMOE_OK;
 }
 
+int tc_worklists(const slmoe_config *c, const TcForward &f, cudaStream_t st) {
+    const int E = c->E, I = c->I, dl = c->d_latent;
+    const long long Tk = (long long)c->T * c->k;
+    const int nfb1 = (I + 127) / 128, nfb2 = (dl + 255) / 256;
+    const long long Tk_items = (Tk + GROUPED_PASS - 1) / GROUPED_PASS;
+    worklist_kernel<<<1, 1024, 0, st>>>(f.counts, f.offsets, E, nfb1, GCfg<false>::PASS, f.items1, nfb2,
+                                        GCfg<false>::PASS, f.items2, f.counters + 8,
+                                        (int)(nfb1 * (E + Tk_items)), (int)(nfb2 * (E + Tk_items)));
+    return check_launch("worklist");
+}
+
 int tc_forward_back(const slmoe_config *c, const slmoe_weights *w, const TcForward &f, void *y,
                     cudaStream_t st) {
     const int T = c->T, d = c->d, dl = c->d_latent, E = c->E, k = c->k, I = c->I;
@@ -1128,13 +1139,7 @@ int tc_forward_back(const slmoe_config *c, const slmoe_weights *w, const TcForwa
     int rc;
     using bf = __nv_bfloat16;
 
-    // work lists of both routed-expert GEMMs (device-built from the expert counts)
-    const int nfb1 = (I + 127) / 128, nfb2 = (dl + 255) / 256;
-    const long long Tk_items = (Tk + GROUPED_PASS - 1) / GROUPED_PASS;
-    worklist_kernel<<<1, 1024, 0, st>>>(f.counts, f.offsets, E, nfb1, GCfg<false>::PASS, f.items1, nfb2,
-                                        GCfg<false>::PASS, f.items2, f.counters + 8,
-                                        (int)(nfb1 * (E + Tk_items)), (int)(nfb2 * (E + Tk_items)));
-    if ((rc = check_launch("worklist"))) return rc;
+    (void)E;
     {   // routed experts, gate|up + SiTU-GLU: h[perm row] = GLU(W13[e] x_lat[token])
         CUtensorMap wm;
         if ((rc = make_map(&wm, w->W13, (long long)E * 2 * I, dl, dl, 128))) return rc;

@@ -30,6 +30,10 @@ int tc_router_scores(const slmoe_config *c, const void *x, const float *W_r, con
 int tc_forward_front(const slmoe_config *c, const void *x, const slmoe_weights *w,
                      const TcForward &f, cudaStream_t st);
 
+// The work lists of the two routed-expert GEMMs, built on the device from the expert counts
+// and offsets of routing (launched on the routing stream, before it joins the front part).
+int tc_worklists(const slmoe_config *c, const TcForward &f, cudaStream_t st);
+
 // Everything after routing and the front part: the two grouped expert GEMMs, combine +
 // RMSNorm, and the up-projection with the shared experts' down-projection.
 int tc_forward_back(const slmoe_config *c, const slmoe_weights *w, const TcForward &f, void *y,
