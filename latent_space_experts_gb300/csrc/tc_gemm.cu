@@ -607,13 +607,13 @@ done:
 // (the MMA's M) times the pass's tokens (N <= PASS, rounded to 16).  NSUB = 2 pairs the gate
 // rows fb*128.. with the up rows I + fb*128.. for the fused SiTU-GLU, or two blocks of 128
 // output features (expert down).  The weights stream from HBM through a 128 KB ring of TMA
-// loads; the pass's token rows are gathered from L2 by cp.async into a 3-deep ring, each
+// loads; the pass's token rows are gathered from L2 by cp.async into a 4-deep ring, each
 // gather thread signalling a stage with cp.async.mbarrier.arrive.noinc (the MMA thread fences
 // the generic-proxy writes to the async proxy after its wait).  Items come from a list built
 // on the device (expert-major, then feature block, then pass, so the passes of one weight tile
 // are adjacent and the CTAs that take them together share it through L2) and are handed out
 // dynamically through a global counter, so the heavy skew of expert loads cannot leave one
-// CTA with all the hot experts.  Both routed-expert GEMMs use 256-token passes with one TMEM
+// CTA with all the hot experts.  Both routed-expert GEMMs use 192-token passes with one TMEM
 // accumulator set drained by 8 epilogue warps while the weight ring keeps streaming.  (With
 // DBUF, passes hold <= 128 tokens and alternate between two accumulator sets so that an
 // item's epilogue overlaps the next item's MMAs; measured slower, because tcgen05.ld traffic
