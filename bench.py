@@ -147,6 +147,21 @@ def barrier(world):
         dist.barrier()
 
 
+def oracle_inputs(inp):
+    """The layer inputs on the host for the oracle: the dense tensors (x, router, latent
+    projections, shared experts, norm) widened to the oracle's fp64 once, as the GPU keeps
+    its weights resident; the routed experts' weights (40 GB in fp64 at K3) stay in their
+    storage type and the oracle widens each chosen expert's matrices per call."""
+    import numpy as np
+    out = {}
+    for k, v in inp.items():
+        if v is None or k in ("W13", "W2"):
+            out[k] = v.cpu() if v is not None else None
+        else:
+            out[k] = np.ascontiguousarray(v.detach().cpu().double().numpy())
+    return out
+
+
 def oracle_sample(shp, inp_cpu, n_tok):
     """Time the fp64 oracle on n_tok tokens of the workload (routing included)."""
     import numpy as np
@@ -162,15 +177,16 @@ def oracle_tokens(shp, inp_cpu, target_s):
     """Tokens per oracle sample so that one sample takes at most about target_s seconds.
     Trials double the token count until one takes a quarter of the target; the count is then
     scaled by target / trial time.  A sample's cost grows more slowly than its token count
-    (the dense weights are widened once per sample, and tokens share experts), so the
-    scaled sample does not overshoot."""
+    (tokens share experts, whose weights are widened once per sample), so the scaled sample
+    does not overshoot."""
+    cap = 4096
     n = min(4, shp.T)
     while True:
         _, dt = oracle_sample(shp, inp_cpu, n)
-        if dt >= target_s / 4 or n >= min(shp.T, 1024):
+        if dt >= target_s / 4 or n >= min(shp.T, cap):
             break
-        n = min(2 * n, shp.T, 1024)
-    return max(1, min(shp.T, 1024, int(n * target_s / max(dt, 1e-6))))
+        n = min(2 * n, shp.T, cap)
+    return max(1, min(shp.T, cap, int(n * target_s / max(dt, 1e-6))))
 
 
 def profiled_traffic(stage):
@@ -216,7 +232,7 @@ def run_reference(args):
     shp = synthetic.LAYERS[args.workload]
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = synthetic.layer_inputs(shp, seed=0, device=dev)
-    inp_cpu = {k: (v.cpu() if v is not None else None) for k, v in inp.items()}
+    inp_cpu = oracle_inputs(inp)
     del inp
     # each step is a bounded sample: the whole run (warm-up + timed) takes about ref_seconds
     n_tok = args.ref_tokens or oracle_tokens(shp, inp_cpu, args.ref_seconds / max(1, args.steps + args.warmup))
@@ -294,7 +310,7 @@ def main():
                     help="about how long the whole reference run (warm-up + timed steps) takes")
     ap.add_argument("--cpu-baseline-tokens", type=int, default=None,
                     help="oracle tokens of the cpu_baseline sample (default: sized from --cpu-seconds)")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-seconds", type=float, default=25.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--qb-only", action="store_true", help="only the QB engine measurement")
     ap.add_argument("--no-graph", action="store_true", help="time the step without a CUDA graph")
@@ -458,7 +474,7 @@ def main():
     # ---------------- oracle on the host cores (bounded sample)
     cpu_base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        inp_cpu = {k: (v.cpu() if v is not None else None) for k, v in inp.items()}
+        inp_cpu = oracle_inputs(inp)
         n_tok = args.cpu_baseline_tokens or oracle_tokens(shp, inp_cpu, args.cpu_seconds)
         v, dt = oracle_sample(shp, inp_cpu, n_tok)
         cpu_base = {"value": round(v, 3), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
