@@ -289,10 +289,23 @@ def qb_engine(hbm):
     g1.record(stream)
     torch.cuda.synchronize()
     tu = g0.elapsed_time(g1) / reps * 1e-3
+    # the fixed-step rule QB replaces, on the loads of one micro-batch
+    counts = torch.full((q.E,), q.T * q.k // q.E, dtype=torch.int32, device="cuda")
+    counts[: q.E // 2] += 1
+    counts[q.E // 2:] -= 1
+    sbias = torch.zeros(q.E, device="cuda")
+    for _ in range(3):
+        lse.slmoe_signsgd_update(counts, q.E, 1e-3, sbias)
+    g0.record(stream)
+    for _ in range(reps):
+        lse.slmoe_signsgd_update(counts, q.E, 1e-3, sbias)
+    g1.record(stream)
+    torch.cuda.synchronize()
+    ts = g0.elapsed_time(g1) / reps * 1e-3
     qbytes = q.T * q.E * 4 + 2 * q.E * q.nbins * 4
     return {"GB/s": round(qbytes / tq / 1e9, 1), "frac_of_hbm": round(qbytes / tq / 1e9 / hbm, 4),
             "us_per_micro_batch": round(tq * 1e6, 2), "bytes": qbytes,
-            "update_us": round(tu * 1e6, 2),
+            "update_us": round(tu * 1e6, 2), "signsgd_update_us": round(ts * 1e6, 2),
             "engine_ms": round((q.micro_batches * tq + tu) * 1e3, 4),
             "note": "65536 x 896 fp32 scores per micro-batch (235 MB > L2); engine = 8 histograms + 1 update"}
 

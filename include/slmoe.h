@@ -236,6 +236,25 @@ SLMOE_API int slmoe_qb_update(const uint32_t *hist, int32_t E, int32_t nbins, in
                     float *q_out, float *bias, void *stream);
 
 /*
+ * slmoe_signsgd_update - the fixed-step bias update that QB replaces, kept as the
+ * comparison engine for it.  [K3-news] §02 (K2 balances without an auxiliary loss by moving
+ * each expert's selection bias, SignSGD-like, a fixed step up or down); [K3-arch]
+ * 负载均衡优化 (the SignSGD-style rule of K2, unstable at K3's expert count).  The pages
+ * print no formula; this library fixes it as:
+ *   N = sum_e counts[e];   bias[e] += step * sign(N - E * counts[e])
+ *   i.e. an expert loaded below the mean load N / E is raised by step, one above it is
+ *   lowered by step, one exactly at the mean is left as it is.  The sign is exact (int64);
+ *   the update is one fp32 add (round to nearest) per expert.
+ *   counts [E] int32: tokens routed to each expert since the last update (the counts of
+ *   slmoe_route, summed over micro-batches by the caller if wanted); bias [E] fp32, updated in
+ *   place; step > 0 and finite (the pages give no value).  E <= 65536.  One thread block; no
+ *   workspace.
+ * Errors: SLMOE_EINVAL on null or misaligned pointers, E outside [1, 65536], a step that is
+ *   not finite and positive.
+ */
+SLMOE_API int slmoe_signsgd_update(const int32_t *counts, int32_t E, float step, float *bias, void *stream);
+
+/*
  * slmoe_forward - one Stable LatentMoE layer (the FFN branch; the residual add is left to
  * the caller).  [K3-news] §01-§02, [K3-arch] SiTU激活优化 / 归一化策略调整,
  * [SLMoE] Latent-Space MoE.

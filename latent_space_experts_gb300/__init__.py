@@ -14,9 +14,9 @@ from . import _build
 
 __all__ = ["SlmoeError", "Config", "Weights", "WorkspaceLayout", "load", "build", "config",
            "weights", "slmoe_workspace_size", "slmoe_workspace_layout_get", "slmoe_route",
-           "slmoe_route_noalloc",
-           "slmoe_qb_histogram", "slmoe_qb_update", "slmoe_forward", "slmoe_device_sm_count",
-           "workspace_views", "slmoe_last_error", "slmoe_set_stage_events", "slmoe_launch_count", "F32", "BF16", "LIB_PATH"]
+           "slmoe_route_noalloc", "slmoe_qb_histogram", "slmoe_qb_update", "slmoe_signsgd_update",
+           "slmoe_forward", "slmoe_device_sm_count", "workspace_views", "slmoe_last_error",
+           "slmoe_set_stage_events", "slmoe_launch_count", "F32", "BF16", "LIB_PATH"]
 
 F32, BF16 = 0, 1
 LIB_PATH = _build.LIB
@@ -73,6 +73,7 @@ def load():
         "slmoe_route_noalloc": (ctypes.c_int, [CP, P, P, P, P, P, P, P, P, P, P, P, P, P, P]),
         "slmoe_qb_histogram": (ctypes.c_int, [P, I64, I32, I32, P, P, P]),
         "slmoe_qb_update": (ctypes.c_int, [P, I32, I32, I32, P, P, P]),
+        "slmoe_signsgd_update": (ctypes.c_int, [P, I32, ctypes.c_float, P, P]),
         "slmoe_forward": (ctypes.c_int, [CP, P, WP, P, P, P, P, P, P, P, SZ, P]),
         "slmoe_set_stage_events": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]),
         "slmoe_launch_count": (ctypes.c_longlong, []),
@@ -212,6 +213,10 @@ def slmoe_qb_histogram(scores, T, E, nbins, hist, status=None, stream=None):
 
 def slmoe_qb_update(hist, E, nbins, k, q_out, bias, stream=None):
     _check(load().slmoe_qb_update(_ptr(hist), E, nbins, k, _ptr(q_out), _ptr(bias), _stream(stream)))
+
+
+def slmoe_signsgd_update(counts, E, step, bias, stream=None):
+    _check(load().slmoe_signsgd_update(_ptr(counts), E, float(step), _ptr(bias), _stream(stream)))
 
 
 def slmoe_forward(cfg, x, w: Weights, bias, logit_offset, y, topk_idx_out, hist, status, workspace,

@@ -1,6 +1,7 @@
 // The C ABI of slmoe.h: argument validation, the workspace layout, and the sequencing of
 // the kernels of one call on the caller's stream.  Nothing here synchronises the host.
 #include <atomic>
+#include <cmath>
 #include <mutex>
 #include <cstdarg>
 #include <cstdio>
@@ -361,6 +362,16 @@ int slmoe_qb_update(const uint32_t *hist, int32_t E, int32_t nbins, int32_t k, f
     if (((uintptr_t)hist & 3u) || ((uintptr_t)bias & 3u) || ((uintptr_t)q_out & 3u))
         return fail(SLMOE_EINVAL, "hist, bias and q_out must be 4-byte aligned");
     return launch_qb_update(hist, E, nbins, k, q_out, bias, static_cast<cudaStream_t>(stream));
+}
+
+int slmoe_signsgd_update(const int32_t *counts, int32_t E, float step, float *bias, void *stream) {
+    g_err[0] = 0;
+    if (E < 1 || E > 65536) return fail(SLMOE_EINVAL, "E outside [1, 65536]");
+    if (!std::isfinite(step) || !(step > 0.0f)) return fail(SLMOE_EINVAL, "step must be finite and > 0");
+    if (!counts || !bias) return fail(SLMOE_EINVAL, "counts and bias are required");
+    if (((uintptr_t)counts & 3u) || ((uintptr_t)bias & 3u))
+        return fail(SLMOE_EINVAL, "counts and bias must be 4-byte aligned");
+    return launch_signsgd_update(counts, E, step, bias, static_cast<cudaStream_t>(stream));
 }
 
 int slmoe_forward(const slmoe_config *cfg, const void *x, const slmoe_weights *w,

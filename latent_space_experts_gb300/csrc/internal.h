@@ -77,6 +77,7 @@ int launch_qb_histogram(const float *scores, int64_t T, int E, int nbins, uint32
                         int32_t *status, cudaStream_t st);
 int launch_qb_update(const uint32_t *hist, int E, int nbins, int k, float *q_out, float *bias,
                      cudaStream_t st);
+int launch_signsgd_update(const int32_t *counts, int E, float step, float *bias, cudaStream_t st);
 
 // ---------------------------------------------------------------- combine + RMSNorm
 int launch_combine_rmsnorm(int dtype, const void *y_e, const float *topk_w,

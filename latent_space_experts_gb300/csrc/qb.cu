@@ -434,4 +434,42 @@ int launch_qb_update(const uint32_t *hist, int E, int nbins, int k, float *q_out
     return check_launch("qb_update");
 }
 
+// ---------------------------------------------------------------- fixed-step (SignSGD) update
+// The rule QB replaces ([K3-news] §02: K2 moves each expert's selection bias by a fixed step,
+// up or down): bias[e] += step * sign(N - E * counts[e]), N = sum of the counts, i.e. the sign
+// of (mean load - load of e), taken in exact int64 arithmetic; bias is left untouched where
+// the load equals the mean.  One block: the threads sum the counts (int64), then each updates
+// its experts with one fp32 add.
+constexpr int SG_THREADS = 1024;
+
+__global__ void __launch_bounds__(SG_THREADS) signsgd_update_kernel(const int32_t *__restrict__ counts, int E,
+                                                                    float step, float *__restrict__ bias) {
+    __shared__ long long wsum[SG_THREADS / 32];
+    __shared__ long long total;
+    long long acc = 0;
+    for (int e = threadIdx.x; e < E; e += SG_THREADS) acc += counts[e];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    if (lane == 0) wsum[w] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        long long t = 0;
+        for (int i = 0; i < SG_THREADS / 32; ++i) t += wsum[i];
+        total = t;
+    }
+    __syncthreads();
+    const long long N = total;
+    for (int e = threadIdx.x; e < E; e += SG_THREADS) {
+        const long long diff = N - (long long)E * counts[e];
+        if (diff > 0) bias[e] = __fadd_rn(bias[e], step);
+        else if (diff < 0) bias[e] = __fadd_rn(bias[e], -step);
+    }
+}
+
+int launch_signsgd_update(const int32_t *counts, int E, float step, float *bias, cudaStream_t st) {
+    signsgd_update_kernel<<<1, SG_THREADS, 0, st>>>(counts, E, step, bias);
+    return check_launch("signsgd_update");
+}
+
 }  // namespace slmoe

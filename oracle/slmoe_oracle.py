@@ -23,10 +23,13 @@ Readings where the pages are silent (all listed again in the design notes):
   * QB histograms bin the raw scores; the quantile is read by linear interpolation inside
     the bin that holds fractional rank r = (1 - k/E) * N; the update b_e <- mean(q) - q_e
     overwrites the bias.
+  * the K2 rule that QB replaces (fixed-step, SignSGD-like) moves b_e by +step when the
+    expert's load is below the mean load, by -step when above, not at all when equal.
 
-Parity pins live in ``tests/test_oracle_pins.py``.  Two quantities stay "parity unpinned"
-by the pages: the exact bias-update formula (the pages defer it to a technical report)
-and the balance that QB reaches on a given input.
+Parity pins live in ``tests/test_oracle_pins.py``.  Three quantities stay "parity unpinned"
+by the pages: the exact bias-update formula (the pages defer it to a technical report),
+the fixed-step size of the SignSGD-like rule, and the balance that either rule reaches on
+a given input.
 """
 from __future__ import annotations
 
@@ -271,6 +274,26 @@ def qb_update(hist, k):
     q = qb_quantile(hist, k)
     cbar = q.mean()
     return q, cbar - q
+
+
+def signsgd_update(counts, bias, step):
+    """The fixed-step bias update of K2 that QB replaces ([K3-news] §02: each expert's
+    selection bias moves a fixed step up or down; [K3-arch] 负载均衡优化: the SignSGD-style
+    rule).  With loads n_e and mean load N / E:  b_e + step if n_e < N / E, b_e - step if
+    n_e > N / E, b_e if equal.  The comparison is made on the integers N and E * n_e; the
+    sum is formed in fp64 (exact for fp32 operands within 29 binary orders of each other)
+    and stored as fp32, the type of the bias."""
+    n = np.asarray(counts, dtype=np.int64)
+    E = n.shape[0]
+    N = int(n.sum())
+    b = np.asarray(bias, dtype=np.float32).copy()
+    for e in range(E):
+        diff = N - E * int(n[e])
+        if diff > 0:
+            b[e] = np.float32(float(b[e]) + float(np.float32(step)))
+        elif diff < 0:
+            b[e] = np.float32(float(b[e]) - float(np.float32(step)))
+    return b
 
 
 def expert_output(inp, e, h):

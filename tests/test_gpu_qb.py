@@ -145,3 +145,69 @@ def test_qb_rebalances_k3_routing():
     r0, r1 = L0.max() / L0.mean(), L1.max() / L1.mean()
     print(f"max/mean load before QB {r0:.2f}, after {r1:.2f}")
     assert r1 < r0
+
+
+def signsgd_case(E, seed, big=False):
+    """Counts with an exact integer mean m that many experts hit exactly (zero-sum
+    deviations around m), so all three branches of the rule are taken; biases with -0.0."""
+    rng = np.random.default_rng(seed)
+    m = (1 << 28) if big else 3000
+    dev = np.zeros(E, np.int64)
+    half = rng.integers(-2000, 2001, size=E // 2)
+    half[rng.random(E // 2) < 0.3] = 0
+    dev[0:2 * (E // 2):2], dev[1:2 * (E // 2):2] = half, -half      # pairs +d, -d: sum 0
+    dev = rng.permutation(dev)
+    n = m + dev
+    assert n.min() >= 0 and n.max() < 2**31
+    b = rng.normal(scale=0.05, size=E).astype(np.float32)
+    b[::5] = -0.0
+    return n.astype(np.int32), b
+
+
+@pytest.mark.parametrize("E,big", [(1, False), (7, False), (896, False), (1000, False),
+                                   (8, True), (65536, False)])
+def test_signsgd_update_matches_the_oracle_bit_for_bit(E, big):
+    need_gpu()
+    n, b0 = signsgd_case(E, seed=E, big=big)
+    step = np.float32(1e-3)
+    counts = torch.from_numpy(n).cuda()
+    bias = torch.from_numpy(b0.copy()).cuda()
+    lse.slmoe_signsgd_update(counts, E, float(step), bias)
+    ref = oracle.signsgd_update(n, b0, step)
+    assert np.array_equal(bias.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    moved = (bias.cpu().numpy().view(np.uint32) != b0.view(np.uint32)).sum()
+    assert moved == int((n.astype(np.int64) * E != int(n.astype(np.int64).sum())).sum())
+
+
+def test_signsgd_loop_on_k3_micro_batches_follows_the_oracle():
+    """Eight micro-batches of K3-shaped scores (E = 896, k = 16): each is routed with the
+    current bias (top-k on the host, test infrastructure), its loads feed one fixed-step
+    update on the GPU, and the GPU bias follows the oracle's bit for bit.  On a held-out
+    micro-batch the max/mean load is reported for no balancing, the fixed-step rule and QB
+    (one update from the same eight histograms); the pages fix no target value."""
+    need_gpu()
+    q = synthetic.QB
+    T, step = 8192, np.float32(1e-3)
+    bias_g = torch.zeros(q.E, device="cuda")
+    bias_o = np.zeros(q.E, np.float32)
+    hist = torch.zeros(q.E, q.nbins, dtype=torch.int32, device="cuda")
+    for m in range(q.micro_batches):
+        sc = synthetic.qb_scores(m, q, device="cuda", T=T)
+        gpu_hist(sc, q.nbins, hist)
+        sel, _, _ = oracle.select_topk(sc.cpu().numpy(), bias_o, q.k)
+        L = oracle.expert_loads(sel, q.E).astype(np.int32)
+        assert L.sum() == T * q.k
+        lse.slmoe_signsgd_update(torch.from_numpy(L).cuda(), q.E, float(step), bias_g)
+        bias_o = oracle.signsgd_update(L, bias_o, step)
+        assert np.array_equal(bias_g.cpu().numpy().view(np.uint32), bias_o.view(np.uint32)), m
+    qbias = torch.empty(q.E, device="cuda")
+    lse.slmoe_qb_update(hist, q.E, q.nbins, q.k, None, qbias)
+    held = synthetic.qb_scores(q.micro_batches, q, device="cuda", T=T).cpu().numpy()
+    ratios = {}
+    for name, b in (("none", np.zeros(q.E)), ("fixed step", bias_o), ("QB", qbias.cpu().numpy())):
+        sel, _, _ = oracle.select_topk(held, b, q.k)
+        L = oracle.expert_loads(sel, q.E)
+        assert L.sum() == T * q.k
+        ratios[name] = L.max() / L.mean()
+    print("max/mean load on a held-out micro-batch:", {k: round(v, 2) for k, v in ratios.items()})
+    assert ratios["QB"] < ratios["none"]

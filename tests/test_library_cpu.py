@@ -91,3 +91,20 @@ def test_null_and_misaligned_arguments_fail_before_launch(lib):
     rc = lib.slmoe_forward(ctypes.byref(cfg), fake, ctypes.byref(w), fake, None, fake, None, None,
                            None, fake, n, None)
     assert rc == -1 and "W_r" in lib.slmoe_last_error().decode()
+
+
+@pytest.mark.parametrize("E,step", [(0, 1e-3), (65537, 1e-3), (4, 0.0), (4, -1e-3),
+                                    (4, float("inf")), (4, float("nan"))])
+def test_signsgd_update_rejects_bad_arguments(lib, E, step):
+    fake = ctypes.c_void_p(1 << 20)                 # never dereferenced: validation fails first
+    assert lib.slmoe_signsgd_update(fake, E, step, fake, None) == -1
+    assert lib.slmoe_last_error().decode() != ""
+
+
+def test_signsgd_update_rejects_null_and_misaligned_pointers(lib):
+    fake = ctypes.c_void_p(1 << 20)
+    mis = ctypes.c_void_p((1 << 20) + 2)
+    assert lib.slmoe_signsgd_update(None, 4, 1e-3, fake, None) == -1
+    assert lib.slmoe_signsgd_update(fake, 4, 1e-3, None, None) == -1
+    assert lib.slmoe_signsgd_update(mis, 4, 1e-3, fake, None) == -1
+    assert "aligned" in lib.slmoe_last_error().decode()

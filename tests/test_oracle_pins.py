@@ -363,3 +363,73 @@ def test_qb_rebalances_loads():
     L1 = oracle.expert_loads(sel1, E)
     assert L0.sum() == L1.sum() == 20000 * k
     assert L1.max() / L1.mean() < 0.5 * (L0.max() / L0.mean())
+
+
+# ---------------------------------------------------------------- fixed-step (SignSGD) rule
+def test_signsgd_hand_cases():
+    """[K3-news] §02: K2 raises or lowers each expert's selection bias by a fixed step."""
+    step = np.float32(1e-3)
+    b = oracle.signsgd_update([3, 1, 2], np.zeros(3, np.float32), step)    # mean 2
+    assert b.tolist() == [-step, step, 0.0]
+    b = oracle.signsgd_update([1, 2], np.array([0.5, 0.5], np.float32), 0.25)   # mean 1.5
+    assert b.tolist() == [0.75, 0.25]
+    b = oracle.signsgd_update([0, 0, 0, 9], np.array([0, 0, 0, 0], np.float32), 0.5)
+    assert b.tolist() == [0.5, 0.5, 0.5, -0.5]
+    neg0 = np.array([-0.0, 1.0], np.float32)
+    b = oracle.signsgd_update([5, 5], neg0, 0.5)                           # every load at the mean
+    assert np.array_equal(b.view(np.uint32), neg0.view(np.uint32))
+
+
+def test_signsgd_sign_rule_and_step_against_exact_arithmetic():
+    """The direction is decided by exact rational comparison with the mean load, and each
+    moved bias equals the fp32 round-to-nearest sum of the old bias and +-step."""
+    from fractions import Fraction
+    rng = np.random.default_rng(11)
+    for E in (1, 2, 7, 64, 897):
+        n = rng.integers(0, 40, size=E)
+        if E > 2:
+            n[: E // 3] = int(round(n.mean()))                   # many loads near the mean
+        b0 = rng.normal(scale=0.05, size=E).astype(np.float32)
+        step = np.float32(rng.uniform(1e-4, 1e-2))
+        b1 = oracle.signsgd_update(n, b0, step)
+        mean = Fraction(int(n.sum()), E)
+        for e in range(E):
+            if Fraction(int(n[e])) < mean:
+                want = np.float32(b0[e]) + step                   # numpy fp32 add (IEEE RN)
+            elif Fraction(int(n[e])) > mean:
+                want = np.float32(b0[e]) - step
+            else:
+                want = b0[e]
+            assert b1[e].view(np.uint32) == np.float32(want).view(np.uint32), e
+
+
+def test_signsgd_needs_many_steps_where_qb_needs_one():
+    """[K3-news] §02 / [K3-arch] 负载均衡优化: the fixed-step rule probes its way to balance,
+    QB reads the thresholds from the score distribution in one update.  On a skewed router
+    one fixed step of 1e-3 leaves the imbalance almost unchanged, QB halves it at once, and
+    repeated fixed steps keep shrinking it (the step size itself is the caller's: the pages
+    give none)."""
+    E, k = 64, 4
+    rng = np.random.default_rng(7)
+    mu = rng.normal(scale=0.5, size=E)
+    s = (1 / (1 + np.exp(-(rng.normal(size=(20000, E)) + mu)))).astype(np.float32)
+
+    def imbalance(bias):
+        sel, _, _ = oracle.select_topk(s, bias, k)
+        L = oracle.expert_loads(sel, E)
+        assert L.sum() == 20000 * k
+        return L.max() / L.mean(), L
+
+    r0, L0 = imbalance(np.zeros(E))
+    b = oracle.signsgd_update(L0, np.zeros(E, np.float32), 1e-3)
+    r1, _ = imbalance(b)
+    _, bq = oracle.qb_update(oracle.qb_histogram(s), k)
+    rq, _ = imbalance(bq)
+    assert r1 > 0.9 * r0 and rq < 0.5 * r0
+    b = np.zeros(E, np.float32)
+    for _ in range(60):
+        _, L = imbalance(b)
+        b = oracle.signsgd_update(L, b, 1e-2)
+    r60, _ = imbalance(b)
+    assert r60 < 0.75 * r0
+
