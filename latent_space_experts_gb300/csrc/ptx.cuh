@@ -67,6 +67,16 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t *b, uint32_t parity) {
         if ((it & 255u) == 0 && gtimer() - t0 > WAIT_LIMIT_NS) return false;
     }
 }
+// After an abort: wait (bounded) for the last fill of every stage of a TMA ring whose producer
+// stopped at ring position (stage, phase), so that no copy lands in shared memory after the
+// block has exited.  Stages below `stage` were last filled in the current lap (parity phase),
+// the others in the lap before (parity phase ^ 1), if the ring has wrapped at least once.
+__device__ __forceinline__ void drain_ring(uint64_t *full, int stages, int stage, uint32_t phase, bool wrapped) {
+    for (int i = 0; i < stages; ++i) {
+        if (i < stage) mbar_wait_drain(&full[i], phase);
+        else if (wrapped) mbar_wait_drain(&full[i], phase ^ 1);
+    }
+}
 // 2-D tiled TMA load of one box at (c0 = innermost, c1) into shared memory; completion is
 // counted in bytes on the mbarrier.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint64_t *bar,

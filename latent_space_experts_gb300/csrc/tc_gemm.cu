@@ -206,11 +206,15 @@ __global__ void __launch_bounds__(DenseCfg<BN, EPI, PACC>::THREADS, 1) dense_ker
     uint64_t *tempty = tfull + 2;
     uint64_t *tq_full = tempty + 2;
     uint64_t *tq_empty = tq_full + TQ;
-    int *tq_ids = reinterpret_cast<int *>(tq_empty + TQ);
+    uint64_t *mma_drain = tq_empty + TQ;
+    int *tq_ids = reinterpret_cast<int *>(mma_drain + 1);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tq_ids + TQ);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int p_stage = 0;                  // the TMA producer's ring position, kept for the drain
+    uint32_t p_phase = 0;
+    bool p_wrapped = false;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
@@ -220,6 +224,7 @@ __global__ void __launch_bounds__(DenseCfg<BN, EPI, PACC>::THREADS, 1) dense_ker
             mbar_init(&tfull[b], 1);
             mbar_init(&tempty[b], Cfg::EPI_WARPS);
         }
+        mbar_init(mma_drain, 1);
         for (int q = 0; q < TQ; ++q) {
             mbar_init(&tq_full[q], 1);
             mbar_init(&tq_empty[q], 1 + Cfg::EPI_WARPS);
@@ -235,8 +240,8 @@ __global__ void __launch_bounds__(DenseCfg<BN, EPI, PACC>::THREADS, 1) dense_ker
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer
-        int stage = 0;
-        uint32_t phase = 0;
+        int &stage = p_stage;
+        uint32_t &phase = p_phase;
         int qs = 0, it = 0;
         uint32_t qp = 0;
         for (;;) {
@@ -263,7 +268,7 @@ __global__ void __launch_bounds__(DenseCfg<BN, EPI, PACC>::THREADS, 1) dense_ker
                     } else {
                         tma_load_2d(sb, &maps.b[s], &full[stage], kb * Cfg::BK, n0);
                     }
-                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; p_wrapped = true; }
                 }
             }
         }
@@ -409,6 +414,14 @@ __global__ void __launch_bounds__(DenseCfg<BN, EPI, PACC>::THREADS, 1) dense_ker
     }
 done:
     __syncthreads();
+    if (*abort_flag) {   // every role has stopped: let copies and MMAs in flight finish
+        if (warp == 0 && lane == 0) drain_ring(full, STAGES, p_stage, p_phase, p_wrapped);
+        if (warp == 1 && lane == 0) {
+            umma_commit(mma_drain);
+            mbar_wait_drain(mma_drain, 0);
+        }
+        __syncthreads();
+    }
     if (warp == 1) {
         tc_after();
         tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
@@ -452,12 +465,14 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_kernel(const __grid_cons
     uint64_t *tempty = tfull + 2;
     uint64_t *tq_full = tempty + 2;
     uint64_t *tq_empty = tq_full + TQ;
-    int *tq_ids = reinterpret_cast<int *>(tq_empty + TQ);
+    uint64_t *mma_drain = tq_empty + TQ;
+    int *tq_ids = reinterpret_cast<int *>(mma_drain + 1);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tq_ids + TQ);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
+        mbar_init(mma_drain, 1);
         for (int s = 0; s < RT_STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
@@ -484,25 +499,28 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_kernel(const __grid_cons
     if (warp == 0 && lane == 0) {
         int stage = 0;
         uint32_t phase = 0;
+        bool wrapped = false;
         int qs = 0, it = 0;
         uint32_t qp = 0;
         for (;;) {
             const int tile = a.counter ? atomicAdd(a.counter, 1) : (int)blockIdx.x + (it++) * (int)gridDim.x;
-            if (!tq_push(tq_ids, tq_full, tq_empty, qs, qp, tile, abort_flag)) goto done;
+            if (!tq_push(tq_ids, tq_full, tq_empty, qs, qp, tile, abort_flag)) goto producer_out;
             if (tile >= a.tiles) break;
             const int m0 = (tile / a.tiles_n) * 128;
             const int n0 = (tile % a.tiles_n) * RT_BN;
             for (int s = 0; s < a.nseg; ++s) {
                 for (int kb = 0; kb < a.kblocks[s]; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) goto done;
+                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) goto producer_out;
                     mbar_expect_tx(&full[stage], RT_STAGE);
                     const uint32_t sa = su32(smem + stage * RT_STAGE);
                     tma_load_2d(sa, &maps.a[s], &full[stage], kb * 64, m0);
                     tma_load_2d(sa + 128 * 128, &maps.b[s], &full[stage], kb * 64, n0);
-                    if (++stage == RT_STAGES) { stage = 0; phase ^= 1; }
+                    if (++stage == RT_STAGES) { stage = 0; phase ^= 1; wrapped = true; }
                 }
             }
         }
+    producer_out:   // wait (bounded) until every copy issued has landed
+        drain_ring(full, RT_STAGES, stage, phase, wrapped);
     } else if (warp == 1 && lane == 0) {
         constexpr uint32_t IDESC = idesc_bf16(128, RT_BN);
         int stage = 0;
@@ -513,17 +531,17 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_kernel(const __grid_cons
         uint32_t qp = 0;
         for (;;) {
             int tile;
-            if (!tq_pop(tq_ids, tq_full, tq_empty, qs, qp, tile, abort_flag, false)) goto done;
+            if (!tq_pop(tq_ids, tq_full, tq_empty, qs, qp, tile, abort_flag, false)) goto mma_out;
             if (tile >= a.tiles) break;
             int kg = 0;
             for (int s = 0; s < a.nseg; ++s) {
                 for (int kb = 0; kb < a.kblocks[s]; ++kb, ++kg) {
                     const bool first = (kg % RT_DRAIN) == 0;
                     if (first) {
-                        if (!mbar_wait(&tempty[buf], bphase ^ 1, abort_flag)) goto done;
+                        if (!mbar_wait(&tempty[buf], bphase ^ 1, abort_flag)) goto mma_out;
                         tc_after();
                     }
-                    if (!mbar_wait(&full[stage], phase, abort_flag)) goto done;
+                    if (!mbar_wait(&full[stage], phase, abort_flag)) goto mma_out;
                     tc_after();
                     const uint32_t d = tmem_base + buf * 256;
                     const uint32_t sa = su32(smem + stage * RT_STAGE);
@@ -540,6 +558,9 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_kernel(const __grid_cons
                 }
             }
         }
+    mma_out:        // wait (bounded) until every MMA issued has finished
+        umma_commit(mma_drain);
+        mbar_wait_drain(mma_drain, 0);
     } else if (warp >= 2) {
         const int q = warp & 3;
         const int half = (warp - 2) >> 2;             // column half drained by this warp
@@ -773,11 +794,16 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
     uint64_t *b_empty = b_full + BST;
     uint64_t *tfull = b_empty + BST;
     uint64_t *tempty = tfull + NBUF;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + NBUF);
+    uint64_t *mma_drain = tempty + NBUF;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int p_stage = 0;                  // the weight producer's ring position, kept for the drain
+    uint32_t p_phase = 0;
+    bool p_wrapped = false;
     if (threadIdx.x == 0) {
+        mbar_init(mma_drain, 1);
         for (int s = 0; s < G_TQ; ++s) {
             mbar_init(&q_full[s], 1);
             mbar_init(&q_empty[s], 1 + Cfg::EPI_WARPS + 4);  // MMA thread, epilogue and gather warps
@@ -821,8 +847,10 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
         // ------------------------------------------------ item fetch + weights by TMA
         const uint64_t pol_first = policy_evict_first();
         const int n_items = *a.n_items;
-        int stage = 0, qs = 0;
-        uint32_t phase = 0, qp = 0;
+        int &stage = p_stage;
+        uint32_t &phase = p_phase;
+        int qs = 0;
+        uint32_t qp = 0;
         for (;;) {
             const int idx = atomicAdd(a.counter, 1);
             const int4 it = idx < n_items ? a.items[idx] : make_int4(0, 0, 0, -1);
@@ -845,7 +873,7 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
                     tma_load_2d_hint(sa, &wmap, &a_full[stage], kb * 64, row0, pol_first);
                     tma_load_2d_hint(sa + 128 * 128, &wmap, &a_full[stage], kb * 64, row0 + a.a_sub1, pol_first);
                 }
-                if (++stage == AST) { stage = 0; phase ^= 1; }
+                if (++stage == AST) { stage = 0; phase ^= 1; p_wrapped = true; }
             }
         }
     } else if (warp == 1 && lane == 0) {
@@ -987,6 +1015,16 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
     }
 done:
     __syncthreads();
+    if (*abort_flag) {   // every role has stopped: let copies and MMAs in flight finish
+        if (warp == 0 && lane == 0) {
+            drain_ring(a_full, AST, p_stage, p_phase, p_wrapped);
+        }
+        if (warp == 1 && lane == 0) {
+            umma_commit(mma_drain);
+            mbar_wait_drain(mma_drain, 0);
+        }
+        __syncthreads();
+    }
     if (warp == 1) {
         tc_after();
         tmem_dealloc(tmem_base, 512);
@@ -1080,6 +1118,8 @@ int tc_router_scores(const slmoe_config *c, const void *x, const float *W_r, con
     a.tiles_n = (a.N + RT_BN - 1) / RT_BN;
     a.tiles = ((a.M + 127) / 128) * a.tiles_n;
     if (a.tiles == 0) return SLMOE_OK;
+    for (int s = 1; s < a.nseg; ++s)
+        if (a.kblocks[s] != a.kblocks[0]) return fail(SLMOE_EINVAL, "router pieces differ in K");
     if ((rc = set_smem(router_kernel, RT_SMEM))) return rc;
     const int sms = sm_count();
     router_kernel<<<a.tiles < sms ? a.tiles : sms, RT_THREADS, RT_SMEM, st>>>(maps, a);
