@@ -108,3 +108,12 @@ def test_signsgd_update_rejects_null_and_misaligned_pointers(lib):
     assert lib.slmoe_signsgd_update(fake, 4, 1e-3, None, None) == -1
     assert lib.slmoe_signsgd_update(mis, 4, 1e-3, fake, None) == -1
     assert "aligned" in lib.slmoe_last_error().decode()
+
+
+def test_empty_batch_forward_returns_before_any_cuda_call(lib):
+    """T = 0: nothing to compute, so slmoe_forward succeeds without touching its pointers."""
+    cfg = lse.config(synthetic.shape_with("mid", T=0))
+    w = lse.Weights()
+    rc = lib.slmoe_forward(ctypes.byref(cfg), None, ctypes.byref(w), None, None, None, None, None,
+                           None, None, 0, None)
+    assert rc == 0
