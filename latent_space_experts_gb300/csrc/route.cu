@@ -16,7 +16,6 @@ namespace slmoe {
 namespace {
 
 constexpr int TOPK_MAX_WARPS = 16;    // one token per warp when shared memory allows
-constexpr int MAX_E = 4096;
 constexpr int LIST = 4;              // candidates each lane keeps in registers
 
 __device__ __forceinline__ bool beats(float v, int i, float w, int j) {

@@ -38,18 +38,14 @@
 namespace slmoe {
 namespace {
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 // Arrive on the mbarrier once all of this thread's earlier cp.async copies have landed;
 // the barrier's expected count includes this arrival (noinc).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(su32(bar)) : "memory");
 }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+// Wait for every cp.async this thread has issued, committed to a group or not (the gather
+// copies are tracked by mbarrier arrivals, not by groups, so a group wait would miss them).
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(slot)),
                  "r"(ncols)
@@ -978,7 +974,7 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
         for (;;) {
             int4 it;
             if (!pop(qs, qp, it, true)) {
-                cp_async_wait<0>();
+                cp_async_wait_all();
                 goto done;
             }
             if (it.w < 0) break;
@@ -994,7 +990,7 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
             }
             for (int kb = 0; kb < a.kblocks; ++kb) {
                 if (!mbar_wait(&b_empty[stage], phase ^ 1, abort_flag)) {
-                    cp_async_wait<0>();
+                    cp_async_wait_all();
                     goto done;
                 }
                 const uint32_t sb = su32(sB + stage * Cfg::B_BYTES);
@@ -1011,7 +1007,7 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
                 if (++stage == BST) { stage = 0; phase ^= 1; }
             }
         }
-        cp_async_wait<0>();
+        cp_async_wait_all();
     }
 done:
     __syncthreads();
