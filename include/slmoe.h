@@ -185,8 +185,8 @@ SLMOE_API int slmoe_route(const slmoe_config *cfg, const void *x, const float *W
  * given) accumulates as in slmoe_route, so the caller zeroes it.
  *
  * Set-up: the first call on each device looks up the scratch's device address with that
- * device current (cudaGetSymbolAddress) and keeps it; make that first call before any
- * stream capture.  Later calls on the device reuse the address.
+ * device current (cudaGetSymbolAddress) and keeps it; later calls on the device reuse the
+ * address.
  *
  * Overlap: there is one scratch per device, shared by every call on that device.  Two calls
  * that can run at the same time on one device (different streams not ordered by events, or
