@@ -186,7 +186,8 @@ struct DenseCfg {
     static constexpr int EPI_WARPS = 4 * MSUB;
     static constexpr int THREADS = (2 + EPI_WARPS) * 32;  // TMA, MMA, epilogue
     static constexpr int SMEM = STAGES * STAGE + 1024 + 256;
-    static_assert(TMEM_COLS == 512 && STAGES >= 3, "dense tile shape");
+    static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0 && TMEM_COLS >= 32 && TMEM_COLS <= 512 && STAGES >= 3,
+                  "dense tile shape");
 };
 
 template <int BN, int EPI, int PACC>
@@ -1077,6 +1078,21 @@ int launch_dense(const TmaPack &maps, DenseArgs a, cudaStream_t st) {
     return check_launch("dense_kernel");
 }
 
+// Weight-tile width of a dense GEMM: 256 rows, except for a batch of one row tile (decode),
+// where the GEMM is bound by its weight reads and 64-row tiles spread them over four times as
+// many SMs.  (Larger batches keep the wide tiles even when they do not fill the SMs: with
+// 4096 tokens the narrow tiles were 40 % slower.)
+int dense_bn(long long M, long long n_out, bool glu) {
+    const long long wide_out = glu ? 128 : 256;
+    const long long tiles = ((M + 255) / 256) * ((n_out + wide_out - 1) / wide_out);
+    return (M <= 256 && tiles < sm_count()) ? 64 : 256;
+}
+
+template <int EPI>
+int launch_dense_bn(int bn, const TmaPack &maps, const DenseArgs &a, cudaStream_t st) {
+    return bn == 64 ? launch_dense<64, EPI, 1>(maps, a, st) : launch_dense<256, EPI, 1>(maps, a, st);
+}
+
 template <int EPI, bool DBUF>
 int launch_grouped(const CUtensorMap &wmap, const GroupedArgs &a, cudaStream_t st) {
     auto kern = grouped_kernel<EPI, DBUF>;
@@ -1131,26 +1147,29 @@ int tc_forward_front(const slmoe_config *c, const void *x, const slmoe_weights *
     {   // latent down-projection: x_lat = x W_in^T
         TmaPack maps;
         memset(&maps, 0, sizeof(maps));
+        const int bn = dense_bn(T, dl, false);
         if ((rc = make_map(&maps.a[0], x, T, d, d, 128))) return rc;
-        if ((rc = make_map(&maps.b[0], w->W_in, dl, d, d, 256))) return rc;
+        if ((rc = make_map(&maps.b[0], w->W_in, dl, d, d, bn))) return rc;
         DenseArgs a = {};
         a.M = T; a.N = dl; a.nseg = 1; a.kblocks[0] = (d + 63) / 64;
         a.C = f.x_lat; a.ldc = dl; a.status = f.status; a.counter = f.counters + 1;
-        if ((rc = launch_dense<256, EPI_BF16, 1>(maps, a, st))) return rc;
+        if ((rc = launch_dense_bn<EPI_BF16>(bn, maps, a, st))) return rc;
     }
     stage_event(3, st);
+    const int bn_s = dense_bn(T, Is, true);
     for (int s = 0; s < ns; ++s) {   // shared experts, gate|up + SiTU-GLU on full d
         TmaPack maps;
         memset(&maps, 0, sizeof(maps));
         if ((rc = make_map(&maps.a[0], x, T, d, d, 128))) return rc;
+        // the weight tile is bn_s / 2 gate rows and bn_s / 2 up rows, loaded as two boxes
         if ((rc = make_map(&maps.b[0], static_cast<const bf *>(w->W13_s) + (size_t)s * 2 * Is * d, 2 * Is, d, d,
-                           128)))
+                           bn_s / 2)))
             return rc;
         DenseArgs a = {};
         a.M = T; a.N = Is; a.nseg = 1; a.kblocks[0] = (d + 63) / 64; a.glu_up_row = Is;
         a.C = static_cast<bf *>(f.h_s) + (size_t)s * Is; a.ldc = (long long)ns * Is;
         a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status; a.counter = f.counters + 2 + s;
-        if ((rc = launch_dense<256, EPI_GLU, 1>(maps, a, st))) return rc;
+        if ((rc = launch_dense_bn<EPI_GLU>(bn_s, maps, a, st))) return rc;
     }
     stage_event(7, st);
     return SLMOE_OK;
@@ -1213,20 +1232,21 @@ int tc_forward_back(const slmoe_config *c, const slmoe_weights *w, const TcForwa
         memset(&maps, 0, sizeof(maps));
         DenseArgs a = {};
         a.M = T; a.N = d; a.nseg = 1 + ns;
+        const int bn = dense_bn(T, d, false);
         if ((rc = make_map(&maps.a[0], f.z, T, dl, dl, 128))) return rc;
-        if ((rc = make_map(&maps.b[0], w->W_out, d, dl, dl, 256))) return rc;
+        if ((rc = make_map(&maps.b[0], w->W_out, d, dl, dl, bn))) return rc;
         a.kblocks[0] = (dl + 63) / 64;
         for (int s = 0; s < ns; ++s) {
             if ((rc = make_map(&maps.a[1 + s], static_cast<const bf *>(f.h_s) + (size_t)s * Is, T, Is,
                                (long long)ns * Is, 128)))
                 return rc;
             if ((rc = make_map(&maps.b[1 + s], static_cast<const bf *>(w->W2_s) + (size_t)s * d * Is, d, Is, Is,
-                               256)))
+                               bn)))
                 return rc;
             a.kblocks[1 + s] = (Is + 63) / 64;
         }
         a.C = y; a.ldc = d; a.status = f.status; a.counter = f.counters + 5;
-        if ((rc = launch_dense<256, EPI_F32, 1>(maps, a, st))) return rc;
+        if ((rc = launch_dense_bn<EPI_F32>(bn, maps, a, st))) return rc;
     }
     stage_event(8, st);
     return SLMOE_OK;

@@ -152,6 +152,21 @@ def test_identical_experts_reduce_to_dense_on_gpu():
     assert_close_rms(y, ref["y"], BF16_TOL, "y")
 
 
+def test_forward_wide_dense_tiles_with_ragged_rows():
+    """The 256-wide weight tiles of the dense GEMMs with a ragged last row tile (10000 = 39 * 256
+    + 16) and several waves of tiles: sampled tokens, including the last rows, against the
+    oracle.  (Batches of one row tile take the 64-wide tiles: the decode-sized tests.)"""
+    need_gpu()
+    shp = synthetic.shape_with("mid", T=10000)
+    inp = synthetic.layer_inputs(shp, seed=6, device="cuda")
+    y, topk, views = run_forward(shp, inp)
+    tok = np.unique(np.concatenate([np.arange(shp.T - 20, shp.T),
+                                    np.random.default_rng(2).choice(shp.T, 60, replace=False)]))
+    ref = oracle.forward(inp, shp.k, forced_topk_idx=topk, tokens=tok)
+    assert_close_rms(y[torch.as_tensor(tok, device="cuda")], ref["y"], BF16_TOL, "y")
+    assert_close_rms(views["z"][torch.as_tensor(tok, device="cuda")], ref["z"], BF16_TOL, "z", BF16_STORE)
+
+
 def _k3_sampled(name, heavy_skew, n_tok):
     shp = synthetic.LAYERS[name]
     inp = synthetic.layer_inputs(shp, seed=0, device="cuda", heavy_skew=heavy_skew)
