@@ -107,6 +107,8 @@ int make_layout(const slmoe_config *c, Layout *L) {
         L->items1 = take(nfb1 * (E + (Tk + GROUPED_PASS - 1) / GROUPED_PASS) * 16);
         L->items2 = take(nfb2 * (E + (Tk + GROUPED_PASS - 1) / GROUPED_PASS) * 16);
     }
+    if (c->dtype == SLMOE_BF16 && T <= (size_t)ROUTER_SPLITK_MAX_M)
+        L->rt_split = take(ROUTER_SPLITK_MAX * T * E * 4);
     L->pub.total = off;
     return SLMOE_OK;
 }
@@ -167,7 +169,8 @@ static int route_impl(const slmoe_config *c, const Layout &L, char *ws, const vo
     int rc;
     if (c->dtype == SLMOE_BF16) {
         rc = tc_router_scores(c, x, W_r, mu, reinterpret_cast<__nv_bfloat16 *>(ws + L.wr_split),
-                              R.scores, status, R.counters, st);
+                              R.scores, status, R.counters,
+                              L.rt_split ? reinterpret_cast<float *>(ws + L.rt_split) : nullptr, st);
     } else {
         SimtGemm g = {};
         g.seg[0] = {x, W_r, c->d, c->d, c->d, 0};
@@ -538,8 +541,10 @@ extern "C" int slmoe_route_noalloc(const slmoe_config *cfg, const void *x, const
                     S.total, (size_t)SLMOE_ROUTE_NOALLOC_SCRATCH_BYTES);
     char *scr = nullptr;
     if ((rc = route_scratch(&scr))) return rc;
-    // route_impl reads the split router weights at ws + L.wr_split
+    // route_impl reads the split router weights at ws + L.wr_split; the fixed scratch holds no
+    // split-K router sums, so the router runs unsplit here
     L.wr_split = S.wr_split;
+    L.rt_split = 0;
     Routing R = {scores ? scores : reinterpret_cast<float *>(scr + S.scores), topk_idx, topk_w,
                  counts, offsets, perm, slot_pos, reinterpret_cast<int32_t *>(scr + S.chunk_counts),
                  reinterpret_cast<int *>(scr + S.counters)};

@@ -25,6 +25,7 @@ struct Layout {
     size_t wr_split;       // bf16 [3, E, d]: router weight split hi / mid / lo
     size_t counters;       // int32 [16]: tile counters of the dynamically scheduled kernels
     size_t items1, items2; // int4 work lists of the routed-expert GEMMs (bf16 type)
+    size_t rt_split;       // fp32 split-K logit sums of the router (bf16 type, small batches)
     size_t nchunks;
 };
 int make_layout(const slmoe_config *cfg, Layout *L);
@@ -71,6 +72,10 @@ constexpr int ROUTE_CHUNK = 16;  // tokens per top-k block / permutation chunk
 // Tokens per pass of the routed-expert GEMMs: an expert with n tokens makes ceil(n / pass)
 // work items per feature block, which also sizes the work lists in the workspace.
 constexpr int GROUPED_PASS = 192;
+// The router of a batch of at most ROUTER_SPLITK_MAX_M tokens splits its K blocks over up to
+// ROUTER_SPLITK_MAX CTAs per tile (their fp32 partial logits live in the workspace).
+constexpr int ROUTER_SPLITK_MAX_M = 256;
+constexpr int ROUTER_SPLITK_MAX = 16;
 
 // ---------------------------------------------------------------- QB
 int launch_qb_histogram(const float *scores, int64_t T, int E, int nbins, uint32_t *hist,

@@ -147,6 +147,11 @@ struct DenseArgs {
     float beta1, beta2;
     int32_t *status;
     int *counter;          // nullable: global tile counter (zeroed) for dynamic scheduling
+    // router split K: tile t covers output tile t % tiles_mn and the K blocks of split
+    // t / tiles_mn of ksplit; the raw fp32 sums go to partial[split][row][col] (row stride ldp)
+    int ksplit, tiles_mn;
+    float *partial;
+    long long ldp;
 };
 
 // Tile order of the dense kernel: bands of DENSE_BAND row tiles, rows fastest inside a band,
@@ -452,6 +457,23 @@ __device__ __forceinline__ void drain_add(uint32_t taddr, float *acc) {
         for (int i = 0; i < 16; ++i) acc[16 * b + i] += __uint_as_float(r[b][i]);
 }
 
+// Output tile and K range (global K blocks [g0, g1) over the three pieces) of a router tile
+// id; with SPLIT, tile t covers output tile t % tiles_mn and split t / tiles_mn of ksplit.
+template <bool SPLIT>
+__device__ __forceinline__ void router_tile(const DenseArgs &a, int tile, int ktot, int &m0, int &n0, int &g0,
+                                            int &g1) {
+    int mn = tile, ks = 0;
+    if (SPLIT) {
+        ks = tile / a.tiles_mn;
+        mn = tile - ks * a.tiles_mn;
+    }
+    m0 = (mn / a.tiles_n) * 128;
+    n0 = (mn % a.tiles_n) * RT_BN;
+    g0 = SPLIT ? (int)((long long)ks * ktot / a.ksplit) : 0;
+    g1 = SPLIT ? (int)((long long)(ks + 1) * ktot / a.ksplit) : ktot;
+}
+
+template <bool SPLIT>
 __global__ void __launch_bounds__(RT_THREADS, 1) router_kernel(const __grid_constant__ TmaPack maps,
                                                                const DenseArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -503,10 +525,11 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_kernel(const __grid_cons
             const int tile = a.counter ? atomicAdd(a.counter, 1) : (int)blockIdx.x + (it++) * (int)gridDim.x;
             if (!tq_push(tq_ids, tq_full, tq_empty, qs, qp, tile, abort_flag)) goto producer_out;
             if (tile >= a.tiles) break;
-            const int m0 = (tile / a.tiles_n) * 128;
-            const int n0 = (tile % a.tiles_n) * RT_BN;
-            for (int s = 0; s < a.nseg; ++s) {
-                for (int kb = 0; kb < a.kblocks[s]; ++kb) {
+            int m0, n0, g0, g1;
+            router_tile<SPLIT>(a, tile, ktot, m0, n0, g0, g1);
+            for (int s = 0, g = 0; s < a.nseg; ++s) {
+                for (int kb = 0; kb < a.kblocks[s]; ++kb, ++g) {
+                    if (SPLIT && (g < g0 || g >= g1)) continue;
                     if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) goto producer_out;
                     mbar_expect_tx(&full[stage], RT_STAGE);
                     const uint32_t sa = su32(smem + stage * RT_STAGE);
@@ -530,9 +553,13 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_kernel(const __grid_cons
             int tile;
             if (!tq_pop(tq_ids, tq_full, tq_empty, qs, qp, tile, abort_flag, false)) goto mma_out;
             if (tile >= a.tiles) break;
-            int kg = 0;
-            for (int s = 0; s < a.nseg; ++s) {
-                for (int kb = 0; kb < a.kblocks[s]; ++kb, ++kg) {
+            int m0, n0, g0, g1;
+            router_tile<SPLIT>(a, tile, ktot, m0, n0, g0, g1);
+            const int klen = g1 - g0;
+            int kg = 0;                               // K blocks of this tile so far
+            for (int s = 0, g = 0; s < a.nseg; ++s) {
+                for (int kb = 0; kb < a.kblocks[s]; ++kb, ++g) {
+                    if (SPLIT && (g < g0 || g >= g1)) continue;
                     const bool first = (kg % RT_DRAIN) == 0;
                     if (first) {
                         if (!mbar_wait(&tempty[buf], bphase ^ 1, abort_flag)) goto mma_out;
@@ -548,10 +575,11 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_kernel(const __grid_cons
                         umma(d, sdesc(sa + kk * 32), sdesc(sb + kk * 32), IDESC, (!first || kk > 0) ? 1u : 0u);
                     umma_commit(&empty[stage]);
                     if (++stage == RT_STAGES) { stage = 0; phase ^= 1; }
-                    if ((kg % RT_DRAIN) == RT_DRAIN - 1 || kg == ktot - 1) {
+                    if ((kg % RT_DRAIN) == RT_DRAIN - 1 || kg == klen - 1) {
                         umma_commit(&tfull[buf]);
                         if (++buf == 2) { buf = 0; bphase ^= 1; }
                     }
+                    ++kg;
                 }
             }
         }
@@ -562,7 +590,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_kernel(const __grid_cons
         const int q = warp & 3;
         const int half = (warp - 2) >> 2;             // column half drained by this warp
         const int row_in_tile = q * 32 + lane;
-        const int nchunks = (ktot + RT_DRAIN - 1) / RT_DRAIN;
+        const int nchunks_all = (ktot + RT_DRAIN - 1) / RT_DRAIN;
         int buf = 0;
         uint32_t bphase = 0;
         int qs = 0;
@@ -571,6 +599,12 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_kernel(const __grid_cons
             int tile;
             if (!tq_pop(tq_ids, tq_full, tq_empty, qs, qp, tile, abort_flag, true)) goto done;
             if (tile >= a.tiles) break;
+            int nchunks = nchunks_all;
+            if constexpr (SPLIT) {
+                int m0s, n0s, g0, g1;
+                router_tile<true>(a, tile, ktot, m0s, n0s, g0, g1);
+                nchunks = (g1 - g0 + RT_DRAIN - 1) / RT_DRAIN;
+            }
             float acc[RT_HALF];
 #pragma unroll
             for (int i = 0; i < RT_HALF; ++i) acc[i] = 0.f;
@@ -584,6 +618,20 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_kernel(const __grid_cons
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty[buf]);
                 if (++buf == 2) { buf = 0; bphase ^= 1; }
+            }
+            if constexpr (SPLIT) {
+                // raw fp32 logit sums of this split; router_splitk_reduce_kernel adds the
+                // splits in order, then the offset and the sigmoid
+                const int ks = tile / a.tiles_mn, mn = tile - ks * a.tiles_mn;
+                const int row = (mn / a.tiles_n) * 128 + row_in_tile;
+                const int n0 = (mn % a.tiles_n) * RT_BN + half * RT_HALF;
+                if (row < a.M) {
+                    float *P = a.partial + ((long long)ks * a.M + row) * a.ldp;
+#pragma unroll
+                    for (int i = 0; i < RT_HALF; ++i)
+                        if (n0 + i < a.N) P[n0 + i] = acc[i];
+                }
+                continue;
             }
             const int row = (tile / a.tiles_n) * 128 + row_in_tile;
             const int n0 = (tile % a.tiles_n) * RT_BN + half * RT_HALF;
@@ -1104,8 +1152,24 @@ int launch_grouped(const CUtensorMap &wmap, const GroupedArgs &a, cudaStream_t s
 
 }  // namespace
 
+// Split-K finish of the router: scores = sigmoid(sum of the splits' logit sums, in split
+// order, + mu) -- the router epilogue's formula.
+__global__ void __launch_bounds__(256) router_splitk_reduce_kernel(const float *__restrict__ P, int S, int M,
+                                                                  int E, const float *__restrict__ mu,
+                                                                  float *__restrict__ scores) {
+    const long long total = (long long)M * E;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int e = (int)(idx % E);
+        float acc = 0.f;
+        for (int ks = 0; ks < S; ++ks) acc += P[(long long)ks * total + idx];
+        const float v = acc + (mu ? mu[e] : 0.f);
+        scores[idx] = 1.0f / (1.0f + expf(-v));
+    }
+}
+
 int tc_router_scores(const slmoe_config *c, const void *x, const float *W_r, const float *mu,
-                     __nv_bfloat16 *wsplit, float *scores, int32_t *status, int *counter,
+                     __nv_bfloat16 *wsplit, float *scores, int32_t *status, int *counter, float *partial,
                      cudaStream_t st) {
     const long long n = (long long)c->E * c->d;
     split_router_kernel<<<(int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096), 256, 0, st>>>(W_r, wsplit, n);
@@ -1128,13 +1192,37 @@ int tc_router_scores(const slmoe_config *c, const void *x, const float *W_r, con
     a.status = status;
     a.counter = counter;
     a.tiles_n = (a.N + RT_BN - 1) / RT_BN;
-    a.tiles = ((a.M + 127) / 128) * a.tiles_n;
+    a.tiles_mn = ((a.M + 127) / 128) * a.tiles_n;
+    a.tiles = a.tiles_mn;
     if (a.tiles == 0) return SLMOE_OK;
+    const int sms = sm_count();
+    // a batch of at most ROUTER_SPLITK_MAX_M tokens has too few tiles to fill the SMs: split
+    // the 3 x d / 64 K blocks over up to ROUTER_SPLITK_MAX CTAs per tile (at least two
+    // drain chunks each), fp32 logit sums in the workspace, finished by the reduce kernel
     for (int s = 1; s < a.nseg; ++s)
         if (a.kblocks[s] != a.kblocks[0]) return fail(SLMOE_EINVAL, "router pieces differ in K");
-    if ((rc = set_smem(router_kernel, RT_SMEM))) return rc;
-    const int sms = sm_count();
-    router_kernel<<<a.tiles < sms ? a.tiles : sms, RT_THREADS, RT_SMEM, st>>>(maps, a);
+    int S = 1;
+    if (partial && a.M <= ROUTER_SPLITK_MAX_M && a.tiles_mn < sms) {
+        const int ktot = 3 * a.kblocks[0];
+        S = (sms + a.tiles_mn - 1) / a.tiles_mn;
+        if (S > ROUTER_SPLITK_MAX) S = ROUTER_SPLITK_MAX;
+        if (S > ktot / (2 * RT_DRAIN)) S = ktot / (2 * RT_DRAIN);
+    }
+    if (S >= 2) {
+        a.ksplit = S;
+        a.partial = partial;
+        a.ldp = a.N;
+        a.tiles = a.tiles_mn * S;
+        if ((rc = set_smem(router_kernel<true>, RT_SMEM))) return rc;
+        router_kernel<true><<<a.tiles < sms ? a.tiles : sms, RT_THREADS, RT_SMEM, st>>>(maps, a);
+        if ((rc = check_launch("router_kernel"))) return rc;
+        const long long total = (long long)a.M * a.N;
+        const long long blocks = (total + 255) / 256 < 4LL * sms ? (total + 255) / 256 : 4LL * sms;
+        router_splitk_reduce_kernel<<<(int)blocks, 256, 0, st>>>(partial, S, a.M, a.N, mu, scores);
+        return check_launch("router_splitk_reduce");
+    }
+    if ((rc = set_smem(router_kernel<false>, RT_SMEM))) return rc;
+    router_kernel<false><<<a.tiles < sms ? a.tiles : sms, RT_THREADS, RT_SMEM, st>>>(maps, a);
     return check_launch("router_kernel");
 }
 

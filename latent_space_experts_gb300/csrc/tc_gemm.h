@@ -20,9 +20,10 @@ struct TcForward {
 // Router scores s = sigmoid(x W_r^T + mu) with fp32-faithful logits: W_r is split into three
 // bf16 pieces (hi + mid + lo == W_r exactly) whose products with the bf16 x are exact in
 // fp32, accumulated on the tensor cores.  wsplit: workspace [3, E, d] bf16.
-// counter: nullable zeroed tile counter for dynamic scheduling.
+// counter: nullable zeroed tile counter for dynamic scheduling.  partial: nullable workspace
+// for split-K logit sums of a small batch ([ROUTER_SPLITK_MAX, T, E] fp32).
 int tc_router_scores(const slmoe_config *c, const void *x, const float *W_r, const float *mu,
-                     __nv_bfloat16 *wsplit, float *scores, int32_t *status, int *counter,
+                     __nv_bfloat16 *wsplit, float *scores, int32_t *status, int *counter, float *partial,
                      cudaStream_t st);
 
 // The parts of the layer that need only x: latent down-projection and the shared experts'
