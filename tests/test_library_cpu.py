@@ -117,3 +117,16 @@ def test_empty_batch_forward_returns_before_any_cuda_call(lib):
     rc = lib.slmoe_forward(ctypes.byref(cfg), None, ctypes.byref(w), None, None, None, None, None,
                            None, None, 0, None)
     assert rc == 0
+
+
+def test_small_batches_get_room_for_the_split_router():
+    """A bf16 batch of at most 256 tokens reserves [16, T, E] fp32 for the router's split-K
+    logit sums in the workspace; a larger batch does not split and needs no such room."""
+    E = 896
+    def total(T):
+        return lse.slmoe_workspace_size(lse.config(synthetic.shape_with("k3_decode", T=T)))
+    # growth from 256 to 257 tokens loses the split region (16 * 256 * E * 4 bytes) but adds
+    # one token's worth of everything else
+    per_token = total(300) - total(299)
+    assert total(257) < total(256) + per_token
+    assert total(256) - total(255) >= 16 * E * 4
