@@ -177,7 +177,10 @@ SLMOE_API int slmoe_route(const slmoe_config *cfg, const void *x, const float *W
  * each piece rounded up to 256 bytes.  With E = 896 and d = 7168 (bf16) that is 36.8 MiB
  * plus about 0.2 KiB per token with a caller scores buffer, 3.7 KiB per token without one.
  * A call that needs more returns SLMOE_ENOSPACE before anything is launched, and
- * slmoe_last_error() gives the bytes it needed.
+ * slmoe_last_error() gives the bytes it needed.  A bf16 batch of at most 256 tokens also
+ * takes 16 * T * E * 4 bytes for the split-K router sums that slmoe_route uses at that size,
+ * when they fit under the limit; when they do not, the router runs unsplit here and its fp32
+ * logits may differ from slmoe_route's in the last bits (the sums are added in another order).
  *
  * Zeroing: nothing in the scratch has to be zeroed by the caller.  The tile counters, the
  * only part that must start at zero, are cleared by each call on its own stream before its

@@ -488,7 +488,7 @@ static int route_scratch(char **out) {
 // per-chunk expert counts, the split router weights (bf16 type) and, when the caller passes
 // no scores buffer, the scores.  Returns the bytes needed.
 struct RouteScratch {
-    size_t counters, chunk_counts, wr_split, scores, total;
+    size_t counters, chunk_counts, wr_split, scores, rt_split, total;
 };
 
 static RouteScratch route_scratch_layout(const slmoe_config *c, size_t nchunks, bool own_scores) {
@@ -504,6 +504,15 @@ static RouteScratch route_scratch_layout(const slmoe_config *c, size_t nchunks, 
     s.wr_split = c->dtype == SLMOE_BF16 ? take((size_t)3 * c->E * c->d * 2) : 0;
     s.scores = own_scores ? take((size_t)c->T * c->E * 4) : 0;
     s.total = off;
+    // the split-K router sums of a small bf16 batch, as in the workspace layout, when they fit
+    // (else the router runs unsplit, its fp32 logit sums added in another order)
+    if (c->dtype == SLMOE_BF16 && c->T <= ROUTER_SPLITK_MAX_M) {
+        const size_t at = take((size_t)ROUTER_SPLITK_MAX * c->T * c->E * 4);
+        if (off <= (size_t)SLMOE_ROUTE_NOALLOC_SCRATCH_BYTES) {
+            s.rt_split = at;
+            s.total = off;
+        }
+    }
     return s;
 }
 
@@ -541,10 +550,9 @@ extern "C" int slmoe_route_noalloc(const slmoe_config *cfg, const void *x, const
                     S.total, (size_t)SLMOE_ROUTE_NOALLOC_SCRATCH_BYTES);
     char *scr = nullptr;
     if ((rc = route_scratch(&scr))) return rc;
-    // route_impl reads the split router weights at ws + L.wr_split; the fixed scratch holds no
-    // split-K router sums, so the router runs unsplit here
+    // route_impl reads the split router weights and the split-K router sums at these offsets
     L.wr_split = S.wr_split;
-    L.rt_split = 0;
+    L.rt_split = S.rt_split;
     Routing R = {scores ? scores : reinterpret_cast<float *>(scr + S.scores), topk_idx, topk_w,
                  counts, offsets, perm, slot_pos, reinterpret_cast<int32_t *>(scr + S.chunk_counts),
                  reinterpret_cast<int *>(scr + S.counters)};
