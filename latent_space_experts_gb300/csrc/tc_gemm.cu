@@ -1,30 +1,34 @@
 // tcgen05 / TMEM / TMA kernels of the bf16 layer type (sm_103a).
 //
-// Two persistent, warp-specialised GEMM kernels carry every contraction of the layer:
+// Three persistent, warp-specialised kernels carry every contraction of the layer; in each,
+// one thread issues TMA loads, one thread issues tcgen05.mma (M = 128, K = 16) into TMEM,
+// and epilogue warps read the accumulators back with tcgen05.ld.
 //
 //  * dense_kernel  C[T, N] = epi(A[T, K] B[N, K]^T) with A = activations, B = weights, both
-//    loaded by TMA into 128-byte-swizzled shared memory; one thread issues
-//    tcgen05.mma (M = 128, N = BN, K = 16) into a double-buffered TMEM accumulator, four
-//    epilogue warps read it back with tcgen05.ld.  K may be cut into up to four segments,
-//    each with its own pair of tensor maps; the segments add into one accumulator
-//    (used for y = z W_out^T + sum_s h_s W2_s^T and for the three router weight pieces).
-//    Epilogues: bf16 store, fp32 store and SiTU-GLU (gate tile rows 0..127, up rows
-//    128..255 of B).
+//    loaded by TMA into 128-byte-swizzled shared memory.  A tile is two 128-row sub-tiles
+//    sharing one weight tile of BN rows (256; 64 for a batch of one row tile), with a
+//    single-buffered accumulator drained by 8 epilogue warps.  K may be cut into up to four
+//    segments, each with its own pair of tensor maps, added into one accumulator (used for
+//    y = z W_out^T + sum_s h_s W2_s^T).  Epilogues: bf16 store, fp32 store and SiTU-GLU
+//    (gate rows in the first half of the weight tile, up rows in the second).
 //
 //  * router_kernel  the router logits over three bf16 pieces of W_r with the TMEM
-//    accumulator drained into fp32 registers every few K blocks, then sigmoid(logit + mu).
+//    accumulator drained into fp32 registers every few K blocks, then sigmoid(logit + mu);
+//    a small batch splits the K blocks over several CTAs per tile (router_kernel<true>)
+//    and a reduce kernel adds their fp32 sums before the sigmoid.
 //
 //  * grouped_kernel  the routed experts, with the weights as the MMA's M operand
-//    ("swap AB"): for expert e and a block of 256 output features it computes
-//    D[feature, token] = W_e[feature, :] . X[token, :] for all tokens routed to e (up to 256
-//    per pass, N rounded to 16).  The tokens' rows are gathered by index with cp.async into
-//    the same swizzled layout a TMA load would produce, so the weights - the bytes that
+//    ("swap AB"): a work item is an expert, a block of output features (128 for gate|up,
+//    whose gate and up rows make the two M sub-tiles; 256 for down) and a pass of up to 192
+//    of its tokens (N rounded to 16).  The tokens' rows are gathered by index with cp.async
+//    into the same swizzled layout a TMA load would produce, so the weights - the bytes that
 //    bound this step - stream from HBM once per expert while the few tokens of each expert
 //    cost a 16-wide MMA column granule instead of a 128-row tile.
 //    Epilogues: SiTU-GLU -> h (expert gate/up), bf16 store -> y_e (expert down).
 //
 // Every wait on an mbarrier is bounded (%globaltimer); on expiry the kernel sets a shared
-// abort flag, every role leaves its loop, status[2] is set and TMEM is freed.
+// abort flag and every role leaves its loop; the TMA producer then waits (bounded) for the
+// copies it issued and the MMA thread for its MMAs, status[2] is set and TMEM is freed.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -174,9 +178,10 @@ __device__ __forceinline__ void dense_tile_mn(int tile, int tiles, int tiles_n, 
 // 64-wide K block is MSUB * 16 KB of activations + BN * 128 bytes of weights feeding MSUB * 4
 // MMAs: with MSUB = 2 a stage (64 KB) covers 1024 MMA cycles and three stages cover the
 // ~3000-cycle latency of a loaded L2, where single-row-tile stages (48 KB, 512 cycles) left
-// the tensor pipe waiting a third of the time.  The sub-tiles' accumulators fill the 512 TMEM
-// columns, so the accumulator is single-buffered; each sub-tile has its own 4 epilogue
-// warps to drain it quickly.
+// the tensor pipe waiting a third of the time.  At BN = 256 the sub-tiles' accumulators fill
+// the 512 TMEM columns, so the accumulator is single-buffered; each sub-tile has its own 4
+// epilogue warps to drain it quickly.  (BN = 64, for a batch of one row tile, keeps the same
+// structure in 128 columns.)
 template <int BN, int EPI, int PACC>
 struct DenseCfg {
     static constexpr int BM = 128, BK = 64, MSUB = 2, BM_TILE = BM * MSUB;
