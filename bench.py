@@ -131,14 +131,21 @@ def dist_setup(args):
     return world, rank, local
 
 
-def max_over_ranks(v, world):
+def max_over_ranks(v, world, device="cuda"):
+    """The largest of the ranks' values (the slowest rank's time), on every rank."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(units_per_rank, world, ms_per_step):
+    """Whole-job throughput: the units every rank processed in one step, over the step time
+    of the slowest rank (replicas: each rank runs the full batch)."""
+    return units_per_rank * world / (ms_per_step * 1e-3)
 
 
 def barrier(world):
@@ -529,9 +536,9 @@ def main():
                     "sample": f"{n_tok} tokens of the {args.workload} batch, fp64 numpy ({dt:.1f} s)"}
 
     if rank == 0:
-        tokens = shp.T * world
+        tokens = shp.T
         line = {
-            "metric": METRIC, "value": round(tokens / (ms * 1e-3), 1), "unit": UNIT, "n_gpus": world,
+            "metric": METRIC, "value": round(job_throughput(tokens, world, ms), 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": shp.dtype,
             "data": "synthetic",
@@ -548,7 +555,7 @@ def main():
             "stages": stages,
             "qb_histogram": qb,
             "cpu_baseline": cpu_base,
-            "e2e": {"value": round(tokens / (ms_e2e * 1e-3), 1), "unit": UNIT,
+            "e2e": {"value": round(job_throughput(tokens, world, ms_e2e), 1), "unit": UNIT,
                     "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
                     "d2h_bytes_per_step": y_host[0].numel() * y_host[0].element_size(),
                     "copies": "own streams, double-buffered, overlapping the neighbouring steps"},
