@@ -51,3 +51,19 @@ def test_one_rank_is_the_plain_time():
     import bench
     assert bench.max_over_ranks(2.0, 1) == 2.0
     assert bench.job_throughput(8192, 1, 4.0) == pytest.approx(8192 / 4e-3)
+
+
+def test_oracle_inputs_widened_once_give_the_same_layer():
+    """bench.py hands the oracle its dense inputs already in fp64 (as the GPU keeps its weights
+    resident): the oracle's results are the same as from the stored inputs."""
+    import numpy as np
+    import bench
+    import oracle
+    import synthetic
+    shp = synthetic.shape_with("mid", T=48, d=256, d_latent=128, E=16, k=2, I=64, I_shared=128)
+    inp = synthetic.layer_inputs(shp, seed=9)
+    tok = np.arange(0, 48, 3)
+    a = oracle.forward({k: (v.cpu() if v is not None else None) for k, v in inp.items()}, shp.k, tokens=tok)
+    b = oracle.forward(bench.oracle_inputs(inp), shp.k, tokens=tok)
+    assert np.array_equal(a["topk_idx"], b["topk_idx"])
+    assert np.array_equal(a["y"], b["y"])
