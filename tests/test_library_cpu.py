@@ -130,3 +130,31 @@ def test_small_batches_get_room_for_the_split_router():
     per_token = total(300) - total(299)
     assert total(257) < total(256) + per_token
     assert total(256) - total(255) >= 16 * E * 4
+
+
+def test_router_weight_split_is_exact_in_three_bf16_pieces():
+    """The router's fp32 weights go to the tensor cores as three bf16 pieces, hi = bf16(w),
+    mid = bf16(w - hi), lo = bf16(w - hi - mid) (round to nearest, differences in fp32):
+    hi + mid + lo == w exactly for normal fp32 values, and each piece times a bf16 activation
+    is exact in fp32, so the logits are the fp32 weights' logits up to the order of the adds.
+    Checked here with torch's round-to-nearest bf16 conversion, the same rounding the GPU
+    split uses."""
+    import numpy as np
+    import torch
+    rng = np.random.default_rng(3)
+    mant = rng.uniform(1.0, 2.0, 200000)
+    expo = rng.integers(-60, 61, 200000)
+    sign = rng.choice([-1.0, 1.0], 200000)
+    w = torch.from_numpy((sign * mant * 2.0 ** expo).astype(np.float32))
+    w = torch.cat([w, torch.randn(100000) / 84.7])                 # the K3 router's N(0, 1/d)
+    hi = w.to(torch.bfloat16)
+    r1 = w - hi.float()
+    mid = r1.to(torch.bfloat16)
+    r2 = r1 - mid.float()
+    lo = r2.to(torch.bfloat16)
+    assert torch.equal(lo.float(), r2)                             # the remainder fits bf16
+    total = hi.double() + mid.double() + lo.double()
+    assert torch.equal(total, w.double())
+    x = torch.randn(300000).to(torch.bfloat16)
+    for piece in (hi, mid, lo):                                     # products exact in fp32
+        assert torch.equal((x.float() * piece.float()).double(), x.double() * piece.double())
