@@ -49,28 +49,39 @@ def peaks():
 
 
 def work_model(shp, counts=None):
-    """Algorithmic FLOPs and bytes per stage for one step (weights touched + kernel I/O)."""
+    """FLOPs and bytes per stage of one step.  "bytes" are the algorithmic bytes the survey
+    counts (weights touched, the layer's input x and its fp32 output y); "inter" are the
+    intermediates a stage reads or writes (scores, x_lat, h, y_e, z, h_s), which a fused
+    design could avoid and which are reported separately."""
     T, d, dl, E, k, I, ns, Is = shp.T, shp.d, shp.d_latent, shp.E, shp.k, shp.I, shp.n_shared, shp.I_shared
     touched = E if counts is None else int((counts > 0).sum())
     st = {
-        "router": dict(flops=2 * T * d * E, bytes=T * d * 2 + E * d * 4 + T * E * 4, bound="tensor"),
-        "topk+permute+hist": dict(flops=0, bytes=2 * T * E * 4 + T * k * 16, bound="hbm"),
-        "down": dict(flops=2 * T * d * dl, bytes=T * d * 2 + dl * d * 2 + T * dl * 2, bound="tensor"),
-        "expert gate|up": dict(flops=2 * T * k * dl * 2 * I,
-                               bytes=touched * 2 * I * dl * 2 + T * dl * 2 + T * k * I * 2, bound="hbm"),
-        "expert down": dict(flops=2 * T * k * I * dl,
-                            bytes=touched * dl * I * 2 + T * k * I * 2 + T * k * dl * 2, bound="hbm"),
-        "combine+rmsnorm": dict(flops=0, bytes=T * k * dl * 2 + T * dl * 2, bound="hbm"),
-        "shared gate|up": dict(flops=2 * T * d * 2 * Is * ns, bytes=T * d * 2 + ns * 2 * Is * d * 2 + T * ns * Is * 2,
-                               bound="tensor"),
-        "up+shared down": dict(flops=2 * T * (dl + ns * Is) * d,
-                               bytes=T * dl * 2 + T * ns * Is * 2 + d * (dl + ns * Is) * 2 + T * d * 2,
-                               bound="tensor"),
+        "router": dict(flops=2 * T * d * E, bytes=T * d * 2 + E * d * 4, inter=T * E * 4, bound="tensor"),
+        "topk+permute+hist": dict(flops=0, bytes=0, inter=2 * T * E * 4 + T * k * 16, bound="hbm"),
+        "down": dict(flops=2 * T * d * dl, bytes=T * d * 2 + dl * d * 2, inter=T * dl * 2, bound="tensor"),
+        "expert gate|up": dict(flops=2 * T * k * dl * 2 * I, bytes=touched * 2 * I * dl * 2,
+                               inter=T * dl * 2 + T * k * I * 2, bound="hbm"),
+        "expert down": dict(flops=2 * T * k * I * dl, bytes=touched * dl * I * 2,
+                            inter=T * k * I * 2 + T * k * dl * 2, bound="hbm"),
+        "combine+rmsnorm": dict(flops=0, bytes=0, inter=T * k * dl * 2 + T * dl * 2 + T * k * 8, bound="hbm"),
+        "shared gate|up": dict(flops=2 * T * d * 2 * Is * ns, bytes=T * d * 2 + ns * 2 * Is * d * 2,
+                               inter=T * ns * Is * 2, bound="tensor"),
+        "up+shared down": dict(flops=2 * T * (dl + ns * Is) * d, bytes=d * (dl + ns * Is) * 2 + T * d * 4,
+                               inter=T * dl * 2 + T * ns * Is * 2, bound="tensor"),
     }
     layer_flops = sum(v["flops"] for v in st.values())
     layer_bytes = (E * d * 4 + dl * d * 2 + touched * 3 * I * dl * 2 + d * dl * 2 + ns * 3 * Is * d * 2
-                   + T * d * 2 * 2)
+                   + T * d * 2 + T * d * 4)
     return st, layer_flops, layer_bytes
+
+
+def tensor_peak(pk, timed_s, reasons):
+    """The bf16 tensor peak a tensor-bound figure is judged against: the burst figure for a
+    timed region shorter than two seconds or one that saw no power capping, the sustained
+    figure (a seconds-long loop under the power cap) otherwise."""
+    if timed_s >= 2.0 and "sw_power_cap" in (reasons or []):
+        return pk["bf16_tflops_sustained"], "sustained bf16"
+    return pk["bf16_tflops"], "burst bf16"
 
 
 class ClockSampler:
@@ -169,8 +180,13 @@ def oracle_inputs(inp):
     return out
 
 
+# Tokens of the workload's batch that one oracle sample runs (both the cpu_baseline leg and
+# each step of --impl reference time this same sample, so the two figures agree).
+CPU_SAMPLE_TOKENS = 512
+
+
 def oracle_sample(shp, inp_cpu, n_tok):
-    """Time the fp64 oracle on n_tok tokens of the workload (routing included)."""
+    """Time the fp64 oracle on the first n_tok tokens of the batch (routing included)."""
     import numpy as np
     import oracle
     tok = np.arange(n_tok)
@@ -180,20 +196,13 @@ def oracle_sample(shp, inp_cpu, n_tok):
     return n_tok / dt, dt
 
 
-def oracle_tokens(shp, inp_cpu, target_s):
-    """Tokens per oracle sample so that one sample takes at most about target_s seconds.
-    Trials double the token count until one takes a quarter of the target; the count is then
-    scaled by target / trial time.  A sample's cost grows more slowly than its token count
-    (tokens share experts, whose weights are widened once per sample), so the scaled sample
-    does not overshoot."""
-    cap = 4096
-    n = min(4, shp.T)
-    while True:
-        _, dt = oracle_sample(shp, inp_cpu, n)
-        if dt >= target_s / 4 or n >= min(shp.T, cap):
-            break
-        n = min(2 * n, shp.T, cap)
-    return max(1, min(shp.T, cap, int(n * target_s / max(dt, 1e-6))))
+def oracle_sample_threads(shp, inp_cpu, n_tok, threads):
+    """oracle_sample with the BLAS thread pools limited to `threads` (None: as configured)."""
+    if threads is None:
+        return oracle_sample(shp, inp_cpu, n_tok)
+    import threadpoolctl
+    with threadpoolctl.threadpool_limits(limits=threads):
+        return oracle_sample(shp, inp_cpu, n_tok)
 
 
 def profiled_traffic(stage):
@@ -228,8 +237,21 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
+def reference_tokens(shp, inp_cpu, args):
+    """Oracle tokens per reference step: the cpu_baseline sample (CPU_SAMPLE_TOKENS), unless
+    --steps + --warmup samples of it would take much longer than --ref-seconds; then the
+    sample shrinks so that the run stays within a few minutes (said in the line)."""
+    n = min(shp.T, args.ref_tokens or CPU_SAMPLE_TOKENS)
+    _, dt = oracle_sample(shp, inp_cpu, n)
+    runs = args.steps + args.warmup
+    if args.ref_tokens is None and runs * dt > args.ref_seconds:
+        n = max(8, int(n * args.ref_seconds / (runs * dt)))
+    return n
+
+
 def run_reference(args):
-    """The oracle as the reference arm: fp64 CPU forward on a bounded token sample per step."""
+    """The oracle as the reference arm: fp64 CPU forward on a bounded token sample per step
+    (the same sample the cpu_baseline leg of the default run times)."""
     import torch
     import synthetic
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -241,8 +263,7 @@ def run_reference(args):
     inp = synthetic.layer_inputs(shp, seed=0, device=dev)
     inp_cpu = oracle_inputs(inp)
     del inp
-    # each step is a bounded sample: the whole run (warm-up + timed) takes about ref_seconds
-    n_tok = args.ref_tokens or oracle_tokens(shp, inp_cpu, args.ref_seconds / max(1, args.steps + args.warmup))
+    n_tok = reference_tokens(shp, inp_cpu, args)
     for _ in range(args.warmup):
         oracle_sample(shp, inp_cpu, n_tok)
     t = []
@@ -259,8 +280,8 @@ def run_reference(args):
                        "E": shp.E, "k": shp.k, "I": shp.I, "n_shared": shp.n_shared,
                        "I_shared": shp.I_shared, "sample_tokens_per_step": n_tok},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-                             "sample": f"{n_tok} tokens of the {args.workload} batch per step (routing, "
-                                       f"experts, norm, shared experts), fp64 numpy"},
+                             "sample": f"the first {n_tok} tokens of the {args.workload} batch per step "
+                                       f"(routing, experts, norm, shared experts), fp64 numpy, all cores"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
@@ -317,6 +338,129 @@ def qb_engine(hbm):
             "note": "65536 x 896 fp32 scores per micro-batch (235 MB > L2); engine = 8 histograms + 1 update"}
 
 
+def qb_balance(step=1e-3):
+    """QB-engine balance on the GPU: eight 65536 x 896 micro-batches of scores are binned into
+    one histogram and routed (slmoe_topk) with a bias that the fixed-step rule updates after
+    each micro-batch; one QB update then reads the histogram.  A held-out micro-batch (seed 9)
+    is routed with no bias, with the fixed-step bias and with the QB bias, and max/mean
+    expert load is reported for each (the pages fix no target)."""
+    import torch
+    import latent_space_experts_gb300 as lse
+    import synthetic
+    q = synthetic.QB
+    E, k, T = q.E, q.k, q.T
+    hist = torch.zeros(E, q.nbins, dtype=torch.int32, device="cuda")
+    ws = torch.empty(lse.slmoe_topk_workspace_size(T, E, k), dtype=torch.uint8, device="cuda")
+    buf = dict(topk_idx=torch.empty(T, k, dtype=torch.int32, device="cuda"),
+               topk_w=torch.empty(T, k, dtype=torch.float32, device="cuda"),
+               counts=torch.empty(E, dtype=torch.int32, device="cuda"),
+               offsets=torch.empty(E + 1, dtype=torch.int32, device="cuda"),
+               perm=torch.empty(T * k, dtype=torch.int32, device="cuda"),
+               slot_pos=torch.empty(T * k, dtype=torch.int32, device="cuda"))
+
+    def route(scores, bias):
+        lse.slmoe_topk(scores, bias, T, E, k, buf["topk_idx"], buf["topk_w"], buf["counts"], buf["offsets"],
+                       buf["perm"], buf["slot_pos"], None, ws)
+        return buf["counts"]
+
+    fixed = torch.zeros(E, device="cuda")
+    for m in range(q.micro_batches):
+        sc = synthetic.qb_scores(m, q, device="cuda")
+        lse.slmoe_qb_histogram(sc, T, E, q.nbins, hist)
+        lse.slmoe_signsgd_update(route(sc, fixed), E, step, fixed)
+        del sc
+    qbias = torch.empty(E, device="cuda")
+    lse.slmoe_qb_update(hist, E, q.nbins, k, None, qbias)
+    held = synthetic.qb_scores(q.micro_batches, q, device="cuda")
+    out = {}
+    for name, b in (("no bias", torch.zeros(E, device="cuda")), (f"{q.micro_batches} fixed steps of {step:g}", fixed),
+                    ("QB", qbias)):
+        c = route(held, b).double()
+        out[name] = round(float(c.max() / c.mean()), 3)
+    torch.cuda.synchronize()
+    return {"max_over_mean_load": out,
+            "held_out": f"micro-batch {q.micro_batches + 1} (seed {q.micro_batches + 1}), {T} tokens x {E} experts, top-{k}",
+            "routing": "slmoe_topk on the GPU; histograms and both bias updates on the GPU"}
+
+
+class LayerRun:
+    """One layer configuration on the device: workspace, outputs, the step (slmoe_forward +
+    slmoe_qb_update) and, unless disabled, a CUDA graph of that step."""
+
+    def __init__(self, shp, inp, x, mu, use_graph=True, warmup=3):
+        import torch
+        import latent_space_experts_gb300 as lse
+        self.lse, self.shp, self.inp, self.x, self.mu = lse, shp, inp, x, mu
+        self.cfg = lse.config(shp)
+        self.ws = torch.zeros(lse.slmoe_workspace_size(self.cfg), dtype=torch.uint8, device="cuda")
+        self.y = torch.empty(shp.T, shp.d, dtype=torch.float32, device="cuda")
+        self.hist = torch.zeros(shp.E, shp.nbins, dtype=torch.int32, device="cuda")
+        self.bias = inp["bias"].clone()
+        self.status = torch.zeros(4, dtype=torch.int32, device="cuda")
+        self.W = lse.weights(inp)
+        self.stream = torch.cuda.current_stream()
+        for _ in range(max(3, warmup)):
+            self.step(self.x)
+        torch.cuda.synchronize()
+        self.check_status()
+        self.graph, self.launches_per_step = None, None
+        if use_graph:
+            l_cap = lse.slmoe_launch_count()
+            self.graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.graph):
+                self.step(self.x)
+            self.launches_per_step = lse.slmoe_launch_count() - l_cap
+            for _ in range(3):
+                self.graph.replay()
+            torch.cuda.synchronize()
+            self.check_status()
+
+    def step(self, x, out=None):
+        shp = self.shp
+        self.lse.slmoe_forward(self.cfg, x, self.W, self.bias, self.mu, self.y if out is None else out, None,
+                               self.hist, self.status, self.ws)
+        self.lse.slmoe_qb_update(self.hist, shp.E, shp.nbins, shp.k, None, self.bias)
+
+    def check_status(self):
+        st = self.status.cpu().tolist()
+        assert st[1:3] == [0, 0], f"device status {st}"
+
+    def timed(self, steps):
+        """ms per step over `steps` steps, CUDA events on the launching stream; and the number
+        of this library's kernels launched in that region."""
+        import torch
+        l0 = self.lse.slmoe_launch_count()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(self.stream)
+        for _ in range(steps):
+            if self.graph is not None:
+                self.graph.replay()
+            else:
+                self.step(self.x)
+        e1.record(self.stream)
+        torch.cuda.synchronize()
+        launches = (self.launches_per_step * steps if self.graph is not None
+                    else self.lse.slmoe_launch_count() - l0)
+        return e0.elapsed_time(e1) / steps, launches
+
+    def counts(self):
+        return self.lse.workspace_views(self.cfg, self.ws)["counts"].cpu().numpy()
+
+
+def layer_summary(run, ms, pk, timed_s, reasons):
+    """Tokens/s and the whole-layer roofline of one timed layer configuration."""
+    st_model, flops, nbytes = work_model(run.shp, run.counts())
+    tc, tc_kind = tensor_peak(pk, timed_s, reasons)
+    t_flops, t_bytes = flops / (tc * 1e12), nbytes / (pk["hbm_gbs"] * 1e9)
+    t_layer = max(t_flops, t_bytes)
+    return {"ms_per_step": round(ms, 4), "tokens_per_s": round(run.shp.T / (ms * 1e-3), 1),
+            "layer_roofline": {"ms": round(t_layer * 1e3, 4), "frac": round(t_layer * 1e3 / ms, 4),
+                               "bound": "tensor" if t_flops >= t_bytes else "hbm", "flops": flops,
+                               "bytes": nbytes, "tensor_peak_tflops": tc, "tensor_peak": tc_kind,
+                               "hbm_gbs": pk["hbm_gbs"]},
+            "experts_touched": int((run.counts() > 0).sum())}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -325,13 +469,12 @@ def main():
     ap.add_argument("--workload", default="k3_prefill", choices=["k3_prefill", "k3_decode", "mid", "k3_slice", "k3_dense"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-tokens", type=int, default=None,
-                    help="oracle tokens per reference step (default: sized from --ref-seconds)")
-    ap.add_argument("--ref-seconds", type=float, default=120.0,
-                    help="about how long the whole reference run (warm-up + timed steps) takes")
-    ap.add_argument("--cpu-baseline-tokens", type=int, default=None,
-                    help="oracle tokens of the cpu_baseline sample (default: sized from --cpu-seconds)")
-    ap.add_argument("--cpu-seconds", type=float, default=25.0)
+                    help="oracle tokens per reference step (default: the cpu_baseline sample)")
+    ap.add_argument("--ref-seconds", type=float, default=240.0,
+                    help="the reference run shrinks its sample if it would take much longer than this")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the decode / mid sub-results and the QB balance in the line")
     ap.add_argument("--qb-only", action="store_true", help="only the QB engine measurement")
     ap.add_argument("--no-graph", action="store_true", help="time the step without a CUDA graph")
     ap.add_argument("--skew", action="store_true", help="heavy skew (10%% hot experts)")
@@ -347,83 +490,45 @@ def main():
     world, rank, local = dist_setup(args)
     lse.build()
     lse.load()
+    pk, pk_kind = peaks()
+    hbm = pk["hbm_gbs"]
     if args.qb_only:
         if rank == 0:
-            pk, pk_kind = peaks()
-            print(json.dumps({"qb_histogram": qb_engine(pk["hbm_gbs"]), "peak_source": pk_kind}))
+            print(json.dumps({"qb_histogram": qb_engine(hbm), "peak_source": pk_kind}))
         return
     shp = synthetic.LAYERS[args.workload]
-    cfg = lse.config(shp)
     inp = synthetic.layer_inputs(shp, seed=rank, device="cuda", heavy_skew=args.skew)
-    ws = torch.zeros(lse.slmoe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
-    y = torch.empty(shp.T, shp.d, dtype=torch.float32, device="cuda")
-    hist = torch.zeros(shp.E, shp.nbins, dtype=torch.int32, device="cuda")
-    bias = inp["bias"].clone()
-    status = torch.zeros(4, dtype=torch.int32, device="cuda")
-    W = lse.weights(inp)
-    stream = torch.cuda.current_stream()
-
-    def step(x, out=None):
-        lse.slmoe_forward(cfg, x, W, bias, inp["logit_offset"], y if out is None else out, None, hist,
-                          status, ws)
-        lse.slmoe_qb_update(hist, shp.E, shp.nbins, shp.k, None, bias)
-
-    for _ in range(max(3, args.warmup)):
-        step(inp["x"])
-    torch.cuda.synchronize()
-    assert status.cpu().tolist()[1:3] == [0, 0], f"device status {status.cpu().tolist()}"
-
-    # the timed step is replayed from a CUDA graph of the same calls (the library's launches are
-    # stream-ordered, its auxiliary stream joins the capture through the fork/join events);
-    # the graph only removes host launch gaps between the step's ~15 kernels
-    graph = None
-    launches_per_step = None
-    if not args.no_graph:
-        l_cap = lse.slmoe_launch_count()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            step(inp["x"])
-        launches_per_step = lse.slmoe_launch_count() - l_cap
-        for _ in range(3):
-            graph.replay()
-        torch.cuda.synchronize()
-        assert status.cpu().tolist()[1:3] == [0, 0], f"device status {status.cpu().tolist()}"
+    run = LayerRun(shp, inp, inp["x"], inp["logit_offset"], use_graph=not args.no_graph, warmup=args.warmup)
+    for _ in range(max(0, args.warmup - 3)):
+        run.timed(1)
 
     # ---------------- device-resident timing
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if sampler:
         sampler.start()
-    l0 = lse.slmoe_launch_count()
     barrier(world)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     w0 = time.time()
-    e0.record(stream)
-    for _ in range(args.steps):
-        if graph is not None:
-            graph.replay()
-        else:
-            step(inp["x"])
-    e1.record(stream)
-    torch.cuda.synchronize()
+    ms_rank, launches = run.timed(args.steps)
     w1 = time.time()
     barrier(world)
-    launches = (launches_per_step * args.steps if graph is not None
-                else lse.slmoe_launch_count() - l0)
-    ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
+    ms = max_over_ranks(ms_rank, world)
     clocks = sampler.stop(w0, w1) if sampler else None
+    timed_s = ms * args.steps * 1e-3
+    reasons = clocks["reasons"] if clocks else []
+    run.check_status()
 
     # ---------------- per-stage timing (events recorded by the library on this stream)
     nst = len(STAGES)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)] for _ in range(min(args.steps, 50))]
     for row in ev:
         for e in row:
-            e.record(stream)
+            e.record(run.stream)
     torch.cuda.synchronize()
     stage_ms = [0.0] * nst
     for row in ev:
         lse.slmoe_set_stage_events(row)
-        step(inp["x"])
+        run.step(run.x)
     lse.slmoe_set_stage_events(None)
     torch.cuda.synchronize()
     # stage i ends at event i.  On the bf16 type the down-projection (3) and the shared
@@ -440,17 +545,16 @@ def main():
             else:
                 t_start = t[start_of.get(i, i - 1)]
             stage_ms[i] += (t[i] - t_start) / len(ev)
-    counts = lse.workspace_views(cfg, ws)["counts"].cpu().numpy()
+    counts = run.counts()
     st_model, layer_flops, layer_bytes = work_model(shp, counts)
-    pk, pk_kind = peaks()
-    hbm = pk["hbm_gbs"]
-    tc = pk["bf16_tflops_sustained"]
+    tc, tc_kind = tensor_peak(pk, timed_s, reasons)
     stages = {}
     for i in range(1, nst):
         m = st_model[STAGES[i]]
         t = stage_ms[i] * 1e-3
         stages[STAGES[i]] = {"ms": round(stage_ms[i], 4),
                              "GB/s": round(m["bytes"] / t / 1e9, 1) if t > 0 else None,
+                             "GB/s_with_intermediates": round((m["bytes"] + m["inter"]) / t / 1e9, 1) if t > 0 else None,
                              "TFLOP/s": round(m["flops"] / t / 1e12, 1) if t > 0 else None,
                              "bound": m["bound"]}
     # the dominant kernel on the critical path (the concurrent front part excluded)
@@ -459,20 +563,26 @@ def main():
     t_dom = stage_ms[dom] * 1e-3
     if dm["bound"] == "hbm":
         roof = {"bound": "hbm", "achieved": round(dm["bytes"] / t_dom / 1e9, 1), "peak": hbm, "unit": "GB/s"}
+        roof["achieved_with_intermediates"] = round((dm["bytes"] + dm["inter"]) / t_dom / 1e9, 1)
+        roof["peak_source"] = f"{pk_kind} hbm copy"
     else:
         roof = {"bound": "tensor", "achieved": round(dm["flops"] / t_dom / 1e12, 1), "peak": tc,
-                "unit": "TFLOP/s"}
+                "unit": "TFLOP/s", "peak_source": f"{pk_kind} {tc_kind}"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
     roof["traffic"] = profiled_traffic(STAGES[dom]) if args.workload == "k3_prefill" else None
     roof["kernel"] = STAGES[dom]
-    roof["peak_source"] = f"{pk_kind} ({'sustained bf16' if roof['bound'] == 'tensor' else 'hbm copy'})"
-    t_layer = max(layer_flops / (tc * 1e12), layer_bytes / (hbm * 1e9))
+    roof["algorithmic_bytes"] = dm["bytes"]
+    summary = layer_summary(run, ms, pk, timed_s, reasons)
+    lr = summary["layer_roofline"]
+    t_sus = max(layer_flops / (pk["bf16_tflops_sustained"] * 1e12), layer_bytes / (hbm * 1e9))
+    lr["frac_vs_sustained_peak"] = round(t_sus * 1e3 / ms, 4)
 
     # ---------------- end to end through the public API, host buffers
     # Every step uploads its input from pinned host memory and reads its result back.  As a
     # serving loop would, the copies run on their own streams with two device buffers each, so
     # that step i+1's upload and step i's read-back overlap the compute of the steps beside them;
     # the timed region runs from before the first upload to the end of the last read-back.
+    stream, y = run.stream, run.y
     x_host = inp["x"].cpu().pin_memory()
     y_host = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for _ in range(2)]
     x_dev = [torch.empty_like(inp["x"]) for _ in range(2)]
@@ -498,15 +608,15 @@ def main():
             stream.wait_event(ready[b])
             if out[b] is not None:              # y buffer b: step i-2's read-back is done
                 stream.wait_event(out[b])
-            step(x_dev[b], y_dev[b])
+            run.step(x_dev[b], y_dev[b])
             done[b] = stream.record_event()
             s_out.wait_event(done[b])
             with torch.cuda.stream(s_out):
                 y_host[b].copy_(y_dev[b], non_blocking=True)
                 out[b] = s_out.record_event()
-        for ev in out:
-            if ev is not None:
-                stream.wait_event(ev)
+        for ev_ in out:
+            if ev_ is not None:
+                stream.wait_event(ev_)
 
     w0e = torch.cuda.Event()
     w0e.record(stream)
@@ -519,21 +629,45 @@ def main():
     e2e_steps(n_e2e, f0)
     f1.record(stream)
     torch.cuda.synchronize()
-    assert status.cpu().tolist()[1:3] == [0, 0], f"device status {status.cpu().tolist()}"
+    run.check_status()
     assert torch.equal(y_host[(n_e2e - 1) % 2], y_dev[(n_e2e - 1) % 2].cpu())
     ms_e2e = max_over_ranks(f0.elapsed_time(f1), world) / n_e2e
+    del x_host, y_host, x_dev, y_dev
 
-    # ---------------- QB engine histogram bandwidth (65536 x 896 fp32 per micro-batch)
+    # ---------------- the other layer workloads and the QB engine (rank 0, reported only)
+    extra = {}
     qb = qb_engine(hbm) if rank == 0 else None
+    if rank == 0 and not args.no_extra:
+        if args.workload == "k3_prefill":
+            # K3 decode: the same weights, the first 128 tokens of the batch; uniform and with
+            # heavy skew (10 % of the experts get +2 on their logit offset)
+            dshp = synthetic.LAYERS["k3_decode"]
+            for name, skew in (("k3_decode", False), ("k3_decode_heavy_skew", True)):
+                mu = synthetic.logit_offset(dshp, seed=rank, device="cuda", heavy_skew=skew)
+                drun = LayerRun(dshp, inp, inp["x"][: dshp.T].contiguous(), mu)
+                dms, _ = drun.timed(200)
+                extra[name] = layer_summary(drun, dms, pk, dms * 0.2, reasons)
+                del drun
+        mshp = synthetic.LAYERS["mid"]
+        minp = synthetic.layer_inputs(mshp, seed=0, device="cuda")
+        mrun = LayerRun(mshp, minp, minp["x"], minp["logit_offset"])
+        mms, _ = mrun.timed(200)
+        extra["mid"] = layer_summary(mrun, mms, pk, mms * 0.2, reasons)
+        del mrun, minp
+        extra["qb_balance"] = qb_balance()
 
-    # ---------------- oracle on the host cores (bounded sample)
+    # ---------------- oracle on the host cores (the same sample the reference arm times)
     cpu_base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         inp_cpu = oracle_inputs(inp)
-        n_tok = args.cpu_baseline_tokens or oracle_tokens(shp, inp_cpu, args.cpu_seconds)
-        v, dt = oracle_sample(shp, inp_cpu, n_tok)
-        cpu_base = {"value": round(v, 3), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-                    "sample": f"{n_tok} tokens of the {args.workload} batch, fp64 numpy ({dt:.1f} s)"}
+        n_tok = min(shp.T, CPU_SAMPLE_TOKENS)
+        oracle_sample(shp, inp_cpu, min(n_tok, 16))          # page in the widened inputs
+        v_all, dt_all = oracle_sample_threads(shp, inp_cpu, n_tok, None)
+        v_one, dt_one = oracle_sample_threads(shp, inp_cpu, n_tok, 1)
+        cpu_base = {"value": round(v_all, 3), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                    "sample": f"the first {n_tok} tokens of the {args.workload} batch, fp64 numpy "
+                              f"({dt_all:.1f} s on all cores)",
+                    "one_thread": {"value": round(v_one, 3), "seconds": round(dt_one, 1)}}
 
     if rank == 0:
         tokens = shp.T
@@ -547,17 +681,16 @@ def main():
                        "router": "fp32 logits (3-piece bf16 split)", "skew": bool(args.skew),
                        "parallelism": f"replicas x{world}",
                        "l2": "no flush: weights (10.2 GB at K3) exceed L2 every step",
-                       "cuda_graph": graph is not None},
+                       "cuda_graph": run.graph is not None},
             "roofline": roof,
-            "layer_roofline": {"ms": round(t_layer * 1e3, 4), "frac": round(t_layer * 1e3 / ms, 4),
-                               "flops": layer_flops, "bytes": layer_bytes,
-                               "peaks": f"{pk_kind}: {tc} TFLOP/s sustained bf16, {hbm} GB/s"},
+            "layer_roofline": lr,
             "stages": stages,
             "qb_histogram": qb,
+            "workloads": extra,
             "cpu_baseline": cpu_base,
             "e2e": {"value": round(job_throughput(tokens, world, ms_e2e), 1), "unit": UNIT,
-                    "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
-                    "d2h_bytes_per_step": y_host[0].numel() * y_host[0].element_size(),
+                    "h2d_bytes_per_step": inp["x"].numel() * inp["x"].element_size(),
+                    "d2h_bytes_per_step": y.numel() * y.element_size(),
                     "copies": "own streams, double-buffered, overlapping the neighbouring steps"},
             "gpu_launches": launches,
             "clocks": clocks,

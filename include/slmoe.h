@@ -188,8 +188,10 @@ SLMOE_API int slmoe_route(const slmoe_config *cfg, const void *x, const float *W
  * given) accumulates as in slmoe_route, so the caller zeroes it.
  *
  * Set-up: the first call on each device looks up the scratch's device address with that
- * device current (cudaGetSymbolAddress) and keeps it; later calls on the device reuse the
- * address.
+ * device current (cudaGetSymbolAddress) and keeps it, tied to the id of the device's CUDA
+ * context; later calls in that context reuse the address, and a call made after the context
+ * was destroyed and made again (cudaDeviceReset) looks it up anew.  Make the first call on a
+ * device before capturing any stream into a CUDA graph.
  *
  * Overlap: there is one scratch per device, shared by every call on that device.  Two calls
  * that can run at the same time on one device (different streams not ordered by events, or
@@ -205,6 +207,44 @@ SLMOE_API int slmoe_route_noalloc(const slmoe_config *cfg, const void *x, const 
                 const float *bias, const float *logit_offset, int32_t *topk_idx, float *topk_w,
                 float *scores, int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *slot_pos,
                 uint32_t *hist, int32_t *status, void *stream);
+
+/*
+ * slmoe_topk - biased top-k selection, gate weights and the expert-sorted permutation from
+ * router scores that are already computed (the scores a call of slmoe_route kept, or the
+ * micro-batches of a Quantile Balancing engine that re-routes with updated biases).
+ *   [K3-news] §02 (selection by score plus a per-expert bias that only steers selection);
+ *   [K3-arch] 负载均衡优化 (QB re-centres the biases so that routing by biased score balances
+ *   the loads).  The same kernels and rules as the selection and permutation of slmoe_route:
+ *   choose the k experts with the largest scores[t,e] + bias[e] (fp32 add), ties to the lower
+ *   index, slots by biased score descending; topk_w = chosen raw scores renormalised;
+ *   counts, offsets, perm and slot_pos as in slmoe_route.
+ * Arguments: scores [T,E] fp32; bias [E] fp32; outputs as slmoe_route (all required when
+ *   T > 0; counts and offsets always); status as above (status[0] counts NaN scores);
+ *   workspace of at least slmoe_topk_workspace_size(T, E, k) bytes (per-chunk expert
+ *   counts), 256-byte aligned.  1 <= k <= min(E, 32), E <= 4096, T * k < 2^30.
+ * Errors: SLMOE_EINVAL on a null or misaligned pointer or a bad shape, SLMOE_ENOSPACE on a
+ *   short workspace, SLMOE_ECUDA on a launch failure.
+ */
+SLMOE_API size_t slmoe_topk_workspace_size(int32_t T, int32_t E, int32_t k);
+SLMOE_API int slmoe_topk(const float *scores, const float *bias, int32_t T, int32_t E, int32_t k,
+                int32_t *topk_idx, float *topk_w, int32_t *counts, int32_t *offsets, int32_t *perm,
+                int32_t *slot_pos, int32_t *status, void *workspace, size_t workspace_bytes,
+                void *stream);
+
+/*
+ * slmoe_wait_abort_check - exercises the failure path of the tensor-core kernels: every wait
+ * of theirs on an mbarrier is bounded, and when one runs out the kernel stops all of its
+ * roles, lets copies and MMAs already issued finish, frees its tensor memory, sets
+ * status[2] = 1 and returns, leaving the context usable.  This call launches one tile of
+ * the dense GEMM kernel whose copy-issuing thread is told to issue nothing, so the
+ * MMA-issuing thread's first wait can only run out, after wait_limit_ns nanoseconds (every
+ * wait of this launch has that limit; the layer calls use 4 s).  Nothing is read and
+ * nothing but status is written.  The pages have no counterpart: this is for failure-
+ * detection tests.  status: device int32[4], zeroed by the caller; wait_limit_ns in
+ * (0, 6e10].  Errors: SLMOE_EINVAL on a null or misaligned status or a limit out of range,
+ * SLMOE_ECUDA on a launch failure.
+ */
+SLMOE_API int slmoe_wait_abort_check(int32_t *status, uint64_t wait_limit_ns, void *stream);
 
 /*
  * slmoe_qb_histogram - add per-expert score histograms of one micro-batch.

@@ -14,7 +14,8 @@ from . import _build
 
 __all__ = ["SlmoeError", "Config", "Weights", "WorkspaceLayout", "load", "build", "config",
            "weights", "slmoe_workspace_size", "slmoe_workspace_layout_get", "slmoe_route",
-           "slmoe_route_noalloc", "slmoe_qb_histogram", "slmoe_qb_update", "slmoe_signsgd_update",
+           "slmoe_route_noalloc", "slmoe_topk", "slmoe_topk_workspace_size", "slmoe_wait_abort_check",
+           "slmoe_qb_histogram", "slmoe_qb_update", "slmoe_signsgd_update",
            "slmoe_forward", "slmoe_device_sm_count", "workspace_views", "slmoe_last_error",
            "slmoe_set_stage_events", "slmoe_launch_count", "F32", "BF16", "LIB_PATH"]
 
@@ -71,6 +72,9 @@ def load():
         "slmoe_device_sm_count": (ctypes.c_int, []),
         "slmoe_route": (ctypes.c_int, [CP, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
         "slmoe_route_noalloc": (ctypes.c_int, [CP, P, P, P, P, P, P, P, P, P, P, P, P, P, P]),
+        "slmoe_topk_workspace_size": (SZ, [I32, I32, I32]),
+        "slmoe_topk": (ctypes.c_int, [P, P, I32, I32, I32, P, P, P, P, P, P, P, P, SZ, P]),
+        "slmoe_wait_abort_check": (ctypes.c_int, [P, ctypes.c_uint64, P]),
         "slmoe_qb_histogram": (ctypes.c_int, [P, I64, I32, I32, P, P, P]),
         "slmoe_qb_update": (ctypes.c_int, [P, I32, I32, I32, P, P, P]),
         "slmoe_signsgd_update": (ctypes.c_int, [P, I32, ctypes.c_float, P, P]),
@@ -204,6 +208,25 @@ def slmoe_route_noalloc(cfg, x, W_r, bias, logit_offset, topk_idx, topk_w, score
                                       _ptr(logit_offset), _ptr(topk_idx), _ptr(topk_w), _ptr(scores),
                                       _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(slot_pos),
                                       _ptr(hist), _ptr(status), _stream(stream)))
+
+
+def slmoe_topk_workspace_size(T, E, k) -> int:
+    n = load().slmoe_topk_workspace_size(T, E, k)
+    if n == 0:
+        raise SlmoeError(-1, load().slmoe_last_error().decode())
+    return n
+
+
+def slmoe_topk(scores, bias, T, E, k, topk_idx, topk_w, counts, offsets, perm, slot_pos, status,
+               workspace, stream=None):
+    _check(load().slmoe_topk(_ptr(scores), _ptr(bias), T, E, k, _ptr(topk_idx), _ptr(topk_w),
+                             _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(slot_pos), _ptr(status),
+                             _ptr(workspace), workspace.numel() * workspace.element_size(),
+                             _stream(stream)))
+
+
+def slmoe_wait_abort_check(status, wait_limit_ns, stream=None):
+    _check(load().slmoe_wait_abort_check(_ptr(status), int(wait_limit_ns), _stream(stream)))
 
 
 def slmoe_qb_histogram(scores, T, E, nbins, hist, status=None, stream=None):

@@ -1,5 +1,7 @@
 // The C ABI of slmoe.h: argument validation, the workspace layout, and the sequencing of
 // the kernels of one call on the caller's stream.  Nothing here synchronises the host.
+#include <cudaTypedefs.h>
+
 #include <atomic>
 #include <cmath>
 #include <mutex>
@@ -377,6 +379,51 @@ int slmoe_signsgd_update(const int32_t *counts, int32_t E, float step, float *bi
     return launch_signsgd_update(counts, E, step, bias, static_cast<cudaStream_t>(stream));
 }
 
+size_t slmoe_topk_workspace_size(int32_t T, int32_t E, int32_t k) {
+    if (T < 0 || E < 1 || E > 4096 || k < 1 || k > E || k > 32 || (int64_t)T * k > (int64_t)INT32_MAX / 2) {
+        fail(SLMOE_EINVAL, "T = %d, E = %d, k = %d outside the supported range", T, E, k);
+        return 0;
+    }
+    const size_t nchunks = ((size_t)T + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
+    return align_up((nchunks ? nchunks : 1) * (size_t)E * 4, 256);
+}
+
+int slmoe_topk(const float *scores, const float *bias, int32_t T, int32_t E, int32_t k, int32_t *topk_idx,
+               float *topk_w, int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *slot_pos,
+               int32_t *status, void *workspace, size_t workspace_bytes, void *stream) {
+    g_err[0] = 0;
+    const size_t need = slmoe_topk_workspace_size(T, E, k);
+    if (need == 0) return SLMOE_EINVAL;
+    REQ(counts, "counts");
+    REQ(offsets, "offsets");
+    OPT(status, "status");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        if (cudaMemsetAsync(counts, 0, (size_t)E * 4, st) != cudaSuccess ||
+            cudaMemsetAsync(offsets, 0, ((size_t)E + 1) * 4, st) != cudaSuccess)
+            return check_launch("memset");
+        return SLMOE_OK;
+    }
+    REQ(scores, "scores"); REQ(bias, "bias"); REQ(topk_idx, "topk_idx"); REQ(topk_w, "topk_w");
+    REQ(perm, "perm"); REQ(slot_pos, "slot_pos"); REQ(workspace, "workspace");
+    if (workspace_bytes < need)
+        return fail(SLMOE_ENOSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
+    int32_t *chunk_counts = static_cast<int32_t *>(workspace);
+    const int nchunks = (T + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
+    int rc;
+    if ((rc = launch_topk(scores, bias, T, E, k, topk_idx, topk_w, chunk_counts, status, st))) return rc;
+    if ((rc = launch_scan(chunk_counts, nchunks, E, counts, st))) return rc;
+    return launch_scatter(topk_idx, chunk_counts, counts, T, E, k, offsets, perm, slot_pos, st);
+}
+
+int slmoe_wait_abort_check(int32_t *status, uint64_t wait_limit_ns, void *stream) {
+    g_err[0] = 0;
+    REQ(status, "status");
+    if (wait_limit_ns == 0 || wait_limit_ns > 60000000000ull)
+        return fail(SLMOE_EINVAL, "wait_limit_ns must be in (0, 60 s]");
+    return tc_wait_abort_check(status, wait_limit_ns, static_cast<cudaStream_t>(stream));
+}
+
 int slmoe_forward(const slmoe_config *cfg, const void *x, const slmoe_weights *w,
                   const float *bias, const float *logit_offset, void *y, int32_t *topk_idx_out,
                   uint32_t *hist, int32_t *status, void *workspace, size_t workspace_bytes,
@@ -463,24 +510,66 @@ int slmoe_forward(const slmoe_config *cfg, const void *x, const slmoe_weights *w
 namespace slmoe {
 
 static __device__ __align__(256) unsigned char g_route_scratch[SLMOE_ROUTE_NOALLOC_SCRATCH_BYTES];
-static char *g_route_scratch_ptr[MAX_DEVICES];
+
+// The scratch's device address belongs to the context that loaded this library's device
+// code.  It is cached per device together with that context's id (cuCtxGetId: unique for the
+// life of the process), so a call after cudaDeviceReset, or after the device's context was
+// destroyed and made again, looks the address up anew instead of using a stale one.
+struct ScratchAddr {
+    unsigned long long ctx_id = 0;
+    char *ptr = nullptr;
+};
+static ScratchAddr g_route_scratch_addr[MAX_DEVICES];
 static std::mutex g_route_scratch_mu;
+static PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+static PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+
+static int driver_fn(const char *name, int version, void **fn) {
+    cudaDriverEntryPointQueryResult q;
+    const cudaError_t e = cudaGetDriverEntryPointByVersion(name, fn, version, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !*fn) {
+        cudaGetLastError();
+        return fail(SLMOE_ECUDA, "driver entry point %s not available", name);
+    }
+    return SLMOE_OK;
+}
+
+// Id of the current context, or 0 when the thread has none yet (called with
+// g_route_scratch_mu held).
+static int current_ctx_id(unsigned long long *id) {
+    int rc;
+    if (!g_ctx_current && (rc = driver_fn("cuCtxGetCurrent", 4000, (void **)&g_ctx_current))) return rc;
+    if (!g_ctx_id && (rc = driver_fn("cuCtxGetId", 12000, (void **)&g_ctx_id))) return rc;
+    CUcontext ctx = nullptr;
+    *id = 0;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS) return fail(SLMOE_ECUDA, "cuCtxGetCurrent failed");
+    if (ctx && g_ctx_id(ctx, id) != CUDA_SUCCESS) return fail(SLMOE_ECUDA, "cuCtxGetId failed");
+    return SLMOE_OK;
+}
 
 static int route_scratch(char **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES)
         return fail(SLMOE_ECUDA, "no current device");
     std::lock_guard<std::mutex> lock(g_route_scratch_mu);
-    if (!g_route_scratch_ptr[dev]) {
+    unsigned long long id = 0;
+    int rc = current_ctx_id(&id);
+    if (rc) return rc;
+    ScratchAddr &s = g_route_scratch_addr[dev];
+    if (!s.ptr || id == 0 || s.ctx_id != id) {
+        // set-up: the lookup also makes the device's primary context current if it was not
         char *ptr = nullptr;
         const cudaError_t e = cudaGetSymbolAddress((void **)&ptr, g_route_scratch);
         if (e != cudaSuccess || !ptr) {
             cudaGetLastError();
             return fail(SLMOE_ECUDA, "device address of the routing scratch: %s", cudaGetErrorString(e));
         }
-        g_route_scratch_ptr[dev] = ptr;
+        if ((rc = current_ctx_id(&id))) return rc;
+        if (id == 0) return fail(SLMOE_ECUDA, "no current CUDA context after set-up");
+        s.ptr = ptr;
+        s.ctx_id = id;
     }
-    *out = g_route_scratch_ptr[dev];
+    *out = s.ptr;
     return SLMOE_OK;
 }
 

@@ -7,9 +7,18 @@
 
 namespace slmoe {
 
-// Every mbarrier wait gives up after this long (%globaltimer, ns): the kernel then sets its
-// abort flag, every role leaves its loop and the launch reports status[2].
+// Every mbarrier wait gives up after this long (%globaltimer, ns) unless a launch sets its own
+// limit: the kernel then sets its abort flag, every role leaves its loop and the launch
+// reports status[2].
 constexpr uint64_t WAIT_LIMIT_NS = 4000000000ull;
+
+// Bounded-wait state of one thread block, in shared memory: the abort flag every role polls
+// and the time limit of each wait.
+struct WaitCtl {
+    int abort;
+    int pad;
+    unsigned long long limit_ns;
+};
 
 __device__ __forceinline__ uint32_t su32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -40,22 +49,28 @@ __device__ __forceinline__ bool mbar_try(uint32_t addr, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait for the phase of the given parity.  False = gave up (abort flag set, or set
-// by another role meanwhile).
-__device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, volatile int *abort_flag) {
+// Bounded wait for the phase of the given parity.  False = gave up (the limit ran out, or
+// another role set the abort flag meanwhile).
+__device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, volatile WaitCtl *wc) {
     const uint32_t a = su32(b);
     if (mbar_try(a, parity)) return true;
     const uint64_t t0 = gtimer();
+    const uint64_t limit = wc->limit_ns;
     for (uint32_t it = 1;; ++it) {
         if (mbar_try(a, parity)) return true;
         if ((it & 255u) == 0) {
-            if (*abort_flag) return false;
-            if (gtimer() - t0 > WAIT_LIMIT_NS) {
-                *abort_flag = 1;
+            if (wc->abort) return false;
+            if (gtimer() - t0 > limit) {
+                wc->abort = 1;
                 return false;
             }
         }
     }
+}
+// Set-up of a block's wait state by one thread (limit_ns = 0 takes the default).
+__device__ __forceinline__ void wait_ctl_init(volatile WaitCtl *wc, unsigned long long limit_ns) {
+    wc->abort = 0;
+    wc->limit_ns = limit_ns ? limit_ns : WAIT_LIMIT_NS;
 }
 // The same wait with its own time limit and no abort flag: used to drain copies still in
 // flight after an abort, so that nothing lands in shared memory after the block exits.

@@ -93,7 +93,7 @@ __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.
 // blockIdx.x, blockIdx.x + gridDim.x, ...; an id >= tiles ends every role's loop.
 constexpr int TQ = 2;
 __device__ __forceinline__ bool tq_push(int *ids, uint64_t *full, uint64_t *empty, int &slot, uint32_t &ph,
-                                        int tile, volatile int *abort_flag) {
+                                        int tile, volatile WaitCtl *abort_flag) {
     if (!mbar_wait(&empty[slot], ph ^ 1, abort_flag)) return false;
     ids[slot] = tile;
     mbar_arrive(&full[slot]);
@@ -102,7 +102,7 @@ __device__ __forceinline__ bool tq_push(int *ids, uint64_t *full, uint64_t *empt
 }
 // pop for a single consumer thread (arrives itself) or a warp (lane 0 arrives after the warp read)
 __device__ __forceinline__ bool tq_pop(int *ids, uint64_t *full, uint64_t *empty, int &slot, uint32_t &ph,
-                                       int &tile, volatile int *abort_flag, bool warp_wide) {
+                                       int &tile, volatile WaitCtl *abort_flag, bool warp_wide) {
     if (!mbar_wait(&full[slot], ph, abort_flag)) return false;
     tile = ids[slot];
     if (warp_wide) {
@@ -156,6 +156,10 @@ struct DenseArgs {
     int ksplit, tiles_mn;
     float *partial;
     long long ldp;
+    unsigned long long wait_limit_ns;   // 0 = the default limit of every bounded wait
+    // failure-path check only: the producer issues no copies, so the MMA thread's wait on
+    // the first stage can only run out (nothing is in flight when the kernel aborts)
+    int stall_producer;
 };
 
 // Tile order of the dense kernel: bands of DENSE_BAND row tiles, rows fastest inside a band,
@@ -216,7 +220,7 @@ __global__ void __launch_bounds__(DenseCfg<BN, EPI, PACC>::THREADS, 1) dense_ker
     uint64_t *mma_drain = tq_empty + TQ;
     int *tq_ids = reinterpret_cast<int *>(mma_drain + 1);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tq_ids + TQ);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile WaitCtl *abort_flag = reinterpret_cast<volatile WaitCtl *>(tmem_slot + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int p_stage = 0;                  // the TMA producer's ring position, kept for the drain
@@ -236,7 +240,7 @@ __global__ void __launch_bounds__(DenseCfg<BN, EPI, PACC>::THREADS, 1) dense_ker
             mbar_init(&tq_full[q], 1);
             mbar_init(&tq_empty[q], 1 + Cfg::EPI_WARPS);
         }
-        *abort_flag = 0;
+        wait_ctl_init(abort_flag, a.wait_limit_ns);
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
@@ -261,6 +265,7 @@ __global__ void __launch_bounds__(DenseCfg<BN, EPI, PACC>::THREADS, 1) dense_ker
             const int n0 = tn * Cfg::BN_OUT;
             for (int s = 0; s < a.nseg; ++s) {
                 for (int kb = 0; kb < a.kblocks[s]; ++kb) {
+                    if (a.stall_producer) continue;
                     if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) goto done;
                     mbar_expect_tx(&full[stage], Cfg::STAGE);
                     const uint32_t sa = su32(smem + stage * Cfg::STAGE);
@@ -421,7 +426,7 @@ __global__ void __launch_bounds__(DenseCfg<BN, EPI, PACC>::THREADS, 1) dense_ker
     }
 done:
     __syncthreads();
-    if (*abort_flag) {   // every role has stopped: let copies and MMAs in flight finish
+    if (abort_flag->abort) {   // every role has stopped: let copies and MMAs in flight finish
         if (warp == 0 && lane == 0) drain_ring(full, STAGES, p_stage, p_phase, p_wrapped);
         if (warp == 1 && lane == 0) {
             umma_commit(mma_drain);
@@ -433,7 +438,7 @@ done:
         tc_after();
         tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
     }
-    if (threadIdx.x == 0 && *abort_flag && a.status) atomicExch(&a.status[ST_TIMEOUT], 1);
+    if (threadIdx.x == 0 && abort_flag->abort && a.status) atomicExch(&a.status[ST_TIMEOUT], 1);
 }
 
 // ---------------------------------------------------------------- router logits
@@ -492,7 +497,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_kernel(const __grid_cons
     uint64_t *mma_drain = tq_empty + TQ;
     int *tq_ids = reinterpret_cast<int *>(mma_drain + 1);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tq_ids + TQ);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile WaitCtl *abort_flag = reinterpret_cast<volatile WaitCtl *>(tmem_slot + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -509,7 +514,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) router_kernel(const __grid_cons
             mbar_init(&tq_full[q], 1);
             mbar_init(&tq_empty[q], 9);
         }
-        *abort_flag = 0;
+        wait_ctl_init(abort_flag, a.wait_limit_ns);
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc(tmem_slot, 512);
@@ -670,7 +675,7 @@ done:
         tc_after();
         tmem_dealloc(tmem_base, 512);
     }
-    if (threadIdx.x == 0 && *abort_flag && a.status) atomicExch(&a.status[ST_TIMEOUT], 1);
+    if (threadIdx.x == 0 && abort_flag->abort && a.status) atomicExch(&a.status[ST_TIMEOUT], 1);
 }
 
 // ---------------------------------------------------------------- grouped (routed experts)
@@ -728,6 +733,7 @@ struct GroupedArgs {
     int out_cols;
     float beta1, beta2;
     int32_t *status;
+    unsigned long long wait_limit_ns;   // 0 = the default limit of every bounded wait
 };
 
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *map, uint64_t *bar,
@@ -846,7 +852,7 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
     uint64_t *tempty = tfull + NBUF;
     uint64_t *mma_drain = tempty + NBUF;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_drain + 1);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile WaitCtl *abort_flag = reinterpret_cast<volatile WaitCtl *>(tmem_slot + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int p_stage = 0;                  // the weight producer's ring position, kept for the drain
@@ -870,7 +876,7 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
             mbar_init(&tfull[b], 1);
             mbar_init(&tempty[b], Cfg::EPI_WARPS);
         }
-        *abort_flag = 0;
+        wait_ctl_init(abort_flag, a.wait_limit_ns);
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc(tmem_slot, 512);
@@ -1065,7 +1071,7 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
     }
 done:
     __syncthreads();
-    if (*abort_flag) {   // every role has stopped: let copies and MMAs in flight finish
+    if (abort_flag->abort) {   // every role has stopped: let copies and MMAs in flight finish
         if (warp == 0 && lane == 0) {
             drain_ring(a_full, AST, p_stage, p_phase, p_wrapped);
         }
@@ -1079,7 +1085,7 @@ done:
         tc_after();
         tmem_dealloc(tmem_base, 512);
     }
-    if (threadIdx.x == 0 && *abort_flag && a.status) atomicExch(&a.status[ST_TIMEOUT], 1);
+    if (threadIdx.x == 0 && abort_flag->abort && a.status) atomicExch(&a.status[ST_TIMEOUT], 1);
 }
 
 // ---------------------------------------------------------------- router weight split
@@ -1343,6 +1349,31 @@ int tc_forward_back(const slmoe_config *c, const slmoe_weights *w, const TcForwa
     }
     stage_event(8, st);
     return SLMOE_OK;
+}
+
+// One tile of the dense kernel whose producer issues no copies: the MMA thread's first wait
+// runs out after wait_limit_ns, every role leaves its loop, there is nothing in flight to
+// drain, TMEM is freed and status[2] is set.  No operand is read (the tensor maps are never
+// used) and nothing but status is written (M = 0: no output row exists).
+int tc_wait_abort_check(int32_t *status, unsigned long long wait_limit_ns, cudaStream_t st) {
+    using Cfg = DenseCfg<64, EPI_BF16, 1>;
+    TmaPack maps;
+    memset(&maps, 0, sizeof(maps));
+    DenseArgs a = {};
+    a.M = 0;
+    a.N = 64;
+    a.nseg = 1;
+    a.kblocks[0] = 1;
+    a.tiles_n = 1;
+    a.tiles = 1;
+    a.status = status;
+    a.wait_limit_ns = wait_limit_ns;
+    a.stall_producer = 1;
+    auto kern = dense_kernel<64, EPI_BF16, 1>;
+    int rc = set_smem(kern, Cfg::SMEM);
+    if (rc) return rc;
+    kern<<<1, Cfg::THREADS, Cfg::SMEM, st>>>(maps, a);
+    return check_launch("dense_kernel (wait abort check)");
 }
 
 }  // namespace slmoe

@@ -40,4 +40,8 @@ int tc_worklists(const slmoe_config *c, const TcForward &f, cudaStream_t st);
 int tc_forward_back(const slmoe_config *c, const slmoe_weights *w, const TcForward &f, void *y,
                     cudaStream_t st);
 
+// Failure-path check: one launch of a tensor-core kernel whose bounded waits must run out
+// (see slmoe_wait_abort_check).
+int tc_wait_abort_check(int32_t *status, unsigned long long wait_limit_ns, cudaStream_t st);
+
 }  // namespace slmoe

@@ -123,6 +123,22 @@ def _normal(shape, std, seed, tid, device, chunk_rows=None):
     return out
 
 
+def logit_offset(shape: LayerShape | str, seed: int = 0, device="cpu", heavy_skew=False):
+    """The per-expert router logit offset mu of a layer (None when the shape has none):
+    mu_e ~ N(0, mu_std^2); heavy skew adds +2 on a seeded 10 % of the experts."""
+    if isinstance(shape, str):
+        shape = LAYERS[shape]
+    if shape.mu_std <= 0:
+        return None
+    E = shape.E
+    mu = _normal((E,), shape.mu_std, seed, "mu", device)
+    if heavy_skew:
+        gs = _gen(seed, "skew", device)
+        hot = torch.randperm(E, generator=gs, device=device)[: math.ceil(0.1 * E)]
+        mu[hot] += 2.0
+    return mu
+
+
 def layer_inputs(shape: LayerShape | str, seed: int = 0, device="cpu", heavy_skew=False,
                  gamma_ones=False, T: int | None = None):
     """All inputs of one layer call as torch tensors on ``device``.
@@ -154,13 +170,7 @@ def layer_inputs(shape: LayerShape | str, seed: int = 0, device="cpu", heavy_ske
     W_r = _normal((E, d), 1.0 / math.sqrt(d), seed, "W_r", device)
     bias = _normal((E,), shape.bias_std, seed, "bias", device) if shape.bias_std > 0 else \
         torch.zeros(E, dtype=torch.float32, device=device)
-    mu = None
-    if shape.mu_std > 0:
-        mu = _normal((E,), shape.mu_std, seed, "mu", device)
-        if heavy_skew:
-            gs = _gen(seed, "skew", device)
-            hot = torch.randperm(E, generator=gs, device=device)[: math.ceil(0.1 * E)]
-            mu[hot] += 2.0
+    mu = logit_offset(shape, seed, device, heavy_skew)
     if gamma_ones:
         gamma = torch.ones(dl, dtype=torch.float32, device=device)
     else:

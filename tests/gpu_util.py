@@ -68,3 +68,71 @@ def run_route(cfg, inp, hist=None, status=None):
                     hist, status, ws)
     torch.cuda.synchronize()
     return {n: v.cpu() for n, v in b.items()}
+
+
+def host(a):
+    """A numpy copy of a torch tensor (any device) or an array-like."""
+    if hasattr(a, "detach"):
+        return a.detach().cpu().numpy()
+    return np.asarray(a)
+
+
+def check_topk_valid(scores_f32, bias_f32, sel, w):
+    """Every token's selection is a valid biased top-k under the GPU's own fp32 scores, with
+    the stated rules (vectorised over tokens): k distinct experts, slots ordered by fp32
+    biased score descending with ties to the lower index, every unchosen expert below the
+    weakest chosen one (or equal to it with a higher index), gate weights summing to 1."""
+    s = host(scores_f32).astype(np.float32)
+    T, E = s.shape
+    k = sel.shape[1]
+    if T == 0:
+        return
+    assert sel.min() >= 0 and sel.max() < E
+    vb = s + host(bias_f32).astype(np.float32)[None, :]          # the fp32 add of the kernel
+    srt = np.sort(sel, axis=1)
+    assert np.all(srt[:, 1:] != srt[:, :-1]), "repeated expert in a token's selection"
+    rows = np.arange(T)[:, None]
+    v = vb[rows, sel]
+    nxt_ok = (v[:, :-1] > v[:, 1:]) | ((v[:, :-1] == v[:, 1:]) & (sel[:, :-1] < sel[:, 1:]))
+    assert np.all(nxt_ok), "slot order"
+    worst = v[:, -1]
+    worst_idx = sel[:, -1]
+    chosen = np.zeros((T, E), bool)
+    chosen[rows, sel] = True
+    idx = np.arange(E)[None, :]
+    ok = chosen | (vb < worst[:, None]) | ((vb == worst[:, None]) & (idx > worst_idx[:, None]))
+    bad = np.nonzero(~ok.all(axis=1))[0]
+    assert bad.size == 0, f"tokens {bad[:5]} leave out an expert that beats a chosen one"
+    assert np.all(np.abs(np.asarray(w, np.float64).sum(axis=1) - 1.0) < 1e-5)
+
+
+def check_selection_and_permutation(scores_ref, scores_gpu, bias, sel, w, counts, offsets, perm,
+                                    slot_pos, score_tol, near_tie_bound):
+    """Bit-exact selection on every token whose oracle k-th/(k+1)-th biased gap is at least
+    NEAR_TIE, gate weights within 1e-5, validity of every token's selection, and the
+    permutation outputs equal to the oracle's permutation of the GPU's selection.  Returns
+    (near-tie tokens, max score error); asserts the near-tie count <= near_tie_bound."""
+    import oracle
+    T, k = sel.shape
+    E = scores_gpu.shape[1]
+    s_gpu = host(scores_gpu).astype(np.float32)
+    serr = float(np.max(np.abs(s_gpu.astype(np.float64) - scores_ref))) if T else 0.0
+    assert serr <= score_tol, f"score error {serr:.2e}"
+    sel_ref, gates_ref, gap = oracle.select_topk(scores_ref, bias, k)
+    keep = gap >= NEAR_TIE
+    n_tie = int((~keep).sum())
+    assert n_tie <= near_tie_bound, f"{n_tie} near-tie tokens > bound {near_tie_bound}"
+    o_gpu, o_ref = np.argsort(sel, axis=1), np.argsort(sel_ref, axis=1)
+    rows = np.arange(T)[:, None]
+    e_gpu, e_ref = sel[rows, o_gpu], sel_ref[rows, o_ref]
+    diff = np.nonzero(keep & np.any(e_gpu != e_ref, axis=1))[0]
+    assert diff.size == 0, f"selection differs on tokens {diff[:5]}"
+    werr = np.abs(np.asarray(w, np.float64)[rows, o_gpu] - gates_ref[rows, o_ref])[keep]
+    assert werr.size == 0 or werr.max() <= 1e-5, f"gate weight error {werr.max():.2e}"
+    check_topk_valid(s_gpu, bias, sel, w)
+    c_ref, off_ref, perm_ref, sp_ref = oracle.permutation(sel, E)
+    assert np.array_equal(np.asarray(counts), c_ref)
+    assert np.array_equal(np.asarray(offsets), off_ref)
+    assert np.array_equal(np.asarray(perm)[:T * k], perm_ref)
+    assert np.array_equal(np.asarray(slot_pos).reshape(-1)[:T * k].reshape(T, k), sp_ref)
+    return n_tie, serr

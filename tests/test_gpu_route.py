@@ -7,7 +7,8 @@ import torch
 import oracle
 import synthetic
 import latent_space_experts_gb300 as lse
-from gpu_util import NEAR_TIE, need_gpu, run_route, to_dev
+from gpu_util import (NEAR_TIE, check_selection_and_permutation, need_gpu, route_buffers, run_route,
+                      to_dev)
 
 # Router scores must stay within half the near-tie gap of the oracle: then every token whose
 # k-th/(k+1)-th biased gap is >= 1e-5 is decided the same way on both sides.
@@ -141,3 +142,77 @@ def test_route_empty_batch():
                     None, ws)
     torch.cuda.synchronize()
     assert counts.sum().item() == 0 and offsets.sum().item() == 0
+
+
+def gpu_topk(scores, bias, k, status=None):
+    """slmoe_topk through the C ABI on a [T, E] fp32 score matrix already on the device."""
+    T, E = scores.shape
+    b = route_buffers(T, E, k)
+    del b["scores"]
+    ws = torch.empty(lse.slmoe_topk_workspace_size(T, E, k), dtype=torch.uint8, device="cuda")
+    lse.slmoe_topk(scores, bias, T, E, k, b["topk_idx"], b["topk_w"], b["counts"], b["offsets"],
+                   b["perm"], b["slot_pos"], status, ws)
+    torch.cuda.synchronize()
+    return {n: v.cpu().numpy() for n, v in b.items()}
+
+
+def check_topk_call(scores, bias, k, near_tie_bound):
+    out = gpu_topk(scores, bias, k)
+    s_ref = scores.double().cpu().numpy()          # the very fp32 scores, widened exactly
+    return check_selection_and_permutation(
+        s_ref, scores, bias, out["topk_idx"], out["topk_w"], out["counts"], out["offsets"],
+        out["perm"], out["slot_pos"], 0.0, near_tie_bound), out
+
+
+@pytest.mark.parametrize("micro_batch,bias_std", [(0, 0.0), (1, 0.05)])
+def test_topk_from_scores_at_the_qb_engine_size(micro_batch, bias_std):
+    """65536 tokens x 896 experts, top-16, from the QB engine's fp32 scores."""
+    need_gpu()
+    q = synthetic.QB
+    sc = synthetic.qb_scores(micro_batch, q, device="cuda")
+    g = torch.Generator(device="cpu").manual_seed(77 + micro_batch)
+    bias = (torch.randn(q.E, generator=g) * bias_std).cuda()
+    (n_tie, _), out = check_topk_call(sc, bias, q.k, int(0.05 * q.T))
+    assert out["counts"].sum() == q.T * q.k
+    print(f"QB-engine top-k: near-tie tokens {n_tie}/{q.T}")
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 896, 16), (333, 7, 3), (100, 64, 32), (5, 4096, 32),
+                                   (1000, 1, 1), (4097, 300, 10)])
+def test_topk_from_scores_edge_shapes(T, E, k):
+    need_gpu()
+    g = torch.Generator(device="cpu").manual_seed(T * 31 + E)
+    sc = torch.sigmoid(torch.randn(T, E, generator=g)).cuda()
+    bias = (torch.randn(E, generator=g) * 0.1).cuda()
+    check_topk_call(sc, bias, k, T)
+
+
+def test_topk_exact_ties_nan_and_empty():
+    need_gpu()
+    T, E, k = 40, 16, 4
+    sc = torch.full((T, E), 0.5, device="cuda")
+    sc[3, 5] = float("nan")
+    bias = torch.zeros(E, device="cuda")
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    out = gpu_topk(sc, bias, k, status)
+    assert int(status[0]) == 1
+    exp = np.tile(np.arange(4), (T, 1))
+    assert np.array_equal(out["topk_idx"], exp)
+    assert np.allclose(out["topk_w"], 0.25)
+    ws = torch.empty(lse.slmoe_topk_workspace_size(0, E, k), dtype=torch.uint8, device="cuda")
+    counts = torch.full((E,), 3, dtype=torch.int32, device="cuda")
+    offsets = torch.full((E + 1,), 3, dtype=torch.int32, device="cuda")
+    lse.slmoe_topk(None, None, 0, E, k, None, None, counts, offsets, None, None, None, ws)
+    torch.cuda.synchronize()
+    assert int(counts.abs().sum()) == 0 and int(offsets.abs().sum()) == 0
+
+
+def test_route_k3_router_shape():
+    """slmoe_route at the K3 router's widths (d = 7168, E = 896, k = 16) with a ragged
+    number of tokens: the top-k kernel's looping path for large E and several scan chunks."""
+    need_gpu()
+    shp = synthetic.shape_with("k3_decode", T=1000, d_latent=64, I=64, n_shared=0)
+    inp = synthetic.layer_inputs(shp, seed=9)
+    excluded, serr = check_route(shp, inp, score_tol=SCORE_TOL)
+    assert excluded <= 0.05 * shp.T
+    print(f"K3 router shape: near-tie tokens excluded {excluded}/{shp.T}, max score err {serr:.2e}")

@@ -158,3 +158,32 @@ def test_router_weight_split_is_exact_in_three_bf16_pieces():
     x = torch.randn(300000).to(torch.bfloat16)
     for piece in (hi, mid, lo):                                     # products exact in fp32
         assert torch.equal((x.float() * piece.float()).double(), x.double() * piece.double())
+
+
+@pytest.mark.parametrize("T,E,k", [(-1, 8, 2), (10, 0, 1), (10, 8, 9), (10, 64, 33), (10, 5000, 4),
+                                   (1 << 30, 64, 2)])
+def test_topk_workspace_rejects_bad_shapes(lib, T, E, k):
+    assert lib.slmoe_topk_workspace_size(T, E, k) == 0
+    assert lib.slmoe_last_error().decode() != ""
+
+
+def test_topk_workspace_size(lib):
+    # one int32 count per (16-token chunk, expert), rounded up to 256 bytes
+    assert lib.slmoe_topk_workspace_size(65536, 896, 16) == 4096 * 896 * 4
+    assert lib.slmoe_topk_workspace_size(17, 3, 1) == 256
+    assert lib.slmoe_topk_workspace_size(0, 8, 2) > 0
+
+
+def test_topk_and_abort_check_validate_on_the_host(lib):
+    """Null or misaligned pointers and bad limits are refused before any CUDA call."""
+    fake = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 4)
+    ws = lib.slmoe_topk_workspace_size(64, 16, 2)
+    args = lambda counts: (fake, fake, 64, 16, 2, fake, fake, counts, fake, fake, fake, None, fake, ws, None)
+    assert lib.slmoe_topk(*args(None)) == -1
+    assert lib.slmoe_topk(*args(odd)) == -1
+    assert lib.slmoe_topk(fake, fake, 64, 16, 2, fake, fake, fake, fake, fake, fake, None, fake, ws - 256,
+                          None) == -4
+    assert lib.slmoe_wait_abort_check(None, 1000, None) == -1
+    assert lib.slmoe_wait_abort_check(fake, 0, None) == -1
+    assert lib.slmoe_wait_abort_check(fake, 10 ** 12, None) == -1
