@@ -196,13 +196,45 @@ def oracle_sample(shp, inp_cpu, n_tok):
     return n_tok / dt, dt
 
 
+def _blas_threads_fns():
+    """(get, set) of the BLAS thread count of the OpenBLAS that numpy loaded, looked up in the
+    process's own mapped libraries (no extra package needed); (None, None) if not found."""
+    import ctypes
+    import numpy  # noqa: F401  (loads the BLAS)
+    try:
+        paths = {l.split()[-1] for l in open("/proc/self/maps") if "blas" in l.lower() and ".so" in l}
+    except OSError:
+        return None, None
+    for path in sorted(paths):
+        try:
+            lib = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for get, set_ in (("scipy_openblas_get_num_threads64_", "scipy_openblas_set_num_threads64_"),
+                          ("openblas_get_num_threads64_", "openblas_set_num_threads64_"),
+                          ("openblas_get_num_threads", "openblas_set_num_threads")):
+            if hasattr(lib, get) and hasattr(lib, set_):
+                g, s = getattr(lib, get), getattr(lib, set_)
+                g.restype = ctypes.c_int
+                s.argtypes = [ctypes.c_int]
+                return g, s
+    return None, None
+
+
 def oracle_sample_threads(shp, inp_cpu, n_tok, threads):
-    """oracle_sample with the BLAS thread pools limited to `threads` (None: as configured)."""
+    """oracle_sample with the BLAS limited to `threads` threads (None: as configured).
+    Returns (tokens/s, seconds) or (None, None) when the BLAS thread count cannot be set."""
     if threads is None:
         return oracle_sample(shp, inp_cpu, n_tok)
-    import threadpoolctl
-    with threadpoolctl.threadpool_limits(limits=threads):
+    get, set_ = _blas_threads_fns()
+    if get is None:
+        return None, None
+    before = get()
+    set_(threads)
+    try:
         return oracle_sample(shp, inp_cpu, n_tok)
+    finally:
+        set_(before)
 
 
 def profiled_traffic(stage):
@@ -228,13 +260,11 @@ def profiled_traffic(stage):
 
 
 def cpu_cores():
-    try:
-        import threadpoolctl
-        info = threadpoolctl.threadpool_info()
-        n = max((i.get("num_threads", 1) for i in info), default=1)
-        return int(n)
-    except Exception:
-        return os.cpu_count() or 1
+    """Threads the oracle's BLAS runs on (the host's core count if it cannot be read)."""
+    get, _ = _blas_threads_fns()
+    if get is not None:
+        return int(get())
+    return os.cpu_count() or 1
 
 
 def reference_tokens(shp, inp_cpu, args):
@@ -667,7 +697,8 @@ def main():
         cpu_base = {"value": round(v_all, 3), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                     "sample": f"the first {n_tok} tokens of the {args.workload} batch, fp64 numpy "
                               f"({dt_all:.1f} s on all cores)",
-                    "one_thread": {"value": round(v_one, 3), "seconds": round(dt_one, 1)}}
+                    "one_thread": ({"value": round(v_one, 3), "seconds": round(dt_one, 1)} if v_one
+                                   else "BLAS thread count not settable here")}
 
     if rank == 0:
         tokens = shp.T
