@@ -1,7 +1,7 @@
 """Oracle for the Stable LatentMoE forward path and its Quantile Balancing engine.
 
 TEST INFRASTRUCTURE ONLY.  This module is a plain, slow, obviously correct fp64 CPU
-statement of what the layer computes.  Only the tests, the smoke check of
+statement of what the layer computes, forward and backward.  Only the tests, the smoke check of
 ``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` may import it; the product
 library never does, and it shares no code with the CUDA path.
 
@@ -299,3 +299,137 @@ def signsgd_update(counts, bias, step):
 def expert_output(inp, e, h):
     """y_e = W2[e] . h for given hidden rows (used to check one stage)."""
     return f64(h) @ f64(inp["W2"][int(e)]).T
+
+
+# ----------------------------------------------------------------------------------------
+# Backward pass of the layer  ([K3-arch] SiTU激活优化 / 归一化策略调整 / 负载均衡优化;
+# [SLMoE] 训练基础设施).  The pages train this layer; its gradient is the chain rule of the
+# forward above, written out step by step in the same notation.  The selection (top-k of
+# s + b) is piecewise constant and passes no gradient; the bias b is not trained by
+# gradients (QB sets it), and the logit offset mu is an input of the synthetic workload.
+# ----------------------------------------------------------------------------------------
+
+def situ_grad(g, beta=BETA1):
+    """d/dg [beta tanh(g/beta) sigmoid(g)] = sech^2(g/beta) sigmoid(g)
+    + beta tanh(g/beta) sigmoid(g) (1 - sigmoid(g))."""
+    g = np.asarray(g, dtype=np.float64)
+    th = np.tanh(g / beta)
+    sg = sigmoid(g)
+    return (1.0 - th * th) * sg + beta * th * sg * (1.0 - sg)
+
+
+def softcap_grad(u, beta=BETA2):
+    """d/du [beta tanh(u/beta)] = 1 - tanh^2(u/beta)."""
+    th = np.tanh(np.asarray(u, dtype=np.float64) / beta)
+    return 1.0 - th * th
+
+
+def situ_glu_backward(gu, dh, beta1=BETA1, beta2=BETA2):
+    """Gradient of h = SiTU(g) * softcap(u) with respect to [g | u] (same layout as gu)."""
+    half = gu.shape[-1] // 2
+    g, u = gu[..., :half], gu[..., half:]
+    dg = dh * softcap(u, beta2) * situ_grad(g, beta1)
+    du = dh * situ(g, beta1) * softcap_grad(u, beta2)
+    return np.concatenate([dg, du], axis=-1)
+
+
+def rmsnorm_backward(c, gamma, dz, eps=EPS):
+    """z = gamma * c / r with r = sqrt(mean(c^2) + eps):
+    dc = gamma dz / r - c * sum(gamma dz c) / (n r^3);  dgamma = sum_t dz * c / r."""
+    c, dz, gm = f64(c), f64(dz), f64(gamma)
+    n = c.shape[1]
+    r = np.sqrt(np.mean(c * c, axis=1, keepdims=True) + eps)
+    gdz = gm[None, :] * dz
+    dc = gdz / r - c * np.sum(gdz * c, axis=1, keepdims=True) / (n * r ** 3)
+    dgamma = np.sum(dz * c / r, axis=0)
+    return dc, dgamma
+
+
+def backward(inp, k, dy, beta1=BETA1, beta2=BETA2, eps=EPS, forced_topk_idx=None):
+    """Gradients of sum(dy * y) for one layer call, in fp64.
+
+    dy [T, d] is the gradient arriving at the layer output y.  Returns dx [T, d] and the
+    weight gradients dW_r [E, d], dW_in [d_l, d], dW13 [E, 2I, d_l], dW2 [E, d_l, I],
+    dgamma [d_l], dW_out [d, d_l], dW13_s [n_s, 2I_s, d], dW2_s [n_s, d, I_s], plus the
+    intermediates dz, dc, dg (gate weights), dx_lat and dlogit (router logits, [T, E]).
+    The selection is the oracle's own unless forced_topk_idx gives it.
+    """
+    x = f64(inp["x"])
+    T, d = x.shape
+    dy = f64(dy)
+    W_r, W_in, W_out = f64(inp["W_r"]), f64(inp["W_in"]), f64(inp["W_out"])
+    E = W_r.shape[0]
+
+    # forward quantities the gradient needs (recomputed here, in fp64)
+    s = router_scores(x, W_r, inp.get("logit_offset"))
+    if forced_topk_idx is None:
+        sel, gates, _ = select_topk(s, inp["bias"], k)
+    else:
+        sel = np.asarray(forced_topk_idx).astype(np.int64)
+        chosen = s[np.arange(T)[:, None], sel]
+        gates = chosen / chosen.sum(axis=1, keepdims=True)
+    x_lat = x @ W_in.T
+    d_lat = x_lat.shape[1]
+    W13, W2 = inp["W13"], inp["W2"]
+    c = np.zeros((T, d_lat))
+    ye_of = {}
+    for e in np.unique(sel):
+        tt, jj = np.nonzero(sel == e)
+        gu = x_lat[tt] @ f64(W13[int(e)]).T
+        h = situ_glu(gu, beta1, beta2)
+        ye = h @ f64(W2[int(e)]).T
+        ye_of[int(e)] = (tt, jj, gu, h, ye)
+        np.add.at(c, tt, gates[tt, jj][:, None] * ye)
+    r = np.sqrt(np.mean(c * c, axis=1, keepdims=True) + eps)
+    z = f64(inp["gamma"])[None, :] * c / r
+
+    # up-projection y_routed = z W_out^T
+    dW_out = dy.T @ z
+    dz = dy @ W_out
+    # RMSNorm after the combine
+    dc, dgamma = rmsnorm_backward(c, inp["gamma"], dz, eps)
+
+    # combine c_t = sum_j g[t,j] y_e(t,j), then the routed experts
+    dg = np.zeros((T, k))
+    dx_lat = np.zeros_like(x_lat)
+    dW13 = np.zeros((E,) + tuple(W13.shape[1:]))
+    dW2 = np.zeros((E,) + tuple(W2.shape[1:]))
+    for e, (tt, jj, gu, h, ye) in ye_of.items():
+        dg[tt, jj] = np.sum(dc[tt] * ye, axis=1)
+        dye = gates[tt, jj][:, None] * dc[tt]
+        dW2[e] = dye.T @ h
+        dh = dye @ f64(W2[e])
+        dgu = situ_glu_backward(gu, dh, beta1, beta2)
+        dW13[e] = dgu.T @ x_lat[tt]
+        np.add.at(dx_lat, tt, dgu @ f64(W13[e]))
+
+    # latent down-projection x_lat = x W_in^T
+    dW_in = dx_lat.T @ x
+    dx = dx_lat @ W_in
+
+    # router: g_j = s_j / S over the chosen experts, s = sigmoid(logit)
+    rows = np.arange(T)[:, None]
+    s_sel = s[rows, sel]
+    S = s_sel.sum(axis=1, keepdims=True)
+    ds_sel = (dg - np.sum(gates * dg, axis=1, keepdims=True)) / S
+    dlogit = np.zeros((T, E))
+    dlogit[rows, sel] = ds_sel * s_sel * (1.0 - s_sel)
+    dW_r = dlogit.T @ x
+    dx += dlogit @ W_r
+
+    # shared experts on the full width
+    W13_s, W2_s = inp["W13_s"], inp["W2_s"]
+    dW13_s = np.zeros(W13_s.shape)
+    dW2_s = np.zeros(W2_s.shape)
+    for si in range(W13_s.shape[0]):
+        gu = x @ f64(W13_s[si]).T
+        h = situ_glu(gu, beta1, beta2)
+        dW2_s[si] = dy.T @ h
+        dh = dy @ f64(W2_s[si])
+        dgu = situ_glu_backward(gu, dh, beta1, beta2)
+        dW13_s[si] = dgu.T @ x
+        dx += dgu @ f64(W13_s[si])
+
+    return dict(dx=dx, dW_r=dW_r, dW_in=dW_in, dW13=dW13, dW2=dW2, dgamma=dgamma, dW_out=dW_out,
+                dW13_s=dW13_s, dW2_s=dW2_s, dz=dz, dc=dc, dg=dg, dx_lat=dx_lat, dlogit=dlogit,
+                topk_idx=sel, gates=gates, c=c, z=z)
