@@ -320,6 +320,56 @@ SLMOE_API int slmoe_forward(const slmoe_config *cfg, const void *x, const slmoe_
                   int32_t *topk_idx_out, uint32_t *hist, int32_t *status,
                   void *workspace, size_t workspace_bytes, void *stream);
 
+/* Weight gradients of one layer, all fp32 and laid out as the weights (slmoe_weights). */
+typedef struct slmoe_grads {
+    float *dW_r;         /* [E, d]                   */
+    float *dW_in;        /* [d_latent, d]            */
+    float *dW13;         /* [E, 2I, d_latent]        */
+    float *dW2;          /* [E, d_latent, I]         */
+    float *dgamma;       /* [d_latent]               */
+    float *dW_out;       /* [d, d_latent]            */
+    float *dW13_s;       /* [n_shared, 2I_shared, d] */
+    float *dW2_s;        /* [n_shared, d, I_shared]  */
+} slmoe_grads;
+
+/* Bytes of workspace a slmoe_backward call with this config needs (0 on an invalid config
+ * or the fp32 layer type). */
+SLMOE_API size_t slmoe_backward_workspace_size(const slmoe_config *cfg);
+
+/*
+ * slmoe_backward - gradients of one Stable LatentMoE layer call, for training it
+ *   ([K3-arch] SiTU激活优化 / 归一化策略调整 / 负载均衡优化; [SLMoE] 训练基础设施: the pages
+ *   train this layer, with histograms added across gradient-accumulation steps).
+ *   Given dy = dL/dy for the layer output y of a slmoe_forward call, this computes the chain
+ *   rule of that forward step by step:
+ *     dW_out (+)= dy^T z;  dz = dy W_out;  RMSNorm:  dc = gamma dz / r - c (sum gamma dz c) / (n r^3),
+ *       dgamma (+)= sum_t dz c / r  (c recomputed from y_e and the gate weights, r = sqrt(mean c^2 + eps));
+ *     combine: dy_e(t,j) = g[t,j] dc_t,  dg[t,j] = dc_t . y_e(t,j);
+ *     routed expert e:  dW2[e] (+)= dy_e^T h;  dh = dy_e W2[e];
+ *       [dg | du] = [dh softcap(u) SiTU'(g) | dh SiTU(g) softcap'(u)]  ([g | u] recomputed);
+ *       dW13[e] (+)= [dg | du]^T x_lat;  dx_lat += [dg | du] W13[e]  (summed over the k slots);
+ *     dW_in (+)= dx_lat^T x;  dx = dx_lat W_in + (router) + (shared experts);
+ *     router: ds_j = (dg_j - sum_i g_i dg_i) / sum_i s_i over the chosen experts,
+ *       dlogit = ds s (1 - s) on the chosen experts (0 elsewhere), dW_r (+)= dlogit^T x,
+ *       dx += dlogit W_r;  the selection itself and the bias pass no gradient;
+ *     shared expert s: dW2_s (+)= dy^T h_s, [dg | du] as above from x W13_s^T (recomputed),
+ *       dW13_s (+)= [dg | du]^T x, dx += [dg | du] W13_s.
+ * Arguments: cfg, x, w as the forward call (bf16 layer type only); dy [T,d] fp32; dx [T,d]
+ *   fp32 (written); grads: every pointer required, fp32, written (accumulate = 0) or added
+ *   into (accumulate = 1, for gradient accumulation across micro-batches); fwd_workspace: the
+ *   workspace of the slmoe_forward call on the same x, weights, bias and logit offset, not
+ *   modified since (its routing, x_lat, h, y_e, z and h_s are read, nothing is written);
+ *   status as above; workspace of slmoe_backward_workspace_size(cfg) bytes.
+ *   Contractions run on the tensor cores (bf16 operands, fp32 accumulation); dz, dx and the
+ *   weight gradients are fp32; the intermediates dy_e, [dg | du] and dx_lat are bf16.
+ * Errors: SLMOE_EINVAL on a null or misaligned pointer or a bad config, SLMOE_EUNSUPPORTED for
+ *   the fp32 layer type, SLMOE_ENOSPACE on a short workspace, SLMOE_ECUDA on a launch failure.
+ */
+SLMOE_API int slmoe_backward(const slmoe_config *cfg, const void *x, const slmoe_weights *w,
+                   const float *dy, float *dx, const slmoe_grads *grads, int accumulate,
+                   const void *fwd_workspace, size_t fwd_workspace_bytes, int32_t *status,
+                   void *workspace, size_t workspace_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

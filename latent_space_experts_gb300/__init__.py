@@ -16,7 +16,8 @@ __all__ = ["SlmoeError", "Config", "Weights", "WorkspaceLayout", "load", "build"
            "weights", "slmoe_workspace_size", "slmoe_workspace_layout_get", "slmoe_route",
            "slmoe_route_noalloc", "slmoe_topk", "slmoe_topk_workspace_size", "slmoe_wait_abort_check",
            "slmoe_qb_histogram", "slmoe_qb_update", "slmoe_signsgd_update",
-           "slmoe_forward", "slmoe_device_sm_count", "workspace_views", "slmoe_last_error",
+           "slmoe_forward", "slmoe_backward", "slmoe_backward_workspace_size", "Grads", "grads",
+           "slmoe_device_sm_count", "workspace_views", "slmoe_last_error",
            "slmoe_set_stage_events", "slmoe_launch_count", "F32", "BF16", "LIB_PATH"]
 
 F32, BF16 = 0, 1
@@ -40,6 +41,11 @@ class Config(ctypes.Structure):
 class Weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("W_r", "W_in", "W13", "W2", "gamma", "W_out", "W13_s", "W2_s")]
+
+
+class Grads(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("dW_r", "dW_in", "dW13", "dW2", "dgamma", "dW_out", "dW13_s", "dW2_s")]
 
 
 class WorkspaceLayout(ctypes.Structure):
@@ -79,6 +85,9 @@ def load():
         "slmoe_qb_update": (ctypes.c_int, [P, I32, I32, I32, P, P, P]),
         "slmoe_signsgd_update": (ctypes.c_int, [P, I32, ctypes.c_float, P, P]),
         "slmoe_forward": (ctypes.c_int, [CP, P, WP, P, P, P, P, P, P, P, SZ, P]),
+        "slmoe_backward_workspace_size": (SZ, [CP]),
+        "slmoe_backward": (ctypes.c_int, [CP, P, WP, P, P, ctypes.POINTER(Grads), ctypes.c_int, P, SZ, P, P,
+                                          SZ, P]),
         "slmoe_set_stage_events": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]),
         "slmoe_launch_count": (ctypes.c_longlong, []),
     }
@@ -121,6 +130,11 @@ def config(shape, T=None) -> Config:
 def weights(inp: dict) -> Weights:
     return Weights(*[_ptr(inp[n]) for n in ("W_r", "W_in", "W13", "W2", "gamma", "W_out",
                                              "W13_s", "W2_s")])
+
+
+def grads(g: dict) -> Grads:
+    """A Grads struct from a dict of fp32 CUDA tensors named as its fields."""
+    return Grads(*[_ptr(g[n]) for n in ("dW_r", "dW_in", "dW13", "dW2", "dgamma", "dW_out", "dW13_s", "dW2_s")])
 
 
 def slmoe_last_error() -> str:
@@ -248,3 +262,19 @@ def slmoe_forward(cfg, x, w: Weights, bias, logit_offset, y, topk_idx_out, hist,
                                 _ptr(logit_offset), _ptr(y), _ptr(topk_idx_out), _ptr(hist),
                                 _ptr(status), _ptr(workspace),
                                 workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def slmoe_backward_workspace_size(cfg: Config) -> int:
+    n = load().slmoe_backward_workspace_size(ctypes.byref(cfg))
+    if n == 0:
+        raise SlmoeError(-1, load().slmoe_last_error().decode())
+    return n
+
+
+def slmoe_backward(cfg, x, w: Weights, dy, dx, g: Grads, accumulate, fwd_workspace, status, workspace,
+                   stream=None):
+    _check(load().slmoe_backward(ctypes.byref(cfg), _ptr(x), ctypes.byref(w), _ptr(dy), _ptr(dx),
+                                 ctypes.byref(g), int(accumulate), _ptr(fwd_workspace),
+                                 fwd_workspace.numel() * fwd_workspace.element_size(), _ptr(status),
+                                 _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                 _stream(stream)))

@@ -424,6 +424,61 @@ int slmoe_wait_abort_check(int32_t *status, uint64_t wait_limit_ns, void *stream
     return tc_wait_abort_check(status, wait_limit_ns, static_cast<cudaStream_t>(stream));
 }
 
+size_t slmoe_backward_workspace_size(const slmoe_config *cfg) {
+    Layout L;
+    if (make_layout(cfg, &L)) return 0;
+    if (cfg->dtype != SLMOE_BF16) {
+        fail(SLMOE_EUNSUPPORTED, "the backward is built for the bf16 layer type");
+        return 0;
+    }
+    return backward_workspace_bytes(cfg, nullptr);
+}
+
+int slmoe_backward(const slmoe_config *cfg, const void *x, const slmoe_weights *w, const float *dy, float *dx,
+                   const slmoe_grads *grads, int accumulate, const void *fwd_workspace, size_t fwd_workspace_bytes,
+                   int32_t *status, void *workspace, size_t workspace_bytes, void *stream) {
+    g_err[0] = 0;
+    Layout L;
+    int rc = make_layout(cfg, &L);
+    if (rc) return rc;
+    if (cfg->dtype != SLMOE_BF16) return fail(SLMOE_EUNSUPPORTED, "the backward is built for the bf16 layer type");
+    if (cfg->T == 0) return SLMOE_OK;
+    if (cfg->E > 4096) return fail(SLMOE_EUNSUPPORTED, "E > 4096");
+    if (!w || !grads) return fail(SLMOE_EINVAL, "weights and grads are required");
+    REQ(x, "x"); REQ(dy, "dy"); REQ(dx, "dx");
+    REQ(w->W_r, "W_r"); REQ(w->W_in, "W_in"); REQ(w->W13, "W13"); REQ(w->W2, "W2");
+    REQ(w->gamma, "gamma"); REQ(w->W_out, "W_out");
+    REQ(grads->dW_r, "dW_r"); REQ(grads->dW_in, "dW_in"); REQ(grads->dW13, "dW13"); REQ(grads->dW2, "dW2");
+    REQ(grads->dgamma, "dgamma"); REQ(grads->dW_out, "dW_out");
+    if (cfg->n_shared > 0) {
+        REQ(w->W13_s, "W13_s"); REQ(w->W2_s, "W2_s"); REQ(grads->dW13_s, "dW13_s"); REQ(grads->dW2_s, "dW2_s");
+    }
+    OPT(status, "status");
+    REQ(fwd_workspace, "fwd_workspace");
+    if (fwd_workspace_bytes < L.pub.total)
+        return fail(SLMOE_ENOSPACE, "forward workspace %zu bytes < %zu", fwd_workspace_bytes, L.pub.total);
+    REQ(workspace, "workspace");
+    const size_t need = backward_workspace_bytes(cfg, nullptr);
+    if (workspace_bytes < need) return fail(SLMOE_ENOSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
+    if (accumulate != 0 && accumulate != 1) return fail(SLMOE_EINVAL, "accumulate must be 0 or 1");
+    const char *fw = static_cast<const char *>(fwd_workspace);
+    FwdSaved fs;
+    fs.scores = reinterpret_cast<const float *>(fw + L.pub.scores);
+    fs.topk_w = reinterpret_cast<const float *>(fw + L.pub.topk_w);
+    fs.topk_idx = reinterpret_cast<const int32_t *>(fw + L.pub.topk_idx);
+    fs.counts = reinterpret_cast<const int32_t *>(fw + L.pub.counts);
+    fs.offsets = reinterpret_cast<const int32_t *>(fw + L.pub.offsets);
+    fs.perm = reinterpret_cast<const int32_t *>(fw + L.pub.perm);
+    fs.slot_pos = reinterpret_cast<const int32_t *>(fw + L.pub.slot_pos);
+    fs.x_lat = reinterpret_cast<const __nv_bfloat16 *>(fw + L.pub.x_lat);
+    fs.h = reinterpret_cast<const __nv_bfloat16 *>(fw + L.pub.h);
+    fs.y_e = reinterpret_cast<const __nv_bfloat16 *>(fw + L.pub.y_e);
+    fs.z = reinterpret_cast<const __nv_bfloat16 *>(fw + L.pub.z);
+    fs.h_s = reinterpret_cast<const __nv_bfloat16 *>(fw + L.pub.h_s);
+    return tc_backward(cfg, x, w, dy, dx, grads, accumulate, fs, static_cast<char *>(workspace), status,
+                       static_cast<cudaStream_t>(stream));
+}
+
 int slmoe_forward(const slmoe_config *cfg, const void *x, const slmoe_weights *w,
                   const float *bias, const float *logit_offset, void *y, int32_t *topk_idx_out,
                   uint32_t *hist, int32_t *status, void *workspace, size_t workspace_bytes,

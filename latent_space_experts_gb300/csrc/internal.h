@@ -1,6 +1,7 @@
 // Internal launcher interface shared by the library's translation units (host side).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -88,5 +89,21 @@ int launch_signsgd_update(const int32_t *counts, int E, float step, float *bias,
 int launch_combine_rmsnorm(int dtype, const void *y_e, const float *topk_w,
                            const int32_t *slot_pos, const float *gamma, int T, int d_latent,
                            int k, float eps, void *z, cudaStream_t st);
+
+// ---------------------------------------------------------------- backward (bf16 type)
+// Intermediates of a forward call that the backward reads (views into its workspace).
+struct FwdSaved {
+    const float *scores, *topk_w;
+    const int32_t *topk_idx, *counts, *offsets, *perm, *slot_pos;
+    const __nv_bfloat16 *x_lat, *h, *y_e, *z, *h_s;
+};
+struct BwdLayout {
+    size_t dy_b, dz, dye, dg, gu, dgu, dxe, dx_lat, gu_s, dgu_s, dl_perm, dgamma_part, counters;
+    size_t items1, items2, items3, cap1, cap2, cap3, nblk, total;
+};
+size_t backward_workspace_bytes(const slmoe_config *c, BwdLayout *L);
+int tc_backward(const slmoe_config *c, const void *x, const slmoe_weights *w, const float *dy, float *dx,
+                const slmoe_grads *g, int accumulate, const FwdSaved &fs, char *ws, int32_t *status,
+                cudaStream_t st);
 
 }  // namespace slmoe

@@ -1,0 +1,120 @@
+"""GPU parity of slmoe_backward against the oracle's fp64 backward.
+
+The forward runs first (slmoe_forward); the oracle takes the GPU's selection (forced routing)
+and computes every gradient in fp64 from the exact inputs, without emulating the bf16
+roundings of the GPU's intermediates.  Each gradient must be within 2e-2 RMS(ref) of the
+oracle's, elementwise (the bf16 bound of the forward).  Gradient accumulation across
+micro-batches (accumulate = 1) must add the micro-batches' gradients, while the forward's QB
+histograms add in the same way.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+import latent_space_experts_gb300 as lse
+from gpu_util import BF16_TOL, assert_close_rms, need_gpu, to_dev
+
+pytestmark = pytest.mark.gpu
+
+GRADS = ("dW_r", "dW_in", "dW13", "dW2", "dgamma", "dW_out", "dW13_s", "dW2_s")
+WEIGHT_OF = dict(dW_r="W_r", dW_in="W_in", dW13="W13", dW2="W2", dgamma="gamma", dW_out="W_out",
+                 dW13_s="W13_s", dW2_s="W2_s")
+
+
+def zero_grads(inp):
+    return {g: torch.zeros(inp[w].shape, dtype=torch.float32, device="cuda") for g, w in WEIGHT_OF.items()}
+
+
+def forward_backward(shape, inp, dy, grads, accumulate, hist=None):
+    cfg = lse.config(shape)
+    ws = torch.zeros(lse.slmoe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    y = torch.empty(shape.T, shape.d, dtype=torch.float32, device="cuda")
+    topk = torch.empty(shape.T, shape.k, dtype=torch.int32, device="cuda")
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    W = lse.weights(inp)
+    lse.slmoe_forward(cfg, inp["x"], W, inp["bias"], inp.get("logit_offset"), y, topk, hist, status, ws)
+    bws = torch.zeros(lse.slmoe_backward_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    dx = torch.full((shape.T, shape.d), float("nan"), dtype=torch.float32, device="cuda")
+    lse.slmoe_backward(cfg, inp["x"], W, dy, dx, lse.grads(grads), accumulate, ws, status, bws)
+    torch.cuda.synchronize()
+    assert status.cpu().tolist()[1:3] == [0, 0], status
+    return y, topk.cpu().numpy(), dx
+
+
+def layer(over, seed):
+    shp = synthetic.shape_with("mid", **over)
+    inp_cpu = synthetic.layer_inputs(shp, seed=seed)
+    g = torch.Generator().manual_seed(100 + seed)
+    dy = torch.randn(shp.T, shp.d, generator=g)
+    return shp, inp_cpu, dy
+
+
+def check_grads(shp, inp_cpu, dy_cpu, dx, grads, topk, scale=1.0, what="", skip=()):
+    ref = oracle.backward(inp_cpu, shp.k, dy_cpu.double().numpy(), forced_topk_idx=topk)
+    ratios = {"dx": assert_close_rms(dx, ref["dx"], BF16_TOL, f"{what} dx")}
+    for name in GRADS:
+        if name in skip or (name in ("dW13_s", "dW2_s") and shp.n_shared == 0):
+            continue
+        ratios[name] = assert_close_rms(grads[name], scale * ref[name], BF16_TOL, f"{what} {name}")
+    print(what, {k: f"{v:.2e}" for k, v in ratios.items()})
+    return ref
+
+
+@pytest.mark.parametrize("over,seed", [
+    (dict(T=300, d=512), 0),                                     # several tiles, ragged T
+    (dict(T=130, d=256, d_latent=384, E=8, k=8, I=128), 1),      # k = E, ragged latent tiles
+    (dict(T=77, d=512, E=40, k=3, I=192, n_shared=0), 2),        # experts without tokens, no shared
+    (dict(T=600, d=512, E=2, k=1, I=384, n_shared=3, I_shared=320), 3),   # > 256 rows per expert
+])
+def test_backward_matches_the_oracle(over, seed):
+    need_gpu()
+    shp, inp_cpu, dy = layer(over, seed)
+    inp = to_dev(inp_cpu)
+    grads = zero_grads(inp)
+    for g in grads.values():
+        g.fill_(float("nan"))              # accumulate = 0 must overwrite every element
+    _, topk, dx = forward_backward(shp, inp, dy.cuda(), grads, 0)
+    check_grads(shp, inp_cpu, dy, dx, grads, topk, what=str(over))
+
+
+def test_backward_accumulates_across_micro_batches_with_the_qb_histogram():
+    """Two micro-batches: weight gradients added in place (accumulate = 1 after a first call
+    with 0), and the forward's QB histograms of the two batches added in place, as gradient
+    accumulation does ([K3-arch] 负载均衡优化: the distribution adds across accumulation steps)."""
+    need_gpu()
+    shp = synthetic.shape_with("mid", T=200, d=512)
+    inps = [synthetic.layer_inputs(shp, seed=s) for s in (5, 5)]
+    # the same weights, different tokens and output gradients for the second micro-batch
+    g = torch.Generator().manual_seed(9)
+    inps[1]["x"] = torch.randn(shp.T, shp.d, generator=g).to(torch.bfloat16)
+    dys = [torch.randn(shp.T, shp.d, generator=g) for _ in range(2)]
+    grads = zero_grads(to_dev(inps[0]))
+    hist = torch.zeros(shp.E, shp.nbins, dtype=torch.int32, device="cuda")
+    refs = []
+    for m in range(2):
+        inp = to_dev(inps[m])
+        _, topk, dx = forward_backward(shp, inp, dys[m].cuda(), grads, 1 if m else 0, hist=hist)
+        ref = oracle.backward(inps[m], shp.k, dys[m].double().numpy(), forced_topk_idx=topk)
+        assert_close_rms(dx, ref["dx"], BF16_TOL, f"dx micro-batch {m}")
+        refs.append(ref)
+    for name in GRADS:
+        assert_close_rms(grads[name], refs[0][name] + refs[1][name], BF16_TOL, f"accumulated {name}")
+    h = hist.cpu().numpy().view(np.uint32).astype(np.int64)
+    assert np.all(h.sum(axis=1) == 2 * shp.T)
+
+
+def test_backward_of_identical_experts_gives_no_router_gradient():
+    """All routed experts equal: the gate weights sum to 1, so the router gradient vanishes
+    (up to bf16 rounding) while the expert gradients do not."""
+    need_gpu()
+    shp, inp_cpu, dy = layer(dict(T=256, d=512), 6)
+    inp_cpu["W13"][:] = inp_cpu["W13"][0]
+    inp_cpu["W2"][:] = inp_cpu["W2"][0]
+    inp = to_dev(inp_cpu)
+    grads = zero_grads(inp)
+    _, topk, dx = forward_backward(shp, inp, dy.cuda(), grads, 0)
+    ref = check_grads(shp, inp_cpu, dy, dx, grads, topk, what="identical experts", skip=("dW_r",))
+    assert np.max(np.abs(ref["dW_r"])) < 1e-12
+    assert float(grads["dW_r"].abs().max()) <= 1e-3 * float(grads["dW_in"].abs().max())
