@@ -17,7 +17,9 @@
 //    weights as M: "swap AB"), and per-expert weight-gradient tiles whose K is the expert's
 //    own segment of rows in expert-sorted order;
 //  * epilogues: fp32 store or accumulate (optionally transposed), bf16 store, and the
-//    SiTU-GLU derivative, which turns dh into [dg | du] using the recomputed pre-activations.
+//    SiTU-GLU derivative, which turns dh into [dg | du] using the recomputed pre-activations
+//    (kept in fp32: near saturation the derivatives of SiTU and of the soft cap change by a
+//    few per cent across one bf16 step of their argument).
 //
 // The memory-bound steps are plain kernels: RMSNorm + combine backward (dc, the gradient of
 // each expert output, of each gate weight, and per-block dgamma sums), the per-token sum of
@@ -76,7 +78,7 @@ struct BArgs {
     long long ldc, cstride;
     int out_t;               // 1: C[n][m] instead of C[m][n]
     int accumulate;          // fp32 epilogue: add into C instead of storing
-    const bf16 *gu;          // SiTU-GLU derivative: pre-activations [rows, 2F] (gate | up)
+    const float *gu;         // SiTU-GLU derivative: fp32 pre-activations [rows, 2F] (gate | up)
     long long ld_gu;
     int F;
     bf16 *dgu;               // ... and its output [rows, 2F]
@@ -392,8 +394,8 @@ __global__ void __launch_bounds__(BG_THREADS, 1) bgemm_kernel(const BArgs a) {
                         const long long row = a.out_t ? (long long)(it.n0 + c + j) : (long long)m;
                         const int f = a.out_t ? m : it.n0 + c + j;
                         const float dh = __uint_as_float(r[j]);
-                        const float g = __bfloat162float(a.gu[row * a.ld_gu + f]);
-                        const float u = __bfloat162float(a.gu[row * a.ld_gu + a.F + f]);
+                        const float g = a.gu[row * a.ld_gu + f];
+                        const float u = a.gu[row * a.ld_gu + a.F + f];
                         const float tu = tanhf(u / a.beta2);
                         const float cap = a.beta2 * tu;
                         a.dgu[row * a.ld_dgu + f] = __float2bfloat16_rn(dh * cap * situ_grad_f(g, a.beta1));
@@ -558,8 +560,9 @@ __global__ void dgamma_reduce_kernel(const float *__restrict__ part, int nblk, i
     dgamma[i] = s + (accumulate ? dgamma[i] : 0.f);
 }
 
-// dx_lat[t] = sum_j dxe[slot_pos[t, j]] (fp32, slot order), stored bf16; 8 values per thread.
-__global__ void slot_reduce_kernel(const bf16 *__restrict__ dxe, const int32_t *__restrict__ slot_pos, int T,
+// dx_lat[t] = sum_j dxe[slot_pos[t, j]] (fp32 rows, added in slot order), stored bf16; 8 values
+// per thread.
+__global__ void slot_reduce_kernel(const float *__restrict__ dxe, const int32_t *__restrict__ slot_pos, int T,
                                    int dl, int k, bf16 *__restrict__ out) {
     const int per_row = dl / 8;
     const long long total = (long long)T * per_row;
@@ -568,10 +571,11 @@ __global__ void slot_reduce_kernel(const bf16 *__restrict__ dxe, const int32_t *
         const int t = (int)(idx / per_row), c = (int)(idx - (long long)t * per_row);
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         for (int j = 0; j < k; ++j) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(dxe + (long long)slot_pos[(long long)t * k + j] * dl + 8 * c);
-            const bf16 *b = reinterpret_cast<const bf16 *>(&v);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) acc[q] += __bfloat162float(b[q]);
+            const float *src = dxe + (long long)slot_pos[(long long)t * k + j] * dl + 8 * c;
+            const float4 v0 = *reinterpret_cast<const float4 *>(src);
+            const float4 v1 = *reinterpret_cast<const float4 *>(src + 4);
+            acc[0] += v0.x; acc[1] += v0.y; acc[2] += v0.z; acc[3] += v0.w;
+            acc[4] += v1.x; acc[5] += v1.y; acc[6] += v1.z; acc[7] += v1.w;
         }
         *reinterpret_cast<uint4 *>(out + (long long)t * dl + 8 * c) =
             make_uint4(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]), pack_bf16(acc[4], acc[5]),
@@ -700,11 +704,11 @@ size_t backward_workspace_bytes(const slmoe_config *c, BwdLayout *L) {
     l.dz = take(T * dl * 4);
     l.dye = take(Tk * dl * 2);
     l.dg = take(Tk * 4);
-    l.gu = take(Tk * 2 * I * 2);
+    l.gu = take(Tk * 2 * I * 4);
     l.dgu = take(Tk * 2 * I * 2);
-    l.dxe = take(Tk * dl * 2);
+    l.dxe = take(Tk * dl * 4);
     l.dx_lat = take(T * dl * 2);
-    l.gu_s = take(T * 2 * Is * 2);
+    l.gu_s = take(T * 2 * Is * 4);
     l.dgu_s = take(T * 2 * Is * 2);
     l.dl_perm = take(Tk * 4);
     l.nblk = (T + RB_TOK - 1) / RB_TOK;
@@ -736,11 +740,11 @@ int tc_backward(const slmoe_config *c, const void *x, const slmoe_weights *w, co
     float *dz = reinterpret_cast<float *>(ws + L.dz);
     bf16 *dye = reinterpret_cast<bf16 *>(ws + L.dye);
     float *dg = reinterpret_cast<float *>(ws + L.dg);
-    bf16 *gu = reinterpret_cast<bf16 *>(ws + L.gu);
+    float *gu = reinterpret_cast<float *>(ws + L.gu);
     bf16 *dgu = reinterpret_cast<bf16 *>(ws + L.dgu);
-    bf16 *dxe = reinterpret_cast<bf16 *>(ws + L.dxe);
+    float *dxe = reinterpret_cast<float *>(ws + L.dxe);
     bf16 *dx_lat = reinterpret_cast<bf16 *>(ws + L.dx_lat);
-    bf16 *gu_s = reinterpret_cast<bf16 *>(ws + L.gu_s);
+    float *gu_s = reinterpret_cast<float *>(ws + L.gu_s);
     bf16 *dgu_s = reinterpret_cast<bf16 *>(ws + L.dgu_s);
     float *dl_perm = reinterpret_cast<float *>(ws + L.dl_perm);
     float *dgamma_part = reinterpret_cast<float *>(ws + L.dgamma_part);
@@ -774,7 +778,7 @@ int tc_backward(const slmoe_config *c, const void *x, const slmoe_weights *w, co
         const bf16 *W2s = static_cast<const bf16 *>(w->W2_s) + (size_t)s * d * Is;
         int *cs = cnt + 2 + 5 * s;
         // pre-activations gu_s = x W13_s^T (recomputed)
-        if ((rc = launch_bg<BE_BF16, false, false, BG_DENSE>(
+        if ((rc = launch_bg<BE_F32, false, false, BG_DENSE>(
                  dense_args(T, 2 * Is, d, op(x, d), op(W13s, d), gu_s, 2 * Is, 0, cs + 0, status), st)))
             return rc;
         // dh_s = dy W2_s, turned into [dg | du] by the SiTU-GLU derivative
@@ -828,7 +832,7 @@ int tc_backward(const slmoe_config *c, const void *x, const slmoe_weights *w, co
         BArgs a = pass_args(2 * I, dl, op(w->W13, dl, (long long)2 * I * dl), op(fs.x_lat, dl, 0, fs.perm), items1,
                             cnt + 20, L.cap1, cnt + 17);
         a.C = gu; a.ldc = 2 * I;
-        if ((rc = launch_bg<BE_BF16, false, false, BG_PASS>(a, st))) return rc;
+        if ((rc = launch_bg<BE_F32, false, false, BG_PASS>(a, st))) return rc;
     }
     // dh = W2[e]^T dy_e  (swap AB: W2[e] stored [d_l, I] is MN-major), then [dg | du]
     {
@@ -842,7 +846,7 @@ int tc_backward(const slmoe_config *c, const void *x, const slmoe_weights *w, co
         BArgs a = pass_args(dl, 2 * I, op(w->W13, dl, (long long)2 * I * dl), op(dgu, 2 * I), items3, cnt + 22,
                             L.cap3, cnt + 19);
         a.C = dxe; a.ldc = dl;
-        if ((rc = launch_bg<BE_BF16, true, false, BG_PASS>(a, st))) return rc;
+        if ((rc = launch_bg<BE_F32, true, false, BG_PASS>(a, st))) return rc;
     }
     // routed weight gradients, K = the expert's rows: dW2[e] (+)= dy_e^T h, dW13[e] (+)= dgu^T x_lat
     {

@@ -51,14 +51,20 @@ def layer(over, seed):
     return shp, inp_cpu, dy
 
 
+def err_stats(got, ref):
+    got = got.detach().double().cpu().numpy() if hasattr(got, "detach") else np.asarray(got, np.float64)
+    err = np.abs(got - ref)
+    r = float(np.sqrt(np.mean(ref * ref)))
+    return float(err.max()) / r, float(np.max(err / (np.abs(ref) + r)))
+
+
 def check_grads(shp, inp_cpu, dy_cpu, dx, grads, topk, scale=1.0, what="", skip=()):
     ref = oracle.backward(inp_cpu, shp.k, dy_cpu.double().numpy(), forced_topk_idx=topk)
-    ratios = {"dx": assert_close_rms(dx, ref["dx"], BF16_TOL, f"{what} dx")}
-    for name in GRADS:
-        if name in skip or (name in ("dW13_s", "dW2_s") and shp.n_shared == 0):
-            continue
-        ratios[name] = assert_close_rms(grads[name], scale * ref[name], BF16_TOL, f"{what} {name}")
-    print(what, {k: f"{v:.2e}" for k, v in ratios.items()})
+    pairs = [("dx", dx, ref["dx"])] + [(n, grads[n], scale * ref[n]) for n in GRADS
+                                       if n not in skip and not (n in ("dW13_s", "dW2_s") and shp.n_shared == 0)]
+    print(what, {n: "max/RMS %.2e, max/(|ref|+RMS) %.2e" % err_stats(g, r) for n, g, r in pairs})
+    for n, g, r in pairs:
+        assert_close_rms(g, r, BF16_TOL, f"{what} {n}")
     return ref
 
 
