@@ -336,6 +336,16 @@ typedef struct slmoe_grads {
  * or the fp32 layer type). */
 SLMOE_API size_t slmoe_backward_workspace_size(const slmoe_config *cfg);
 
+/* Byte offsets of the backward's intermediates inside its workspace (readable after the call):
+ * dz fp32 [T,d_latent]; dy_e bf16 [T*k, d_latent] and dgu bf16 [T*k, 2I] (rows in the forward's
+ * expert order); dg fp32 [T,k] (gate-weight gradients); gu fp32 [T*k, 2I] (recomputed
+ * pre-activations of the routed experts); dx_lat bf16 [T,d_latent]; gu_s fp32 and dgu_s bf16
+ * [T, 2I_shared] of the last shared expert.  Returns SLMOE_OK or an error code. */
+typedef struct slmoe_backward_layout {
+    size_t dz, dye, dg, gu, dgu, dx_lat, gu_s, dgu_s, total;
+} slmoe_backward_layout;
+SLMOE_API int slmoe_backward_layout_get(const slmoe_config *cfg, slmoe_backward_layout *out);
+
 /*
  * slmoe_backward - gradients of one Stable LatentMoE layer call, for training it
  *   ([K3-arch] SiTU激活优化 / 归一化策略调整 / 负载均衡优化; [SLMoE] 训练基础设施: the pages

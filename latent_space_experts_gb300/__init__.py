@@ -16,7 +16,8 @@ __all__ = ["SlmoeError", "Config", "Weights", "WorkspaceLayout", "load", "build"
            "weights", "slmoe_workspace_size", "slmoe_workspace_layout_get", "slmoe_route",
            "slmoe_route_noalloc", "slmoe_topk", "slmoe_topk_workspace_size", "slmoe_wait_abort_check",
            "slmoe_qb_histogram", "slmoe_qb_update", "slmoe_signsgd_update",
-           "slmoe_forward", "slmoe_backward", "slmoe_backward_workspace_size", "Grads", "grads",
+           "slmoe_forward", "slmoe_backward", "slmoe_backward_workspace_size", "slmoe_backward_layout_get",
+           "backward_views", "Grads", "grads",
            "slmoe_device_sm_count", "workspace_views", "slmoe_last_error",
            "slmoe_set_stage_events", "slmoe_launch_count", "F32", "BF16", "LIB_PATH"]
 
@@ -46,6 +47,10 @@ class Weights(ctypes.Structure):
 class Grads(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("dW_r", "dW_in", "dW13", "dW2", "dgamma", "dW_out", "dW13_s", "dW2_s")]
+
+
+class BackwardLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in ("dz", "dye", "dg", "gu", "dgu", "dx_lat", "gu_s", "dgu_s", "total")]
 
 
 class WorkspaceLayout(ctypes.Structure):
@@ -86,6 +91,7 @@ def load():
         "slmoe_signsgd_update": (ctypes.c_int, [P, I32, ctypes.c_float, P, P]),
         "slmoe_forward": (ctypes.c_int, [CP, P, WP, P, P, P, P, P, P, P, SZ, P]),
         "slmoe_backward_workspace_size": (SZ, [CP]),
+        "slmoe_backward_layout_get": (ctypes.c_int, [CP, ctypes.POINTER(BackwardLayout)]),
         "slmoe_backward": (ctypes.c_int, [CP, P, WP, P, P, ctypes.POINTER(Grads), ctypes.c_int, P, SZ, P, P,
                                           SZ, P]),
         "slmoe_set_stage_events": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]),
@@ -278,3 +284,29 @@ def slmoe_backward(cfg, x, w: Weights, dy, dx, g: Grads, accumulate, fwd_workspa
                                  fwd_workspace.numel() * fwd_workspace.element_size(), _ptr(status),
                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
                                  _stream(stream)))
+
+
+def slmoe_backward_layout_get(cfg: Config) -> dict:
+    out = BackwardLayout()
+    _check(load().slmoe_backward_layout_get(ctypes.byref(cfg), ctypes.byref(out)))
+    return {n: getattr(out, n) for n, _ in BackwardLayout._fields_}
+
+
+def backward_views(cfg: Config, ws):
+    """torch views of the backward's intermediates inside its workspace (uint8, on the device)."""
+    import torch
+    L = slmoe_backward_layout_get(cfg)
+    T, k, dl, I, Is = cfg.T, cfg.k, cfg.d_latent, cfg.I, cfg.I_shared
+
+    def view(name, dtype, shape):
+        n = 1
+        for s in shape:
+            n *= s
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        return ws[L[name]:L[name] + nbytes].view(dtype).view(*shape)
+
+    bf = torch.bfloat16
+    return dict(dz=view("dz", torch.float32, (T, dl)), dye=view("dye", bf, (T * k, dl)),
+                dg=view("dg", torch.float32, (T, k)), gu=view("gu", torch.float32, (T * k, 2 * I)),
+                dgu=view("dgu", bf, (T * k, 2 * I)), dx_lat=view("dx_lat", bf, (T, dl)),
+                gu_s=view("gu_s", torch.float32, (T, 2 * Is)), dgu_s=view("dgu_s", bf, (T, 2 * Is)))

@@ -434,6 +434,16 @@ size_t slmoe_backward_workspace_size(const slmoe_config *cfg) {
     return backward_workspace_bytes(cfg, nullptr);
 }
 
+int slmoe_backward_layout_get(const slmoe_config *cfg, slmoe_backward_layout *out) {
+    if (!out) return fail(SLMOE_EINVAL, "out is NULL");
+    if (slmoe_backward_workspace_size(cfg) == 0) return cfg && cfg->dtype != SLMOE_BF16 ? SLMOE_EUNSUPPORTED : SLMOE_EINVAL;
+    BwdLayout L;
+    backward_workspace_bytes(cfg, &L);
+    out->dz = L.dz; out->dye = L.dye; out->dg = L.dg; out->gu = L.gu; out->dgu = L.dgu;
+    out->dx_lat = L.dx_lat; out->gu_s = L.gu_s; out->dgu_s = L.dgu_s; out->total = L.total;
+    return SLMOE_OK;
+}
+
 int slmoe_backward(const slmoe_config *cfg, const void *x, const slmoe_weights *w, const float *dy, float *dx,
                    const slmoe_grads *grads, int accumulate, const void *fwd_workspace, size_t fwd_workspace_bytes,
                    int32_t *status, void *workspace, size_t workspace_bytes, void *stream) {

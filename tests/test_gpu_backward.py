@@ -14,7 +14,7 @@ import torch
 import oracle
 import synthetic
 import latent_space_experts_gb300 as lse
-from gpu_util import BF16_TOL, assert_close_rms, need_gpu, to_dev
+from gpu_util import BF16_STORE, BF16_TOL, assert_close_rms, need_gpu, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -124,3 +124,91 @@ def test_backward_of_identical_experts_gives_no_router_gradient():
     ref = check_grads(shp, inp_cpu, dy, dx, grads, topk, what="identical experts", skip=("dW_r",))
     assert np.max(np.abs(ref["dW_r"])) < 1e-12
     assert float(grads["dW_r"].abs().max()) <= 1e-3 * float(grads["dW_in"].abs().max())
+
+
+SAME = 2e-3     # stage checks from the GPU's own operands: exact bf16 products, fp32 sums
+
+
+def f64(t):
+    return t.detach().double().cpu().numpy()
+
+
+def bf16_round(a):
+    return torch.as_tensor(np.asarray(a, np.float32)).to(torch.bfloat16).double().numpy()
+
+
+def check_backward_stages(shp, inp, fw, bw, grads, dy, experts):
+    """Each backward stage against the oracle's formula applied to the GPU's own inputs of
+    that stage (so a stage is judged on its own arithmetic, not on the roundings before it)."""
+    T, k, I = shp.T, shp.k, shp.I
+    perm, offsets = f64(fw["perm"]).astype(np.int64), f64(fw["offsets"]).astype(np.int64)
+    slot_pos = f64(fw["slot_pos"]).astype(np.int64).reshape(T, k)
+    dy_b = bf16_round(f64(dy))
+    W_out = oracle.f64(inp["W_out"])
+    assert_close_rms(bw["dz"], dy_b @ W_out, SAME, "stage dz")
+    assert_close_rms(grads["dW_out"], dy_b.T @ f64(fw["z"]), SAME, "stage dW_out")
+    # norm + combine backward from the GPU's y_e and gates
+    ye = f64(fw["y_e"])
+    gw = f64(fw["topk_w"])
+    c = np.einsum("tj,tjd->td", gw, ye[slot_pos])
+    dc, dgamma = oracle.rmsnorm_backward(c, inp["gamma"], f64(bw["dz"]), shp.eps)
+    assert_close_rms(grads["dgamma"], dgamma, SAME, "stage dgamma")
+    dye_ref = np.zeros_like(ye)
+    dye_ref[slot_pos.reshape(-1)] = (gw[:, :, None] * dc[:, None, :]).reshape(T * k, -1)
+    assert_close_rms(bw["dye"], dye_ref, SAME, "stage dy_e", BF16_STORE)
+    assert_close_rms(bw["dg"], np.einsum("td,tjd->tj", dc, ye[slot_pos]), SAME, "stage dg")
+    xl = f64(fw["x_lat"])
+    h = f64(fw["h"])
+    dye = f64(bw["dye"])
+    gu = f64(bw["gu"])
+    dgu = f64(bw["dgu"])
+    for e in experts:
+        p = np.arange(offsets[e], offsets[e + 1])
+        if p.size == 0:
+            continue
+        W13, W2 = oracle.f64(inp["W13"][int(e)]), oracle.f64(inp["W2"][int(e)])
+        assert_close_rms(gu[p], xl[perm[p]] @ W13.T, SAME, f"stage gu expert {e}")
+        dgu_ref = oracle.situ_glu_backward(gu[p], dye[p] @ W2)
+        assert_close_rms(dgu[p], dgu_ref, SAME, f"stage dgu expert {e}", BF16_STORE)
+        assert_close_rms(grads["dW2"][int(e)], dye[p].T @ h[p], SAME, f"stage dW2 expert {e}")
+        assert_close_rms(grads["dW13"][int(e)], dgu[p].T @ xl[perm[p]], SAME, f"stage dW13 expert {e}")
+    # x_lat gradient: each row's W13[e]^T dgu summed over the token's slots
+    dxe = np.zeros((T * k, xl.shape[1]))
+    for e in np.unique(np.searchsorted(offsets, np.arange(T * k), side="right") - 1):
+        p = np.arange(offsets[e], offsets[e + 1])
+        dxe[p] = dgu[p] @ oracle.f64(inp["W13"][int(e)])
+    dx_lat_ref = dxe[slot_pos].sum(axis=1)
+    assert_close_rms(bw["dx_lat"], dx_lat_ref, SAME, "stage dx_lat", BF16_STORE)
+    x = oracle.f64(inp["x"])
+    assert_close_rms(grads["dW_in"], f64(bw["dx_lat"]).T @ x, SAME, "stage dW_in")
+    if shp.n_shared:
+        s = shp.n_shared - 1
+        W13s, W2s = oracle.f64(inp["W13_s"][s]), oracle.f64(inp["W2_s"][s])
+        gus = f64(bw["gu_s"])
+        assert_close_rms(gus, x @ W13s.T, SAME, "stage gu_s")
+        assert_close_rms(bw["dgu_s"], oracle.situ_glu_backward(gus, dy_b @ W2s), SAME, "stage dgu_s", BF16_STORE)
+        assert_close_rms(grads["dW13_s"][s], f64(bw["dgu_s"]).T @ x, SAME, "stage dW13_s")
+        hs = f64(fw["h_s"])[:, s * shp.I_shared:(s + 1) * shp.I_shared]
+        assert_close_rms(grads["dW2_s"][s], dy_b.T @ hs, SAME, "stage dW2_s")
+
+
+@pytest.mark.parametrize("over,seed", [(dict(T=300, d=512), 0), (dict(T=77, d=512, E=40, k=3, I=192), 2)])
+def test_backward_stages(over, seed):
+    need_gpu()
+    shp, inp_cpu, dy = layer(over, seed)
+    inp = to_dev(inp_cpu)
+    grads = zero_grads(inp)
+    cfg = lse.config(shp)
+    ws = torch.zeros(lse.slmoe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    y = torch.empty(shp.T, shp.d, dtype=torch.float32, device="cuda")
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    W = lse.weights(inp)
+    lse.slmoe_forward(cfg, inp["x"], W, inp["bias"], inp["logit_offset"], y, None, None, status, ws)
+    bws = torch.zeros(lse.slmoe_backward_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    dx = torch.empty(shp.T, shp.d, dtype=torch.float32, device="cuda")
+    dyd = dy.cuda()
+    lse.slmoe_backward(cfg, inp["x"], W, dyd, dx, lse.grads(grads), 0, ws, status, bws)
+    torch.cuda.synchronize()
+    assert status.cpu().tolist() == [0, 0, 0, 0]
+    check_backward_stages(shp, inp_cpu, lse.workspace_views(cfg, ws), lse.backward_views(cfg, bws), grads, dyd,
+                          range(shp.E))
