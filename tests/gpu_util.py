@@ -9,6 +9,11 @@ NEAR_TIE = 1e-5          # tokens whose oracle k-th/(k+1)-th biased gap is below
 BF16_TOL = 2e-2          # max|err| <= 2e-2 * RMS(ref) on bf16 paths
 F32_TOL = 1e-4           # max|err| <= 1e-4 * RMS(ref) on fp32 paths
 BF16_STORE = 2.0 ** -7   # extra elementwise allowance for intermediates stored in bf16
+# Backward gradients pass through up to four bf16 roundings (dy, dy_e, [dg | du], dx_lat; and
+# the forward's stored x_lat, h, y_e, z): relative RMS error about 2^-9 * sqrt(4) / sqrt(3) =
+# 2.3e-3 per product.  Held to a relative Frobenius error of 1e-2 and a max error of 0.1 RMS.
+BWD_FRO = 1e-2
+BWD_MAX = 0.1
 
 
 def need_gpu():
@@ -136,3 +141,18 @@ def check_selection_and_permutation(scores_ref, scores_gpu, bias, sel, w, counts
     assert np.array_equal(np.asarray(perm)[:T * k], perm_ref)
     assert np.array_equal(np.asarray(slot_pos).reshape(-1)[:T * k].reshape(T, k), sp_ref)
     return n_tie, serr
+
+
+def assert_close_grad(got, ref, what=""):
+    """Backward gradients: ||got - ref||_F <= BWD_FRO ||ref||_F and max|got - ref| <= BWD_MAX RMS(ref).
+    Returns (Frobenius ratio, max / RMS)."""
+    got = got.detach().double().cpu().numpy() if hasattr(got, "detach") else np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    err = got - ref
+    fro = float(np.linalg.norm(err) / max(np.linalg.norm(ref), 1e-300))
+    mx = float(np.max(np.abs(err)) / max(rms(ref), 1e-300))
+    assert fro <= BWD_FRO, f"{what}: relative Frobenius error {fro:.3e} > {BWD_FRO}"
+    assert mx <= BWD_MAX, f"{what}: max error {mx:.3e} RMS > {BWD_MAX}"
+    return fro, mx

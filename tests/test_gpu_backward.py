@@ -2,10 +2,13 @@
 
 The forward runs first (slmoe_forward); the oracle takes the GPU's selection (forced routing)
 and computes every gradient in fp64 from the exact inputs, without emulating the bf16
-roundings of the GPU's intermediates.  Each gradient must be within 2e-2 RMS(ref) of the
-oracle's, elementwise (the bf16 bound of the forward).  Gradient accumulation across
-micro-batches (accumulate = 1) must add the micro-batches' gradients, while the forward's QB
-histograms add in the same way.
+roundings of the GPU's intermediates.  End to end, each gradient must be within a relative
+Frobenius error of 1e-2 and a max error of 0.1 RMS(ref) (gpu_util.BWD_FRO / BWD_MAX: four bf16
+roundings lie between the inputs and a gradient).  Each stage is also checked on its own, from
+the GPU's own inputs of that stage, at 2e-3 RMS (exact bf16 products, fp32 sums), with the
+mid workload's x outliers (1 % of x scaled by 50) that push the gates into saturation.
+Gradient accumulation across micro-batches (accumulate = 1) must add the micro-batches'
+gradients, while the forward's QB histograms add in the same way.
 """
 import numpy as np
 import pytest
@@ -14,7 +17,7 @@ import torch
 import oracle
 import synthetic
 import latent_space_experts_gb300 as lse
-from gpu_util import BF16_STORE, BF16_TOL, assert_close_rms, need_gpu, to_dev
+from gpu_util import BF16_STORE, assert_close_grad, assert_close_rms, need_gpu, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -44,6 +47,8 @@ def forward_backward(shape, inp, dy, grads, accumulate, hist=None):
 
 
 def layer(over, seed):
+    over = dict(over)
+    over.setdefault("x_outliers", False)
     shp = synthetic.shape_with("mid", **over)
     inp_cpu = synthetic.layer_inputs(shp, seed=seed)
     g = torch.Generator().manual_seed(100 + seed)
@@ -64,7 +69,7 @@ def check_grads(shp, inp_cpu, dy_cpu, dx, grads, topk, scale=1.0, what="", skip=
                                        if n not in skip and not (n in ("dW13_s", "dW2_s") and shp.n_shared == 0)]
     print(what, {n: "max/RMS %.2e, max/(|ref|+RMS) %.2e" % err_stats(g, r) for n, g, r in pairs})
     for n, g, r in pairs:
-        assert_close_rms(g, r, BF16_TOL, f"{what} {n}")
+        assert_close_grad(g, r, f"{what} {n}")
     return ref
 
 
@@ -103,10 +108,10 @@ def test_backward_accumulates_across_micro_batches_with_the_qb_histogram():
         inp = to_dev(inps[m])
         _, topk, dx = forward_backward(shp, inp, dys[m].cuda(), grads, 1 if m else 0, hist=hist)
         ref = oracle.backward(inps[m], shp.k, dys[m].double().numpy(), forced_topk_idx=topk)
-        assert_close_rms(dx, ref["dx"], BF16_TOL, f"dx micro-batch {m}")
+        assert_close_grad(dx, ref["dx"], f"dx micro-batch {m}")
         refs.append(ref)
     for name in GRADS:
-        assert_close_rms(grads[name], refs[0][name] + refs[1][name], BF16_TOL, f"accumulated {name}")
+        assert_close_grad(grads[name], refs[0][name] + refs[1][name], f"accumulated {name}")
     h = hist.cpu().numpy().view(np.uint32).astype(np.int64)
     assert np.all(h.sum(axis=1) == 2 * shp.T)
 
@@ -192,7 +197,9 @@ def check_backward_stages(shp, inp, fw, bw, grads, dy, experts):
         assert_close_rms(grads["dW2_s"][s], dy_b.T @ hs, SAME, "stage dW2_s")
 
 
-@pytest.mark.parametrize("over,seed", [(dict(T=300, d=512), 0), (dict(T=77, d=512, E=40, k=3, I=192), 2)])
+@pytest.mark.parametrize("over,seed", [(dict(T=300, d=512, x_outliers=True), 0),
+                                       (dict(T=77, d=512, E=40, k=3, I=192, x_outliers=True), 2),
+                                       (dict(T=600, d=512, E=2, k=1, I=384, n_shared=3, I_shared=320), 3)])
 def test_backward_stages(over, seed):
     need_gpu()
     shp, inp_cpu, dy = layer(over, seed)
