@@ -477,6 +477,62 @@ class LayerRun:
         return self.lse.workspace_views(self.cfg, self.ws)["counts"].cpu().numpy()
 
 
+def backward_work(shp):
+    """FLOPs and algorithmic bytes of one slmoe_backward call: every contraction of the
+    backward (dgrad and wgrad of the up-projection, shared experts, routed experts and
+    down-projection, plus the recomputed pre-activations of both kinds of experts and the
+    router's two thin products), and the bytes of the weights read, the fp32 gradients
+    written, x and dy read and dx written."""
+    T, d, dl, E, k, I, ns, Is = shp.T, shp.d, shp.d_latent, shp.E, shp.k, shp.I, shp.n_shared, shp.I_shared
+    Tk = T * k
+    flops = (2 * 2 * T * d * dl            # dz, dW_out
+             + ns * 2 * T * d * 8 * Is     # gu_s recompute (2 Is), dh_s (Is), dW2_s (Is), dx (2 Is), dW13_s (2 Is)
+             + 2 * Tk * dl * 8 * I         # gu recompute (2I), dh (I), dx_lat rows (2I), dW2 (I), dW13 (2I)
+             + 2 * 2 * T * dl * d          # dx from dx_lat, dW_in
+             + 2 * 2 * Tk * d)             # router: dx and dW_r
+    weights = E * d * 4 + dl * d * 2 + E * 3 * I * dl * 2 + d * dl * 2 + ns * 3 * Is * d * 2
+    grads = (E * d + dl * d + E * 3 * I * dl + dl + d * dl + ns * 3 * Is * d) * 4
+    nbytes = weights + grads + T * d * 2 + T * d * 4 + T * d * 4
+    return flops, nbytes
+
+
+def backward_bench(run, pk, reps=5):
+    """slmoe_backward of the bench batch (after one forward that leaves its intermediates in
+    the workspace): ms per call, CUDA events on the launching stream, and its roofline."""
+    import torch
+    lse, shp, cfg = run.lse, run.shp, run.cfg
+    g = {n: torch.zeros(run.inp[w].shape, dtype=torch.float32, device="cuda") for n, w in
+         (("dW_r", "W_r"), ("dW_in", "W_in"), ("dW13", "W13"), ("dW2", "W2"), ("dgamma", "gamma"),
+          ("dW_out", "W_out"), ("dW13_s", "W13_s"), ("dW2_s", "W2_s"))}
+    G = lse.grads(g)
+    bws = torch.zeros(lse.slmoe_backward_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    dy = torch.randn(shp.T, shp.d, generator=gen, device="cuda")
+    dx = torch.empty(shp.T, shp.d, dtype=torch.float32, device="cuda")
+    run.step(run.x)
+    st = torch.zeros(4, dtype=torch.int32, device="cuda")
+    for _ in range(2):
+        lse.slmoe_backward(cfg, run.x, run.W, dy, dx, G, 0, run.ws, st, bws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(run.stream)
+    for _ in range(reps):
+        lse.slmoe_backward(cfg, run.x, run.W, dy, dx, G, 0, run.ws, st, bws)
+    e1.record(run.stream)
+    torch.cuda.synchronize()
+    assert st.cpu().tolist()[1:3] == [0, 0], st
+    ms = e0.elapsed_time(e1) / reps
+    flops, nbytes = backward_work(shp)
+    tc = pk["bf16_tflops"]
+    t_roof = max(flops / (tc * 1e12), nbytes / (pk["hbm_gbs"] * 1e9))
+    del g, G, bws
+    return {"ms_per_call": round(ms, 3), "tokens_per_s": round(shp.T / (ms * 1e-3), 1),
+            "TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 1),
+            "roofline": {"ms": round(t_roof * 1e3, 4), "frac": round(t_roof * 1e3 / ms, 4), "flops": flops,
+                         "bytes": nbytes, "tensor_peak_tflops": tc, "hbm_gbs": pk["hbm_gbs"]},
+            "note": "weight gradients fp32 (overwritten); contractions on tcgen05 (bf16 operands)"}
+
+
 def layer_summary(run, ms, pk, timed_s, reasons):
     """Tokens/s and the whole-layer roofline of one timed layer configuration."""
     st_model, flops, nbytes = work_model(run.shp, run.counts())
@@ -685,6 +741,8 @@ def main():
         extra["mid"] = layer_summary(mrun, mms, pk, mms * 0.2, reasons)
         del mrun, minp
         extra["qb_balance"] = qb_balance()
+        if args.workload == "k3_prefill":
+            extra["k3_prefill_backward"] = backward_bench(run, pk)
 
     # ---------------- oracle on the host cores (the same sample the reference arm times)
     cpu_base = None

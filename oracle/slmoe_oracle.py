@@ -345,18 +345,29 @@ def rmsnorm_backward(c, gamma, dz, eps=EPS):
     return dc, dgamma
 
 
-def backward(inp, k, dy, beta1=BETA1, beta2=BETA2, eps=EPS, forced_topk_idx=None):
+def backward(inp, k, dy, beta1=BETA1, beta2=BETA2, eps=EPS, forced_topk_idx=None, tokens=None):
     """Gradients of sum(dy * y) for one layer call, in fp64.
 
     dy [T, d] is the gradient arriving at the layer output y.  Returns dx [T, d] and the
     weight gradients dW_r [E, d], dW_in [d_l, d], dW13 [E, 2I, d_l], dW2 [E, d_l, I],
     dgamma [d_l], dW_out [d, d_l], dW13_s [n_s, 2I_s, d], dW2_s [n_s, d, I_s], plus the
     intermediates dz, dc, dg (gate weights), dx_lat and dlogit (router logits, [T, E]).
-    The selection is the oracle's own unless forced_topk_idx gives it.
+    The selection is the oracle's own unless forced_topk_idx gives it.  ``tokens`` restricts
+    the call to a subset of token rows (dy rows of those tokens): every per-token result (dx,
+    dz, dc, dg, dx_lat, dlogit) is then that of the full call for those tokens, while the
+    weight gradients hold only those tokens' contributions.
     """
-    x = f64(inp["x"])
+    x_all = inp["x"]
+    if tokens is not None:
+        tok = np.asarray(tokens)
+        x = f64(x_all[tok])
+        dy = f64(dy)[tok] if f64(dy).shape[0] == x_all.shape[0] else f64(dy)
+        if forced_topk_idx is not None:
+            forced_topk_idx = np.asarray(forced_topk_idx)[tok]
+    else:
+        x = f64(x_all)
+        dy = f64(dy)
     T, d = x.shape
-    dy = f64(dy)
     W_r, W_in, W_out = f64(inp["W_r"]), f64(inp["W_in"]), f64(inp["W_out"])
     E = W_r.shape[0]
 

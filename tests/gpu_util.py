@@ -151,6 +151,9 @@ def assert_close_grad(got, ref, what=""):
     assert got.shape == ref.shape, (what, got.shape, ref.shape)
     assert np.all(np.isfinite(got)), f"{what}: non-finite values"
     err = got - ref
+    if not np.any(ref):                       # a gradient that vanishes exactly (e.g. dW_r at k = 1)
+        assert not np.any(got), f"{what}: expected exact zeros, max |got| {np.max(np.abs(got)):.3e}"
+        return 0.0, 0.0
     fro = float(np.linalg.norm(err) / max(np.linalg.norm(ref), 1e-300))
     mx = float(np.max(np.abs(err)) / max(rms(ref), 1e-300))
     assert fro <= BWD_FRO, f"{what}: relative Frobenius error {fro:.3e} > {BWD_FRO}"

@@ -133,3 +133,14 @@ def test_backward_with_identical_experts_has_no_router_gradient():
     dgu = oracle.situ_glu_backward(gu, g["dc"] @ inp["W2"][0])
     assert np.allclose(g["dW13"].sum(axis=0), dgu.T @ x_lat, atol=1e-12)
     assert np.allclose(g["dW2"].sum(axis=0), g["dc"].T @ h, atol=1e-12)
+
+
+def test_backward_token_subsets_match_the_full_call():
+    """Per-token results of a token subset equal the full call's rows for those tokens."""
+    shp, inp = tiny_layer(7)
+    dy = np.random.default_rng(8).normal(size=(shp.T, shp.d))
+    full = oracle.backward(inp, shp.k, dy)
+    tok = [0, 3, 4]
+    sub = oracle.backward(inp, shp.k, dy, forced_topk_idx=full["topk_idx"], tokens=tok)
+    for name in ("dx", "dz", "dc", "dg", "dx_lat", "dlogit"):
+        assert np.allclose(sub[name], full[name][tok], atol=1e-12, rtol=0), name
