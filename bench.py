@@ -562,6 +562,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the decode / mid sub-results and the QB balance in the line")
     ap.add_argument("--qb-only", action="store_true", help="only the QB engine measurement")
+    ap.add_argument("--bwd-only", action="store_true",
+                    help="only the backward measurement of the workload (one forward first)")
     ap.add_argument("--no-graph", action="store_true", help="time the step without a CUDA graph")
     ap.add_argument("--skew", action="store_true", help="heavy skew (10%% hot experts)")
     args = ap.parse_args()
@@ -584,6 +586,11 @@ def main():
         return
     shp = synthetic.LAYERS[args.workload]
     inp = synthetic.layer_inputs(shp, seed=rank, device="cuda", heavy_skew=args.skew)
+    if args.bwd_only:
+        if rank == 0:
+            brun = LayerRun(shp, inp, inp["x"], inp["logit_offset"], use_graph=False)
+            print(json.dumps({"workload": args.workload, "backward": backward_bench(brun, pk, reps=args.steps)}))
+        return
     run = LayerRun(shp, inp, inp["x"], inp["logit_offset"], use_graph=not args.no_graph, warmup=args.warmup)
     for _ in range(max(0, args.warmup - 3)):
         run.timed(1)
