@@ -454,6 +454,7 @@ int slmoe_backward(const slmoe_config *cfg, const void *x, const slmoe_weights *
     if (cfg->dtype != SLMOE_BF16) return fail(SLMOE_EUNSUPPORTED, "the backward is built for the bf16 layer type");
     if (cfg->T == 0) return SLMOE_OK;
     if (cfg->E > 4096) return fail(SLMOE_EUNSUPPORTED, "E > 4096");
+    if (cfg->d_latent > 8192) return fail(SLMOE_EUNSUPPORTED, "d_latent > 8192 in the backward");
     if (!w || !grads) return fail(SLMOE_EINVAL, "weights and grads are required");
     REQ(x, "x"); REQ(dy, "dy"); REQ(dx, "dx");
     REQ(w->W_r, "W_r"); REQ(w->W_in, "W_in"); REQ(w->W13, "W13"); REQ(w->W2, "W2");
@@ -485,6 +486,9 @@ int slmoe_backward(const slmoe_config *cfg, const void *x, const slmoe_weights *
     fs.y_e = reinterpret_cast<const __nv_bfloat16 *>(fw + L.pub.y_e);
     fs.z = reinterpret_cast<const __nv_bfloat16 *>(fw + L.pub.z);
     fs.h_s = reinterpret_cast<const __nv_bfloat16 *>(fw + L.pub.h_s);
+    fs.items1 = reinterpret_cast<const int4 *>(fw + L.items1);
+    fs.items2 = reinterpret_cast<const int4 *>(fw + L.items2);
+    fs.n_items = reinterpret_cast<const int *>(fw + L.counters) + 8;
     return tc_backward(cfg, x, w, dy, dx, grads, accumulate, fs, static_cast<char *>(workspace), status,
                        static_cast<cudaStream_t>(stream));
 }

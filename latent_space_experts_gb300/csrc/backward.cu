@@ -33,6 +33,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
+#include "tc_gemm.h"
 #include "tcgen05.cuh"
 
 namespace slmoe {
@@ -50,10 +51,13 @@ constexpr int BG_MMA_WARP = 4;
 constexpr int BG_EPI_WARP0 = 5;                    // warps 5-8
 constexpr int BG_THREADS = 9 * 32;
 constexpr int BG_Q = 4;
-constexpr int BG_SMEM = BG_STAGES * BG_STAGE + 1024 + 512;
+constexpr int BG_STG_LD = 65;                      // fp32 staging row of 64 columns (+1 against bank conflicts)
+constexpr int BG_STG = 4 * 32 * BG_STG_LD * 4;     // one 32 x 64 staging tile per epilogue warp
+constexpr int BG_SMEM = BG_STAGES * BG_STAGE + BG_STG + 1024 + 512;
 constexpr int BG_BAND = 8;                         // row tiles per band of the dense tile order
 
 enum { BG_DENSE = 0, BG_PASS = 1, BG_WGRAD = 2 };
+constexpr int A_MN_ = 1, B_MN_ = 2;   // tc_dense_gemm operand majorness
 enum { BE_F32 = 0, BE_BF16 = 1, BE_DGLU = 2 };
 
 // One operand as stored: lines of ld elements; a grouped operand's expert e starts estride
@@ -140,13 +144,6 @@ __device__ __forceinline__ BItem fetch_item(const BArgs &a) {
     return it;
 }
 
-// Descriptor of an MN-major operand tile: lines of 64 M (or N) values per K row, 8-row
-// (1024-byte) swizzle atoms along K, and the next 64 M (or N) values lbo bytes further on.
-__device__ __forceinline__ uint64_t mn_desc(uint32_t saddr, uint32_t lbo) {
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) | ((uint64_t)(1024 >> 4) << 32) |
-           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
 // Copies of one operand tile (extent x 64 K) for one stage.  t = loader thread 0..127.
 //  K-major: line r = row r of the tile (M or N index), chunk c = K values 8c..8c+7.
 //  MN-major: line (g, kr) = K row kr of the 64-wide group g, chunk c = values 64g+8c..+7.
@@ -203,7 +200,8 @@ template <int EPI, bool A_MN, bool B_MN, int MODE>
 __global__ void __launch_bounds__(BG_THREADS, 1) bgemm_kernel(const BArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    BItem *q_items = reinterpret_cast<BItem *>(smem + BG_STAGES * BG_STAGE);
+    float *stg_all = reinterpret_cast<float *>(smem + BG_STAGES * BG_STAGE);
+    BItem *q_items = reinterpret_cast<BItem *>(smem + BG_STAGES * BG_STAGE + BG_STG);
     uint64_t *q_full = reinterpret_cast<uint64_t *>(q_items + BG_Q);
     uint64_t *q_empty = q_full + BG_Q;
     uint64_t *full = q_empty + BG_Q;
@@ -349,6 +347,37 @@ __global__ void __launch_bounds__(BG_THREADS, 1) bgemm_kernel(const BArgs a) {
             if (!mbar_wait(&tfull[buf], tph, wc)) break;
             tc_after();
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + buf * 256;
+            if (EPI == BE_F32 && !a.out_t) {
+                // 64 columns at a time through a 32 x 64 staging tile: each lane writes its row,
+                // then the warp stores one row at a time as two 128-byte runs (coalesced)
+                float *stg = stg_all + (warp - BG_EPI_WARP0) * 32 * BG_STG_LD;
+                float *C = static_cast<float *>(a.C) + (long long)it.e * (MODE == BG_WGRAD ? a.cstride : 0);
+                for (int c0 = 0; c0 < it.nv; c0 += 64) {
+#pragma unroll
+                    for (int cc = 0; cc < 64; cc += 16) {
+                        uint32_t r[16];
+                        TMEM_LD16(tb + c0 + cc, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) stg[lane * BG_STG_LD + cc + j] = __uint_as_float(r[j]);
+                    }
+                    __syncwarp();
+                    for (int rr = 0; rr < 32; ++rr) {
+                        const int mi = q * 32 + rr;
+                        if (mi >= it.mv) break;
+                        float *row = C + (long long)(it.m0 + mi) * a.ldc + it.n0 + c0;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int col = lane + 32 * h;
+                            if (c0 + col < it.nv) {
+                                const float v = stg[rr * BG_STG_LD + col];
+                                row[col] = a.accumulate ? row[col] + v : v;
+                            }
+                        }
+                    }
+                    __syncwarp();
+                }
+            } else
             for (int c = 0; c < it.nv; c += 16) {
                 uint32_t r[16];
                 TMEM_LD16(tb + c, r);
@@ -492,34 +521,52 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
     return s;
 }
 
-// RMSNorm + combine backward, RB_TOK tokens per block in order.  Per token: c = sum_j g_j y_e
-// (fp32, slot order, as the forward combine), r = sqrt(mean c^2 + eps), A = sum_i gamma_i dz_i
-// c_i; dc = gamma dz / r - c A / (n r^3); the expert-row gradient g_j dc (bf16, at the row's
+// RMSNorm + combine backward, RB_TOK tokens per block in order, 8 features per thread and
+// chunk (16-byte loads and stores).  Per token: c = sum_j g_j y_e (fp32, slot order, as the
+// forward combine), r = sqrt(mean c^2 + eps), A = sum_i gamma_i dz_i c_i;
+// dc = gamma dz / r - c A / (n r^3); the expert-row gradient g_j dc (bf16, at the row's
 // position in expert order), the gate-weight gradient dc . y_e(t, j), and the block's dgamma
 // sum of dz c / r (one row per block, added across blocks in order by dgamma_reduce_kernel).
 constexpr int RB_TOK = 16;
+constexpr int RB_MAXCH = 4;          // 8-feature chunks per thread: d_latent <= 8 * 256 * 4
 __global__ void __launch_bounds__(256) rms_combine_bwd_kernel(
     const bf16 *__restrict__ y_e, const float *__restrict__ topk_w, const int32_t *__restrict__ slot_pos,
     const float *__restrict__ gamma, const float *__restrict__ dz, int T, int dl, int k, float eps,
     bf16 *__restrict__ dye, float *__restrict__ dg, float *__restrict__ dgamma_part) {
-    extern __shared__ float sm[];
-    float *c = sm;                 // [dl]
-    float *dgp = sm + dl;          // [dl] this block's dgamma sum
-    float *red = sm + 2 * dl;      // [32 + 32]
-    const int tid = threadIdx.x;
-    for (int i = tid; i < dl; i += blockDim.x) dgp[i] = 0.f;
+    __shared__ float red[64];
+    __shared__ float redk[8][32];
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int nch = dl / 8;
+    float dgp[RB_MAXCH][8];
+#pragma unroll
+    for (int u = 0; u < RB_MAXCH; ++u)
+#pragma unroll
+        for (int v = 0; v < 8; ++v) dgp[u][v] = 0.f;
     const int t0 = blockIdx.x * RB_TOK;
     for (int t = t0; t < min(T, t0 + RB_TOK); ++t) {
         const int32_t *sp = slot_pos + (long long)t * k;
         const float *gw = topk_w + (long long)t * k;
         const float *dzt = dz + (long long)t * dl;
+        float cv[RB_MAXCH][8];
         float ss = 0.f, A = 0.f;
-        for (int i = tid; i < dl; i += blockDim.x) {
-            float v = 0.f;
-            for (int j = 0; j < k; ++j) v += gw[j] * __bfloat162float(y_e[(long long)sp[j] * dl + i]);
-            c[i] = v;
-            ss += v * v;
-            A += gamma[i] * dzt[i] * v;
+#pragma unroll
+        for (int u = 0; u < RB_MAXCH; ++u) {
+            const int ch = tid + u * 256;
+#pragma unroll
+            for (int v = 0; v < 8; ++v) cv[u][v] = 0.f;
+            if (ch < nch) {
+                for (int j = 0; j < k; ++j) {
+                    const uint4 q = *reinterpret_cast<const uint4 *>(y_e + (long long)sp[j] * dl + 8 * ch);
+                    const bf16 *b = reinterpret_cast<const bf16 *>(&q);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) cv[u][v] += gw[j] * __bfloat162float(b[v]);
+                }
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                    ss += cv[u][v] * cv[u][v];
+                    A += gamma[8 * ch + v] * dzt[8 * ch + v] * cv[u][v];
+                }
+            }
         }
         ss = block_sum(ss, red);
         A = block_sum(A, red + 32);
@@ -529,26 +576,57 @@ __global__ void __launch_bounds__(256) rms_combine_bwd_kernel(
         float dgl[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) dgl[j] = 0.f;
-        for (int i = tid; i < dl; i += blockDim.x) {
-            const float dci = gamma[i] * dzt[i] * ir - c[i] * coef;
-            dgp[i] += dzt[i] * c[i] * ir;
+#pragma unroll
+        for (int u = 0; u < RB_MAXCH; ++u) {
+            const int ch = tid + u * 256;
+            if (ch >= nch) continue;
+            float dc[8];
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                const float dzv = dzt[8 * ch + v];
+                dc[v] = gamma[8 * ch + v] * dzv * ir - cv[u][v] * coef;
+                dgp[u][v] += dzv * cv[u][v] * ir;
+            }
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 if (j < k) {
-                    const long long rw = (long long)sp[j] * dl + i;
-                    dgl[j] += dci * __bfloat162float(y_e[rw]);
-                    dye[rw] = __float2bfloat16_rn(gw[j] * dci);
+                    const long long rw = (long long)sp[j] * dl + 8 * ch;
+                    const uint4 q = *reinterpret_cast<const uint4 *>(y_e + rw);
+                    const bf16 *b = reinterpret_cast<const bf16 *>(&q);
+                    float dot = 0.f;
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) dot += dc[v] * __bfloat162float(b[v]);
+                    dgl[j] += dot;
+                    const float gj = gw[j];
+                    *reinterpret_cast<uint4 *>(dye + rw) =
+                        make_uint4(pack_bf16(gj * dc[0], gj * dc[1]), pack_bf16(gj * dc[2], gj * dc[3]),
+                                   pack_bf16(gj * dc[4], gj * dc[5]), pack_bf16(gj * dc[6], gj * dc[7]));
                 }
             }
         }
-        for (int j = 0; j < k; ++j) {
-            const float s = block_sum(dgl[j], red);
-            if (tid == 0) dg[(long long)t * k + j] = s;
+        // all k gate-weight sums at once: warp sums, then one thread per slot over the warps
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if (j < k) {
+                const float v = warp_sum(dgl[j]);
+                if (lane == 0) redk[w][j] = v;
+            }
+        }
+        __syncthreads();
+        if (tid < k) {
+            float sum = 0.f;
+            for (int i = 0; i < (int)(blockDim.x >> 5); ++i) sum += redk[i][tid];
+            dg[(long long)t * k + tid] = sum;
         }
         __syncthreads();
     }
-    __syncthreads();
-    for (int i = tid; i < dl; i += blockDim.x) dgamma_part[(long long)blockIdx.x * dl + i] = dgp[i];
+#pragma unroll
+    for (int u = 0; u < RB_MAXCH; ++u) {
+        const int ch = tid + u * 256;
+        if (ch < nch)
+#pragma unroll
+            for (int v = 0; v < 8; ++v) dgamma_part[(long long)blockIdx.x * dl + 8 * ch + v] = dgp[u][v];
+    }
 }
 
 __global__ void dgamma_reduce_kernel(const float *__restrict__ part, int nblk, int dl, float *dgamma,
@@ -723,6 +801,8 @@ size_t backward_workspace_bytes(const slmoe_config *c, BwdLayout *L) {
     l.items1 = take(cap1 * 16);
     l.items2 = take(cap2 * 16);
     l.items3 = take(cap3 * 16);
+    l.cap_dglu = (I + 255) / 256 * (E + (Tk + GROUPED_PASS - 1) / GROUPED_PASS);
+    l.items_dglu = take(l.cap_dglu * 16);
     l.total = off;
     if (L) *L = l;
     return off;
@@ -765,89 +845,64 @@ int tc_backward(const slmoe_config *c, const void *x, const slmoe_weights *w, co
         f32_to_bf16_kernel<<<(int)(blocks > 0 ? blocks : 1), 256, 0, st>>>(dy, dy_b, n);
         if ((rc = check_launch("f32_to_bf16"))) return rc;
     }
-    // up-projection: dz = dy W_out (fp32), dW_out (+)= dy^T z
-    if ((rc = launch_bg<BE_F32, false, true, BG_DENSE>(
-             dense_args(T, dl, d, op(dy_b, d), op(w->W_out, dl), dz, dl, 0, cnt + 0, status), st)))
+    auto opnd = [](const void *p, long long pitch) { TcOperand o; o.p = p; o.pitch = pitch; return o; };
+    // up-projection: dz = dy W_out (fp32; W_out stored [d, d_l] is MN-major here),
+    // dW_out (+)= dy^T z (both operands MN-major)
+    if ((rc = tc_dense_gemm(B_MN_, T, dl, d, opnd(dy_b, d), opnd(w->W_out, dl), dz, dl, 0, nullptr, status, cnt + 0,
+                            st)))
         return rc;
-    if ((rc = launch_bg<BE_F32, true, true, BG_DENSE>(
-             dense_args(d, dl, T, op(dy_b, d), op(fs.z, dl), g->dW_out, dl, accumulate, cnt + 1, status), st)))
+    if ((rc = tc_dense_gemm(A_MN_ | B_MN_, d, dl, T, opnd(dy_b, d), opnd(fs.z, dl), g->dW_out, dl, accumulate, nullptr,
+                            status, cnt + 1, st)))
         return rc;
     // shared experts
     for (int s = 0; s < ns; ++s) {
         const bf16 *W13s = static_cast<const bf16 *>(w->W13_s) + (size_t)s * 2 * Is * d;
         const bf16 *W2s = static_cast<const bf16 *>(w->W2_s) + (size_t)s * d * Is;
         int *cs = cnt + 2 + 5 * s;
-        // pre-activations gu_s = x W13_s^T (recomputed)
-        if ((rc = launch_bg<BE_F32, false, false, BG_DENSE>(
-                 dense_args(T, 2 * Is, d, op(x, d), op(W13s, d), gu_s, 2 * Is, 0, cs + 0, status), st)))
+        // pre-activations gu_s = x W13_s^T (recomputed, fp32)
+        if ((rc = tc_dense_gemm(0, T, 2 * Is, d, opnd(x, d), opnd(W13s, d), gu_s, 2 * Is, 0, nullptr, status, cs + 0,
+                                st)))
             return rc;
-        // dh_s = dy W2_s, turned into [dg | du] by the SiTU-GLU derivative
-        {
-            BArgs a = dense_args(T, Is, d, op(dy_b, d), op(W2s, Is), nullptr, 0, 0, cs + 1, status);
-            a.gu = gu_s; a.ld_gu = 2 * Is; a.F = Is; a.dgu = dgu_s; a.ld_dgu = 2 * Is;
-            a.beta1 = c->beta1; a.beta2 = c->beta2;
-            if ((rc = launch_bg<BE_DGLU, false, true, BG_DENSE>(a, st))) return rc;
-        }
+        // dh_s = dy W2_s (W2_s stored [d, I_s]), turned into [dg | du] by the SiTU-GLU derivative
+        TcDglu dgl;
+        dgl.gu = gu_s; dgl.ld_gu = 2 * Is; dgl.F = Is; dgl.dgu = dgu_s; dgl.ld_dgu = 2 * Is;
+        dgl.beta1 = c->beta1; dgl.beta2 = c->beta2;
+        if ((rc = tc_dense_gemm(B_MN_, T, Is, d, opnd(dy_b, d), opnd(W2s, Is), nullptr, 0, 0, &dgl, status, cs + 1, st)))
+            return rc;
         // dW2_s (+)= dy^T h_s  (h_s from the forward)
-        if ((rc = launch_bg<BE_F32, true, true, BG_DENSE>(
-                 dense_args(d, Is, T, op(dy_b, d), op(fs.h_s + (size_t)s * Is, (long long)ns * Is),
-                            g->dW2_s + (size_t)s * d * Is, Is, accumulate, cs + 2, status), st)))
+        if ((rc = tc_dense_gemm(A_MN_ | B_MN_, d, Is, T, opnd(dy_b, d), opnd(fs.h_s + (size_t)s * Is, (long long)ns * Is),
+                                g->dW2_s + (size_t)s * d * Is, Is, accumulate, nullptr, status, cs + 2, st)))
             return rc;
-        // dx += dgu_s W13_s;  dW13_s (+)= dgu_s^T x
-        if ((rc = launch_bg<BE_F32, false, true, BG_DENSE>(
-                 dense_args(T, d, 2 * Is, op(dgu_s, 2 * Is), op(W13s, d), dx, d, 1, cs + 3, status), st)))
+        // dx += [dg | du] W13_s  (W13_s stored [2 I_s, d]);  dW13_s (+)= [dg | du]^T x
+        if ((rc = tc_dense_gemm(B_MN_, T, d, 2 * Is, opnd(dgu_s, 2 * Is), opnd(W13s, d), dx, d, 1, nullptr, status,
+                                cs + 3, st)))
             return rc;
-        if ((rc = launch_bg<BE_F32, true, true, BG_DENSE>(
-                 dense_args(2 * Is, d, T, op(dgu_s, 2 * Is), op(x, d), g->dW13_s + (size_t)s * 2 * Is * d, d,
-                            accumulate, cs + 4, status), st)))
+        if ((rc = tc_dense_gemm(A_MN_ | B_MN_, 2 * Is, d, T, opnd(dgu_s, 2 * Is), opnd(x, d),
+                                g->dW13_s + (size_t)s * 2 * Is * d, d, accumulate, nullptr, status, cs + 4, st)))
             return rc;
     }
     // RMSNorm + combine backward
     {
-        const size_t smem = (2 * (size_t)dl + 64) * sizeof(float);
-        rms_combine_bwd_kernel<<<(int)L.nblk, 256, smem, st>>>(fs.y_e, fs.topk_w, fs.slot_pos, w->gamma, dz, T, dl, k,
+        rms_combine_bwd_kernel<<<(int)L.nblk, 256, 0, st>>>(fs.y_e, fs.topk_w, fs.slot_pos, w->gamma, dz, T, dl, k,
                                                                c->eps, dye, dg, dgamma_part);
         if ((rc = check_launch("rms_combine_bwd"))) return rc;
         dgamma_reduce_kernel<<<(dl + 255) / 256, 256, 0, st>>>(dgamma_part, (int)L.nblk, dl, g->dgamma, accumulate);
         if ((rc = check_launch("dgamma_reduce"))) return rc;
     }
-    // work lists of the three grouped dgrad GEMMs
-    pass_list_kernel<<<1, 1024, 0, st>>>(fs.counts, fs.offsets, E, (2 * I + 127) / 128, BG_BN, items1, cnt + 20,
-                                         (int)L.cap1);
-    if ((rc = check_launch("pass_list"))) return rc;
-    pass_list_kernel<<<1, 1024, 0, st>>>(fs.counts, fs.offsets, E, (I + 127) / 128, BG_BN, items2, cnt + 21,
-                                         (int)L.cap2);
-    if ((rc = check_launch("pass_list"))) return rc;
-    pass_list_kernel<<<1, 1024, 0, st>>>(fs.counts, fs.offsets, E, (dl + 127) / 128, BG_BN, items3, cnt + 22,
-                                         (int)L.cap3);
-    if ((rc = check_launch("pass_list"))) return rc;
-    auto pass_args = [&](int M, int K, BOp A, BOp B, const int4 *items, int *n_items, long long cap, int *counter) {
-        BArgs a = {};
-        a.A = A; a.B = B; a.M = M; a.K = K; a.items = items; a.n_items = n_items; a.units = (int)cap;
-        a.counter = counter; a.out_t = 1; a.status = status;
-        return a;
-    };
-    // pre-activations of the routed experts: gu[row] = W13[e] x_lat[perm[row]]
-    {
-        BArgs a = pass_args(2 * I, dl, op(w->W13, dl, (long long)2 * I * dl), op(fs.x_lat, dl, 0, fs.perm), items1,
-                            cnt + 20, L.cap1, cnt + 17);
-        a.C = gu; a.ldc = 2 * I;
-        if ((rc = launch_bg<BE_F32, false, false, BG_PASS>(a, st))) return rc;
-    }
-    // dh = W2[e]^T dy_e  (swap AB: W2[e] stored [d_l, I] is MN-major), then [dg | du]
-    {
-        BArgs a = pass_args(I, dl, op(w->W2, I, (long long)dl * I), op(dye, dl), items2, cnt + 21, L.cap2, cnt + 18);
-        a.gu = gu; a.ld_gu = 2 * I; a.F = I; a.dgu = dgu; a.ld_dgu = 2 * I;
-        a.beta1 = c->beta1; a.beta2 = c->beta2;
-        if ((rc = launch_bg<BE_DGLU, true, false, BG_PASS>(a, st))) return rc;
-    }
-    // x_lat gradient per expert row: dxe[row] = W13[e]^T dgu[row]
-    {
-        BArgs a = pass_args(dl, 2 * I, op(w->W13, dl, (long long)2 * I * dl), op(dgu, 2 * I), items3, cnt + 22,
-                            L.cap3, cnt + 19);
-        a.C = dxe; a.ldc = dl;
-        if ((rc = launch_bg<BE_F32, true, false, BG_PASS>(a, st))) return rc;
-    }
+    // routed experts on the forward's grouped kernel: pre-activations (the forward's gate|up
+    // list), dh -> [dg | du] (a list of 256-feature blocks of I), x_lat rows (the down list)
+    int4 *items_dglu = reinterpret_cast<int4 *>(ws + L.items_dglu);
+    if ((rc = tc_worklist_single(fs.counts, fs.offsets, E, (I + 255) / 256, items_dglu, cnt + 28, (int)L.cap_dglu, st)))
+        return rc;
+    if ((rc = tc_grouped_bwd(TC_BWD_GU32, c, w->W13, fs.x_lat, fs.perm, fs.items1, fs.n_items, cnt + 17, gu, nullptr,
+                             nullptr, status, st)))
+        return rc;
+    if ((rc = tc_grouped_bwd(TC_BWD_DGLU, c, w->W2, dye, nullptr, items_dglu, cnt + 28, cnt + 18, nullptr, gu, dgu,
+                             status, st)))
+        return rc;
+    if ((rc = tc_grouped_bwd(TC_BWD_DXE, c, w->W13, dgu, nullptr, fs.items2, fs.n_items + 1, cnt + 19, dxe, nullptr,
+                             nullptr, status, st)))
+        return rc;
     // routed weight gradients, K = the expert's rows: dW2[e] (+)= dy_e^T h, dW13[e] (+)= dgu^T x_lat
     {
         BArgs a = dense_args(dl, I, 0, op(dye, dl), op(fs.h, I), g->dW2, I, accumulate, cnt + 23, status);
@@ -865,11 +920,11 @@ int tc_backward(const slmoe_config *c, const void *x, const slmoe_weights *w, co
         slot_reduce_kernel<<<(int)(blocks > 0 ? blocks : 1), 256, 0, st>>>(dxe, fs.slot_pos, T, dl, k, dx_lat);
         if ((rc = check_launch("slot_reduce"))) return rc;
     }
-    if ((rc = launch_bg<BE_F32, false, true, BG_DENSE>(
-             dense_args(T, d, dl, op(dx_lat, dl), op(w->W_in, d), dx, d, 1, cnt + 25, status), st)))
+    if ((rc = tc_dense_gemm(B_MN_, T, d, dl, opnd(dx_lat, dl), opnd(w->W_in, d), dx, d, 1, nullptr, status, cnt + 25,
+                            st)))
         return rc;
-    if ((rc = launch_bg<BE_F32, true, true, BG_DENSE>(
-             dense_args(dl, d, T, op(dx_lat, dl), op(x, d), g->dW_in, d, accumulate, cnt + 26, status), st)))
+    if ((rc = tc_dense_gemm(A_MN_ | B_MN_, dl, d, T, opnd(dx_lat, dl), opnd(x, d), g->dW_in, d, accumulate, nullptr,
+                            status, cnt + 26, st)))
         return rc;
     // router
     router_bwd_kernel<<<T, 256, 0, st>>>(fs.scores, fs.topk_idx, fs.topk_w, fs.slot_pos, dg, w->W_r, E, d, k, dx,

@@ -96,10 +96,13 @@ struct FwdSaved {
     const float *scores, *topk_w;
     const int32_t *topk_idx, *counts, *offsets, *perm, *slot_pos;
     const __nv_bfloat16 *x_lat, *h, *y_e, *z, *h_s;
+    const int4 *items1, *items2;   // the forward's work lists (gate|up, down) and their counts
+    const int *n_items;            // [2]
 };
 struct BwdLayout {
     size_t dy_b, dz, dye, dg, gu, dgu, dxe, dx_lat, gu_s, dgu_s, dl_perm, dgamma_part, counters;
     size_t items1, items2, items3, cap1, cap2, cap3, nblk, total;
+    size_t items_dglu, cap_dglu;
 };
 size_t backward_workspace_bytes(const slmoe_config *c, BwdLayout *L);
 int tc_backward(const slmoe_config *c, const void *x, const slmoe_weights *w, const float *dy, float *dx,

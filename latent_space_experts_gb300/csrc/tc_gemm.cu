@@ -74,6 +74,12 @@ __device__ __forceinline__ bool tq_pop(int *ids, uint64_t *full, uint64_t *empty
 
 // ---------------------------------------------------------------- dense kernel
 constexpr int EPI_BF16 = 0, EPI_GLU = 1, EPI_F32 = 3;
+// Backward epilogues: dense SiTU-GLU derivative (rows = tokens); grouped (rows = features):
+// fp32 gate|up pre-activations, fp32 transposed store, SiTU-GLU derivative.
+constexpr int EPI_DGLU = 4, EPI_GU32 = 5, EPI_F32T = 6, EPI_DGLU_T = 7;
+// Operand majorness of the dense kernel (template MAJ): bit 0 = A MN-major, bit 1 = B MN-major.
+// An MN-major operand is stored [K rows, M (or N) columns]; TMA loads it in 64 x 64 boxes.
+constexpr int A_MN = 1, B_MN = 2;
 
 struct TmaPack {
     CUtensorMap a[4];
@@ -101,6 +107,14 @@ struct DenseArgs {
     // failure-path check only: the producer issues no copies, so the MMA thread's wait on
     // the first stage can only run out (nothing is in flight when the kernel aborts)
     int stall_producer;
+    int accumulate;        // EPI_F32: add into C instead of storing
+    // EPI_DGLU: dh (the accumulator) -> [dg | du] from the fp32 pre-activations gu [rows, 2F]
+    const float *gu;
+    long long ld_gu;
+    int F;
+    __nv_bfloat16 *dgu;
+    long long ld_dgu;
+    float dbeta1, dbeta2;
 };
 
 // Tile order of the dense kernel: bands of DENSE_BAND row tiles, rows fastest inside a band,
@@ -145,7 +159,21 @@ struct DenseCfg {
                   "dense tile shape");
 };
 
-template <int BN, int EPI, int PACC>
+// SiTU and its derivative for the backward epilogues (fp32, CUDA math functions).
+__device__ __forceinline__ float situ_val(float g, float b1) { return b1 * tanhf(g / b1) * (1.0f / (1.0f + expf(-g))); }
+__device__ __forceinline__ float situ_der(float g, float b1) {
+    const float th = tanhf(g / b1);
+    const float sg = 1.0f / (1.0f + expf(-g));
+    return (1.0f - th * th) * sg + b1 * th * sg * (1.0f - sg);
+}
+// [dg, du] of h = SiTU(g) * b2 tanh(u / b2) for an upstream dh.
+__device__ __forceinline__ void dglu(float dh, float g, float u, float b1, float b2, float &dg, float &du) {
+    const float tu = tanhf(u / b2);
+    dg = dh * (b2 * tu) * situ_der(g, b1);
+    du = dh * situ_val(g, b1) * (1.0f - tu * tu);
+}
+
+template <int BN, int EPI, int PACC, int MAJ = 0>
 __global__ void __launch_bounds__(DenseCfg<BN, EPI, PACC>::THREADS, 1) dense_kernel(const __grid_constant__ TmaPack maps,
                                                                                   const DenseArgs a) {
     using Cfg = DenseCfg<BN, EPI, PACC>;
@@ -212,9 +240,20 @@ __global__ void __launch_bounds__(DenseCfg<BN, EPI, PACC>::THREADS, 1) dense_ker
                     const uint32_t sa = su32(smem + stage * Cfg::STAGE);
                     const uint32_t sb = sa + Cfg::MSUB * Cfg::A_BYTES;
 #pragma unroll
-                    for (int j = 0; j < Cfg::MSUB; ++j)
-                        tma_load_2d(sa + j * Cfg::A_BYTES, &maps.a[s], &full[stage], kb * Cfg::BK, m0 + j * Cfg::BM);
-                    if (EPI == EPI_GLU) {
+                    for (int j = 0; j < Cfg::MSUB; ++j) {
+                        if (MAJ & A_MN) {
+                            tma_load_2d(sa + j * Cfg::A_BYTES, &maps.a[s], &full[stage], m0 + j * Cfg::BM, kb * Cfg::BK);
+                            tma_load_2d(sa + j * Cfg::A_BYTES + 8192, &maps.a[s], &full[stage], m0 + j * Cfg::BM + 64,
+                                        kb * Cfg::BK);
+                        } else {
+                            tma_load_2d(sa + j * Cfg::A_BYTES, &maps.a[s], &full[stage], kb * Cfg::BK, m0 + j * Cfg::BM);
+                        }
+                    }
+                    if (MAJ & B_MN) {
+#pragma unroll
+                        for (int g = 0; g < BN / 64; ++g)
+                            tma_load_2d(sb + g * 8192, &maps.b[s], &full[stage], n0 + 64 * g, kb * Cfg::BK);
+                    } else if (EPI == EPI_GLU) {
                         tma_load_2d(sb, &maps.b[s], &full[stage], kb * Cfg::BK, n0);
                         tma_load_2d(sb + (BN / 2) * 128, &maps.b[s], &full[stage], kb * Cfg::BK,
                                     n0 + a.glu_up_row);
@@ -227,7 +266,8 @@ __global__ void __launch_bounds__(DenseCfg<BN, EPI, PACC>::THREADS, 1) dense_ker
         }
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------ MMA issuer
-        constexpr uint32_t IDESC = idesc_bf16(128, BN);
+        constexpr uint32_t IDESC =
+            idesc_bf16(128, BN) | ((MAJ & A_MN) ? (1u << 15) : 0u) | ((MAJ & B_MN) ? (1u << 16) : 0u);
         int stage = 0;
         uint32_t phase = 0;
         int buf = 0;
@@ -249,11 +289,14 @@ __global__ void __launch_bounds__(DenseCfg<BN, EPI, PACC>::THREADS, 1) dense_ker
                     const uint32_t sb = sa + Cfg::MSUB * Cfg::A_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t bd = sdesc(sb + kk * 32);
+                        const uint64_t bd = (MAJ & B_MN) ? mn_desc(sb + kk * 2048, 8192) : sdesc(sb + kk * 32);
 #pragma unroll
-                        for (int j = 0; j < Cfg::MSUB; ++j)
-                            umma(tmem_base + j * Cfg::ACC + (kg % PACC) * BN, sdesc(sa + j * Cfg::A_BYTES + kk * 32), bd,
-                                 IDESC, (kg >= PACC || kk > 0) ? 1u : 0u);
+                        for (int j = 0; j < Cfg::MSUB; ++j) {
+                            const uint32_t aj = sa + j * Cfg::A_BYTES;
+                            const uint64_t ad = (MAJ & A_MN) ? mn_desc(aj + kk * 2048, 8192) : sdesc(aj + kk * 32);
+                            umma(tmem_base + j * Cfg::ACC + (kg % PACC) * BN, ad, bd, IDESC,
+                                 (kg >= PACC || kk > 0) ? 1u : 0u);
+                        }
                     }
                     umma_commit(&empty[stage]);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -321,12 +364,37 @@ __global__ void __launch_bounds__(DenseCfg<BN, EPI, PACC>::THREADS, 1) dense_ker
                     if (row_ok) {
                         if (n + 16 <= a.N) {
 #pragma unroll
-                            for (int i = 0; i < 16; i += 4)
-                                *reinterpret_cast<float4 *>(C + n + i) =
-                                    make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
-                                                __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+                            for (int i = 0; i < 16; i += 4) {
+                                float4 o = make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
+                                                       __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+                                if (a.accumulate) {
+                                    const float4 p = *reinterpret_cast<const float4 *>(C + n + i);
+                                    o.x += p.x; o.y += p.y; o.z += p.z; o.w += p.w;
+                                }
+                                *reinterpret_cast<float4 *>(C + n + i) = o;
+                            }
                         } else {
-                            for (int i = 0; i < 16 && n + i < a.N; ++i) C[n + i] = __uint_as_float(r[i]);
+                            for (int i = 0; i < 16 && n + i < a.N; ++i)
+                                C[n + i] = __uint_as_float(r[i]) + (a.accumulate ? C[n + i] : 0.f);
+                        }
+                    }
+                }
+            } else if (EPI == EPI_DGLU) {
+                // rows are tokens, columns features f: gate at f, up at F + f
+                const float *gr = a.gu + (long long)row * a.ld_gu;
+                __nv_bfloat16 *dr = a.dgu + (long long)row * a.ld_dgu;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 16) {
+                    uint32_t r[16];
+                    TMEM_LD16(tb + c, r);
+                    tmem_wait_ld();
+                    const int n = n0 + c;
+                    if (row_ok) {
+                        for (int i = 0; i < 16 && n + i < a.N; ++i) {
+                            float dg, du;
+                            dglu(__uint_as_float(r[i]), gr[n + i], gr[a.F + n + i], a.dbeta1, a.dbeta2, dg, du);
+                            dr[n + i] = __float2bfloat16_rn(dg);
+                            dr[a.F + n + i] = __float2bfloat16_rn(du);
                         }
                     }
                 }
@@ -669,12 +737,16 @@ struct GroupedArgs {
     const __nv_bfloat16 *b_src;
     long long b_ld;
     int b_K;
-    __nv_bfloat16 *out;
+    void *out;            // bf16 (forward epilogues) or fp32 (EPI_GU32, EPI_F32T)
     long long out_ld;
-    int out_cols;
+    int out_cols;         // features of the output (EPI_GU32 / EPI_DGLU_T: the up half's offset F)
     float beta1, beta2;
     int32_t *status;
     unsigned long long wait_limit_ns;   // 0 = the default limit of every bounded wait
+    const float *gu;      // EPI_DGLU_T: fp32 pre-activations [rows, 2F]
+    long long ld_gu;
+    __nv_bfloat16 *dgu;   // EPI_DGLU_T: [dg | du] out, bf16 [rows, 2F]
+    long long ld_dgu;
 };
 
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *map, uint64_t *bar,
@@ -756,7 +828,11 @@ worklist_kernel(const int32_t *__restrict__ counts, const int32_t *__restrict__ 
     }
 }
 
-template <int EPI, bool DBUF>
+// AMN: the weights are MN-major (stored [K rows, features], the transposed use of a forward
+// weight in the backward): each 128-feature sub-tile is two 64 x 64 TMA boxes; a_rows_pe is then
+// the K rows per expert, a_fb_stride the features per block and a_sub1 the second sub-tile's
+// feature offset.
+template <int EPI, bool DBUF, bool AMN = false>
 __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const __grid_constant__ CUtensorMap wmap,
                                                                const GroupedArgs a) {
     using Cfg = GCfg<DBUF>;
@@ -846,7 +922,15 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
                 if (!mbar_wait(&a_empty[stage], phase ^ 1, abort_flag)) goto done;
                 mbar_expect_tx(&a_full[stage], Cfg::A_BYTES);
                 const uint32_t sa = su32(sA + stage * Cfg::A_BYTES);
-                if (multi) {       // other passes of this tile run alongside: normal L2 policy
+                if (AMN) {         // features fb * stride (+ sub1), K rows of expert it.x
+                    const int f0 = fb * a.a_fb_stride, kr = it.x * a.a_rows_pe + kb * 64;
+#pragma unroll
+                    for (int sub = 0; sub < 2; ++sub)
+#pragma unroll
+                        for (int g = 0; g < 2; ++g)
+                            tma_load_2d_hint(sa + sub * 128 * 128 + g * 8192, &wmap, &a_full[stage],
+                                             f0 + sub * a.a_sub1 + 64 * g, kr, pol_first);
+                } else if (multi) {   // other passes of this tile run alongside: normal L2 policy
                     tma_load_2d(sa, &wmap, &a_full[stage], kb * 64, row0);
                     tma_load_2d(sa + 128 * 128, &wmap, &a_full[stage], kb * 64, row0 + a.a_sub1);
                 } else {           // streamed once
@@ -864,7 +948,7 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
             int4 it;
             if (!pop(qs, qp, it, false)) goto done;
             if (it.w < 0) break;
-            const uint32_t idesc = idesc_bf16(128, (it.w + 15) & ~15);
+            const uint32_t idesc = idesc_bf16(128, (it.w + 15) & ~15) | (AMN ? (1u << 15) : 0u);
             if (!mbar_wait(&tempty[buf], tph ^ 1, abort_flag)) goto done;
             tc_after();
             const uint32_t d = tmem_base + buf * 256;
@@ -879,8 +963,13 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
                     const uint64_t bd = sdesc(sb + kk * 32);
-                    umma(d, sdesc(sa + kk * 32), bd, idesc, acc);
-                    umma(d + SUB1, sdesc(sa + 128 * 128 + kk * 32), bd, idesc, acc);
+                    if (AMN) {
+                        umma(d, mn_desc(sa + kk * 2048, 8192), bd, idesc, acc);
+                        umma(d + SUB1, mn_desc(sa + 128 * 128 + kk * 2048, 8192), bd, idesc, acc);
+                    } else {
+                        umma(d, sdesc(sa + kk * 32), bd, idesc, acc);
+                        umma(d + SUB1, sdesc(sa + 128 * 128 + kk * 32), bd, idesc, acc);
+                    }
                 }
                 umma_commit(&a_empty[as]);
                 umma_commit(&b_empty[bs]);
@@ -908,14 +997,15 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
             if (!mbar_wait(&tfull[buf], tph, abort_flag)) goto done;
             tc_after();
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + buf * 256;
-            // GLU: the sub-tiles are the gate and up rows of h column fb*128 + lf.  Plain: they
-            // are output features fb*256 + lf and fb*256 + 128 + lf.
-            const int f = (EPI == EPI_GLU ? fb * 128 : fb * 256) + lf;
+            // GLU / GU32: the sub-tiles are the gate and up rows of feature fb*128 + lf.
+            // Otherwise they are features fb*256 + lf and fb*256 + 128 + lf.
+            constexpr bool GU_LAYOUT = EPI == EPI_GLU || EPI == EPI_GU32;
+            const int f = (GU_LAYOUT ? fb * 128 : fb * 256) + lf;
             const bool ok = f < a.out_cols;
-            const bool ok1 = f + 128 < a.out_cols;
-            __nv_bfloat16 *o = a.out + (long long)it.z * a.out_ld + f;
+            const bool ok1 = GU_LAYOUT ? ok : f + 128 < a.out_cols;
             for (int c = half * 16; c < Np; c += 16 * WPQ) {
                 if (EPI == EPI_GLU) {
+                    __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.out) + (long long)it.z * a.out_ld + f;
                     uint32_t g[16], v[16];
                     TMEM_LD16(tb + c, g);
                     TMEM_LD16(tb + SUB1 + c, v);
@@ -934,10 +1024,38 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
                     tmem_wait_ld();
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        if (c + j < N) {
-                            __nv_bfloat16 *orow = o + (long long)(c + j) * a.out_ld;
-                            if (ok) orow[0] = __float2bfloat16_rn(__uint_as_float(r0[j]));
-                            if (ok1) orow[128] = __float2bfloat16_rn(__uint_as_float(r1[j]));
+                        if (c + j >= N) continue;
+                        const long long row = (long long)it.z + c + j;
+                        const float v0 = __uint_as_float(r0[j]), v1 = __uint_as_float(r1[j]);
+                        if (EPI == EPI_BF16) {
+                            __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) + row * a.out_ld + f;
+                            if (ok) orow[0] = __float2bfloat16_rn(v0);
+                            if (ok1) orow[128] = __float2bfloat16_rn(v1);
+                        } else if (EPI == EPI_F32T) {
+                            float *orow = static_cast<float *>(a.out) + row * a.out_ld + f;
+                            if (ok) orow[0] = v0;
+                            if (ok1) orow[128] = v1;
+                        } else if (EPI == EPI_GU32) {      // gate at f, up at F + f
+                            float *orow = static_cast<float *>(a.out) + row * a.out_ld + f;
+                            if (ok) {
+                                orow[0] = v0;
+                                orow[a.out_cols] = v1;
+                            }
+                        } else if (EPI == EPI_DGLU_T) {    // dh of features f and f + 128
+                            const float *gr = a.gu + row * a.ld_gu;
+                            __nv_bfloat16 *dr = a.dgu + row * a.ld_dgu;
+                            const int F = a.out_cols;
+                            float dg, du;
+                            if (ok) {
+                                dglu(v0, gr[f], gr[F + f], a.beta1, a.beta2, dg, du);
+                                dr[f] = __float2bfloat16_rn(dg);
+                                dr[F + f] = __float2bfloat16_rn(du);
+                            }
+                            if (ok1) {
+                                dglu(v1, gr[f + 128], gr[F + f + 128], a.beta1, a.beta2, dg, du);
+                                dr[f + 128] = __float2bfloat16_rn(dg);
+                                dr[F + f + 128] = __float2bfloat16_rn(du);
+                            }
                         }
                     }
                 }
@@ -1046,13 +1164,13 @@ int set_smem(K kern, int bytes) {
     return SLMOE_OK;
 }
 
-template <int BN, int EPI, int PACC>
+template <int BN, int EPI, int PACC, int MAJ = 0>
 int launch_dense(const TmaPack &maps, DenseArgs a, cudaStream_t st) {
     using Cfg = DenseCfg<BN, EPI, PACC>;
     a.tiles_n = (a.N + Cfg::BN_OUT - 1) / Cfg::BN_OUT;
     a.tiles = ((a.M + Cfg::BM_TILE - 1) / Cfg::BM_TILE) * a.tiles_n;
     if (a.tiles == 0) return SLMOE_OK;
-    auto kern = dense_kernel<BN, EPI, PACC>;
+    auto kern = dense_kernel<BN, EPI, PACC, MAJ>;
     int rc = set_smem(kern, Cfg::SMEM);
     if (rc) return rc;
     const int sms = sm_count();
@@ -1076,9 +1194,9 @@ int launch_dense_bn(int bn, const TmaPack &maps, const DenseArgs &a, cudaStream_
     return bn == 64 ? launch_dense<64, EPI, 1>(maps, a, st) : launch_dense<256, EPI, 1>(maps, a, st);
 }
 
-template <int EPI, bool DBUF>
+template <int EPI, bool DBUF, bool AMN = false>
 int launch_grouped(const CUtensorMap &wmap, const GroupedArgs &a, cudaStream_t st) {
-    auto kern = grouped_kernel<EPI, DBUF>;
+    auto kern = grouped_kernel<EPI, DBUF, AMN>;
     int rc = set_smem(kern, GCfg<DBUF>::SMEM);
     if (rc) return rc;
     kern<<<sm_count(), GCfg<DBUF>::THREADS, GCfg<DBUF>::SMEM, st>>>(wmap, a);
@@ -1273,6 +1391,94 @@ int tc_forward_back(const slmoe_config *c, const slmoe_weights *w, const TcForwa
     }
     stage_event(8, st);
     return SLMOE_OK;
+}
+
+// ---------------------------------------------------------------- backward contractions
+namespace {
+template <int EPI, int MAJ>
+int launch_tc_bwd_dense(int bn, const TmaPack &maps, const DenseArgs &a, cudaStream_t st) {
+    return bn == 64 ? launch_dense<64, EPI, 1, MAJ>(maps, a, st) : launch_dense<256, EPI, 1, MAJ>(maps, a, st);
+}
+template <int EPI>
+int launch_tc_bwd_maj(int maj, int bn, const TmaPack &maps, const DenseArgs &a, cudaStream_t st) {
+    switch (maj) {
+    case 0: return launch_tc_bwd_dense<EPI, 0>(bn, maps, a, st);
+    case A_MN: return launch_tc_bwd_dense<EPI, A_MN>(bn, maps, a, st);
+    case B_MN: return launch_tc_bwd_dense<EPI, B_MN>(bn, maps, a, st);
+    default: return launch_tc_bwd_dense<EPI, A_MN | B_MN>(bn, maps, a, st);
+    }
+}
+}  // namespace
+
+int tc_dense_gemm(int maj, int M, int N, int K, TcOperand A, TcOperand B, void *C, long long ldc, int accumulate,
+                  const TcDglu *dg, int32_t *status, int *counter, cudaStream_t st) {
+    if (M == 0 || N == 0) return SLMOE_OK;
+    if (K == 0) return fail(SLMOE_EINVAL, "dense GEMM with K = 0");
+    const int bn = dense_bn(M, N, false);
+    TmaPack maps;
+    memset(&maps, 0, sizeof(maps));
+    int rc;
+    if (maj & A_MN) rc = make_map(&maps.a[0], A.p, K, M, A.pitch, 64);
+    else rc = make_map(&maps.a[0], A.p, M, K, A.pitch, 128);
+    if (rc) return rc;
+    if (maj & B_MN) rc = make_map(&maps.b[0], B.p, K, N, B.pitch, 64);
+    else rc = make_map(&maps.b[0], B.p, N, K, B.pitch, bn);
+    if (rc) return rc;
+    DenseArgs a = {};
+    a.M = M; a.N = N; a.nseg = 1; a.kblocks[0] = (K + 63) / 64;
+    a.C = C; a.ldc = ldc; a.accumulate = accumulate; a.status = status; a.counter = counter;
+    if (dg) {
+        a.gu = dg->gu; a.ld_gu = dg->ld_gu; a.F = dg->F; a.dgu = dg->dgu; a.ld_dgu = dg->ld_dgu;
+        a.dbeta1 = dg->beta1; a.dbeta2 = dg->beta2;
+        return launch_tc_bwd_maj<EPI_DGLU>(maj, bn, maps, a, st);
+    }
+    return launch_tc_bwd_maj<EPI_F32>(maj, bn, maps, a, st);
+}
+
+int tc_grouped_bwd(int kind, const slmoe_config *c, const void *W, const void *rows, const int32_t *row_index,
+                   const int4 *items, const int *n_items, int *counter, void *out, const float *gu,
+                   __nv_bfloat16 *dgu, int32_t *status, cudaStream_t st) {
+    const int E = c->E, I = c->I, dl = c->d_latent;
+    CUtensorMap wm;
+    GroupedArgs a = {};
+    a.items = items; a.n_items = n_items; a.counter = counter; a.status = status;
+    a.beta1 = c->beta1; a.beta2 = c->beta2;
+    a.b_index = row_index;
+    a.b_src = static_cast<const __nv_bfloat16 *>(rows);
+    a.out = out;
+    int rc;
+    if (kind == TC_BWD_GU32) {
+        // pre-activations of the routed experts, as the forward gate|up: gu[row] = W13[e] x_lat
+        if ((rc = make_map(&wm, W, (long long)E * 2 * I, dl, dl, 128))) return rc;
+        a.kblocks = (dl + 63) / 64;
+        a.a_rows_pe = 2 * I; a.a_sub1 = I; a.a_fb_stride = 128;
+        a.b_ld = dl; a.b_K = dl;
+        a.out_ld = 2 * I; a.out_cols = I;
+        return launch_grouped<EPI_GU32, false>(wm, a, st);
+    }
+    if (kind == TC_BWD_DGLU) {
+        // dh = W2[e]^T dy_e (W2[e] stored [d_l, I]: MN-major), then [dg | du]
+        if ((rc = make_map(&wm, W, (long long)E * dl, I, I, 64))) return rc;
+        a.kblocks = (dl + 63) / 64;
+        a.a_rows_pe = dl; a.a_sub1 = 128; a.a_fb_stride = 256;
+        a.b_ld = dl; a.b_K = dl;
+        a.out_cols = I; a.gu = gu; a.ld_gu = 2 * I; a.dgu = dgu; a.ld_dgu = 2 * I;
+        return launch_grouped<EPI_DGLU_T, false, true>(wm, a, st);
+    }
+    // TC_BWD_DXE: the x_lat gradient of each expert row, W13[e]^T [dg | du] (W13[e] stored [2I, d_l])
+    if ((rc = make_map(&wm, W, (long long)E * 2 * I, dl, dl, 64))) return rc;
+    a.kblocks = (2 * I + 63) / 64;
+    a.a_rows_pe = 2 * I; a.a_sub1 = 128; a.a_fb_stride = 256;
+    a.b_ld = 2 * I; a.b_K = 2 * I;
+    a.out_ld = dl; a.out_cols = dl;
+    return launch_grouped<EPI_F32T, false, true>(wm, a, st);
+}
+
+int tc_worklist_single(const int32_t *counts, const int32_t *offsets, int E, int nfb, int4 *items, int *n_items,
+                       int max_items, cudaStream_t st) {
+    worklist_kernel<<<1, 1024, 0, st>>>(counts, offsets, E, nfb, GCfg<false>::PASS, items, 0, GCfg<false>::PASS, items,
+                                        n_items, max_items, 0);
+    return check_launch("worklist");
 }
 
 // One tile of the dense kernel whose producer issues no copies: the MMA thread's first wait

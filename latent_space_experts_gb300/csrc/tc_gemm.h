@@ -40,6 +40,40 @@ int tc_worklists(const slmoe_config *c, const TcForward &f, cudaStream_t st);
 int tc_forward_back(const slmoe_config *c, const slmoe_weights *w, const TcForward &f, void *y,
                     cudaStream_t st);
 
+// ---------------------------------------------------------------- backward contractions
+// A stored row-major matrix: p, its rows, columns and pitch (elements).  The dense GEMM reads A
+// as [M rows, K cols] (K-major) or [K rows, M cols] (MN-major, maj & 1), B as [N rows, K cols]
+// or [K rows, N cols] (maj & 2).
+struct TcOperand {
+    const void *p;
+    long long pitch;
+};
+// SiTU-GLU derivative epilogue: the accumulator is dh [rows, F]; gu holds the fp32 gate and up
+// pre-activations [rows, 2F]; [dg | du] goes to dgu (bf16, [rows, 2F]).
+struct TcDglu {
+    const float *gu;
+    long long ld_gu;
+    int F;
+    __nv_bfloat16 *dgu;
+    long long ld_dgu;
+    float beta1, beta2;
+};
+// C[M, N] = (or +=) A . B^T in fp32 (dg == NULL), or the SiTU-GLU derivative of it.
+int tc_dense_gemm(int maj, int M, int N, int K, TcOperand A, TcOperand B, void *C, long long ldc, int accumulate,
+                  const TcDglu *dg, int32_t *status, int *counter, cudaStream_t st);
+enum { TC_BWD_GU32 = 0, TC_BWD_DGLU = 1, TC_BWD_DXE = 2 };
+// Grouped backward contractions on the routed experts' work lists (items of 192-token passes):
+//   TC_BWD_GU32: gu[row] = W13[e] rows[index[row]] (fp32 gate|up pre-activations; the forward's
+//                gate|up list, 128-feature blocks);
+//   TC_BWD_DGLU: [dg | du][row] from dh = W2[e]^T rows[row] and gu (list of 256-feature blocks of I);
+//   TC_BWD_DXE:  out[row] = W13[e]^T rows[row] (fp32; the forward's down list, 256-feature blocks).
+int tc_grouped_bwd(int kind, const slmoe_config *c, const void *W, const void *rows, const int32_t *row_index,
+                   const int4 *items, const int *n_items, int *counter, void *out, const float *gu,
+                   __nv_bfloat16 *dgu, int32_t *status, cudaStream_t st);
+// One work list of nfb feature blocks (192-token passes) from the expert counts and offsets.
+int tc_worklist_single(const int32_t *counts, const int32_t *offsets, int E, int nfb, int4 *items, int *n_items,
+                       int max_items, cudaStream_t st);
+
 // Failure-path check: one launch of a tensor-core kernel whose bounded waits must run out
 // (see slmoe_wait_abort_check).
 int tc_wait_abort_check(int32_t *status, unsigned long long wait_limit_ns, cudaStream_t st);

@@ -60,6 +60,13 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
     return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
+// MN-major operand tile: lines of 64 M (or N) values per K row in the 128-byte swizzle, 8-row
+// (1024-byte) atoms along K, the next 64 M (or N) values lbo bytes further on.  The start
+// address advances 2048 bytes (two atoms) per K = 16 step.
+__device__ __forceinline__ uint64_t mn_desc(uint32_t saddr, uint32_t lbo) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
 // Instruction descriptor, kind::f16: bf16 A and B (K-major), fp32 D, shape M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
