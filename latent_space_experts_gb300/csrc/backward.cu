@@ -353,26 +353,42 @@ __global__ void __launch_bounds__(BG_THREADS, 1) bgemm_kernel(const BArgs a) {
                 float *stg = stg_all + (warp - BG_EPI_WARP0) * 32 * BG_STG_LD;
                 float *C = static_cast<float *>(a.C) + (long long)it.e * (MODE == BG_WGRAD ? a.cstride : 0);
                 for (int c0 = 0; c0 < it.nv; c0 += 64) {
+                    uint32_t r[4][16];
 #pragma unroll
-                    for (int cc = 0; cc < 64; cc += 16) {
-                        uint32_t r[16];
-                        TMEM_LD16(tb + c0 + cc, r);
-                        tmem_wait_ld();
+                    for (int u = 0; u < 4; ++u) TMEM_LD16(tb + c0 + 16 * u, r[u]);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) stg[lane * BG_STG_LD + cc + j] = __uint_as_float(r[j]);
-                    }
+                    for (int u = 0; u < 4; ++u)
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) stg[lane * BG_STG_LD + 16 * u + j] = __uint_as_float(r[u][j]);
                     __syncwarp();
-                    for (int rr = 0; rr < 32; ++rr) {
-                        const int mi = q * 32 + rr;
-                        if (mi >= it.mv) break;
-                        float *row = C + (long long)(it.m0 + mi) * a.ldc + it.n0 + c0;
+                    // eight rows at a time: all staging reads (and, when adding, all reads of C)
+                    // issued before the stores, so the latencies overlap
+                    const bool c_ok[2] = {c0 + lane < it.nv, c0 + lane + 32 < it.nv};
+#pragma unroll 1
+                    for (int rr0 = 0; rr0 < 32; rr0 += 8) {
+                        float v[8][2];
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int col = lane + 32 * h;
-                            if (c0 + col < it.nv) {
-                                const float v = stg[rr * BG_STG_LD + col];
-                                row[col] = a.accumulate ? row[col] + v : v;
+                        for (int i = 0; i < 8; ++i)
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) v[i][h] = stg[(rr0 + i) * BG_STG_LD + lane + 32 * h];
+                        if (a.accumulate) {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const int mi = q * 32 + rr0 + i;
+                                const float *row = C + (long long)(it.m0 + mi) * a.ldc + it.n0 + c0;
+#pragma unroll
+                                for (int h = 0; h < 2; ++h)
+                                    if (mi < it.mv && c_ok[h]) v[i][h] += row[lane + 32 * h];
                             }
+                        }
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int mi = q * 32 + rr0 + i;
+                            float *row = C + (long long)(it.m0 + mi) * a.ldc + it.n0 + c0;
+#pragma unroll
+                            for (int h = 0; h < 2; ++h)
+                                if (mi < it.mv && c_ok[h]) row[lane + 32 * h] = v[i][h];
                         }
                     }
                     __syncwarp();
