@@ -35,6 +35,7 @@
 #include "ptx.cuh"
 #include "tc_gemm.h"
 #include "tcgen05.cuh"
+#include "tmap.h"
 
 namespace slmoe {
 namespace {
@@ -196,8 +197,12 @@ __device__ __forceinline__ float situ_grad_f(float g, float b1) {
     return (1.0f - th * th) * sg + b1 * th * sg * (1.0f - sg);
 }
 
-template <int EPI, bool A_MN, bool B_MN, int MODE>
-__global__ void __launch_bounds__(BG_THREADS, 1) bgemm_kernel(const BArgs a) {
+// B_TMA: the B operand (MN-major, stored rows in expert order) comes by TMA in 64 x 64 boxes
+// from bmap; rows past the expert's segment then hold other experts' values, which meet the
+// zero-filled rows of A past the segment, so they add nothing.
+template <int EPI, bool A_MN, bool B_MN, int MODE, bool B_TMA = false>
+__global__ void __launch_bounds__(BG_THREADS, 1) bgemm_kernel(const __grid_constant__ CUtensorMap bmap,
+                                                              const BArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *stg_all = reinterpret_cast<float *>(smem + BG_STAGES * BG_STAGE);
@@ -219,7 +224,7 @@ __global__ void __launch_bounds__(BG_THREADS, 1) bgemm_kernel(const BArgs a) {
             mbar_init(&q_empty[i], 4 + 1 + 4);   // loader warps, MMA thread, epilogue warps
         }
         for (int s = 0; s < BG_STAGES; ++s) {
-            mbar_init(&full[s], BG_LOADERS);
+            mbar_init(&full[s], BG_LOADERS + (B_TMA ? 1 : 0));
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -249,11 +254,16 @@ __global__ void __launch_bounds__(BG_THREADS, 1) bgemm_kernel(const BArgs a) {
         return true;
     };
 
+    int l_stage = 0;                  // loader ring position, kept for the drain of TMA copies
+    uint32_t l_phase = 0;
+    bool l_wrapped = false;
     if (warp < 4) {
         // ------------------------------------------------ loaders (warp 0 lane 0 also fetches)
         const int t = threadIdx.x;
-        int qs = 0, fs = 0, stage = 0;
-        uint32_t qp = 0, fp = 0, phase = 0;
+        int qs = 0, fs = 0;
+        int &stage = l_stage;
+        uint32_t qp = 0, fp = 0;
+        uint32_t &phase = l_phase;
         for (;;) {
             if (warp == 0) {
                 int ok = 1;
@@ -279,9 +289,18 @@ __global__ void __launch_bounds__(BG_THREADS, 1) bgemm_kernel(const BArgs a) {
                 const uint32_t sa = su32(smem + stage * BG_STAGE);
                 const uint32_t sb = sa + BG_A_BYTES;
                 load_tile<A_MN, 128>(sa, a.A, it.e, it.m0, it.mv, it.kr0, kb * 64, it.klen, t);
-                load_tile<B_MN, BG_BN>(sb, a.B, it.e, it.n0, it.nv, it.kr0, kb * 64, it.klen, t);
+                if (B_TMA) {
+                    if (t == 0) {
+                        mbar_expect_tx(&full[stage], BG_B_BYTES);
+#pragma unroll
+                        for (int g = 0; g < BG_BN / 64; ++g)
+                            tma_load_2d(sb + g * 8192, &bmap, &full[stage], it.n0 + 64 * g, it.kr0 + kb * 64);
+                    }
+                } else {
+                    load_tile<B_MN, BG_BN>(sb, a.B, it.e, it.n0, it.nv, it.kr0, kb * 64, it.klen, t);
+                }
                 cp_async_arrive_noinc(&full[stage]);
-                if (++stage == BG_STAGES) { stage = 0; phase ^= 1; }
+                if (++stage == BG_STAGES) { stage = 0; phase ^= 1; l_wrapped = true; }
             }
             if (aborted) break;
         }
@@ -340,7 +359,8 @@ __global__ void __launch_bounds__(BG_THREADS, 1) bgemm_kernel(const BArgs a) {
                 // an expert without rows: its weight-gradient tile is zero (stored unless adding)
                 if (EPI == BE_F32 && !a.accumulate && row_ok) {
                     float *C = static_cast<float *>(a.C) + (long long)it.e * a.cstride;
-                    for (int j = 0; j < it.nv; ++j) C[(long long)m * a.ldc + it.n0 + j] = 0.f;
+                    for (int j = 0; j < it.nv; ++j)
+                        C[a.out_t ? (long long)(it.n0 + j) * a.ldc + m : (long long)m * a.ldc + it.n0 + j] = 0.f;
                 }
                 continue;
             }
@@ -419,11 +439,19 @@ __global__ void __launch_bounds__(BG_THREADS, 1) bgemm_kernel(const BArgs a) {
                             for (int j = 0; j < nj; ++j)
                                 row[j] = __uint_as_float(r[j]) + (a.accumulate ? row[j] : 0.f);
                         }
-                    } else {
-                        for (int j = 0; j < nj; ++j) {
-                            float *o = C + (long long)(it.n0 + c + j) * a.ldc + m;
-                            *o = __uint_as_float(r[j]) + (a.accumulate ? *o : 0.f);
+                    } else {   // lanes are consecutive m: every store is one 128-byte run
+                        float *o = C + (long long)(it.n0 + c) * a.ldc + m;
+                        float v[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+                        if (a.accumulate) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                if (j < nj) v[j] += o[(long long)j * a.ldc];
                         }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            if (j < nj) o[(long long)j * a.ldc] = v[j];
                     }
                 } else if (EPI == BE_BF16) {
                     bf16 *C = static_cast<bf16 *>(a.C);
@@ -456,7 +484,8 @@ __global__ void __launch_bounds__(BG_THREADS, 1) bgemm_kernel(const BArgs a) {
         }
     }
     __syncthreads();
-    if (wc->abort) {   // let MMAs in flight finish before TMEM is freed (loaders waited above)
+    if (wc->abort) {   // let copies and MMAs in flight finish before TMEM is freed
+        if (B_TMA && threadIdx.x == 0) drain_ring(full, BG_STAGES, l_stage, l_phase, l_wrapped);
         if (warp == BG_MMA_WARP && lane == 0) {
             umma_commit(mma_drain);
             mbar_wait_drain(mma_drain, 0);
@@ -741,15 +770,22 @@ __global__ void __launch_bounds__(256) router_wgrad_kernel(const bf16 *__restric
 }
 
 // ---------------------------------------------------------------- host side
-template <int EPI, bool AMN, bool BMN, int MODE>
-int launch_bg(BArgs a, cudaStream_t st) {
-    auto kern = bgemm_kernel<EPI, AMN, BMN, MODE>;
+template <int EPI, bool AMN, bool BMN, int MODE, bool B_TMA = false>
+int launch_bg(BArgs a, cudaStream_t st, long long b_rows = 0) {
+    auto kern = bgemm_kernel<EPI, AMN, BMN, MODE, B_TMA>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BG_SMEM);
     if (e != cudaSuccess) return fail(SLMOE_ECUDA, "smem attribute: %s", cudaGetErrorString(e));
     if (MODE != BG_PASS && a.units == 0) return SLMOE_OK;
+    CUtensorMap bmap;
+    memset(&bmap, 0, sizeof(bmap));
+    if (B_TMA) {   // B stored [b_rows, N] (MN-major), 64 x 64 boxes, 128-byte swizzle
+        int rc = tmap_encode_2d(&bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.B.p, b_rows, a.N, a.B.ld, 64, 64,
+                                CU_TENSOR_MAP_SWIZZLE_128B);
+        if (rc) return rc;
+    }
     const int sms = sm_count();
     const int grid = (MODE != BG_PASS && a.units < sms) ? a.units : sms;
-    kern<<<grid, BG_THREADS, BG_SMEM, st>>>(a);
+    kern<<<grid, BG_THREADS, BG_SMEM, st>>>(bmap, a);
     return check_launch("bgemm_kernel");
 }
 
@@ -919,15 +955,18 @@ int tc_backward(const slmoe_config *c, const void *x, const slmoe_weights *w, co
     if ((rc = tc_grouped_bwd(TC_BWD_DXE, c, w->W13, dgu, nullptr, fs.items2, fs.n_items + 1, cnt + 19, dxe, nullptr,
                              nullptr, status, st)))
         return rc;
-    // routed weight gradients, K = the expert's rows: dW2[e] (+)= dy_e^T h, dW13[e] (+)= dgu^T x_lat
+    // routed weight gradients, K = the expert's rows, computed transposed so that each lane
+    // (an M index) stores along a row of the gradient:
+    //   dW2[e]^T  [I, d_l]  = h^T dy_e             (A = h, B = dy_e by TMA)
+    //   dW13[e]^T [d_l, 2I] = x_lat[perm]^T [dg|du] (A = x_lat gathered, B = [dg|du] by TMA)
     {
-        BArgs a = dense_args(dl, I, 0, op(dye, dl), op(fs.h, I), g->dW2, I, accumulate, cnt + 23, status);
-        a.offsets = fs.offsets; a.units = E * a.tiles_m * a.tiles_n; a.cstride = (long long)dl * I;
-        if ((rc = launch_bg<BE_F32, true, true, BG_WGRAD>(a, st))) return rc;
-        BArgs b = dense_args(2 * I, dl, 0, op(dgu, 2 * I), op(fs.x_lat, dl, 0, fs.perm), g->dW13, dl, accumulate,
+        BArgs a = dense_args(I, dl, 0, op(fs.h, I), op(dye, dl), g->dW2, I, accumulate, cnt + 23, status);
+        a.offsets = fs.offsets; a.units = E * a.tiles_m * a.tiles_n; a.cstride = (long long)dl * I; a.out_t = 1;
+        if ((rc = launch_bg<BE_F32, true, true, BG_WGRAD, true>(a, st, Tk))) return rc;
+        BArgs b = dense_args(dl, 2 * I, 0, op(fs.x_lat, dl, 0, fs.perm), op(dgu, 2 * I), g->dW13, dl, accumulate,
                              cnt + 24, status);
-        b.offsets = fs.offsets; b.units = E * b.tiles_m * b.tiles_n; b.cstride = (long long)2 * I * dl;
-        if ((rc = launch_bg<BE_F32, true, true, BG_WGRAD>(b, st))) return rc;
+        b.offsets = fs.offsets; b.units = E * b.tiles_m * b.tiles_n; b.cstride = (long long)2 * I * dl; b.out_t = 1;
+        if ((rc = launch_bg<BE_F32, true, true, BG_WGRAD, true>(b, st, Tk))) return rc;
     }
     // dx_lat = sum over the token's k rows; then the latent down-projection
     {
