@@ -444,3 +444,56 @@ def backward(inp, k, dy, beta1=BETA1, beta2=BETA2, eps=EPS, forced_topk_idx=None
     return dict(dx=dx, dW_r=dW_r, dW_in=dW_in, dW13=dW13, dW2=dW2, dgamma=dgamma, dW_out=dW_out,
                 dW13_s=dW13_s, dW2_s=dW2_s, dz=dz, dc=dc, dg=dg, dx_lat=dx_lat, dlogit=dlogit,
                 topk_idx=sel, gates=gates, c=c, z=z)
+
+
+# ----------------------------------------------------------------------------------------
+# MXFP4 weights  ([SLMoE] 训练基础设施: MXFP4 weights, from quantisation-aware training on).
+# The pages name the format only; this is the OCP Microscaling (MX) block format restated
+# from its definition: blocks of 32 consecutive values along K share one power-of-two scale
+# X = 2^e, stored as an E8M0 byte (e + 127); each value is an FP4 E2M1 number (sign bit,
+# two exponent bits with bias 1, one mantissa bit), so magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+# Conversion of a block: e = floor(log2(max |v|)) - 2 (2 = the largest E2M1 exponent),
+# clamped to [-127, 127] (-127 for an all-zero block); each v / X goes to the nearest E2M1
+# magnitude, ties to the even mantissa, values past 6 to 6 (saturation); the sign bit is
+# set for v < 0.  Packing: two codes per byte, the lower-indexed value in the low nibble.
+# ----------------------------------------------------------------------------------------
+
+MX_BLOCK = 32
+E2M1_MAGNITUDES = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def mxfp4_quantize(W):
+    """(packed uint8 [..., K/2], scales uint8 [..., K/32]) of W [..., K] (K a multiple of 32)."""
+    w = f64(W)
+    K = w.shape[-1]
+    blocks = w.reshape(w.shape[:-1] + (K // MX_BLOCK, MX_BLOCK))
+    amax = np.max(np.abs(blocks), axis=-1)
+    e = np.full(amax.shape, -127, dtype=np.int64)
+    nz = amax > 0
+    e[nz] = np.floor(np.log2(amax[nz])).astype(np.int64) - 2
+    e = np.clip(e, -127, 127)
+    scaled = blocks / np.ldexp(1.0, e)[..., None]
+    mag = np.abs(scaled)
+    # nearest magnitude; on a tie the even index (mantissa bit 0) wins
+    dist = np.abs(mag[..., None] - E2M1_MAGNITUDES)
+    best = dist.min(axis=-1, keepdims=True)
+    cand = dist == best
+    even = cand & (np.arange(8) % 2 == 0)
+    idx = np.where(even.any(axis=-1), np.argmax(even, axis=-1), np.argmax(cand, axis=-1))
+    codes = (idx | np.where(scaled < 0, 8, 0)).astype(np.uint8)
+    codes = codes.reshape(w.shape)
+    packed = (codes[..., 0::2] | (codes[..., 1::2] << 4)).astype(np.uint8)
+    return packed, (e + 127).astype(np.uint8)
+
+
+def mxfp4_dequantize(packed, scales):
+    """The values [..., K] (fp64) that MXFP4 codes and their block scales stand for."""
+    p = np.asarray(packed, dtype=np.uint8)
+    codes = np.empty(p.shape[:-1] + (2 * p.shape[-1],), dtype=np.uint8)
+    codes[..., 0::2] = p & 15
+    codes[..., 1::2] = p >> 4
+    mag = E2M1_MAGNITUDES[codes & 7]
+    val = np.where(codes & 8, -mag, mag)
+    X = np.ldexp(1.0, np.asarray(scales, dtype=np.int64) - 127)
+    K = codes.shape[-1]
+    return (val.reshape(codes.shape[:-1] + (K // MX_BLOCK, MX_BLOCK)) * X[..., None]).reshape(codes.shape)
