@@ -61,6 +61,13 @@ extern "C" {
 
 #define SLMOE_F32  0             /* x, projection weights and intermediates in fp32      */
 #define SLMOE_BF16 1             /* the same in bf16 (fp32 accumulation, fp32 router)    */
+/* SLMOE_BF16 with the routed experts' weights W13 and W2 in MXFP4 ([SLMoE] 训练基础设施:
+ * MXFP4 weights; see slmoe_mxfp4_quantize for the format): W13 / W2 then point to packed
+ * codes [E, 2I, d_latent/2] / [E, d_latent, I/2] (bytes) with block scales W13_scale
+ * [E, 2I, d_latent/32] / W2_scale [E, d_latent, I/32].  The routed experts compute in f16
+ * (x_lat and h are kept in f16; each weight tile is dequantised on chip, exactly for block
+ * scales in [2^-23, 2^13]); everything else is as SLMOE_BF16. */
+#define SLMOE_MXFP4 2
 
 /* Shape and constants of one layer.  beta1 / beta2 are the SiTU and soft-cap constants
  * ([K3-arch] SiTU激活优化: 4 and 25), eps the RMSNorm epsilon, nbins the QB histogram
@@ -95,6 +102,8 @@ typedef struct slmoe_weights {
     const void  *W_out;  /* [d, d_latent]             act  latent up-proj       */
     const void  *W13_s;  /* [n_shared, 2I_shared, d]  act  shared gate|up       */
     const void  *W2_s;   /* [n_shared, d, I_shared]   act  shared down          */
+    const uint8_t *W13_scale;  /* SLMOE_MXFP4 only: [E, 2I, d_latent/32] E8M0    */
+    const uint8_t *W2_scale;   /* SLMOE_MXFP4 only: [E, d_latent, I/32]   E8M0    */
 } slmoe_weights;
 
 /* Byte offsets of the intermediates inside the workspace, so that a caller can read a
@@ -245,6 +254,21 @@ SLMOE_API int slmoe_topk(const float *scores, const float *bias, int32_t T, int3
  * SLMOE_ECUDA on a launch failure.
  */
 SLMOE_API int slmoe_wait_abort_check(int32_t *status, uint64_t wait_limit_ns, void *stream);
+
+/*
+ * slmoe_mxfp4_quantize - bf16 weights to MXFP4 ([SLMoE] 训练基础设施: MXFP4 weights; the
+ *   format is the OCP Microscaling one).  W [rows, K] bf16, K a multiple of 32.  Each block of
+ *   32 consecutive values of a row shares the scale 2^e with e = floor(log2 max|v|) - 2,
+ *   clamped to [-127, 127] (-127 for an all-zero block), stored as the byte e + 127 in
+ *   scales [rows, K/32]; each value becomes the FP4 E2M1 code (sign, 2 exponent bits with
+ *   bias 1, 1 mantissa bit: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6) nearest to v / 2^e, ties to
+ *   the even mantissa, saturating at 6, sign bit for v < 0; two codes per byte in
+ *   packed [rows, K/2], the lower-indexed value in the low nibble.  W 16-byte aligned.
+ *   Errors: SLMOE_EINVAL on null or misaligned pointers, rows < 0, K not a positive multiple
+ *   of 32.
+ */
+SLMOE_API int slmoe_mxfp4_quantize(const void *W, int64_t rows, int32_t K, uint8_t *packed, uint8_t *scales,
+                                   void *stream);
 
 /*
  * slmoe_qb_histogram - add per-expert score histograms of one micro-batch.

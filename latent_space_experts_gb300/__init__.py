@@ -14,14 +14,14 @@ from . import _build
 
 __all__ = ["SlmoeError", "Config", "Weights", "WorkspaceLayout", "load", "build", "config",
            "weights", "slmoe_workspace_size", "slmoe_workspace_layout_get", "slmoe_route",
-           "slmoe_route_noalloc", "slmoe_topk", "slmoe_topk_workspace_size", "slmoe_wait_abort_check",
+           "slmoe_route_noalloc", "slmoe_topk", "slmoe_mxfp4_quantize", "slmoe_topk_workspace_size", "slmoe_wait_abort_check",
            "slmoe_qb_histogram", "slmoe_qb_update", "slmoe_signsgd_update",
            "slmoe_forward", "slmoe_backward", "slmoe_backward_workspace_size", "slmoe_backward_layout_get",
            "backward_views", "Grads", "grads",
            "slmoe_device_sm_count", "workspace_views", "slmoe_last_error",
-           "slmoe_set_stage_events", "slmoe_launch_count", "F32", "BF16", "LIB_PATH"]
+           "slmoe_set_stage_events", "slmoe_launch_count", "F32", "BF16", "MXFP4", "LIB_PATH"]
 
-F32, BF16 = 0, 1
+F32, BF16, MXFP4 = 0, 1, 2
 LIB_PATH = _build.LIB
 
 
@@ -41,7 +41,7 @@ class Config(ctypes.Structure):
 
 class Weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
-                ("W_r", "W_in", "W13", "W2", "gamma", "W_out", "W13_s", "W2_s")]
+                ("W_r", "W_in", "W13", "W2", "gamma", "W_out", "W13_s", "W2_s", "W13_scale", "W2_scale")]
 
 
 class Grads(ctypes.Structure):
@@ -86,6 +86,7 @@ def load():
         "slmoe_topk_workspace_size": (SZ, [I32, I32, I32]),
         "slmoe_topk": (ctypes.c_int, [P, P, I32, I32, I32, P, P, P, P, P, P, P, P, SZ, P]),
         "slmoe_wait_abort_check": (ctypes.c_int, [P, ctypes.c_uint64, P]),
+        "slmoe_mxfp4_quantize": (ctypes.c_int, [P, I64, I32, P, P, P]),
         "slmoe_qb_histogram": (ctypes.c_int, [P, I64, I32, I32, P, P, P]),
         "slmoe_qb_update": (ctypes.c_int, [P, I32, I32, I32, P, P, P]),
         "slmoe_signsgd_update": (ctypes.c_int, [P, I32, ctypes.c_float, P, P]),
@@ -125,17 +126,21 @@ def _check(rc):
         raise SlmoeError(rc, load().slmoe_last_error().decode())
 
 
-def config(shape, T=None) -> Config:
-    """A Config from a ``synthetic.LayerShape``-like object (T overridable)."""
+def config(shape, T=None, dtype=None) -> Config:
+    """A Config from a ``synthetic.LayerShape``-like object (T and the layer type overridable)."""
+    if dtype is None:
+        dtype = BF16 if shape.dtype == "bf16" else F32
     return Config(T=shape.T if T is None else T, d=shape.d, d_latent=shape.d_latent, E=shape.E,
                   k=shape.k, I=shape.I, n_shared=shape.n_shared, I_shared=shape.I_shared,
                   nbins=shape.nbins, beta1=shape.beta1, beta2=shape.beta2, eps=shape.eps,
-                  dtype=BF16 if shape.dtype == "bf16" else F32)
+                  dtype=dtype)
 
 
 def weights(inp: dict) -> Weights:
-    return Weights(*[_ptr(inp[n]) for n in ("W_r", "W_in", "W13", "W2", "gamma", "W_out",
-                                             "W13_s", "W2_s")])
+    """A Weights struct from a dict of CUDA tensors; for the MXFP4 layer type the dict holds the
+    packed codes as W13 / W2 and their scales as W13_scale / W2_scale."""
+    return Weights(*[_ptr(inp.get(n)) for n in ("W_r", "W_in", "W13", "W2", "gamma", "W_out",
+                                                 "W13_s", "W2_s", "W13_scale", "W2_scale")])
 
 
 def grads(g: dict) -> Grads:
@@ -243,6 +248,10 @@ def slmoe_topk(scores, bias, T, E, k, topk_idx, topk_w, counts, offsets, perm, s
                              _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(slot_pos), _ptr(status),
                              _ptr(workspace), workspace.numel() * workspace.element_size(),
                              _stream(stream)))
+
+
+def slmoe_mxfp4_quantize(W, rows, K, packed, scales, stream=None):
+    _check(load().slmoe_mxfp4_quantize(_ptr(W), rows, K, _ptr(packed), _ptr(scales), _stream(stream)))
 
 
 def slmoe_wait_abort_check(status, wait_limit_ns, stream=None):

@@ -50,15 +50,15 @@ static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 int validate_config(const slmoe_config *c) {
     if (!c) return fail(SLMOE_EINVAL, "config is NULL");
-    if (c->dtype != SLMOE_F32 && c->dtype != SLMOE_BF16)
-        return fail(SLMOE_EINVAL, "dtype %d is neither SLMOE_F32 nor SLMOE_BF16", c->dtype);
+    if (c->dtype != SLMOE_F32 && c->dtype != SLMOE_BF16 && c->dtype != SLMOE_MXFP4)
+        return fail(SLMOE_EINVAL, "dtype %d is not SLMOE_F32, SLMOE_BF16 or SLMOE_MXFP4", c->dtype);
     if (c->T < 0) return fail(SLMOE_EINVAL, "T = %d < 0", c->T);
     if (c->E < 1 || c->E > 4096) return fail(SLMOE_EINVAL, "E = %d outside [1, 4096]", c->E);
     if (c->k < 1 || c->k > c->E || c->k > 32)
         return fail(SLMOE_EINVAL, "k = %d outside [1, min(E, 32)]", c->k);
     if (c->nbins < 1 || c->nbins > 1024) return fail(SLMOE_EINVAL, "nbins = %d outside [1, 1024]", c->nbins);
     if (c->n_shared < 0 || c->n_shared > 3) return fail(SLMOE_EINVAL, "n_shared = %d outside [0, 3]", c->n_shared);
-    const int m = c->dtype == SLMOE_BF16 ? 64 : 8;
+    const int m = c->dtype != SLMOE_F32 ? 64 : 8;
     if (c->d < m || c->d % m) return fail(SLMOE_EINVAL, "d = %d is not a positive multiple of %d", c->d, m);
     if (c->d_latent < m || c->d_latent % m)
         return fail(SLMOE_EINVAL, "d_latent = %d is not a positive multiple of %d", c->d_latent, m);
@@ -75,7 +75,7 @@ int validate_config(const slmoe_config *c) {
 int make_layout(const slmoe_config *c, Layout *L) {
     int rc = validate_config(c);
     if (rc) return rc;
-    const size_t T = c->T, E = c->E, k = c->k, es = c->dtype == SLMOE_BF16 ? 2 : 4;
+    const size_t T = c->T, E = c->E, k = c->k, es = c->dtype != SLMOE_F32 ? 2 : 4;
     const size_t nchunks = (T + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -99,9 +99,9 @@ int make_layout(const slmoe_config *c, Layout *L) {
     L->pub.z = take(T * c->d_latent * es);
     L->pub.h_s = take(T * (size_t)c->n_shared * c->I_shared * es);
     L->pub.status = take(16);
-    L->wr_split = c->dtype == SLMOE_BF16 ? take(3 * E * c->d * 2) : 0;
+    L->wr_split = c->dtype != SLMOE_F32 ? take(3 * E * c->d * 2) : 0;
     L->counters = take(16 * 4);
-    if (c->dtype == SLMOE_BF16) {
+    if (c->dtype != SLMOE_F32) {
         // work items: nfb feature blocks x (one pass per expert + one per full pass of tokens)
         const size_t Tk = T * k;
         const size_t nfb1 = (c->I + 127) / 128, nfb2 = (c->d_latent + 255) / 256;
@@ -109,7 +109,7 @@ int make_layout(const slmoe_config *c, Layout *L) {
         L->items1 = take(nfb1 * (E + (Tk + GROUPED_PASS - 1) / GROUPED_PASS) * 16);
         L->items2 = take(nfb2 * (E + (Tk + GROUPED_PASS - 1) / GROUPED_PASS) * 16);
     }
-    if (c->dtype == SLMOE_BF16 && T <= (size_t)ROUTER_SPLITK_MAX_M)
+    if (c->dtype != SLMOE_F32 && T <= (size_t)ROUTER_SPLITK_MAX_M)
         L->rt_split = take(ROUTER_SPLITK_MAX * T * E * 4);
     L->pub.total = off;
     return SLMOE_OK;
@@ -169,7 +169,7 @@ static int route_impl(const slmoe_config *c, const Layout &L, char *ws, const vo
                       const float *W_r, const float *bias, const float *mu, const Routing &R,
                       uint32_t *hist, int32_t *status, cudaStream_t st) {
     int rc;
-    if (c->dtype == SLMOE_BF16) {
+    if (c->dtype != SLMOE_F32) {
         rc = tc_router_scores(c, x, W_r, mu, reinterpret_cast<__nv_bfloat16 *>(ws + L.wr_split),
                               R.scores, status, R.counters,
                               L.rt_split ? reinterpret_cast<float *>(ws + L.rt_split) : nullptr, st);
@@ -416,6 +416,15 @@ int slmoe_topk(const float *scores, const float *bias, int32_t T, int32_t E, int
     return launch_scatter(topk_idx, chunk_counts, counts, T, E, k, offsets, perm, slot_pos, st);
 }
 
+int slmoe_mxfp4_quantize(const void *W, int64_t rows, int32_t K, uint8_t *packed, uint8_t *scales, void *stream) {
+    g_err[0] = 0;
+    if (rows < 0 || K <= 0 || K % 32) return fail(SLMOE_EINVAL, "rows >= 0 and K a positive multiple of 32 required");
+    if (rows == 0) return SLMOE_OK;
+    REQ(W, "W"); REQ(packed, "packed");
+    if (!scales) return fail(SLMOE_EINVAL, "scales is NULL");
+    return launch_mxfp4_quantize(W, rows, K, packed, scales, static_cast<cudaStream_t>(stream));
+}
+
 int slmoe_wait_abort_check(int32_t *status, uint64_t wait_limit_ns, void *stream) {
     g_err[0] = 0;
     REQ(status, "status");
@@ -510,6 +519,7 @@ int slmoe_forward(const slmoe_config *cfg, const void *x, const slmoe_weights *w
     REQ(w->W_r, "W_r"); REQ(w->W_in, "W_in"); REQ(w->W13, "W13"); REQ(w->W2, "W2");
     REQ(w->gamma, "gamma"); REQ(w->W_out, "W_out");
     if (cfg->n_shared > 0) { REQ(w->W13_s, "W13_s"); REQ(w->W2_s, "W2_s"); }
+    if (cfg->dtype == SLMOE_MXFP4) { REQ(w->W13_scale, "W13_scale"); REQ(w->W2_scale, "W2_scale"); }
     OPT(topk_idx_out, "topk_idx_out"); OPT(hist, "hist"); OPT(status, "status");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     char *ws = static_cast<char *>(workspace);
@@ -659,12 +669,12 @@ static RouteScratch route_scratch_layout(const slmoe_config *c, size_t nchunks, 
     };
     s.counters = take(16 * sizeof(int));
     s.chunk_counts = take(nchunks * (size_t)c->E * 4);
-    s.wr_split = c->dtype == SLMOE_BF16 ? take((size_t)3 * c->E * c->d * 2) : 0;
+    s.wr_split = c->dtype != SLMOE_F32 ? take((size_t)3 * c->E * c->d * 2) : 0;
     s.scores = own_scores ? take((size_t)c->T * c->E * 4) : 0;
     s.total = off;
     // the split-K router sums of a small bf16 batch, as in the workspace layout, when they fit
     // (else the router runs unsplit, its fp32 logit sums added in another order)
-    if (c->dtype == SLMOE_BF16 && c->T <= ROUTER_SPLITK_MAX_M) {
+    if (c->dtype != SLMOE_F32 && c->T <= ROUTER_SPLITK_MAX_M) {
         const size_t at = take((size_t)ROUTER_SPLITK_MAX * c->T * c->E * 4);
         if (off <= (size_t)SLMOE_ROUTE_NOALLOC_SCRATCH_BYTES) {
             s.rt_split = at;

@@ -90,6 +90,9 @@ int launch_combine_rmsnorm(int dtype, const void *y_e, const float *topk_w,
                            const int32_t *slot_pos, const float *gamma, int T, int d_latent,
                            int k, float eps, void *z, cudaStream_t st);
 
+// ---------------------------------------------------------------- MXFP4 weights
+int launch_mxfp4_quantize(const void *W, long long rows, int K, uint8_t *packed, uint8_t *scales, cudaStream_t st);
+
 // ---------------------------------------------------------------- backward (bf16 type)
 // Intermediates of a forward call that the backward reads (views into its workspace).
 struct FwdSaved {

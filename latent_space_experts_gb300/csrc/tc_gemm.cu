@@ -32,6 +32,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cuda_fp16.h>
+
 #include <cstring>
 
 #include "common.cuh"
@@ -77,6 +79,8 @@ constexpr int EPI_BF16 = 0, EPI_GLU = 1, EPI_F32 = 3;
 // Backward epilogues: dense SiTU-GLU derivative (rows = tokens); grouped (rows = features):
 // fp32 gate|up pre-activations, fp32 transposed store, SiTU-GLU derivative.
 constexpr int EPI_DGLU = 4, EPI_GU32 = 5, EPI_F32T = 6, EPI_DGLU_T = 7;
+// f16 store (the MXFP4 layer's latent activations).
+constexpr int EPI_F16 = 8;
 // Operand majorness of the dense kernel (template MAJ): bit 0 = A MN-major, bit 1 = B MN-major.
 // An MN-major operand is stored [K rows, M (or N) columns]; TMA loads it in 64 x 64 boxes.
 constexpr int A_MN = 1, B_MN = 2;
@@ -327,7 +331,30 @@ __global__ void __launch_bounds__(DenseCfg<BN, EPI, PACC>::THREADS, 1) dense_ker
             const int n0 = tn * Cfg::BN_OUT;
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + sub * Cfg::ACC;
             const bool row_ok = row < a.M;
-            if (EPI == EPI_BF16) {
+            if (EPI == EPI_F16) {
+                __half *C = static_cast<__half *>(a.C) + (long long)row * a.ldc;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 16) {
+                    uint32_t r[16];
+                    TMEM_LD16(tb + c, r);
+                    tmem_wait_ld();
+                    const int n = n0 + c;
+                    if (row_ok) {
+                        if (n + 16 <= a.N) {
+                            uint32_t w[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                __half2 hv = __floats2half2_rn(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                                w[i] = *reinterpret_cast<uint32_t *>(&hv);
+                            }
+                            *reinterpret_cast<uint4 *>(C + n) = make_uint4(w[0], w[1], w[2], w[3]);
+                            *reinterpret_cast<uint4 *>(C + n + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+                        } else {
+                            for (int i = 0; i < 16 && n + i < a.N; ++i) C[n + i] = __float2half_rn(__uint_as_float(r[i]));
+                        }
+                    }
+                }
+            } else if (EPI == EPI_BF16) {
                 __nv_bfloat16 *C = static_cast<__nv_bfloat16 *>(a.C) + (long long)row * a.ldc;
 #pragma unroll 1
                 for (int c = 0; c < BN; c += 16) {
@@ -706,12 +733,18 @@ done:
 constexpr int G_GATHER_THREADS = 128;
 constexpr int G_TQ = 4;                           // item queue slots
 
-template <bool DBUF>
+// FP4: the weights arrive as packed MXFP4 (32 bytes per row per 64-wide K block) through a
+// 4-deep ring of their own; four dequantising warps turn each stage into the f16 tile the MMA
+// reads (the ring of f16 tiles then needs only 3 stages: it hides the dequantisation, not HBM).
+template <bool DBUF, bool FP4 = false>
 struct GCfg {
     static constexpr int NSUB = 2;
     static constexpr int PASS = DBUF ? 128 : GROUPED_PASS;   // tokens per pass
     static constexpr int A_BYTES = NSUB * 128 * 128;
-    static constexpr int A_STAGES = DBUF ? 5 : 4;         // 160 KB / 128 KB of weights in flight
+    static constexpr int A_STAGES = FP4 ? 3 : (DBUF ? 5 : 4);  // 160 KB / 128 KB of weights in flight
+    static constexpr int RAW_BYTES = NSUB * 128 * 32;
+    static constexpr int RAW_STAGES = FP4 ? 4 : 0;
+    static constexpr int DQ_WARPS = FP4 ? 4 : 0;
     static constexpr int B_BYTES = PASS * 128;
     static constexpr int B_STAGES = 4;
     static constexpr int NBUF = DBUF ? 2 : 1;
@@ -720,8 +753,10 @@ struct GCfg {
     // drains, so it gets two warps per TMEM lane quadrant; the double-buffered one overlaps
     static constexpr int EPI_WARPS = DBUF ? 4 : 8;
     static constexpr int GATHER_WARP0 = 2 + EPI_WARPS;
-    static constexpr int THREADS = (2 + EPI_WARPS + 4) * 32;   // TMA, MMA, epilogue, 4 gather warps
-    static constexpr int SMEM = A_STAGES * A_BYTES + B_STAGES * B_BYTES + 1024 + 512;
+    static constexpr int DQ_WARP0 = GATHER_WARP0 + 4;
+    // TMA, MMA, epilogue, 4 gather warps (+ 4 dequantising warps)
+    static constexpr int THREADS = (2 + EPI_WARPS + 4 + DQ_WARPS) * 32;
+    static constexpr int SMEM = A_STAGES * A_BYTES + B_STAGES * B_BYTES + RAW_STAGES * RAW_BYTES + 1024 + 512;
     static_assert(SMEM <= 232448, "shared memory");
 };
 
@@ -747,6 +782,8 @@ struct GroupedArgs {
     long long ld_gu;
     __nv_bfloat16 *dgu;   // EPI_DGLU_T: [dg | du] out, bf16 [rows, 2F]
     long long ld_dgu;
+    const uint8_t *a_scales;   // FP4: E8M0 block scales of the weight rows, a_scale_ld bytes per row
+    int a_scale_ld;
 };
 
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *map, uint64_t *bar,
@@ -832,16 +869,45 @@ worklist_kernel(const int32_t *__restrict__ counts, const int32_t *__restrict__ 
 // weight in the backward): each 128-feature sub-tile is two 64 x 64 TMA boxes; a_rows_pe is then
 // the K rows per expert, a_fb_stride the features per block and a_sub1 the second sub-tile's
 // feature offset.
-template <int EPI, bool DBUF, bool AMN = false>
-__global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const __grid_constant__ CUtensorMap wmap,
-                                                               const GroupedArgs a) {
-    using Cfg = GCfg<DBUF>;
+// f16 bits of 2^e: normal for e >= -14, subnormal down to 2^-24, 0 below, infinity above 15.
+__device__ __forceinline__ uint32_t f16_pow2(int e) {
+    if (e > 15) return 0x7C00u;
+    if (e >= -14) return (uint32_t)(e + 15) << 10;
+    if (e >= -24) return 1u << (e + 24);
+    return 0u;
+}
+// Four FP4 E2M1 codes (one per byte nibble pair: 8 codes in a word) -> 8 f16 scaled by s (f16x2).
+__device__ __forceinline__ uint4 dequant8(uint32_t w, uint32_t s2) {
+    uint32_t h[4];
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(h[i]) : "r"(s2));
+    return make_uint4(h[0], h[1], h[2], h[3]);
+}
+// Instruction descriptor, kind::f16 with f16 A and B (K-major), fp32 D, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+template <int EPI, bool DBUF, bool AMN = false, bool FP4 = false>
+__global__ void __launch_bounds__(GCfg<DBUF, FP4>::THREADS, 1) grouped_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                                    const GroupedArgs a) {
+    using Cfg = GCfg<DBUF, FP4>;
     constexpr int AST = Cfg::A_STAGES, BST = Cfg::B_STAGES, NBUF = Cfg::NBUF, SUB1 = Cfg::SUB1_COL;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;
     uint8_t *sB = smem + AST * Cfg::A_BYTES;
-    int4 *q_items = reinterpret_cast<int4 *>(sB + BST * Cfg::B_BYTES);
+    uint8_t *sRaw = sB + BST * Cfg::B_BYTES;
+    int4 *q_items = reinterpret_cast<int4 *>(sRaw + Cfg::RAW_STAGES * Cfg::RAW_BYTES);
+    constexpr int RST = Cfg::RAW_STAGES > 0 ? Cfg::RAW_STAGES : 1;
     uint64_t *q_full = reinterpret_cast<uint64_t *>(q_items + G_TQ);
     uint64_t *q_empty = q_full + G_TQ;
     uint64_t *a_full = q_empty + G_TQ;
@@ -851,7 +917,9 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
     uint64_t *tfull = b_empty + BST;
     uint64_t *tempty = tfull + NBUF;
     uint64_t *mma_drain = tempty + NBUF;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_drain + 1);
+    uint64_t *raw_full = mma_drain + 1;        // FP4 only
+    uint64_t *raw_empty = raw_full + RST;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(raw_empty + RST);
     volatile WaitCtl *abort_flag = reinterpret_cast<volatile WaitCtl *>(tmem_slot + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -862,11 +930,16 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
         mbar_init(mma_drain, 1);
         for (int s = 0; s < G_TQ; ++s) {
             mbar_init(&q_full[s], 1);
-            mbar_init(&q_empty[s], 1 + Cfg::EPI_WARPS + 4);  // MMA thread, epilogue and gather warps
+            // MMA thread, epilogue, gather (and dequantising) warps
+            mbar_init(&q_empty[s], 1 + Cfg::EPI_WARPS + 4 + Cfg::DQ_WARPS);
         }
         for (int s = 0; s < AST; ++s) {
-            mbar_init(&a_full[s], 1);
+            mbar_init(&a_full[s], FP4 ? Cfg::DQ_WARPS : 1);
             mbar_init(&a_empty[s], 1);
+        }
+        for (int s = 0; s < Cfg::RAW_STAGES; ++s) {
+            mbar_init(&raw_full[s], 1);
+            mbar_init(&raw_empty[s], Cfg::DQ_WARPS);
         }
         for (int s = 0; s < BST; ++s) {
             mbar_init(&b_full[s], G_GATHER_THREADS);
@@ -918,6 +991,17 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
             const int fb = it.y & 0xffff;
             const bool multi = (it.y >> 16) != 0;
             const int row0 = it.x * a.a_rows_pe + fb * a.a_fb_stride;
+            if (FP4) {             // packed MXFP4 rows into the raw ring (32 bytes per row and K block)
+                for (int kb = 0; kb < a.kblocks; ++kb) {
+                    if (!mbar_wait(&raw_empty[stage], phase ^ 1, abort_flag)) goto done;
+                    mbar_expect_tx(&raw_full[stage], Cfg::RAW_BYTES);
+                    const uint32_t sr = su32(sRaw + stage * Cfg::RAW_BYTES);
+                    tma_load_2d_hint(sr, &wmap, &raw_full[stage], kb * 32, row0, pol_first);
+                    tma_load_2d_hint(sr + 128 * 32, &wmap, &raw_full[stage], kb * 32, row0 + a.a_sub1, pol_first);
+                    if (++stage == Cfg::RAW_STAGES) { stage = 0; phase ^= 1; p_wrapped = true; }
+                }
+                continue;
+            }
             for (int kb = 0; kb < a.kblocks; ++kb) {
                 if (!mbar_wait(&a_empty[stage], phase ^ 1, abort_flag)) goto done;
                 mbar_expect_tx(&a_full[stage], Cfg::A_BYTES);
@@ -948,7 +1032,8 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
             int4 it;
             if (!pop(qs, qp, it, false)) goto done;
             if (it.w < 0) break;
-            const uint32_t idesc = idesc_bf16(128, (it.w + 15) & ~15) | (AMN ? (1u << 15) : 0u);
+            const uint32_t idesc = (FP4 ? idesc_f16(128, (it.w + 15) & ~15) : idesc_bf16(128, (it.w + 15) & ~15)) |
+                                   (AMN ? (1u << 15) : 0u);
             if (!mbar_wait(&tempty[buf], tph ^ 1, abort_flag)) goto done;
             tc_after();
             const uint32_t d = tmem_base + buf * 256;
@@ -1005,17 +1090,22 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
             const bool ok1 = GU_LAYOUT ? ok : f + 128 < a.out_cols;
             for (int c = half * 16; c < Np; c += 16 * WPQ) {
                 if (EPI == EPI_GLU) {
-                    __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.out) + (long long)it.z * a.out_ld + f;
                     uint32_t g[16], v[16];
                     TMEM_LD16(tb + c, g);
                     TMEM_LD16(tb + SUB1 + c, v);
                     tmem_wait_ld();
                     if (ok) {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            if (c + j < N)
-                                o[(long long)(c + j) * a.out_ld] = __float2bfloat16_rn(situ_glu_fast(
-                                    __uint_as_float(g[j]), __uint_as_float(v[j]), ib1, a.beta1, ib2, a.beta2));
+                        for (int j = 0; j < 16; ++j) {
+                            if (c + j >= N) continue;
+                            const float hv = situ_glu_fast(__uint_as_float(g[j]), __uint_as_float(v[j]), ib1, a.beta1,
+                                                           ib2, a.beta2);
+                            const long long at = ((long long)it.z + c + j) * a.out_ld + f;
+                            if (FP4)   // the MXFP4 layer keeps the routed experts' activations in f16
+                                static_cast<__half *>(a.out)[at] = __float2half_rn(hv);
+                            else
+                                static_cast<__nv_bfloat16 *>(a.out)[at] = __float2bfloat16_rn(hv);
+                        }
                     }
                 } else {
                     uint32_t r0[16], r1[16];
@@ -1064,6 +1154,69 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[buf]);
             if (++buf == NBUF) { buf = 0; tph ^= 1; }
+        }
+    } else if (FP4 && warp >= Cfg::DQ_WARP0) {
+        // ------------------------------------------------ MXFP4 -> f16 (4 warps): thread t turns
+        // row t of both 128-row sub-tiles of a stage into the swizzled K-major f16 layout; the
+        // 16 block-scale bytes of 8 stages are loaded one group ahead
+        const int t = threadIdx.x - Cfg::DQ_WARP0 * 32;
+        int qs = 0, rs = 0, as = 0;
+        uint32_t qp = 0, rph = 0, aph = 0;
+        for (;;) {
+            int4 it;
+            if (!pop(qs, qp, it, true)) goto done;
+            if (it.w < 0) break;
+            const int fb = it.y & 0xffff;
+            const long long wrow0 = (long long)it.x * a.a_rows_pe + fb * a.a_fb_stride + t;
+            const uint8_t *sc0 = a.a_scales + wrow0 * a.a_scale_ld;
+            const uint8_t *sc1 = a.a_scales + (wrow0 + a.a_sub1) * a.a_scale_ld;
+            const int ngroups = (a.kblocks + 7) / 8;
+            uint4 cur0 = *reinterpret_cast<const uint4 *>(sc0), cur1 = *reinterpret_cast<const uint4 *>(sc1);
+            uint4 nxt0 = cur0, nxt1 = cur1;
+            if (ngroups > 1) {
+                nxt0 = *reinterpret_cast<const uint4 *>(sc0 + 16);
+                nxt1 = *reinterpret_cast<const uint4 *>(sc1 + 16);
+            }
+            for (int kb = 0; kb < a.kblocks; ++kb) {
+                if (kb > 0 && (kb & 7) == 0) {        // next group of 8 stages
+                    cur0 = nxt0;
+                    cur1 = nxt1;
+                    const int g = (kb >> 3) + 1;
+                    if (g < ngroups) {
+                        nxt0 = *reinterpret_cast<const uint4 *>(sc0 + 16 * g);
+                        nxt1 = *reinterpret_cast<const uint4 *>(sc1 + 16 * g);
+                    }
+                }
+                if (!mbar_wait(&raw_full[rs], rph, abort_flag)) goto done;
+                if (!mbar_wait(&a_empty[as], aph ^ 1, abort_flag)) goto done;
+                const uint8_t *raw = sRaw + rs * Cfg::RAW_BYTES;
+                uint8_t *dstA = sA + as * Cfg::A_BYTES;
+#pragma unroll
+                for (int sub = 0; sub < 2; ++sub) {
+                    const uint4 cs = sub ? cur1 : cur0;
+                    const uint32_t cw[4] = {cs.x, cs.y, cs.z, cs.w};
+                    const int pos = (kb & 7) * 2;             // this stage's two scale bytes
+                    const uint32_t e0 = (cw[pos >> 2] >> (8 * (pos & 3))) & 0xFF;
+                    const uint32_t e1 = (cw[(pos + 1) >> 2] >> (8 * ((pos + 1) & 3))) & 0xFF;
+                    const uint32_t s0 = f16_pow2((int)e0 - 127), s1 = f16_pow2((int)e1 - 127);
+                    const uint32_t s0x2 = s0 | (s0 << 16), s1x2 = s1 | (s1 << 16);
+                    const uint4 p0 = *reinterpret_cast<const uint4 *>(raw + sub * 128 * 32 + t * 32);
+                    const uint4 p1 = *reinterpret_cast<const uint4 *>(raw + sub * 128 * 32 + t * 32 + 16);
+                    const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+                    uint8_t *rowp = dstA + sub * 128 * 128 + (t >> 3) * 1024 + (t & 7) * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)   // chunk c = K values 8c .. 8c + 7
+                        *reinterpret_cast<uint4 *>(rowp + ((c ^ (t & 7)) << 4)) = dequant8(words[c], c < 4 ? s0x2 : s1x2);
+                }
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&raw_empty[rs]);
+                    mbar_arrive(&a_full[as]);
+                }
+                if (++rs == Cfg::RAW_STAGES) { rs = 0; rph ^= 1; }
+                if (++as == AST) { as = 0; aph ^= 1; }
+            }
         }
     } else if (warp >= Cfg::GATHER_WARP0) {
         // ------------------------------------------------ token-row gather (cp.async, kept in L2)
@@ -1115,7 +1268,8 @@ done:
     __syncthreads();
     if (abort_flag->abort) {   // every role has stopped: let copies and MMAs in flight finish
         if (warp == 0 && lane == 0) {
-            drain_ring(a_full, AST, p_stage, p_phase, p_wrapped);
+            if (FP4) drain_ring(raw_full, Cfg::RAW_STAGES, p_stage, p_phase, p_wrapped);
+            else drain_ring(a_full, AST, p_stage, p_phase, p_wrapped);
         }
         if (warp == 1 && lane == 0) {
             umma_commit(mma_drain);
@@ -1194,12 +1348,13 @@ int launch_dense_bn(int bn, const TmaPack &maps, const DenseArgs &a, cudaStream_
     return bn == 64 ? launch_dense<64, EPI, 1>(maps, a, st) : launch_dense<256, EPI, 1>(maps, a, st);
 }
 
-template <int EPI, bool DBUF, bool AMN = false>
+template <int EPI, bool DBUF, bool AMN = false, bool FP4 = false>
 int launch_grouped(const CUtensorMap &wmap, const GroupedArgs &a, cudaStream_t st) {
-    auto kern = grouped_kernel<EPI, DBUF, AMN>;
-    int rc = set_smem(kern, GCfg<DBUF>::SMEM);
+    using Cfg = GCfg<DBUF, FP4>;
+    auto kern = grouped_kernel<EPI, DBUF, AMN, FP4>;
+    int rc = set_smem(kern, Cfg::SMEM);
     if (rc) return rc;
-    kern<<<sm_count(), GCfg<DBUF>::THREADS, GCfg<DBUF>::SMEM, st>>>(wmap, a);
+    kern<<<sm_count(), Cfg::THREADS, Cfg::SMEM, st>>>(wmap, a);
     return check_launch("grouped_kernel");
 }
 
@@ -1294,7 +1449,9 @@ int tc_forward_front(const slmoe_config *c, const void *x, const slmoe_weights *
         DenseArgs a = {};
         a.M = T; a.N = dl; a.nseg = 1; a.kblocks[0] = (d + 63) / 64;
         a.C = f.x_lat; a.ldc = dl; a.status = f.status; a.counter = f.counters + 1;
-        if ((rc = launch_dense_bn<EPI_BF16>(bn, maps, a, st))) return rc;
+        if (c->dtype == SLMOE_MXFP4) rc = launch_dense_bn<EPI_F16>(bn, maps, a, st);
+        else rc = launch_dense_bn<EPI_BF16>(bn, maps, a, st);
+        if (rc) return rc;
     }
     stage_event(3, st);
     const int bn_s = dense_bn(T, Is, true);
@@ -1336,32 +1493,45 @@ int tc_forward_back(const slmoe_config *c, const slmoe_weights *w, const TcForwa
     using bf = __nv_bfloat16;
 
     (void)E;
+    const bool fp4 = c->dtype == SLMOE_MXFP4;
     {   // routed experts, gate|up + SiTU-GLU: h[perm row] = GLU(W13[e] x_lat[token])
         CUtensorMap wm;
-        if ((rc = make_map(&wm, w->W13, (long long)E * 2 * I, dl, dl, 128))) return rc;
+        if (fp4) rc = tmap_encode_2d(&wm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w->W13, (long long)E * 2 * I, dl / 2,
+                                     dl / 2, 32, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+        else rc = make_map(&wm, w->W13, (long long)E * 2 * I, dl, dl, 128);
+        if (rc) return rc;
         GroupedArgs a = {};
         a.kblocks = (dl + 63) / 64;
         a.a_rows_pe = 2 * I; a.a_sub1 = I; a.a_fb_stride = 128;
         a.items = f.items1; a.n_items = f.counters + 8; a.counter = f.counters + 6;
         a.b_index = f.perm;
         a.b_src = static_cast<const bf *>(f.x_lat); a.b_ld = dl; a.b_K = dl;
-        a.out = static_cast<bf *>(f.h); a.out_ld = I; a.out_cols = I;
+        a.out = f.h; a.out_ld = I; a.out_cols = I;
         a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
-        if ((rc = launch_grouped<EPI_GLU, false>(wm, a, st))) return rc;
+        a.a_scales = w->W13_scale; a.a_scale_ld = dl / 32;
+        if (fp4) rc = launch_grouped<EPI_GLU, false, false, true>(wm, a, st);
+        else rc = launch_grouped<EPI_GLU, false>(wm, a, st);
+        if (rc) return rc;
     }
     stage_event(4, st);
     {   // routed experts, down: y_e[row] = W2[e] h[row]
         CUtensorMap wm;
-        if ((rc = make_map(&wm, w->W2, (long long)E * dl, I, I, 128))) return rc;
+        if (fp4) rc = tmap_encode_2d(&wm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w->W2, (long long)E * dl, I / 2, I / 2,
+                                     32, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+        else rc = make_map(&wm, w->W2, (long long)E * dl, I, I, 128);
+        if (rc) return rc;
         GroupedArgs a = {};
         a.kblocks = (I + 63) / 64;
         a.a_rows_pe = dl; a.a_sub1 = 128; a.a_fb_stride = 256;
         a.items = f.items2; a.n_items = f.counters + 9; a.counter = f.counters + 7;
         a.b_index = nullptr;
         a.b_src = static_cast<const bf *>(f.h); a.b_ld = I; a.b_K = I;
-        a.out = static_cast<bf *>(f.y_e); a.out_ld = dl; a.out_cols = dl;
+        a.out = f.y_e; a.out_ld = dl; a.out_cols = dl;
         a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
-        if ((rc = launch_grouped<EPI_BF16, false>(wm, a, st))) return rc;
+        a.a_scales = w->W2_scale; a.a_scale_ld = I / 32;
+        if (fp4) rc = launch_grouped<EPI_BF16, false, false, true>(wm, a, st);
+        else rc = launch_grouped<EPI_BF16, false>(wm, a, st);
+        if (rc) return rc;
     }
     stage_event(5, st);
     (void)Tk;
