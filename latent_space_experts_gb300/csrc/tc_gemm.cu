@@ -784,6 +784,7 @@ struct GroupedArgs {
     long long ld_dgu;
     const uint8_t *a_scales;   // FP4: E8M0 block scales of the weight rows, a_scale_ld bytes per row
     int a_scale_ld;
+    long long a_rows_total;    // FP4: rows of the whole weight tensor (rows past it read scale 0)
 };
 
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *map, uint64_t *bar,
@@ -1157,8 +1158,9 @@ __global__ void __launch_bounds__(GCfg<DBUF, FP4>::THREADS, 1) grouped_kernel(co
         }
     } else if (FP4 && warp >= Cfg::DQ_WARP0) {
         // ------------------------------------------------ MXFP4 -> f16 (4 warps): thread t turns
-        // row t of both 128-row sub-tiles of a stage into the swizzled K-major f16 layout; the
-        // 16 block-scale bytes of 8 stages are loaded one group ahead
+        // row t of both 128-row sub-tiles of a stage into the swizzled K-major f16 layout.  A
+        // stage needs two scale bytes per row (2-byte aligned: a row holds K/32 bytes, K a
+        // multiple of 64); they are loaded 8 stages ahead through a register queue.
         const int t = threadIdx.x - Cfg::DQ_WARP0 * 32;
         int qs = 0, rs = 0, as = 0;
         uint32_t qp = 0, rph = 0, aph = 0;
@@ -1168,37 +1170,34 @@ __global__ void __launch_bounds__(GCfg<DBUF, FP4>::THREADS, 1) grouped_kernel(co
             if (it.w < 0) break;
             const int fb = it.y & 0xffff;
             const long long wrow0 = (long long)it.x * a.a_rows_pe + fb * a.a_fb_stride + t;
-            const uint8_t *sc0 = a.a_scales + wrow0 * a.a_scale_ld;
-            const uint8_t *sc1 = a.a_scales + (wrow0 + a.a_sub1) * a.a_scale_ld;
-            const int ngroups = (a.kblocks + 7) / 8;
-            uint4 cur0 = *reinterpret_cast<const uint4 *>(sc0), cur1 = *reinterpret_cast<const uint4 *>(sc1);
-            uint4 nxt0 = cur0, nxt1 = cur1;
-            if (ngroups > 1) {
-                nxt0 = *reinterpret_cast<const uint4 *>(sc0 + 16);
-                nxt1 = *reinterpret_cast<const uint4 *>(sc1 + 16);
+            const uint16_t *sc0 = reinterpret_cast<const uint16_t *>(a.a_scales + wrow0 * a.a_scale_ld);
+            const uint16_t *sc1 = reinterpret_cast<const uint16_t *>(a.a_scales + (wrow0 + a.a_sub1) * a.a_scale_ld);
+            // a feature block may run past the last expert's rows: TMA fills those weight rows
+            // with zeros, and their scales are not read
+            const bool in0 = wrow0 < a.a_rows_total, in1 = wrow0 + a.a_sub1 < a.a_rows_total;
+            uint32_t qa[8], qb[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                qa[i] = (in0 && i < a.kblocks) ? sc0[i] : 0u;
+                qb[i] = (in1 && i < a.kblocks) ? sc1[i] : 0u;
             }
             for (int kb = 0; kb < a.kblocks; ++kb) {
-                if (kb > 0 && (kb & 7) == 0) {        // next group of 8 stages
-                    cur0 = nxt0;
-                    cur1 = nxt1;
-                    const int g = (kb >> 3) + 1;
-                    if (g < ngroups) {
-                        nxt0 = *reinterpret_cast<const uint4 *>(sc0 + 16 * g);
-                        nxt1 = *reinterpret_cast<const uint4 *>(sc1 + 16 * g);
-                    }
+                const uint32_t cur0 = qa[0], cur1 = qb[0];
+#pragma unroll
+                for (int i = 0; i < 7; ++i) {
+                    qa[i] = qa[i + 1];
+                    qb[i] = qb[i + 1];
                 }
+                qa[7] = (in0 && kb + 8 < a.kblocks) ? sc0[kb + 8] : 0u;
+                qb[7] = (in1 && kb + 8 < a.kblocks) ? sc1[kb + 8] : 0u;
                 if (!mbar_wait(&raw_full[rs], rph, abort_flag)) goto done;
                 if (!mbar_wait(&a_empty[as], aph ^ 1, abort_flag)) goto done;
                 const uint8_t *raw = sRaw + rs * Cfg::RAW_BYTES;
                 uint8_t *dstA = sA + as * Cfg::A_BYTES;
 #pragma unroll
                 for (int sub = 0; sub < 2; ++sub) {
-                    const uint4 cs = sub ? cur1 : cur0;
-                    const uint32_t cw[4] = {cs.x, cs.y, cs.z, cs.w};
-                    const int pos = (kb & 7) * 2;             // this stage's two scale bytes
-                    const uint32_t e0 = (cw[pos >> 2] >> (8 * (pos & 3))) & 0xFF;
-                    const uint32_t e1 = (cw[(pos + 1) >> 2] >> (8 * ((pos + 1) & 3))) & 0xFF;
-                    const uint32_t s0 = f16_pow2((int)e0 - 127), s1 = f16_pow2((int)e1 - 127);
+                    const uint32_t cs = sub ? cur1 : cur0;     // bytes 2 kb (low) and 2 kb + 1
+                    const uint32_t s0 = f16_pow2((int)(cs & 0xFF) - 127), s1 = f16_pow2((int)(cs >> 8) - 127);
                     const uint32_t s0x2 = s0 | (s0 << 16), s1x2 = s1 | (s1 << 16);
                     const uint4 p0 = *reinterpret_cast<const uint4 *>(raw + sub * 128 * 32 + t * 32);
                     const uint4 p1 = *reinterpret_cast<const uint4 *>(raw + sub * 128 * 32 + t * 32 + 16);
@@ -1508,7 +1507,7 @@ int tc_forward_back(const slmoe_config *c, const slmoe_weights *w, const TcForwa
         a.b_src = static_cast<const bf *>(f.x_lat); a.b_ld = dl; a.b_K = dl;
         a.out = f.h; a.out_ld = I; a.out_cols = I;
         a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
-        a.a_scales = w->W13_scale; a.a_scale_ld = dl / 32;
+        a.a_scales = w->W13_scale; a.a_scale_ld = dl / 32; a.a_rows_total = (long long)E * 2 * I;
         if (fp4) rc = launch_grouped<EPI_GLU, false, false, true>(wm, a, st);
         else rc = launch_grouped<EPI_GLU, false>(wm, a, st);
         if (rc) return rc;
@@ -1528,7 +1527,7 @@ int tc_forward_back(const slmoe_config *c, const slmoe_weights *w, const TcForwa
         a.b_src = static_cast<const bf *>(f.h); a.b_ld = I; a.b_K = I;
         a.out = f.y_e; a.out_ld = dl; a.out_cols = dl;
         a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
-        a.a_scales = w->W2_scale; a.a_scale_ld = I / 32;
+        a.a_scales = w->W2_scale; a.a_scale_ld = I / 32; a.a_rows_total = (long long)E * dl;
         if (fp4) rc = launch_grouped<EPI_BF16, false, false, true>(wm, a, st);
         else rc = launch_grouped<EPI_BF16, false>(wm, a, st);
         if (rc) return rc;
