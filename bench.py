@@ -48,20 +48,23 @@ def peaks():
     return PEAKS_FALLBACK, "fallback"
 
 
-def work_model(shp, counts=None):
+def work_model(shp, counts=None, expert_weight_bytes=2.0):
     """FLOPs and bytes per stage of one step.  "bytes" are the algorithmic bytes the survey
     counts (weights touched, the layer's input x and its fp32 output y); "inter" are the
     intermediates a stage reads or writes (scores, x_lat, h, y_e, z, h_s), which a fused
-    design could avoid and which are reported separately."""
+    design could avoid and which are reported separately.  expert_weight_bytes: bytes per
+    routed-expert weight (2 for bf16; 17/32 for MXFP4: half a byte per code plus one scale
+    byte per 32)."""
+    wb = expert_weight_bytes
     T, d, dl, E, k, I, ns, Is = shp.T, shp.d, shp.d_latent, shp.E, shp.k, shp.I, shp.n_shared, shp.I_shared
     touched = E if counts is None else int((counts > 0).sum())
     st = {
         "router": dict(flops=2 * T * d * E, bytes=T * d * 2 + E * d * 4, inter=T * E * 4, bound="tensor"),
         "topk+permute+hist": dict(flops=0, bytes=0, inter=2 * T * E * 4 + T * k * 16, bound="hbm"),
         "down": dict(flops=2 * T * d * dl, bytes=T * d * 2 + dl * d * 2, inter=T * dl * 2, bound="tensor"),
-        "expert gate|up": dict(flops=2 * T * k * dl * 2 * I, bytes=touched * 2 * I * dl * 2,
+        "expert gate|up": dict(flops=2 * T * k * dl * 2 * I, bytes=int(touched * 2 * I * dl * wb),
                                inter=T * dl * 2 + T * k * I * 2, bound="hbm"),
-        "expert down": dict(flops=2 * T * k * I * dl, bytes=touched * dl * I * 2,
+        "expert down": dict(flops=2 * T * k * I * dl, bytes=int(touched * dl * I * wb),
                             inter=T * k * I * 2 + T * k * dl * 2, bound="hbm"),
         "combine+rmsnorm": dict(flops=0, bytes=0, inter=T * k * dl * 2 + T * dl * 2 + T * k * 8, bound="hbm"),
         "shared gate|up": dict(flops=2 * T * d * 2 * Is * ns, bytes=T * d * 2 + ns * 2 * Is * d * 2,
@@ -70,8 +73,8 @@ def work_model(shp, counts=None):
                                inter=T * dl * 2 + T * ns * Is * 2, bound="tensor"),
     }
     layer_flops = sum(v["flops"] for v in st.values())
-    layer_bytes = (E * d * 4 + dl * d * 2 + touched * 3 * I * dl * 2 + d * dl * 2 + ns * 3 * Is * d * 2
-                   + T * d * 2 + T * d * 4)
+    layer_bytes = int(E * d * 4 + dl * d * 2 + touched * 3 * I * dl * wb + d * dl * 2 + ns * 3 * Is * d * 2
+                      + T * d * 2 + T * d * 4)
     return st, layer_flops, layer_bytes
 
 
@@ -417,11 +420,12 @@ class LayerRun:
     """One layer configuration on the device: workspace, outputs, the step (slmoe_forward +
     slmoe_qb_update) and, unless disabled, a CUDA graph of that step."""
 
-    def __init__(self, shp, inp, x, mu, use_graph=True, warmup=3):
+    def __init__(self, shp, inp, x, mu, use_graph=True, warmup=3, dtype=None):
         import torch
         import latent_space_experts_gb300 as lse
         self.lse, self.shp, self.inp, self.x, self.mu = lse, shp, inp, x, mu
-        self.cfg = lse.config(shp)
+        self.cfg = lse.config(shp, dtype=dtype)
+        self.expert_weight_bytes = 17 / 32 if dtype == lse.MXFP4 else 2.0
         self.ws = torch.zeros(lse.slmoe_workspace_size(self.cfg), dtype=torch.uint8, device="cuda")
         self.y = torch.empty(shp.T, shp.d, dtype=torch.float32, device="cuda")
         self.hist = torch.zeros(shp.E, shp.nbins, dtype=torch.int32, device="cuda")
@@ -535,7 +539,7 @@ def backward_bench(run, pk, reps=5):
 
 def layer_summary(run, ms, pk, timed_s, reasons):
     """Tokens/s and the whole-layer roofline of one timed layer configuration."""
-    st_model, flops, nbytes = work_model(run.shp, run.counts())
+    st_model, flops, nbytes = work_model(run.shp, run.counts(), run.expert_weight_bytes)
     tc, tc_kind = tensor_peak(pk, timed_s, reasons)
     t_flops, t_bytes = flops / (tc * 1e12), nbytes / (pk["hbm_gbs"] * 1e9)
     t_layer = max(t_flops, t_bytes)
@@ -741,6 +745,24 @@ def main():
                 dms, _ = drun.timed(200)
                 extra[name] = layer_summary(drun, dms, pk, dms * 0.2, reasons)
                 del drun
+        if args.workload == "k3_prefill":
+            # the MXFP4 layer type: the same weights with the routed experts quantised once
+            mx = dict(inp)
+            for name in ("W13", "W2"):
+                W = inp[name]
+                K = W.shape[-1]
+                mx[name] = torch.empty(W.shape[:-1] + (K // 2,), dtype=torch.uint8, device="cuda")
+                mx[name + "_scale"] = torch.empty(W.shape[:-1] + (K // 32,), dtype=torch.uint8, device="cuda")
+                lse.slmoe_mxfp4_quantize(W, W.numel() // K, K, mx[name], mx[name + "_scale"])
+            for name, T in (("k3_decode_mxfp4", 128), ("k3_prefill_mxfp4", shp.T)):
+                s_mx = synthetic.shape_with(shp, T=T)
+                mrun = LayerRun(s_mx, mx, inp["x"][:T].contiguous(), inp["logit_offset"], dtype=lse.MXFP4)
+                mms, _ = mrun.timed(100)
+                extra[name] = layer_summary(mrun, mms, pk, mms * 0.1, reasons)
+                extra[name]["note"] = ("routed-expert weights MXFP4 (E2M1 + E8M0 per 32), dequantised on chip "
+                                       "into f16 tiles; latent activations f16; the rest as the bf16 layer")
+                del mrun
+            del mx
         mshp = synthetic.LAYERS["mid"]
         minp = synthetic.layer_inputs(mshp, seed=0, device="cuda")
         mrun = LayerRun(mshp, minp, minp["x"], minp["logit_offset"])
