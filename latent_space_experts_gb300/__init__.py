@@ -191,7 +191,8 @@ def workspace_views(cfg: Config, ws):
     """torch views of the intermediates inside a workspace tensor (uint8, on the device)."""
     import torch
     L = slmoe_workspace_layout_get(cfg)
-    act = torch.bfloat16 if cfg.dtype == BF16 else torch.float32
+    act = torch.float32 if cfg.dtype == F32 else torch.bfloat16
+    lat = torch.float16 if cfg.dtype == MXFP4 else act     # the MXFP4 type keeps x_lat and h in f16
     T, k, E = cfg.T, cfg.k, cfg.E
 
     def view(name, dtype, shape):
@@ -208,8 +209,8 @@ def workspace_views(cfg: Config, ws):
                 offsets=view("offsets", torch.int32, (E + 1,)),
                 perm=view("perm", torch.int32, (T * k,)),
                 slot_pos=view("slot_pos", torch.int32, (T, k)),
-                x_lat=view("x_lat", act, (T, cfg.d_latent)),
-                h=view("h", act, (T * k, cfg.I)),
+                x_lat=view("x_lat", lat, (T, cfg.d_latent)),
+                h=view("h", lat, (T * k, cfg.I)),
                 y_e=view("y_e", act, (T * k, cfg.d_latent)),
                 z=view("z", act, (T, cfg.d_latent)),
                 h_s=view("h_s", act, (T, cfg.n_shared * cfg.I_shared)),
