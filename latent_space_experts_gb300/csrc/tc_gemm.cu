@@ -733,17 +733,19 @@ done:
 constexpr int G_GATHER_THREADS = 128;
 constexpr int G_TQ = 4;                           // item queue slots
 
-// FP4: the weights arrive as packed MXFP4 (32 bytes per row per 64-wide K block) through a
-// 4-deep ring of their own; four dequantising warps turn each stage into the f16 tile the MMA
-// reads (the ring of f16 tiles then needs only 3 stages: it hides the dequantisation, not HBM).
+// FP4: the weights arrive as packed MXFP4 through a ring of their own, 128 bytes per row (four
+// 64-wide K blocks: whole L2 lines) per raw stage, in the 128-byte swizzle; four dequantising
+// warps turn each K block into the f16 tile the MMA reads (two f16 stages suffice: they hide
+// the dequantisation, the raw ring hides HBM).
 template <bool DBUF, bool FP4 = false>
 struct GCfg {
     static constexpr int NSUB = 2;
     static constexpr int PASS = DBUF ? 128 : GROUPED_PASS;   // tokens per pass
     static constexpr int A_BYTES = NSUB * 128 * 128;
-    static constexpr int A_STAGES = FP4 ? 3 : (DBUF ? 5 : 4);  // 160 KB / 128 KB of weights in flight
-    static constexpr int RAW_BYTES = NSUB * 128 * 32;
-    static constexpr int RAW_STAGES = FP4 ? 4 : 0;
+    static constexpr int A_STAGES = FP4 ? 2 : (DBUF ? 5 : 4);  // 160 KB / 128 KB of weights in flight
+    static constexpr int RAW_KB = 4;                        // K blocks per raw stage
+    static constexpr int RAW_BYTES = NSUB * 128 * 32 * RAW_KB;
+    static constexpr int RAW_STAGES = FP4 ? 2 : 0;
     static constexpr int DQ_WARPS = FP4 ? 4 : 0;
     static constexpr int B_BYTES = PASS * 128;
     static constexpr int B_STAGES = 4;
@@ -992,13 +994,15 @@ __global__ void __launch_bounds__(GCfg<DBUF, FP4>::THREADS, 1) grouped_kernel(co
             const int fb = it.y & 0xffff;
             const bool multi = (it.y >> 16) != 0;
             const int row0 = it.x * a.a_rows_pe + fb * a.a_fb_stride;
-            if (FP4) {             // packed MXFP4 rows into the raw ring (32 bytes per row and K block)
-                for (int kb = 0; kb < a.kblocks; ++kb) {
+            if (FP4) {             // packed MXFP4 rows into the raw ring, 128 bytes (4 K blocks) per row
+                const int ngroups = (a.kblocks + Cfg::RAW_KB - 1) / Cfg::RAW_KB;
+                for (int rg = 0; rg < ngroups; ++rg) {
                     if (!mbar_wait(&raw_empty[stage], phase ^ 1, abort_flag)) goto done;
                     mbar_expect_tx(&raw_full[stage], Cfg::RAW_BYTES);
                     const uint32_t sr = su32(sRaw + stage * Cfg::RAW_BYTES);
-                    tma_load_2d_hint(sr, &wmap, &raw_full[stage], kb * 32, row0, pol_first);
-                    tma_load_2d_hint(sr + 128 * 32, &wmap, &raw_full[stage], kb * 32, row0 + a.a_sub1, pol_first);
+                    tma_load_2d_hint(sr, &wmap, &raw_full[stage], rg * 128, row0, pol_first);
+                    tma_load_2d_hint(sr + Cfg::RAW_BYTES / 2, &wmap, &raw_full[stage], rg * 128, row0 + a.a_sub1,
+                                     pol_first);
                     if (++stage == Cfg::RAW_STAGES) { stage = 0; phase ^= 1; p_wrapped = true; }
                 }
                 continue;
@@ -1190,7 +1194,8 @@ __global__ void __launch_bounds__(GCfg<DBUF, FP4>::THREADS, 1) grouped_kernel(co
                 }
                 qa[7] = (in0 && kb + 8 < a.kblocks) ? sc0[kb + 8] : 0u;
                 qb[7] = (in1 && kb + 8 < a.kblocks) ? sc1[kb + 8] : 0u;
-                if (!mbar_wait(&raw_full[rs], rph, abort_flag)) goto done;
+                const int j = kb % Cfg::RAW_KB;               // K block inside the raw stage
+                if (j == 0 && !mbar_wait(&raw_full[rs], rph, abort_flag)) goto done;
                 if (!mbar_wait(&a_empty[as], aph ^ 1, abort_flag)) goto done;
                 const uint8_t *raw = sRaw + rs * Cfg::RAW_BYTES;
                 uint8_t *dstA = sA + as * Cfg::A_BYTES;
@@ -1199,8 +1204,11 @@ __global__ void __launch_bounds__(GCfg<DBUF, FP4>::THREADS, 1) grouped_kernel(co
                     const uint32_t cs = sub ? cur1 : cur0;     // bytes 2 kb (low) and 2 kb + 1
                     const uint32_t s0 = f16_pow2((int)(cs & 0xFF) - 127), s1 = f16_pow2((int)(cs >> 8) - 127);
                     const uint32_t s0x2 = s0 | (s0 << 16), s1x2 = s1 | (s1 << 16);
-                    const uint4 p0 = *reinterpret_cast<const uint4 *>(raw + sub * 128 * 32 + t * 32);
-                    const uint4 p1 = *reinterpret_cast<const uint4 *>(raw + sub * 128 * 32 + t * 32 + 16);
+                    // row t of the sub-tile: 128 bytes in the 128-byte swizzle (16-byte chunk q of
+                    // the row at position q ^ (t % 8)); this K block is chunks 2j and 2j + 1
+                    const uint8_t *rrow = raw + sub * (Cfg::RAW_BYTES / 2) + (t >> 3) * 1024 + (t & 7) * 128;
+                    const uint4 p0 = *reinterpret_cast<const uint4 *>(rrow + (((2 * j) ^ (t & 7)) << 4));
+                    const uint4 p1 = *reinterpret_cast<const uint4 *>(rrow + (((2 * j + 1) ^ (t & 7)) << 4));
                     const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
                     uint8_t *rowp = dstA + sub * 128 * 128 + (t >> 3) * 1024 + (t & 7) * 128;
 #pragma unroll
@@ -1209,11 +1217,12 @@ __global__ void __launch_bounds__(GCfg<DBUF, FP4>::THREADS, 1) grouped_kernel(co
                 }
                 fence_proxy_async();
                 __syncwarp();
+                const bool raw_done = j == Cfg::RAW_KB - 1 || kb == a.kblocks - 1;
                 if (lane == 0) {
-                    mbar_arrive(&raw_empty[rs]);
+                    if (raw_done) mbar_arrive(&raw_empty[rs]);
                     mbar_arrive(&a_full[as]);
                 }
-                if (++rs == Cfg::RAW_STAGES) { rs = 0; rph ^= 1; }
+                if (raw_done && ++rs == Cfg::RAW_STAGES) { rs = 0; rph ^= 1; }
                 if (++as == AST) { as = 0; aph ^= 1; }
             }
         }
@@ -1496,7 +1505,7 @@ int tc_forward_back(const slmoe_config *c, const slmoe_weights *w, const TcForwa
     {   // routed experts, gate|up + SiTU-GLU: h[perm row] = GLU(W13[e] x_lat[token])
         CUtensorMap wm;
         if (fp4) rc = tmap_encode_2d(&wm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w->W13, (long long)E * 2 * I, dl / 2,
-                                     dl / 2, 32, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+                                     dl / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
         else rc = make_map(&wm, w->W13, (long long)E * 2 * I, dl, dl, 128);
         if (rc) return rc;
         GroupedArgs a = {};
@@ -1516,7 +1525,7 @@ int tc_forward_back(const slmoe_config *c, const slmoe_weights *w, const TcForwa
     {   // routed experts, down: y_e[row] = W2[e] h[row]
         CUtensorMap wm;
         if (fp4) rc = tmap_encode_2d(&wm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w->W2, (long long)E * dl, I / 2, I / 2,
-                                     32, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+                                     128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
         else rc = make_map(&wm, w->W2, (long long)E * dl, I, I, 128);
         if (rc) return rc;
         GroupedArgs a = {};
