@@ -371,6 +371,20 @@ def qb_engine(hbm):
             "note": "65536 x 896 fp32 scores per micro-batch (235 MB > L2); engine = 8 histograms + 1 update"}
 
 
+def mxfp4_inputs(inp):
+    """The layer inputs with the routed experts' W13 / W2 quantised to MXFP4 on the device."""
+    import torch
+    import latent_space_experts_gb300 as lse
+    mx = dict(inp)
+    for name in ("W13", "W2"):
+        W = inp[name]
+        K = W.shape[-1]
+        mx[name] = torch.empty(W.shape[:-1] + (K // 2,), dtype=torch.uint8, device="cuda")
+        mx[name + "_scale"] = torch.empty(W.shape[:-1] + (K // 32,), dtype=torch.uint8, device="cuda")
+        lse.slmoe_mxfp4_quantize(W, W.numel() // K, K, mx[name], mx[name + "_scale"])
+    return mx
+
+
 def qb_balance(step=1e-3):
     """QB-engine balance on the GPU: eight 65536 x 896 micro-batches of scores are binned into
     one histogram and routed (slmoe_topk) with a bias that the fixed-step rule updates after
@@ -570,6 +584,8 @@ def main():
                     help="only the backward measurement of the workload (one forward first)")
     ap.add_argument("--no-graph", action="store_true", help="time the step without a CUDA graph")
     ap.add_argument("--skew", action="store_true", help="heavy skew (10%% hot experts)")
+    ap.add_argument("--mxfp4", action="store_true",
+                    help="run the workload as the MXFP4 layer type (routed-expert weights quantised once)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -595,7 +611,9 @@ def main():
             brun = LayerRun(shp, inp, inp["x"], inp["logit_offset"], use_graph=False)
             print(json.dumps({"workload": args.workload, "backward": backward_bench(brun, pk, reps=args.steps)}))
         return
-    run = LayerRun(shp, inp, inp["x"], inp["logit_offset"], use_graph=not args.no_graph, warmup=args.warmup)
+    run_inp = mxfp4_inputs(inp) if args.mxfp4 else inp
+    run = LayerRun(shp, run_inp, inp["x"], inp["logit_offset"], use_graph=not args.no_graph, warmup=args.warmup,
+                   dtype=lse.MXFP4 if args.mxfp4 else None)
     for _ in range(max(0, args.warmup - 3)):
         run.timed(1)
 
@@ -643,7 +661,7 @@ def main():
                 t_start = t[start_of.get(i, i - 1)]
             stage_ms[i] += (t[i] - t_start) / len(ev)
     counts = run.counts()
-    st_model, layer_flops, layer_bytes = work_model(shp, counts)
+    st_model, layer_flops, layer_bytes = work_model(shp, counts, run.expert_weight_bytes)
     tc, tc_kind = tensor_peak(pk, timed_s, reasons)
     stages = {}
     for i in range(1, nst):
@@ -747,13 +765,7 @@ def main():
                 del drun
         if args.workload == "k3_prefill":
             # the MXFP4 layer type: the same weights with the routed experts quantised once
-            mx = dict(inp)
-            for name in ("W13", "W2"):
-                W = inp[name]
-                K = W.shape[-1]
-                mx[name] = torch.empty(W.shape[:-1] + (K // 2,), dtype=torch.uint8, device="cuda")
-                mx[name + "_scale"] = torch.empty(W.shape[:-1] + (K // 32,), dtype=torch.uint8, device="cuda")
-                lse.slmoe_mxfp4_quantize(W, W.numel() // K, K, mx[name], mx[name + "_scale"])
+            mx = mxfp4_inputs(inp)
             for name, T in (("k3_decode_mxfp4", 128), ("k3_prefill_mxfp4", shp.T)):
                 s_mx = synthetic.shape_with(shp, T=T)
                 mrun = LayerRun(s_mx, mx, inp["x"][:T].contiguous(), inp["logit_offset"], dtype=lse.MXFP4)
@@ -797,6 +809,7 @@ def main():
             "config": {"workload": args.workload, "T": shp.T, "d": shp.d, "d_latent": shp.d_latent,
                        "E": shp.E, "k": shp.k, "I": shp.I, "n_shared": shp.n_shared, "I_shared": shp.I_shared,
                        "router": "fp32 logits (3-piece bf16 split)", "skew": bool(args.skew),
+                       "routed_expert_weights": "mxfp4" if args.mxfp4 else "bf16",
                        "parallelism": f"replicas x{world}",
                        "l2": "no flush: weights (10.2 GB at K3) exceed L2 every step",
                        "cuda_graph": run.graph is not None},
