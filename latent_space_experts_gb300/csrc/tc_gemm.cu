@@ -735,17 +735,21 @@ constexpr int G_TQ = 4;                           // item queue slots
 
 // FP4: the weights arrive as packed MXFP4 through a ring of their own, 128 bytes per row (four
 // 64-wide K blocks: whole L2 lines) per raw stage, in the 128-byte swizzle; four dequantising
-// warps turn each K block into the f16 tile the MMA reads (two f16 stages suffice: they hide
-// the dequantisation, the raw ring hides HBM).
+// warps (one per TMEM lane quadrant) turn each K block into f16 and store it straight into
+// tensor memory, where the MMA takes its A operand: the tile never passes through shared
+// memory.  Two A stages live in the TMEM columns beside the accumulator (192..255 and
+// 448..511; a pass holds at most 192 tokens, so the accumulator uses columns below 192 and
+// 256..447).
 template <bool DBUF, bool FP4 = false>
 struct GCfg {
     static constexpr int NSUB = 2;
     static constexpr int PASS = DBUF ? 128 : GROUPED_PASS;   // tokens per pass
     static constexpr int A_BYTES = NSUB * 128 * 128;
     static constexpr int A_STAGES = FP4 ? 2 : (DBUF ? 5 : 4);  // 160 KB / 128 KB of weights in flight
+    static constexpr int A_SMEM_STAGES = FP4 ? 0 : A_STAGES;  // FP4: the A stages are in TMEM
     static constexpr int RAW_KB = 4;                        // K blocks per raw stage
     static constexpr int RAW_BYTES = NSUB * 128 * 32 * RAW_KB;
-    static constexpr int RAW_STAGES = FP4 ? 2 : 0;
+    static constexpr int RAW_STAGES = FP4 ? 4 : 0;
     static constexpr int DQ_WARPS = FP4 ? 4 : 0;
     static constexpr int B_BYTES = PASS * 128;
     static constexpr int B_STAGES = 4;
@@ -758,7 +762,7 @@ struct GCfg {
     static constexpr int DQ_WARP0 = GATHER_WARP0 + 4;
     // TMA, MMA, epilogue, 4 gather warps (+ 4 dequantising warps)
     static constexpr int THREADS = (2 + EPI_WARPS + 4 + DQ_WARPS) * 32;
-    static constexpr int SMEM = A_STAGES * A_BYTES + B_STAGES * B_BYTES + RAW_STAGES * RAW_BYTES + 1024 + 512;
+    static constexpr int SMEM = A_SMEM_STAGES * A_BYTES + B_STAGES * B_BYTES + RAW_STAGES * RAW_BYTES + 1024 + 512;
     static_assert(SMEM <= 232448, "shared memory");
 };
 
@@ -907,7 +911,7 @@ __global__ void __launch_bounds__(GCfg<DBUF, FP4>::THREADS, 1) grouped_kernel(co
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;
-    uint8_t *sB = smem + AST * Cfg::A_BYTES;
+    uint8_t *sB = smem + Cfg::A_SMEM_STAGES * Cfg::A_BYTES;
     uint8_t *sRaw = sB + BST * Cfg::B_BYTES;
     int4 *q_items = reinterpret_cast<int4 *>(sRaw + Cfg::RAW_STAGES * Cfg::RAW_BYTES);
     constexpr int RST = Cfg::RAW_STAGES > 0 ? Cfg::RAW_STAGES : 1;
@@ -1047,13 +1051,17 @@ __global__ void __launch_bounds__(GCfg<DBUF, FP4>::THREADS, 1) grouped_kernel(co
                 if (!mbar_wait(&b_full[bs], bph, abort_flag)) goto done;
                 fence_proxy_async();
                 tc_after();
-                const uint32_t sa = su32(sA + as * Cfg::A_BYTES);
+                const uint32_t sa = su32(sA + (FP4 ? 0 : as) * Cfg::A_BYTES);
                 const uint32_t sb = su32(sB + bs * Cfg::B_BYTES);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
                     const uint64_t bd = sdesc(sb + kk * 32);
-                    if (AMN) {
+                    if (FP4) {     // A from TMEM: 8 columns (16 f16 values) per K = 16 step
+                        const uint32_t ta = tmem_base + (as == 0 ? 192u : 448u) + kk * 8;
+                        umma_ts(d, ta, bd, idesc, acc);
+                        umma_ts(d + SUB1, ta + 32, bd, idesc, acc);
+                    } else if (AMN) {
                         umma(d, mn_desc(sa + kk * 2048, 8192), bd, idesc, acc);
                         umma(d + SUB1, mn_desc(sa + 128 * 128 + kk * 2048, 8192), bd, idesc, acc);
                     } else {
@@ -1161,11 +1169,13 @@ __global__ void __launch_bounds__(GCfg<DBUF, FP4>::THREADS, 1) grouped_kernel(co
             if (++buf == NBUF) { buf = 0; tph ^= 1; }
         }
     } else if (FP4 && warp >= Cfg::DQ_WARP0) {
-        // ------------------------------------------------ MXFP4 -> f16 (4 warps): thread t turns
-        // row t of both 128-row sub-tiles of a stage into the swizzled K-major f16 layout.  A
-        // stage needs two scale bytes per row (2-byte aligned: a row holds K/32 bytes, K a
-        // multiple of 64); they are loaded 8 stages ahead through a register queue.
-        const int t = threadIdx.x - Cfg::DQ_WARP0 * 32;
+        // ------------------------------------------------ MXFP4 -> f16 (4 warps): the warp of
+        // TMEM lane quadrant q turns rows 32q .. 32q + 31 of both 128-row sub-tiles of a stage
+        // into f16 and stores them into the stage's TMEM columns (row = lane, two f16 values
+        // per column, K order).  A stage needs two scale bytes per row (2-byte aligned: a row
+        // holds K/32 bytes, K a multiple of 64); they are loaded 8 stages ahead.
+        const int t = (warp & 3) * 32 + lane;              // the row of this thread
+        const uint32_t tq = tmem_base + ((uint32_t)((warp & 3) * 32) << 16);
         int qs = 0, rs = 0, as = 0;
         uint32_t qp = 0, rph = 0, aph = 0;
         for (;;) {
@@ -1197,8 +1207,8 @@ __global__ void __launch_bounds__(GCfg<DBUF, FP4>::THREADS, 1) grouped_kernel(co
                 const int j = kb % Cfg::RAW_KB;               // K block inside the raw stage
                 if (j == 0 && !mbar_wait(&raw_full[rs], rph, abort_flag)) goto done;
                 if (!mbar_wait(&a_empty[as], aph ^ 1, abort_flag)) goto done;
+                tc_after();
                 const uint8_t *raw = sRaw + rs * Cfg::RAW_BYTES;
-                uint8_t *dstA = sA + as * Cfg::A_BYTES;
 #pragma unroll
                 for (int sub = 0; sub < 2; ++sub) {
                     const uint32_t cs = sub ? cur1 : cur0;     // bytes 2 kb (low) and 2 kb + 1
@@ -1210,12 +1220,16 @@ __global__ void __launch_bounds__(GCfg<DBUF, FP4>::THREADS, 1) grouped_kernel(co
                     const uint4 p0 = *reinterpret_cast<const uint4 *>(rrow + (((2 * j) ^ (t & 7)) << 4));
                     const uint4 p1 = *reinterpret_cast<const uint4 *>(rrow + (((2 * j + 1) ^ (t & 7)) << 4));
                     const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-                    uint8_t *rowp = dstA + sub * 128 * 128 + (t >> 3) * 1024 + (t & 7) * 128;
+                    uint32_t v[32];
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)   // chunk c = K values 8c .. 8c + 7
-                        *reinterpret_cast<uint4 *>(rowp + ((c ^ (t & 7)) << 4)) = dequant8(words[c], c < 4 ? s0x2 : s1x2);
+                    for (int c = 0; c < 8; ++c) {   // words c = K values 8c .. 8c + 7
+                        const uint4 h = dequant8(words[c], c < 4 ? s0x2 : s1x2);
+                        v[4 * c] = h.x; v[4 * c + 1] = h.y; v[4 * c + 2] = h.z; v[4 * c + 3] = h.w;
+                    }
+                    tmem_st32(tq + (as == 0 ? 192u : 448u) + 32 * sub, v);
                 }
-                fence_proxy_async();
+                tmem_wait_st();
+                tc_before();
                 __syncwarp();
                 const bool raw_done = j == Cfg::RAW_KB - 1 || kb == a.kblocks - 1;
                 if (lane == 0) {
