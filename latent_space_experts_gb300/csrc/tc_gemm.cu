@@ -734,25 +734,25 @@ constexpr int G_GATHER_THREADS = 128;
 constexpr int G_TQ = 4;                           // item queue slots
 
 // FP4: the weights arrive as packed MXFP4 through a ring of their own, 128 bytes per row (four
-// 64-wide K blocks: whole L2 lines) per raw stage, in the 128-byte swizzle; eight dequantising
-// warps (one per TMEM lane quadrant and sub-tile) turn each K block into f16 and store it straight into
+// 64-wide K blocks: whole L2 lines) per raw stage, in the 128-byte swizzle; four dequantising
+// warps (one per TMEM lane quadrant) turn each K block into f16 and store it straight into
 // tensor memory, where the MMA takes its A operand: the tile never passes through shared
-// memory.  Two A stages live in the TMEM columns beside the accumulator (192..255 and
-// 448..511; a pass holds at most 192 tokens, so the accumulator uses columns below 192 and
-// 256..447).
+// memory.  Four A stages of 64 columns live in the TMEM columns beside the accumulator
+// (128..255 and 384..511: FP4 passes hold at most 128 tokens, so the accumulator uses columns
+// below 128 and 256..383).
 template <bool DBUF, bool FP4 = false>
 struct GCfg {
     static constexpr int NSUB = 2;
-    static constexpr int PASS = DBUF ? 128 : GROUPED_PASS;   // tokens per pass
+    static constexpr int PASS = (DBUF || FP4) ? 128 : GROUPED_PASS;   // tokens per pass
     static constexpr int A_BYTES = NSUB * 128 * 128;
-    static constexpr int A_STAGES = FP4 ? 2 : (DBUF ? 5 : 4);  // 160 KB / 128 KB of weights in flight
+    static constexpr int A_STAGES = FP4 ? 4 : (DBUF ? 5 : 4);  // 160 KB / 128 KB of weights in flight
     static constexpr int A_SMEM_STAGES = FP4 ? 0 : A_STAGES;  // FP4: the A stages are in TMEM
     static constexpr int RAW_KB = 4;                        // K blocks per raw stage
     static constexpr int RAW_BYTES = NSUB * 128 * 32 * RAW_KB;
     static constexpr int RAW_STAGES = FP4 ? 4 : 0;
-    static constexpr int DQ_WARPS = FP4 ? 8 : 0;
+    static constexpr int DQ_WARPS = FP4 ? 4 : 0;
     static constexpr int B_BYTES = PASS * 128;
-    static constexpr int B_STAGES = 4;
+    static constexpr int B_STAGES = FP4 ? 6 : 4;
     static constexpr int NBUF = DBUF ? 2 : 1;
     static constexpr int SUB1_COL = DBUF ? 128 : 256;
     // epilogue warps: the single-buffered accumulator (long passes) stalls the MMAs while it
@@ -898,6 +898,8 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w, uint32_t s2) {
     for (int i = 0; i < 4; ++i) asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(h[i]) : "r"(s2));
     return make_uint4(h[0], h[1], h[2], h[3]);
 }
+// TMEM column of FP4 A stage s (two 32-column sub-tiles each).
+__device__ __forceinline__ uint32_t fp4_a_col(int s) { return s < 2 ? 128u + 64u * s : 384u + 64u * (s - 2); }
 // Instruction descriptor, kind::f16 with f16 A and B (K-major), fp32 D, shape M x N.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
     return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
@@ -1058,7 +1060,7 @@ __global__ void __launch_bounds__(GCfg<DBUF, FP4>::THREADS, 1) grouped_kernel(co
                     const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
                     const uint64_t bd = sdesc(sb + kk * 32);
                     if (FP4) {     // A from TMEM: 8 columns (16 f16 values) per K = 16 step
-                        const uint32_t ta = tmem_base + (as == 0 ? 192u : 448u) + kk * 8;
+                        const uint32_t ta = tmem_base + fp4_a_col(as) + kk * 8;
                         umma_ts(d, ta, bd, idesc, acc);
                         umma_ts(d + SUB1, ta + 32, bd, idesc, acc);
                     } else if (AMN) {
@@ -1169,14 +1171,13 @@ __global__ void __launch_bounds__(GCfg<DBUF, FP4>::THREADS, 1) grouped_kernel(co
             if (++buf == NBUF) { buf = 0; tph ^= 1; }
         }
     } else if (FP4 && warp >= Cfg::DQ_WARP0) {
-        // ------------------------------------------------ MXFP4 -> f16 (8 warps): the warp of
-        // TMEM lane quadrant q and sub-tile u turns rows 32q .. 32q + 31 of sub-tile u of a
-        // stage into f16 and stores them into the stage's TMEM columns (row = lane, two f16
-        // values per column, K order).  A stage needs two scale bytes per row (2-byte aligned:
-        // a row holds K/32 bytes, K a multiple of 64); they are loaded 8 stages ahead.
+        // ------------------------------------------------ MXFP4 -> f16 (4 warps): the warp of
+        // TMEM lane quadrant q turns rows 32q .. 32q + 31 of both 128-row sub-tiles of a stage
+        // into f16 and stores them into the stage's TMEM columns (row = lane, two f16 values
+        // per column, K order).  A stage needs two scale bytes per row (2-byte aligned: a row
+        // holds K/32 bytes, K a multiple of 64); they are loaded 8 stages ahead.
         const int t = (warp & 3) * 32 + lane;              // the row of this thread
-        const int sub = (warp - Cfg::DQ_WARP0) >> 2;       // its sub-tile
-        const uint32_t tq = tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + 32 * sub;
+        const uint32_t tq = tmem_base + ((uint32_t)((warp & 3) * 32) << 16);
         int qs = 0, rs = 0, as = 0;
         uint32_t qp = 0, rph = 0, aph = 0;
         for (;;) {
@@ -1184,39 +1185,51 @@ __global__ void __launch_bounds__(GCfg<DBUF, FP4>::THREADS, 1) grouped_kernel(co
             if (!pop(qs, qp, it, true)) goto done;
             if (it.w < 0) break;
             const int fb = it.y & 0xffff;
-            const long long wrow = (long long)it.x * a.a_rows_pe + fb * a.a_fb_stride + sub * a.a_sub1 + t;
-            const uint16_t *sc = reinterpret_cast<const uint16_t *>(a.a_scales + wrow * a.a_scale_ld);
+            const long long wrow0 = (long long)it.x * a.a_rows_pe + fb * a.a_fb_stride + t;
+            const uint16_t *sc0 = reinterpret_cast<const uint16_t *>(a.a_scales + wrow0 * a.a_scale_ld);
+            const uint16_t *sc1 = reinterpret_cast<const uint16_t *>(a.a_scales + (wrow0 + a.a_sub1) * a.a_scale_ld);
             // a feature block may run past the last expert's rows: TMA fills those weight rows
             // with zeros, and their scales are not read
-            const bool in = wrow < a.a_rows_total;
-            uint32_t qa[8];
+            const bool in0 = wrow0 < a.a_rows_total, in1 = wrow0 + a.a_sub1 < a.a_rows_total;
+            uint32_t qa[8], qb[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) qa[i] = (in && i < a.kblocks) ? sc[i] : 0u;
+            for (int i = 0; i < 8; ++i) {
+                qa[i] = (in0 && i < a.kblocks) ? sc0[i] : 0u;
+                qb[i] = (in1 && i < a.kblocks) ? sc1[i] : 0u;
+            }
             for (int kb = 0; kb < a.kblocks; ++kb) {
-                const uint32_t cs = qa[0];                     // bytes 2 kb (low) and 2 kb + 1
+                const uint32_t cur0 = qa[0], cur1 = qb[0];
 #pragma unroll
-                for (int i = 0; i < 7; ++i) qa[i] = qa[i + 1];
-                qa[7] = (in && kb + 8 < a.kblocks) ? sc[kb + 8] : 0u;
+                for (int i = 0; i < 7; ++i) {
+                    qa[i] = qa[i + 1];
+                    qb[i] = qb[i + 1];
+                }
+                qa[7] = (in0 && kb + 8 < a.kblocks) ? sc0[kb + 8] : 0u;
+                qb[7] = (in1 && kb + 8 < a.kblocks) ? sc1[kb + 8] : 0u;
                 const int j = kb % Cfg::RAW_KB;               // K block inside the raw stage
                 if (j == 0 && !mbar_wait(&raw_full[rs], rph, abort_flag)) goto done;
                 if (!mbar_wait(&a_empty[as], aph ^ 1, abort_flag)) goto done;
                 tc_after();
-                const uint32_t s0 = f16_pow2((int)(cs & 0xFF) - 127), s1 = f16_pow2((int)(cs >> 8) - 127);
-                const uint32_t s0x2 = s0 | (s0 << 16), s1x2 = s1 | (s1 << 16);
-                // row t of the sub-tile: 128 bytes in the 128-byte swizzle (16-byte chunk q of the
-                // row at position q ^ (t % 8)); this K block is chunks 2j and 2j + 1
-                const uint8_t *rrow = sRaw + rs * Cfg::RAW_BYTES + sub * (Cfg::RAW_BYTES / 2) + (t >> 3) * 1024 +
-                                      (t & 7) * 128;
-                const uint4 p0 = *reinterpret_cast<const uint4 *>(rrow + (((2 * j) ^ (t & 7)) << 4));
-                const uint4 p1 = *reinterpret_cast<const uint4 *>(rrow + (((2 * j + 1) ^ (t & 7)) << 4));
-                const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-                uint32_t v[32];
+                const uint8_t *raw = sRaw + rs * Cfg::RAW_BYTES;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {   // words c = K values 8c .. 8c + 7
-                    const uint4 h = dequant8(words[c], c < 4 ? s0x2 : s1x2);
-                    v[4 * c] = h.x; v[4 * c + 1] = h.y; v[4 * c + 2] = h.z; v[4 * c + 3] = h.w;
+                for (int sub = 0; sub < 2; ++sub) {
+                    const uint32_t cs = sub ? cur1 : cur0;     // bytes 2 kb (low) and 2 kb + 1
+                    const uint32_t s0 = f16_pow2((int)(cs & 0xFF) - 127), s1 = f16_pow2((int)(cs >> 8) - 127);
+                    const uint32_t s0x2 = s0 | (s0 << 16), s1x2 = s1 | (s1 << 16);
+                    // row t of the sub-tile: 128 bytes in the 128-byte swizzle (16-byte chunk q of
+                    // the row at position q ^ (t % 8)); this K block is chunks 2j and 2j + 1
+                    const uint8_t *rrow = raw + sub * (Cfg::RAW_BYTES / 2) + (t >> 3) * 1024 + (t & 7) * 128;
+                    const uint4 p0 = *reinterpret_cast<const uint4 *>(rrow + (((2 * j) ^ (t & 7)) << 4));
+                    const uint4 p1 = *reinterpret_cast<const uint4 *>(rrow + (((2 * j + 1) ^ (t & 7)) << 4));
+                    const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+                    uint32_t v[32];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {   // words c = K values 8c .. 8c + 7
+                        const uint4 h = dequant8(words[c], c < 4 ? s0x2 : s1x2);
+                        v[4 * c] = h.x; v[4 * c + 1] = h.y; v[4 * c + 2] = h.z; v[4 * c + 3] = h.w;
+                    }
+                    tmem_st32(tq + fp4_a_col(as) + 32 * sub, v);
                 }
-                tmem_st32(tq + (as == 0 ? 192u : 448u), v);
                 tmem_wait_st();
                 tc_before();
                 __syncwarp();
@@ -1488,10 +1501,10 @@ int tc_worklists(const slmoe_config *c, const TcForward &f, cudaStream_t st) {
     const int E = c->E, I = c->I, dl = c->d_latent;
     const long long Tk = (long long)c->T * c->k;
     const int nfb1 = (I + 127) / 128, nfb2 = (dl + 255) / 256;
-    const long long Tk_items = (Tk + GROUPED_PASS - 1) / GROUPED_PASS;
-    worklist_kernel<<<1, 1024, 0, st>>>(f.counts, f.offsets, E, nfb1, GCfg<false>::PASS, f.items1, nfb2,
-                                        GCfg<false>::PASS, f.items2, f.counters + 8,
-                                        (int)(nfb1 * (E + Tk_items)), (int)(nfb2 * (E + Tk_items)));
+    const int pass = grouped_pass(c->dtype);
+    const long long Tk_items = (Tk + pass - 1) / pass;
+    worklist_kernel<<<1, 1024, 0, st>>>(f.counts, f.offsets, E, nfb1, pass, f.items1, nfb2, pass, f.items2,
+                                        f.counters + 8, (int)(nfb1 * (E + Tk_items)), (int)(nfb2 * (E + Tk_items)));
     return check_launch("worklist");
 }
 
