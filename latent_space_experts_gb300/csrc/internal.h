@@ -73,10 +73,6 @@ constexpr int ROUTE_CHUNK = 16;  // tokens per top-k block / permutation chunk
 // Tokens per pass of the routed-expert GEMMs: an expert with n tokens makes ceil(n / pass)
 // work items per feature block, which also sizes the work lists in the workspace.
 constexpr int GROUPED_PASS = 192;
-// The MXFP4 layer type's grouped kernels take 128-token passes (their TMEM holds four
-// dequantised weight stages beside the accumulator).
-constexpr int GROUPED_PASS_FP4 = 128;
-inline int grouped_pass(int dtype) { return dtype == SLMOE_MXFP4 ? GROUPED_PASS_FP4 : GROUPED_PASS; }
 // The router of a batch of at most ROUTER_SPLITK_MAX_M tokens splits its K blocks over up to
 // ROUTER_SPLITK_MAX CTAs per tile (their fp32 partial logits live in the workspace).
 constexpr int ROUTER_SPLITK_MAX_M = 256;

@@ -737,22 +737,22 @@ constexpr int G_TQ = 4;                           // item queue slots
 // 64-wide K blocks: whole L2 lines) per raw stage, in the 128-byte swizzle; four dequantising
 // warps (one per TMEM lane quadrant) turn each K block into f16 and store it straight into
 // tensor memory, where the MMA takes its A operand: the tile never passes through shared
-// memory.  Four A stages of 64 columns live in the TMEM columns beside the accumulator
-// (128..255 and 384..511: FP4 passes hold at most 128 tokens, so the accumulator uses columns
-// below 128 and 256..383).
+// memory.  Two A stages live in the TMEM columns beside the accumulator (192..255 and
+// 448..511; a pass holds at most 192 tokens, so the accumulator uses columns below 192 and
+// 256..447).
 template <bool DBUF, bool FP4 = false>
 struct GCfg {
     static constexpr int NSUB = 2;
-    static constexpr int PASS = (DBUF || FP4) ? 128 : GROUPED_PASS;   // tokens per pass
+    static constexpr int PASS = DBUF ? 128 : GROUPED_PASS;   // tokens per pass
     static constexpr int A_BYTES = NSUB * 128 * 128;
-    static constexpr int A_STAGES = FP4 ? 4 : (DBUF ? 5 : 4);  // 160 KB / 128 KB of weights in flight
+    static constexpr int A_STAGES = FP4 ? 2 : (DBUF ? 5 : 4);  // 160 KB / 128 KB of weights in flight
     static constexpr int A_SMEM_STAGES = FP4 ? 0 : A_STAGES;  // FP4: the A stages are in TMEM
     static constexpr int RAW_KB = 4;                        // K blocks per raw stage
     static constexpr int RAW_BYTES = NSUB * 128 * 32 * RAW_KB;
     static constexpr int RAW_STAGES = FP4 ? 4 : 0;
     static constexpr int DQ_WARPS = FP4 ? 4 : 0;
     static constexpr int B_BYTES = PASS * 128;
-    static constexpr int B_STAGES = FP4 ? 6 : 4;
+    static constexpr int B_STAGES = 4;
     static constexpr int NBUF = DBUF ? 2 : 1;
     static constexpr int SUB1_COL = DBUF ? 128 : 256;
     // epilogue warps: the single-buffered accumulator (long passes) stalls the MMAs while it
@@ -898,8 +898,6 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w, uint32_t s2) {
     for (int i = 0; i < 4; ++i) asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(h[i]) : "r"(s2));
     return make_uint4(h[0], h[1], h[2], h[3]);
 }
-// TMEM column of FP4 A stage s (two 32-column sub-tiles each).
-__device__ __forceinline__ uint32_t fp4_a_col(int s) { return s < 2 ? 128u + 64u * s : 384u + 64u * (s - 2); }
 // Instruction descriptor, kind::f16 with f16 A and B (K-major), fp32 D, shape M x N.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
     return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
@@ -1060,7 +1058,7 @@ __global__ void __launch_bounds__(GCfg<DBUF, FP4>::THREADS, 1) grouped_kernel(co
                     const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
                     const uint64_t bd = sdesc(sb + kk * 32);
                     if (FP4) {     // A from TMEM: 8 columns (16 f16 values) per K = 16 step
-                        const uint32_t ta = tmem_base + fp4_a_col(as) + kk * 8;
+                        const uint32_t ta = tmem_base + (as == 0 ? 192u : 448u) + kk * 8;
                         umma_ts(d, ta, bd, idesc, acc);
                         umma_ts(d + SUB1, ta + 32, bd, idesc, acc);
                     } else if (AMN) {
@@ -1228,7 +1226,7 @@ __global__ void __launch_bounds__(GCfg<DBUF, FP4>::THREADS, 1) grouped_kernel(co
                         const uint4 h = dequant8(words[c], c < 4 ? s0x2 : s1x2);
                         v[4 * c] = h.x; v[4 * c + 1] = h.y; v[4 * c + 2] = h.z; v[4 * c + 3] = h.w;
                     }
-                    tmem_st32(tq + fp4_a_col(as) + 32 * sub, v);
+                    tmem_st32(tq + (as == 0 ? 192u : 448u) + 32 * sub, v);
                 }
                 tmem_wait_st();
                 tc_before();
@@ -1501,10 +1499,10 @@ int tc_worklists(const slmoe_config *c, const TcForward &f, cudaStream_t st) {
     const int E = c->E, I = c->I, dl = c->d_latent;
     const long long Tk = (long long)c->T * c->k;
     const int nfb1 = (I + 127) / 128, nfb2 = (dl + 255) / 256;
-    const int pass = grouped_pass(c->dtype);
-    const long long Tk_items = (Tk + pass - 1) / pass;
-    worklist_kernel<<<1, 1024, 0, st>>>(f.counts, f.offsets, E, nfb1, pass, f.items1, nfb2, pass, f.items2,
-                                        f.counters + 8, (int)(nfb1 * (E + Tk_items)), (int)(nfb2 * (E + Tk_items)));
+    const long long Tk_items = (Tk + GROUPED_PASS - 1) / GROUPED_PASS;
+    worklist_kernel<<<1, 1024, 0, st>>>(f.counts, f.offsets, E, nfb1, GCfg<false>::PASS, f.items1, nfb2,
+                                        GCfg<false>::PASS, f.items2, f.counters + 8,
+                                        (int)(nfb1 * (E + Tk_items)), (int)(nfb2 * (E + Tk_items)));
     return check_launch("worklist");
 }
 
