@@ -151,13 +151,18 @@ def rmsnorm(c, gamma, eps=EPS):
     return f64(gamma)[None, :] * c / np.sqrt(np.mean(c * c, axis=1, keepdims=True) + eps)
 
 
-def forward(inp, k, beta1=BETA1, beta2=BETA2, eps=EPS, forced_topk_idx=None, tokens=None):
+def forward(inp, k, beta1=BETA1, beta2=BETA2, eps=EPS, forced_topk_idx=None, tokens=None,
+            mx_activations=False):
     """One Stable LatentMoE layer (the FFN branch, no residual add) in fp64.
 
     inp: dict of the layer inputs (see ``synthetic.layer_inputs``).  ``tokens`` restricts
     the computation to a subset of token rows (every step is per token);
     ``forced_topk_idx`` [T_all, k] replaces the oracle's own selection (the gates are
     still the oracle's renormalised fp64 scores of the forced experts).
+    ``mx_activations`` takes the layer with MXFP4 weights and MXFP8 activations ([SLMoE]
+    训练基础设施): x_lat and each routed expert's h pass through MXFP8 (``mxfp8_round_trip``,
+    blocks of 32 along d_latent and I) before they meet the expert weights; inp["W13"] /
+    inp["W2"] then hold the weights' dequantised values.
 
     Returns a dict with scores, topk_idx, gates, gap, x_lat, c (the gate-weighted combine),
     z (after RMSNorm), y_routed (z projected up), y_shared and y.
@@ -184,11 +189,14 @@ def forward(inp, k, beta1=BETA1, beta2=BETA2, eps=EPS, forced_topk_idx=None, tok
     # routed experts in latent space, gate-weighted sum over the k chosen experts
     W13, W2 = inp["W13"], inp["W2"]
     d_lat = x_lat.shape[1]
+    x_in = mxfp8_round_trip(x_lat) if mx_activations else x_lat
     c = np.zeros((T, d_lat))
     for e in np.unique(sel):
         tt, jj = np.nonzero(sel == e)
-        gu = x_lat[tt] @ f64(W13[int(e)]).T               # [n, 2I]: gate rows first
+        gu = x_in[tt] @ f64(W13[int(e)]).T                 # [n, 2I]: gate rows first
         h = situ_glu(gu, beta1, beta2)
+        if mx_activations:
+            h = mxfp8_round_trip(h)
         y_e = h @ f64(W2[int(e)]).T                        # [n, d_latent]
         np.add.at(c, tt, gates[tt, jj][:, None] * y_e)
 
@@ -497,3 +505,80 @@ def mxfp4_dequantize(packed, scales):
     X = np.ldexp(1.0, np.asarray(scales, dtype=np.int64) - 127)
     K = codes.shape[-1]
     return (val.reshape(codes.shape[:-1] + (K // MX_BLOCK, MX_BLOCK)) * X[..., None]).reshape(codes.shape)
+
+
+# ----------------------------------------------------------------------------------------
+# MXFP8 activations  ([SLMoE] 训练基础设施: MXFP8 activations beside the MXFP4 weights).  The
+# same OCP Microscaling block format with FP8 E4M3 elements: sign bit, four exponent bits with
+# bias 7 and three mantissa bits, so normal values 2^(E-7) (1 + m/8) for E = 1..15 (E = 15 with
+# m = 7 is NaN, so the largest value is 448) and subnormal values m/8 * 2^-6.  A block of 32
+# consecutive values along K shares X = 2^e, e = floor(log2(max |v|)) - 8 (8 = the largest E4M3
+# exponent), clamped to [-127, 127] (-127 for an all-zero block), stored as the E8M0 byte
+# e + 127.  Each v / X goes to the nearest E4M3 value, ties to the even mantissa, values past
+# 448 to 448 (saturation); the sign bit is set for v < 0, so a negative value that rounds to
+# zero is -0.  Which activations are MXFP8 is a reading: the pages name the formats only.
+# Here they are the two operands that meet the MXFP4 weights, x_lat (before the experts'
+# gate/up) and h (before the experts' down), blocked along the contraction dimension.
+# ----------------------------------------------------------------------------------------
+
+E4M3_MAX = 448.0
+
+
+def e4m3_round(v):
+    """Nearest E4M3 value to each v (fp64), ties to the even mantissa, saturating at 448."""
+    v = f64(v)
+    a = np.abs(v)
+    _, ex = np.frexp(a)                      # a = f * 2^ex, f in [0.5, 1): floor(log2 a) = ex - 1
+    p = np.maximum(ex.astype(np.int64) - 1, -6)
+    step = np.ldexp(1.0, p - 3)              # grid step of the binade (subnormals: 2^-9)
+    r = np.minimum(np.rint(a / step) * step, E4M3_MAX)
+    return np.where(v < 0, -r, r)
+
+
+def e4m3_encode(r, negative):
+    """E4M3 codes (uint8) of values r that are on the E4M3 grid; `negative` sets the sign bit."""
+    a = np.abs(f64(r))
+    _, ex = np.frexp(a)
+    p = ex.astype(np.int64) - 1
+    normal = a >= 2.0 ** -6
+    E = np.where(normal, p + 7, 0)
+    M = np.where(normal, np.ldexp(a, -p) * 8 - 8, a * 2.0 ** 9)
+    code = (E << 3) | M.astype(np.int64)
+    return (code | np.where(negative, 0x80, 0)).astype(np.uint8)
+
+
+def e4m3_decode(codes):
+    """Values (fp64) of E4M3 codes; the two NaN codes decode to NaN."""
+    c = np.asarray(codes, dtype=np.int64)
+    E = (c >> 3) & 15
+    M = c & 7
+    mag = np.where(E == 0, M / 8.0 * 2.0 ** -6, (1 + M / 8.0) * np.ldexp(1.0, E - 7))
+    mag = np.where((E == 15) & (M == 7), np.nan, mag)
+    return np.where(c & 0x80, -mag, mag)
+
+
+def mxfp8_quantize(V):
+    """(codes uint8 [..., K], scales uint8 [..., K/32]) of V [..., K] (K a multiple of 32)."""
+    v = f64(V)
+    K = v.shape[-1]
+    blocks = v.reshape(v.shape[:-1] + (K // MX_BLOCK, MX_BLOCK))
+    amax = np.max(np.abs(blocks), axis=-1)
+    _, ex = np.frexp(amax)
+    e = np.where(amax > 0, ex.astype(np.int64) - 1 - 8, -127)
+    e = np.clip(e, -127, 127)
+    scaled = blocks / np.ldexp(1.0, e)[..., None]
+    codes = e4m3_encode(e4m3_round(scaled), scaled < 0).reshape(v.shape)
+    return codes, (e + 127).astype(np.uint8)
+
+
+def mxfp8_dequantize(codes, scales):
+    """The values [..., K] (fp64) that MXFP8 codes and their block scales stand for."""
+    val = e4m3_decode(codes)
+    X = np.ldexp(1.0, np.asarray(scales, dtype=np.int64) - 127)
+    K = val.shape[-1]
+    return (val.reshape(val.shape[:-1] + (K // MX_BLOCK, MX_BLOCK)) * X[..., None]).reshape(val.shape)
+
+
+def mxfp8_round_trip(V):
+    """V quantised to MXFP8 and back (fp64): the value an MXFP8 activation carries."""
+    return mxfp8_dequantize(*mxfp8_quantize(V))
