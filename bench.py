@@ -48,24 +48,30 @@ def peaks():
     return PEAKS_FALLBACK, "fallback"
 
 
-def work_model(shp, counts=None, expert_weight_bytes=2.0):
+# The block-scaled MMA of the MXFP4 layer (E2M1 x E4M3) runs at the FP8 tensor rate: the
+# measured bf16 peak times the nominal ratio 4.5 / 2.25 PFLOP/s.
+MX_TENSOR_RATIO = 2.0
+
+
+def work_model(shp, counts=None, mx=False):
     """FLOPs and bytes per stage of one step.  "bytes" are the algorithmic bytes the survey
     counts (weights touched, the layer's input x and its fp32 output y); "inter" are the
     intermediates a stage reads or writes (scores, x_lat, h, y_e, z, h_s), which a fused
-    design could avoid and which are reported separately.  expert_weight_bytes: bytes per
-    routed-expert weight (2 for bf16; 17/32 for MXFP4: half a byte per code plus one scale
-    byte per 32)."""
-    wb = expert_weight_bytes
+    design could avoid and which are reported separately.  mx: the MXFP4 layer type, whose
+    routed-expert weights take 17/32 bytes each (half a byte per code plus one scale byte per
+    32) and whose x_lat and h are MXFP8 (33/32 bytes per value)."""
+    wb = 17 / 32 if mx else 2.0
+    ab = 33 / 32 if mx else 2.0          # bytes per x_lat / h value
     T, d, dl, E, k, I, ns, Is = shp.T, shp.d, shp.d_latent, shp.E, shp.k, shp.I, shp.n_shared, shp.I_shared
     touched = E if counts is None else int((counts > 0).sum())
     st = {
         "router": dict(flops=2 * T * d * E, bytes=T * d * 2 + E * d * 4, inter=T * E * 4, bound="tensor"),
         "topk+permute+hist": dict(flops=0, bytes=0, inter=2 * T * E * 4 + T * k * 16, bound="hbm"),
-        "down": dict(flops=2 * T * d * dl, bytes=T * d * 2 + dl * d * 2, inter=T * dl * 2, bound="tensor"),
+        "down": dict(flops=2 * T * d * dl, bytes=T * d * 2 + dl * d * 2, inter=int(T * dl * ab), bound="tensor"),
         "expert gate|up": dict(flops=2 * T * k * dl * 2 * I, bytes=int(touched * 2 * I * dl * wb),
-                               inter=T * dl * 2 + T * k * I * 2, bound="hbm"),
+                               inter=int(T * dl * ab + T * k * I * ab), bound="hbm"),
         "expert down": dict(flops=2 * T * k * I * dl, bytes=int(touched * dl * I * wb),
-                            inter=T * k * I * 2 + T * k * dl * 2, bound="hbm"),
+                            inter=int(T * k * I * ab) + T * k * dl * 2, bound="hbm"),
         "combine+rmsnorm": dict(flops=0, bytes=0, inter=T * k * dl * 2 + T * dl * 2 + T * k * 8, bound="hbm"),
         "shared gate|up": dict(flops=2 * T * d * 2 * Is * ns, bytes=T * d * 2 + ns * 2 * Is * d * 2,
                                inter=T * ns * Is * 2, bound="tensor"),
@@ -439,7 +445,7 @@ class LayerRun:
         import latent_space_experts_gb300 as lse
         self.lse, self.shp, self.inp, self.x, self.mu = lse, shp, inp, x, mu
         self.cfg = lse.config(shp, dtype=dtype)
-        self.expert_weight_bytes = 17 / 32 if dtype == lse.MXFP4 else 2.0
+        self.mx = dtype == lse.MXFP4
         self.ws = torch.zeros(lse.slmoe_workspace_size(self.cfg), dtype=torch.uint8, device="cuda")
         self.y = torch.empty(shp.T, shp.d, dtype=torch.float32, device="cuda")
         self.hist = torch.zeros(shp.E, shp.nbins, dtype=torch.int32, device="cuda")
@@ -551,18 +557,26 @@ def backward_bench(run, pk, reps=5):
             "note": "weight gradients fp32 (overwritten); contractions on tcgen05 (bf16 operands)"}
 
 
+def tensor_seconds(st_model, flops, tc, mx):
+    """Time of the layer's FLOPs at the tensor peak tc (TFLOP/s); on the MXFP4 layer type the
+    routed experts' FLOPs run at MX_TENSOR_RATIO times that rate."""
+    routed = st_model["expert gate|up"]["flops"] + st_model["expert down"]["flops"] if mx else 0
+    return (flops - routed) / (tc * 1e12) + routed / (MX_TENSOR_RATIO * tc * 1e12)
+
+
 def layer_summary(run, ms, pk, timed_s, reasons):
     """Tokens/s and the whole-layer roofline of one timed layer configuration."""
-    st_model, flops, nbytes = work_model(run.shp, run.counts(), run.expert_weight_bytes)
+    st_model, flops, nbytes = work_model(run.shp, run.counts(), run.mx)
     tc, tc_kind = tensor_peak(pk, timed_s, reasons)
-    t_flops, t_bytes = flops / (tc * 1e12), nbytes / (pk["hbm_gbs"] * 1e9)
+    t_flops, t_bytes = tensor_seconds(st_model, flops, tc, run.mx), nbytes / (pk["hbm_gbs"] * 1e9)
     t_layer = max(t_flops, t_bytes)
+    lr = {"ms": round(t_layer * 1e3, 4), "frac": round(t_layer * 1e3 / ms, 4),
+          "bound": "tensor" if t_flops >= t_bytes else "hbm", "flops": flops,
+          "bytes": nbytes, "tensor_peak_tflops": tc, "tensor_peak": tc_kind, "hbm_gbs": pk["hbm_gbs"]}
+    if run.mx:
+        lr["routed_expert_tensor_peak"] = f"{MX_TENSOR_RATIO:g} x {tc_kind} (block-scaled FP8 rate, nominal ratio)"
     return {"ms_per_step": round(ms, 4), "tokens_per_s": round(run.shp.T / (ms * 1e-3), 1),
-            "layer_roofline": {"ms": round(t_layer * 1e3, 4), "frac": round(t_layer * 1e3 / ms, 4),
-                               "bound": "tensor" if t_flops >= t_bytes else "hbm", "flops": flops,
-                               "bytes": nbytes, "tensor_peak_tflops": tc, "tensor_peak": tc_kind,
-                               "hbm_gbs": pk["hbm_gbs"]},
-            "experts_touched": int((run.counts() > 0).sum())}
+            "layer_roofline": lr, "experts_touched": int((run.counts() > 0).sum())}
 
 
 def main():
@@ -661,7 +675,7 @@ def main():
                 t_start = t[start_of.get(i, i - 1)]
             stage_ms[i] += (t[i] - t_start) / len(ev)
     counts = run.counts()
-    st_model, layer_flops, layer_bytes = work_model(shp, counts, run.expert_weight_bytes)
+    st_model, layer_flops, layer_bytes = work_model(shp, counts, run.mx)
     tc, tc_kind = tensor_peak(pk, timed_s, reasons)
     stages = {}
     for i in range(1, nst):
@@ -689,7 +703,7 @@ def main():
     roof["algorithmic_bytes"] = dm["bytes"]
     summary = layer_summary(run, ms, pk, timed_s, reasons)
     lr = summary["layer_roofline"]
-    t_sus = max(layer_flops / (pk["bf16_tflops_sustained"] * 1e12), layer_bytes / (hbm * 1e9))
+    t_sus = max(tensor_seconds(st_model, layer_flops, pk["bf16_tflops_sustained"], run.mx), layer_bytes / (hbm * 1e9))
     lr["frac_vs_sustained_peak"] = round(t_sus * 1e3 / ms, 4)
 
     # ---------------- end to end through the public API, host buffers
@@ -771,8 +785,9 @@ def main():
                 mrun = LayerRun(s_mx, mx, inp["x"][:T].contiguous(), inp["logit_offset"], dtype=lse.MXFP4)
                 mms, _ = mrun.timed(100)
                 extra[name] = layer_summary(mrun, mms, pk, mms * 0.1, reasons)
-                extra[name]["note"] = ("routed-expert weights MXFP4 (E2M1 + E8M0 per 32), dequantised on chip "
-                                       "into f16 tiles; latent activations f16; the rest as the bf16 layer")
+                extra[name]["note"] = ("routed experts on the block-scaled tensor cores: weights MXFP4 (E2M1 + "
+                                       "E8M0 per 32), x_lat and h MXFP8 (E4M3 + E8M0 per 32); the rest as the "
+                                       "bf16 layer")
                 del mrun
             del mx
         mshp = synthetic.LAYERS["mid"]

@@ -61,12 +61,15 @@ extern "C" {
 
 #define SLMOE_F32  0             /* x, projection weights and intermediates in fp32      */
 #define SLMOE_BF16 1             /* the same in bf16 (fp32 accumulation, fp32 router)    */
-/* SLMOE_BF16 with the routed experts' weights W13 and W2 in MXFP4 ([SLMoE] 训练基础设施:
- * MXFP4 weights; see slmoe_mxfp4_quantize for the format): W13 / W2 then point to packed
- * codes [E, 2I, d_latent/2] / [E, d_latent, I/2] (bytes) with block scales W13_scale
- * [E, 2I, d_latent/32] / W2_scale [E, d_latent, I/32].  The routed experts compute in f16
- * (x_lat and h are kept in f16; each weight tile is dequantised on chip, exactly for block
- * scales in [2^-23, 2^13]); everything else is as SLMOE_BF16. */
+/* The layer with MXFP4 weights and MXFP8 activations in the routed experts ([SLMoE]
+ * 训练基础设施: MXFP4 weights, MXFP8 activations): W13 / W2 point to packed MXFP4 codes
+ * [E, 2I, d_latent/2] / [E, d_latent, I/2] (bytes, 32-byte aligned; see slmoe_mxfp4_quantize)
+ * with block scales W13_scale [E, 2I, d_latent/32] / W2_scale [E, d_latent, I/32].  The
+ * routed experts' inputs x_lat and h are MXFP8 (see slmoe_mxfp8_quantize: blocks of 32 along
+ * d_latent and I), produced by the epilogues of the down-projection and of the experts'
+ * gate/up, and every routed-expert contraction runs on the block-scaled tensor cores (E2M1
+ * x E4M3 products, exact, fp32 accumulation).  d_latent and I must be multiples of 128.
+ * Everything else (router, shared experts, projections, y_e, z) is as SLMOE_BF16. */
 #define SLMOE_MXFP4 2
 
 /* Shape and constants of one layer.  beta1 / beta2 are the SiTU and soft-cap constants
@@ -111,7 +114,9 @@ typedef struct slmoe_weights {
  * Types: scores fp32 [T,E]; topk_idx int32 [T,k]; topk_w fp32 [T,k]; counts int32 [E];
  * offsets int32 [E+1]; perm int32 [T*k]; slot_pos int32 [T*k]; x_lat act [T,d_latent];
  * h act [T*k, I] (rows in perm order); y_e act [T*k, d_latent] (rows in perm order);
- * z act [T,d_latent]; h_s act [T, n_shared*I_shared]; status int32 [4]. */
+ * z act [T,d_latent]; h_s act [T, n_shared*I_shared]; status int32 [4].  act is fp32 for
+ * SLMOE_F32 and bf16 otherwise, except that SLMOE_MXFP4 keeps x_lat and h as MXFP8: codes
+ * [rows, K] bytes followed directly by their scales [rows, K/32] (K = d_latent, I). */
 typedef struct slmoe_workspace_layout {
     size_t scores, topk_idx, topk_w, counts, offsets, perm, slot_pos;
     size_t x_lat, h, y_e, z, h_s, status;
@@ -268,6 +273,21 @@ SLMOE_API int slmoe_wait_abort_check(int32_t *status, uint64_t wait_limit_ns, vo
  *   of 32.
  */
 SLMOE_API int slmoe_mxfp4_quantize(const void *W, int64_t rows, int32_t K, uint8_t *packed, uint8_t *scales,
+                                   void *stream);
+
+/*
+ * slmoe_mxfp8_quantize - fp32 values to MXFP8 ([SLMoE] 训练基础设施: MXFP8 activations; the
+ *   format is the OCP Microscaling one with FP8 E4M3 elements).  X [rows, K] fp32, K a
+ *   multiple of 32.  Each block of 32 consecutive values of a row shares the scale 2^e with
+ *   e = floor(log2 max|v|) - 8, clamped to [-127, 127] (-127 for an all-zero block), stored
+ *   as the byte e + 127 in scales [rows, K/32]; each value becomes the E4M3 code (sign, 4
+ *   exponent bits with bias 7, 3 mantissa bits; largest value 448) nearest to v / 2^e, ties
+ *   to the even mantissa, saturating at 448, sign bit for v < 0; codes [rows, K].  This is
+ *   the conversion the SLMOE_MXFP4 layer applies to x_lat and h.  X and codes 16-byte
+ *   aligned.  Errors: SLMOE_EINVAL on null or misaligned pointers, rows < 0, K not a positive
+ *   multiple of 32.
+ */
+SLMOE_API int slmoe_mxfp8_quantize(const float *X, int64_t rows, int32_t K, uint8_t *codes, uint8_t *scales,
                                    void *stream);
 
 /*

@@ -14,7 +14,7 @@ from . import _build
 
 __all__ = ["SlmoeError", "Config", "Weights", "WorkspaceLayout", "load", "build", "config",
            "weights", "slmoe_workspace_size", "slmoe_workspace_layout_get", "slmoe_route",
-           "slmoe_route_noalloc", "slmoe_topk", "slmoe_mxfp4_quantize", "slmoe_topk_workspace_size", "slmoe_wait_abort_check",
+           "slmoe_route_noalloc", "slmoe_topk", "slmoe_mxfp4_quantize", "slmoe_mxfp8_quantize", "slmoe_topk_workspace_size", "slmoe_wait_abort_check",
            "slmoe_qb_histogram", "slmoe_qb_update", "slmoe_signsgd_update",
            "slmoe_forward", "slmoe_backward", "slmoe_backward_workspace_size", "slmoe_backward_layout_get",
            "backward_views", "Grads", "grads",
@@ -87,6 +87,7 @@ def load():
         "slmoe_topk": (ctypes.c_int, [P, P, I32, I32, I32, P, P, P, P, P, P, P, P, SZ, P]),
         "slmoe_wait_abort_check": (ctypes.c_int, [P, ctypes.c_uint64, P]),
         "slmoe_mxfp4_quantize": (ctypes.c_int, [P, I64, I32, P, P, P]),
+        "slmoe_mxfp8_quantize": (ctypes.c_int, [P, I64, I32, P, P, P]),
         "slmoe_qb_histogram": (ctypes.c_int, [P, I64, I32, I32, P, P, P]),
         "slmoe_qb_update": (ctypes.c_int, [P, I32, I32, I32, P, P, P]),
         "slmoe_signsgd_update": (ctypes.c_int, [P, I32, ctypes.c_float, P, P]),
@@ -192,15 +193,23 @@ def workspace_views(cfg: Config, ws):
     import torch
     L = slmoe_workspace_layout_get(cfg)
     act = torch.float32 if cfg.dtype == F32 else torch.bfloat16
-    lat = torch.float16 if cfg.dtype == MXFP4 else act     # the MXFP4 type keeps x_lat and h in f16
     T, k, E = cfg.T, cfg.k, cfg.E
 
-    def view(name, dtype, shape):
+    def view(name, dtype, shape, at=0):
         n = 1
         for s in shape:
             n *= s
         nbytes = n * torch.empty((), dtype=dtype).element_size()
-        return ws[L[name]:L[name] + nbytes].view(dtype).view(*shape)
+        return ws[L[name] + at:L[name] + at + nbytes].view(dtype).view(*shape)
+
+    if cfg.dtype == MXFP4:   # x_lat and h as MXFP8: codes, then their block scales
+        dl, I = cfg.d_latent, cfg.I
+        lat = dict(x_lat=view("x_lat", torch.uint8, (T, dl)),
+                   x_lat_scales=view("x_lat", torch.uint8, (T, dl // 32), at=T * dl),
+                   h=view("h", torch.uint8, (T * k, I)),
+                   h_scales=view("h", torch.uint8, (T * k, I // 32), at=T * k * I))
+    else:
+        lat = dict(x_lat=view("x_lat", act, (T, cfg.d_latent)), h=view("h", act, (T * k, cfg.I)))
 
     return dict(scores=view("scores", torch.float32, (T, E)),
                 topk_idx=view("topk_idx", torch.int32, (T, k)),
@@ -209,8 +218,7 @@ def workspace_views(cfg: Config, ws):
                 offsets=view("offsets", torch.int32, (E + 1,)),
                 perm=view("perm", torch.int32, (T * k,)),
                 slot_pos=view("slot_pos", torch.int32, (T, k)),
-                x_lat=view("x_lat", lat, (T, cfg.d_latent)),
-                h=view("h", lat, (T * k, cfg.I)),
+                **lat,
                 y_e=view("y_e", act, (T * k, cfg.d_latent)),
                 z=view("z", act, (T, cfg.d_latent)),
                 h_s=view("h_s", act, (T, cfg.n_shared * cfg.I_shared)),
@@ -253,6 +261,10 @@ def slmoe_topk(scores, bias, T, E, k, topk_idx, topk_w, counts, offsets, perm, s
 
 def slmoe_mxfp4_quantize(W, rows, K, packed, scales, stream=None):
     _check(load().slmoe_mxfp4_quantize(_ptr(W), rows, K, _ptr(packed), _ptr(scales), _stream(stream)))
+
+
+def slmoe_mxfp8_quantize(X, rows, K, codes, scales, stream=None):
+    _check(load().slmoe_mxfp8_quantize(_ptr(X), rows, K, _ptr(codes), _ptr(scales), _stream(stream)))
 
 
 def slmoe_wait_abort_check(status, wait_limit_ns, stream=None):

@@ -65,6 +65,8 @@ int validate_config(const slmoe_config *c) {
     if (c->I < m || c->I % m) return fail(SLMOE_EINVAL, "I = %d is not a positive multiple of %d", c->I, m);
     if (c->n_shared > 0 && (c->I_shared < m || c->I_shared % m))
         return fail(SLMOE_EINVAL, "I_shared = %d is not a positive multiple of %d", c->I_shared, m);
+    if (c->dtype == SLMOE_MXFP4 && (c->d_latent % 128 || c->I % 128))
+        return fail(SLMOE_EINVAL, "SLMOE_MXFP4 needs d_latent and I multiples of 128 (%d, %d)", c->d_latent, c->I);
     if (!(c->beta1 > 0.f) || !(c->beta2 > 0.f) || !(c->eps >= 0.f))
         return fail(SLMOE_EINVAL, "beta1, beta2 must be > 0 and eps >= 0");
     if ((int64_t)c->T * c->k > (int64_t)INT32_MAX / 2)
@@ -425,6 +427,15 @@ int slmoe_mxfp4_quantize(const void *W, int64_t rows, int32_t K, uint8_t *packed
     return launch_mxfp4_quantize(W, rows, K, packed, scales, static_cast<cudaStream_t>(stream));
 }
 
+int slmoe_mxfp8_quantize(const float *X, int64_t rows, int32_t K, uint8_t *codes, uint8_t *scales, void *stream) {
+    g_err[0] = 0;
+    if (rows < 0 || K <= 0 || K % 32) return fail(SLMOE_EINVAL, "rows >= 0 and K a positive multiple of 32 required");
+    if (rows == 0) return SLMOE_OK;
+    REQ(X, "X"); REQ(codes, "codes");
+    if (!scales) return fail(SLMOE_EINVAL, "scales is NULL");
+    return launch_mxfp8_quantize(X, rows, K, codes, scales, static_cast<cudaStream_t>(stream));
+}
+
 int slmoe_wait_abort_check(int32_t *status, uint64_t wait_limit_ns, void *stream) {
     g_err[0] = 0;
     REQ(status, "status");
@@ -519,7 +530,12 @@ int slmoe_forward(const slmoe_config *cfg, const void *x, const slmoe_weights *w
     REQ(w->W_r, "W_r"); REQ(w->W_in, "W_in"); REQ(w->W13, "W13"); REQ(w->W2, "W2");
     REQ(w->gamma, "gamma"); REQ(w->W_out, "W_out");
     if (cfg->n_shared > 0) { REQ(w->W13_s, "W13_s"); REQ(w->W2_s, "W2_s"); }
-    if (cfg->dtype == SLMOE_MXFP4) { REQ(w->W13_scale, "W13_scale"); REQ(w->W2_scale, "W2_scale"); }
+    if (cfg->dtype == SLMOE_MXFP4) {
+        REQ(w->W13_scale, "W13_scale"); REQ(w->W2_scale, "W2_scale");
+        // the packed weights are read by TMA with the FP4 expansion, which wants 32-byte alignment
+        if (((uintptr_t)w->W13 | (uintptr_t)w->W2) & 31u)
+            return fail(SLMOE_EINVAL, "W13 / W2 (MXFP4) are not 32-byte aligned");
+    }
     OPT(topk_idx_out, "topk_idx_out"); OPT(hist, "hist"); OPT(status, "status");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     char *ws = static_cast<char *>(workspace);

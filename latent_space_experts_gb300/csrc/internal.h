@@ -92,6 +92,7 @@ int launch_combine_rmsnorm(int dtype, const void *y_e, const float *topk_w,
 
 // ---------------------------------------------------------------- MXFP4 weights
 int launch_mxfp4_quantize(const void *W, long long rows, int K, uint8_t *packed, uint8_t *scales, cudaStream_t st);
+int launch_mxfp8_quantize(const float *X, long long rows, int K, uint8_t *codes, uint8_t *scales, cudaStream_t st);
 
 // ---------------------------------------------------------------- backward (bf16 type)
 // Intermediates of a forward call that the backward reads (views into its workspace).

@@ -40,6 +40,7 @@
 #include "ptx.cuh"
 #include "tc_gemm.h"
 #include "tcgen05.cuh"
+#include "mx.cuh"
 #include "tmap.h"
 
 namespace slmoe {
@@ -79,8 +80,9 @@ constexpr int EPI_BF16 = 0, EPI_GLU = 1, EPI_F32 = 3;
 // Backward epilogues: dense SiTU-GLU derivative (rows = tokens); grouped (rows = features):
 // fp32 gate|up pre-activations, fp32 transposed store, SiTU-GLU derivative.
 constexpr int EPI_DGLU = 4, EPI_GU32 = 5, EPI_F32T = 6, EPI_DGLU_T = 7;
-// f16 store (the MXFP4 layer's latent activations).
-constexpr int EPI_F16 = 8;
+// MXFP8 store (the MXFP4 layer's latent activations): codes [rows, N] and E8M0 scales
+// [rows, N / 32], N a multiple of 32.
+constexpr int EPI_MX8 = 8;
 // Operand majorness of the dense kernel (template MAJ): bit 0 = A MN-major, bit 1 = B MN-major.
 // An MN-major operand is stored [K rows, M (or N) columns]; TMA loads it in 64 x 64 boxes.
 constexpr int A_MN = 1, B_MN = 2;
@@ -119,6 +121,8 @@ struct DenseArgs {
     __nv_bfloat16 *dgu;
     long long ld_dgu;
     float dbeta1, dbeta2;
+    uint8_t *scales;       // EPI_MX8: block scales, ld_scales bytes per row
+    long long ld_scales;
 };
 
 // Tile order of the dense kernel: bands of DENSE_BAND row tiles, rows fastest inside a band,
@@ -331,27 +335,28 @@ __global__ void __launch_bounds__(DenseCfg<BN, EPI, PACC>::THREADS, 1) dense_ker
             const int n0 = tn * Cfg::BN_OUT;
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + sub * Cfg::ACC;
             const bool row_ok = row < a.M;
-            if (EPI == EPI_F16) {
-                __half *C = static_cast<__half *>(a.C) + (long long)row * a.ldc;
+            if (EPI == EPI_MX8) {
+                // 32-column chunks: one MXFP8 block of this thread's row per chunk
+                uint8_t *C = static_cast<uint8_t *>(a.C) + (long long)row * a.ldc;
+                uint8_t *S = a.scales + (long long)row * a.ld_scales;
 #pragma unroll 1
-                for (int c = 0; c < BN; c += 16) {
-                    uint32_t r[16];
-                    TMEM_LD16(tb + c, r);
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t r0[16], r1[16];
+                    TMEM_LD16(tb + c, r0);
+                    TMEM_LD16(tb + c + 16, r1);
                     tmem_wait_ld();
                     const int n = n0 + c;
-                    if (row_ok) {
-                        if (n + 16 <= a.N) {
-                            uint32_t w[8];
+                    if (row_ok && n < a.N) {
+                        float v[32];
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                __half2 hv = __floats2half2_rn(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-                                w[i] = *reinterpret_cast<uint32_t *>(&hv);
-                            }
-                            *reinterpret_cast<uint4 *>(C + n) = make_uint4(w[0], w[1], w[2], w[3]);
-                            *reinterpret_cast<uint4 *>(C + n + 8) = make_uint4(w[4], w[5], w[6], w[7]);
-                        } else {
-                            for (int i = 0; i < 16 && n + i < a.N; ++i) C[n + i] = __float2half_rn(__uint_as_float(r[i]));
+                        for (int i = 0; i < 16; ++i) {
+                            v[i] = __uint_as_float(r0[i]);
+                            v[16 + i] = __uint_as_float(r1[i]);
                         }
+                        uint32_t w[8];
+                        S[n >> 5] = (uint8_t)mx8_quant32(v, w);
+                        *reinterpret_cast<uint4 *>(C + n) = make_uint4(w[0], w[1], w[2], w[3]);
+                        *reinterpret_cast<uint4 *>(C + n + 16) = make_uint4(w[4], w[5], w[6], w[7]);
                     }
                 }
             } else if (EPI == EPI_BF16) {
@@ -733,24 +738,12 @@ done:
 constexpr int G_GATHER_THREADS = 128;
 constexpr int G_TQ = 4;                           // item queue slots
 
-// FP4: the weights arrive as packed MXFP4 through a ring of their own, 128 bytes per row (four
-// 64-wide K blocks: whole L2 lines) per raw stage, in the 128-byte swizzle; four dequantising
-// warps (one per TMEM lane quadrant) turn each K block into f16 and store it straight into
-// tensor memory, where the MMA takes its A operand: the tile never passes through shared
-// memory.  Two A stages live in the TMEM columns beside the accumulator (192..255 and
-// 448..511; a pass holds at most 192 tokens, so the accumulator uses columns below 192 and
-// 256..447).
-template <bool DBUF, bool FP4 = false>
+template <bool DBUF>
 struct GCfg {
     static constexpr int NSUB = 2;
     static constexpr int PASS = DBUF ? 128 : GROUPED_PASS;   // tokens per pass
     static constexpr int A_BYTES = NSUB * 128 * 128;
-    static constexpr int A_STAGES = FP4 ? 2 : (DBUF ? 5 : 4);  // 160 KB / 128 KB of weights in flight
-    static constexpr int A_SMEM_STAGES = FP4 ? 0 : A_STAGES;  // FP4: the A stages are in TMEM
-    static constexpr int RAW_KB = 4;                        // K blocks per raw stage
-    static constexpr int RAW_BYTES = NSUB * 128 * 32 * RAW_KB;
-    static constexpr int RAW_STAGES = FP4 ? 4 : 0;
-    static constexpr int DQ_WARPS = FP4 ? 4 : 0;
+    static constexpr int A_STAGES = DBUF ? 5 : 4;            // 160 KB / 128 KB of weights in flight
     static constexpr int B_BYTES = PASS * 128;
     static constexpr int B_STAGES = 4;
     static constexpr int NBUF = DBUF ? 2 : 1;
@@ -759,10 +752,8 @@ struct GCfg {
     // drains, so it gets two warps per TMEM lane quadrant; the double-buffered one overlaps
     static constexpr int EPI_WARPS = DBUF ? 4 : 8;
     static constexpr int GATHER_WARP0 = 2 + EPI_WARPS;
-    static constexpr int DQ_WARP0 = GATHER_WARP0 + 4;
-    // TMA, MMA, epilogue, 4 gather warps (+ 4 dequantising warps)
-    static constexpr int THREADS = (2 + EPI_WARPS + 4 + DQ_WARPS) * 32;
-    static constexpr int SMEM = A_SMEM_STAGES * A_BYTES + B_STAGES * B_BYTES + RAW_STAGES * RAW_BYTES + 1024 + 512;
+    static constexpr int THREADS = (2 + EPI_WARPS + 4) * 32;   // TMA, MMA, epilogue, 4 gather warps
+    static constexpr int SMEM = A_STAGES * A_BYTES + B_STAGES * B_BYTES + 1024 + 512;
     static_assert(SMEM <= 232448, "shared memory");
 };
 
@@ -788,9 +779,16 @@ struct GroupedArgs {
     long long ld_gu;
     __nv_bfloat16 *dgu;   // EPI_DGLU_T: [dg | du] out, bf16 [rows, 2F]
     long long ld_dgu;
-    const uint8_t *a_scales;   // FP4: E8M0 block scales of the weight rows, a_scale_ld bytes per row
+    // MXFP4 layer (grouped_mx_kernel): E8M0 block scales of the weight rows (a_scale_ld bytes
+    // per row; rows at or past a_rows_total read scale 0), of the token rows (b_scale_ld bytes
+    // per row of b_src) and of the MXFP8 output rows (EPI_GLU: out_scale_ld bytes per row)
+    const uint8_t *a_scales;
     int a_scale_ld;
-    long long a_rows_total;    // FP4: rows of the whole weight tensor (rows past it read scale 0)
+    long long a_rows_total;
+    const uint8_t *b_scales;
+    int b_scale_ld;
+    uint8_t *out_scales;
+    int out_scale_ld;
 };
 
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *map, uint64_t *bar,
@@ -876,45 +874,16 @@ worklist_kernel(const int32_t *__restrict__ counts, const int32_t *__restrict__ 
 // weight in the backward): each 128-feature sub-tile is two 64 x 64 TMA boxes; a_rows_pe is then
 // the K rows per expert, a_fb_stride the features per block and a_sub1 the second sub-tile's
 // feature offset.
-// f16 bits of 2^e: normal for e >= -14, subnormal down to 2^-24, 0 below, infinity above 15.
-__device__ __forceinline__ uint32_t f16_pow2(int e) {
-    if (e > 15) return 0x7C00u;
-    if (e >= -14) return (uint32_t)(e + 15) << 10;
-    if (e >= -24) return 1u << (e + 24);
-    return 0u;
-}
-// Four FP4 E2M1 codes (one per byte nibble pair: 8 codes in a word) -> 8 f16 scaled by s (f16x2).
-__device__ __forceinline__ uint4 dequant8(uint32_t w, uint32_t s2) {
-    uint32_t h[4];
-    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
-        : "r"(w));
-#pragma unroll
-    for (int i = 0; i < 4; ++i) asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(h[i]) : "r"(s2));
-    return make_uint4(h[0], h[1], h[2], h[3]);
-}
-// Instruction descriptor, kind::f16 with f16 A and B (K-major), fp32 D, shape M x N.
-__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
-    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-template <int EPI, bool DBUF, bool AMN = false, bool FP4 = false>
-__global__ void __launch_bounds__(GCfg<DBUF, FP4>::THREADS, 1) grouped_kernel(const __grid_constant__ CUtensorMap wmap,
-                                                                    const GroupedArgs a) {
-    using Cfg = GCfg<DBUF, FP4>;
+template <int EPI, bool DBUF, bool AMN = false>
+__global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                               const GroupedArgs a) {
+    using Cfg = GCfg<DBUF>;
     constexpr int AST = Cfg::A_STAGES, BST = Cfg::B_STAGES, NBUF = Cfg::NBUF, SUB1 = Cfg::SUB1_COL;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;
-    uint8_t *sB = smem + Cfg::A_SMEM_STAGES * Cfg::A_BYTES;
-    uint8_t *sRaw = sB + BST * Cfg::B_BYTES;
-    int4 *q_items = reinterpret_cast<int4 *>(sRaw + Cfg::RAW_STAGES * Cfg::RAW_BYTES);
-    constexpr int RST = Cfg::RAW_STAGES > 0 ? Cfg::RAW_STAGES : 1;
+    uint8_t *sB = smem + AST * Cfg::A_BYTES;
+    int4 *q_items = reinterpret_cast<int4 *>(sB + BST * Cfg::B_BYTES);
     uint64_t *q_full = reinterpret_cast<uint64_t *>(q_items + G_TQ);
     uint64_t *q_empty = q_full + G_TQ;
     uint64_t *a_full = q_empty + G_TQ;
@@ -924,9 +893,7 @@ __global__ void __launch_bounds__(GCfg<DBUF, FP4>::THREADS, 1) grouped_kernel(co
     uint64_t *tfull = b_empty + BST;
     uint64_t *tempty = tfull + NBUF;
     uint64_t *mma_drain = tempty + NBUF;
-    uint64_t *raw_full = mma_drain + 1;        // FP4 only
-    uint64_t *raw_empty = raw_full + RST;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(raw_empty + RST);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_drain + 1);
     volatile WaitCtl *abort_flag = reinterpret_cast<volatile WaitCtl *>(tmem_slot + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -937,16 +904,11 @@ __global__ void __launch_bounds__(GCfg<DBUF, FP4>::THREADS, 1) grouped_kernel(co
         mbar_init(mma_drain, 1);
         for (int s = 0; s < G_TQ; ++s) {
             mbar_init(&q_full[s], 1);
-            // MMA thread, epilogue, gather (and dequantising) warps
-            mbar_init(&q_empty[s], 1 + Cfg::EPI_WARPS + 4 + Cfg::DQ_WARPS);
+            mbar_init(&q_empty[s], 1 + Cfg::EPI_WARPS + 4);   // MMA thread, epilogue, gather warps
         }
         for (int s = 0; s < AST; ++s) {
-            mbar_init(&a_full[s], FP4 ? Cfg::DQ_WARPS : 1);
+            mbar_init(&a_full[s], 1);
             mbar_init(&a_empty[s], 1);
-        }
-        for (int s = 0; s < Cfg::RAW_STAGES; ++s) {
-            mbar_init(&raw_full[s], 1);
-            mbar_init(&raw_empty[s], Cfg::DQ_WARPS);
         }
         for (int s = 0; s < BST; ++s) {
             mbar_init(&b_full[s], G_GATHER_THREADS);
@@ -998,19 +960,6 @@ __global__ void __launch_bounds__(GCfg<DBUF, FP4>::THREADS, 1) grouped_kernel(co
             const int fb = it.y & 0xffff;
             const bool multi = (it.y >> 16) != 0;
             const int row0 = it.x * a.a_rows_pe + fb * a.a_fb_stride;
-            if (FP4) {             // packed MXFP4 rows into the raw ring, 128 bytes (4 K blocks) per row
-                const int ngroups = (a.kblocks + Cfg::RAW_KB - 1) / Cfg::RAW_KB;
-                for (int rg = 0; rg < ngroups; ++rg) {
-                    if (!mbar_wait(&raw_empty[stage], phase ^ 1, abort_flag)) goto done;
-                    mbar_expect_tx(&raw_full[stage], Cfg::RAW_BYTES);
-                    const uint32_t sr = su32(sRaw + stage * Cfg::RAW_BYTES);
-                    tma_load_2d_hint(sr, &wmap, &raw_full[stage], rg * 128, row0, pol_first);
-                    tma_load_2d_hint(sr + Cfg::RAW_BYTES / 2, &wmap, &raw_full[stage], rg * 128, row0 + a.a_sub1,
-                                     pol_first);
-                    if (++stage == Cfg::RAW_STAGES) { stage = 0; phase ^= 1; p_wrapped = true; }
-                }
-                continue;
-            }
             for (int kb = 0; kb < a.kblocks; ++kb) {
                 if (!mbar_wait(&a_empty[stage], phase ^ 1, abort_flag)) goto done;
                 mbar_expect_tx(&a_full[stage], Cfg::A_BYTES);
@@ -1041,8 +990,7 @@ __global__ void __launch_bounds__(GCfg<DBUF, FP4>::THREADS, 1) grouped_kernel(co
             int4 it;
             if (!pop(qs, qp, it, false)) goto done;
             if (it.w < 0) break;
-            const uint32_t idesc = (FP4 ? idesc_f16(128, (it.w + 15) & ~15) : idesc_bf16(128, (it.w + 15) & ~15)) |
-                                   (AMN ? (1u << 15) : 0u);
+            const uint32_t idesc = idesc_bf16(128, (it.w + 15) & ~15) | (AMN ? (1u << 15) : 0u);
             if (!mbar_wait(&tempty[buf], tph ^ 1, abort_flag)) goto done;
             tc_after();
             const uint32_t d = tmem_base + buf * 256;
@@ -1051,17 +999,13 @@ __global__ void __launch_bounds__(GCfg<DBUF, FP4>::THREADS, 1) grouped_kernel(co
                 if (!mbar_wait(&b_full[bs], bph, abort_flag)) goto done;
                 fence_proxy_async();
                 tc_after();
-                const uint32_t sa = su32(sA + (FP4 ? 0 : as) * Cfg::A_BYTES);
+                const uint32_t sa = su32(sA + as * Cfg::A_BYTES);
                 const uint32_t sb = su32(sB + bs * Cfg::B_BYTES);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
                     const uint64_t bd = sdesc(sb + kk * 32);
-                    if (FP4) {     // A from TMEM: 8 columns (16 f16 values) per K = 16 step
-                        const uint32_t ta = tmem_base + (as == 0 ? 192u : 448u) + kk * 8;
-                        umma_ts(d, ta, bd, idesc, acc);
-                        umma_ts(d + SUB1, ta + 32, bd, idesc, acc);
-                    } else if (AMN) {
+                    if (AMN) {
                         umma(d, mn_desc(sa + kk * 2048, 8192), bd, idesc, acc);
                         umma(d + SUB1, mn_desc(sa + 128 * 128 + kk * 2048, 8192), bd, idesc, acc);
                     } else {
@@ -1114,10 +1058,7 @@ __global__ void __launch_bounds__(GCfg<DBUF, FP4>::THREADS, 1) grouped_kernel(co
                             const float hv = situ_glu_fast(__uint_as_float(g[j]), __uint_as_float(v[j]), ib1, a.beta1,
                                                            ib2, a.beta2);
                             const long long at = ((long long)it.z + c + j) * a.out_ld + f;
-                            if (FP4)   // the MXFP4 layer keeps the routed experts' activations in f16
-                                static_cast<__half *>(a.out)[at] = __float2half_rn(hv);
-                            else
-                                static_cast<__nv_bfloat16 *>(a.out)[at] = __float2bfloat16_rn(hv);
+                            static_cast<__nv_bfloat16 *>(a.out)[at] = __float2bfloat16_rn(hv);
                         }
                     }
                 } else {
@@ -1167,78 +1108,6 @@ __global__ void __launch_bounds__(GCfg<DBUF, FP4>::THREADS, 1) grouped_kernel(co
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[buf]);
             if (++buf == NBUF) { buf = 0; tph ^= 1; }
-        }
-    } else if (FP4 && warp >= Cfg::DQ_WARP0) {
-        // ------------------------------------------------ MXFP4 -> f16 (4 warps): the warp of
-        // TMEM lane quadrant q turns rows 32q .. 32q + 31 of both 128-row sub-tiles of a stage
-        // into f16 and stores them into the stage's TMEM columns (row = lane, two f16 values
-        // per column, K order).  A stage needs two scale bytes per row (2-byte aligned: a row
-        // holds K/32 bytes, K a multiple of 64); they are loaded 8 stages ahead.
-        const int t = (warp & 3) * 32 + lane;              // the row of this thread
-        const uint32_t tq = tmem_base + ((uint32_t)((warp & 3) * 32) << 16);
-        int qs = 0, rs = 0, as = 0;
-        uint32_t qp = 0, rph = 0, aph = 0;
-        for (;;) {
-            int4 it;
-            if (!pop(qs, qp, it, true)) goto done;
-            if (it.w < 0) break;
-            const int fb = it.y & 0xffff;
-            const long long wrow0 = (long long)it.x * a.a_rows_pe + fb * a.a_fb_stride + t;
-            const uint16_t *sc0 = reinterpret_cast<const uint16_t *>(a.a_scales + wrow0 * a.a_scale_ld);
-            const uint16_t *sc1 = reinterpret_cast<const uint16_t *>(a.a_scales + (wrow0 + a.a_sub1) * a.a_scale_ld);
-            // a feature block may run past the last expert's rows: TMA fills those weight rows
-            // with zeros, and their scales are not read
-            const bool in0 = wrow0 < a.a_rows_total, in1 = wrow0 + a.a_sub1 < a.a_rows_total;
-            uint32_t qa[8], qb[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                qa[i] = (in0 && i < a.kblocks) ? sc0[i] : 0u;
-                qb[i] = (in1 && i < a.kblocks) ? sc1[i] : 0u;
-            }
-            for (int kb = 0; kb < a.kblocks; ++kb) {
-                const uint32_t cur0 = qa[0], cur1 = qb[0];
-#pragma unroll
-                for (int i = 0; i < 7; ++i) {
-                    qa[i] = qa[i + 1];
-                    qb[i] = qb[i + 1];
-                }
-                qa[7] = (in0 && kb + 8 < a.kblocks) ? sc0[kb + 8] : 0u;
-                qb[7] = (in1 && kb + 8 < a.kblocks) ? sc1[kb + 8] : 0u;
-                const int j = kb % Cfg::RAW_KB;               // K block inside the raw stage
-                if (j == 0 && !mbar_wait(&raw_full[rs], rph, abort_flag)) goto done;
-                if (!mbar_wait(&a_empty[as], aph ^ 1, abort_flag)) goto done;
-                tc_after();
-                const uint8_t *raw = sRaw + rs * Cfg::RAW_BYTES;
-#pragma unroll
-                for (int sub = 0; sub < 2; ++sub) {
-                    const uint32_t cs = sub ? cur1 : cur0;     // bytes 2 kb (low) and 2 kb + 1
-                    const uint32_t s0 = f16_pow2((int)(cs & 0xFF) - 127), s1 = f16_pow2((int)(cs >> 8) - 127);
-                    const uint32_t s0x2 = s0 | (s0 << 16), s1x2 = s1 | (s1 << 16);
-                    // row t of the sub-tile: 128 bytes in the 128-byte swizzle (16-byte chunk q of
-                    // the row at position q ^ (t % 8)); this K block is chunks 2j and 2j + 1
-                    const uint8_t *rrow = raw + sub * (Cfg::RAW_BYTES / 2) + (t >> 3) * 1024 + (t & 7) * 128;
-                    const uint4 p0 = *reinterpret_cast<const uint4 *>(rrow + (((2 * j) ^ (t & 7)) << 4));
-                    const uint4 p1 = *reinterpret_cast<const uint4 *>(rrow + (((2 * j + 1) ^ (t & 7)) << 4));
-                    const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-                    uint32_t v[32];
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {   // words c = K values 8c .. 8c + 7
-                        const uint4 h = dequant8(words[c], c < 4 ? s0x2 : s1x2);
-                        v[4 * c] = h.x; v[4 * c + 1] = h.y; v[4 * c + 2] = h.z; v[4 * c + 3] = h.w;
-                    }
-                    tmem_st32(tq + (as == 0 ? 192u : 448u) + 32 * sub, v);
-                }
-                tmem_wait_st();
-                tc_before();
-                __syncwarp();
-                const bool raw_done = j == Cfg::RAW_KB - 1 || kb == a.kblocks - 1;
-                if (lane == 0) {
-                    if (raw_done) mbar_arrive(&raw_empty[rs]);
-                    mbar_arrive(&a_full[as]);
-                }
-                if (raw_done && ++rs == Cfg::RAW_STAGES) { rs = 0; rph ^= 1; }
-                if (++as == AST) { as = 0; aph ^= 1; }
-            }
         }
     } else if (warp >= Cfg::GATHER_WARP0) {
         // ------------------------------------------------ token-row gather (cp.async, kept in L2)
@@ -1290,9 +1159,352 @@ done:
     __syncthreads();
     if (abort_flag->abort) {   // every role has stopped: let copies and MMAs in flight finish
         if (warp == 0 && lane == 0) {
-            if (FP4) drain_ring(raw_full, Cfg::RAW_STAGES, p_stage, p_phase, p_wrapped);
-            else drain_ring(a_full, AST, p_stage, p_phase, p_wrapped);
+            drain_ring(a_full, AST, p_stage, p_phase, p_wrapped);
         }
+        if (warp == 1 && lane == 0) {
+            umma_commit(mma_drain);
+            mbar_wait_drain(mma_drain, 0);
+        }
+        __syncthreads();
+    }
+    if (warp == 1) {
+        tc_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+    if (threadIdx.x == 0 && abort_flag->abort && a.status) atomicExch(&a.status[ST_TIMEOUT], 1);
+}
+
+// ---------------------------------------------------------------- grouped, MXFP4 x MXFP8
+// The routed experts of the MXFP4 layer on the block-scaled tensor cores (kind::mxf8f6f4):
+// the same work items, queue, weight ring and token gather as grouped_kernel, with K blocks
+// of 128 (one 128-byte swizzled row of E4M3 tokens; four K = 32 MMAs per sub-tile).  The
+// weights stream packed (64 bytes per row and K block) and TMA expands them into one byte per
+// E2M1 value in shared memory (the 16U4_ALIGN16B type: 16 values in each 16-byte chunk, whose
+// completion counts the packed bytes).  Four scale warps, one per TMEM lane quadrant, write
+// each stage's E8M0 scales into tensor memory where the MMA reads them: a stage slot of 16
+// columns above the accumulator (192 + 16 s) holds the weight rows' scales of sub-tile 0
+// (columns +0..3: lane quadrant q reads column +q), of sub-tile 1 (+4..7) and the tokens'
+// scales (+8..13: token n at lane n % 32 of every quadrant, column +8 + n / 32), four K = 32
+// steps to a 32-bit column.  EPI_GLU writes h as MXFP8: a warp's 32 lanes are 32 consecutive
+// features of one token, one block, so the block maximum is a warp reduction.
+template <int EPI>
+struct MxCfg {
+    static constexpr int NSUB = 2;
+    static constexpr int PASS = GROUPED_PASS;          // tokens per pass (<= 256: 8 scale columns)
+    static constexpr int KB = 128;                     // K per stage
+    static constexpr int A_BYTES = NSUB * 128 * KB;    // one byte per value in shared memory
+    static constexpr int A_TX = A_BYTES / 2;           // packed bytes the TMA counts
+    static constexpr int A_STAGES = 4;
+    static constexpr int B_BYTES = PASS * KB;
+    static constexpr int B_STAGES = 4;
+    static constexpr int SUB1_COL = 256;
+    static constexpr int SF_COL = 192;                 // stage slots: SF_COL + 16 s, s < A_STAGES
+    static constexpr int EPI_WARPS = 8;
+    static constexpr int GATHER_WARP0 = 2 + EPI_WARPS;
+    static constexpr int SF_WARP0 = GATHER_WARP0 + 4;
+    static constexpr int THREADS = (SF_WARP0 + 4) * 32;  // TMA, MMA, epilogue, gather, scale warps
+    static constexpr int SMEM = A_STAGES * A_BYTES + B_STAGES * B_BYTES + 1024 + 512;
+    static_assert(SMEM <= 232448, "shared memory");
+    static_assert(PASS <= SF_COL && SF_COL + 16 * A_STAGES <= SUB1_COL && SUB1_COL + PASS <= 512, "TMEM columns");
+};
+
+template <int EPI>
+__global__ void __launch_bounds__(MxCfg<EPI>::THREADS, 1) grouped_mx_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                                           const GroupedArgs a) {
+    using Cfg = MxCfg<EPI>;
+    constexpr int AST = Cfg::A_STAGES, BST = Cfg::B_STAGES, SUB1 = Cfg::SUB1_COL;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + AST * Cfg::A_BYTES;
+    int4 *q_items = reinterpret_cast<int4 *>(sB + BST * Cfg::B_BYTES);
+    uint64_t *q_full = reinterpret_cast<uint64_t *>(q_items + G_TQ);
+    uint64_t *q_empty = q_full + G_TQ;
+    uint64_t *a_full = q_empty + G_TQ;
+    uint64_t *a_empty = a_full + AST;
+    uint64_t *sf_full = a_empty + AST;
+    uint64_t *b_full = sf_full + AST;
+    uint64_t *b_empty = b_full + BST;
+    uint64_t *tfull = b_empty + BST;
+    uint64_t *tempty = tfull + 1;
+    uint64_t *mma_drain = tempty + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_drain + 1);
+    volatile WaitCtl *abort_flag = reinterpret_cast<volatile WaitCtl *>(tmem_slot + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int p_stage = 0;                  // the weight producer's ring position, kept for the drain
+    uint32_t p_phase = 0;
+    bool p_wrapped = false;
+    if (threadIdx.x == 0) {
+        mbar_init(mma_drain, 1);
+        for (int s = 0; s < G_TQ; ++s) {
+            mbar_init(&q_full[s], 1);
+            mbar_init(&q_empty[s], 1 + Cfg::EPI_WARPS + 4 + 4);   // MMA thread, epilogue, gather, scale warps
+        }
+        for (int s = 0; s < AST; ++s) {
+            mbar_init(&a_full[s], 1);
+            mbar_init(&a_empty[s], 1);
+            mbar_init(&sf_full[s], 4);
+        }
+        for (int s = 0; s < BST; ++s) {
+            mbar_init(&b_full[s], G_GATHER_THREADS);
+            mbar_init(&b_empty[s], 1);
+        }
+        mbar_init(tfull, 1);
+        mbar_init(tempty, Cfg::EPI_WARPS);
+        wait_ctl_init(abort_flag, a.wait_limit_ns);
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, 512);
+    tc_before();
+    __syncthreads();
+    tc_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    auto pop = [&](int &qs, uint32_t &qp, int4 &it, bool warp_wide) -> bool {
+        if (!mbar_wait(&q_full[qs], qp, abort_flag)) return false;
+        it = q_items[qs];
+        if (warp_wide) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&q_empty[qs]);
+        } else {
+            mbar_arrive(&q_empty[qs]);
+        }
+        if (++qs == G_TQ) { qs = 0; qp ^= 1; }
+        return true;
+    };
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ item fetch + packed weights by TMA
+        const uint64_t pol_first = policy_evict_first();
+        const int n_items = *a.n_items;
+        int &stage = p_stage;
+        uint32_t &phase = p_phase;
+        int qs = 0;
+        uint32_t qp = 0;
+        for (;;) {
+            const int idx = atomicAdd(a.counter, 1);
+            const int4 it = idx < n_items ? a.items[idx] : make_int4(0, 0, 0, -1);
+            if (!mbar_wait(&q_empty[qs], qp ^ 1, abort_flag)) goto done;
+            q_items[qs] = it;
+            mbar_arrive(&q_full[qs]);
+            if (++qs == G_TQ) { qs = 0; qp ^= 1; }
+            if (it.w < 0) break;
+            const int fb = it.y & 0xffff;
+            const bool multi = (it.y >> 16) != 0;
+            const int row0 = it.x * a.a_rows_pe + fb * a.a_fb_stride;
+            for (int kb = 0; kb < a.kblocks; ++kb) {
+                if (!mbar_wait(&a_empty[stage], phase ^ 1, abort_flag)) goto done;
+                mbar_expect_tx(&a_full[stage], Cfg::A_TX);
+                const uint32_t sa = su32(sA + stage * Cfg::A_BYTES);
+                if (multi) {       // other passes of this tile run alongside: normal L2 policy
+                    tma_load_2d(sa, &wmap, &a_full[stage], kb * Cfg::KB, row0);
+                    tma_load_2d(sa + 128 * Cfg::KB, &wmap, &a_full[stage], kb * Cfg::KB, row0 + a.a_sub1);
+                } else {           // streamed once
+                    tma_load_2d_hint(sa, &wmap, &a_full[stage], kb * Cfg::KB, row0, pol_first);
+                    tma_load_2d_hint(sa + 128 * Cfg::KB, &wmap, &a_full[stage], kb * Cfg::KB, row0 + a.a_sub1,
+                                     pol_first);
+                }
+                if (++stage == AST) { stage = 0; phase ^= 1; p_wrapped = true; }
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------ MMA issuer
+        int as = 0, bs = 0, qs = 0;
+        uint32_t aph = 0, bph = 0, tph = 0, qp = 0;
+        for (;;) {
+            int4 it;
+            if (!pop(qs, qp, it, false)) goto done;
+            if (it.w < 0) break;
+            const int Np = (it.w + 15) & ~15;
+            if (!mbar_wait(tempty, tph ^ 1, abort_flag)) goto done;
+            tc_after();
+            const uint32_t d = tmem_base;
+            for (int kb = 0; kb < a.kblocks; ++kb) {
+                if (!mbar_wait(&a_full[as], aph, abort_flag)) goto done;
+                if (!mbar_wait(&sf_full[as], aph, abort_flag)) goto done;
+                if (!mbar_wait(&b_full[bs], bph, abort_flag)) goto done;
+                fence_proxy_async();
+                tc_after();
+                const uint32_t sa = su32(sA + as * Cfg::A_BYTES);
+                const uint32_t sb = su32(sB + bs * Cfg::B_BYTES);
+                const uint32_t sf = tmem_base + Cfg::SF_COL + 16 * as;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+                    const uint32_t idesc = idesc_mx(128, Np, kk);
+                    const uint64_t bd = sdesc(sb + kk * 32);
+                    umma_mx(d, sdesc(sa + kk * 32), bd, idesc, sf, sf + 8, acc);
+                    umma_mx(d + SUB1, sdesc(sa + 128 * Cfg::KB + kk * 32), bd, idesc, sf + 4, sf + 8, acc);
+                }
+                umma_commit(&a_empty[as]);
+                umma_commit(&b_empty[bs]);
+                if (++as == AST) { as = 0; aph ^= 1; }
+                if (++bs == BST) { bs = 0; bph ^= 1; }
+            }
+            umma_commit(tfull);
+            tph ^= 1;
+        }
+    } else if (warp >= 2 && warp < Cfg::GATHER_WARP0) {
+        // ------------------------------------------------ epilogue: warp w reads TMEM lane
+        // quadrant w % 4; the two warps of a quadrant take alternate 16-column chunks
+        constexpr int WPQ = Cfg::EPI_WARPS / 4;
+        const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const int lf = q * 32 + lane;                 // feature inside a 128-row sub-tile
+        const float ib1 = 1.0f / a.beta1, ib2 = 1.0f / a.beta2;
+        int qs = 0;
+        uint32_t tph = 0, qp = 0;
+        for (;;) {
+            int4 it;
+            if (!pop(qs, qp, it, true)) goto done;
+            if (it.w < 0) break;
+            const int fb = it.y & 0xffff, N = it.w, Np = (N + 15) & ~15;
+            if (!mbar_wait(tfull, tph, abort_flag)) goto done;
+            tc_after();
+            const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16);
+            for (int c = half * 16; c < Np; c += 16 * WPQ) {
+                uint32_t r0[16], r1[16];
+                TMEM_LD16(tb + c, r0);
+                TMEM_LD16(tb + SUB1 + c, r1);
+                tmem_wait_ld();
+                if (EPI == EPI_GLU) {
+                    // sub-tiles = gate and up rows of feature f; h -> MXFP8 over the warp's 32
+                    // features (one block), token by token
+                    const int f = fb * 128 + lf;
+                    uint8_t *codes = static_cast<uint8_t *>(a.out) + f;
+                    uint32_t my_scale = 0;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float hv = situ_glu_fast(__uint_as_float(r0[j]), __uint_as_float(r1[j]), ib1, a.beta1,
+                                                       ib2, a.beta2);
+                        const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv)));
+                        const int e = mx8_exp(__uint_as_float(amax));
+                        const uint32_t code = e4m3x2(hv * mx8_inv_scale(e), 0.f) & 0xFFu;
+                        if (c + j < N) codes[((long long)it.z + c + j) * a.out_ld] = (uint8_t)code;
+                        if (lane == j) my_scale = (uint32_t)(e + 127);
+                    }
+                    if (lane < 16 && c + lane < N)
+                        a.out_scales[((long long)it.z + c + lane) * a.out_scale_ld + (f >> 5)] = (uint8_t)my_scale;
+                } else {
+                    // expert down: features fb * 256 + lf and fb * 256 + 128 + lf, y_e in bf16
+                    const int f = fb * 256 + lf;
+                    const bool ok = f < a.out_cols, ok1 = f + 128 < a.out_cols;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        if (c + j >= N) continue;
+                        __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) + ((long long)it.z + c + j) * a.out_ld + f;
+                        if (ok) orow[0] = __float2bfloat16_rn(__uint_as_float(r0[j]));
+                        if (ok1) orow[128] = __float2bfloat16_rn(__uint_as_float(r1[j]));
+                    }
+                }
+            }
+            tc_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty);
+            tph ^= 1;
+        }
+    } else if (warp >= Cfg::GATHER_WARP0 && warp < Cfg::SF_WARP0) {
+        // ------------------------------------------------ token-row gather (cp.async, kept in L2)
+        const uint64_t pol = policy_evict_last();
+        const int gt = threadIdx.x - Cfg::GATHER_WARP0 * 32;   // 0..127
+        const int ch = gt & 7;                         // 16-byte chunk of the 128-byte row
+        const int rsub = gt >> 3;                      // rows rsub, rsub + 16, ...
+        const uint8_t *bsrc = reinterpret_cast<const uint8_t *>(a.b_src);
+        int stage = 0, qs = 0;
+        uint32_t phase = 0, qp = 0;
+        for (;;) {
+            int4 it;
+            if (!pop(qs, qp, it, true)) {
+                cp_async_wait_all();
+                goto done;
+            }
+            if (it.w < 0) break;
+            const int N = it.w, Np = (N + 15) & ~15;
+            constexpr int RJ = Cfg::PASS / 16;
+            const uint8_t *src[RJ];
+#pragma unroll
+            for (int j = 0; j < RJ; ++j) {
+                const int r = rsub + 16 * j;
+                long long row = 0;
+                if (r < N) row = a.b_index ? a.b_index[it.z + r] : (long long)(it.z + r);
+                src[j] = bsrc + row * a.b_ld + ch * 16;
+            }
+            for (int kb = 0; kb < a.kblocks; ++kb) {
+                if (!mbar_wait(&b_empty[stage], phase ^ 1, abort_flag)) {
+                    cp_async_wait_all();
+                    goto done;
+                }
+                const uint32_t sb = su32(sB + stage * Cfg::B_BYTES);
+#pragma unroll
+                for (int j = 0; j < RJ; ++j) {
+                    const int r = rsub + 16 * j;
+                    if (r < Np) {
+                        const uint32_t dst = sb + r * 128 + ((ch ^ (r & 7)) << 4);
+                        cp_async16_hint(dst, src[j] + kb * Cfg::KB, r < N ? 16u : 0u, pol);
+                    }
+                }
+                cp_async_arrive_noinc(&b_full[stage]);
+                if (++stage == BST) { stage = 0; phase ^= 1; }
+            }
+        }
+        cp_async_wait_all();
+    } else if (warp >= Cfg::SF_WARP0) {
+        // ------------------------------------------------ block scales into tensor memory: the
+        // warp of lane quadrant q writes, for each stage, the weight-row scales of its 32 rows
+        // of both sub-tiles and every token's scales (the same in each quadrant)
+        const int q = warp & 3;
+        const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16);
+        constexpr int NJ = Cfg::PASS / 32;
+        int qs = 0, as = 0;
+        uint32_t qp = 0, aph = 0;
+        for (;;) {
+            int4 it;
+            if (!pop(qs, qp, it, true)) goto done;
+            if (it.w < 0) break;
+            const int fb = it.y & 0xffff, N = it.w;
+            const long long wrow0 = (long long)it.x * a.a_rows_pe + fb * a.a_fb_stride + q * 32 + lane;
+            const long long wrow1 = wrow0 + a.a_sub1;
+            // a feature block may run past the last expert's rows: TMA fills those weight rows
+            // with zeros, and their scales are not read
+            const uint32_t *sa0 = wrow0 < a.a_rows_total
+                                      ? reinterpret_cast<const uint32_t *>(a.a_scales + wrow0 * a.a_scale_ld) : nullptr;
+            const uint32_t *sa1 = wrow1 < a.a_rows_total
+                                      ? reinterpret_cast<const uint32_t *>(a.a_scales + wrow1 * a.a_scale_ld) : nullptr;
+            const uint32_t *sbr[NJ];
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) {
+                const int n = 32 * j + lane;
+                sbr[j] = nullptr;
+                if (n < N) {
+                    const long long row = a.b_index ? a.b_index[it.z + n] : (long long)(it.z + n);
+                    sbr[j] = reinterpret_cast<const uint32_t *>(a.b_scales + row * a.b_scale_ld);
+                }
+            }
+            for (int kb = 0; kb < a.kblocks; ++kb) {
+                const uint32_t w0 = sa0 ? __ldg(sa0 + kb) : 0u;
+                const uint32_t w1 = sa1 ? __ldg(sa1 + kb) : 0u;
+                uint32_t wb[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+                for (int j = 0; j < NJ; ++j) wb[j] = sbr[j] ? __ldg(sbr[j] + kb) : 0u;
+                if (!mbar_wait(&a_empty[as], aph ^ 1, abort_flag)) goto done;
+                tc_after();
+                const uint32_t col = Cfg::SF_COL + 16 * as;
+                tmem_st1(tq + col + q, w0);
+                tmem_st1(tq + col + 4 + q, w1);
+                tmem_st8(tq + col + 8, wb);
+                tmem_wait_st();
+                tc_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sf_full[as]);
+                if (++as == AST) { as = 0; aph ^= 1; }
+            }
+        }
+    }
+done:
+    __syncthreads();
+    if (abort_flag->abort) {   // every role has stopped: let copies and MMAs in flight finish
+        if (warp == 0 && lane == 0) drain_ring(a_full, AST, p_stage, p_phase, p_wrapped);
         if (warp == 1 && lane == 0) {
             umma_commit(mma_drain);
             mbar_wait_drain(mma_drain, 0);
@@ -1370,10 +1582,20 @@ int launch_dense_bn(int bn, const TmaPack &maps, const DenseArgs &a, cudaStream_
     return bn == 64 ? launch_dense<64, EPI, 1>(maps, a, st) : launch_dense<256, EPI, 1>(maps, a, st);
 }
 
-template <int EPI, bool DBUF, bool AMN = false, bool FP4 = false>
+template <int EPI>
+int launch_grouped_mx(const CUtensorMap &wmap, const GroupedArgs &a, cudaStream_t st) {
+    using Cfg = MxCfg<EPI>;
+    auto kern = grouped_mx_kernel<EPI>;
+    int rc = set_smem(kern, Cfg::SMEM);
+    if (rc) return rc;
+    kern<<<sm_count(), Cfg::THREADS, Cfg::SMEM, st>>>(wmap, a);
+    return check_launch("grouped_mx_kernel");
+}
+
+template <int EPI, bool DBUF, bool AMN = false>
 int launch_grouped(const CUtensorMap &wmap, const GroupedArgs &a, cudaStream_t st) {
-    using Cfg = GCfg<DBUF, FP4>;
-    auto kern = grouped_kernel<EPI, DBUF, AMN, FP4>;
+    using Cfg = GCfg<DBUF>;
+    auto kern = grouped_kernel<EPI, DBUF, AMN>;
     int rc = set_smem(kern, Cfg::SMEM);
     if (rc) return rc;
     kern<<<sm_count(), Cfg::THREADS, Cfg::SMEM, st>>>(wmap, a);
@@ -1471,8 +1693,13 @@ int tc_forward_front(const slmoe_config *c, const void *x, const slmoe_weights *
         DenseArgs a = {};
         a.M = T; a.N = dl; a.nseg = 1; a.kblocks[0] = (d + 63) / 64;
         a.C = f.x_lat; a.ldc = dl; a.status = f.status; a.counter = f.counters + 1;
-        if (c->dtype == SLMOE_MXFP4) rc = launch_dense_bn<EPI_F16>(bn, maps, a, st);
-        else rc = launch_dense_bn<EPI_BF16>(bn, maps, a, st);
+        if (c->dtype == SLMOE_MXFP4) {   // MXFP8 codes [T, dl], then their scales [T, dl / 32]
+            a.scales = static_cast<uint8_t *>(f.x_lat) + (size_t)T * dl;
+            a.ld_scales = dl / 32;
+            rc = launch_dense_bn<EPI_MX8>(bn, maps, a, st);
+        } else {
+            rc = launch_dense_bn<EPI_BF16>(bn, maps, a, st);
+        }
         if (rc) return rc;
     }
     stage_event(3, st);
@@ -1506,6 +1733,51 @@ int tc_worklists(const slmoe_config *c, const TcForward &f, cudaStream_t st) {
     return check_launch("worklist");
 }
 
+// The routed experts of the MXFP4 layer: gate|up + SiTU-GLU (h as MXFP8) and down on the
+// block-scaled tensor cores, K blocks of 128.  Packed weights [rows, K / 2] bytes through TMA
+// (16U4_ALIGN16B: K a multiple of 128, the base 32-byte aligned); x_lat and h are MXFP8 codes
+// [rows, K] followed by their scales [rows, K / 32] in their workspace regions.
+static int mx_routed_experts(const slmoe_config *c, const slmoe_weights *w, const TcForward &f,
+                             cudaStream_t st) {
+    const int T = c->T, dl = c->d_latent, E = c->E, I = c->I;
+    const long long Tk = (long long)T * c->k;
+    uint8_t *xq = static_cast<uint8_t *>(f.x_lat), *hq = static_cast<uint8_t *>(f.h);
+    int rc;
+    {   // gate|up + SiTU-GLU: h[perm row] = GLU(W13[e] x_lat[token]), MXFP8 along I
+        CUtensorMap wm;
+        if ((rc = tmap_encode_fp4(&wm, w->W13, (long long)E * 2 * I, dl))) return rc;
+        GroupedArgs a = {};
+        a.kblocks = dl / 128;
+        a.a_rows_pe = 2 * I; a.a_sub1 = I; a.a_fb_stride = 128;
+        a.items = f.items1; a.n_items = f.counters + 8; a.counter = f.counters + 6;
+        a.b_index = f.perm;
+        a.b_src = reinterpret_cast<const __nv_bfloat16 *>(xq); a.b_ld = dl; a.b_K = dl;
+        a.out = hq; a.out_ld = I; a.out_cols = I;
+        a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
+        a.a_scales = w->W13_scale; a.a_scale_ld = dl / 32; a.a_rows_total = (long long)E * 2 * I;
+        a.b_scales = xq + (size_t)T * dl; a.b_scale_ld = dl / 32;
+        a.out_scales = hq + (size_t)Tk * I; a.out_scale_ld = I / 32;
+        if ((rc = launch_grouped_mx<EPI_GLU>(wm, a, st))) return rc;
+    }
+    stage_event(4, st);
+    {   // down: y_e[row] = W2[e] h[row] (bf16)
+        CUtensorMap wm;
+        if ((rc = tmap_encode_fp4(&wm, w->W2, (long long)E * dl, I))) return rc;
+        GroupedArgs a = {};
+        a.kblocks = I / 128;
+        a.a_rows_pe = dl; a.a_sub1 = 128; a.a_fb_stride = 256;
+        a.items = f.items2; a.n_items = f.counters + 9; a.counter = f.counters + 7;
+        a.b_index = nullptr;
+        a.b_src = reinterpret_cast<const __nv_bfloat16 *>(hq); a.b_ld = I; a.b_K = I;
+        a.out = f.y_e; a.out_ld = dl; a.out_cols = dl;
+        a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
+        a.a_scales = w->W2_scale; a.a_scale_ld = I / 32; a.a_rows_total = (long long)E * dl;
+        a.b_scales = hq + (size_t)Tk * I; a.b_scale_ld = I / 32;
+        if ((rc = launch_grouped_mx<EPI_BF16>(wm, a, st))) return rc;
+    }
+    return SLMOE_OK;
+}
+
 int tc_forward_back(const slmoe_config *c, const slmoe_weights *w, const TcForward &f, void *y,
                     cudaStream_t st) {
     const int T = c->T, d = c->d, dl = c->d_latent, E = c->E, k = c->k, I = c->I;
@@ -1515,45 +1787,36 @@ int tc_forward_back(const slmoe_config *c, const slmoe_weights *w, const TcForwa
     using bf = __nv_bfloat16;
 
     (void)E;
-    const bool fp4 = c->dtype == SLMOE_MXFP4;
-    {   // routed experts, gate|up + SiTU-GLU: h[perm row] = GLU(W13[e] x_lat[token])
-        CUtensorMap wm;
-        if (fp4) rc = tmap_encode_2d(&wm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w->W13, (long long)E * 2 * I, dl / 2,
-                                     dl / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-        else rc = make_map(&wm, w->W13, (long long)E * 2 * I, dl, dl, 128);
-        if (rc) return rc;
-        GroupedArgs a = {};
-        a.kblocks = (dl + 63) / 64;
-        a.a_rows_pe = 2 * I; a.a_sub1 = I; a.a_fb_stride = 128;
-        a.items = f.items1; a.n_items = f.counters + 8; a.counter = f.counters + 6;
-        a.b_index = f.perm;
-        a.b_src = static_cast<const bf *>(f.x_lat); a.b_ld = dl; a.b_K = dl;
-        a.out = f.h; a.out_ld = I; a.out_cols = I;
-        a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
-        a.a_scales = w->W13_scale; a.a_scale_ld = dl / 32; a.a_rows_total = (long long)E * 2 * I;
-        if (fp4) rc = launch_grouped<EPI_GLU, false, false, true>(wm, a, st);
-        else rc = launch_grouped<EPI_GLU, false>(wm, a, st);
-        if (rc) return rc;
-    }
-    stage_event(4, st);
-    {   // routed experts, down: y_e[row] = W2[e] h[row]
-        CUtensorMap wm;
-        if (fp4) rc = tmap_encode_2d(&wm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w->W2, (long long)E * dl, I / 2, I / 2,
-                                     128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-        else rc = make_map(&wm, w->W2, (long long)E * dl, I, I, 128);
-        if (rc) return rc;
-        GroupedArgs a = {};
-        a.kblocks = (I + 63) / 64;
-        a.a_rows_pe = dl; a.a_sub1 = 128; a.a_fb_stride = 256;
-        a.items = f.items2; a.n_items = f.counters + 9; a.counter = f.counters + 7;
-        a.b_index = nullptr;
-        a.b_src = static_cast<const bf *>(f.h); a.b_ld = I; a.b_K = I;
-        a.out = f.y_e; a.out_ld = dl; a.out_cols = dl;
-        a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
-        a.a_scales = w->W2_scale; a.a_scale_ld = I / 32; a.a_rows_total = (long long)E * dl;
-        if (fp4) rc = launch_grouped<EPI_BF16, false, false, true>(wm, a, st);
-        else rc = launch_grouped<EPI_BF16, false>(wm, a, st);
-        if (rc) return rc;
+    if (c->dtype == SLMOE_MXFP4) {
+        if ((rc = mx_routed_experts(c, w, f, st))) return rc;
+    } else {
+        {   // routed experts, gate|up + SiTU-GLU: h[perm row] = GLU(W13[e] x_lat[token])
+            CUtensorMap wm;
+            if ((rc = make_map(&wm, w->W13, (long long)E * 2 * I, dl, dl, 128))) return rc;
+            GroupedArgs a = {};
+            a.kblocks = (dl + 63) / 64;
+            a.a_rows_pe = 2 * I; a.a_sub1 = I; a.a_fb_stride = 128;
+            a.items = f.items1; a.n_items = f.counters + 8; a.counter = f.counters + 6;
+            a.b_index = f.perm;
+            a.b_src = static_cast<const bf *>(f.x_lat); a.b_ld = dl; a.b_K = dl;
+            a.out = f.h; a.out_ld = I; a.out_cols = I;
+            a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
+            if ((rc = launch_grouped<EPI_GLU, false>(wm, a, st))) return rc;
+        }
+        stage_event(4, st);
+        {   // routed experts, down: y_e[row] = W2[e] h[row]
+            CUtensorMap wm;
+            if ((rc = make_map(&wm, w->W2, (long long)E * dl, I, I, 128))) return rc;
+            GroupedArgs a = {};
+            a.kblocks = (I + 63) / 64;
+            a.a_rows_pe = dl; a.a_sub1 = 128; a.a_fb_stride = 256;
+            a.items = f.items2; a.n_items = f.counters + 9; a.counter = f.counters + 7;
+            a.b_index = nullptr;
+            a.b_src = static_cast<const bf *>(f.h); a.b_ld = I; a.b_K = I;
+            a.out = f.y_e; a.out_ld = dl; a.out_cols = dl;
+            a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
+            if ((rc = launch_grouped<EPI_BF16, false>(wm, a, st))) return rc;
+        }
     }
     stage_event(5, st);
     (void)Tk;

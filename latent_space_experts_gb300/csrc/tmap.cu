@@ -41,4 +41,19 @@ int tmap_encode_2d(CUtensorMap *m, CUtensorMapDataType dtype, int elem_bytes, co
     return SLMOE_OK;
 }
 
+int tmap_encode_fp4(CUtensorMap *m, const void *base, long long rows, long long K) {
+    int rc = get_encode();
+    if (rc) return rc;
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
+    cuuint32_t box[2] = {128, 128};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void *>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(SLMOE_ECUDA, "cuTensorMapEncodeTiled (FP4) failed (%d): rows %lld K %lld", (int)r, rows, K);
+    return SLMOE_OK;
+}
+
 }  // namespace slmoe

@@ -152,7 +152,7 @@ def rmsnorm(c, gamma, eps=EPS):
 
 
 def forward(inp, k, beta1=BETA1, beta2=BETA2, eps=EPS, forced_topk_idx=None, tokens=None,
-            mx_activations=False):
+            mx_activations=False, forced_mx=None):
     """One Stable LatentMoE layer (the FFN branch, no residual add) in fp64.
 
     inp: dict of the layer inputs (see ``synthetic.layer_inputs``).  ``tokens`` restricts
@@ -162,7 +162,11 @@ def forward(inp, k, beta1=BETA1, beta2=BETA2, eps=EPS, forced_topk_idx=None, tok
     ``mx_activations`` takes the layer with MXFP4 weights and MXFP8 activations ([SLMoE]
     训练基础设施): x_lat and each routed expert's h pass through MXFP8 (``mxfp8_round_trip``,
     blocks of 32 along d_latent and I) before they meet the expert weights; inp["W13"] /
-    inp["W2"] then hold the weights' dequantised values.
+    inp["W2"] then hold the weights' dequantised values.  ``forced_mx`` replaces the MXFP8
+    rounding decisions with given ones, as ``forced_topk_idx`` does the selection (a value
+    within floating-point error of a rounding midpoint has two valid codes): a dict with the
+    dequantised x_lat [T_all, d_latent], the dequantised h of every (token, slot) pair in
+    permutation order [T_all * k, I] and slot_pos [T_all, k] (the pair's row in that order).
 
     Returns a dict with scores, topk_idx, gates, gap, x_lat, c (the gate-weighted combine),
     z (after RMSNorm), y_routed (z projected up), y_shared and y.
@@ -189,13 +193,18 @@ def forward(inp, k, beta1=BETA1, beta2=BETA2, eps=EPS, forced_topk_idx=None, tok
     # routed experts in latent space, gate-weighted sum over the k chosen experts
     W13, W2 = inp["W13"], inp["W2"]
     d_lat = x_lat.shape[1]
-    x_in = mxfp8_round_trip(x_lat) if mx_activations else x_lat
+    if forced_mx is not None:
+        x_in = f64(forced_mx["x_lat"][tok])
+    else:
+        x_in = mxfp8_round_trip(x_lat) if mx_activations else x_lat
     c = np.zeros((T, d_lat))
     for e in np.unique(sel):
         tt, jj = np.nonzero(sel == e)
         gu = x_in[tt] @ f64(W13[int(e)]).T                 # [n, 2I]: gate rows first
         h = situ_glu(gu, beta1, beta2)
-        if mx_activations:
+        if forced_mx is not None:
+            h = f64(forced_mx["h"][np.asarray(forced_mx["slot_pos"])[tok[tt], jj]])
+        elif mx_activations:
             h = mxfp8_round_trip(h)
         y_e = h @ f64(W2[int(e)]).T                        # [n, d_latent]
         np.add.at(c, tt, gates[tt, jj][:, None] * y_e)

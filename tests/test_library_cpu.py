@@ -187,3 +187,23 @@ def test_topk_and_abort_check_validate_on_the_host(lib):
     assert lib.slmoe_wait_abort_check(None, 1000, None) == -1
     assert lib.slmoe_wait_abort_check(fake, 0, None) == -1
     assert lib.slmoe_wait_abort_check(fake, 10 ** 12, None) == -1
+
+
+@pytest.mark.parametrize("field,value,ok", [("d_latent", 320, False), ("I", 192, False), ("d_latent", 384, True),
+                                            ("I", 384, True)])
+def test_mxfp4_layer_needs_128_multiples(lib, field, value, ok):
+    """The MXFP4 layer reads K blocks of 128 (d_latent and I) on the block-scaled tensor cores."""
+    cfg = lse.config(synthetic.LAYERS["mid"], dtype=lse.MXFP4)
+    setattr(cfg, field, value)
+    assert (lib.slmoe_workspace_size(ctypes.byref(cfg)) > 0) == ok
+
+
+def test_mxfp8_quantize_validates_on_the_host(lib):
+    fake = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 4)
+    assert lib.slmoe_mxfp8_quantize(fake, 4, 48, fake, fake, None) == -1      # K not a multiple of 32
+    assert lib.slmoe_mxfp8_quantize(fake, -1, 32, fake, fake, None) == -1
+    assert lib.slmoe_mxfp8_quantize(None, 4, 32, fake, fake, None) == -1
+    assert lib.slmoe_mxfp8_quantize(odd, 4, 32, fake, fake, None) == -1
+    assert lib.slmoe_mxfp8_quantize(fake, 4, 32, fake, None, None) == -1
+    assert lib.slmoe_mxfp8_quantize(fake, 0, 32, fake, fake, None) == 0       # nothing to do

@@ -141,9 +141,12 @@ def test_scalar_loop_layer_matches_the_oracle():
     inp["W2"] = oracle.mxfp4_dequantize(*oracle.mxfp4_quantize(rng.normal(size=(E, dl, I)) / 8))
     ref = oracle.forward(inp, k, mx_activations=True)
     sel, gates = ref["topk_idx"], ref["gates"]
+    slot_pos = oracle.permutation(sel, E)[3]
+    forced = dict(x_lat=np.zeros((T, dl)), h=np.zeros((T * k, I)), slot_pos=slot_pos)
     for t in range(T):
         x_lat = [sum(inp["x"][t, i] * inp["W_in"][o, i] for i in range(d)) for o in range(dl)]
         x_q = oracle.mxfp8_round_trip(np.array(x_lat))
+        forced["x_lat"][t] = x_q
         c = [0.0] * dl
         for j in range(k):
             e = int(sel[t, j])
@@ -153,6 +156,12 @@ def test_scalar_loop_layer_matches_the_oracle():
                 u = sum(x_q[i] * inp["W13"][e][I + f, i] for i in range(dl))
                 h.append(4 * math.tanh(g / 4) / (1 + math.exp(-g)) * 25 * math.tanh(u / 25))
             h_q = oracle.mxfp8_round_trip(np.array(h))
+            forced["h"][slot_pos[t, j]] = h_q
             for o in range(dl):
                 c[o] += gates[t, j] * sum(h_q[f] * inp["W2"][e][o, f] for f in range(I))
         assert np.allclose(c, ref["c"][t], rtol=1e-12, atol=1e-12)
+    # the same decisions handed in as forced ones (rows of h in permutation order) give the same layer
+    again = oracle.forward(inp, k, forced_topk_idx=sel, forced_mx=forced)
+    assert np.allclose(again["y"], ref["y"], rtol=1e-12, atol=1e-12)
+    sub = oracle.forward(inp, k, forced_topk_idx=sel, forced_mx=forced, tokens=[2, 0])
+    assert np.allclose(sub["y"], ref["y"][[2, 0]], rtol=1e-12, atol=1e-12)
