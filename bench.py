@@ -584,7 +584,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="k3_prefill", choices=["k3_prefill", "k3_decode", "mid", "k3_slice", "k3_dense"])
+    ap.add_argument("--workload", default="k3_prefill", choices=["k3_prefill", "k3_decode", "mid", "k3_slice", "k3_decode_slice",
+                                                                     "k3_dense"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-tokens", type=int, default=None,
                     help="oracle tokens per reference step (default: the cpu_baseline sample)")

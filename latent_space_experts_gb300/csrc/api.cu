@@ -108,8 +108,9 @@ int make_layout(const slmoe_config *c, Layout *L) {
         const size_t Tk = T * k;
         const size_t nfb1 = (c->I + 127) / 128, nfb2 = (c->d_latent + 255) / 256;
         // per feature block at most E + ceil(T k / pass) passes (sum of ceil(n_e / pass))
-        L->items1 = take(nfb1 * (E + (Tk + GROUPED_PASS - 1) / GROUPED_PASS) * 16);
-        L->items2 = take(nfb2 * (E + (Tk + GROUPED_PASS - 1) / GROUPED_PASS) * 16);
+        const size_t pass = grouped_pass(c);
+        L->items1 = take(nfb1 * (E + (Tk + pass - 1) / pass) * 16);
+        L->items2 = take(nfb2 * (E + (Tk + pass - 1) / pass) * 16);
     }
     if (c->dtype != SLMOE_F32 && T <= (size_t)ROUTER_SPLITK_MAX_M)
         L->rt_split = take(ROUTER_SPLITK_MAX * T * E * 4);

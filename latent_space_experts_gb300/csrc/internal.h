@@ -73,6 +73,14 @@ constexpr int ROUTE_CHUNK = 16;  // tokens per top-k block / permutation chunk
 // Tokens per pass of the routed-expert GEMMs: an expert with n tokens makes ceil(n / pass)
 // work items per feature block, which also sizes the work lists in the workspace.
 constexpr int GROUPED_PASS = 192;
+// The MXFP4 layer's routed-expert GEMMs take short passes when the batch gives an expert few
+// tokens on average (decode): their small token stages leave shared memory for more weight
+// stages in flight.
+constexpr int MX_SHORT_PASS = 32, MX_LONG_PASS = 192;
+inline int grouped_pass(const slmoe_config *c) {
+    if (c->dtype != SLMOE_MXFP4) return GROUPED_PASS;
+    return (long long)c->T * c->k <= 8LL * c->E ? MX_SHORT_PASS : MX_LONG_PASS;
+}
 // The router of a batch of at most ROUTER_SPLITK_MAX_M tokens splits its K blocks over up to
 // ROUTER_SPLITK_MAX CTAs per tile (their fp32 partial logits live in the workspace).
 constexpr int ROUTER_SPLITK_MAX_M = 256;

@@ -1176,56 +1176,63 @@ done:
 
 // ---------------------------------------------------------------- grouped, MXFP4 x MXFP8
 // The routed experts of the MXFP4 layer on the block-scaled tensor cores (kind::mxf8f6f4):
-// the same work items, queue, weight ring and token gather as grouped_kernel, with K blocks
-// of 128 (one 128-byte swizzled row of E4M3 tokens; four K = 32 MMAs per sub-tile).  The
-// weights stream packed (64 bytes per row and K block) and TMA expands them into one byte per
-// E2M1 value in shared memory (the 16U4_ALIGN16B type: 16 values in each 16-byte chunk, whose
-// completion counts the packed bytes).  Four scale warps, one per TMEM lane quadrant, write
-// each stage's E8M0 scales into tensor memory where the MMA reads them: a stage slot of 16
-// columns above the accumulator (192 + 16 s) holds the weight rows' scales of sub-tile 0
-// (columns +0..3: lane quadrant q reads column +q), of sub-tile 1 (+4..7) and the tokens'
-// scales (+8..13: token n at lane n % 32 of every quadrant, column +8 + n / 32), four K = 32
-// steps to a 32-bit column.  EPI_GLU writes h as MXFP8: a warp's 32 lanes are 32 consecutive
-// features of one token, one block, so the block maximum is a warp reduction.
-template <int EPI>
+// the same work items and queue as grouped_kernel, with K blocks of 128 (four K = 32 MMAs per
+// sub-tile).  The MMA wants the E2M1 weights one byte per value: each 16-byte chunk of a
+// 128-byte (K = 128) row holds 16 values in its first 8 bytes, in the 128-byte swizzle, which
+// TMA writes from the packed rows itself (the 16U4_ALIGN16B type, whose completion counts the
+// packed bytes).  Its boxes are 64 bytes wide, and TMA moves about 0.18 box rows per clock per
+// SM (a probe: 64-byte rows stream at 4.2 TB/s whatever the ring depth, 128-byte rows at
+// 6.8-7.0 TB/s), which bounds this weight stream; packed 128-byte rows expanded by a warp in
+// shared memory, or 8-byte cp.async copies into the layout, both measured slower.  Four loader
+// warps gather the pass's token rows from L2 (16-byte cp.async; E4M3 codes, 128 bytes per row
+// and stage) into the same ring stage.  The same warps, one per TMEM lane quadrant, write each
+// stage's E8M0 scales into
+// tensor memory where the MMA reads them: a slot of 16 columns between the accumulators
+// (SF_COL + 16 s) holds the weight rows' scales of sub-tile 0 (columns +0..3: lane quadrant q
+// reads column +q), of sub-tile 1 (+4..7) and the tokens' scales (+8..13: token n at lane
+// n % 32 of every quadrant, column +8 + n / 32), four K = 32 steps to a 32-bit column.  EPI_GLU
+// writes h as MXFP8: a warp's 32 lanes are 32 consecutive features of one token, one block, so
+// the block maximum is a warp reduction.
+template <int EPI, int PASS_>
 struct MxCfg {
     static constexpr int NSUB = 2;
-    static constexpr int PASS = GROUPED_PASS;          // tokens per pass (<= 256: 8 scale columns)
+    static constexpr int PASS = PASS_;                 // tokens per pass (<= 192: scale columns)
     static constexpr int KB = 128;                     // K per stage
-    static constexpr int A_BYTES = NSUB * 128 * KB;    // one byte per value in shared memory
-    static constexpr int A_TX = A_BYTES / 2;           // packed bytes the TMA counts
-    static constexpr int A_STAGES = 4;
+    static constexpr int A_BYTES = NSUB * 128 * KB;    // one byte per weight value (half padding)
     static constexpr int B_BYTES = PASS * KB;
-    static constexpr int B_STAGES = 4;
+    static constexpr int STAGE = A_BYTES + B_BYTES;
+    // the weights' bytes in flight are 16 KB of HBM a stage: as many stages as fit
+    static constexpr int STAGES = (224 * 1024) / STAGE < 8 ? (224 * 1024) / STAGE : 8;
     static constexpr int SUB1_COL = 256;
-    static constexpr int SF_COL = 192;                 // stage slots: SF_COL + 16 s, s < A_STAGES
+    // scale slots of the stages: SF_COL + 16 s, between the two accumulators
+    static constexpr int SF_COL = PASS <= 64 ? 64 : PASS;
     static constexpr int EPI_WARPS = 8;
-    static constexpr int GATHER_WARP0 = 2 + EPI_WARPS;
-    static constexpr int SF_WARP0 = GATHER_WARP0 + 4;
-    static constexpr int THREADS = (SF_WARP0 + 4) * 32;  // TMA, MMA, epilogue, gather, scale warps
-    static constexpr int SMEM = A_STAGES * A_BYTES + B_STAGES * B_BYTES + 1024 + 512;
-    static_assert(SMEM <= 232448, "shared memory");
-    static_assert(PASS <= SF_COL && SF_COL + 16 * A_STAGES <= SUB1_COL && SUB1_COL + PASS <= 512, "TMEM columns");
+    static constexpr int LOAD_WARP0 = 2 + EPI_WARPS;
+    static constexpr int THREADS = (LOAD_WARP0 + 4) * 32;  // items + weights, MMA, epilogue, loaders
+    // after the ring: the item queue, the mbarriers (queue, weights, token rows, scales, stage
+    // free, accumulator, drain), the TMEM address and the wait state
+    static constexpr int TAIL = 16 * G_TQ + 8 * (2 * G_TQ + 4 * STAGES + 3) + 8 + 16;
+    static constexpr int SMEM = STAGES * STAGE + 1024 + TAIL;
+    static_assert(STAGES >= 3 && SMEM <= 232448, "shared memory");
+    static_assert(PASS <= SF_COL && SF_COL + 16 * STAGES <= SUB1_COL && SUB1_COL + PASS <= 512 && SF_COL % 16 == 0,
+                  "TMEM columns");
 };
 
-template <int EPI>
-__global__ void __launch_bounds__(MxCfg<EPI>::THREADS, 1) grouped_mx_kernel(const __grid_constant__ CUtensorMap wmap,
-                                                                           const GroupedArgs a) {
-    using Cfg = MxCfg<EPI>;
-    constexpr int AST = Cfg::A_STAGES, BST = Cfg::B_STAGES, SUB1 = Cfg::SUB1_COL;
+template <int EPI, int PASS>
+__global__ void __launch_bounds__(MxCfg<EPI, PASS>::THREADS, 1) grouped_mx_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                                                 const GroupedArgs a) {
+    using Cfg = MxCfg<EPI, PASS>;
+    constexpr int ST = Cfg::STAGES, SUB1 = Cfg::SUB1_COL;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sA = smem;
-    uint8_t *sB = smem + AST * Cfg::A_BYTES;
-    int4 *q_items = reinterpret_cast<int4 *>(sB + BST * Cfg::B_BYTES);
+    int4 *q_items = reinterpret_cast<int4 *>(smem + ST * Cfg::STAGE);
     uint64_t *q_full = reinterpret_cast<uint64_t *>(q_items + G_TQ);
     uint64_t *q_empty = q_full + G_TQ;
-    uint64_t *a_full = q_empty + G_TQ;
-    uint64_t *a_empty = a_full + AST;
-    uint64_t *sf_full = a_empty + AST;
-    uint64_t *b_full = sf_full + AST;
-    uint64_t *b_empty = b_full + BST;
-    uint64_t *tfull = b_empty + BST;
+    uint64_t *a_full = q_empty + G_TQ;      // a stage's weights have landed
+    uint64_t *full = a_full + ST;           // its token rows have landed
+    uint64_t *sf_full = full + ST;          // its scales are in tensor memory
+    uint64_t *empty = sf_full + ST;         // the MMAs that read it are done
+    uint64_t *tfull = empty + ST;
     uint64_t *tempty = tfull + 1;
     uint64_t *mma_drain = tempty + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_drain + 1);
@@ -1239,16 +1246,13 @@ __global__ void __launch_bounds__(MxCfg<EPI>::THREADS, 1) grouped_mx_kernel(cons
         mbar_init(mma_drain, 1);
         for (int s = 0; s < G_TQ; ++s) {
             mbar_init(&q_full[s], 1);
-            mbar_init(&q_empty[s], 1 + Cfg::EPI_WARPS + 4 + 4);   // MMA thread, epilogue, gather, scale warps
+            mbar_init(&q_empty[s], 1 + Cfg::EPI_WARPS + 4);   // MMA thread, epilogue, loader warps
         }
-        for (int s = 0; s < AST; ++s) {
+        for (int s = 0; s < ST; ++s) {
             mbar_init(&a_full[s], 1);
-            mbar_init(&a_empty[s], 1);
+            mbar_init(&full[s], G_GATHER_THREADS);
             mbar_init(&sf_full[s], 4);
-        }
-        for (int s = 0; s < BST; ++s) {
-            mbar_init(&b_full[s], G_GATHER_THREADS);
-            mbar_init(&b_empty[s], 1);
+            mbar_init(&empty[s], 1);
         }
         mbar_init(tfull, 1);
         mbar_init(tempty, Cfg::EPI_WARPS);
@@ -1275,11 +1279,11 @@ __global__ void __launch_bounds__(MxCfg<EPI>::THREADS, 1) grouped_mx_kernel(cons
     };
 
     if (warp == 0 && lane == 0) {
-        // ------------------------------------------------ item fetch + packed weights by TMA
+        // ------------------------------------------------ item fetch + weights by TMA
         const uint64_t pol_first = policy_evict_first();
         const int n_items = *a.n_items;
-        int &stage = p_stage;
-        uint32_t &phase = p_phase;
+        int &s = p_stage;
+        uint32_t &ph = p_phase;
         int qs = 0;
         uint32_t qp = 0;
         for (;;) {
@@ -1290,28 +1294,27 @@ __global__ void __launch_bounds__(MxCfg<EPI>::THREADS, 1) grouped_mx_kernel(cons
             mbar_arrive(&q_full[qs]);
             if (++qs == G_TQ) { qs = 0; qp ^= 1; }
             if (it.w < 0) break;
-            const int fb = it.y & 0xffff;
             const bool multi = (it.y >> 16) != 0;
-            const int row0 = it.x * a.a_rows_pe + fb * a.a_fb_stride;
+            const int row0 = it.x * a.a_rows_pe + (it.y & 0xffff) * a.a_fb_stride;
             for (int kb = 0; kb < a.kblocks; ++kb) {
-                if (!mbar_wait(&a_empty[stage], phase ^ 1, abort_flag)) goto done;
-                mbar_expect_tx(&a_full[stage], Cfg::A_TX);
-                const uint32_t sa = su32(sA + stage * Cfg::A_BYTES);
+                if (!mbar_wait(&empty[s], ph ^ 1, abort_flag)) goto done;
+                mbar_expect_tx(&a_full[s], Cfg::A_BYTES / 2);
+                const uint32_t sa = su32(smem + s * Cfg::STAGE);
                 if (multi) {       // other passes of this tile run alongside: normal L2 policy
-                    tma_load_2d(sa, &wmap, &a_full[stage], kb * Cfg::KB, row0);
-                    tma_load_2d(sa + 128 * Cfg::KB, &wmap, &a_full[stage], kb * Cfg::KB, row0 + a.a_sub1);
+                    tma_load_2d(sa, &wmap, &a_full[s], kb * Cfg::KB, row0);
+                    tma_load_2d(sa + 128 * Cfg::KB, &wmap, &a_full[s], kb * Cfg::KB, row0 + a.a_sub1);
                 } else {           // streamed once
-                    tma_load_2d_hint(sa, &wmap, &a_full[stage], kb * Cfg::KB, row0, pol_first);
-                    tma_load_2d_hint(sa + 128 * Cfg::KB, &wmap, &a_full[stage], kb * Cfg::KB, row0 + a.a_sub1,
+                    tma_load_2d_hint(sa, &wmap, &a_full[s], kb * Cfg::KB, row0, pol_first);
+                    tma_load_2d_hint(sa + 128 * Cfg::KB, &wmap, &a_full[s], kb * Cfg::KB, row0 + a.a_sub1,
                                      pol_first);
                 }
-                if (++stage == AST) { stage = 0; phase ^= 1; p_wrapped = true; }
+                if (++s == ST) { s = 0; ph ^= 1; p_wrapped = true; }
             }
         }
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------ MMA issuer
-        int as = 0, bs = 0, qs = 0;
-        uint32_t aph = 0, bph = 0, tph = 0, qp = 0;
+        int s = 0, qs = 0;
+        uint32_t ph = 0, tph = 0, qp = 0;
         for (;;) {
             int4 it;
             if (!pop(qs, qp, it, false)) goto done;
@@ -1321,14 +1324,14 @@ __global__ void __launch_bounds__(MxCfg<EPI>::THREADS, 1) grouped_mx_kernel(cons
             tc_after();
             const uint32_t d = tmem_base;
             for (int kb = 0; kb < a.kblocks; ++kb) {
-                if (!mbar_wait(&a_full[as], aph, abort_flag)) goto done;
-                if (!mbar_wait(&sf_full[as], aph, abort_flag)) goto done;
-                if (!mbar_wait(&b_full[bs], bph, abort_flag)) goto done;
+                if (!mbar_wait(&a_full[s], ph, abort_flag)) goto done;
+                if (!mbar_wait(&full[s], ph, abort_flag)) goto done;
+                if (!mbar_wait(&sf_full[s], ph, abort_flag)) goto done;
                 fence_proxy_async();
                 tc_after();
-                const uint32_t sa = su32(sA + as * Cfg::A_BYTES);
-                const uint32_t sb = su32(sB + bs * Cfg::B_BYTES);
-                const uint32_t sf = tmem_base + Cfg::SF_COL + 16 * as;
+                const uint32_t sa = su32(smem + s * Cfg::STAGE);
+                const uint32_t sb = sa + Cfg::A_BYTES;
+                const uint32_t sf = tmem_base + Cfg::SF_COL + 16 * s;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
@@ -1337,15 +1340,13 @@ __global__ void __launch_bounds__(MxCfg<EPI>::THREADS, 1) grouped_mx_kernel(cons
                     umma_mx(d, sdesc(sa + kk * 32), bd, idesc, sf, sf + 8, acc);
                     umma_mx(d + SUB1, sdesc(sa + 128 * Cfg::KB + kk * 32), bd, idesc, sf + 4, sf + 8, acc);
                 }
-                umma_commit(&a_empty[as]);
-                umma_commit(&b_empty[bs]);
-                if (++as == AST) { as = 0; aph ^= 1; }
-                if (++bs == BST) { bs = 0; bph ^= 1; }
+                umma_commit(&empty[s]);
+                if (++s == ST) { s = 0; ph ^= 1; }
             }
             umma_commit(tfull);
             tph ^= 1;
         }
-    } else if (warp >= 2 && warp < Cfg::GATHER_WARP0) {
+    } else if (warp >= 2 && warp < Cfg::LOAD_WARP0) {
         // ------------------------------------------------ epilogue: warp w reads TMEM lane
         // quadrant w % 4; the two warps of a quadrant take alternate 16-column chunks
         constexpr int WPQ = Cfg::EPI_WARPS / 4;
@@ -1404,15 +1405,22 @@ __global__ void __launch_bounds__(MxCfg<EPI>::THREADS, 1) grouped_mx_kernel(cons
             if (lane == 0) mbar_arrive(tempty);
             tph ^= 1;
         }
-    } else if (warp >= Cfg::GATHER_WARP0 && warp < Cfg::SF_WARP0) {
-        // ------------------------------------------------ token-row gather (cp.async, kept in L2)
-        const uint64_t pol = policy_evict_last();
-        const int gt = threadIdx.x - Cfg::GATHER_WARP0 * 32;   // 0..127
-        const int ch = gt & 7;                         // 16-byte chunk of the 128-byte row
-        const int rsub = gt >> 3;                      // rows rsub, rsub + 16, ...
+    } else if (warp >= Cfg::LOAD_WARP0) {
+        // ------------------------------------------------ loaders: per stage, the pass's token
+        // rows (16-byte copies from L2) and the scales
+        const uint64_t pol_last = policy_evict_last();
+        const int lt = threadIdx.x - Cfg::LOAD_WARP0 * 32;    // 0..127
+        const int ch = lt & 7;                         // 16-byte chunk of a token row
+        const int rsub = lt >> 3;                      // token rows rsub, rsub + 16, ...
+        const int q = warp & 3;
+        const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16);
         const uint8_t *bsrc = reinterpret_cast<const uint8_t *>(a.b_src);
-        int stage = 0, qs = 0;
-        uint32_t phase = 0, qp = 0;
+        const uint32_t *bw = reinterpret_cast<const uint32_t *>(a.b_scales);
+        constexpr int RJ = Cfg::PASS / 16;
+        constexpr int NJ = Cfg::PASS / 32;
+        constexpr int PF = 2;                          // scale words loaded PF stages ahead
+        int s = 0, qs = 0;
+        uint32_t ph = 0, qp = 0;
         for (;;) {
             int4 it;
             if (!pop(qs, qp, it, true)) {
@@ -1420,8 +1428,8 @@ __global__ void __launch_bounds__(MxCfg<EPI>::THREADS, 1) grouped_mx_kernel(cons
                 goto done;
             }
             if (it.w < 0) break;
-            const int N = it.w, Np = (N + 15) & ~15;
-            constexpr int RJ = Cfg::PASS / 16;
+            const int fb = it.y & 0xffff, N = it.w, Np = (N + 15) & ~15;
+            const long long wrow0 = (long long)it.x * a.a_rows_pe + fb * a.a_fb_stride;
             const uint8_t *src[RJ];
 #pragma unroll
             for (int j = 0; j < RJ; ++j) {
@@ -1430,81 +1438,80 @@ __global__ void __launch_bounds__(MxCfg<EPI>::THREADS, 1) grouped_mx_kernel(cons
                 if (r < N) row = a.b_index ? a.b_index[it.z + r] : (long long)(it.z + r);
                 src[j] = bsrc + row * a.b_ld + ch * 16;
             }
-            for (int kb = 0; kb < a.kblocks; ++kb) {
-                if (!mbar_wait(&b_empty[stage], phase ^ 1, abort_flag)) {
-                    cp_async_wait_all();
-                    goto done;
-                }
-                const uint32_t sb = su32(sB + stage * Cfg::B_BYTES);
-#pragma unroll
-                for (int j = 0; j < RJ; ++j) {
-                    const int r = rsub + 16 * j;
-                    if (r < Np) {
-                        const uint32_t dst = sb + r * 128 + ((ch ^ (r & 7)) << 4);
-                        cp_async16_hint(dst, src[j] + kb * Cfg::KB, r < N ? 16u : 0u, pol);
-                    }
-                }
-                cp_async_arrive_noinc(&b_full[stage]);
-                if (++stage == BST) { stage = 0; phase ^= 1; }
-            }
-        }
-        cp_async_wait_all();
-    } else if (warp >= Cfg::SF_WARP0) {
-        // ------------------------------------------------ block scales into tensor memory: the
-        // warp of lane quadrant q writes, for each stage, the weight-row scales of its 32 rows
-        // of both sub-tiles and every token's scales (the same in each quadrant)
-        const int q = warp & 3;
-        const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16);
-        constexpr int NJ = Cfg::PASS / 32;
-        int qs = 0, as = 0;
-        uint32_t qp = 0, aph = 0;
-        for (;;) {
-            int4 it;
-            if (!pop(qs, qp, it, true)) goto done;
-            if (it.w < 0) break;
-            const int fb = it.y & 0xffff, N = it.w;
-            const long long wrow0 = (long long)it.x * a.a_rows_pe + fb * a.a_fb_stride + q * 32 + lane;
-            const long long wrow1 = wrow0 + a.a_sub1;
-            // a feature block may run past the last expert's rows: TMA fills those weight rows
-            // with zeros, and their scales are not read
-            const uint32_t *sa0 = wrow0 < a.a_rows_total
-                                      ? reinterpret_cast<const uint32_t *>(a.a_scales + wrow0 * a.a_scale_ld) : nullptr;
-            const uint32_t *sa1 = wrow1 < a.a_rows_total
-                                      ? reinterpret_cast<const uint32_t *>(a.a_scales + wrow1 * a.a_scale_ld) : nullptr;
-            const uint32_t *sbr[NJ];
+            const long long srow0 = wrow0 + q * 32 + lane;
+            const long long srow1 = srow0 + a.a_sub1;
+            const uint32_t *sa0 = srow0 < a.a_rows_total
+                                      ? reinterpret_cast<const uint32_t *>(a.a_scales + srow0 * a.a_scale_ld) : nullptr;
+            const uint32_t *sa1 = srow1 < a.a_rows_total
+                                      ? reinterpret_cast<const uint32_t *>(a.a_scales + srow1 * a.a_scale_ld) : nullptr;
+            int sbr[NJ];                               // token 32 j + lane's scale words at bw + sbr[j]
 #pragma unroll
             for (int j = 0; j < NJ; ++j) {
                 const int n = 32 * j + lane;
-                sbr[j] = nullptr;
-                if (n < N) {
-                    const long long row = a.b_index ? a.b_index[it.z + n] : (long long)(it.z + n);
-                    sbr[j] = reinterpret_cast<const uint32_t *>(a.b_scales + row * a.b_scale_ld);
+                sbr[j] = -1;
+                if (n < N) sbr[j] = (a.b_index ? a.b_index[it.z + n] : it.z + n) * (a.b_scale_ld >> 2);
+            }
+            // a ring of PF register slots (static indices: the loop is unrolled by PF) hides the
+            // L2 latency of the gathered scale loads
+            uint32_t qa0[PF], qa1[PF], qb[PF][NJ];
+#pragma unroll
+            for (int i = 0; i < PF; ++i) {
+                const bool in = i < a.kblocks;
+                qa0[i] = (in && sa0) ? __ldg(sa0 + i) : 0u;
+                qa1[i] = (in && sa1) ? __ldg(sa1 + i) : 0u;
+#pragma unroll
+                for (int j = 0; j < NJ; ++j) qb[i][j] = (in && sbr[j] >= 0) ? __ldg(bw + sbr[j] + i) : 0u;
+            }
+            for (int kb0 = 0; kb0 < a.kblocks; kb0 += PF) {
+#pragma unroll
+                for (int u = 0; u < PF; ++u) {
+                    const int kb = kb0 + u;
+                    if (kb < a.kblocks) {
+                        if (!mbar_wait(&empty[s], ph ^ 1, abort_flag)) {
+                            cp_async_wait_all();
+                            goto done;
+                        }
+                        const uint32_t sb = su32(smem + s * Cfg::STAGE) + Cfg::A_BYTES;
+#pragma unroll
+                        for (int j = 0; j < RJ; ++j) {
+                            const int r = rsub + 16 * j;
+                            if (r < Np) {
+                                const uint32_t dst = sb + r * 128 + ((ch ^ (r & 7)) << 4);
+                                cp_async16_hint(dst, src[j] + kb * Cfg::KB, r < N ? 16u : 0u, pol_last);
+                            }
+                        }
+                        cp_async_arrive_noinc(&full[s]);
+                        const uint32_t w0 = qa0[u], w1 = qa1[u];
+                        uint32_t wb[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+                        for (int j = 0; j < NJ; ++j) wb[j] = qb[u][j];
+                        const int kn = kb + PF;
+                        const bool in = kn < a.kblocks;
+                        qa0[u] = (in && sa0) ? __ldg(sa0 + kn) : 0u;
+                        qa1[u] = (in && sa1) ? __ldg(sa1 + kn) : 0u;
+#pragma unroll
+                        for (int j = 0; j < NJ; ++j) qb[u][j] = (in && sbr[j] >= 0) ? __ldg(bw + sbr[j] + kn) : 0u;
+                        tc_after();
+                        const uint32_t col = Cfg::SF_COL + 16 * s;
+                        tmem_st1(tq + col + q, w0);
+                        tmem_st1(tq + col + 4 + q, w1);
+                        tmem_st8(tq + col + 8, wb);
+                        tmem_wait_st();
+                        tc_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&sf_full[s]);
+                        if (++s == ST) { s = 0; ph ^= 1; }
+                    }
                 }
             }
-            for (int kb = 0; kb < a.kblocks; ++kb) {
-                const uint32_t w0 = sa0 ? __ldg(sa0 + kb) : 0u;
-                const uint32_t w1 = sa1 ? __ldg(sa1 + kb) : 0u;
-                uint32_t wb[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-#pragma unroll
-                for (int j = 0; j < NJ; ++j) wb[j] = sbr[j] ? __ldg(sbr[j] + kb) : 0u;
-                if (!mbar_wait(&a_empty[as], aph ^ 1, abort_flag)) goto done;
-                tc_after();
-                const uint32_t col = Cfg::SF_COL + 16 * as;
-                tmem_st1(tq + col + q, w0);
-                tmem_st1(tq + col + 4 + q, w1);
-                tmem_st8(tq + col + 8, wb);
-                tmem_wait_st();
-                tc_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sf_full[as]);
-                if (++as == AST) { as = 0; aph ^= 1; }
-            }
         }
+        cp_async_wait_all();
     }
 done:
     __syncthreads();
-    if (abort_flag->abort) {   // every role has stopped: let copies and MMAs in flight finish
-        if (warp == 0 && lane == 0) drain_ring(a_full, AST, p_stage, p_phase, p_wrapped);
+    if (abort_flag->abort) {   // every role has stopped: let copies and MMAs in flight finish (the
+                               // loaders waited for their own copies)
+        if (warp == 0 && lane == 0) drain_ring(a_full, ST, p_stage, p_phase, p_wrapped);
         if (warp == 1 && lane == 0) {
             umma_commit(mma_drain);
             mbar_wait_drain(mma_drain, 0);
@@ -1582,10 +1589,10 @@ int launch_dense_bn(int bn, const TmaPack &maps, const DenseArgs &a, cudaStream_
     return bn == 64 ? launch_dense<64, EPI, 1>(maps, a, st) : launch_dense<256, EPI, 1>(maps, a, st);
 }
 
-template <int EPI>
+template <int EPI, int PASS>
 int launch_grouped_mx(const CUtensorMap &wmap, const GroupedArgs &a, cudaStream_t st) {
-    using Cfg = MxCfg<EPI>;
-    auto kern = grouped_mx_kernel<EPI>;
+    using Cfg = MxCfg<EPI, PASS>;
+    auto kern = grouped_mx_kernel<EPI, PASS>;
     int rc = set_smem(kern, Cfg::SMEM);
     if (rc) return rc;
     kern<<<sm_count(), Cfg::THREADS, Cfg::SMEM, st>>>(wmap, a);
@@ -1726,10 +1733,10 @@ int tc_worklists(const slmoe_config *c, const TcForward &f, cudaStream_t st) {
     const int E = c->E, I = c->I, dl = c->d_latent;
     const long long Tk = (long long)c->T * c->k;
     const int nfb1 = (I + 127) / 128, nfb2 = (dl + 255) / 256;
-    const long long Tk_items = (Tk + GROUPED_PASS - 1) / GROUPED_PASS;
-    worklist_kernel<<<1, 1024, 0, st>>>(f.counts, f.offsets, E, nfb1, GCfg<false>::PASS, f.items1, nfb2,
-                                        GCfg<false>::PASS, f.items2, f.counters + 8,
-                                        (int)(nfb1 * (E + Tk_items)), (int)(nfb2 * (E + Tk_items)));
+    const int pass = grouped_pass(c);
+    const long long Tk_items = (Tk + pass - 1) / pass;
+    worklist_kernel<<<1, 1024, 0, st>>>(f.counts, f.offsets, E, nfb1, pass, f.items1, nfb2, pass, f.items2,
+                                        f.counters + 8, (int)(nfb1 * (E + Tk_items)), (int)(nfb2 * (E + Tk_items)));
     return check_launch("worklist");
 }
 
@@ -1757,7 +1764,9 @@ static int mx_routed_experts(const slmoe_config *c, const slmoe_weights *w, cons
         a.a_scales = w->W13_scale; a.a_scale_ld = dl / 32; a.a_rows_total = (long long)E * 2 * I;
         a.b_scales = xq + (size_t)T * dl; a.b_scale_ld = dl / 32;
         a.out_scales = hq + (size_t)Tk * I; a.out_scale_ld = I / 32;
-        if ((rc = launch_grouped_mx<EPI_GLU>(wm, a, st))) return rc;
+        rc = grouped_pass(c) == MX_SHORT_PASS ? launch_grouped_mx<EPI_GLU, MX_SHORT_PASS>(wm, a, st)
+                                              : launch_grouped_mx<EPI_GLU, MX_LONG_PASS>(wm, a, st);
+        if (rc) return rc;
     }
     stage_event(4, st);
     {   // down: y_e[row] = W2[e] h[row] (bf16)
@@ -1773,7 +1782,9 @@ static int mx_routed_experts(const slmoe_config *c, const slmoe_weights *w, cons
         a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
         a.a_scales = w->W2_scale; a.a_scale_ld = I / 32; a.a_rows_total = (long long)E * dl;
         a.b_scales = hq + (size_t)Tk * I; a.b_scale_ld = I / 32;
-        if ((rc = launch_grouped_mx<EPI_BF16>(wm, a, st))) return rc;
+        rc = grouped_pass(c) == MX_SHORT_PASS ? launch_grouped_mx<EPI_BF16, MX_SHORT_PASS>(wm, a, st)
+                                              : launch_grouped_mx<EPI_BF16, MX_LONG_PASS>(wm, a, st);
+        if (rc) return rc;
     }
     return SLMOE_OK;
 }

@@ -15,7 +15,7 @@ int tmap_encode_2d(CUtensorMap *m, CUtensorMapDataType dtype, int elem_bytes, co
 
 // Packed FP4 codes: rows x K values, K / 2 bytes per row (K a multiple of 128, the base 32-byte
 // aligned), read in boxes of 128 values x 128 rows with the 128-byte swizzle and expanded in
-// shared memory to one byte per value (16 values in each 16-byte chunk).
+// shared memory to one byte per value (16 values in the first half of each 16-byte chunk).
 int tmap_encode_fp4(CUtensorMap *m, const void *base, long long rows, long long K);
 
 }  // namespace slmoe

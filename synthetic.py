@@ -67,6 +67,10 @@ LAYERS = {
     # and about the same tokens per expert (1170 * 16 / 128 = 146), 1.5 GB on the device
     "k3_slice": LayerShape("k3_slice", T=1170, d=7168, d_latent=3584, E=128, k=16, I=512,
                            n_shared=2, I_shared=2048, dtype="bf16", mu_std=0.5),
+    # a 1/7 slice of the K3 decode batch for profiler captures: about 2.3 tokens per expert
+    # (18 * 16 / 128), as in the 128-token batch over 896 experts
+    "k3_decode_slice": LayerShape("k3_decode_slice", T=18, d=7168, d_latent=3584, E=128, k=16, I=512,
+                                  n_shared=2, I_shared=2048, dtype="bf16", mu_std=0.5),
     # the K3 prefill batch and widths with 16 experts (top-2): the dense GEMMs (router,
     # down-projection, shared experts, up-projection) at full size, 1.6 GB on the device
     "k3_dense": LayerShape("k3_dense", T=8192, d=7168, d_latent=3584, E=16, k=2, I=512,

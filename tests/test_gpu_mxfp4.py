@@ -192,11 +192,19 @@ def check_stages(shp, ref_inp, views, topk, rows_per_expert=None):
 
 
 @pytest.mark.parametrize("over", [dict(T=300, d=512), dict(T=129, E=40, k=3, I=128, d=512),
-                                  dict(T=600, E=2, k=1, I=384, d_latent=384, d=512), dict(T=1, d=512)])
+                                  dict(T=600, E=2, k=1, I=384, d_latent=384, d=512), dict(T=1, d=512),
+                                  dict(T=512, E=128, k=2, d=512, hot=True)])
 def test_mxfp4_layer_matches_the_oracle(over):
+    """Long (192-token) passes, and short (32-token) passes when the batch gives an expert at
+    most 8 tokens on average (T = 1; the hot case, where every token also picks expert 5,
+    so that it takes 16 short passes)."""
     need_gpu()
+    over = dict(over)
+    hot = over.pop("hot", False)
     shp = synthetic.shape_with("mid", **over)
     inp = to_dev(synthetic.layer_inputs(shp, seed=12))
+    if hot:
+        inp["bias"][5] += 10.0
     q, ref_inp = mxfp4_layer(inp)
     y, topk, views = run_mxfp4(shp, q)
     check_stages(shp, ref_inp, views, topk)
