@@ -2,30 +2,18 @@
 //
 // The gradient is the chain rule of the forward (K3 architecture write-up, SiTU激活优化 /
 // 归一化策略调整; the concept note's 训练基础设施 trains this layer), run against the
-// intermediates a forward call leaves in its workspace.  Every contraction goes through one
-// tcgen05 kernel, bgemm_kernel:
-//
-//  * a tile is 128 rows (the MMA's M) x up to 256 columns (N), K in blocks of 64;
-//  * four loader warps fill a 4-stage ring with cp.async (16-byte chunks, zero-filled past
-//    the edges), writing each operand either K-major (a row of 64 K values per 128-byte line)
-//    or MN-major (a line of 64 M or N values per K row), both in the 128-byte swizzle, so
-//    dgrad and wgrad read W and the activations as they are stored, without transposes;
-//  * one thread issues tcgen05.mma (M = 128, K = 16) into a double-buffered TMEM
-//    accumulator; four epilogue warps drain it while the next tile accumulates;
-//  * work comes from a global counter in three modes: dense tiles (banded for L2 reuse),
-//    per-expert token passes from a device-built list (the routed experts' dgrad, with the
-//    weights as M: "swap AB"), and per-expert weight-gradient tiles whose K is the expert's
-//    own segment of rows in expert-sorted order;
-//  * epilogues: fp32 store or accumulate (optionally transposed), bf16 store, and the
-//    SiTU-GLU derivative, which turns dh into [dg | du] using the recomputed pre-activations
-//    (kept in fp32: near saturation the derivatives of SiTU and of the soft cap change by a
-//    few per cent across one bf16 step of their argument).
-//
-// The memory-bound steps are plain kernels: RMSNorm + combine backward (dc, the gradient of
-// each expert output, of each gate weight, and per-block dgamma sums), the per-token sum of
-// the k expert-row gradients of x_lat, and the router (gate renormalisation, sigmoid, the
-// router's share of dx and dW_r).  Every reduction runs in a fixed order, so results do not
-// depend on scheduling.
+// intermediates a forward call leaves in its workspace.  The contractions reuse the forward's
+// tcgen05 kernels (tc_gemm.cu): the dense kernel with MN-major operands and fp32, accumulating
+// or SiTU-GLU-derivative epilogues for the dense gradients, and the grouped kernel over the
+// forward's work lists for the routed experts' pre-activations (recomputed in fp32: near
+// saturation the derivatives of SiTU and of the soft cap change by a few per cent across one
+// bf16 step of their argument), dh with the SiTU-GLU derivative, and the x_lat gradient of
+// each slot.  This file adds the routed experts' weight gradients (wgrad_kernel: per expert,
+// K = the expert's own rows) and the memory-bound steps as plain kernels: RMSNorm + combine
+// backward (dc, the gradient of each expert output, of each gate weight, and per-block dgamma
+// sums), the per-token sum of the k slot gradients of x_lat, and the router (gate
+// renormalisation, sigmoid, the router's share of dx and dW_r).  Every reduction runs in a
+// fixed order, so results do not depend on scheduling.
 #include <cuda_bf16.h>
 
 #include <cstring>
@@ -42,176 +30,114 @@ namespace {
 
 using bf16 = __nv_bfloat16;
 
-constexpr int BG_BN = 256;
-constexpr int BG_STAGES = 4;
-constexpr int BG_A_BYTES = 128 * 128;              // 128 M x 64 K
-constexpr int BG_B_BYTES = BG_BN * 128;            // 256 N x 64 K
-constexpr int BG_STAGE = BG_A_BYTES + BG_B_BYTES;
-constexpr int BG_LOADERS = 128;                    // warps 0-3
-constexpr int BG_MMA_WARP = 4;
-constexpr int BG_EPI_WARP0 = 5;                    // warps 5-8
-constexpr int BG_THREADS = 9 * 32;
-constexpr int BG_Q = 4;
-constexpr int BG_STG_LD = 65;                      // fp32 staging row of 64 columns (+1 against bank conflicts)
-constexpr int BG_STG = 4 * 32 * BG_STG_LD * 4;     // one 32 x 64 staging tile per epilogue warp
-constexpr int BG_SMEM = BG_STAGES * BG_STAGE + BG_STG + 1024 + 512;
-constexpr int BG_BAND = 8;                         // row tiles per band of the dense tile order
+// ---------------------------------------------------------------- routed weight gradients
+// wgrad_kernel: for each expert e, C_e^T = A_e^T B_e with K = the expert's own rows in
+// expert-sorted order (offsets[e] .. offsets[e + 1]): a tile is 128 M (A's features: the MMA's
+// M, the gradient's contiguous dimension) x 256 N (B's features), K in blocks of 64.  A and B
+// are stored [rows, features] (MN-major operands); A's rows may be gathered through an index,
+// B's are contiguous and come by TMA in 64 x 64 boxes.  Four loader warps fill a 4-stage ring
+// (A by cp.async, 16-byte chunks zero-filled past the segment), one thread issues the MMAs
+// into a double-buffered TMEM accumulator, and eight epilogue warps (two per lane quadrant,
+// half the columns each) store the fp32 tile transposed: the lanes of a warp are consecutive
+// M, so every store is one 128-byte run of a gradient row.  The kernel is bound by those fp32
+// stores (19.7 GB at K3): TMEM is read 64 columns per wait so that the stores keep flowing.
+constexpr int WG_BN = 256;
+constexpr int WG_STAGES = 4;
+constexpr int WG_A_BYTES = 128 * 128;              // 128 M x 64 K
+constexpr int WG_B_BYTES = WG_BN * 128;            // 256 N x 64 K
+constexpr int WG_STAGE = WG_A_BYTES + WG_B_BYTES;
+constexpr int WG_LOADERS = 128;                    // warps 0-3
+constexpr int WG_MMA_WARP = 4;
+constexpr int WG_EPI_WARP0 = 5;                    // warps 5-12
+constexpr int WG_EPI_WARPS = 8;
+constexpr int WG_THREADS = (WG_EPI_WARP0 + WG_EPI_WARPS) * 32;
+constexpr int WG_Q = 4;
+constexpr int WG_SMEM = WG_STAGES * WG_STAGE + 1024 + 512;
+constexpr int WG_BAND = 8;                         // M tiles per band of an expert's tile order
+constexpr int A_MN_ = 1, B_MN_ = 2;                // tc_dense_gemm operand majorness
 
-enum { BG_DENSE = 0, BG_PASS = 1, BG_WGRAD = 2 };
-constexpr int A_MN_ = 1, B_MN_ = 2;   // tc_dense_gemm operand majorness
-enum { BE_F32 = 0, BE_BF16 = 1, BE_DGLU = 2 };
-
-// One operand as stored: lines of ld elements; a grouped operand's expert e starts estride
-// elements further on; index (nullable) maps a line number to the stored line.
+// One operand as stored: lines of ld elements; index (nullable) maps a line number to the
+// stored line.
 struct BOp {
     const bf16 *p;
     long long ld;
-    long long estride;
     const int32_t *index;
 };
 
-struct BArgs {
+struct WArgs {
     BOp A, B;
-    int M, N, K;             // dense: the GEMM; pass: M features per expert, K; wgrad: M x N per expert
-    int tiles_m, tiles_n;    // 128 x 256 tiles of M x N (dense, wgrad)
-    int units;               // dense: tiles; wgrad: E * tiles; pass: list capacity
-    const int4 *items;       // pass: {expert, M block, first row in expert order, rows}
-    const int *n_items;      // pass: number of items (device)
-    const int32_t *offsets;  // wgrad: per-expert row segments [E + 1]
+    int M, N;                // per expert: gradient tile space M x N
+    int tiles_m, tiles_n;    // 128 x 256 tiles
+    int units;               // E * tiles_m * tiles_n
+    const int32_t *offsets;  // per-expert row segments [E + 1]
     int *counter;            // zeroed work counter
-    void *C;                 // output (fp32 or bf16); wgrad: expert e at C + e * cstride
+    float *C;                // expert e's gradient at C + e * cstride, stored [N][M] (row pitch ldc)
     long long ldc, cstride;
-    int out_t;               // 1: C[n][m] instead of C[m][n]
-    int accumulate;          // fp32 epilogue: add into C instead of storing
-    const float *gu;         // SiTU-GLU derivative: fp32 pre-activations [rows, 2F] (gate | up)
-    long long ld_gu;
-    int F;
-    bf16 *dgu;               // ... and its output [rows, 2F]
-    long long ld_dgu;
-    float beta1, beta2;
+    int accumulate;          // add into C instead of storing
     int32_t *status;
     unsigned long long wait_limit_ns;
 };
 
-struct BItem {
+struct WItem {
     int e, m0, n0, mv, nv, kr0, klen;   // e < 0: end of work
 };
 
-__device__ __forceinline__ void band_tile(int tile, int tiles_m, int tiles_n, int &tm, int &tn) {
-    const int per_band = BG_BAND * tiles_n;
-    const int band = tile / per_band;
-    const int m_first = band * BG_BAND;
-    const int bm = min(BG_BAND, tiles_m - m_first);
-    const int r = tile - band * per_band;
-    tm = m_first + r % bm;
-    tn = r / bm;
-}
-
-template <int MODE>
-__device__ __forceinline__ BItem fetch_item(const BArgs &a) {
-    BItem it;
+__device__ __forceinline__ WItem fetch_item(const WArgs &a) {
+    WItem it;
     it.e = -1;
     const int u = atomicAdd(a.counter, 1);
-    if (MODE == BG_PASS) {
-        if (u >= *a.n_items || u >= a.units) return it;
-        const int4 v = a.items[u];
-        it.e = v.x;
-        it.m0 = v.y * 128;
-        it.mv = min(128, a.M - it.m0);
-        it.n0 = v.z;
-        it.nv = v.w;
-        it.kr0 = 0;
-        it.klen = a.K;
-        return it;
-    }
     if (u >= a.units) return it;
     const int per = a.tiles_m * a.tiles_n;
-    int tm, tn;
-    if (MODE == BG_DENSE) {
-        band_tile(u, a.tiles_m, a.tiles_n, tm, tn);
-        it.e = 0;
-        it.kr0 = 0;
-        it.klen = a.K;
-    } else {
-        it.e = u / per;
-        band_tile(u - it.e * per, a.tiles_m, a.tiles_n, tm, tn);
-        it.kr0 = a.offsets[it.e];
-        it.klen = a.offsets[it.e + 1] - it.kr0;
-    }
-    it.m0 = tm * 128;
-    it.n0 = tn * BG_BN;
+    it.e = u / per;
+    // bands of WG_BAND M tiles, M fastest inside a band: the tiles in flight share B strips
+    const int t = u - it.e * per;
+    const int per_band = WG_BAND * a.tiles_n;
+    const int band = t / per_band;
+    const int m_first = band * WG_BAND;
+    const int bm = min(WG_BAND, a.tiles_m - m_first);
+    const int r = t - band * per_band;
+    it.m0 = (m_first + r % bm) * 128;
+    it.n0 = (r / bm) * WG_BN;
     it.mv = min(128, a.M - it.m0);
-    it.nv = min(BG_BN, a.N - it.n0);
+    it.nv = min(WG_BN, a.N - it.n0);
+    it.kr0 = a.offsets[it.e];
+    it.klen = a.offsets[it.e + 1] - it.kr0;
     return it;
 }
 
-// Copies of one operand tile (extent x 64 K) for one stage.  t = loader thread 0..127.
-//  K-major: line r = row r of the tile (M or N index), chunk c = K values 8c..8c+7.
-//  MN-major: line (g, kr) = K row kr of the 64-wide group g, chunk c = values 64g+8c..+7.
-template <bool MN, int EXTENT>
-__device__ __forceinline__ void load_tile(uint32_t sbase, const BOp &op, int e, int mn0, int mnv, int kr0,
-                                          int k0, int klen, int t) {
-    constexpr int CHUNKS = EXTENT * 8;                  // 16-byte chunks of the tile
-    const bf16 *base = op.p + (long long)e * op.estride;
+// The A tile of one stage (64 K rows x 128 M, MN-major: a line of 64 M values per K row, two
+// 64-wide groups, 128-byte swizzle) by cp.async; t = loader thread 0..127.
+__device__ __forceinline__ void load_a(uint32_t sbase, const BOp &op, int m0, int mv, int kr0, int k0, int klen,
+                                       int t) {
 #pragma unroll 4
-    for (int q = t; q < CHUNKS; q += BG_LOADERS) {
-        int line, c;
-        long long src_line;
-        bool ok;
-        uint32_t dst;
-        long long col;
-        if (!MN) {
-            line = q >> 3;
-            c = q & 7;
-            ok = line < mnv && k0 + 8 * c < klen;
-            const int row = mn0 + (line < mnv ? line : 0);
-            src_line = op.index ? op.index[row] : row;
-            col = k0 + 8 * c;
-            dst = sbase + (line >> 3) * 1024 + (line & 7) * 128 + ((c ^ (line & 7)) << 4);
-        } else {
-            // 64 K rows x (EXTENT / 64) groups x 8 chunks; consecutive threads walk one K row
-            const int per_row = EXTENT / 8;              // chunks per K row
-            const int kr = q / per_row;
-            const int w = q - kr * per_row;
-            const int g = w >> 3;
-            c = w & 7;
-            ok = k0 + kr < klen && 64 * g + 8 * c < mnv;
-            const int krow = kr0 + k0 + (k0 + kr < klen ? kr : 0);
-            src_line = op.index ? op.index[krow] : krow;
-            col = mn0 + 64 * g + 8 * c;
-            dst = sbase + g * 8192 + (kr >> 3) * 1024 + (kr & 7) * 128 + ((c ^ (kr & 7)) << 4);
-            if (!ok) col = mn0;
-        }
-        const bf16 *src = base + src_line * op.ld + (ok ? col : 0);
+    for (int q = t; q < 128 * 8; q += WG_LOADERS) {
+        // 64 K rows x 2 groups x 8 chunks; consecutive threads walk one K row
+        const int kr = q >> 4;
+        const int w = q & 15;
+        const int g = w >> 3, c = w & 7;
+        const bool ok = k0 + kr < klen && 64 * g + 8 * c < mv;
+        const int krow = kr0 + k0 + (k0 + kr < klen ? kr : 0);
+        const long long src_line = op.index ? op.index[krow] : krow;
+        const long long col = ok ? m0 + 64 * g + 8 * c : m0;
+        const uint32_t dst = sbase + g * 8192 + (kr >> 3) * 1024 + (kr & 7) * 128 + ((c ^ (kr & 7)) << 4);
+        const bf16 *src = op.p + src_line * op.ld + (ok ? col : 0);
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(ok ? 16u : 0u)
                      : "memory");
     }
 }
 
-__device__ __forceinline__ float situ_f(float g, float b1) {
-    return b1 * tanhf(g / b1) * (1.0f / (1.0f + expf(-g)));
-}
-__device__ __forceinline__ float situ_grad_f(float g, float b1) {
-    const float th = tanhf(g / b1);
-    const float sg = 1.0f / (1.0f + expf(-g));
-    return (1.0f - th * th) * sg + b1 * th * sg * (1.0f - sg);
-}
-
-// B_TMA: the B operand (MN-major, stored rows in expert order) comes by TMA in 64 x 64 boxes
-// from bmap; rows past the expert's segment then hold other experts' values, which meet the
-// zero-filled rows of A past the segment, so they add nothing.
-template <int EPI, bool A_MN, bool B_MN, int MODE, bool B_TMA = false>
-__global__ void __launch_bounds__(BG_THREADS, 1) bgemm_kernel(const __grid_constant__ CUtensorMap bmap,
-                                                              const BArgs a) {
+// B rows past the expert's segment (TMA boxes of 64 K rows) hold other experts' values; they
+// meet the zero-filled rows of A past the segment, so they add nothing.
+__global__ void __launch_bounds__(WG_THREADS, 1) wgrad_kernel(const __grid_constant__ CUtensorMap bmap,
+                                                              const WArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float *stg_all = reinterpret_cast<float *>(smem + BG_STAGES * BG_STAGE);
-    BItem *q_items = reinterpret_cast<BItem *>(smem + BG_STAGES * BG_STAGE + BG_STG);
-    uint64_t *q_full = reinterpret_cast<uint64_t *>(q_items + BG_Q);
-    uint64_t *q_empty = q_full + BG_Q;
-    uint64_t *full = q_empty + BG_Q;
-    uint64_t *empty = full + BG_STAGES;
-    uint64_t *tfull = empty + BG_STAGES;
+    WItem *q_items = reinterpret_cast<WItem *>(smem + WG_STAGES * WG_STAGE);
+    uint64_t *q_full = reinterpret_cast<uint64_t *>(q_items + WG_Q);
+    uint64_t *q_empty = q_full + WG_Q;
+    uint64_t *full = q_empty + WG_Q;
+    uint64_t *empty = full + WG_STAGES;
+    uint64_t *tfull = empty + WG_STAGES;
     uint64_t *tempty = tfull + 2;
     uint64_t *mma_drain = tempty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_drain + 1);
@@ -219,29 +145,29 @@ __global__ void __launch_bounds__(BG_THREADS, 1) bgemm_kernel(const __grid_const
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < BG_Q; ++i) {
+        for (int i = 0; i < WG_Q; ++i) {
             mbar_init(&q_full[i], 1);
-            mbar_init(&q_empty[i], 4 + 1 + 4);   // loader warps, MMA thread, epilogue warps
+            mbar_init(&q_empty[i], 4 + 1 + WG_EPI_WARPS);   // loader warps, MMA thread, epilogue warps
         }
-        for (int s = 0; s < BG_STAGES; ++s) {
-            mbar_init(&full[s], BG_LOADERS + (B_TMA ? 1 : 0));
+        for (int s = 0; s < WG_STAGES; ++s) {
+            mbar_init(&full[s], WG_LOADERS + 1);             // A's cp.async arrivals + B's TMA
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], 4);
+            mbar_init(&tempty[b], WG_EPI_WARPS);
         }
         mbar_init(mma_drain, 1);
         wait_ctl_init(wc, a.wait_limit_ns);
         fence_barrier_init();
     }
-    if (warp == BG_MMA_WARP) tmem_alloc(tmem_slot, 512);
+    if (warp == WG_MMA_WARP) tmem_alloc(tmem_slot, 512);
     tc_before();
     __syncthreads();
     tc_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    auto pop = [&](int &qs, uint32_t &qp, BItem &it, bool warp_wide) -> bool {
+    auto pop = [&](int &qs, uint32_t &qp, WItem &it, bool warp_wide) -> bool {
         if (!mbar_wait(&q_full[qs], qp, wc)) return false;
         it = q_items[qs];
         if (warp_wide) {
@@ -250,7 +176,7 @@ __global__ void __launch_bounds__(BG_THREADS, 1) bgemm_kernel(const __grid_const
         } else {
             mbar_arrive(&q_empty[qs]);
         }
-        if (++qs == BG_Q) { qs = 0; qp ^= 1; }
+        if (++qs == WG_Q) { qs = 0; qp ^= 1; }
         return true;
     };
 
@@ -268,7 +194,7 @@ __global__ void __launch_bounds__(BG_THREADS, 1) bgemm_kernel(const __grid_const
             if (warp == 0) {
                 int ok = 1;
                 if (lane == 0) {
-                    const BItem nx = fetch_item<MODE>(a);
+                    const WItem nx = fetch_item(a);
                     if (mbar_wait(&q_empty[fs], fp ^ 1, wc)) {
                         q_items[fs] = nx;
                         mbar_arrive(&q_full[fs]);
@@ -277,46 +203,41 @@ __global__ void __launch_bounds__(BG_THREADS, 1) bgemm_kernel(const __grid_const
                     }
                 }
                 if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-                if (++fs == BG_Q) { fs = 0; fp ^= 1; }
+                if (++fs == WG_Q) { fs = 0; fp ^= 1; }
             }
-            BItem it;
+            WItem it;
             if (!pop(qs, qp, it, true)) break;
             if (it.e < 0) break;
             const int nkb = (it.klen + 63) / 64;
             bool aborted = false;
             for (int kb = 0; kb < nkb; ++kb) {
                 if (!mbar_wait(&empty[stage], phase ^ 1, wc)) { aborted = true; break; }
-                const uint32_t sa = su32(smem + stage * BG_STAGE);
-                const uint32_t sb = sa + BG_A_BYTES;
-                load_tile<A_MN, 128>(sa, a.A, it.e, it.m0, it.mv, it.kr0, kb * 64, it.klen, t);
-                if (B_TMA) {
-                    if (t == 0) {
-                        mbar_expect_tx(&full[stage], BG_B_BYTES);
+                const uint32_t sa = su32(smem + stage * WG_STAGE);
+                const uint32_t sb = sa + WG_A_BYTES;
+                load_a(sa, a.A, it.m0, it.mv, it.kr0, kb * 64, it.klen, t);
+                if (t == 0) {
+                    mbar_expect_tx(&full[stage], WG_B_BYTES);
 #pragma unroll
-                        for (int g = 0; g < BG_BN / 64; ++g)
-                            tma_load_2d(sb + g * 8192, &bmap, &full[stage], it.n0 + 64 * g, it.kr0 + kb * 64);
-                    }
-                } else {
-                    load_tile<B_MN, BG_BN>(sb, a.B, it.e, it.n0, it.nv, it.kr0, kb * 64, it.klen, t);
+                    for (int g = 0; g < WG_BN / 64; ++g)
+                        tma_load_2d(sb + g * 8192, &bmap, &full[stage], it.n0 + 64 * g, it.kr0 + kb * 64);
                 }
                 cp_async_arrive_noinc(&full[stage]);
-                if (++stage == BG_STAGES) { stage = 0; phase ^= 1; l_wrapped = true; }
+                if (++stage == WG_STAGES) { stage = 0; phase ^= 1; l_wrapped = true; }
             }
             if (aborted) break;
         }
         cp_async_wait_all();
-    } else if (warp == BG_MMA_WARP) {
+    } else if (warp == WG_MMA_WARP) {
         if (lane == 0) {
             int qs = 0, stage = 0, buf = 0;
             uint32_t qp = 0, phase = 0, tph = 0;
+            constexpr uint32_t IDESC = idesc_bf16(128, WG_BN) | (1u << 15) | (1u << 16);   // A, B MN-major
             for (;;) {
-                BItem it;
+                WItem it;
                 if (!pop(qs, qp, it, false)) break;
                 if (it.e < 0) break;
                 const int nkb = (it.klen + 63) / 64;
                 if (nkb == 0) continue;                    // nothing to accumulate (empty expert)
-                const int n16 = (MODE == BG_PASS ? it.nv : BG_BN) + 15 & ~15;
-                const uint32_t idesc = idesc_bf16(128, n16) | (A_MN ? (1u << 15) : 0u) | (B_MN ? (1u << 16) : 0u);
                 if (!mbar_wait(&tempty[buf], tph ^ 1, wc)) break;
                 tc_after();
                 const uint32_t d = tmem_base + buf * 256;
@@ -325,16 +246,14 @@ __global__ void __launch_bounds__(BG_THREADS, 1) bgemm_kernel(const __grid_const
                     if (!mbar_wait(&full[stage], phase, wc)) { aborted = true; break; }
                     fence_proxy_async();
                     tc_after();
-                    const uint32_t sa = su32(smem + stage * BG_STAGE);
-                    const uint32_t sb = sa + BG_A_BYTES;
+                    const uint32_t sa = su32(smem + stage * WG_STAGE);
+                    const uint32_t sb = sa + WG_A_BYTES;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = A_MN ? mn_desc(sa + kk * 2048, 8192) : sdesc(sa + kk * 32);
-                        const uint64_t bd = B_MN ? mn_desc(sb + kk * 2048, 8192) : sdesc(sb + kk * 32);
-                        umma(d, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma(d, mn_desc(sa + kk * 2048, 8192), mn_desc(sb + kk * 2048, 8192), IDESC,
+                             (kb > 0 || kk > 0) ? 1u : 0u);
                     umma_commit(&empty[stage]);
-                    if (++stage == BG_STAGES) { stage = 0; phase ^= 1; }
+                    if (++stage == WG_STAGES) { stage = 0; phase ^= 1; }
                 }
                 if (aborted) break;
                 umma_commit(&tfull[buf]);
@@ -343,139 +262,51 @@ __global__ void __launch_bounds__(BG_THREADS, 1) bgemm_kernel(const __grid_const
         }
     } else {
         // ------------------------------------------------ epilogue: warp w drains TMEM lanes
-        // 32 (w % 4) .. + 31, i.e. tile rows (M) of that quadrant
+        // 32 (w % 4) .. + 31 (tile rows M of that quadrant), columns 128 h .. 128 h + 127
         const int q = warp & 3;
+        const int h = (warp - WG_EPI_WARP0) >> 2;
         const int i = q * 32 + lane;
         int qs = 0, buf = 0;
         uint32_t qp = 0, tph = 0;
         for (;;) {
-            BItem it;
+            WItem it;
             if (!pop(qs, qp, it, true)) break;
             if (it.e < 0) break;
             const int nkb = (it.klen + 63) / 64;
             const bool row_ok = i < it.mv;
             const int m = it.m0 + i;
+            const int c_end = min(it.nv, 128 * h + 128);
+            float *C = a.C + (long long)it.e * a.cstride;
             if (nkb == 0) {
                 // an expert without rows: its weight-gradient tile is zero (stored unless adding)
-                if (EPI == BE_F32 && !a.accumulate && row_ok) {
-                    float *C = static_cast<float *>(a.C) + (long long)it.e * a.cstride;
-                    for (int j = 0; j < it.nv; ++j)
-                        C[a.out_t ? (long long)(it.n0 + j) * a.ldc + m : (long long)m * a.ldc + it.n0 + j] = 0.f;
-                }
+                if (!a.accumulate && row_ok)
+                    for (int j = 128 * h; j < c_end; ++j) C[(long long)(it.n0 + j) * a.ldc + m] = 0.f;
                 continue;
             }
             if (!mbar_wait(&tfull[buf], tph, wc)) break;
             tc_after();
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + buf * 256;
-            if (EPI == BE_F32 && !a.out_t) {
-                // 64 columns at a time through a 32 x 64 staging tile: each lane writes its row,
-                // then the warp stores one row at a time as two 128-byte runs (coalesced)
-                float *stg = stg_all + (warp - BG_EPI_WARP0) * 32 * BG_STG_LD;
-                float *C = static_cast<float *>(a.C) + (long long)it.e * (MODE == BG_WGRAD ? a.cstride : 0);
-                for (int c0 = 0; c0 < it.nv; c0 += 64) {
-                    uint32_t r[4][16];
+            for (int c0 = 128 * h; c0 < c_end; c0 += 64) {
+                uint32_t r[4][16];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) TMEM_LD16(tb + c0 + 16 * u, r[u]);
-                    tmem_wait_ld();
+                for (int u = 0; u < 4; ++u) TMEM_LD16(tb + c0 + 16 * u, r[u]);
+                tmem_wait_ld();
+                if (!row_ok) continue;
+                float *o = C + (long long)(it.n0 + c0) * a.ldc + m;
+                const int nj = min(64, it.nv - c0);
+                if (a.accumulate) {
 #pragma unroll
                     for (int u = 0; u < 4; ++u)
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) stg[lane * BG_STG_LD + 16 * u + j] = __uint_as_float(r[u][j]);
-                    __syncwarp();
-                    // eight rows at a time: all staging reads (and, when adding, all reads of C)
-                    // issued before the stores, so the latencies overlap
-                    const bool c_ok[2] = {c0 + lane < it.nv, c0 + lane + 32 < it.nv};
-#pragma unroll 1
-                    for (int rr0 = 0; rr0 < 32; rr0 += 8) {
-                        float v[8][2];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-#pragma unroll
-                            for (int h = 0; h < 2; ++h) v[i][h] = stg[(rr0 + i) * BG_STG_LD + lane + 32 * h];
-                        if (a.accumulate) {
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const int mi = q * 32 + rr0 + i;
-                                const float *row = C + (long long)(it.m0 + mi) * a.ldc + it.n0 + c0;
-#pragma unroll
-                                for (int h = 0; h < 2; ++h)
-                                    if (mi < it.mv && c_ok[h]) v[i][h] += row[lane + 32 * h];
-                            }
-                        }
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const int mi = q * 32 + rr0 + i;
-                            float *row = C + (long long)(it.m0 + mi) * a.ldc + it.n0 + c0;
-#pragma unroll
-                            for (int h = 0; h < 2; ++h)
-                                if (mi < it.mv && c_ok[h]) row[lane + 32 * h] = v[i][h];
-                        }
-                    }
-                    __syncwarp();
-                }
-            } else
-            for (int c = 0; c < it.nv; c += 16) {
-                uint32_t r[16];
-                TMEM_LD16(tb + c, r);
-                tmem_wait_ld();
-                if (!row_ok) continue;
-                const int nj = min(16, it.nv - c);
-                if (EPI == BE_F32) {
-                    float *C = static_cast<float *>(a.C) + (long long)it.e * (MODE == BG_WGRAD ? a.cstride : 0);
-                    if (!a.out_t) {
-                        float *row = C + (long long)m * a.ldc + it.n0 + c;
-                        if (nj == 16 && (a.ldc & 3) == 0) {
-#pragma unroll
-                            for (int v = 0; v < 16; v += 4) {
-                                float4 o = make_float4(__uint_as_float(r[v]), __uint_as_float(r[v + 1]),
-                                                       __uint_as_float(r[v + 2]), __uint_as_float(r[v + 3]));
-                                if (a.accumulate) {
-                                    const float4 p = *reinterpret_cast<const float4 *>(row + v);
-                                    o.x += p.x; o.y += p.y; o.z += p.z; o.w += p.w;
-                                }
-                                *reinterpret_cast<float4 *>(row + v) = o;
-                            }
-                        } else {
-                            for (int j = 0; j < nj; ++j)
-                                row[j] = __uint_as_float(r[j]) + (a.accumulate ? row[j] : 0.f);
-                        }
-                    } else {   // lanes are consecutive m: every store is one 128-byte run
-                        float *o = C + (long long)(it.n0 + c) * a.ldc + m;
-                        float v[16];
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
-                        if (a.accumulate) {
-#pragma unroll
-                            for (int j = 0; j < 16; ++j)
-                                if (j < nj) v[j] += o[(long long)j * a.ldc];
-                        }
-#pragma unroll
                         for (int j = 0; j < 16; ++j)
-                            if (j < nj) o[(long long)j * a.ldc] = v[j];
-                    }
-                } else if (EPI == BE_BF16) {
-                    bf16 *C = static_cast<bf16 *>(a.C);
-                    if (!a.out_t) {
-                        bf16 *row = C + (long long)m * a.ldc + it.n0 + c;
-                        for (int j = 0; j < nj; ++j) row[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
-                    } else {
-                        for (int j = 0; j < nj; ++j)
-                            C[(long long)(it.n0 + c + j) * a.ldc + m] = __float2bfloat16_rn(__uint_as_float(r[j]));
-                    }
-                } else {   // BE_DGLU: the accumulator is dh; rows x features by orientation
-                    for (int j = 0; j < nj; ++j) {
-                        const long long row = a.out_t ? (long long)(it.n0 + c + j) : (long long)m;
-                        const int f = a.out_t ? m : it.n0 + c + j;
-                        const float dh = __uint_as_float(r[j]);
-                        const float g = a.gu[row * a.ld_gu + f];
-                        const float u = a.gu[row * a.ld_gu + a.F + f];
-                        const float tu = tanhf(u / a.beta2);
-                        const float cap = a.beta2 * tu;
-                        a.dgu[row * a.ld_dgu + f] = __float2bfloat16_rn(dh * cap * situ_grad_f(g, a.beta1));
-                        a.dgu[row * a.ld_dgu + a.F + f] =
-                            __float2bfloat16_rn(dh * situ_f(g, a.beta1) * (1.0f - tu * tu));
-                    }
+                            if (16 * u + j < nj)
+                                r[u][j] = __float_as_uint(__uint_as_float(r[u][j]) + o[(long long)(16 * u + j) * a.ldc]);
                 }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (16 * u + j < nj) o[(long long)(16 * u + j) * a.ldc] = __uint_as_float(r[u][j]);
             }
             tc_before();
             __syncwarp();
@@ -485,61 +316,18 @@ __global__ void __launch_bounds__(BG_THREADS, 1) bgemm_kernel(const __grid_const
     }
     __syncthreads();
     if (wc->abort) {   // let copies and MMAs in flight finish before TMEM is freed
-        if (B_TMA && threadIdx.x == 0) drain_ring(full, BG_STAGES, l_stage, l_phase, l_wrapped);
-        if (warp == BG_MMA_WARP && lane == 0) {
+        if (threadIdx.x == 0) drain_ring(full, WG_STAGES, l_stage, l_phase, l_wrapped);
+        if (warp == WG_MMA_WARP && lane == 0) {
             umma_commit(mma_drain);
             mbar_wait_drain(mma_drain, 0);
         }
         __syncthreads();
     }
-    if (warp == BG_MMA_WARP) {
+    if (warp == WG_MMA_WARP) {
         tc_after();
         tmem_dealloc(tmem_base, 512);
     }
     if (threadIdx.x == 0 && wc->abort && a.status) atomicExch(&a.status[ST_TIMEOUT], 1);
-}
-
-// Token passes of at most cap rows per expert (balanced), times nmb M blocks: the work list of
-// a grouped dgrad GEMM, built on the device from the expert counts and offsets.
-__global__ void __launch_bounds__(1024) pass_list_kernel(const int32_t *__restrict__ counts,
-                                                         const int32_t *__restrict__ offsets, int E, int nmb,
-                                                         int cap, int4 *__restrict__ items, int *n_items,
-                                                         int max_items) {
-    __shared__ int base_s[4096 + 1];
-    __shared__ int wsum[32];
-    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    const int per = (E + blockDim.x - 1) / blockDim.x;
-    const int e0 = tid * per;
-    int loc = 0;
-    for (int e = e0; e < e0 + per && e < E; ++e) loc += nmb * ((counts[e] + cap - 1) / cap);
-    int incl = loc;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-    }
-    if (lane == 31) wsum[w] = incl;
-    __syncthreads();
-    int base = incl - loc;
-    for (int i = 0; i < w; ++i) base += wsum[i];
-    for (int e = e0; e < e0 + per && e < E; ++e) {
-        base_s[e] = base;
-        base += nmb * ((counts[e] + cap - 1) / cap);
-    }
-    if (tid == blockDim.x - 1) *n_items = min(base, max_items);
-    __syncthreads();
-    for (int e = w; e < E; e += blockDim.x >> 5) {
-        const int n = counts[e], off = offsets[e];
-        const int np = (n + cap - 1) / cap;
-        if (np == 0) continue;
-        const int chunk = (n + np - 1) / np;
-        for (int j = lane; j < nmb * np; j += 32) {
-            const int mb = j / np, pass = j - mb * np;
-            const int c0 = pass * chunk;
-            if (base_s[e] + j < max_items)
-                items[base_s[e] + j] = make_int4(e, mb, off + c0, min(chunk, n - c0));
-        }
-    }
 }
 
 // ---------------------------------------------------------------- memory-bound steps
@@ -770,51 +558,33 @@ __global__ void __launch_bounds__(256) router_wgrad_kernel(const bf16 *__restric
 }
 
 // ---------------------------------------------------------------- host side
-template <int EPI, bool AMN, bool BMN, int MODE, bool B_TMA = false>
-int launch_bg(BArgs a, cudaStream_t st, long long b_rows = 0) {
-    auto kern = bgemm_kernel<EPI, AMN, BMN, MODE, B_TMA>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BG_SMEM);
-    if (e != cudaSuccess) return fail(SLMOE_ECUDA, "smem attribute: %s", cudaGetErrorString(e));
-    if (MODE != BG_PASS && a.units == 0) return SLMOE_OK;
-    CUtensorMap bmap;
-    memset(&bmap, 0, sizeof(bmap));
-    if (B_TMA) {   // B stored [b_rows, N] (MN-major), 64 x 64 boxes, 128-byte swizzle
-        int rc = tmap_encode_2d(&bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.B.p, b_rows, a.N, a.B.ld, 64, 64,
-                                CU_TENSOR_MAP_SWIZZLE_128B);
-        if (rc) return rc;
-    }
-    const int sms = sm_count();
-    const int grid = (MODE != BG_PASS && a.units < sms) ? a.units : sms;
-    kern<<<grid, BG_THREADS, BG_SMEM, st>>>(bmap, a);
-    return check_launch("bgemm_kernel");
-}
-
-BArgs dense_args(int M, int N, int K, BOp A, BOp B, void *C, long long ldc, int accumulate, int *counter,
-                 int32_t *status) {
-    BArgs a = {};
-    a.A = A;
-    a.B = B;
-    a.M = M;
-    a.N = N;
-    a.K = K;
+// Expert e's gradient C_e [N][M] = (A_e^T B_e)^T over its rows: A [rows, M] (optionally gathered
+// through a_index), B [rows, N] contiguous (b_rows in all).
+int launch_wgrad(int E, int M, int N, const void *A, long long lda, const int32_t *a_index, const void *B,
+                 long long ldb, long long b_rows, const int32_t *offsets, float *C, int accumulate, int *counter,
+                 int32_t *status, cudaStream_t st) {
+    WArgs a = {};
+    a.A.p = static_cast<const bf16 *>(A); a.A.ld = lda; a.A.index = a_index;
+    a.B.p = static_cast<const bf16 *>(B); a.B.ld = ldb; a.B.index = nullptr;
+    a.M = M; a.N = N;
     a.tiles_m = (M + 127) / 128;
-    a.tiles_n = (N + BG_BN - 1) / BG_BN;
-    a.units = a.tiles_m * a.tiles_n;
-    a.C = C;
-    a.ldc = ldc;
-    a.accumulate = accumulate;
+    a.tiles_n = (N + WG_BN - 1) / WG_BN;
+    a.units = E * a.tiles_m * a.tiles_n;
+    a.offsets = offsets;
     a.counter = counter;
+    a.C = C; a.ldc = M; a.cstride = (long long)M * N;
+    a.accumulate = accumulate;
     a.status = status;
-    return a;
-}
-
-BOp op(const void *p, long long ld, long long estride = 0, const int32_t *index = nullptr) {
-    BOp o;
-    o.p = static_cast<const bf16 *>(p);
-    o.ld = ld;
-    o.estride = estride;
-    o.index = index;
-    return o;
+    cudaError_t e = cudaFuncSetAttribute(wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, WG_SMEM);
+    if (e != cudaSuccess) return fail(SLMOE_ECUDA, "smem attribute: %s", cudaGetErrorString(e));
+    if (a.units == 0) return SLMOE_OK;
+    CUtensorMap bmap;   // B stored [b_rows, N] (MN-major), 64 x 64 boxes, 128-byte swizzle
+    int rc = tmap_encode_2d(&bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, b_rows, N, ldb, 64, 64,
+                            CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc) return rc;
+    const int sms = sm_count();
+    wgrad_kernel<<<a.units < sms ? a.units : sms, WG_THREADS, WG_SMEM, st>>>(bmap, a);
+    return check_launch("wgrad_kernel");
 }
 
 }  // namespace
@@ -844,15 +614,6 @@ size_t backward_workspace_bytes(const slmoe_config *c, BwdLayout *L) {
     l.nblk = (T + RB_TOK - 1) / RB_TOK;
     l.dgamma_part = take(l.nblk * dl * 4);
     l.counters = take(32 * 4);
-    const size_t cap1 = (2 * I + 127) / 128 * (E + (Tk + BG_BN - 1) / BG_BN);
-    const size_t cap2 = (I + 127) / 128 * (E + (Tk + BG_BN - 1) / BG_BN);
-    const size_t cap3 = (dl + 127) / 128 * (E + (Tk + BG_BN - 1) / BG_BN);
-    l.cap1 = cap1;
-    l.cap2 = cap2;
-    l.cap3 = cap3;
-    l.items1 = take(cap1 * 16);
-    l.items2 = take(cap2 * 16);
-    l.items3 = take(cap3 * 16);
     l.cap_dglu = (I + 255) / 256 * (E + (Tk + GROUPED_PASS - 1) / GROUPED_PASS);
     l.items_dglu = take(l.cap_dglu * 16);
     l.total = off;
@@ -881,9 +642,6 @@ int tc_backward(const slmoe_config *c, const void *x, const slmoe_weights *w, co
     float *dl_perm = reinterpret_cast<float *>(ws + L.dl_perm);
     float *dgamma_part = reinterpret_cast<float *>(ws + L.dgamma_part);
     int *cnt = reinterpret_cast<int *>(ws + L.counters);
-    int4 *items1 = reinterpret_cast<int4 *>(ws + L.items1);
-    int4 *items2 = reinterpret_cast<int4 *>(ws + L.items2);
-    int4 *items3 = reinterpret_cast<int4 *>(ws + L.items3);
     int rc;
     if (cudaMemsetAsync(cnt, 0, 32 * sizeof(int), st) != cudaSuccess ||
         cudaMemsetAsync(dx, 0, (size_t)T * d * sizeof(float), st) != cudaSuccess)
@@ -959,15 +717,12 @@ int tc_backward(const slmoe_config *c, const void *x, const slmoe_weights *w, co
     // (an M index) stores along a row of the gradient:
     //   dW2[e]^T  [I, d_l]  = h^T dy_e             (A = h, B = dy_e by TMA)
     //   dW13[e]^T [d_l, 2I] = x_lat[perm]^T [dg|du] (A = x_lat gathered, B = [dg|du] by TMA)
-    {
-        BArgs a = dense_args(I, dl, 0, op(fs.h, I), op(dye, dl), g->dW2, I, accumulate, cnt + 23, status);
-        a.offsets = fs.offsets; a.units = E * a.tiles_m * a.tiles_n; a.cstride = (long long)dl * I; a.out_t = 1;
-        if ((rc = launch_bg<BE_F32, true, true, BG_WGRAD, true>(a, st, Tk))) return rc;
-        BArgs b = dense_args(dl, 2 * I, 0, op(fs.x_lat, dl, 0, fs.perm), op(dgu, 2 * I), g->dW13, dl, accumulate,
-                             cnt + 24, status);
-        b.offsets = fs.offsets; b.units = E * b.tiles_m * b.tiles_n; b.cstride = (long long)2 * I * dl; b.out_t = 1;
-        if ((rc = launch_bg<BE_F32, true, true, BG_WGRAD, true>(b, st, Tk))) return rc;
-    }
+    if ((rc = launch_wgrad(E, I, dl, fs.h, I, nullptr, dye, dl, Tk, fs.offsets, g->dW2, accumulate, cnt + 23,
+                           status, st)))
+        return rc;
+    if ((rc = launch_wgrad(E, dl, 2 * I, fs.x_lat, dl, fs.perm, dgu, 2 * I, Tk, fs.offsets, g->dW13, accumulate,
+                           cnt + 24, status, st)))
+        return rc;
     // dx_lat = sum over the token's k rows; then the latent down-projection
     {
         const long long n = (long long)T * (dl / 8);

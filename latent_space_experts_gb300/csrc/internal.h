@@ -113,7 +113,7 @@ struct FwdSaved {
 };
 struct BwdLayout {
     size_t dy_b, dz, dye, dg, gu, dgu, dxe, dx_lat, gu_s, dgu_s, dl_perm, dgamma_part, counters;
-    size_t items1, items2, items3, cap1, cap2, cap3, nblk, total;
+    size_t nblk, total;
     size_t items_dglu, cap_dglu;
 };
 size_t backward_workspace_bytes(const slmoe_config *c, BwdLayout *L);
