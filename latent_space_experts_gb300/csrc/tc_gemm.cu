@@ -167,18 +167,16 @@ struct DenseCfg {
                   "dense tile shape");
 };
 
-// SiTU and its derivative for the backward epilogues (fp32, CUDA math functions).
-__device__ __forceinline__ float situ_val(float g, float b1) { return b1 * tanhf(g / b1) * (1.0f / (1.0f + expf(-g))); }
-__device__ __forceinline__ float situ_der(float g, float b1) {
+// [dg, du] of h = SiTU(g) * b2 tanh(u / b2) for an upstream dh (fp32, CUDA math functions):
+// with t = tanh(g / b1) and s = sigmoid(g), SiTU = b1 t s and SiTU' = (1 - t^2) s + b1 t s (1 - s);
+// the soft cap's derivative is 1 - tanh(u / b2)^2.  Each transcendental is evaluated once.
+__device__ __forceinline__ void dglu(float dh, float g, float u, float b1, float b2, float &dg, float &du) {
     const float th = tanhf(g / b1);
     const float sg = 1.0f / (1.0f + expf(-g));
-    return (1.0f - th * th) * sg + b1 * th * sg * (1.0f - sg);
-}
-// [dg, du] of h = SiTU(g) * b2 tanh(u / b2) for an upstream dh.
-__device__ __forceinline__ void dglu(float dh, float g, float u, float b1, float b2, float &dg, float &du) {
     const float tu = tanhf(u / b2);
-    dg = dh * (b2 * tu) * situ_der(g, b1);
-    du = dh * situ_val(g, b1) * (1.0f - tu * tu);
+    const float bts = b1 * th * sg;                       // SiTU(g)
+    dg = dh * (b2 * tu) * ((1.0f - th * th) * sg + bts * (1.0f - sg));
+    du = dh * bts * (1.0f - tu * tu);
 }
 
 template <int BN, int EPI, int PACC, int MAJ = 0>
@@ -380,8 +378,9 @@ __global__ void __launch_bounds__(DenseCfg<BN, EPI, PACC>::THREADS, 1) dense_ker
                             *reinterpret_cast<uint4 *>(C + n) = v0;
                             *reinterpret_cast<uint4 *>(C + n + 8) = v1;
                         } else {
-                            for (int i = 0; i < 16 && n + i < a.N; ++i)
-                                C[n + i] = __float2bfloat16_rn(__uint_as_float(r[i]));
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)   // static indices keep r in registers
+                                if (n + i < a.N) C[n + i] = __float2bfloat16_rn(__uint_as_float(r[i]));
                         }
                     }
                 }
@@ -406,23 +405,51 @@ __global__ void __launch_bounds__(DenseCfg<BN, EPI, PACC>::THREADS, 1) dense_ker
                                 *reinterpret_cast<float4 *>(C + n + i) = o;
                             }
                         } else {
-                            for (int i = 0; i < 16 && n + i < a.N; ++i)
-                                C[n + i] = __uint_as_float(r[i]) + (a.accumulate ? C[n + i] : 0.f);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)   // static indices keep r in registers
+                                if (n + i < a.N) C[n + i] = __uint_as_float(r[i]) + (a.accumulate ? C[n + i] : 0.f);
                         }
                     }
                 }
             } else if (EPI == EPI_DGLU) {
-                // rows are tokens, columns features f: gate at f, up at F + f
+                // rows are tokens, columns features f: gate at f, up at F + f; 16 columns at a
+                // time with 16-byte loads of the pre-activations and 16-byte stores of [dg | du]
+                // when the rows allow it (F, the pitches and n 16-element aligned)
                 const float *gr = a.gu + (long long)row * a.ld_gu;
                 __nv_bfloat16 *dr = a.dgu + (long long)row * a.ld_dgu;
+                const bool vec = ((a.F | a.ld_gu | a.ld_dgu) & 15) == 0;
 #pragma unroll 1
                 for (int c = 0; c < BN; c += 16) {
                     uint32_t r[16];
                     TMEM_LD16(tb + c, r);
                     tmem_wait_ld();
                     const int n = n0 + c;
-                    if (row_ok) {
-                        for (int i = 0; i < 16 && n + i < a.N; ++i) {
+                    if (!row_ok) continue;
+                    if (vec && n + 16 <= a.N) {
+                        float g[16], u[16], dg[16], du[16];
+#pragma unroll
+                        for (int i = 0; i < 16; i += 4) {
+                            const float4 gv = *reinterpret_cast<const float4 *>(gr + n + i);
+                            const float4 uv = *reinterpret_cast<const float4 *>(gr + a.F + n + i);
+                            g[i] = gv.x; g[i + 1] = gv.y; g[i + 2] = gv.z; g[i + 3] = gv.w;
+                            u[i] = uv.x; u[i + 1] = uv.y; u[i + 2] = uv.z; u[i + 3] = uv.w;
+                        }
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) dglu(__uint_as_float(r[i]), g[i], u[i], a.dbeta1, a.dbeta2, dg[i], du[i]);
+                        uint32_t pg[8], pu[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            pg[i] = pack_bf16(dg[2 * i], dg[2 * i + 1]);
+                            pu[i] = pack_bf16(du[2 * i], du[2 * i + 1]);
+                        }
+                        *reinterpret_cast<uint4 *>(dr + n) = make_uint4(pg[0], pg[1], pg[2], pg[3]);
+                        *reinterpret_cast<uint4 *>(dr + n + 8) = make_uint4(pg[4], pg[5], pg[6], pg[7]);
+                        *reinterpret_cast<uint4 *>(dr + a.F + n) = make_uint4(pu[0], pu[1], pu[2], pu[3]);
+                        *reinterpret_cast<uint4 *>(dr + a.F + n + 8) = make_uint4(pu[4], pu[5], pu[6], pu[7]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            if (n + i >= a.N) continue;
                             float dg, du;
                             dglu(__uint_as_float(r[i]), gr[n + i], gr[a.F + n + i], a.dbeta1, a.dbeta2, dg, du);
                             dr[n + i] = __float2bfloat16_rn(dg);
@@ -454,7 +481,9 @@ __global__ void __launch_bounds__(DenseCfg<BN, EPI, PACC>::THREADS, 1) dense_ker
                             *reinterpret_cast<uint4 *>(C + n) = v0;
                             *reinterpret_cast<uint4 *>(C + n + 8) = v1;
                         } else {
-                            for (int i = 0; i < 16 && n + i < a.N; ++i) C[n + i] = __float2bfloat16_rn(h[i]);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)   // static indices keep h in registers
+                                if (n + i < a.N) C[n + i] = __float2bfloat16_rn(h[i]);
                         }
                     }
                 }
