@@ -362,6 +362,7 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
 // sum of dz c / r (one row per block, added across blocks in order by dgamma_reduce_kernel).
 constexpr int RB_TOK = 16;
 constexpr int RB_MAXCH = 4;          // 8-feature chunks per thread: d_latent <= 8 * 256 * 4
+template <int MAXCH>
 __global__ void __launch_bounds__(256) rms_combine_bwd_kernel(
     const bf16 *__restrict__ y_e, const float *__restrict__ topk_w, const int32_t *__restrict__ slot_pos,
     const float *__restrict__ gamma, const float *__restrict__ dz, int T, int dl, int k, float eps,
@@ -370,9 +371,9 @@ __global__ void __launch_bounds__(256) rms_combine_bwd_kernel(
     __shared__ float redk[8][32];
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int nch = dl / 8;
-    float dgp[RB_MAXCH][8];
+    float dgp[MAXCH][8];
 #pragma unroll
-    for (int u = 0; u < RB_MAXCH; ++u)
+    for (int u = 0; u < MAXCH; ++u)
 #pragma unroll
         for (int v = 0; v < 8; ++v) dgp[u][v] = 0.f;
     const int t0 = blockIdx.x * RB_TOK;
@@ -380,10 +381,10 @@ __global__ void __launch_bounds__(256) rms_combine_bwd_kernel(
         const int32_t *sp = slot_pos + (long long)t * k;
         const float *gw = topk_w + (long long)t * k;
         const float *dzt = dz + (long long)t * dl;
-        float cv[RB_MAXCH][8];
+        float cv[MAXCH][8];
         float ss = 0.f, A = 0.f;
 #pragma unroll
-        for (int u = 0; u < RB_MAXCH; ++u) {
+        for (int u = 0; u < MAXCH; ++u) {
             const int ch = tid + u * 256;
 #pragma unroll
             for (int v = 0; v < 8; ++v) cv[u][v] = 0.f;
@@ -406,44 +407,39 @@ __global__ void __launch_bounds__(256) rms_combine_bwd_kernel(
         const float r = sqrtf(ss / (float)dl + eps);
         const float ir = 1.0f / r;
         const float coef = A / ((float)dl * r * r * r);
-        float dgl[32];
+        float dc[MAXCH][8];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) dgl[j] = 0.f;
-#pragma unroll
-        for (int u = 0; u < RB_MAXCH; ++u) {
+        for (int u = 0; u < MAXCH; ++u) {
             const int ch = tid + u * 256;
-            if (ch >= nch) continue;
-            float dc[8];
 #pragma unroll
             for (int v = 0; v < 8; ++v) {
-                const float dzv = dzt[8 * ch + v];
-                dc[v] = gamma[8 * ch + v] * dzv * ir - cv[u][v] * coef;
+                const float dzv = ch < nch ? dzt[8 * ch + v] : 0.f;
+                const float gm = ch < nch ? gamma[8 * ch + v] : 0.f;
+                dc[u][v] = gm * dzv * ir - cv[u][v] * coef;
                 dgp[u][v] += dzv * cv[u][v] * ir;
             }
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                if (j < k) {
-                    const long long rw = (long long)sp[j] * dl + 8 * ch;
-                    const uint4 q = *reinterpret_cast<const uint4 *>(y_e + rw);
-                    const bf16 *b = reinterpret_cast<const bf16 *>(&q);
-                    float dot = 0.f;
-#pragma unroll
-                    for (int v = 0; v < 8; ++v) dot += dc[v] * __bfloat162float(b[v]);
-                    dgl[j] += dot;
-                    const float gj = gw[j];
-                    *reinterpret_cast<uint4 *>(dye + rw) =
-                        make_uint4(pack_bf16(gj * dc[0], gj * dc[1]), pack_bf16(gj * dc[2], gj * dc[3]),
-                                   pack_bf16(gj * dc[4], gj * dc[5]), pack_bf16(gj * dc[6], gj * dc[7]));
-                }
-            }
         }
-        // all k gate-weight sums at once: warp sums, then one thread per slot over the warps
+        // slot by slot: dy_e = g_j dc, and the gate-weight gradient's partial dot product,
+        // summed over the warp at once (no per-slot accumulators held across the slots)
+        for (int j = 0; j < k; ++j) {
+            const float gj = gw[j];
+            const long long r0 = (long long)sp[j] * dl;
+            float dot = 0.f;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            if (j < k) {
-                const float v = warp_sum(dgl[j]);
-                if (lane == 0) redk[w][j] = v;
+            for (int u = 0; u < MAXCH; ++u) {
+                const int ch = tid + u * 256;
+                if (ch >= nch) continue;
+                const long long rw = r0 + 8 * ch;
+                const uint4 q = *reinterpret_cast<const uint4 *>(y_e + rw);
+                const bf16 *b = reinterpret_cast<const bf16 *>(&q);
+#pragma unroll
+                for (int v = 0; v < 8; ++v) dot += dc[u][v] * __bfloat162float(b[v]);
+                *reinterpret_cast<uint4 *>(dye + rw) =
+                    make_uint4(pack_bf16(gj * dc[u][0], gj * dc[u][1]), pack_bf16(gj * dc[u][2], gj * dc[u][3]),
+                               pack_bf16(gj * dc[u][4], gj * dc[u][5]), pack_bf16(gj * dc[u][6], gj * dc[u][7]));
             }
+            dot = warp_sum(dot);
+            if (lane == 0) redk[w][j] = dot;
         }
         __syncthreads();
         if (tid < k) {
@@ -454,7 +450,7 @@ __global__ void __launch_bounds__(256) rms_combine_bwd_kernel(
         __syncthreads();
     }
 #pragma unroll
-    for (int u = 0; u < RB_MAXCH; ++u) {
+    for (int u = 0; u < MAXCH; ++u) {
         const int ch = tid + u * 256;
         if (ch < nch)
 #pragma unroll
@@ -693,8 +689,11 @@ int tc_backward(const slmoe_config *c, const void *x, const slmoe_weights *w, co
     }
     // RMSNorm + combine backward
     {
-        rms_combine_bwd_kernel<<<(int)L.nblk, 256, 0, st>>>(fs.y_e, fs.topk_w, fs.slot_pos, w->gamma, dz, T, dl, k,
-                                                               c->eps, dye, dg, dgamma_part);
+        // 8-feature chunks per thread: as few as d_latent needs (registers bound the blocks per SM)
+        const int nch = (dl / 8 + 255) / 256;
+        auto kern = nch <= 1 ? rms_combine_bwd_kernel<1> : nch <= 2 ? rms_combine_bwd_kernel<2> : rms_combine_bwd_kernel<RB_MAXCH>;
+        kern<<<(int)L.nblk, 256, 0, st>>>(fs.y_e, fs.topk_w, fs.slot_pos, w->gamma, dz, T, dl, k, c->eps, dye, dg,
+                                          dgamma_part);
         if ((rc = check_launch("rms_combine_bwd"))) return rc;
         dgamma_reduce_kernel<<<(dl + 255) / 256, 256, 0, st>>>(dgamma_part, (int)L.nblk, dl, g->dgamma, accumulate);
         if ((rc = check_launch("dgamma_reduce"))) return rc;
