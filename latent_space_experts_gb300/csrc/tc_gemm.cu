@@ -1090,6 +1090,44 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
                             static_cast<__nv_bfloat16 *>(a.out)[at] = __float2bfloat16_rn(hv);
                         }
                     }
+                } else if (EPI == EPI_DGLU_T) {
+                    // dh of features f and f + 128 for 16 token rows: the rows' fp32 gate and up
+                    // pre-activations are loaded first, all in flight together (they come from
+                    // HBM), then [dg | du] is computed and stored
+                    uint32_t r0[16], r1[16];
+                    TMEM_LD16(tb + c, r0);
+                    TMEM_LD16(tb + SUB1 + c, r1);
+                    tmem_wait_ld();
+                    const int F = a.out_cols;
+#pragma unroll
+                    for (int j0 = 0; j0 < 16; j0 += 8) {   // 8 rows at a time (registers)
+                        float g0[8], u0[8], g1[8], u1[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const bool in = c + j0 + j < N;
+                            const float *gr = a.gu + ((long long)it.z + c + j0 + j) * a.ld_gu;
+                            g0[j] = (in && ok) ? gr[f] : 0.f;
+                            u0[j] = (in && ok) ? gr[F + f] : 0.f;
+                            g1[j] = (in && ok1) ? gr[f + 128] : 0.f;
+                            u1[j] = (in && ok1) ? gr[F + f + 128] : 0.f;
+                        }
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            if (c + j0 + j >= N) continue;
+                            __nv_bfloat16 *dr = a.dgu + ((long long)it.z + c + j0 + j) * a.ld_dgu;
+                            float dg, du;
+                            if (ok) {
+                                dglu(__uint_as_float(r0[j0 + j]), g0[j], u0[j], a.beta1, a.beta2, dg, du);
+                                dr[f] = __float2bfloat16_rn(dg);
+                                dr[F + f] = __float2bfloat16_rn(du);
+                            }
+                            if (ok1) {
+                                dglu(__uint_as_float(r1[j0 + j]), g1[j], u1[j], a.beta1, a.beta2, dg, du);
+                                dr[f + 128] = __float2bfloat16_rn(dg);
+                                dr[F + f + 128] = __float2bfloat16_rn(du);
+                            }
+                        }
+                    }
                 } else {
                     uint32_t r0[16], r1[16];
                     TMEM_LD16(tb + c, r0);
@@ -1113,21 +1151,6 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
                             if (ok) {
                                 orow[0] = v0;
                                 orow[a.out_cols] = v1;
-                            }
-                        } else if (EPI == EPI_DGLU_T) {    // dh of features f and f + 128
-                            const float *gr = a.gu + row * a.ld_gu;
-                            __nv_bfloat16 *dr = a.dgu + row * a.ld_dgu;
-                            const int F = a.out_cols;
-                            float dg, du;
-                            if (ok) {
-                                dglu(v0, gr[f], gr[F + f], a.beta1, a.beta2, dg, du);
-                                dr[f] = __float2bfloat16_rn(dg);
-                                dr[F + f] = __float2bfloat16_rn(du);
-                            }
-                            if (ok1) {
-                                dglu(v1, gr[f + 128], gr[F + f + 128], a.beta1, a.beta2, dg, du);
-                                dr[f + 128] = __float2bfloat16_rn(dg);
-                                dr[F + f + 128] = __float2bfloat16_rn(du);
                             }
                         }
                     }
