@@ -394,16 +394,22 @@ __global__ void __launch_bounds__(DenseCfg<BN, EPI, PACC>::THREADS, 1) dense_ker
                     const int n = n0 + c;
                     if (row_ok) {
                         if (n + 16 <= a.N) {
+                            float4 o[4];
 #pragma unroll
-                            for (int i = 0; i < 16; i += 4) {
-                                float4 o = make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
-                                                       __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
-                                if (a.accumulate) {
-                                    const float4 p = *reinterpret_cast<const float4 *>(C + n + i);
-                                    o.x += p.x; o.y += p.y; o.z += p.z; o.w += p.w;
+                            for (int i = 0; i < 4; ++i)
+                                o[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                                   __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+                            if (a.accumulate) {   // all four reads in flight before any store
+                                float4 p[4];
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) p[i] = *reinterpret_cast<const float4 *>(C + n + 4 * i);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    o[i].x += p[i].x; o[i].y += p[i].y; o[i].z += p[i].z; o[i].w += p[i].w;
                                 }
-                                *reinterpret_cast<float4 *>(C + n + i) = o;
                             }
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) *reinterpret_cast<float4 *>(C + n + 4 * i) = o[i];
                         } else {
 #pragma unroll
                             for (int i = 0; i < 16; ++i)   // static indices keep r in registers
