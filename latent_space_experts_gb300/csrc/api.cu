@@ -106,7 +106,7 @@ int make_layout(const slmoe_config *c, Layout *L) {
     if (c->dtype != SLMOE_F32) {
         // work items: nfb feature blocks x (one pass per expert + one per full pass of tokens)
         const size_t Tk = T * k;
-        const size_t nfb1 = (c->I + 127) / 128, nfb2 = (c->d_latent + 255) / 256;
+        const size_t nfb1 = (c->I + 127) / 128, nfb2 = (c->d_latent + down_block(c) - 1) / down_block(c);
         // per feature block at most E + ceil(T k / pass) passes (sum of ceil(n_e / pass))
         const size_t pass = grouped_pass(c);
         L->items1 = take(nfb1 * (E + (Tk + pass - 1) / pass) * 16);
@@ -508,7 +508,6 @@ int slmoe_backward(const slmoe_config *cfg, const void *x, const slmoe_weights *
     fs.z = reinterpret_cast<const __nv_bfloat16 *>(fw + L.pub.z);
     fs.h_s = reinterpret_cast<const __nv_bfloat16 *>(fw + L.pub.h_s);
     fs.items1 = reinterpret_cast<const int4 *>(fw + L.items1);
-    fs.items2 = reinterpret_cast<const int4 *>(fw + L.items2);
     fs.n_items = reinterpret_cast<const int *>(fw + L.counters) + 8;
     return tc_backward(cfg, x, w, dy, dx, grads, accumulate, fs, static_cast<char *>(workspace), status,
                        static_cast<cudaStream_t>(stream));

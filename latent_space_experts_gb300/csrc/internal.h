@@ -77,6 +77,11 @@ constexpr int GROUPED_PASS = 192;
 // tokens on average (decode): their small token stages leave shared memory for more weight
 // stages in flight.
 constexpr int MX_SHORT_PASS = 32, MX_LONG_PASS = 192;
+// 128-row weight sub-tiles per work item of the bf16 layer's expert down-projection (one, in
+// one of two accumulator sets; two share one set), and the output features per item (the
+// MXFP4 layer: two sub-tiles).
+constexpr int DOWN_NSUB = 1;
+inline int down_block(const slmoe_config *c) { return c->dtype == SLMOE_MXFP4 ? 256 : 128 * DOWN_NSUB; }
 inline int grouped_pass(const slmoe_config *c) {
     if (c->dtype != SLMOE_MXFP4) return GROUPED_PASS;
     return (long long)c->T * c->k <= 8LL * c->E ? MX_SHORT_PASS : MX_LONG_PASS;
@@ -108,13 +113,14 @@ struct FwdSaved {
     const float *scores, *topk_w;
     const int32_t *topk_idx, *counts, *offsets, *perm, *slot_pos;
     const __nv_bfloat16 *x_lat, *h, *y_e, *z, *h_s;
-    const int4 *items1, *items2;   // the forward's work lists (gate|up, down) and their counts
-    const int *n_items;            // [2]
+    const int4 *items1;            // the forward's gate|up work list and its count
+    const int *n_items;
 };
 struct BwdLayout {
     size_t dy_b, dz, dye, dg, gu, dgu, dxe, dx_lat, gu_s, dgu_s, dl_perm, dgamma_part, counters;
     size_t nblk, total;
-    size_t items_dglu, cap_dglu;
+    size_t items_dglu, cap_dglu;   // 256-feature blocks of I
+    size_t items_dxe, cap_dxe;     // 256-feature blocks of d_latent
 };
 size_t backward_workspace_bytes(const slmoe_config *c, BwdLayout *L);
 int tc_backward(const slmoe_config *c, const void *x, const slmoe_weights *w, const float *dy, float *dx,

@@ -755,40 +755,49 @@ done:
 }
 
 // ---------------------------------------------------------------- grouped (routed experts)
-// A work item is (expert e, feature block fb, token pass): two weight sub-tiles of 128 rows
-// (the MMA's M) times the pass's tokens (N <= PASS, rounded to 16).  NSUB = 2 pairs the gate
-// rows fb*128.. with the up rows I + fb*128.. for the fused SiTU-GLU, or two blocks of 128
-// output features (expert down).  The weights stream from HBM through a 128 KB ring of TMA
-// loads; the pass's token rows are gathered from L2 by cp.async into a 4-deep ring, each
-// gather thread signalling a stage with cp.async.mbarrier.arrive.noinc (the MMA thread fences
-// the generic-proxy writes to the async proxy after its wait).  Items come from a list built
-// on the device (expert-major, then feature block, then pass, so the passes of one weight tile
-// are adjacent and the CTAs that take them together share it through L2) and are handed out
-// dynamically through a global counter, so the heavy skew of expert loads cannot leave one
-// CTA with all the hot experts.  Both routed-expert GEMMs use 192-token passes with one TMEM
-// accumulator set drained by 8 epilogue warps while the weight ring keeps streaming.  (With
-// DBUF, passes hold <= 128 tokens and alternate between two accumulator sets so that an
-// item's epilogue overlaps the next item's MMAs; measured slower, because tcgen05.ld traffic
-// beside running MMAs slows them by up to 2x at these widths.)
+// A work item is (expert e, feature block fb, token pass): weight sub-tiles of 128 rows (the
+// MMA's M) times the pass's tokens (N <= PASS, rounded to 16).  The weights stream from HBM
+// through a ring of TMA loads (112-128 KB in flight); the pass's token rows are gathered from
+// L2 by cp.async into a 4-deep ring, each gather thread signalling a stage with
+// cp.async.mbarrier.arrive.noinc (the MMA thread fences the generic-proxy writes to the async
+// proxy after its wait).  Items come from a list built on the device (expert-major, then
+// feature block, then pass, so the passes of one weight tile are adjacent and the CTAs that
+// take them together share it through L2) and are handed out dynamically through a global
+// counter, so the heavy skew of expert loads cannot leave one CTA with all the hot experts.
+// Both routed-expert GEMMs use 192-token passes drained by 8 epilogue warps.
+//   Gate|up (K = d_latent): NSUB = 2 pairs the gate rows fb*128.. with the up rows I + fb*128..
+//   for the fused SiTU-GLU in one accumulator set; its MMAs are long beside the drain.  (The
+//   backward's grouped GEMMs take this form too, with two blocks of 128 features.)
+//   Down (K = I = 512, DBUF): it drains as many fp32 values as it accumulates over a short K.
+//   Timed per role, the single-set form spent 40 % of its MMA thread's time waiting for the
+//   drain, and the drain's time was the epilogue warps' 2-byte y_e stores stalling on the
+//   memory system (its tensor-memory loads took a few percent of it).  So each item is one
+//   128-feature sub-tile in one of two accumulator sets (columns 0 and 256), and each half of
+//   the epilogue warps stages 16 rows at a time in shared memory, from where one thread
+//   stores them by TMA: the drain overlaps the next item's MMAs and never waits on a store.
+//   (The staged stores with two sub-tiles and one set, or two sets of <= 128-token passes,
+//   measured slower.)
 constexpr int G_GATHER_THREADS = 128;
 constexpr int G_TQ = 4;                           // item queue slots
 
 template <bool DBUF>
 struct GCfg {
-    static constexpr int NSUB = 2;
-    static constexpr int PASS = DBUF ? 128 : GROUPED_PASS;   // tokens per pass
+    static constexpr int NSUB = DBUF ? DOWN_NSUB : 2;        // weight sub-tiles per item
+    static constexpr int PASS = GROUPED_PASS;                // tokens per pass
     static constexpr int A_BYTES = NSUB * 128 * 128;
-    static constexpr int A_STAGES = DBUF ? 5 : 4;            // 160 KB / 128 KB of weights in flight
+    static constexpr int A_STAGES = !DBUF ? 4 : NSUB == 1 ? 7 : 3;   // what shared memory leaves
     static constexpr int B_BYTES = PASS * 128;
     static constexpr int B_STAGES = 4;
-    static constexpr int NBUF = DBUF ? 2 : 1;
-    static constexpr int SUB1_COL = DBUF ? 128 : 256;
-    // epilogue warps: the single-buffered accumulator (long passes) stalls the MMAs while it
-    // drains, so it gets two warps per TMEM lane quadrant; the double-buffered one overlaps
-    static constexpr int EPI_WARPS = DBUF ? 4 : 8;
+    static constexpr int NBUF = DBUF && NSUB == 1 ? 2 : 1;   // accumulator sets, at columns 0 / 256
+    static constexpr int SUB1_COL = 256;                     // sub-tile 1 (NSUB = 2)
+    // two epilogue warps per TMEM lane quadrant
+    static constexpr int EPI_WARPS = 8;
     static constexpr int GATHER_WARP0 = 2 + EPI_WARPS;
     static constexpr int THREADS = (2 + EPI_WARPS + 4) * 32;   // TMA, MMA, epilogue, 4 gather warps
-    static constexpr int SMEM = A_STAGES * A_BYTES + B_STAGES * B_BYTES + 1024 + 512;
+    // DBUF: output staging, two 16-row x (128 NSUB)-feature bf16 chunks per half of the epilogue warps
+    static constexpr int O_CHUNK = 16 * 128 * NSUB * 2;
+    static constexpr int O_BYTES = DBUF ? 4 * O_CHUNK : 0;
+    static constexpr int SMEM = A_STAGES * A_BYTES + B_STAGES * B_BYTES + O_BYTES + 1024 + 512;
     static_assert(SMEM <= 232448, "shared memory");
 };
 
@@ -826,6 +835,37 @@ struct GroupedArgs {
     int out_scale_ld;
 };
 
+// TMA store of a box from shared memory, a 1-D bulk store, and the waits of their bulk groups
+// (this thread's groups only)
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int c0, int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map), "r"(src),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// at most one group still reading shared memory
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// every group complete (its writes performed)
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Named barrier of the four warps of one half of the epilogue (ids 1 and 2), and the same
+// barrier returning whether the predicate held in every thread.
+__device__ __forceinline__ void group_sync(int id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
+__device__ __forceinline__ bool group_all(int id, bool p) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)p), "r"(id)
+        : "memory");
+    return r != 0;
+}
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *map, uint64_t *bar,
                                                  int c0, int c1, uint64_t policy) {
     asm volatile(
@@ -911,14 +951,18 @@ worklist_kernel(const int32_t *__restrict__ counts, const int32_t *__restrict__ 
 // feature offset.
 template <int EPI, bool DBUF, bool AMN = false>
 __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                               const __grid_constant__ CUtensorMap omap,
                                                                const GroupedArgs a) {
     using Cfg = GCfg<DBUF>;
     constexpr int AST = Cfg::A_STAGES, BST = Cfg::B_STAGES, NBUF = Cfg::NBUF, SUB1 = Cfg::SUB1_COL;
+    constexpr bool TWO = Cfg::NSUB == 2;
+    static_assert(!DBUF || (EPI == EPI_BF16 && !AMN), "staged output: the expert down-projection only");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;
     uint8_t *sB = smem + AST * Cfg::A_BYTES;
-    int4 *q_items = reinterpret_cast<int4 *>(sB + BST * Cfg::B_BYTES);
+    uint8_t *sO = sB + BST * Cfg::B_BYTES;     // DBUF output staging
+    int4 *q_items = reinterpret_cast<int4 *>(sO + Cfg::O_BYTES);
     uint64_t *q_full = reinterpret_cast<uint64_t *>(q_items + G_TQ);
     uint64_t *q_empty = q_full + G_TQ;
     uint64_t *a_full = q_empty + G_TQ;
@@ -1009,10 +1053,11 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
                                              f0 + sub * a.a_sub1 + 64 * g, kr, pol_first);
                 } else if (multi) {   // other passes of this tile run alongside: normal L2 policy
                     tma_load_2d(sa, &wmap, &a_full[stage], kb * 64, row0);
-                    tma_load_2d(sa + 128 * 128, &wmap, &a_full[stage], kb * 64, row0 + a.a_sub1);
+                    if (TWO) tma_load_2d(sa + 128 * 128, &wmap, &a_full[stage], kb * 64, row0 + a.a_sub1);
                 } else {           // streamed once
                     tma_load_2d_hint(sa, &wmap, &a_full[stage], kb * 64, row0, pol_first);
-                    tma_load_2d_hint(sa + 128 * 128, &wmap, &a_full[stage], kb * 64, row0 + a.a_sub1, pol_first);
+                    if (TWO)
+                        tma_load_2d_hint(sa + 128 * 128, &wmap, &a_full[stage], kb * 64, row0 + a.a_sub1, pol_first);
                 }
                 if (++stage == AST) { stage = 0; phase ^= 1; p_wrapped = true; }
             }
@@ -1045,7 +1090,7 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
                         umma(d + SUB1, mn_desc(sa + 128 * 128 + kk * 2048, 8192), bd, idesc, acc);
                     } else {
                         umma(d, sdesc(sa + kk * 32), bd, idesc, acc);
-                        umma(d + SUB1, sdesc(sa + 128 * 128 + kk * 32), bd, idesc, acc);
+                        if (TWO) umma(d + SUB1, sdesc(sa + 128 * 128 + kk * 32), bd, idesc, acc);
                     }
                 }
                 umma_commit(&a_empty[as]);
@@ -1064,22 +1109,67 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
         const int half = (warp - 2) >> 2;
         const int lf = q * 32 + lane;                 // feature inside a 128-row sub-tile
         const float ib1 = 1.0f / a.beta1, ib2 = 1.0f / a.beta2;
+        const bool lead = lane == 0 && ((warp - 2) & 3) == 0;   // issues a half's output stores
+        int ocnt = 0;                                          // a half's staged chunks
         int buf = 0, qs = 0;
         uint32_t tph = 0, qp = 0;
         for (;;) {
-            int4 it;
-            if (!pop(qs, qp, it, true)) goto done;
+            int4 it = make_int4(0, 0, 0, -1);
+            bool okw = pop(qs, qp, it, true);
+            if (okw && it.w >= 0) okw = mbar_wait(&tfull[buf], tph, abort_flag);
+            // DBUF: the four warps of a half meet at named barriers inside an item, so they
+            // leave together or go on together (one barrier per item, whatever each waited for)
+            if (DBUF) okw = group_all(1 + half, okw);
+            if (!okw) goto done;
             if (it.w < 0) break;
             const int fb = it.y & 0xffff, N = it.w, Np = (N + 15) & ~15;
-            if (!mbar_wait(&tfull[buf], tph, abort_flag)) goto done;
             tc_after();
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + buf * 256;
             // GLU / GU32: the sub-tiles are the gate and up rows of feature fb*128 + lf.
-            // Otherwise they are features fb*256 + lf and fb*256 + 128 + lf.
+            // Otherwise they are features fb*256 + lf and fb*256 + 128 + lf (one sub-tile:
+            // feature fb*128 + lf).
             constexpr bool GU_LAYOUT = EPI == EPI_GLU || EPI == EPI_GU32;
-            const int f = (GU_LAYOUT ? fb * 128 : fb * 256) + lf;
+            const int f = (GU_LAYOUT || !TWO ? fb * 128 : fb * 256) + lf;
             const bool ok = f < a.out_cols;
-            const bool ok1 = GU_LAYOUT ? ok : f + 128 < a.out_cols;
+            const bool ok1 = TWO && (GU_LAYOUT ? ok : f + 128 < a.out_cols);
+            if constexpr (DBUF) {
+                // one 128-feature sub-tile, rows of y_e: each half stages 16 rows at a time in
+                // shared memory (two buffers) and one thread stores them by TMA, so that the
+                // epilogue warps never wait on global stores (they held up the drain, and with
+                // it the MMAs, far longer than the reads of tensor memory did)
+                constexpr int OW = 128 * Cfg::NSUB;     // features of a staged row
+                for (int c = half * 16; c < Np; c += 32) {
+                    uint8_t *stg = sO + (half * 2 + (ocnt & 1)) * Cfg::O_CHUNK;
+                    uint32_t r0[16], r1[16];
+                    TMEM_LD16(tb + c, r0);
+                    if (TWO) TMEM_LD16(tb + SUB1 + c, r1);
+                    if (lead) bulk_wait_read1();   // the store two chunks back has read this buffer
+                    group_sync(1 + half);
+                    tmem_wait_ld();
+                    __nv_bfloat16 *srow = reinterpret_cast<__nv_bfloat16 *>(stg) + lf;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        srow[j * OW] = __float2bfloat16_rn(__uint_as_float(r0[j]));
+                        if (TWO) srow[j * OW + 128] = __float2bfloat16_rn(__uint_as_float(r1[j]));
+                    }
+                    fence_proxy_async();
+                    group_sync(1 + half);
+                    if (lead) {
+                        const int rows = N - c < 16 ? N - c : 16;
+                        if (rows == 16) {
+                            tma_store_2d(&omap, su32(stg), fb * OW, it.z + c);
+                        } else {   // the item's last rows: one bulk store each, clipped to d_out
+                            const int cols = a.out_cols - fb * OW < OW ? a.out_cols - fb * OW : OW;
+                            for (int r = 0; r < rows; ++r)
+                                bulk_store(static_cast<__nv_bfloat16 *>(a.out) + (long long)(it.z + c + r) * a.out_ld +
+                                               fb * OW,
+                                           su32(stg) + r * OW * 2, (uint32_t)cols * 2);
+                        }
+                        bulk_commit();
+                    }
+                    ++ocnt;
+                }
+            } else
             for (int c = half * 16; c < Np; c += 16 * WPQ) {
                 if (EPI == EPI_GLU) {
                     uint32_t g[16], v[16];
@@ -1137,13 +1227,13 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
                 } else {
                     uint32_t r0[16], r1[16];
                     TMEM_LD16(tb + c, r0);
-                    TMEM_LD16(tb + SUB1 + c, r1);
+                    if (TWO) TMEM_LD16(tb + SUB1 + c, r1);
                     tmem_wait_ld();
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         if (c + j >= N) continue;
                         const long long row = (long long)it.z + c + j;
-                        const float v0 = __uint_as_float(r0[j]), v1 = __uint_as_float(r1[j]);
+                        const float v0 = __uint_as_float(r0[j]), v1 = TWO ? __uint_as_float(r1[j]) : 0.f;
                         if (EPI == EPI_BF16) {
                             __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) + row * a.out_ld + f;
                             if (ok) orow[0] = __float2bfloat16_rn(v0);
@@ -1214,6 +1304,7 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
         cp_async_wait_all();
     }
 done:
+    if (DBUF) bulk_wait_all();   // output stores read shared memory until they complete
     __syncthreads();
     if (abort_flag->abort) {   // every role has stopped: let copies and MMAs in flight finish
         if (warp == 0 && lane == 0) {
@@ -1657,13 +1748,17 @@ int launch_grouped_mx(const CUtensorMap &wmap, const GroupedArgs &a, cudaStream_
     return check_launch("grouped_mx_kernel");
 }
 
+// omap: the output's tensor map (DBUF: bf16 [rows, out_cols], boxes of 128 features x 16 rows)
 template <int EPI, bool DBUF, bool AMN = false>
-int launch_grouped(const CUtensorMap &wmap, const GroupedArgs &a, cudaStream_t st) {
+int launch_grouped(const CUtensorMap &wmap, const GroupedArgs &a, cudaStream_t st, const CUtensorMap *omap = nullptr) {
     using Cfg = GCfg<DBUF>;
     auto kern = grouped_kernel<EPI, DBUF, AMN>;
     int rc = set_smem(kern, Cfg::SMEM);
     if (rc) return rc;
-    kern<<<sm_count(), Cfg::THREADS, Cfg::SMEM, st>>>(wmap, a);
+    CUtensorMap none;
+    memset(&none, 0, sizeof(none));
+    if (DBUF && !omap) return fail(SLMOE_EINVAL, "grouped_kernel: the one-sub-tile variant needs its output map");
+    kern<<<sm_count(), Cfg::THREADS, Cfg::SMEM, st>>>(wmap, omap ? *omap : none, a);
     return check_launch("grouped_kernel");
 }
 
@@ -1790,7 +1885,7 @@ int tc_forward_front(const slmoe_config *c, const void *x, const slmoe_weights *
 int tc_worklists(const slmoe_config *c, const TcForward &f, cudaStream_t st) {
     const int E = c->E, I = c->I, dl = c->d_latent;
     const long long Tk = (long long)c->T * c->k;
-    const int nfb1 = (I + 127) / 128, nfb2 = (dl + 255) / 256;
+    const int nfb1 = (I + 127) / 128, nfb2 = (dl + down_block(c) - 1) / down_block(c);
     const int pass = grouped_pass(c);
     const long long Tk_items = (Tk + pass - 1) / pass;
     worklist_kernel<<<1, 1024, 0, st>>>(f.counts, f.offsets, E, nfb1, pass, f.items1, nfb2, pass, f.items2,
@@ -1878,13 +1973,17 @@ int tc_forward_back(const slmoe_config *c, const slmoe_weights *w, const TcForwa
             if ((rc = make_map(&wm, w->W2, (long long)E * dl, I, I, 128))) return rc;
             GroupedArgs a = {};
             a.kblocks = (I + 63) / 64;
-            a.a_rows_pe = dl; a.a_sub1 = 128; a.a_fb_stride = 256;
+            a.a_rows_pe = dl; a.a_sub1 = 128; a.a_fb_stride = 128 * DOWN_NSUB;
             a.items = f.items2; a.n_items = f.counters + 9; a.counter = f.counters + 7;
             a.b_index = nullptr;
             a.b_src = static_cast<const bf *>(f.h); a.b_ld = I; a.b_K = I;
             a.out = f.y_e; a.out_ld = dl; a.out_cols = dl;
             a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
-            if ((rc = launch_grouped<EPI_BF16, false>(wm, a, st))) return rc;
+            CUtensorMap om;
+            if ((rc = tmap_encode_2d(&om, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, f.y_e, Tk, dl, dl, 128 * DOWN_NSUB, 16,
+                                     CU_TENSOR_MAP_SWIZZLE_NONE)))
+                return rc;
+            if ((rc = launch_grouped<EPI_BF16, true>(wm, a, st, &om))) return rc;
         }
     }
     stage_event(5, st);
