@@ -38,9 +38,13 @@ using bf16 = __nv_bfloat16;
 // B's are contiguous and come by TMA in 64 x 64 boxes.  Four loader warps fill a 4-stage ring
 // (A by cp.async, 16-byte chunks zero-filled past the segment), one thread issues the MMAs
 // into a double-buffered TMEM accumulator, and eight epilogue warps (two per lane quadrant,
-// half the columns each) store the fp32 tile transposed: the lanes of a warp are consecutive
-// M, so every store is one 128-byte run of a gradient row.  The kernel is bound by those fp32
-// stores (19.7 GB at K3): TMEM is read 64 columns per wait so that the stores keep flowing.
+// half the columns each) drain the fp32 tile transposed: 16 gradient rows (tile columns) at a
+// time, each half of the epilogue stages them in shared memory ([16 rows][128 M], two 8 KB
+// buffers) and one thread writes them by TMA (a 128 x 16 box of the gradient seen as
+// [E * N rows, M]; added in by a TMA reduction when accumulating).  The kernel is bound by
+// those fp32 writes (19.7 GB at K3): stored by the epilogue warps themselves they stalled the
+// warps on the memory system (4.3 TB/s, where a plain store stream of the same pattern
+// reaches 6.5 TB/s).
 constexpr int WG_BN = 256;
 constexpr int WG_STAGES = 4;
 constexpr int WG_A_BYTES = 128 * 128;              // 128 M x 64 K
@@ -52,7 +56,10 @@ constexpr int WG_EPI_WARP0 = 5;                    // warps 5-12
 constexpr int WG_EPI_WARPS = 8;
 constexpr int WG_THREADS = (WG_EPI_WARP0 + WG_EPI_WARPS) * 32;
 constexpr int WG_Q = 4;
-constexpr int WG_SMEM = WG_STAGES * WG_STAGE + 1024 + 512;
+constexpr int WG_O_CHUNK = 16 * 128 * 4;            // 16 gradient rows x 128 M, fp32
+constexpr int WG_O_BYTES = 4 * WG_O_CHUNK;          // two buffers per half of the epilogue
+constexpr int WG_SMEM = WG_STAGES * WG_STAGE + WG_O_BYTES + 1024 + 512;
+static_assert(WG_SMEM <= 232448, "shared memory");
 constexpr int WG_BAND = 8;                         // M tiles per band of an expert's tile order
 constexpr int A_MN_ = 1, B_MN_ = 2;                // tc_dense_gemm operand majorness
 
@@ -128,11 +135,15 @@ __device__ __forceinline__ void load_a(uint32_t sbase, const BOp &op, int m0, in
 
 // B rows past the expert's segment (TMA boxes of 64 K rows) hold other experts' values; they
 // meet the zero-filled rows of A past the segment, so they add nothing.
+// cmap: the gradients as one fp32 matrix [E * N rows, M] (expert e's row n at e * N + n),
+// boxes of 128 x 16, no swizzle.
 __global__ void __launch_bounds__(WG_THREADS, 1) wgrad_kernel(const __grid_constant__ CUtensorMap bmap,
+                                                              const __grid_constant__ CUtensorMap cmap,
                                                               const WArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    WItem *q_items = reinterpret_cast<WItem *>(smem + WG_STAGES * WG_STAGE);
+    uint8_t *sO = smem + WG_STAGES * WG_STAGE;        // output staging
+    WItem *q_items = reinterpret_cast<WItem *>(sO + WG_O_BYTES);
     uint64_t *q_full = reinterpret_cast<uint64_t *>(q_items + WG_Q);
     uint64_t *q_empty = q_full + WG_Q;
     uint64_t *full = q_empty + WG_Q;
@@ -266,11 +277,18 @@ __global__ void __launch_bounds__(WG_THREADS, 1) wgrad_kernel(const __grid_const
         const int q = warp & 3;
         const int h = (warp - WG_EPI_WARP0) >> 2;
         const int i = q * 32 + lane;
+        const bool lead = lane == 0 && q == 0;       // issues its half's output writes
+        int ocnt = 0;
         int qs = 0, buf = 0;
         uint32_t qp = 0, tph = 0;
         for (;;) {
             WItem it;
-            if (!pop(qs, qp, it, true)) break;
+            it.e = -1;
+            bool okw = pop(qs, qp, it, true);
+            if (okw && it.e >= 0 && it.klen > 0) okw = mbar_wait(&tfull[buf], tph, wc);
+            // the four warps of a half meet at named barriers inside an item: they leave
+            // together or go on together (one barrier per item, whatever each waited for)
+            if (!group_all(1 + h, okw)) break;
             if (it.e < 0) break;
             const int nkb = (it.klen + 63) / 64;
             const bool row_ok = i < it.mv;
@@ -283,30 +301,42 @@ __global__ void __launch_bounds__(WG_THREADS, 1) wgrad_kernel(const __grid_const
                     for (int j = 128 * h; j < c_end; ++j) C[(long long)(it.n0 + j) * a.ldc + m] = 0.f;
                 continue;
             }
-            if (!mbar_wait(&tfull[buf], tph, wc)) break;
             tc_after();
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + buf * 256;
+            const int grow0 = it.e * a.N + it.n0;       // the tile's first row in cmap
             for (int c0 = 128 * h; c0 < c_end; c0 += 64) {
                 uint32_t r[4][16];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) TMEM_LD16(tb + c0 + 16 * u, r[u]);
                 tmem_wait_ld();
-                if (!row_ok) continue;
-                float *o = C + (long long)(it.n0 + c0) * a.ldc + m;
-                const int nj = min(64, it.nv - c0);
-                if (a.accumulate) {
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
+                for (int u = 0; u < 4; ++u) {
+                    const int cu = c0 + 16 * u;
+                    if (cu >= c_end) break;                  // the same for every warp of the half
+                    if (c_end - cu < 16) {
+                        // a partial block of gradient rows (N not a multiple of 16): direct
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
-                            if (16 * u + j < nj)
-                                r[u][j] = __float_as_uint(__uint_as_float(r[u][j]) + o[(long long)(16 * u + j) * a.ldc]);
+                            if (row_ok && j < c_end - cu) {
+                                float *o = C + (long long)(it.n0 + cu + j) * a.ldc + m;
+                                *o = __uint_as_float(r[u][j]) + (a.accumulate ? *o : 0.f);
+                            }
+                        continue;
+                    }
+                    float *stg = reinterpret_cast<float *>(sO + (h * 2 + (ocnt & 1)) * WG_O_CHUNK);
+                    if (lead) bulk_wait_read1();       // the write two chunks back has read this buffer
+                    group_sync(1 + h);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) stg[j * 128 + i] = __uint_as_float(r[u][j]);
+                    fence_proxy_async();
+                    group_sync(1 + h);
+                    if (lead) {   // columns past M are cut off by the map's bounds
+                        if (a.accumulate) tma_reduce_add_2d(&cmap, su32(stg), it.m0, grow0 + cu);
+                        else tma_store_2d(&cmap, su32(stg), it.m0, grow0 + cu);
+                        bulk_commit();
+                    }
+                    ++ocnt;
                 }
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        if (16 * u + j < nj) o[(long long)(16 * u + j) * a.ldc] = __uint_as_float(r[u][j]);
             }
             tc_before();
             __syncwarp();
@@ -314,6 +344,7 @@ __global__ void __launch_bounds__(WG_THREADS, 1) wgrad_kernel(const __grid_const
             if (++buf == 2) { buf = 0; tph ^= 1; }
         }
     }
+    bulk_wait_all();   // output writes read shared memory until they complete
     __syncthreads();
     if (wc->abort) {   // let copies and MMAs in flight finish before TMEM is freed
         if (threadIdx.x == 0) drain_ring(full, WG_STAGES, l_stage, l_phase, l_wrapped);
@@ -578,8 +609,12 @@ int launch_wgrad(int E, int M, int N, const void *A, long long lda, const int32_
     int rc = tmap_encode_2d(&bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, b_rows, N, ldb, 64, 64,
                             CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc) return rc;
+    CUtensorMap cmap;   // the gradients, [E * N, M] fp32, 128 x 16 boxes
+    if ((rc = tmap_encode_2d(&cmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, (long long)E * N, M, M, 128, 16,
+                             CU_TENSOR_MAP_SWIZZLE_NONE)))
+        return rc;
     const int sms = sm_count();
-    wgrad_kernel<<<a.units < sms ? a.units : sms, WG_THREADS, WG_SMEM, st>>>(bmap, a);
+    wgrad_kernel<<<a.units < sms ? a.units : sms, WG_THREADS, WG_SMEM, st>>>(bmap, cmap, a);
     return check_launch("wgrad_kernel");
 }
 
