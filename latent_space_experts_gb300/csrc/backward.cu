@@ -113,21 +113,30 @@ __device__ __forceinline__ WItem fetch_item(const WArgs &a) {
 }
 
 // The A tile of one stage (64 K rows x 128 M, MN-major: a line of 64 M values per K row, two
-// 64-wide groups, 128-byte swizzle) by cp.async; t = loader thread 0..127.
-__device__ __forceinline__ void load_a(uint32_t sbase, const BOp &op, int m0, int mv, int kr0, int k0, int klen,
-                                       int t) {
-#pragma unroll 4
-    for (int q = t; q < 128 * 8; q += WG_LOADERS) {
-        // 64 K rows x 2 groups x 8 chunks; consecutive threads walk one K row
-        const int kr = q >> 4;
-        const int w = q & 15;
-        const int g = w >> 3, c = w & 7;
-        const bool ok = k0 + kr < klen && 64 * g + 8 * c < mv;
+// 64-wide groups, 128-byte swizzle) by cp.async; t = loader thread 0..127.  Thread t copies
+// chunk t % 16 of K rows t / 16 + 8 i (i < 8): a_lines gives the stored lines of those rows
+// (through the index when A is gathered; rows past the segment repeat its first row and are
+// zero-filled), so that the index loads of the next K block can be in flight while this one
+// is issued.
+__device__ __forceinline__ void a_lines(const BOp &op, int kr0, int k0, int klen, int t, int (&lines)[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int kr = (t >> 4) + 8 * i;
         const int krow = kr0 + k0 + (k0 + kr < klen ? kr : 0);
-        const long long src_line = op.index ? op.index[krow] : krow;
+        lines[i] = op.index ? op.index[krow] : krow;
+    }
+}
+__device__ __forceinline__ void load_a(uint32_t sbase, const BOp &op, int m0, int mv, int k0, int klen, int t,
+                                       const int (&lines)[8]) {
+    const int w = t & 15;
+    const int g = w >> 3, c = w & 7;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int kr = (t >> 4) + 8 * i;
+        const bool ok = k0 + kr < klen && 64 * g + 8 * c < mv;
         const long long col = ok ? m0 + 64 * g + 8 * c : m0;
         const uint32_t dst = sbase + g * 8192 + (kr >> 3) * 1024 + (kr & 7) * 128 + ((c ^ (kr & 7)) << 4);
-        const bf16 *src = op.p + src_line * op.ld + (ok ? col : 0);
+        const bf16 *src = op.p + (long long)lines[i] * op.ld + (ok ? col : 0);
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(ok ? 16u : 0u)
                      : "memory");
     }
@@ -221,11 +230,14 @@ __global__ void __launch_bounds__(WG_THREADS, 1) wgrad_kernel(const __grid_const
             if (it.e < 0) break;
             const int nkb = (it.klen + 63) / 64;
             bool aborted = false;
+            int lines[8];
+            if (nkb > 0) a_lines(a.A, it.kr0, 0, it.klen, t, lines);
             for (int kb = 0; kb < nkb; ++kb) {
                 if (!mbar_wait(&empty[stage], phase ^ 1, wc)) { aborted = true; break; }
                 const uint32_t sa = su32(smem + stage * WG_STAGE);
                 const uint32_t sb = sa + WG_A_BYTES;
-                load_a(sa, a.A, it.m0, it.mv, it.kr0, kb * 64, it.klen, t);
+                load_a(sa, a.A, it.m0, it.mv, kb * 64, it.klen, t, lines);
+                if (kb + 1 < nkb) a_lines(a.A, it.kr0, (kb + 1) * 64, it.klen, t, lines);
                 if (t == 0) {
                     mbar_expect_tx(&full[stage], WG_B_BYTES);
 #pragma unroll
