@@ -925,7 +925,10 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
     using Cfg = GCfg<DBUF>;
     constexpr int AST = Cfg::A_STAGES, BST = Cfg::B_STAGES, NBUF = Cfg::NBUF, SUB1 = Cfg::SUB1_COL;
     constexpr bool TWO = Cfg::NSUB == 2;
-    static_assert(!DBUF || (EPI == EPI_BF16 && !AMN), "staged output: the expert down-projection only");
+    // staged output (TMA stores): the forward's expert down-projection
+    constexpr bool STAGED = DBUF && EPI == EPI_BF16;
+    static_assert(!DBUF || (EPI == EPI_BF16 && !AMN) || (AMN && (EPI == EPI_DGLU_T || EPI == EPI_F32T)),
+                  "one sub-tile in two accumulator sets: expert down, and the backward's MN-major GEMMs");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;
@@ -1015,7 +1018,7 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
                 if (AMN) {         // features fb * stride (+ sub1), K rows of expert it.x
                     const int f0 = fb * a.a_fb_stride, kr = it.x * a.a_rows_pe + kb * 64;
 #pragma unroll
-                    for (int sub = 0; sub < 2; ++sub)
+                    for (int sub = 0; sub < Cfg::NSUB; ++sub)
 #pragma unroll
                         for (int g = 0; g < 2; ++g)
                             tma_load_2d_hint(sa + sub * 128 * 128 + g * 8192, &wmap, &a_full[stage],
@@ -1056,7 +1059,7 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
                     const uint64_t bd = sdesc(sb + kk * 32);
                     if (AMN) {
                         umma(d, mn_desc(sa + kk * 2048, 8192), bd, idesc, acc);
-                        umma(d + SUB1, mn_desc(sa + 128 * 128 + kk * 2048, 8192), bd, idesc, acc);
+                        if (TWO) umma(d + SUB1, mn_desc(sa + 128 * 128 + kk * 2048, 8192), bd, idesc, acc);
                     } else {
                         umma(d, sdesc(sa + kk * 32), bd, idesc, acc);
                         if (TWO) umma(d + SUB1, sdesc(sa + 128 * 128 + kk * 32), bd, idesc, acc);
@@ -1088,7 +1091,7 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
             if (okw && it.w >= 0) okw = mbar_wait(&tfull[buf], tph, abort_flag);
             // DBUF: the four warps of a half meet at named barriers inside an item, so they
             // leave together or go on together (one barrier per item, whatever each waited for)
-            if (DBUF) okw = group_all(1 + half, okw);
+            if (STAGED) okw = group_all(1 + half, okw);
             if (!okw) goto done;
             if (it.w < 0) break;
             const int fb = it.y & 0xffff, N = it.w, Np = (N + 15) & ~15;
@@ -1101,7 +1104,7 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
             const int f = (GU_LAYOUT || !TWO ? fb * 128 : fb * 256) + lf;
             const bool ok = f < a.out_cols;
             const bool ok1 = TWO && (GU_LAYOUT ? ok : f + 128 < a.out_cols);
-            if constexpr (DBUF) {
+            if constexpr (STAGED) {
                 // one 128-feature sub-tile, rows of y_e: each half stages 16 rows at a time in
                 // shared memory (two buffers) and one thread stores them by TMA, so that the
                 // epilogue warps never wait on global stores (they held up the drain, and with
@@ -1161,7 +1164,7 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
                     // HBM), then [dg | du] is computed and stored
                     uint32_t r0[16], r1[16];
                     TMEM_LD16(tb + c, r0);
-                    TMEM_LD16(tb + SUB1 + c, r1);
+                    if (TWO) TMEM_LD16(tb + SUB1 + c, r1);
                     tmem_wait_ld();
                     const int F = a.out_cols;
 #pragma unroll
@@ -1186,7 +1189,7 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
                                 dr[f] = __float2bfloat16_rn(dg);
                                 dr[F + f] = __float2bfloat16_rn(du);
                             }
-                            if (ok1) {
+                            if (TWO && ok1) {
                                 dglu(__uint_as_float(r1[j0 + j]), g1[j], u1[j], a.beta1, a.beta2, dg, du);
                                 dr[f + 128] = __float2bfloat16_rn(dg);
                                 dr[F + f + 128] = __float2bfloat16_rn(du);
@@ -1273,7 +1276,7 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
         cp_async_wait_all();
     }
 done:
-    if (DBUF) bulk_wait_all();   // output stores read shared memory until they complete
+    if (STAGED) bulk_wait_all();   // output stores read shared memory until they complete
     __syncthreads();
     if (abort_flag->abort) {   // every role has stopped: let copies and MMAs in flight finish
         if (warp == 0 && lane == 0) {
@@ -1726,7 +1729,8 @@ int launch_grouped(const CUtensorMap &wmap, const GroupedArgs &a, cudaStream_t s
     if (rc) return rc;
     CUtensorMap none;
     memset(&none, 0, sizeof(none));
-    if (DBUF && !omap) return fail(SLMOE_EINVAL, "grouped_kernel: the one-sub-tile variant needs its output map");
+    if (DBUF && EPI == EPI_BF16 && !omap)
+        return fail(SLMOE_EINVAL, "grouped_kernel: the staged output needs its tensor map");
     kern<<<sm_count(), Cfg::THREADS, Cfg::SMEM, st>>>(wmap, omap ? *omap : none, a);
     return check_launch("grouped_kernel");
 }
@@ -2052,18 +2056,18 @@ int tc_grouped_bwd(int kind, const slmoe_config *c, const void *W, const void *r
         // dh = W2[e]^T dy_e (W2[e] stored [d_l, I]: MN-major), then [dg | du]
         if ((rc = make_map(&wm, W, (long long)E * dl, I, I, 64))) return rc;
         a.kblocks = (dl + 63) / 64;
-        a.a_rows_pe = dl; a.a_sub1 = 128; a.a_fb_stride = 256;
+        a.a_rows_pe = dl; a.a_sub1 = 0; a.a_fb_stride = 128;   // one 128-feature sub-tile, two sets
         a.b_ld = dl; a.b_K = dl;
         a.out_cols = I; a.gu = gu; a.ld_gu = 2 * I; a.dgu = dgu; a.ld_dgu = 2 * I;
-        return launch_grouped<EPI_DGLU_T, false, true>(wm, a, st);
+        return launch_grouped<EPI_DGLU_T, true, true>(wm, a, st);
     }
     // TC_BWD_DXE: the x_lat gradient of each expert row, W13[e]^T [dg | du] (W13[e] stored [2I, d_l])
     if ((rc = make_map(&wm, W, (long long)E * 2 * I, dl, dl, 64))) return rc;
     a.kblocks = (2 * I + 63) / 64;
-    a.a_rows_pe = 2 * I; a.a_sub1 = 128; a.a_fb_stride = 256;
+    a.a_rows_pe = 2 * I; a.a_sub1 = 0; a.a_fb_stride = 128;   // one 128-feature sub-tile, two sets
     a.b_ld = 2 * I; a.b_K = 2 * I;
     a.out_ld = dl; a.out_cols = dl;
-    return launch_grouped<EPI_F32T, false, true>(wm, a, st);
+    return launch_grouped<EPI_F32T, true, true>(wm, a, st);
 }
 
 int tc_worklist_single(const int32_t *counts, const int32_t *offsets, int E, int nfb, int4 *items, int *n_items,
