@@ -39,9 +39,10 @@ using bf16 = __nv_bfloat16;
 // (A by cp.async, 16-byte chunks zero-filled past the segment), one thread issues the MMAs
 // into a double-buffered TMEM accumulator, and eight epilogue warps (two per lane quadrant,
 // half the columns each) drain the fp32 tile transposed: 16 gradient rows (tile columns) at a
-// time, each half of the epilogue stages them in shared memory ([16 rows][128 M], two 8 KB
-// buffers) and one thread writes them by TMA (a 128 x 16 box of the gradient seen as
-// [E * N rows, M]; added in by a TMA reduction when accumulating).  The kernel is bound by
+// time, each warp stages its 32 M lanes of them in shared memory ([16 rows][32 M], two 2 KB
+// buffers per warp) and its first lane writes them by TMA (a 32 x 16 box of the gradient seen
+// as [E * N rows, M], full 128-byte lines; added in by a TMA reduction when accumulating), so
+// that no warp waits on another.  The kernel is bound by
 // those fp32 writes (19.7 GB at K3): stored by the epilogue warps themselves they stalled the
 // warps on the memory system (4.3 TB/s, where a plain store stream of the same pattern
 // reaches 6.5 TB/s).
@@ -56,8 +57,8 @@ constexpr int WG_EPI_WARP0 = 5;                    // warps 5-12
 constexpr int WG_EPI_WARPS = 8;
 constexpr int WG_THREADS = (WG_EPI_WARP0 + WG_EPI_WARPS) * 32;
 constexpr int WG_Q = 4;
-constexpr int WG_O_CHUNK = 16 * 128 * 4;            // 16 gradient rows x 128 M, fp32
-constexpr int WG_O_BYTES = 4 * WG_O_CHUNK;          // two buffers per half of the epilogue
+constexpr int WG_O_CHUNK = 16 * 32 * 4;             // 16 gradient rows x 32 M, fp32
+constexpr int WG_O_BYTES = 2 * WG_EPI_WARPS * WG_O_CHUNK;   // two buffers per epilogue warp
 constexpr int WG_SMEM = WG_STAGES * WG_STAGE + WG_O_BYTES + 1024 + 512;
 static_assert(WG_SMEM <= 232448, "shared memory");
 constexpr int WG_BAND = 8;                         // M tiles per band of an expert's tile order
@@ -145,7 +146,7 @@ __device__ __forceinline__ void load_a(uint32_t sbase, const BOp &op, int m0, in
 // B rows past the expert's segment (TMA boxes of 64 K rows) hold other experts' values; they
 // meet the zero-filled rows of A past the segment, so they add nothing.
 // cmap: the gradients as one fp32 matrix [E * N rows, M] (expert e's row n at e * N + n),
-// boxes of 128 x 16, no swizzle.
+// boxes of 32 x 16, no swizzle.
 __global__ void __launch_bounds__(WG_THREADS, 1) wgrad_kernel(const __grid_constant__ CUtensorMap bmap,
                                                               const __grid_constant__ CUtensorMap cmap,
                                                               const WArgs a) {
@@ -289,18 +290,13 @@ __global__ void __launch_bounds__(WG_THREADS, 1) wgrad_kernel(const __grid_const
         const int q = warp & 3;
         const int h = (warp - WG_EPI_WARP0) >> 2;
         const int i = q * 32 + lane;
-        const bool lead = lane == 0 && q == 0;       // issues its half's output writes
+        uint8_t *stg_w = sO + (warp - WG_EPI_WARP0) * 2 * WG_O_CHUNK;   // this warp's two buffers
         int ocnt = 0;
         int qs = 0, buf = 0;
         uint32_t qp = 0, tph = 0;
         for (;;) {
             WItem it;
-            it.e = -1;
-            bool okw = pop(qs, qp, it, true);
-            if (okw && it.e >= 0 && it.klen > 0) okw = mbar_wait(&tfull[buf], tph, wc);
-            // the four warps of a half meet at named barriers inside an item: they leave
-            // together or go on together (one barrier per item, whatever each waited for)
-            if (!group_all(1 + h, okw)) break;
+            if (!pop(qs, qp, it, true)) break;
             if (it.e < 0) break;
             const int nkb = (it.klen + 63) / 64;
             const bool row_ok = i < it.mv;
@@ -313,9 +309,11 @@ __global__ void __launch_bounds__(WG_THREADS, 1) wgrad_kernel(const __grid_const
                     for (int j = 128 * h; j < c_end; ++j) C[(long long)(it.n0 + j) * a.ldc + m] = 0.f;
                 continue;
             }
+            if (!mbar_wait(&tfull[buf], tph, wc)) break;
             tc_after();
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + buf * 256;
             const int grow0 = it.e * a.N + it.n0;       // the tile's first row in cmap
+            const bool warp_ok = it.m0 + q * 32 < a.M;  // the warp's 32 M lanes start inside M
             for (int c0 = 128 * h; c0 < c_end; c0 += 64) {
                 uint32_t r[4][16];
 #pragma unroll
@@ -335,16 +333,16 @@ __global__ void __launch_bounds__(WG_THREADS, 1) wgrad_kernel(const __grid_const
                             }
                         continue;
                     }
-                    float *stg = reinterpret_cast<float *>(sO + (h * 2 + (ocnt & 1)) * WG_O_CHUNK);
-                    if (lead) bulk_wait_read1();       // the write two chunks back has read this buffer
-                    group_sync(1 + h);
+                    float *stg = reinterpret_cast<float *>(stg_w + (ocnt & 1) * WG_O_CHUNK);
+                    if (lane == 0) bulk_wait_read1();   // the write two chunks back has read this buffer
+                    __syncwarp();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) stg[j * 128 + i] = __uint_as_float(r[u][j]);
+                    for (int j = 0; j < 16; ++j) stg[j * 32 + lane] = __uint_as_float(r[u][j]);
                     fence_proxy_async();
-                    group_sync(1 + h);
-                    if (lead) {   // columns past M are cut off by the map's bounds
-                        if (a.accumulate) tma_reduce_add_2d(&cmap, su32(stg), it.m0, grow0 + cu);
-                        else tma_store_2d(&cmap, su32(stg), it.m0, grow0 + cu);
+                    __syncwarp();
+                    if (lane == 0 && warp_ok) {   // columns past M are cut off by the map's bounds
+                        if (a.accumulate) tma_reduce_add_2d(&cmap, su32(stg), it.m0 + q * 32, grow0 + cu);
+                        else tma_store_2d(&cmap, su32(stg), it.m0 + q * 32, grow0 + cu);
                         bulk_commit();
                     }
                     ++ocnt;
@@ -621,8 +619,8 @@ int launch_wgrad(int E, int M, int N, const void *A, long long lda, const int32_
     int rc = tmap_encode_2d(&bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, b_rows, N, ldb, 64, 64,
                             CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc) return rc;
-    CUtensorMap cmap;   // the gradients, [E * N, M] fp32, 128 x 16 boxes
-    if ((rc = tmap_encode_2d(&cmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, (long long)E * N, M, M, 128, 16,
+    CUtensorMap cmap;   // the gradients, [E * N, M] fp32, 32 x 16 boxes
+    if ((rc = tmap_encode_2d(&cmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, (long long)E * N, M, M, 32, 16,
                              CU_TENSOR_MAP_SWIZZLE_NONE)))
         return rc;
     const int sms = sm_count();
