@@ -408,6 +408,7 @@ __global__ void __launch_bounds__(256) rms_combine_bwd_kernel(
     const bf16 *__restrict__ y_e, const float *__restrict__ topk_w, const int32_t *__restrict__ slot_pos,
     const float *__restrict__ gamma, const float *__restrict__ dz, int T, int dl, int k, float eps,
     bf16 *__restrict__ dye, float *__restrict__ dg, float *__restrict__ dgamma_part) {
+    constexpr int GRP = 8 / MAXCH;   // slot rows loaded together: 8 loads in flight per thread
     __shared__ float red[64];
     __shared__ float redk[8][32];
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -425,17 +426,39 @@ __global__ void __launch_bounds__(256) rms_combine_bwd_kernel(
         float cv[MAXCH][8];
         float ss = 0.f, A = 0.f;
 #pragma unroll
-        for (int u = 0; u < MAXCH; ++u) {
-            const int ch = tid + u * 256;
+        for (int u = 0; u < MAXCH; ++u)
 #pragma unroll
             for (int v = 0; v < 8; ++v) cv[u][v] = 0.f;
-            if (ch < nch) {
-                for (int j = 0; j < k; ++j) {
-                    const uint4 q = *reinterpret_cast<const uint4 *>(y_e + (long long)sp[j] * dl + 8 * ch);
-                    const bf16 *b = reinterpret_cast<const bf16 *>(&q);
+        // the slots' rows GRP at a time, all loaded before any is added; the adds stay in slot
+        // order
+        for (int j0 = 0; j0 < k; j0 += GRP) {
+            uint4 qv[MAXCH][GRP];
 #pragma unroll
-                    for (int v = 0; v < 8; ++v) cv[u][v] += gw[j] * __bfloat162float(b[v]);
+            for (int g = 0; g < GRP; ++g) {
+                const long long r0 = j0 + g < k ? (long long)sp[j0 + g] * dl : 0;
+#pragma unroll
+                for (int u = 0; u < MAXCH; ++u) {
+                    const int ch = tid + u * 256;
+                    if (j0 + g < k && ch < nch) qv[u][g] = *reinterpret_cast<const uint4 *>(y_e + r0 + 8 * ch);
                 }
+            }
+#pragma unroll
+            for (int g = 0; g < GRP; ++g) {
+                if (j0 + g >= k) break;
+                const float wj = gw[j0 + g];
+#pragma unroll
+                for (int u = 0; u < MAXCH; ++u) {
+                    if (tid + u * 256 >= nch) continue;
+                    const bf16 *b = reinterpret_cast<const bf16 *>(&qv[u][g]);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) cv[u][v] += wj * __bfloat162float(b[v]);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < MAXCH; ++u) {
+            const int ch = tid + u * 256;
+            if (ch < nch) {
 #pragma unroll
                 for (int v = 0; v < 8; ++v) {
                     ss += cv[u][v] * cv[u][v];
@@ -461,26 +484,40 @@ __global__ void __launch_bounds__(256) rms_combine_bwd_kernel(
             }
         }
         // slot by slot: dy_e = g_j dc, and the gate-weight gradient's partial dot product,
-        // summed over the warp at once (no per-slot accumulators held across the slots)
-        for (int j = 0; j < k; ++j) {
-            const float gj = gw[j];
-            const long long r0 = (long long)sp[j] * dl;
-            float dot = 0.f;
+        // summed over the warp at once (no per-slot accumulators held across the slots); the
+        // rows are read again GRP slots at a time, loads first
+        for (int j0 = 0; j0 < k; j0 += GRP) {
+            uint4 qv[MAXCH][GRP];
 #pragma unroll
-            for (int u = 0; u < MAXCH; ++u) {
-                const int ch = tid + u * 256;
-                if (ch >= nch) continue;
-                const long long rw = r0 + 8 * ch;
-                const uint4 q = *reinterpret_cast<const uint4 *>(y_e + rw);
-                const bf16 *b = reinterpret_cast<const bf16 *>(&q);
+            for (int g = 0; g < GRP; ++g) {
+                const long long r0 = j0 + g < k ? (long long)sp[j0 + g] * dl : 0;
 #pragma unroll
-                for (int v = 0; v < 8; ++v) dot += dc[u][v] * __bfloat162float(b[v]);
-                *reinterpret_cast<uint4 *>(dye + rw) =
-                    make_uint4(pack_bf16(gj * dc[u][0], gj * dc[u][1]), pack_bf16(gj * dc[u][2], gj * dc[u][3]),
-                               pack_bf16(gj * dc[u][4], gj * dc[u][5]), pack_bf16(gj * dc[u][6], gj * dc[u][7]));
+                for (int u = 0; u < MAXCH; ++u) {
+                    const int ch = tid + u * 256;
+                    if (j0 + g < k && ch < nch) qv[u][g] = *reinterpret_cast<const uint4 *>(y_e + r0 + 8 * ch);
+                }
             }
-            dot = warp_sum(dot);
-            if (lane == 0) redk[w][j] = dot;
+#pragma unroll
+            for (int g = 0; g < GRP; ++g) {
+                if (j0 + g >= k) break;
+                const int j = j0 + g;
+                const float gj = gw[j];
+                const long long r0 = (long long)sp[j] * dl;
+                float dot = 0.f;
+#pragma unroll
+                for (int u = 0; u < MAXCH; ++u) {
+                    const int ch = tid + u * 256;
+                    if (ch >= nch) continue;
+                    const bf16 *b = reinterpret_cast<const bf16 *>(&qv[u][g]);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) dot += dc[u][v] * __bfloat162float(b[v]);
+                    *reinterpret_cast<uint4 *>(dye + r0 + 8 * ch) =
+                        make_uint4(pack_bf16(gj * dc[u][0], gj * dc[u][1]), pack_bf16(gj * dc[u][2], gj * dc[u][3]),
+                                   pack_bf16(gj * dc[u][4], gj * dc[u][5]), pack_bf16(gj * dc[u][6], gj * dc[u][7]));
+                }
+                dot = warp_sum(dot);
+                if (lane == 0) redk[w][j] = dot;
+            }
         }
         __syncthreads();
         if (tid < k) {
