@@ -694,7 +694,7 @@ size_t backward_workspace_bytes(const slmoe_config *c, BwdLayout *L) {
     l.counters = take(32 * 4);
     l.cap_dglu = (I + 127) / 128 * (E + (Tk + GROUPED_PASS - 1) / GROUPED_PASS);
     l.items_dglu = take(l.cap_dglu * 16);
-    l.cap_dxe = (dl + 127) / 128 * (E + (Tk + GROUPED_PASS - 1) / GROUPED_PASS);
+    l.cap_dxe = (dl + 255) / 256 * (E + (Tk + GROUPED_PASS - 1) / GROUPED_PASS);
     l.items_dxe = take(l.cap_dxe * 16);
     l.total = off;
     if (L) *L = l;
@@ -783,14 +783,14 @@ int tc_backward(const slmoe_config *c, const void *x, const slmoe_weights *w, co
         if ((rc = check_launch("dgamma_reduce"))) return rc;
     }
     // routed experts on the forward's grouped kernel: pre-activations (the forward's gate|up
-    // list), dh -> [dg | du] (a list of 128-feature blocks of I), x_lat rows (128-feature
-    // blocks of d_latent); the last two alternate between two accumulator sets
+    // list), dh -> [dg | du] (a list of 128-feature blocks of I, alternating between two
+    // accumulator sets), x_lat rows (256-feature blocks of d_latent)
     // (a single-list build writes its count and a zero after it: counters 28-29 and 30-31)
     int4 *items_dglu = reinterpret_cast<int4 *>(ws + L.items_dglu);
     int4 *items_dxe = reinterpret_cast<int4 *>(ws + L.items_dxe);
     if ((rc = tc_worklist_single(fs.counts, fs.offsets, E, (I + 127) / 128, items_dglu, cnt + 28, (int)L.cap_dglu, st)))
         return rc;
-    if ((rc = tc_worklist_single(fs.counts, fs.offsets, E, (dl + 127) / 128, items_dxe, cnt + 30, (int)L.cap_dxe, st)))
+    if ((rc = tc_worklist_single(fs.counts, fs.offsets, E, (dl + 255) / 256, items_dxe, cnt + 30, (int)L.cap_dxe, st)))
         return rc;
     if ((rc = tc_grouped_bwd(TC_BWD_GU32, c, w->W13, fs.x_lat, fs.perm, fs.items1, fs.n_items, cnt + 17, gu, nullptr,
                              nullptr, status, st)))

@@ -927,8 +927,8 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
     constexpr bool TWO = Cfg::NSUB == 2;
     // staged output (TMA stores): the forward's expert down-projection
     constexpr bool STAGED = DBUF && EPI == EPI_BF16;
-    static_assert(!DBUF || (EPI == EPI_BF16 && !AMN) || (AMN && (EPI == EPI_DGLU_T || EPI == EPI_F32T)),
-                  "one sub-tile in two accumulator sets: expert down, and the backward's MN-major GEMMs");
+    static_assert(!DBUF || (EPI == EPI_BF16 && !AMN) || (EPI == EPI_DGLU_T && AMN),
+                  "one sub-tile in two accumulator sets: expert down, and the backward's dh + SiTU-GLU derivative");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;
@@ -2064,10 +2064,10 @@ int tc_grouped_bwd(int kind, const slmoe_config *c, const void *W, const void *r
     // TC_BWD_DXE: the x_lat gradient of each expert row, W13[e]^T [dg | du] (W13[e] stored [2I, d_l])
     if ((rc = make_map(&wm, W, (long long)E * 2 * I, dl, dl, 64))) return rc;
     a.kblocks = (2 * I + 63) / 64;
-    a.a_rows_pe = 2 * I; a.a_sub1 = 0; a.a_fb_stride = 128;   // one 128-feature sub-tile, two sets
+    a.a_rows_pe = 2 * I; a.a_sub1 = 128; a.a_fb_stride = 256;
     a.b_ld = 2 * I; a.b_K = 2 * I;
     a.out_ld = dl; a.out_cols = dl;
-    return launch_grouped<EPI_F32T, true, true>(wm, a, st);
+    return launch_grouped<EPI_F32T, false, true>(wm, a, st);
 }
 
 int tc_worklist_single(const int32_t *counts, const int32_t *offsets, int E, int nfb, int4 *items, int *n_items,

@@ -66,7 +66,7 @@ enum { TC_BWD_GU32 = 0, TC_BWD_DGLU = 1, TC_BWD_DXE = 2 };
 //   TC_BWD_GU32: gu[row] = W13[e] rows[index[row]] (fp32 gate|up pre-activations; the forward's
 //                gate|up list, 128-feature blocks);
 //   TC_BWD_DGLU: [dg | du][row] from dh = W2[e]^T rows[row] and gu (list of 128-feature blocks of I);
-//   TC_BWD_DXE:  out[row] = W13[e]^T rows[row] (fp32; list of 128-feature blocks of d_latent).
+//   TC_BWD_DXE:  out[row] = W13[e]^T rows[row] (fp32; list of 256-feature blocks of d_latent).
 int tc_grouped_bwd(int kind, const slmoe_config *c, const void *W, const void *rows, const int32_t *row_index,
                    const int4 *items, const int *n_items, int *counter, void *out, const float *gu,
                    __nv_bfloat16 *dgu, int32_t *status, cudaStream_t st);
