@@ -1946,17 +1946,21 @@ int tc_forward_back(const slmoe_config *c, const slmoe_weights *w, const TcForwa
             if ((rc = make_map(&wm, w->W2, (long long)E * dl, I, I, 128))) return rc;
             GroupedArgs a = {};
             a.kblocks = (I + 63) / 64;
-            a.a_rows_pe = dl; a.a_sub1 = 128; a.a_fb_stride = 128 * DOWN_NSUB;
+            a.a_rows_pe = dl; a.a_sub1 = 128; a.a_fb_stride = down_block(c);
             a.items = f.items2; a.n_items = f.counters + 9; a.counter = f.counters + 7;
             a.b_index = nullptr;
             a.b_src = static_cast<const bf *>(f.h); a.b_ld = I; a.b_K = I;
             a.out = f.y_e; a.out_ld = dl; a.out_cols = dl;
             a.beta1 = c->beta1; a.beta2 = c->beta2; a.status = f.status;
-            CUtensorMap om;
-            if ((rc = tmap_encode_2d(&om, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, f.y_e, Tk, dl, dl, 128 * DOWN_NSUB, 16,
-                                     CU_TENSOR_MAP_SWIZZLE_NONE)))
+            if (down_split(c)) {
+                CUtensorMap om;
+                if ((rc = tmap_encode_2d(&om, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, f.y_e, Tk, dl, dl, 128 * DOWN_NSUB, 16,
+                                         CU_TENSOR_MAP_SWIZZLE_NONE)))
+                    return rc;
+                if ((rc = launch_grouped<EPI_BF16, true>(wm, a, st, &om))) return rc;
+            } else if ((rc = launch_grouped<EPI_BF16, false>(wm, a, st))) {
                 return rc;
-            if ((rc = launch_grouped<EPI_BF16, true>(wm, a, st, &om))) return rc;
+            }
         }
     }
     stage_event(5, st);
