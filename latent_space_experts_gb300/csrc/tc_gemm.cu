@@ -764,7 +764,7 @@ done:
 // feature block, then pass, so the passes of one weight tile are adjacent and the CTAs that
 // take them together share it through L2) and are handed out dynamically through a global
 // counter, so the heavy skew of expert loads cannot leave one CTA with all the hot experts.
-// Both routed-expert GEMMs use 192-token passes drained by 8 epilogue warps.
+// Both routed-expert GEMMs use 192-token passes drained by 8 or 12 epilogue warps.
 //   Gate|up (K = d_latent): NSUB = 2 pairs the gate rows fb*128.. with the up rows I + fb*128..
 //   for the fused SiTU-GLU in one accumulator set; its MMAs are long beside the drain.  (The
 //   backward's grouped GEMMs take this form too, with two blocks of 128 features.)
@@ -790,8 +790,10 @@ struct GCfg {
     static constexpr int B_STAGES = 4;
     static constexpr int NBUF = DBUF && NSUB == 1 ? 2 : 1;   // accumulator sets, at columns 0 / 256
     static constexpr int SUB1_COL = 256;                     // sub-tile 1 (NSUB = 2)
-    // two epilogue warps per TMEM lane quadrant
-    static constexpr int EPI_WARPS = 8;
+    // epilogue warps per TMEM lane quadrant: three with one accumulator set, whose drain holds
+    // up the MMAs (1.128 against 1.141 ms for expert gate|up at K3 with two; four, at 80
+    // registers a thread, 1.18 ms), two with two sets
+    static constexpr int EPI_WARPS = DBUF ? 8 : 12;
     static constexpr int GATHER_WARP0 = 2 + EPI_WARPS;
     static constexpr int THREADS = (2 + EPI_WARPS + 4) * 32;   // TMA, MMA, epilogue, 4 gather warps
     // DBUF: output staging, two 16-row x (128 NSUB)-feature bf16 chunks per half of the epilogue warps
