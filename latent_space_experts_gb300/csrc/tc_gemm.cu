@@ -90,6 +90,7 @@ constexpr int A_MN = 1, B_MN = 2;
 struct TmaPack {
     CUtensorMap a[4];
     CUtensorMap b[4];
+    CUtensorMap c;      // EPI_F32: the output, fp32 [M, N], boxes of 32 x 32 in the 128-byte swizzle
 };
 
 struct DenseArgs {
@@ -162,7 +163,9 @@ struct DenseCfg {
     static constexpr int TMEM_COLS = MSUB * ACC;
     static constexpr int EPI_WARPS = 4 * MSUB;
     static constexpr int THREADS = (2 + EPI_WARPS) * 32;  // TMA, MMA, epilogue
-    static constexpr int SMEM = STAGES * STAGE + 1024 + 256;
+    // EPI_F32: a 32 x 32 fp32 staging tile per epilogue warp, written to the output by TMA
+    static constexpr int O_BYTES = EPI == EPI_F32 ? EPI_WARPS * 4096 : 0;
+    static constexpr int SMEM = STAGES * STAGE + O_BYTES + 1024 + 256;
     static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0 && TMEM_COLS >= 32 && TMEM_COLS <= 512 && STAGES >= 3,
                   "dense tile shape");
 };
@@ -186,7 +189,8 @@ __global__ void __launch_bounds__(DenseCfg<BN, EPI, PACC>::THREADS, 1) dense_ker
     constexpr int STAGES = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * Cfg::STAGE);
+    uint8_t *sO = smem + STAGES * Cfg::STAGE;         // EPI_F32 staging
+    uint64_t *full = reinterpret_cast<uint64_t *>(sO + Cfg::O_BYTES);
     uint64_t *empty = full + STAGES;
     uint64_t *tfull = empty + STAGES;
     uint64_t *tempty = tfull + 2;
@@ -385,36 +389,33 @@ __global__ void __launch_bounds__(DenseCfg<BN, EPI, PACC>::THREADS, 1) dense_ker
                     }
                 }
             } else if (EPI == EPI_F32) {
-                float *C = static_cast<float *>(a.C) + (long long)row * a.ldc;
+                // 32 columns at a time: the warp's 32 rows staged in shared memory (the 128-byte
+                // swizzle: 16-byte chunk j of row r at chunk j ^ (r % 8)) and written by one TMA
+                // store, or added in by a TMA reduction, instead of 16-byte stores to 32 rows
+                uint8_t *stg = sO + (warp - 2) * 4096;
+                uint8_t *rowp = stg + lane * 128;
+                const int row0w = tm * Cfg::BM_TILE + sub * Cfg::BM + q * 32;
 #pragma unroll 1
-                for (int c = 0; c < BN; c += 16) {
-                    uint32_t r[16];
-                    TMEM_LD16(tb + c, r);
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t r0[16], r1[16];
+                    TMEM_LD16(tb + c, r0);
+                    TMEM_LD16(tb + c + 16, r1);
+                    if (lane == 0) bulk_wait_read0();   // the warp's last store has read the tile
+                    __syncwarp();
                     tmem_wait_ld();
-                    const int n = n0 + c;
-                    if (row_ok) {
-                        if (n + 16 <= a.N) {
-                            float4 o[4];
 #pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                o[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                                   __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
-                            if (a.accumulate) {   // all four reads in flight before any store
-                                float4 p[4];
-#pragma unroll
-                                for (int i = 0; i < 4; ++i) p[i] = *reinterpret_cast<const float4 *>(C + n + 4 * i);
-#pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    o[i].x += p[i].x; o[i].y += p[i].y; o[i].z += p[i].z; o[i].w += p[i].w;
-                                }
-                            }
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) *reinterpret_cast<float4 *>(C + n + 4 * i) = o[i];
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)   // static indices keep r in registers
-                                if (n + i < a.N) C[n + i] = __uint_as_float(r[i]) + (a.accumulate ? C[n + i] : 0.f);
-                        }
+                    for (int j = 0; j < 4; ++j) {
+                        *reinterpret_cast<uint4 *>(rowp + ((j ^ (lane & 7)) << 4)) =
+                            make_uint4(r0[4 * j], r0[4 * j + 1], r0[4 * j + 2], r0[4 * j + 3]);
+                        *reinterpret_cast<uint4 *>(rowp + (((j + 4) ^ (lane & 7)) << 4)) =
+                            make_uint4(r1[4 * j], r1[4 * j + 1], r1[4 * j + 2], r1[4 * j + 3]);
+                    }
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0 && row0w < a.M && n0 + c < a.N) {   // the map's bounds cut the rest
+                        if (a.accumulate) tma_reduce_add_2d(&maps.c, su32(stg), n0 + c, row0w);
+                        else tma_store_2d(&maps.c, su32(stg), n0 + c, row0w);
+                        bulk_commit();
                     }
                 }
             } else if (EPI == EPI_DGLU) {
@@ -501,6 +502,7 @@ __global__ void __launch_bounds__(DenseCfg<BN, EPI, PACC>::THREADS, 1) dense_ker
         }
     }
 done:
+    if (EPI == EPI_F32) bulk_wait_all();   // output stores read shared memory until they complete
     __syncthreads();
     if (abort_flag->abort) {   // every role has stopped: let copies and MMAs in flight finish
         if (warp == 0 && lane == 0) drain_ring(full, STAGES, p_stage, p_phase, p_wrapped);
@@ -1989,6 +1991,9 @@ int tc_forward_back(const slmoe_config *c, const slmoe_weights *w, const TcForwa
             a.kblocks[1 + s] = (Is + 63) / 64;
         }
         a.C = y; a.ldc = d; a.status = f.status; a.counter = f.counters + 5;
+        if ((rc = tmap_encode_2d(&maps.c, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, y, T, d, d, 32, 32,
+                                 CU_TENSOR_MAP_SWIZZLE_128B)))
+            return rc;
         if ((rc = launch_dense_bn<EPI_F32>(bn, maps, a, st))) return rc;
     }
     stage_event(8, st);
@@ -2034,6 +2039,9 @@ int tc_dense_gemm(int maj, int M, int N, int K, TcOperand A, TcOperand B, void *
         a.dbeta1 = dg->beta1; a.dbeta2 = dg->beta2;
         return launch_tc_bwd_maj<EPI_DGLU>(maj, bn, maps, a, st);
     }
+    if ((rc = tmap_encode_2d(&maps.c, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, M, N, ldc, 32, 32,
+                             CU_TENSOR_MAP_SWIZZLE_128B)))
+        return rc;
     return launch_tc_bwd_maj<EPI_F32>(maj, bn, maps, a, st);
 }
 
