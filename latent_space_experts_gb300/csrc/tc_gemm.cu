@@ -90,7 +90,7 @@ constexpr int A_MN = 1, B_MN = 2;
 struct TmaPack {
     CUtensorMap a[4];
     CUtensorMap b[4];
-    CUtensorMap c;      // EPI_F32: the output, fp32 [M, N], boxes of 32 x 32 in the 128-byte swizzle
+    CUtensorMap c;      // staged output [M, N]: boxes of 32 rows x 128 bytes, 128-byte swizzle
 };
 
 struct DenseArgs {
@@ -163,8 +163,11 @@ struct DenseCfg {
     static constexpr int TMEM_COLS = MSUB * ACC;
     static constexpr int EPI_WARPS = 4 * MSUB;
     static constexpr int THREADS = (2 + EPI_WARPS) * 32;  // TMA, MMA, epilogue
-    // EPI_F32: a 32 x 32 fp32 staging tile per epilogue warp, written to the output by TMA
-    static constexpr int O_BYTES = EPI == EPI_F32 ? EPI_WARPS * 4096 : 0;
+    // staged output: a 4 KB tile per epilogue warp (32 rows x 128 bytes: 32 fp32 or 64 bf16
+    // columns), written to the output by TMA; bf16 outputs need tiles of at least 64 columns.
+    // (The SiTU-GLU output staged the same way measured no faster: its drain is its math.)
+    static constexpr bool STAGE_OUT = EPI == EPI_F32 || (EPI == EPI_BF16 && BN_OUT >= 64);
+    static constexpr int O_BYTES = STAGE_OUT ? EPI_WARPS * 4096 : 0;
     static constexpr int SMEM = STAGES * STAGE + O_BYTES + 1024 + 256;
     static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0 && TMEM_COLS >= 32 && TMEM_COLS <= 512 && STAGES >= 3,
                   "dense tile shape");
@@ -189,7 +192,7 @@ __global__ void __launch_bounds__(DenseCfg<BN, EPI, PACC>::THREADS, 1) dense_ker
     constexpr int STAGES = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sO = smem + STAGES * Cfg::STAGE;         // EPI_F32 staging
+    uint8_t *sO = smem + STAGES * Cfg::STAGE;         // output staging
     uint64_t *full = reinterpret_cast<uint64_t *>(sO + Cfg::O_BYTES);
     uint64_t *empty = full + STAGES;
     uint64_t *tfull = empty + STAGES;
@@ -361,6 +364,38 @@ __global__ void __launch_bounds__(DenseCfg<BN, EPI, PACC>::THREADS, 1) dense_ker
                         *reinterpret_cast<uint4 *>(C + n + 16) = make_uint4(w[4], w[5], w[6], w[7]);
                     }
                 }
+            } else if (EPI == EPI_BF16 && Cfg::STAGE_OUT) {
+                // 64 columns at a time: the warp's 32 rows staged in shared memory (128-byte
+                // swizzle) and written by one TMA store
+                uint8_t *stg = sO + (warp - 2) * 4096;
+                uint8_t *rowp = stg + lane * 128;
+                const int row0w = tm * Cfg::BM_TILE + sub * Cfg::BM + q * 32;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 64) {
+                    uint32_t r[4][16];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) TMEM_LD16(tb + c + 16 * u, r[u]);
+                    if (lane == 0) bulk_wait_read0();   // the warp's last store has read the tile
+                    __syncwarp();
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+#pragma unroll
+                        for (int hv = 0; hv < 2; ++hv) {
+                            const uint32_t *x = r[u] + 8 * hv;
+                            *reinterpret_cast<uint4 *>(rowp + (((2 * u + hv) ^ (lane & 7)) << 4)) = make_uint4(
+                                pack_bf16(__uint_as_float(x[0]), __uint_as_float(x[1])),
+                                pack_bf16(__uint_as_float(x[2]), __uint_as_float(x[3])),
+                                pack_bf16(__uint_as_float(x[4]), __uint_as_float(x[5])),
+                                pack_bf16(__uint_as_float(x[6]), __uint_as_float(x[7])));
+                        }
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0 && row0w < a.M && n0 + c < a.N) {   // the map's bounds cut the rest
+                        tma_store_2d(&maps.c, su32(stg), n0 + c, row0w);
+                        bulk_commit();
+                    }
+                }
             } else if (EPI == EPI_BF16) {
                 __nv_bfloat16 *C = static_cast<__nv_bfloat16 *>(a.C) + (long long)row * a.ldc;
 #pragma unroll 1
@@ -502,7 +537,7 @@ __global__ void __launch_bounds__(DenseCfg<BN, EPI, PACC>::THREADS, 1) dense_ker
         }
     }
 done:
-    if (EPI == EPI_F32) bulk_wait_all();   // output stores read shared memory until they complete
+    if (Cfg::STAGE_OUT) bulk_wait_all();   // output stores read shared memory until they complete
     __syncthreads();
     if (abort_flag->abort) {   // every role has stopped: let copies and MMAs in flight finish
         if (warp == 0 && lane == 0) drain_ring(full, STAGES, p_stage, p_phase, p_wrapped);
@@ -1835,6 +1870,9 @@ int tc_forward_front(const slmoe_config *c, const void *x, const slmoe_weights *
             a.ld_scales = dl / 32;
             rc = launch_dense_bn<EPI_MX8>(bn, maps, a, st);
         } else {
+            if ((rc = tmap_encode_2d(&maps.c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, f.x_lat, T, dl, dl, 64, 32,
+                                     CU_TENSOR_MAP_SWIZZLE_128B)))
+                return rc;
             rc = launch_dense_bn<EPI_BF16>(bn, maps, a, st);
         }
         if (rc) return rc;
