@@ -401,7 +401,7 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
 // dc = gamma dz / r - c A / (n r^3); the expert-row gradient g_j dc (bf16, at the row's
 // position in expert order), the gate-weight gradient dc . y_e(t, j), and the block's dgamma
 // sum of dz c / r (one row per block, added across blocks in order by dgamma_reduce_kernel).
-constexpr int RB_TOK = 16;
+constexpr int RB_TOK = 32;
 constexpr int RB_MAXCH = 4;          // 8-feature chunks per thread: d_latent <= 8 * 256 * 4
 template <int MAXCH>
 __global__ void __launch_bounds__(256) rms_combine_bwd_kernel(
