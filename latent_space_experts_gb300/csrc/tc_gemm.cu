@@ -882,6 +882,23 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
         "l"(map), "r"(su32(bar)), "r"(c0), "r"(c1), "l"(policy)
         : "memory");
 }
+// 8 x 8 transpose within each aligned group of 8 lanes (t = lane % 8): on entry v[i] is row t,
+// column i of the group's matrix; on exit v[i] is row i, column t.  Three exchange stages
+// (lane distance 4, 2, 1), each swapping the off-diagonal halves of 2 x 2 blocks.
+__device__ __forceinline__ void transpose8(float (&v)[8], int t) {
+#pragma unroll
+    for (int s = 4; s >= 1; s >>= 1) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (i & s) continue;
+            const bool hi = (t & s) != 0;
+            const float send = hi ? v[i] : v[i | s];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, s);
+            if (hi) v[i] = recv;
+            else v[i | s] = recv;
+        }
+    }
+}
 // Work lists of both routed-expert GEMMs in one block: per expert ceil(n_e / cap) passes of
 // balanced size (0 when n_e = 0) times nfb feature blocks.  The threads scan the experts'
 // item counts into per-expert bases (kept in shared memory), then each warp writes one
@@ -1187,14 +1204,24 @@ __global__ void __launch_bounds__(GCfg<DBUF>::THREADS, 1) grouped_kernel(const _
                     TMEM_LD16(tb + c, g);
                     TMEM_LD16(tb + SUB1 + c, v);
                     tmem_wait_ld();
-                    if (ok) {
+                    // h of this lane's feature for 8 rows at a time, transposed within each group
+                    // of 8 lanes so that a lane holds 8 consecutive features of one row: one
+                    // 16-byte store per row and group instead of eight 2-byte stores
+                    const int t8 = lane & 7, fg = f - t8;
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            if (c + j >= N) continue;
-                            const float hv = situ_glu_fast(__uint_as_float(g[j]), __uint_as_float(v[j]), ib1, a.beta1,
-                                                           ib2, a.beta2);
-                            const long long at = ((long long)it.z + c + j) * a.out_ld + f;
-                            static_cast<__nv_bfloat16 *>(a.out)[at] = __float2bfloat16_rn(hv);
+                    for (int h8 = 0; h8 < 2; ++h8) {
+                        float hv[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            hv[i] = situ_glu_fast(__uint_as_float(g[8 * h8 + i]), __uint_as_float(v[8 * h8 + i]), ib1,
+                                                  a.beta1, ib2, a.beta2);
+                        transpose8(hv, t8);
+                        const int row = c + 8 * h8 + t8;
+                        if (row < N && fg < a.out_cols) {   // out_cols is a multiple of 8
+                            const uint4 pk = make_uint4(pack_bf16(hv[0], hv[1]), pack_bf16(hv[2], hv[3]),
+                                                        pack_bf16(hv[4], hv[5]), pack_bf16(hv[6], hv[7]));
+                            *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) +
+                                                       ((long long)it.z + row) * a.out_ld + fg) = pk;
                         }
                     }
                 } else if (EPI == EPI_DGLU_T) {
