@@ -124,7 +124,7 @@ struct FwdSaved {
 struct BwdLayout {
     size_t dy_b, dz, dye, dg, gu, dgu, dxe, dx_lat, gu_s, dgu_s, dl_perm, dgamma_part, counters;
     size_t nblk, total;
-    size_t items_dglu, cap_dglu;   // 256-feature blocks of I
+    size_t items_dglu, cap_dglu;   // 128-feature blocks of I
     size_t items_dxe, cap_dxe;     // 256-feature blocks of d_latent
 };
 size_t backward_workspace_bytes(const slmoe_config *c, BwdLayout *L);
