@@ -79,15 +79,23 @@ __device__ __forceinline__ void qb_stage_load(uint32_t *stage, const uint32_t *h
 // the first chunk this is issued before the counting and lands meanwhile); (1) threads with
 // lane = expert add the P CTAs' counters of those rows (local and distributed shared memory,
 // all ranks' loads in flight at once) into the tile; (2) the tile is stored back into hist,
-// coalesced, and the NaN row goes to status[0].  A closing cluster.sync() keeps every CTA's
-// counters alive until the whole cluster has read them.
+// coalesced, and the NaN row goes to status[0].  Each CTA arrives at a closing cluster
+// barrier once its last reads of the other CTAs' counters are done and waits on it just
+// before it exits, so that every CTA's counters stay alive until the whole cluster has read
+// them while the stores of (2) overlap the other CTAs' reads.  P = the cluster size.
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+template <int P>
 __global__ void __launch_bounds__(QB_THREADS, 1)
 qb_hist_kernel(const float *__restrict__ scores, int64_t T, int E, int nbins,
                uint32_t *__restrict__ hist, int32_t *status) {
     extern __shared__ uint32_t hs[];                 // [nbins + 1][QB_SLAB], then the staging tile
     uint32_t *stage = hs + (nbins + 1) * QB_SLAB;
     cg::cluster_group cluster = cg::this_cluster();
-    const int P = (int)cluster.num_blocks();
     const int rank = (int)cluster.block_rank();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     constexpr int nwarps = QB_THREADS / 32;
@@ -135,11 +143,15 @@ qb_hist_kernel(const float *__restrict__ scores, int64_t T, int E, int nbins,
     asm volatile("cp.async.wait_all;" ::: "memory");
     cluster.sync();
 
-    // the cluster's reduction of the owned rows
-    const uint32_t *src[QB_MAX_CLUSTER];
+    // the cluster's reduction of the owned rows: every load of a chunk (CH per thread from
+    // each of the P CTAs) is issued before the first is used
+    const uint32_t *src[P];
 #pragma unroll
-    for (int r = 0; r < QB_MAX_CLUSTER; ++r) src[r] = r < P ? cluster.map_shared_rank(hs, r) : hs;
-    bool overflow = false;
+    for (int r = 0; r < P; ++r) src[r] = cluster.map_shared_rank(hs, r);
+    // loads per thread and rank in flight: 7 x 1024 >= QB_SB x QB_SLAB; fewer for larger P, as
+    // many as the 64 registers of a 1024-thread block hold without spilling
+    constexpr int CH = P <= 4 ? 7 : P == 5 ? 5 : 3;
+    bool overflow = false, arrived = false;
     uint32_t nan_count = 0;
     for (int cb = b_lo; cb < b_hi; cb += QB_SB) {
         const int nbc = min(QB_SB, b_hi - cb);
@@ -148,15 +160,13 @@ qb_hist_kernel(const float *__restrict__ scores, int64_t T, int E, int nbins,
             asm volatile("cp.async.wait_all;" ::: "memory");
             __syncthreads();
         }
-        constexpr int CH = 2;
         for (int i0 = threadIdx.x; i0 < nbc * QB_SLAB; i0 += CH * QB_THREADS) {
-            uint32_t c[CH][QB_MAX_CLUSTER];
+            uint32_t c[CH][P];
 #pragma unroll
             for (int k = 0; k < CH; ++k) {
                 const int i = i0 + k * QB_THREADS;
 #pragma unroll
-                for (int r = 0; r < QB_MAX_CLUSTER; ++r)
-                    c[k][r] = (i < nbc * QB_SLAB && r < P) ? src[r][cb * QB_SLAB + i] : 0u;
+                for (int r = 0; r < P; ++r) c[k][r] = i < nbc * QB_SLAB ? src[r][cb * QB_SLAB + i] : 0u;
             }
 #pragma unroll
             for (int k = 0; k < CH; ++k) {
@@ -165,7 +175,7 @@ qb_hist_kernel(const float *__restrict__ scores, int64_t T, int E, int nbins,
                     uint32_t *slot = stage + (i & 31) * (QB_SB + 1) + (i >> 5);
                     uint64_t sum = *slot;
 #pragma unroll
-                    for (int r = 0; r < QB_MAX_CLUSTER; ++r) sum += c[k][r];
+                    for (int r = 0; r < P; ++r) sum += c[k][r];
                     if (sum > 0xffffffffull) {
                         if (cb + (i >> 5) < nbins) overflow = true;
                         sum = 0xffffffffull;
@@ -173,6 +183,10 @@ qb_hist_kernel(const float *__restrict__ scores, int64_t T, int E, int nbins,
                     *slot = (uint32_t)sum;
                 }
             }
+        }
+        if (cb + QB_SB >= b_hi) {       // this CTA's last reads of the other CTAs' counters
+            cluster_arrive_release();
+            arrived = true;
         }
         __syncthreads();
         for (int i = threadIdx.x; i < ne * nbc; i += QB_THREADS) {
@@ -185,7 +199,8 @@ qb_hist_kernel(const float *__restrict__ scores, int64_t T, int E, int nbins,
     }
     // other CTAs of the cluster may still be reading this CTA's counters (a CTA that owns no
     // rows gets here at once): no CTA leaves before all of them are done
-    cluster.sync();
+    if (!arrived) cluster_arrive_release();
+    cluster_wait_acquire();
     if (status) {
         if (nan_count) atomicAdd(&status[ST_NAN], (int)nan_count);
         if (overflow) atomicExch(&status[ST_OVERFLOW], 1);
@@ -316,13 +331,17 @@ qb_update_kernel(const uint32_t *__restrict__ hist, int E, int nbins, int k,
 // depends on how the SMs are grouped (cudaOccupancyMaxActiveClusters): 28 clusters of 5 may
 // need two waves where 28 clusters of 4 fit in one.  P minimises waves / P (the per-CTA work
 // falls as 1 / P), fewer waves breaking ties.  Cached per device, kernel and shape.
-template <typename K>
-static int qb_cluster_size(K kern, int nslabs, int threads, size_t smem) {
+using QbHistFn = void (*)(const float *, int64_t, int, int, uint32_t *, int32_t *);
+static const QbHistFn kQbHist[QB_MAX_CLUSTER + 1] = {nullptr,           qb_hist_kernel<1>, qb_hist_kernel<2>,
+                                                     qb_hist_kernel<3>, qb_hist_kernel<4>, qb_hist_kernel<5>,
+                                                     qb_hist_kernel<6>, qb_hist_kernel<7>, qb_hist_kernel<8>};
+
+static int qb_cluster_size(int nslabs, int threads, size_t smem) {
     static std::mutex mu;
-    static std::map<std::tuple<int, const void *, int, size_t>, int> cache;
+    static std::map<std::tuple<int, int, size_t>, int> cache;
     int dev = 0;
     cudaGetDevice(&dev);
-    const auto key = std::make_tuple(dev, reinterpret_cast<const void *>(kern), nslabs, smem);
+    const auto key = std::make_tuple(dev, nslabs, smem);
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
@@ -342,7 +361,7 @@ static int qb_cluster_size(K kern, int nslabs, int threads, size_t smem) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
+        if (cudaOccupancyMaxActiveClusters(&n, kQbHist[P], &cfg) != cudaSuccess || n < 1) {
             cudaGetLastError();
             continue;
         }
@@ -362,11 +381,13 @@ int launch_qb_histogram(const float *scores, int64_t T, int E, int nbins, uint32
                         int32_t *status, cudaStream_t st) {
     if (T <= 0) return SLMOE_OK;
     const size_t smem = (size_t)QB_SLAB * (nbins + 1) * sizeof(uint32_t) + QB_STAGE_BYTES;
-    cudaError_t e = cudaFuncSetAttribute(qb_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return fail(SLMOE_ECUDA, "qb smem attribute: %s", cudaGetErrorString(e));
+    for (int p = 1; p <= QB_MAX_CLUSTER; ++p) {
+        cudaError_t e = cudaFuncSetAttribute(kQbHist[p], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return fail(SLMOE_ECUDA, "qb smem attribute: %s", cudaGetErrorString(e));
+    }
+    cudaError_t e;
     const int nslabs = (E + QB_SLAB - 1) / QB_SLAB;
-    const int P = qb_cluster_size(qb_hist_kernel, nslabs, QB_THREADS, smem);
+    const int P = qb_cluster_size(nslabs, QB_THREADS, smem);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(nslabs, P, 1);
     cfg.blockDim = dim3(QB_THREADS, 1, 1);
@@ -379,7 +400,7 @@ int launch_qb_histogram(const float *scores, int64_t T, int E, int nbins, uint32
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, qb_hist_kernel, scores, T, E, nbins, hist, status);
+    e = cudaLaunchKernelEx(&cfg, kQbHist[P], scores, T, E, nbins, hist, status);
     if (e != cudaSuccess) return fail(SLMOE_ECUDA, "qb histogram launch: %s", cudaGetErrorString(e));
     return check_launch("qb_histogram");
 }
