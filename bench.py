@@ -54,8 +54,8 @@ MX_TENSOR_RATIO = 2.0
 
 
 def work_model(shp, counts=None, mx=False):
-    """FLOPs and bytes per stage of one step.  "bytes" are the algorithmic bytes the survey
-    counts (weights touched, the layer's input x and its fp32 output y); "inter" are the
+    """FLOPs and bytes per stage of one step.  "bytes" are the layer's algorithmic bytes
+    (weights touched, the layer's input x and its fp32 output y); "inter" are the
     intermediates a stage reads or writes (scores, x_lat, h, y_e, z, h_s), which a fused
     design could avoid and which are reported separately.  mx: the MXFP4 layer type, whose
     routed-expert weights take 17/32 bytes each (half a byte per code plus one scale byte per
