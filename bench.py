@@ -328,7 +328,8 @@ def run_reference(args):
 def qb_engine(hbm):
     """QB engine on one GPU: histogram bandwidth over one 65536 x 896 fp32 micro-batch of
     scores (235 MB, larger than L2) and the time of one bias update, CUDA events on the
-    launching stream after warm-up."""
+    launching stream.  The histogram is warmed up for about 0.1 s (the clocks settle after
+    whatever ran before) and timed over about 0.2 s, with the SM clocks sampled meanwhile."""
     import torch
     import latent_space_experts_gb300 as lse
     import synthetic
@@ -336,16 +337,21 @@ def qb_engine(hbm):
     q = synthetic.QB
     sc = synthetic.qb_scores(0, q, device="cuda")
     qh = torch.zeros(q.E, q.nbins, dtype=torch.int32, device="cuda")
-    for _ in range(3):
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    for _ in range(2000):
         lse.slmoe_qb_histogram(sc, q.T, q.E, q.nbins, qh)
     torch.cuda.synchronize()
     g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    reps = 50
+    reps = 4000
+    w0 = time.time()
     g0.record(stream)
     for _ in range(reps):
         lse.slmoe_qb_histogram(sc, q.T, q.E, q.nbins, qh)
     g1.record(stream)
     torch.cuda.synchronize()
+    w1 = time.time()
+    clocks = sampler.stop(w0, w1)
     tq = g0.elapsed_time(g1) / reps * 1e-3
     qbias = torch.empty(q.E, device="cuda")
     for _ in range(3):
@@ -373,7 +379,7 @@ def qb_engine(hbm):
     return {"GB/s": round(qbytes / tq / 1e9, 1), "frac_of_hbm": round(qbytes / tq / 1e9 / hbm, 4),
             "us_per_micro_batch": round(tq * 1e6, 2), "bytes": qbytes,
             "update_us": round(tu * 1e6, 2), "signsgd_update_us": round(ts * 1e6, 2),
-            "engine_ms": round((q.micro_batches * tq + tu) * 1e3, 4),
+            "engine_ms": round((q.micro_batches * tq + tu) * 1e3, 4), "clocks": clocks,
             "note": "65536 x 896 fp32 scores per micro-batch (235 MB > L2); engine = 8 histograms + 1 update"}
 
 
