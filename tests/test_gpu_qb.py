@@ -45,8 +45,13 @@ def test_qb_engine_full_size_eight_micro_batches():
 
 
 @pytest.mark.parametrize("T,E,nbins", [(1, 1, 1000), (1000, 33, 1000), (5000, 64, 999), (777, 100, 10),
-                                       (200000, 40, 1000), (3, 2048, 1000), (2000, 70, 1024)])
+                                       (200000, 40, 1000), (3, 2048, 1000), (2000, 70, 1024),
+                                       (3000, 600, 1000), (5, 4096, 1000), (4000, 300, 7)])
 def test_histogram_shapes(T, E, nbins):
+    """Bit-exact bins against the oracle over expert counts that give the launch different
+    cluster sizes (1 to 32 expert slabs and more: the cluster size follows from how many
+    clusters fit at once), ragged last slabs, few and many tokens per CTA, and bin counts
+    whose rows split unevenly over a cluster's CTAs."""
     need_gpu()
     g = torch.Generator(device="cpu").manual_seed(T + E)
     s = torch.rand(T, E, generator=g, dtype=torch.float32)
