@@ -4,9 +4,9 @@
 // Stable LatentMoE block sits after the combine and before the up-projection.
 //   c_t = sum_j topk_w[t,j] * y_e[slot_pos[t,j]]       (fp32, slots in order j = 0..k-1)
 //   z_t = gamma * c_t / sqrt(mean(c_t^2) + eps)
-// One CTA per token; 16-byte vector loads of the k expert rows, eight rows in flight per
-// thread; c_t is staged in shared memory between the two passes.  HBM-bound: it reads k rows
-// of d_latent per token.
+// Resident blocks (as many as fit on the SMs) take the tokens in turn, one token at a time;
+// 16-byte vector loads of the k expert rows, eight rows in flight per thread; c_t is staged
+// in shared memory between the two passes.  HBM-bound: it reads k rows of d_latent per token.
 #include "common.cuh"
 #include "internal.h"
 
@@ -54,62 +54,77 @@ template <typename T>
 __global__ void __launch_bounds__(CB_THREADS)
 combine_rmsnorm_kernel(const T *__restrict__ y_e, const float *__restrict__ topk_w,
                        const int32_t *__restrict__ slot_pos, const float *__restrict__ gamma,
-                       int d_l, int k, float eps, T *__restrict__ z) {
+                       int n_tok, int d_l, int k, float eps, T *__restrict__ z) {
     using U = typename Vec<T>::U;
     constexpr int V = Vec<T>::N;
     extern __shared__ float c_s[];
     __shared__ int64_t rows[32];
     __shared__ float wts[32];
     __shared__ float red[CB_THREADS / 32];
-    const int t = blockIdx.x, tid = threadIdx.x;
-    if (tid < k) {
-        rows[tid] = (int64_t)slot_pos[(int64_t)t * k + tid] * d_l;
-        wts[tid] = topk_w[(int64_t)t * k + tid];
-    }
-    __syncthreads();
-    const int nv = d_l / V;
-    float ss = 0.f;
-    for (int q = tid; q < nv; q += CB_THREADS) {
-        float acc[V];
+    const int tid = threadIdx.x;
+    for (int t = blockIdx.x; t < n_tok; t += gridDim.x) {
+        if (tid < k) {
+            rows[tid] = (int64_t)slot_pos[(int64_t)t * k + tid] * d_l;
+            wts[tid] = topk_w[(int64_t)t * k + tid];
+        }
+        __syncthreads();
+        const int nv = d_l / V;
+        float ss = 0.f;
+        for (int q = tid; q < nv; q += CB_THREADS) {
+            float acc[V];
 #pragma unroll
-        for (int i = 0; i < V; ++i) acc[i] = 0.f;
-        // the slots' rows are loaded CB_GROUP at a time before any is added, so that a thread
-        // keeps that many loads in flight; the adds stay in slot order j = 0..k-1
-        for (int j0 = 0; j0 < k; j0 += CB_GROUP) {
-            U u[CB_GROUP];
+            for (int i = 0; i < V; ++i) acc[i] = 0.f;
+            // the slots' rows are loaded CB_GROUP at a time before any is added, so that a thread
+            // keeps that many loads in flight; the adds stay in slot order j = 0..k-1
+            for (int j0 = 0; j0 < k; j0 += CB_GROUP) {
+                U u[CB_GROUP];
 #pragma unroll
-            for (int g = 0; g < CB_GROUP; ++g)
-                if (j0 + g < k) u[g] = *reinterpret_cast<const U *>(y_e + rows[j0 + g] + (int64_t)q * V);
+                for (int g = 0; g < CB_GROUP; ++g)
+                    if (j0 + g < k) u[g] = *reinterpret_cast<const U *>(y_e + rows[j0 + g] + (int64_t)q * V);
 #pragma unroll
-            for (int g = 0; g < CB_GROUP; ++g) {
-                if (j0 + g < k) {
-                    float f[V];
-                    unpack<T>(u[g], f);
-                    const float wj = wts[j0 + g];
+                for (int g = 0; g < CB_GROUP; ++g) {
+                    if (j0 + g < k) {
+                        float f[V];
+                        unpack<T>(u[g], f);
+                        const float wj = wts[j0 + g];
 #pragma unroll
-                    for (int i = 0; i < V; ++i) acc[i] = fmaf(wj, f[i], acc[i]);
+                        for (int i = 0; i < V; ++i) acc[i] = fmaf(wj, f[i], acc[i]);
+                    }
                 }
             }
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+                c_s[q * V + i] = acc[i];
+                ss = fmaf(acc[i], acc[i], ss);
+            }
         }
+        ss = warp_sum(ss);
+        if ((tid & 31) == 0) red[tid >> 5] = ss;
+        __syncthreads();
+        float tot = 0.f;
 #pragma unroll
-        for (int i = 0; i < V; ++i) {
-            c_s[q * V + i] = acc[i];
-            ss = fmaf(acc[i], acc[i], ss);
+        for (int i = 0; i < CB_THREADS / 32; ++i) tot += red[i];
+        const float scale = 1.0f / sqrtf(tot / (float)d_l + eps);
+        for (int q = tid; q < nv; q += CB_THREADS) {
+            float f[V];
+#pragma unroll
+            for (int i = 0; i < V; ++i) f[i] = gamma[q * V + i] * (c_s[q * V + i] * scale);
+            *reinterpret_cast<U *>(z + (int64_t)t * d_l + (int64_t)q * V) = pack<T>(f);
         }
+        __syncthreads();    // c_s, red and the row offsets are read before the next token writes them
     }
-    ss = warp_sum(ss);
-    if ((tid & 31) == 0) red[tid >> 5] = ss;
-    __syncthreads();
-    float tot = 0.f;
-#pragma unroll
-    for (int i = 0; i < CB_THREADS / 32; ++i) tot += red[i];
-    const float scale = 1.0f / sqrtf(tot / (float)d_l + eps);
-    for (int q = tid; q < nv; q += CB_THREADS) {
-        float f[V];
-#pragma unroll
-        for (int i = 0; i < V; ++i) f[i] = gamma[q * V + i] * (c_s[q * V + i] * scale);
-        *reinterpret_cast<U *>(z + (int64_t)t * d_l + (int64_t)q * V) = pack<T>(f);
+}
+
+// Blocks of the combine that fit on the SMs at once (a host-side occupancy query), at most T.
+template <typename K>
+int combine_grid(K kern, size_t smem, int T) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, CB_THREADS, smem) != cudaSuccess || per_sm < 1) {
+        cudaGetLastError();
+        per_sm = 1;
     }
+    const long long n = (long long)per_sm * sm_count();
+    return (int)(n < T ? n : T);
 }
 
 }  // namespace
@@ -123,14 +138,15 @@ int launch_combine_rmsnorm(int dtype, const void *y_e, const float *topk_w,
         auto kern = combine_rmsnorm_kernel<__nv_bfloat16>;
         if (smem > 48 * 1024)
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        kern<<<T, CB_THREADS, smem, st>>>(static_cast<const __nv_bfloat16 *>(y_e), topk_w, slot_pos,
-                                          gamma, d_latent, k, eps, static_cast<__nv_bfloat16 *>(z));
+        kern<<<combine_grid(kern, smem, T), CB_THREADS, smem, st>>>(static_cast<const __nv_bfloat16 *>(y_e), topk_w,
+                                                                  slot_pos, gamma, T, d_latent, k, eps,
+                                                                  static_cast<__nv_bfloat16 *>(z));
     } else {
         auto kern = combine_rmsnorm_kernel<float>;
         if (smem > 48 * 1024)
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        kern<<<T, CB_THREADS, smem, st>>>(static_cast<const float *>(y_e), topk_w, slot_pos, gamma,
-                                          d_latent, k, eps, static_cast<float *>(z));
+        kern<<<combine_grid(kern, smem, T), CB_THREADS, smem, st>>>(static_cast<const float *>(y_e), topk_w, slot_pos,
+                                                                  gamma, T, d_latent, k, eps, static_cast<float *>(z));
     }
     return check_launch("combine_rmsnorm");
 }
