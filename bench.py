@@ -599,7 +599,7 @@ def main():
                     help="the reference run shrinks its sample if it would take much longer than this")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
-                    help="skip the decode / mid sub-results and the QB balance in the line")
+                    help="skip the decode / mid sub-results, the QB engine and the QB balance in the line")
     ap.add_argument("--qb-only", action="store_true", help="only the QB engine measurement")
     ap.add_argument("--bwd-only", action="store_true",
                     help="only the backward measurement of the workload (one forward first)")
@@ -772,7 +772,7 @@ def main():
 
     # ---------------- the other layer workloads and the QB engine (rank 0, reported only)
     extra = {}
-    qb = qb_engine(hbm) if rank == 0 else None
+    qb = qb_engine(hbm) if rank == 0 and not args.no_extra else None
     if rank == 0 and not args.no_extra:
         if args.workload == "k3_prefill":
             # K3 decode: the same weights, the first 128 tokens of the batch; uniform and with
